@@ -1,0 +1,471 @@
+"""DFlash oracle: numpy fp64 restatement of the draft path (test infrastructure).
+
+Pages cited (by title and section):
+  [tutorial]  "A3-dflash — DFlash: Block Diffusion for Flash Speculative
+              Decoding" (llm-paper-tutorials), §2.1.1 feature extraction
+              (worked example), §2.1.2 KV injection, §2.1.3 parallel drafting.
+  [translation] papercache.org translation of the paper, §3.1 speedup
+              analysis, §4.1 inference design, experimental setup.
+  [notes]     tom-jerr notes on DFlash, "DFlash Inference Workflow" and the
+              acceptance-length identity (proof §1).
+  [reading]   txtmix "DFlash：把扩散模型关进草稿阶段…" source reading, §5 target
+              feature KV injection, §6 one-step denoising, §8 losslessness
+              from the verification rule, §9 one request through the system,
+              §11 dflash_config fields.
+
+Arithmetic: every dot product and reduction in fp64.  Values are then
+rounded at the "storage points" where the GPU path stores a tensor, using
+``store`` (fp32 rounding in f32 mode, fp32-then-bf16 round-to-nearest-even
+in bf16 mode).  The residual stream, the softmax and the logits are fp32.
+Argmax is taken on fp32-rounded logits, lowest index first on ties.
+
+What pins each function (tests/test_oracle_*.py):
+  build_target_layer_ids   rule table + end points + 1-pick middle layer
+  fuse_context             printed worked example ([tutorial] §2.1.1),
+                           RMS = 1 invariant, W_c byte counts
+  rmsnorm                  torch.nn.functional.rms_norm, RMS = 1
+  rope                     complex-multiplication form, relative-position
+                           invariance, identity at position 0, norm kept
+  attention                torch scaled_dot_product_attention (fp64) with
+                           grouped K/V heads, uniform-score closed form
+  draft_layer/draft_block  reductions: zero W_o and W_d give the identity;
+                           zero W_q gives uniform attention (closed form);
+                           context enters only through K/V
+  lm_head_argmax           brute force with planted ties / gaps
+  verify_greedy            exhaustive enumeration on tiny B and V;
+                           tau in [1, B]; E[tau] closed form under planted
+                           Geometric acceptance (Monte Carlo)
+  target_forward + loops   losslessness: speculative output equals the
+                           target's own greedy autoregressive output
+"""
+from __future__ import annotations
+
+import math
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "build_target_layer_ids", "f32", "bf16", "storage", "rmsnorm",
+    "rope_angles", "rope", "linear", "attention", "fuse_context", "inject_kv",
+    "embed_block", "draft_layer", "draft_block", "lm_head_logits",
+    "argmax_lowest", "top2_gap", "verify_greedy", "expected_tau_from_prefix",
+    "TargetCache", "target_forward", "ar_generate", "speculative_generate",
+]
+
+
+# ---------------------------------------------------------------------------
+# target layer selection  ([reading] §5; [translation] experimental setup)
+# ---------------------------------------------------------------------------
+def build_target_layer_ids(num_target_layers: int, n_pick: int) -> List[int]:
+    """Uniformly spaced 0-based layer ids in [1, num_target_layers - 3].
+
+    [reading] §5: picks are spread uniformly between the second layer and
+    the third-from-last (0-based 1 .. num_target_layers-3); a draft that
+    takes a single pick takes the middle layer.  The pages do not say how a
+    non-integer spacing rounds; this reads it as round-half-up.  The middle
+    layer is read as num_target_layers // 2.
+    """
+    if n_pick < 1:
+        raise ValueError("n_pick must be >= 1")
+    if n_pick == 1:
+        return [num_target_layers // 2]
+    lo, hi = 1, num_target_layers - 3
+    if hi < lo:
+        raise ValueError("target too shallow")
+    span = hi - lo
+    ids = []
+    for i in range(n_pick):
+        # round_half_up(i * span / (n_pick - 1)) in exact integer arithmetic
+        num = 2 * i * span + (n_pick - 1)
+        ids.append(lo + num // (2 * (n_pick - 1)))
+    return ids
+
+
+# ---------------------------------------------------------------------------
+# storage rounding
+# ---------------------------------------------------------------------------
+def f32(x) -> np.ndarray:
+    """Round to fp32 (round-to-nearest-even) and return as fp64."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def bf16(x) -> np.ndarray:
+    """Round to fp32, then to bfloat16 (round-to-nearest-even), as fp64.
+
+    bfloat16 keeps the upper 16 bits of an IEEE fp32 word; rounding adds
+    0x7FFF plus the lowest kept bit before truncating."""
+    a = np.asarray(x, dtype=np.float64).astype(np.float32)
+    bits = a.view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def storage(dtype: str):
+    """The rounding applied where the path stores an activation tensor."""
+    return {"f32": f32, "bf16": bf16}[dtype]
+
+
+# ---------------------------------------------------------------------------
+# building blocks
+# ---------------------------------------------------------------------------
+def rmsnorm(x: np.ndarray, gain: np.ndarray, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * gain over the last axis.
+
+    [tutorial] §2.1.1 (the fusion snippet's RMSNorm: eps 1e-6, gain applied
+    after normalisation)."""
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(gain, dtype=np.float64)
+
+
+def linear(x: np.ndarray, W: np.ndarray, chunk: int = 1 << 14) -> np.ndarray:
+    """y = x W^T with W stored out x in (``nn.Linear.weight``), fp64.
+
+    Large W are upcast a block of output rows at a time."""
+    x = np.asarray(x, dtype=np.float64)
+    n_out = W.shape[0]
+    if W.dtype == np.float64 or n_out <= chunk:
+        return x @ np.asarray(W, dtype=np.float64).T
+    out = np.empty(x.shape[:-1] + (n_out,), dtype=np.float64)
+    for s in range(0, n_out, chunk):
+        out[..., s:s + chunk] = x @ W[s:s + chunk].astype(np.float64).T
+    return out
+
+
+def rope_angles(pos: np.ndarray, d: int, theta: float) -> np.ndarray:
+    """phi[p, i] = pos_p * theta^(-2i/d), i < d/2 (fp64)."""
+    i = np.arange(d // 2, dtype=np.float64)
+    inv_freq = theta ** (-2.0 * i / d)
+    return np.asarray(pos, dtype=np.float64)[:, None] * inv_freq[None, :]
+
+
+def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
+    """Rotary embedding with rotate-half pairing (i, i + d/2).
+
+    x: [n, heads, d]; pos: [n].  Pair (x_i, x_{i+d/2}) is rotated by
+    phi = pos * theta^(-2i/d):
+        x_i'       = x_i cos(phi) - x_{i+d/2} sin(phi)
+        x_{i+d/2}' = x_{i+d/2} cos(phi) + x_i sin(phi)
+    (Qwen3/Llama convention, which the draft and target layers follow.)"""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    phi = rope_angles(pos, d, theta)[:, None, :]      # [n, 1, d/2]
+    c, s = np.cos(phi), np.sin(phi)
+    x1, x2 = x[..., : d // 2], x[..., d // 2:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray,
+              key_visible: Optional[np.ndarray] = None) -> np.ndarray:
+    """Softmax attention with grouped K/V heads, fp64.
+
+    q: [n, H, d]; K, V: [m, G, d]; query head h reads K/V head
+    h // (H / G).  Scale 1/sqrt(d).  ``key_visible`` [n, m] (bool) masks
+    keys; None means every key is visible (the draft's bidirectional block
+    over [context ; block], [reading] §6: full-attention layers are
+    non-causal).  Returns [n, H, d]."""
+    n, H, d = q.shape
+    m, G, _ = K.shape
+    rep = H // G
+    out = np.empty((n, H, d), dtype=np.float64)
+    for h in range(H):
+        g = h // rep
+        s = (q[:, h, :] @ K[:, g, :].T) / math.sqrt(d)      # [n, m]
+        if key_visible is not None:
+            s = np.where(key_visible, s, -np.inf)
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=1, keepdims=True)
+        out[:, h, :] = p @ V[:, g, :]
+    return out
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    return x / (1.0 + np.exp(-x))
+
+
+# ---------------------------------------------------------------------------
+# context fusion ([tutorial] §2.1.1 formula and snippet; [reading] §5)
+# ---------------------------------------------------------------------------
+def fuse_context(hiddens: Sequence[np.ndarray], Wc: np.ndarray, g_c: np.ndarray,
+                 eps: float, store=f32) -> np.ndarray:
+    """H_t = RMSNorm(W_c [H^(l1); ...; H^(l5)]).
+
+    The picked layers' hidden states are concatenated along the hidden axis
+    in ascending layer order ([T, 5D]), projected by W_c (D x 5D, no bias:
+    y = x W_c^T) and RMS-normalised.  H_t is stored (``store``)."""
+    X = np.concatenate([np.asarray(h, dtype=np.float64) for h in hiddens], axis=-1)
+    Y = linear(X, Wc)
+    return store(rmsnorm(Y, g_c, eps))
+
+
+# ---------------------------------------------------------------------------
+# K/V injection ([tutorial] §2.1.2; [reading] §5; [translation] §4.1)
+# ---------------------------------------------------------------------------
+def inject_kv(H_t: np.ndarray, layer: dict, pos: np.ndarray, G: int, d: int,
+              theta: float, eps: float, store=f32, qk_norm: bool = True):
+    """Context K/V entries of one draft layer.
+
+    The context feature goes through this layer's k_proj and v_proj only
+    (never Q, o_proj or the FFN): K = RoPE(k_norm(H_t W_k^T), pos),
+    V = H_t W_v^T.  Returns stored K, V of shape [T, G, d]."""
+    T = H_t.shape[0]
+    k = linear(H_t, layer["wk"]).reshape(T, G, d)
+    if qk_norm:
+        k = rmsnorm(k, layer["k_norm"], eps)
+    k = rope(k, pos, theta)
+    v = linear(H_t, layer["wv"]).reshape(T, G, d)
+    return store(k), store(v)
+
+
+# ---------------------------------------------------------------------------
+# block draft forward ([reading] §5, §6, §9; [tutorial] §2.1.2–2.1.3)
+# ---------------------------------------------------------------------------
+def embed_block(embed: np.ndarray, anchor: int, mask_id: int, B: int,
+                scale: float) -> np.ndarray:
+    """Block input [anchor, mask x (B-1)] through the shared embedding, times
+    input_embedding_scale ([reading] §6 and §9), as the fp32 residual."""
+    ids = [int(anchor)] + [int(mask_id)] * (B - 1)
+    return f32(np.asarray(embed[ids], dtype=np.float64) * scale)
+
+
+def draft_layer(x: np.ndarray, layer: dict, ctx_K: np.ndarray, ctx_V: np.ndarray,
+                pos: np.ndarray, H: int, G: int, d: int, theta: float, eps: float,
+                store=f32) -> np.ndarray:
+    """One Qwen3-style draft decoder layer over one sequence's block.
+
+    x: [B, D] fp32 residual.  ctx_K, ctx_V: [L, G, d] injected context.
+    Queries come from the block only; keys/values are [context ; block]
+    concatenated along the sequence ([tutorial] §2.1.2; [reading] §5);
+    attention is bidirectional (no mask).  Then o_proj + residual and a
+    SwiGLU FFN + residual, each sublayer pre-normalised."""
+    B = x.shape[0]
+    h = store(rmsnorm(x, layer["g_in"], eps))
+    q = linear(h, layer["wq"]).reshape(B, H, d)
+    k = linear(h, layer["wk"]).reshape(B, G, d)
+    v = linear(h, layer["wv"]).reshape(B, G, d)
+    q = store(rope(rmsnorm(q, layer["q_norm"], eps), pos, theta))
+    k = store(rope(rmsnorm(k, layer["k_norm"], eps), pos, theta))
+    v = store(v)
+    K = np.concatenate([ctx_K, k], axis=0)
+    Vv = np.concatenate([ctx_V, v], axis=0)
+    o = store(attention(q, K, Vv).reshape(B, H * d))
+    x = f32(x + linear(o, layer["wo"]))
+    h2 = store(rmsnorm(x, layer["g_post"], eps))
+    a = store(silu(linear(h2, layer["wg"])) * linear(h2, layer["wu"]))
+    return f32(x + linear(a, layer["wd"]))
+
+
+def lm_head_logits(hf: np.ndarray, W_lm: np.ndarray) -> np.ndarray:
+    """fp32 logits hf W_lm^T (the target's shared LM head)."""
+    return f32(linear(hf, W_lm))
+
+
+def argmax_lowest(z: np.ndarray) -> np.ndarray:
+    """Argmax over the last axis; ties go to the lowest index."""
+    return np.argmax(z, axis=-1).astype(np.int32)
+
+
+def top2_gap(z: np.ndarray) -> np.ndarray:
+    """Largest minus second-largest value over the last axis (0 on a tie)."""
+    part = np.partition(z, -2, axis=-1)
+    return part[..., -1] - part[..., -2]
+
+
+def draft_block(shape, W: dict, ctx_K: List[List[np.ndarray]],
+                ctx_V: List[List[np.ndarray]], anchors: Sequence[int], B: int,
+                store=f32, return_logits: bool = False):
+    """Single-pass draft of one block per sequence.
+
+    ``shape`` has D, H, G, d, eps, rope_theta, mask_id, embed_scale.
+    ``ctx_K[l][b]`` / ``ctx_V[l][b]``: [L_b, G, d] injected context of
+    layer l, sequence b.  The block [anchor, mask x (B-1)] sits at positions
+    L_b .. L_b + B - 1 ([reading] §9: positions run from start - ctx_len).
+    Every row goes through every layer (the anchor's K/V feed the others);
+    the final RMSNorm and the shared LM head run on rows 1..B-1 only, and
+    each draft id is the argmax of its fp32 logits ([reading] §6, §14).
+
+    Returns ids [batch, B] (column 0 = anchor), gap [batch, B-1] and,
+    if asked, logits [batch, B-1, V]."""
+    batch = len(anchors)
+    ids = np.zeros((batch, B), dtype=np.int32)
+    gaps = np.zeros((batch, B - 1), dtype=np.float64)
+    all_logits = []
+    for b in range(batch):
+        L = ctx_K[0][b].shape[0]
+        pos = np.arange(L, L + B)
+        x = embed_block(W["embed"], anchors[b], shape.mask_id, B, shape.embed_scale)
+        for l, layer in enumerate(W["layers"]):
+            x = draft_layer(x, layer, ctx_K[l][b], ctx_V[l][b], pos, shape.H,
+                            shape.G, shape.d, shape.rope_theta, shape.eps, store)
+        hf = store(rmsnorm(x[1:], W["g_f"], shape.eps))
+        z = lm_head_logits(hf, W["lm_head"])
+        ids[b, 0] = anchors[b]
+        ids[b, 1:] = argmax_lowest(z)
+        gaps[b] = top2_gap(z)
+        if return_logits:
+            all_logits.append(z)
+    if return_logits:
+        return ids, gaps, np.stack(all_logits)
+    return ids, gaps
+
+
+# ---------------------------------------------------------------------------
+# greedy verification ([reading] §8, §9; [translation] §3.1)
+# ---------------------------------------------------------------------------
+def verify_greedy(draft: np.ndarray, post: np.ndarray, start: np.ndarray):
+    """Longest matching prefix plus a bonus token, per sequence.
+
+    draft[b] = [anchor, d_1 .. d_{B-1}]; post[b, j] is the target's argmax at
+    block position j.  a_b counts the leading j >= 1 with
+    draft[b, j] == post[b, j-1] (the first mismatch ends the prefix);
+    bonus_b = post[b, a_b]; tau_b = a_b + 1 in [1, B].  The emitted tokens
+    are draft[b, 1..a_b] then the bonus; the target cache keeps
+    start_b + a_b + 1 entries.
+
+    Returns (accept, bonus, out_tokens [batch, B] padded with -1, new_len)."""
+    draft = np.asarray(draft)
+    post = np.asarray(post)
+    batch, B = draft.shape
+    accept = np.zeros(batch, dtype=np.int32)
+    bonus = np.zeros(batch, dtype=np.int32)
+    out = np.full((batch, B), -1, dtype=np.int32)
+    new_len = np.zeros(batch, dtype=np.int32)
+    for b in range(batch):
+        a = 0
+        while a < B - 1 and draft[b, a + 1] == post[b, a]:
+            a += 1
+        accept[b] = a
+        bonus[b] = post[b, a]
+        out[b, :a] = draft[b, 1:a + 1]
+        out[b, a] = bonus[b]
+        new_len[b] = int(start[b]) + a + 1
+    return accept, bonus, out, new_len
+
+
+def expected_tau_from_prefix(prefix_match_prob: Sequence[float]) -> float:
+    """E[tau] = 1 + sum_k P(first k drafts all match), k = 1 .. B-1.
+
+    [notes] proof §1: for a non-negative integer match length,
+    E = sum_k P(match length >= k) = sum_k P(prefix of length k matches);
+    the bonus token adds one ([translation] §3.1: tau in [1, gamma + 1])."""
+    return 1.0 + float(np.sum(prefix_match_prob))
+
+
+# ---------------------------------------------------------------------------
+# end-to-end check: Llama-style causal target and the two decoders
+# ([reading] §9; [tutorial] data-flow section)
+# ---------------------------------------------------------------------------
+class TargetCache:
+    """Per-layer causal K/V history of one sequence ([G, len, d] lists)."""
+
+    def __init__(self, n_layers: int):
+        self.K = [[] for _ in range(n_layers)]
+        self.V = [[] for _ in range(n_layers)]
+
+    def __len__(self):
+        return len(self.K[0])
+
+    def crop(self, n: int):
+        """Keep the first n positions (the trim after verification)."""
+        for l in range(len(self.K)):
+            del self.K[l][n:]
+            del self.V[l][n:]
+
+
+def target_forward(tshape, TW: dict, cache: TargetCache, tokens: Sequence[int],
+                   tap_ids: Sequence[int], store=f32):
+    """Causal forward of the target over ``tokens`` appended to ``cache``.
+
+    One row at a time (row i at position len(cache) sees keys 0..pos), so a
+    row's result does not depend on how many rows are processed together.
+    Returns (argmax ids per row, taps [n_pick, n, D] fp32): a tap is the
+    residual stream after 0-based decoder layer ``id``."""
+    D, H, G, d = tshape.D, tshape.H, tshape.G, tshape.d
+    ids_out, taps = [], [[] for _ in tap_ids]
+    for tok in tokens:
+        p = len(cache)
+        x = f32(np.asarray(TW["embed"][int(tok)], dtype=np.float64))[None, :]
+        for l, layer in enumerate(TW["layers"]):
+            h = store(rmsnorm(x, layer["g_in"], tshape.eps))
+            q = linear(h, layer["wq"]).reshape(1, H, d)
+            k = linear(h, layer["wk"]).reshape(1, G, d)
+            v = linear(h, layer["wv"]).reshape(1, G, d)
+            q = store(rope(q, np.array([p]), tshape.rope_theta))
+            k = store(rope(k, np.array([p]), tshape.rope_theta))
+            v = store(v)
+            cache.K[l].append(k[0])
+            cache.V[l].append(v[0])
+            K = np.stack(cache.K[l])          # keys 0..p
+            Vv = np.stack(cache.V[l])
+            o = store(attention(q, K, Vv).reshape(1, H * d))
+            x = f32(x + linear(o, layer["wo"]))
+            h2 = store(rmsnorm(x, layer["g_post"], tshape.eps))
+            a = store(silu(linear(h2, layer["wg"])) * linear(h2, layer["wu"]))
+            x = f32(x + linear(a, layer["wd"]))
+            for j, tid in enumerate(tap_ids):
+                if tid == l:
+                    taps[j].append(x[0].copy())
+        hf = store(rmsnorm(x, TW["g_final"], tshape.eps))
+        z = lm_head_logits(hf, TW["lm_head"])
+        ids_out.append(int(argmax_lowest(z)[0]))
+    return np.array(ids_out, dtype=np.int32), np.array(taps, dtype=np.float64)
+
+
+def ar_generate(tshape, TW: dict, prompt: Sequence[int], n_new: int,
+                store=f32) -> np.ndarray:
+    """The target's own greedy autoregressive decode: n_new tokens."""
+    cache = TargetCache(tshape.n_layers)
+    ids, _ = target_forward(tshape, TW, cache, prompt, [], store)
+    out = [int(ids[-1])]
+    while len(out) < n_new:
+        ids, _ = target_forward(tshape, TW, cache, [out[-1]], [], store)
+        out.append(int(ids[0]))
+    return np.array(out, dtype=np.int32)
+
+
+def speculative_generate(tshape, TW: dict, dshape, DW: dict,
+                         prompt: Sequence[int], n_new: int, B: int,
+                         store=f32):
+    """Greedy DFlash loop ([reading] §9 steps 2-6).
+
+    Prefill the target (first token = first anchor; taps of every prompt
+    position become the context); then per round: inject the pending
+    context rows into every draft layer's cache, draft the block
+    [anchor, mask x (B-1)], verify it with one target forward, keep the
+    accepted prefix plus the bonus, crop the target cache to the new start,
+    and keep only the accepted positions' taps as the next context.
+
+    Returns (tokens [n_new], list of tau per round)."""
+    tap_ids = build_target_layer_ids(dshape.n_target_layers, dshape.n_pick)
+    cache = TargetCache(tshape.n_layers)
+    ids, taps = target_forward(tshape, TW, cache, prompt, tap_ids, store)
+    out = [int(ids[-1])]
+    start = len(prompt)
+    ctx_K = [np.zeros((0, dshape.G, dshape.d)) for _ in DW["layers"]]
+    ctx_V = [np.zeros((0, dshape.G, dshape.d)) for _ in DW["layers"]]
+    pending = taps                         # [n_pick, T, D]
+    taus = []
+    while len(out) < n_new:
+        # K/V injection of the pending context rows at their own positions
+        T = pending.shape[1]
+        H_t = fuse_context(list(pending), DW["wc"], DW["g_c"], dshape.eps, store)
+        pos = np.arange(start - T, start)
+        for l, layer in enumerate(DW["layers"]):
+            k, v = inject_kv(H_t, layer, pos, dshape.G, dshape.d,
+                             dshape.rope_theta, dshape.eps, store)
+            ctx_K[l] = np.concatenate([ctx_K[l], k], axis=0)
+            ctx_V[l] = np.concatenate([ctx_V[l], v], axis=0)
+        draft, _ = draft_block(dshape, DW, [[k] for k in ctx_K],
+                               [[v] for v in ctx_V], [out[-1]], B, store)
+        post, vtaps = target_forward(tshape, TW, cache, draft[0], tap_ids, store)
+        accept, bonus, toks, new_len = verify_greedy(draft, post[None, :],
+                                                     np.array([start]))
+        a = int(accept[0])
+        out.extend(int(t) for t in toks[0, :a + 1])
+        cache.crop(int(new_len[0]))
+        pending = vtaps[:, :a + 1, :]
+        start = int(new_len[0])
+        taus.append(a + 1)
+    return np.array(out[:n_new], dtype=np.int32), taus

@@ -1,0 +1,71 @@
+"""Losslessness pins of the oracle's greedy speculative loop.
+
+The greedy DFlash loop must emit exactly the target's own greedy
+autoregressive output (the verification rule makes the draft's quality
+irrelevant to the output)."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from helpers import make_all_accept, tiny_e2e, to_np
+
+
+def _weights(tshape, dshape, seed):
+    TW = to_np(synth.target_weights(tshape, "f32", seed))
+    DW = to_np(synth.draft_weights(dshape, "f32", seed + 1,
+                                   shared={"embed": None, "lm_head": None}))
+    DW["embed"], DW["lm_head"] = TW["embed"], TW["lm_head"]
+    return TW, DW
+
+
+@pytest.mark.parametrize("B", [4, 6])
+def test_speculative_equals_autoregressive(B):
+    tshape, dshape = tiny_e2e()
+    TW, DW = _weights(tshape, dshape, 50 + B)
+    prompt = synth.random_ids(12, tshape.V, seed=3).tolist()
+    n_new = 20
+    ar = O.ar_generate(tshape, TW, prompt, n_new)
+    spec, taus = O.speculative_generate(tshape, TW, dshape, DW, prompt, n_new, B)
+    np.testing.assert_array_equal(spec, ar)
+    assert all(1 <= t <= B for t in taus)
+    assert sum(taus) + 1 >= n_new
+
+
+def test_speculative_all_accepted_blocks():
+    """Every block fully accepted (tau = B): the crop/append bookkeeping of a
+    long accepted prefix still reproduces the autoregressive output."""
+    tshape, dshape = tiny_e2e()
+    TW, DW = _weights(tshape, dshape, 77)
+    c = 5
+    TW, DW = make_all_accept(TW, DW, tshape, c)
+    prompt = synth.random_ids(9, tshape.V, seed=4).tolist() + [c]
+    B, n_new = 4, 17
+    ar = O.ar_generate(tshape, TW, prompt, n_new)
+    assert (ar == c).all()
+    spec, taus = O.speculative_generate(tshape, TW, dshape, DW, prompt, n_new, B)
+    np.testing.assert_array_equal(spec, ar)
+    assert taus == [B] * len(taus)
+
+
+def test_speculative_equals_autoregressive_bf16_storage():
+    tshape, dshape = tiny_e2e()
+    TW, DW = _weights(tshape, dshape, 91)
+    prompt = synth.random_ids(10, tshape.V, seed=5).tolist()
+    ar = O.ar_generate(tshape, TW, prompt, 14, store=O.bf16)
+    spec, _ = O.speculative_generate(tshape, TW, dshape, DW, prompt, 14, 5, store=O.bf16)
+    np.testing.assert_array_equal(spec, ar)
+
+
+def test_draft_block_anchor_column_and_shapes():
+    w = synth.WORKLOADS["tiny_f32"]
+    s = w.draft
+    DW = to_np(synth.draft_weights(s, "f32", w.seed))
+    L = 5
+    rng = np.random.default_rng(0)
+    cK = [[rng.standard_normal((L, s.G, s.d)) for _ in range(2)] for _ in range(s.n_layers)]
+    cV = [[rng.standard_normal((L, s.G, s.d)) for _ in range(2)] for _ in range(s.n_layers)]
+    ids, gaps = O.draft_block(s, DW, cK, cV, [3, 900], w.B)
+    assert ids.shape == (2, w.B) and gaps.shape == (2, w.B - 1)
+    assert list(ids[:, 0]) == [3, 900]
+    assert (gaps >= 0).all() and ids.max() < s.V
