@@ -1,0 +1,472 @@
+"""Throughput of the DFlash draft path on GB300: draft blocks per second.
+
+One step = one speculative round of the hot path on one batch: fuse the
+pending target features (B rows per sequence) and inject them into every
+draft layer's cache, draft one block [anchor, mask x (B-1)] per sequence,
+and verify it greedily against a synthetic target posterior.  The context
+length is reset to L at the start of each step so every step sees the same
+context.  Weights and caches are random-init, seeded; inputs live in HBM
+before the timed region (the value) or in pinned host memory (e2e).
+
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "draft blocks/sec & µs per B=16 block (batch 1/32); % of HBM roofline"
+DEFAULT_WORKLOAD = "qwen3_8b_b1"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes / flops per unit of work
+# ---------------------------------------------------------------------------
+def layer_weight_bytes(s, esz):
+    per = (s.H * s.d * s.D + 2 * s.G * s.d * s.D + s.D * s.H * s.d + 3 * s.F * s.D)
+    return per * s.n_layers * esz
+
+
+def step_bytes(w, lens, esz):
+    """Bytes a step must move at least once: every weight it reads, the
+    cached context K/V, and the small activations in and out."""
+    s = w.draft
+    batch, B = w.batch, w.B
+    rows = batch * B
+    out = {}
+    out["weight_gemm"] = layer_weight_bytes(s, esz) + s.n_layers * rows * (s.D + s.H * s.d + s.F) * esz
+    out["lm_head"] = s.V * s.D * esz + batch * (B - 1) * s.D * esz
+    ctx = sum(int(l) + B for l in lens)     # context after this step's injection
+    out["attention"] = ctx * s.G * s.d * 2 * esz * s.n_layers
+    out["dense_gemm"] = (s.D * s.n_pick * s.D + 2 * s.G * s.d * s.D * s.n_layers) * esz + \
+        rows * s.n_pick * s.D * esz
+    return out
+
+
+# ---------------------------------------------------------------------------
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        try:
+            u = str(torch.cuda.get_device_properties(index).uuid)
+            self.index = u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            self.index = str(index)
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+class Draft:
+    """Device state of one replica: weights, cache, workspace, step buffers."""
+
+    def __init__(self, w, rank, n_steps_total, with_model=True):
+        self.w = w
+        s = w.draft
+        dev = "cuda"
+        self.lens = synth.ctx_lengths(w)
+        self.L_max = max(self.lens)
+        self.batch, self.B = w.batch, w.B
+        rows = self.batch * self.B
+        self.rows = rows
+        td = synth.torch_dtype(w.dtype)
+        seed = w.seed + 100 * rank
+        self.weights = synth.draft_weights(s, w.dtype, seed, device=dev)
+        self.len0 = torch.tensor(self.lens, dtype=torch.int32, device=dev)
+        self.hidden = synth.target_hidden_states(rows, s.D, s.n_pick, w.dtype, seed + 1, device=dev)
+        self.anchor = torch.from_numpy(synth.anchors(self.batch, s.V, s.mask_id, seed)).to(dev)
+        self.post = torch.from_numpy(synth.random_ids((self.batch, self.B), s.V, seed + 2)).to(dev)
+        self.start = torch.tensor(self.lens, dtype=torch.int32, device=dev)
+        if not with_model:
+            return
+        import block_diffusion_drafter_layer_gb300 as dfl
+        from synth.gpu import draft_model, kv_cache
+        self.dfl = dfl
+        cap = self.L_max + 2 * self.B + 8
+        self.model = draft_model(s, w.dtype, self.weights, max_pos=cap + 8)
+        self.kv = kv_cache(s, self.batch, cap, w.dtype)
+        self.ws = self.model.workspace(rows)
+        # prefill context: fuse + inject every sequence's L_b rows
+        self.T_pre = sum(self.lens)
+        self.pre_hidden = synth.target_hidden_states(self.T_pre, s.D, s.n_pick, w.dtype, seed,
+                                                     device=dev)
+        self.pre_Ht = torch.empty(self.T_pre, s.D, dtype=td, device=dev)
+        cu = np.concatenate([[0], np.cumsum(self.lens)[:-1]]).astype(np.int32)
+        self.pre_row0 = torch.from_numpy(cu).to(dev)
+        self.pre_rows = torch.tensor(self.lens, dtype=torch.int32, device=dev)
+        # per-step buffers: B pending feature rows per sequence in, ids out
+        self.Ht = torch.empty(rows, s.D, dtype=td, device=dev)
+        self.row0 = torch.arange(0, rows, self.B, dtype=torch.int32, device=dev)
+        self.nrow = torch.full((self.batch,), self.B, dtype=torch.int32, device=dev)
+        i32 = lambda *sh: torch.empty(*sh, dtype=torch.int32, device=dev)
+        self.ids, self.acc, self.tau, self.bonus = i32(self.batch, self.B), i32(self.batch), \
+            i32(self.batch), i32(self.batch)
+        self.out_tokens = i32(self.batch, self.B)
+
+    def prefill(self):
+        d, m = self.dfl, self.model
+        self.kv.len.zero_()
+        d.dflash_fuse_context(m.handle, self.pre_hidden, self.T_pre, self.pre_Ht, self.ws)
+        d.dflash_inject_kv(m.handle, self.pre_Ht, self.T_pre, self.pre_row0, self.pre_rows,
+                           self.batch, self.kv.struct, self.ws)
+
+    def step(self):
+        d, m = self.dfl, self.model
+        self.kv.len.copy_(self.len0)
+        d.dflash_fuse_context(m.handle, self.hidden, self.rows, self.Ht, self.ws)
+        d.dflash_inject_kv(m.handle, self.Ht, self.rows, self.row0, self.nrow, self.batch,
+                           self.kv.struct, self.ws)
+        d.dflash_draft_block(m.handle, self.anchor, self.batch, self.B, self.kv.struct, self.ids,
+                             None, None, self.ws)
+        d.dflash_verify_greedy(self.ids, self.post, self.batch, self.B, self.start, self.acc,
+                               self.tau, self.bonus, self.out_tokens, None)
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x, world):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(fn, K, world):
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for _ in range(K):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    _barrier(world)
+    return e0.elapsed_time(e1) / 1e3
+
+
+# ---------------------------------------------------------------------------
+def oracle_inputs(st):
+    """Host inputs of one replica for the CPU oracle: the same seeded weights
+    (fp64), step rows, anchors and posterior; the cached context is a seeded
+    synthetic K/V of the same lengths (the oracle never reads anything the
+    CUDA path computed)."""
+    s = st.w.draft
+    to64 = lambda t: t.detach().float().cpu().numpy().astype(np.float64)
+    W = {"wc": to64(st.weights["wc"]), "g_c": to64(st.weights["g_c"]),
+         "g_f": to64(st.weights["g_f"]), "embed": st.weights["embed"].float().cpu().numpy(),
+         "lm_head": to64(st.weights["lm_head"]),
+         "layers": [{k: to64(v) for k, v in lay.items()} for lay in st.weights["layers"]]}
+    K, V = synth.random_kv_cache(st.batch, s.G, st.L_max, s.d, s.n_layers, 0.02 * np.sqrt(s.D),
+                                 st.w.dtype, st.w.seed, device="cuda")
+    cK = [[K[l][b, :, :st.lens[b]].float().cpu().numpy().astype(np.float64).transpose(1, 0, 2)
+           for b in range(st.batch)] for l in range(s.n_layers)]
+    cV = [[V[l][b, :, :st.lens[b]].float().cpu().numpy().astype(np.float64).transpose(1, 0, 2)
+           for b in range(st.batch)] for l in range(s.n_layers)]
+    del K, V
+    hid = [h.float().cpu().numpy().astype(np.float64) for h in st.hidden]
+    return W, cK, cV, hid, st.anchor.cpu().numpy(), st.post.cpu().numpy(), st.start.cpu().numpy()
+
+
+def oracle_step(w, W, cK, cV, hid, anchors, post, start, seqs):
+    """One oracle round for the sequences in ``seqs``: fuse + inject of the
+    B pending rows, draft block, verify."""
+    import oracle as O
+    s, B = w.draft, w.B
+    store = O.storage(w.dtype)
+    rows = np.concatenate([np.arange(b * B, (b + 1) * B) for b in seqs])
+    Ht = O.fuse_context([h[rows] for h in hid], W["wc"], W["g_c"], s.eps, store)
+    K2, V2 = [], []
+    for l, lay in enumerate(W["layers"]):
+        Kl, Vl = [], []
+        for j, b in enumerate(seqs):
+            L = cK[l][b].shape[0]
+            k, v = O.inject_kv(Ht[j * B:(j + 1) * B], lay, np.arange(L, L + B), s.G, s.d,
+                               s.rope_theta, s.eps, store)
+            Kl.append(np.concatenate([cK[l][b], k]))
+            Vl.append(np.concatenate([cV[l][b], v]))
+        K2.append(Kl)
+        V2.append(Vl)
+    ids, _ = O.draft_block(s, W, K2, V2, anchors[list(seqs)], B, store)
+    O.verify_greedy(ids, post[list(seqs)], start[list(seqs)])
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(st, budget_s=12.0):
+    """The oracle as it stands, on this host's cores, one sequence per round,
+    repeated until ``budget_s`` of CPU work; scaled to blocks/s."""
+    W, cK, cV, hid, anchors, post, start = oracle_inputs(st)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(st.w, W, cK, cV, hid, anchors, post, start, [n % st.batch])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 64:
+            break
+    return {"value": n / el, "unit": "blocks/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} oracle rounds (fuse+inject of {st.B} rows, one B={st.B} draft block, "
+                      f"verify) of one sequence each, {el:.1f} s, numpy fp64"}
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    """The CPU oracle on the same workload: each step is one sequence's round
+    (the whole batch's rows are independent), scaled to blocks/s."""
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    st = Draft(w, 0, 1, with_model=False)
+    W, cK, cV, hid, anchors, post, start = oracle_inputs(st)
+    del st
+    torch.cuda.empty_cache()
+    for i in range(args.warmup):
+        oracle_step(w, W, cK, cV, hid, anchors, post, start, [i % w.batch])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_step(w, W, cK, cV, hid, anchors, post, start, [i % w.batch])
+    el = time.perf_counter() - t0
+    value = args.steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "blocks/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, st_lens=synth.ctx_lengths(w)),
+            "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": cpu_cores(),
+                             "kind": "oracle",
+                             "sample": f"each step is one sequence's round (fuse+inject of {w.B} "
+                                       f"rows, one B={w.B} draft block, verify), numpy fp64"},
+            "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _config(w, st_lens):
+    s = w.draft
+    return {"workload": w.name, "draft": f"{s.n_layers} layers, D={s.D}, H={s.H}, G={s.G}, "
+                                         f"d={s.d}, F={s.F}, V={s.V}",
+            "batch": w.batch, "B": w.B, "ctx_len": (w.ctx_len if w.ctx_range is None
+                                                    else f"U{list(w.ctx_range)} mean {np.mean(st_lens):.0f}"),
+            "step": f"fuse+inject {w.B} rows/seq, draft block, verify",
+            "l2": "inputs larger than L2 (weights streamed every step)",
+            "parallelism": "replicas"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+            return
+        run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+def run_ours(args, rank, world, local):
+    import block_diffusion_drafter_layer_gb300 as dfl
+    w = synth.WORKLOADS[args.workload]
+    if w.dtype != "bf16" or w.target is not None:
+        raise SystemExit("bench.py times the bf16 draft workloads")
+    hbm, tf_burst, tf_sust, peak_kind = _peaks()
+    st = Draft(w, rank, args.steps * 3 + args.warmup * 3)
+    esz = 2
+
+    # prefill: the context projection at L (timed on its own)
+    st.prefill()
+    torch.cuda.synchronize()
+    t_fuse = []
+    s = torch.cuda.current_stream()
+    for i in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        dfl.dflash_fuse_context(st.model.handle, st.pre_hidden, st.T_pre, st.pre_Ht, st.ws)
+        e1.record(s)
+        torch.cuda.synchronize()
+        if i:
+            t_fuse.append(e0.elapsed_time(e1) / 1e3)
+    st.prefill()
+    torch.cuda.synchronize()
+    fuse_flops = 2.0 * st.T_pre * w.draft.D * w.draft.n_pick * w.draft.D
+    fuse_tf = fuse_flops / np.median(t_fuse) / 1e12
+
+    # device-resident timed region
+    for _ in range(args.warmup):
+        st.step()
+    n0 = dfl.dflash_launch_count()
+    clocks = Clocks(local)
+    clocks.start()
+    t = time_steps(st.step, args.steps, world)
+    clk = clocks.stop()
+    launches = dfl.dflash_launch_count() - n0
+    t = _max_over_ranks(t, world)
+    blocks = w.batch * args.steps * world
+    value = blocks / t
+    ms_step = t / args.steps * 1e3
+
+    # per-kernel-class device time over an identical region (events per launch)
+    dfl.dflash_timing_enable(st.model.handle, True)
+    for k in range(dfl.K_NCLASS):
+        dfl.dflash_timing_read(st.model.handle, k)
+    time_steps(st.step, args.steps, world)
+    cls = {}
+    for k, name in enumerate(["weight_gemm", "attention", "lm_head", "dense_gemm", "elementwise"]):
+        ms, n = dfl.dflash_timing_read(st.model.handle, k)
+        cls[name] = (ms / args.steps, n / args.steps)
+    dfl.dflash_timing_enable(st.model.handle, False)
+    nbytes = step_bytes(w, st.lens, esz)
+    dom = max(["weight_gemm", "lm_head", "attention", "dense_gemm"], key=lambda k: cls[k][0])
+    ach = nbytes[dom] / (cls[dom][0] / 1e3) / 1e9
+    roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
+            "frac": ach / hbm, "peak_kind": peak_kind,
+            "traffic": None, "launches_per_step": cls[dom][1],
+            "algorithmic_bytes_per_step": nbytes[dom],
+            "class_ms_per_step": {k: round(v[0], 4) for k, v in cls.items()}}
+    total_bytes = sum(nbytes[k] for k in ("weight_gemm", "lm_head", "attention", "dense_gemm"))
+    step_frac = total_bytes / (ms_step / 1e3) / 1e9 / hbm
+
+    # end to end through the C ABI from pinned host memory
+    h_hidden = [torch.empty_like(h, device="cpu").pin_memory() for h in st.hidden]
+    for hh, hd in zip(h_hidden, st.hidden):
+        hh.copy_(hd)
+    h_anchor = st.anchor.cpu().pin_memory()
+    h_post = st.post.cpu().pin_memory()
+    h_ids = torch.empty(st.batch, st.B, dtype=torch.int32).pin_memory()
+    h_acc = torch.empty(st.batch, dtype=torch.int32).pin_memory()
+    h_bonus = torch.empty(st.batch, dtype=torch.int32).pin_memory()
+    h_out = torch.empty(st.batch, st.B, dtype=torch.int32).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for h in h_hidden) + h_anchor.numel() * 4 + h_post.numel() * 4
+    d2h = (h_ids.numel() + h_acc.numel() + h_bonus.numel() + h_out.numel()) * 4
+
+    def e2e_step():
+        for hh, hd in zip(h_hidden, st.hidden):
+            hd.copy_(hh, non_blocking=True)
+        st.anchor.copy_(h_anchor, non_blocking=True)
+        st.post.copy_(h_post, non_blocking=True)
+        st.step()
+        h_ids.copy_(st.ids, non_blocking=True)
+        h_acc.copy_(st.acc, non_blocking=True)
+        h_bonus.copy_(st.bonus, non_blocking=True)
+        h_out.copy_(st.out_tokens, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(args.warmup):
+        e2e_step()
+    t0 = time.perf_counter()
+    _barrier(world)
+    for _ in range(args.steps):
+        e2e_step()
+    _barrier(world)
+    te = _max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": w.batch * args.steps * world / te, "unit": "blocks/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(st)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+                "us_per_block": ms_step * 1e3 / w.batch,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic", "config": _config(w, st.lens),
+                "roofline": roof,
+                "step_hbm_frac": step_frac,
+                "step_algorithmic_bytes": total_bytes,
+                "context_projection": {"T": st.T_pre, "tflops": fuse_tf, "peak": tf_burst,
+                                       "frac": fuse_tf / tf_burst, "unit": "TFLOP/s",
+                                       "peak_kind": f"bf16 burst, {peak_kind}"},
+                "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+                "clocks": clk}
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

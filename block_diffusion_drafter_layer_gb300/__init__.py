@@ -1,0 +1,266 @@
+"""Python binding of libdflash (the DFlash draft path on GB300, sm_103a).
+
+Thin ctypes marshalling over the C ABI in ``include/dflash.h``: every
+function here has the C function's name, turns torch tensors into device
+pointers and the current CUDA stream into a ``cudaStream_t``, and raises
+``DFlashError`` on a non-zero status.  All arithmetic runs in the library's
+CUDA kernels; PyTorch only provides device memory and streams.  Importing
+this module fails loudly if ``libdflash.so`` has not been built.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdflash.so")
+
+MAX_LAYERS = 16
+MAX_PICK = 8
+F32, BF16 = 0, 1
+K_WEIGHT_GEMM, K_ATTENTION, K_LM_HEAD, K_DENSE_GEMM, K_ELEMENTWISE, K_VERIFY = range(6)
+K_NCLASS = 6
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {dflash_strerror(code)} (code {code})")
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libdflash.so is not built ({LIB_PATH}); run "
+                      "block_diffusion_drafter_layer_gb300/build.py")
+_lib = C.CDLL(LIB_PATH)
+
+
+class dflash_config(C.Structure):
+    _fields_ = [("hidden", C.c_int32), ("n_heads", C.c_int32), ("n_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("ffn", C.c_int32), ("vocab", C.c_int32),
+                ("n_layers", C.c_int32), ("n_target_layers", C.c_int32), ("n_pick", C.c_int32),
+                ("target_layer_ids", C.c_int32 * MAX_PICK), ("mask_token_id", C.c_int32),
+                ("max_pos", C.c_int32), ("qk_norm", C.c_int32), ("dtype", C.c_int32),
+                ("rope_theta", C.c_float), ("rms_eps", C.c_float), ("embed_scale", C.c_float)]
+
+
+class dflash_layer_weights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd",
+                                          "g_in", "g_post", "q_norm", "k_norm")]
+
+
+class dflash_weights(C.Structure):
+    _fields_ = [("wc", C.c_void_p), ("g_c", C.c_void_p), ("g_f", C.c_void_p),
+                ("embed", C.c_void_p), ("lm_head", C.c_void_p),
+                ("layers", dflash_layer_weights * MAX_LAYERS)]
+
+
+class dflash_kv(C.Structure):
+    _fields_ = [("k", C.c_void_p * MAX_LAYERS), ("v", C.c_void_p * MAX_LAYERS),
+                ("len", C.c_void_p), ("cap", C.c_int32), ("batch_cap", C.c_int32)]
+
+
+_P = C.c_void_p
+_sig = {
+    "dflash_create": (C.c_int, [C.POINTER(dflash_config), C.POINTER(dflash_weights), C.POINTER(_P)]),
+    "dflash_destroy": (C.c_int, [_P]),
+    "dflash_workspace_bytes": (C.c_size_t, [_P, C.c_int64]),
+    "dflash_build_target_layer_ids": (C.c_int, [C.c_int32, C.c_int32, C.POINTER(C.c_int32)]),
+    "dflash_fuse_context": (C.c_int, [_P, C.POINTER(_P), C.c_int64, _P, _P, C.c_size_t, _P]),
+    "dflash_inject_kv": (C.c_int, [_P, _P, C.c_int64, _P, _P, C.c_int32, C.POINTER(dflash_kv),
+                                   _P, C.c_size_t, _P]),
+    "dflash_draft_block": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.POINTER(dflash_kv), _P, _P,
+                                     _P, _P, C.c_size_t, _P]),
+    "dflash_verify_greedy": (C.c_int, [_P, _P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
+    "dflash_lm_head_argmax": (C.c_int, [_P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
+    "dflash_target_forward": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.POINTER(dflash_kv),
+                                        C.POINTER(C.c_int32), C.c_int32, _P, _P, _P, C.c_size_t,
+                                        _P]),
+    "dflash_get_status": (C.c_int, [_P, _P]),
+    "dflash_strerror": (C.c_char_p, [C.c_int]),
+    "dflash_launch_count": (C.c_int64, []),
+    "dflash_timing_enable": (C.c_int, [_P, C.c_int]),
+    "dflash_timing_read": (C.c_int, [_P, C.c_int32, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
+}
+for _name, (_res, _args) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+EXPORTED = tuple(_sig)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise DFlashError(rc, where)
+
+
+def dflash_strerror(code: int) -> str:
+    return _lib.dflash_strerror(code).decode()
+
+
+def dflash_launch_count() -> int:
+    return int(_lib.dflash_launch_count())
+
+
+def dflash_build_target_layer_ids(n_target_layers: int, n_pick: int) -> list:
+    out = (C.c_int32 * max(n_pick, 1))()
+    _check(_lib.dflash_build_target_layer_ids(n_target_layers, n_pick, out),
+           "dflash_build_target_layer_ids")
+    return list(out)[:n_pick]
+
+
+def dflash_create(cfg: dflash_config, w: dflash_weights) -> int:
+    h = _P()
+    _check(_lib.dflash_create(C.byref(cfg), C.byref(w), C.byref(h)), "dflash_create")
+    return h.value
+
+
+def dflash_destroy(h: int):
+    _check(_lib.dflash_destroy(h), "dflash_destroy")
+
+
+def dflash_workspace_bytes(h: int, max_rows: int) -> int:
+    return int(_lib.dflash_workspace_bytes(h, max_rows))
+
+
+def dflash_fuse_context(h: int, hidden: Sequence[torch.Tensor], T: int, h_t_out: torch.Tensor,
+                        ws: torch.Tensor, stream=None):
+    arr = (_P * len(hidden))(*[_ptr(x) for x in hidden])
+    _check(_lib.dflash_fuse_context(h, arr, T, _ptr(h_t_out), _ptr(ws), ws.numel() * ws.element_size(),
+                                    _stream(stream)), "dflash_fuse_context")
+
+
+def dflash_inject_kv(h: int, h_t: torch.Tensor, n_rows: int, seq_row0: torch.Tensor,
+                     seq_rows: torch.Tensor, batch: int, kv: dflash_kv, ws: torch.Tensor,
+                     stream=None):
+    _check(_lib.dflash_inject_kv(h, _ptr(h_t), n_rows, _ptr(seq_row0), _ptr(seq_rows), batch,
+                                 C.byref(kv), _ptr(ws), ws.numel() * ws.element_size(),
+                                 _stream(stream)), "dflash_inject_kv")
+
+
+def dflash_draft_block(h: int, anchor: torch.Tensor, batch: int, B: int, kv: dflash_kv,
+                       draft_ids: torch.Tensor, top2_gap: Optional[torch.Tensor],
+                       hidden_out: Optional[torch.Tensor], ws: torch.Tensor, stream=None):
+    _check(_lib.dflash_draft_block(h, _ptr(anchor), batch, B, C.byref(kv), _ptr(draft_ids),
+                                   _ptr(top2_gap), _ptr(hidden_out), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream)),
+           "dflash_draft_block")
+
+
+def dflash_verify_greedy(draft: torch.Tensor, post: torch.Tensor, batch: int, B: int,
+                         start: torch.Tensor, accept: torch.Tensor, tau: Optional[torch.Tensor],
+                         bonus: torch.Tensor, out_tokens: torch.Tensor,
+                         new_len: Optional[torch.Tensor], stream=None):
+    _check(_lib.dflash_verify_greedy(_ptr(draft), _ptr(post), batch, B, _ptr(start), _ptr(accept),
+                                     _ptr(tau), _ptr(bonus), _ptr(out_tokens), _ptr(new_len),
+                                     _stream(stream)), "dflash_verify_greedy")
+
+
+def dflash_lm_head_argmax(h: int, x: torch.Tensor, rows: int, norm_gain: torch.Tensor,
+                          ids: torch.Tensor, top2_gap: Optional[torch.Tensor], ws: torch.Tensor,
+                          stream=None):
+    _check(_lib.dflash_lm_head_argmax(h, _ptr(x), rows, _ptr(norm_gain), _ptr(ids), _ptr(top2_gap),
+                                      _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "dflash_lm_head_argmax")
+
+
+def dflash_target_forward(h: int, tokens: torch.Tensor, batch: int, T: int, kv: dflash_kv,
+                          tap_ids: Sequence[int], taps_out: Optional[torch.Tensor],
+                          argmax_out: torch.Tensor, ws: torch.Tensor, stream=None):
+    ids = (C.c_int32 * max(len(tap_ids), 1))(*tap_ids)
+    _check(_lib.dflash_target_forward(h, _ptr(tokens), batch, T, C.byref(kv), ids, len(tap_ids),
+                                      _ptr(taps_out), _ptr(argmax_out), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _stream(stream)),
+           "dflash_target_forward")
+
+
+def dflash_get_status(h: int, stream=None) -> int:
+    return int(_lib.dflash_get_status(h, _stream(stream)))
+
+
+def dflash_timing_enable(h: int, on: bool):
+    _check(_lib.dflash_timing_enable(h, 1 if on else 0), "dflash_timing_enable")
+
+
+def dflash_timing_read(h: int, kclass: int):
+    ms, n = C.c_double(), C.c_int64()
+    _check(_lib.dflash_timing_read(h, kclass, C.byref(ms), C.byref(n)), "dflash_timing_read")
+    return ms.value, n.value
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers: build the C structs from tensors and keep them alive
+# ---------------------------------------------------------------------------
+class Model:
+    """A created handle plus the tensors its weight struct points at."""
+
+    def __init__(self, *, D, H, G, d, F, V, n_layers, dtype: str, weights: dict, max_pos: int,
+                 qk_norm: bool, mask_id: int = 0, n_target_layers: int = 0, n_pick: int = 5,
+                 target_layer_ids: Sequence[int] = (), rope_theta=1e6, eps=1e-6,
+                 embed_scale=1.0):
+        cfg = dflash_config()
+        cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim = D, H, G, d
+        cfg.ffn, cfg.vocab, cfg.n_layers = F, V, n_layers
+        cfg.n_target_layers, cfg.n_pick = n_target_layers, n_pick
+        for i, v in enumerate(target_layer_ids):
+            cfg.target_layer_ids[i] = v
+        cfg.mask_token_id, cfg.max_pos, cfg.qk_norm = mask_id, max_pos, 1 if qk_norm else 0
+        cfg.dtype = BF16 if dtype == "bf16" else F32
+        cfg.rope_theta, cfg.rms_eps, cfg.embed_scale = rope_theta, eps, embed_scale
+        w = dflash_weights()
+        w.wc, w.g_c = _ptr(weights.get("wc")), _ptr(weights.get("g_c"))
+        w.g_f = _ptr(weights.get("g_f", weights.get("g_final")))
+        w.embed, w.lm_head = _ptr(weights["embed"]), _ptr(weights["lm_head"])
+        for l, lay in enumerate(weights["layers"]):
+            for name in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "g_in", "g_post",
+                         "q_norm", "k_norm"):
+                setattr(w.layers[l], name, _ptr(lay.get(name)))
+        self.cfg, self.w, self.weights = cfg, w, weights
+        self.dtype = dtype
+        self.handle = dflash_create(cfg, w)
+
+    def workspace(self, max_rows: int, device="cuda") -> torch.Tensor:
+        n = dflash_workspace_bytes(self.handle, max_rows)
+        return torch.empty(n, dtype=torch.uint8, device=device)
+
+    def close(self):
+        if self.handle:
+            dflash_destroy(self.handle)
+            self.handle = None
+
+
+class KVCache:
+    """Per-layer [batch_cap, G, cap, d] K/V tensors and the int32 length vector."""
+
+    def __init__(self, n_layers: int, batch_cap: int, G: int, cap: int, d: int, dtype: str,
+                 device="cuda", k=None, v=None):
+        td = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.k = k if k is not None else [torch.zeros(batch_cap, G, cap, d, dtype=td, device=device)
+                                          for _ in range(n_layers)]
+        self.v = v if v is not None else [torch.zeros(batch_cap, G, cap, d, dtype=td, device=device)
+                                          for _ in range(n_layers)]
+        self.len = torch.zeros(batch_cap, dtype=torch.int32, device=device)
+        s = dflash_kv()
+        for l in range(n_layers):
+            s.k[l], s.v[l] = _ptr(self.k[l]), _ptr(self.v[l])
+        s.len, s.cap, s.batch_cap = _ptr(self.len), cap, batch_cap
+        self.struct = s

@@ -1,0 +1,519 @@
+// C ABI of libdflash: argument validation, workspace layout and the order of
+// kernels for each call of the DFlash draft path.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "common.cuh"
+
+namespace dflash {
+
+static std::atomic<int64_t> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static cudaEvent_t take_event(dflash_handle* h) {
+  if (!h->free_events.empty()) {
+    cudaEvent_t e = h->free_events.back();
+    h->free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+void launch_begin(dflash_handle* h, int kclass, cudaStream_t s, Timer* t) {
+  t->kclass = kclass;
+  t->a = t->b = nullptr;
+  if (h && h->timing) {
+    t->a = take_event(h);
+    cudaEventRecord(t->a, s);
+  }
+}
+
+int launch_end(dflash_handle* h, cudaStream_t s, Timer* t) {
+  count_launch();
+  const cudaError_t e = cudaGetLastError();
+  if (h && t->a) {
+    t->b = take_event(h);
+    cudaEventRecord(t->b, s);
+    h->pending.push_back(*t);
+  }
+  return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
+static size_t esize(int dtype) { return dtype == DFLASH_BF16 ? 2 : 4; }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Rows of fuse / inject processed per pass (bounds the fp32 staging buffers).
+constexpr int64_t kChunkRows = 4096;
+
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace of a forward pass (draft block, target forward, LM head) over R rows.
+static size_t forward_bytes(const dflash_config& c, int64_t R) {
+  const size_t sz = esize(c.dtype);
+  const int64_t D = c.hidden, Hd = (int64_t)c.n_heads * c.head_dim,
+                Gd = (int64_t)c.n_kv_heads * c.head_dim, F = c.ffn, V = c.vocab;
+  size_t b = 0;
+  b += round256(R * D * 4);           // x
+  b += round256(R * std::max(D, F) * sz);  // h / a
+  b += round256(R * Hd * 4);          // qf
+  b += round256(R * Gd * 4) * 2;      // kf, vf
+  b += round256(R * Hd * sz);         // q
+  b += round256(R * Gd * sz) * 2;     // kb, vb
+  b += round256(R * Hd * sz);         // o
+  b += round256(R * F * 4) * 2;       // gf, uf
+  b += round256(R * D * sz);          // hf
+  b += round256(R * V * 4);           // logits
+  return b + 1024;
+}
+
+// Per-row workspace of fuse / inject passes.
+static size_t chunk_row_bytes(const dflash_config& c) {
+  const int64_t D = c.hidden, Gd = (int64_t)c.n_kv_heads * c.head_dim;
+  return (size_t)std::max<int64_t>(D * 4, 2 * Gd * 4);
+}
+
+struct Fwd {
+  float *x, *qf, *kf, *vf, *gf, *uf, *logits;
+  void *h, *q, *kb, *vb, *o, *hf;
+};
+
+static bool carve_forward(const dflash_config& c, int64_t R, void* ws, size_t ws_bytes, Fwd* f) {
+  const size_t sz = esize(c.dtype);
+  const int64_t D = c.hidden, Hd = (int64_t)c.n_heads * c.head_dim,
+                Gd = (int64_t)c.n_kv_heads * c.head_dim, F = c.ffn, V = c.vocab;
+  Carve cv{(char*)ws, ws_bytes};
+  f->x = cv.take<float>(R * D);
+  f->h = cv.take<char>(R * std::max(D, F) * sz);
+  f->qf = cv.take<float>(R * Hd);
+  f->kf = cv.take<float>(R * Gd);
+  f->vf = cv.take<float>(R * Gd);
+  f->q = cv.take<char>(R * Hd * sz);
+  f->kb = cv.take<char>(R * Gd * sz);
+  f->vb = cv.take<char>(R * Gd * sz);
+  f->o = cv.take<char>(R * Hd * sz);
+  f->gf = cv.take<float>(R * F);
+  f->uf = cv.take<float>(R * F);
+  f->hf = cv.take<char>(R * D * sz);
+  f->logits = cv.take<float>(R * V);
+  return cv.ok;
+}
+
+static ASrc one_src(const void* p, int64_t ld, int K) {
+  ASrc a{};
+  a.p[0] = p;
+  a.nseg = 1;
+  a.seg = K;
+  a.ld = ld;
+  return a;
+}
+
+static const char* byte_off(const void* p, int64_t elems, int dtype) {
+  return (const char*)p + elems * (int64_t)esize(dtype);
+}
+
+// SwiGLU FFN + o_proj residual of one layer (shared by draft and target).
+static int mlp_tail(dflash_handle* h, cudaStream_t s, const dflash_layer_weights& L, Fwd& f,
+                    int64_t R) {
+  const dflash_config& c = h->cfg;
+  const int D = c.hidden, F = c.ffn, Hd = c.n_heads * c.head_dim, dt = c.dtype;
+  int rc;
+  if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, one_src(f.o, Hd, Hd), L.wo, Hd, f.x, D, R, D, Hd,
+                 true)))
+    return rc;
+  if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, L.g_post, R, D, c.rms_eps, 0)))
+    return rc;
+  if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, one_src(f.h, D, D), L.wg, D, f.gf, F, R, F, D,
+                 false)))
+    return rc;
+  if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, one_src(f.h, D, D), L.wu, D, f.uf, F, R, F, D,
+                 false)))
+    return rc;
+  if ((rc = swiglu(h, s, dt, f.gf, f.uf, f.h, R * F))) return rc;
+  return gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, one_src(f.h, F, F), L.wd, F, f.x, D, R, D, F, true);
+}
+
+static int lm_head(dflash_handle* h, cudaStream_t s, Fwd& f, const float* x, int64_t rows,
+                   const float* gain, int skip_first_of, int32_t* ids, float* gap, int rps_out,
+                   const int32_t* anchor) {
+  const dflash_config& c = h->cfg;
+  const int D = c.hidden, V = c.vocab, dt = c.dtype;
+  int rc;
+  if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, x, D, f.hf, D, gain, rows, D, c.rms_eps,
+                         skip_first_of)))
+    return rc;
+  if ((rc = gemm(h, s, DFLASH_K_LM_HEAD, dt, one_src(f.hf, D, D), h->w.lm_head, D, f.logits, V,
+                 rows, V, D, false)))
+    return rc;
+  return argmax_rows(h, s, f.logits, rows, V, ids, gap, rps_out, anchor);
+}
+
+static bool kv_ok(const dflash_handle* h, const dflash_kv* kv, int batch) {
+  if (!kv || !kv->len || kv->cap <= 0 || kv->batch_cap < batch) return false;
+  for (int l = 0; l < h->cfg.n_layers; ++l)
+    if (!kv->k[l] || !kv->v[l] || !aligned16(kv->k[l]) || !aligned16(kv->v[l])) return false;
+  return true;
+}
+
+}  // namespace dflash
+
+using namespace dflash;
+
+extern "C" {
+
+const char* dflash_strerror(int code) {
+  switch (code) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_SHAPE: return "unsupported shape";
+    case DFLASH_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case DFLASH_ERR_CAPACITY: return "K/V cache capacity exceeded";
+    case DFLASH_ERR_UNSUPPORTED: return "unsupported dtype, head_dim or device";
+    case DFLASH_ERR_CUDA: return "CUDA error";
+    case DFLASH_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case DFLASH_ERR_DEVICE_BOUNDS: return "token id or position out of range";
+    case DFLASH_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown error";
+  }
+}
+
+int64_t dflash_launch_count(void) { return g_launches.load(); }
+
+int dflash_build_target_layer_ids(int32_t n_target_layers, int32_t n_pick, int32_t* ids_out) {
+  if (!ids_out || n_pick < 1 || n_pick > DFLASH_MAX_PICK) return DFLASH_ERR_INVALID_ARG;
+  if (n_pick == 1) {
+    ids_out[0] = n_target_layers / 2;
+    return DFLASH_OK;
+  }
+  const int lo = 1, hi = n_target_layers - 3;
+  if (hi < lo) return DFLASH_ERR_SHAPE;
+  const int64_t span = hi - lo;
+  for (int i = 0; i < n_pick; ++i)
+    ids_out[i] = lo + (int32_t)((2 * i * span + (n_pick - 1)) / (2 * (n_pick - 1)));
+  return DFLASH_OK;
+}
+
+int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out) {
+  if (!cfg || !w || !out) return DFLASH_ERR_INVALID_ARG;
+  *out = nullptr;
+  const dflash_config& c = *cfg;
+  if (c.dtype != DFLASH_F32 && c.dtype != DFLASH_BF16) return DFLASH_ERR_UNSUPPORTED;
+  if (c.head_dim != 64 && c.head_dim != 128) return DFLASH_ERR_UNSUPPORTED;
+  if (c.hidden <= 0 || c.hidden % 8 || c.n_heads <= 0 || c.n_kv_heads <= 0 ||
+      c.n_heads % c.n_kv_heads || c.ffn <= 0 || c.ffn % 8 || c.vocab <= 0 || c.n_layers < 1 ||
+      c.n_layers > DFLASH_MAX_LAYERS || c.n_pick < 1 || c.n_pick > DFLASH_MAX_PICK ||
+      c.max_pos <= 0 || c.mask_token_id < 0 || c.mask_token_id >= c.vocab || !(c.rms_eps > 0.f))
+    return DFLASH_ERR_SHAPE;
+  if (!w->embed || !w->lm_head || !w->g_f) return DFLASH_ERR_INVALID_ARG;
+  const void* al[] = {w->embed, w->lm_head, w->wc};
+  for (const void* p : al)
+    if (p && !aligned16(p)) return DFLASH_ERR_ALIGNMENT;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& L = w->layers[l];
+    const void* ps[] = {L.wq, L.wk, L.wv, L.wo, L.wg, L.wu, L.wd};
+    for (const void* p : ps) {
+      if (!p) return DFLASH_ERR_INVALID_ARG;
+      if (!aligned16(p)) return DFLASH_ERR_ALIGNMENT;
+    }
+    if (!L.g_in || !L.g_post) return DFLASH_ERR_INVALID_ARG;
+    if (c.qk_norm && (!L.q_norm || !L.k_norm)) return DFLASH_ERR_INVALID_ARG;
+  }
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DFLASH_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return DFLASH_ERR_UNSUPPORTED;
+
+  dflash_handle* h = new dflash_handle();
+  h->cfg = c;
+  h->w = *w;
+  h->device = dev;
+  if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess) {
+    delete h;
+    return DFLASH_ERR_CUDA;
+  }
+  cudaMemset(h->d_status, 0, sizeof(int));
+  // RoPE table: angle pos * theta^(-2i/d) in double precision, stored as fp32.
+  const int half = c.head_dim / 2;
+  std::vector<float2> tab((size_t)c.max_pos * half);
+  for (int64_t p = 0; p < c.max_pos; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double ang =
+          (double)p * std::pow((double)c.rope_theta, -2.0 * (double)i / (double)c.head_dim);
+      tab[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+    }
+  if (cudaMalloc(&h->d_rope, tab.size() * sizeof(float2)) != cudaSuccess ||
+      cudaMemcpy(h->d_rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
+          cudaSuccess) {
+    cudaFree(h->d_status);
+    cudaFree(h->d_rope);
+    delete h;
+    return DFLASH_ERR_CUDA;
+  }
+  *out = h;
+  return DFLASH_OK;
+}
+
+int dflash_destroy(dflash_handle* h) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  for (auto& t : h->pending) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  for (auto e : h->free_events) cudaEventDestroy(e);
+  cudaFree(h->d_status);
+  cudaFree(h->d_rope);
+  delete h;
+  return DFLASH_OK;
+}
+
+size_t dflash_workspace_bytes(const dflash_handle* h, int64_t max_rows) {
+  if (!h || max_rows < 0) return 0;
+  const int64_t R = std::max<int64_t>(max_rows, 1);
+  // a forward pass over R rows, or fuse / inject in full kChunkRows passes
+  const size_t fwd = forward_bytes(h->cfg, R);
+  const size_t chunk = round256(kChunkRows * chunk_row_bytes(h->cfg)) + 1024;
+  return std::max(fwd, chunk);
+}
+
+int dflash_fuse_context(dflash_handle* h, const void* const* hidden, int64_t T, void* h_t_out,
+                        void* ws, size_t ws_bytes, dflash_stream_t st) {
+  if (!h || !hidden || T < 0) return DFLASH_ERR_INVALID_ARG;
+  if (!h->w.wc || !h->w.g_c) return DFLASH_ERR_INVALID_ARG;
+  if (T == 0) return DFLASH_OK;
+  if (!h_t_out || !ws) return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = h->cfg;
+  for (int i = 0; i < c.n_pick; ++i) {
+    if (!hidden[i]) return DFLASH_ERR_INVALID_ARG;
+    if (!aligned16(hidden[i])) return DFLASH_ERR_ALIGNMENT;
+  }
+  if (!aligned16(h_t_out) || !aligned16(ws)) return DFLASH_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)st;
+  const int D = c.hidden, dt = c.dtype;
+  const int64_t chunk = std::min<int64_t>(kChunkRows, (int64_t)(ws_bytes / (D * 4 + 1)));
+  if (chunk < 1) return DFLASH_ERR_WORKSPACE;
+  float* Y = (float*)ws;
+  for (int64_t r0 = 0; r0 < T; r0 += chunk) {
+    const int64_t n = std::min(chunk, T - r0);
+    ASrc a{};
+    for (int i = 0; i < c.n_pick; ++i) a.p[i] = byte_off(hidden[i], r0 * D, dt);
+    a.nseg = c.n_pick;
+    a.seg = D;
+    a.ld = D;
+    int rc = gemm(h, s, DFLASH_K_DENSE_GEMM, dt, a, h->w.wc, (int64_t)c.n_pick * D, Y, D, n, D,
+                  c.n_pick * D, false);
+    if (rc) return rc;
+    rc = rmsnorm_rows(h, s, DFLASH_F32, dt, Y, D, (void*)byte_off(h_t_out, r0 * D, dt), D, h->w.g_c,
+                      n, D, c.rms_eps, 0);
+    if (rc) return rc;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_inject_kv(dflash_handle* h, const void* h_t, int64_t n_rows, const int32_t* seq_row0,
+                     const int32_t* seq_rows, int32_t batch, const dflash_kv* kv, void* ws,
+                     size_t ws_bytes, dflash_stream_t st) {
+  if (!h || !h_t || !seq_row0 || !seq_rows || !ws || n_rows < 0 || batch < 1)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!kv_ok(h, kv, batch)) return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(h_t) || !aligned16(ws)) return DFLASH_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)st;
+  const dflash_config& c = h->cfg;
+  const int D = c.hidden, G = c.n_kv_heads, d = c.head_dim, Gd = G * d, dt = c.dtype;
+  const int64_t chunk = std::min<int64_t>(kChunkRows, (int64_t)(ws_bytes / (2 * Gd * 4 + 512)));
+  if (chunk < 1) return DFLASH_ERR_WORKSPACE;
+  Carve cv{(char*)ws, ws_bytes};
+  float* kf = cv.take<float>(chunk * Gd);
+  float* vf = cv.take<float>(chunk * Gd);
+  if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+  for (int64_t r0 = 0; r0 < n_rows; r0 += chunk) {
+    const int64_t n = std::min(chunk, n_rows - r0);
+    RowMap rm{1, 0, seq_row0, seq_rows, batch, (int)r0};
+    const ASrc a = one_src(byte_off(h_t, r0 * D, dt), D, D);
+    for (int l = 0; l < c.n_layers; ++l) {
+      const dflash_layer_weights& L = h->w.layers[l];
+      int rc;
+      if ((rc = gemm(h, s, DFLASH_K_DENSE_GEMM, dt, a, L.wk, D, kf, Gd, n, Gd, D, false))) return rc;
+      if ((rc = gemm(h, s, DFLASH_K_DENSE_GEMM, dt, a, L.wv, D, vf, Gd, n, Gd, D, false))) return rc;
+      if ((rc = head_norm_rope(h, s, dt, kf, n, G, d, c.qk_norm ? L.k_norm : nullptr, true, rm,
+                               kv->len, nullptr, kv->k[l], kv->cap, kv->batch_cap)))
+        return rc;
+      if ((rc = head_norm_rope(h, s, dt, vf, n, G, d, nullptr, false, rm, kv->len, nullptr,
+                               kv->v[l], kv->cap, kv->batch_cap)))
+        return rc;
+    }
+  }
+  return advance_len(h, s, kv->len, seq_rows, 0, batch, kv->cap);
+}
+
+int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, int32_t B,
+                       const dflash_kv* kv, int32_t* draft_ids, float* top2_gap, float* hidden_out,
+                       void* ws, size_t ws_bytes, dflash_stream_t st) {
+  if (!h || !anchor || !draft_ids || !ws || batch < 1 || B < 1) return DFLASH_ERR_INVALID_ARG;
+  if (!kv_ok(h, kv, batch)) return DFLASH_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return DFLASH_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)st;
+  const dflash_config& c = h->cfg;
+  const int D = c.hidden, H = c.n_heads, G = c.n_kv_heads, d = c.head_dim, dt = c.dtype;
+  const int Hd = H * d, Gd = G * d;
+  const int64_t R = (int64_t)batch * B;
+  Fwd f;
+  if (!carve_forward(c, R, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
+  int rc;
+  if ((rc = embed_block(h, s, dt, h->w.embed, anchor, c.mask_token_id, batch, B, c.vocab, D,
+                        c.embed_scale, f.x)))
+    return rc;
+  const RowMap rm{0, B, nullptr, nullptr, batch, 0};
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& L = h->w.layers[l];
+    if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, L.g_in, R, D, c.rms_eps, 0)))
+      return rc;
+    const ASrc a = one_src(f.h, D, D);
+    if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, a, L.wq, D, f.qf, Hd, R, Hd, D, false))) return rc;
+    if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, a, L.wk, D, f.kf, Gd, R, Gd, D, false))) return rc;
+    if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, a, L.wv, D, f.vf, Gd, R, Gd, D, false))) return rc;
+    if ((rc = head_norm_rope(h, s, dt, f.qf, R, H, d, c.qk_norm ? L.q_norm : nullptr, true, rm,
+                             kv->len, f.q, nullptr, 0, 0)))
+      return rc;
+    if ((rc = head_norm_rope(h, s, dt, f.kf, R, G, d, c.qk_norm ? L.k_norm : nullptr, true, rm,
+                             kv->len, f.kb, nullptr, 0, 0)))
+      return rc;
+    if ((rc = head_norm_rope(h, s, dt, f.vf, R, G, d, nullptr, false, rm, kv->len, f.vb, nullptr, 0,
+                             0)))
+      return rc;
+    if ((rc = attention(h, s, dt, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch, B,
+                        H, G, d, false, f.o)))
+      return rc;
+    if ((rc = mlp_tail(h, s, L, f, R))) return rc;
+  }
+  if (hidden_out &&
+      cudaMemcpyAsync(hidden_out, f.x, R * D * sizeof(float), cudaMemcpyDeviceToDevice, s))
+    return DFLASH_ERR_CUDA;
+  if (B == 1) {
+    if (cudaMemcpyAsync(draft_ids, anchor, batch * sizeof(int32_t), cudaMemcpyDeviceToDevice, s))
+      return DFLASH_ERR_CUDA;
+    return DFLASH_OK;
+  }
+  return lm_head(h, s, f, f.x, (int64_t)batch * (B - 1), h->w.g_f, B, draft_ids, top2_gap, B,
+                 anchor);
+}
+
+int dflash_verify_greedy(const int32_t* draft, const int32_t* post, int32_t batch, int32_t B,
+                         const int32_t* start, int32_t* accept, int32_t* tau, int32_t* bonus,
+                         int32_t* out_tokens, int32_t* new_len, dflash_stream_t st) {
+  if (!draft || !post || !start || !accept || !bonus || !out_tokens || batch < 0 || B < 1)
+    return DFLASH_ERR_INVALID_ARG;
+  if (batch == 0) return DFLASH_OK;
+  return verify_greedy((cudaStream_t)st, draft, post, batch, B, start, accept, tau, bonus,
+                       out_tokens, new_len);
+}
+
+int dflash_lm_head_argmax(dflash_handle* h, const float* x, int32_t rows, const float* norm_gain,
+                          int32_t* ids, float* top2_gap, void* ws, size_t ws_bytes,
+                          dflash_stream_t st) {
+  if (!h || !x || !norm_gain || !ids || !ws || rows < 0) return DFLASH_ERR_INVALID_ARG;
+  if (rows == 0) return DFLASH_OK;
+  Fwd f;
+  if (!carve_forward(h->cfg, rows, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
+  return lm_head(h, (cudaStream_t)st, f, x, rows, norm_gain, 0, ids, top2_gap, 0, nullptr);
+}
+
+int dflash_target_forward(dflash_handle* h, const int32_t* tokens, int32_t batch, int32_t T,
+                          const dflash_kv* kv, const int32_t* tap_ids, int32_t n_taps,
+                          void* taps_out, int32_t* argmax_out, void* ws, size_t ws_bytes,
+                          dflash_stream_t st) {
+  if (!h || !tokens || !argmax_out || !ws || batch < 1 || T < 1 || n_taps < 0)
+    return DFLASH_ERR_INVALID_ARG;
+  if (n_taps > 0 && (!tap_ids || !taps_out)) return DFLASH_ERR_INVALID_ARG;
+  if (!kv_ok(h, kv, batch)) return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = h->cfg;
+  for (int j = 0; j < n_taps; ++j)
+    if (tap_ids[j] < 0 || tap_ids[j] >= c.n_layers) return DFLASH_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)st;
+  const int D = c.hidden, H = c.n_heads, G = c.n_kv_heads, d = c.head_dim, dt = c.dtype;
+  const int Hd = H * d, Gd = G * d;
+  const int64_t R = (int64_t)batch * T;
+  Fwd f;
+  if (!carve_forward(c, R, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
+  int rc;
+  if ((rc = embed_tokens(h, s, dt, h->w.embed, tokens, (int)R, c.vocab, D, c.embed_scale, f.x)))
+    return rc;
+  const RowMap rm{0, T, nullptr, nullptr, batch, 0};
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& L = h->w.layers[l];
+    if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, L.g_in, R, D, c.rms_eps, 0)))
+      return rc;
+    const ASrc a = one_src(f.h, D, D);
+    if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, a, L.wq, D, f.qf, Hd, R, Hd, D, false))) return rc;
+    if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, a, L.wk, D, f.kf, Gd, R, Gd, D, false))) return rc;
+    if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, a, L.wv, D, f.vf, Gd, R, Gd, D, false))) return rc;
+    if ((rc = head_norm_rope(h, s, dt, f.qf, R, H, d, c.qk_norm ? L.q_norm : nullptr, true, rm,
+                             kv->len, f.q, nullptr, 0, 0)))
+      return rc;
+    if ((rc = head_norm_rope(h, s, dt, f.kf, R, G, d, c.qk_norm ? L.k_norm : nullptr, true, rm,
+                             kv->len, nullptr, kv->k[l], kv->cap, kv->batch_cap)))
+      return rc;
+    if ((rc = head_norm_rope(h, s, dt, f.vf, R, G, d, nullptr, false, rm, kv->len, nullptr,
+                             kv->v[l], kv->cap, kv->batch_cap)))
+      return rc;
+    if ((rc = attention(h, s, dt, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, nullptr, nullptr,
+                        batch, T, H, G, d, true, f.o)))
+      return rc;
+    if ((rc = mlp_tail(h, s, L, f, R))) return rc;
+    for (int j = 0; j < n_taps; ++j)
+      if (tap_ids[j] == l &&
+          (rc = cast_rows(h, s, dt, f.x, (void*)byte_off(taps_out, (int64_t)j * R * D, dt), R * D)))
+        return rc;
+  }
+  if ((rc = lm_head(h, s, f, f.x, R, h->w.g_f, 0, argmax_out, nullptr, 0, nullptr))) return rc;
+  return advance_len(h, s, kv->len, nullptr, T, batch, kv->cap);
+}
+
+int dflash_get_status(dflash_handle* h, dflash_stream_t st) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize((cudaStream_t)st) != cudaSuccess) return DFLASH_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  cudaMemset(h->d_status, 0, sizeof(int));
+  if (v & ST_CAPACITY) return DFLASH_ERR_CAPACITY;
+  if (v & ST_BOUNDS) return DFLASH_ERR_DEVICE_BOUNDS;
+  if (v & ST_TIMEOUT) return DFLASH_ERR_DEVICE_TIMEOUT;
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
+int dflash_timing_enable(dflash_handle* h, int on) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  h->timing = on != 0;
+  return DFLASH_OK;
+}
+
+int dflash_timing_read(dflash_handle* h, int32_t kclass, double* total_ms, int64_t* launches) {
+  if (!h || kclass < 0 || kclass >= DFLASH_K_NCLASS || !total_ms || !launches)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!h->pending.empty()) {
+    for (auto& t : h->pending) {
+      float ms = 0.f;
+      cudaEventSynchronize(t.b);
+      cudaEventElapsedTime(&ms, t.a, t.b);
+      h->ms[t.kclass] += ms;
+      h->launches[t.kclass] += 1;
+      h->free_events.push_back(t.a);
+      h->free_events.push_back(t.b);
+    }
+    h->pending.clear();
+  }
+  *total_ms = h->ms[kclass];
+  *launches = h->launches[kclass];
+  h->ms[kclass] = 0;
+  h->launches[kclass] = 0;
+  return DFLASH_OK;
+}
+
+}  // extern "C"

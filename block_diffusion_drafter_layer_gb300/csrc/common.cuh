@@ -1,0 +1,179 @@
+// Internal declarations shared by the libdflash translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "../../include/dflash.h"
+
+namespace dflash {
+
+using bf16 = __nv_bfloat16;
+
+// ---- device status word bits (OR-ed by kernels, read by dflash_get_status)
+enum : int {
+  ST_CAPACITY = 1,   // a cache append would pass kv->cap
+  ST_BOUNDS = 2,     // a token id or position out of range
+  ST_TIMEOUT = 4,    // a bounded device wait gave up
+};
+
+// ---- conversions ----------------------------------------------------------
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// ---- deterministic block reductions (fixed shuffle tree, then warp 0) ------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+// All threads of the block must call; returns the total to every thread.
+__device__ __forceinline__ float block_sum(float v, float* red /* >= 33 floats */) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    float t = 0.f;
+    for (int i = 0; i < nw; ++i) t += red[i];   // fixed order
+    if (lane == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+__device__ __forceinline__ float block_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    float t = -INFINITY;
+    for (int i = 0; i < nw; ++i) t = fmaxf(t, red[i]);
+    if (lane == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+// ---- which sequence / block position a row belongs to ---------------------
+// Uniform: row r is position r % rps of sequence r / rps.
+// Ranged:  rows row0[b] .. row0[b]+nrows[b]-1 belong to sequence b.
+// A chunk of rows starting at absolute row `offset` maps row r to r + offset.
+struct RowMap {
+  int ranged;
+  int rps;
+  const int32_t* row0;
+  const int32_t* nrows;
+  int batch;
+  int offset;
+  __device__ __forceinline__ bool map(int r, int& b, int& i) const {
+    r += offset;
+    if (!ranged) { b = r / rps; i = r - b * rps; return true; }
+    for (int s = 0; s < batch; ++s) {
+      const int r0 = row0[s], n = nrows[s];
+      if (r >= r0 && r < r0 + n) { b = s; i = r - r0; return true; }
+    }
+    return false;
+  }
+};
+
+// ---- handle ---------------------------------------------------------------
+struct Timer {
+  int kclass;
+  cudaEvent_t a, b;
+};
+
+}  // namespace dflash
+
+struct dflash_handle {
+  dflash_config cfg;
+  dflash_weights w;
+  int device = 0;
+  int* d_status = nullptr;
+  float2* d_rope = nullptr;        // [max_pos, d/2] (cos, sin)
+  bool timing = false;
+  std::vector<cudaEvent_t> free_events;
+  std::vector<dflash::Timer> pending;
+  double ms[DFLASH_K_NCLASS] = {0};
+  int64_t launches[DFLASH_K_NCLASS] = {0};
+};
+
+namespace dflash {
+
+// Launch bookkeeping: count, optional event timing, error check.
+void launch_begin(dflash_handle* h, int kclass, cudaStream_t s, Timer* t);
+int launch_end(dflash_handle* h, cudaStream_t s, Timer* t);
+void count_launch();
+
+// Workspace carving (256-byte aligned bump allocator over the caller's buffer).
+struct Carve {
+  char* base;
+  size_t cap, off = 0;
+  bool ok = true;
+  template <typename T> T* take(size_t n) {
+    off = (off + 255) & ~size_t(255);
+    T* p = reinterpret_cast<T*>(base + off);
+    off += n * sizeof(T);
+    if (off > cap) ok = false;
+    return p;
+  }
+};
+
+// ---- kernel launchers (one translation unit each) --------------------------
+// A operand source: up to DFLASH_MAX_PICK column segments of width seg
+// (column k of row m is seg_ptr[k / seg][m * ld + k % seg]).
+struct ASrc {
+  const void* p[DFLASH_MAX_PICK];
+  int nseg;
+  int seg;
+  int64_t ld;
+};
+
+// C[m, n] (+)= sum_k A[m, k] * W[n, k]; fp32 accumulate in k order.
+int gemm(dflash_handle* h, cudaStream_t s, int kclass, int dtype, const ASrc& A,
+         const void* W, int64_t ldw, float* C, int64_t ldc, int64_t M, int N, int K,
+         bool accumulate);
+
+int embed_block(dflash_handle* h, cudaStream_t s, int dtype, const void* E, const int32_t* anchor,
+                int mask_id, int batch, int B, int V, int D, float scale, float* x);
+int embed_tokens(dflash_handle* h, cudaStream_t s, int dtype, const void* E, const int32_t* tok,
+                 int rows, int V, int D, float scale, float* x);
+// out[r] = rmsnorm(in[r]) * g, in fp32 or dtype; rows selected by `skip_every`
+// (if > 0, input row r' = r + r / (skip_every - 1) + 1 skips every block's first row).
+int rmsnorm_rows(dflash_handle* h, cudaStream_t s, int in_dtype, int out_dtype, const void* in,
+                 int64_t ld_in, void* out, int64_t ld_out, const float* g, int64_t rows, int D,
+                 float eps, int skip_first_of);
+// Per-head (optional RMSNorm) + RoPE on fp32 input [rows, heads*d] -> dtype dst.
+int head_norm_rope(dflash_handle* h, cudaStream_t s, int dtype, const float* in, int64_t rows,
+                   int heads, int d, const float* gain, bool rope, const RowMap& rm,
+                   const int32_t* len, void* dense, void* cache, int cap, int cache_batch);
+int swiglu(dflash_handle* h, cudaStream_t s, int dtype, const float* g, const float* u, void* a,
+           int64_t n);
+int cast_rows(dflash_handle* h, cudaStream_t s, int dtype, const float* in, void* out, int64_t n);
+int advance_len(dflash_handle* h, cudaStream_t s, int32_t* len, const int32_t* nrows, int uniform,
+                int batch, int cap);
+// Attention of block rows over [cache(0..len) ; block] (draft) or cache(0..pos) (causal target).
+int attention(dflash_handle* h, cudaStream_t s, int dtype, const void* q, const void* kc,
+              const void* vc, int cap, const int32_t* len, const void* kb, const void* vb,
+              int batch, int rows_per_seq, int H, int G, int d, bool causal_in_cache, void* o);
+int argmax_rows(dflash_handle* h, cudaStream_t s, const float* logits, int64_t rows, int V,
+                int32_t* ids, float* gap, int rows_per_seq_out, const int32_t* anchor);
+int verify_greedy(cudaStream_t s, const int32_t* draft, const int32_t* post, int batch, int B,
+                  const int32_t* start, int32_t* accept, int32_t* tau, int32_t* bonus,
+                  int32_t* out_tokens, int32_t* new_len);
+
+}  // namespace dflash

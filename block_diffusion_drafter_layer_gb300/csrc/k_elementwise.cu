@@ -1,0 +1,278 @@
+// Row-wise kernels of the draft path: block embedding, RMSNorm, per-head
+// q/k norm + RoPE (+ store into a dense buffer or a K/V cache), SwiGLU, and
+// cache-length bookkeeping.
+#include "common.cuh"
+
+namespace dflash {
+
+// Block input rows [anchor, mask x (B-1)] through the shared embedding, times
+// input_embedding_scale, into the fp32 residual stream (txtmix §6, §9).
+template <typename T>
+__global__ void embed_block_kernel(const T* __restrict__ E, const int32_t* __restrict__ anchor,
+                                   int mask_id, int B, int V, int D, float scale,
+                                   float* __restrict__ x, int* status) {
+  const int r = blockIdx.x;
+  const int b = r / B, i = r - b * B;
+  const int id = (i == 0) ? anchor[b] : mask_id;
+  float* dst = x + (int64_t)r * D;
+  if (id < 0 || id >= V) {
+    if (threadIdx.x == 0) atomicOr(status, ST_BOUNDS);
+    for (int k = threadIdx.x; k < D; k += blockDim.x) dst[k] = 0.f;
+    return;
+  }
+  const T* src = E + (int64_t)id * D;
+  for (int k = threadIdx.x; k < D; k += blockDim.x) dst[k] = to_f(src[k]) * scale;
+}
+
+template <typename T>
+__global__ void embed_tokens_kernel(const T* __restrict__ E, const int32_t* __restrict__ tok, int V,
+                                    int D, float scale, float* __restrict__ x, int* status) {
+  const int r = blockIdx.x;
+  const int id = tok[r];
+  float* dst = x + (int64_t)r * D;
+  if (id < 0 || id >= V) {
+    if (threadIdx.x == 0) atomicOr(status, ST_BOUNDS);
+    for (int k = threadIdx.x; k < D; k += blockDim.x) dst[k] = 0.f;
+    return;
+  }
+  const T* src = E + (int64_t)id * D;
+  for (int k = threadIdx.x; k < D; k += blockDim.x) dst[k] = to_f(src[k]) * scale;
+}
+
+// out[r] = in[r'] / sqrt(mean(in[r']^2) + eps) * g, fp32 arithmetic.
+// skip_first_of > 1 maps output row r to input row r' that skips the first
+// row of every group of skip_first_of rows (the anchor rows of a block).
+template <typename TI, typename TO>
+__global__ void rmsnorm_kernel(const TI* __restrict__ in, int64_t ld_in, TO* __restrict__ out,
+                               int64_t ld_out, const float* __restrict__ g, int D, float eps,
+                               int skip_first_of) {
+  __shared__ float red[33];
+  const int64_t r = blockIdx.x;
+  int64_t ri = r;
+  if (skip_first_of > 1) {
+    const int64_t per = skip_first_of - 1;
+    ri = (r / per) * skip_first_of + (r % per) + 1;
+  }
+  const TI* src = in + ri * ld_in;
+  float ss = 0.f;
+  for (int k = threadIdx.x; k < D; k += blockDim.x) {
+    const float v = to_f(src[k]);
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float rinv = 1.0f / sqrtf(ss / (float)D + eps);
+  TO* dst = out + r * ld_out;
+  for (int k = threadIdx.x; k < D; k += blockDim.x) dst[k] = from_f<TO>(to_f(src[k]) * rinv * g[k]);
+}
+
+// One warp per (row, head): optional per-head RMSNorm, optional RoPE with
+// rotate-half pairs (j, j + d/2), then store (dense or cache at len[b] + i).
+template <typename T>
+__global__ void head_norm_rope_kernel(const float* __restrict__ in, int64_t rows, int heads, int d,
+                                      const float* __restrict__ gain, int use_rope, RowMap rm,
+                                      const int32_t* __restrict__ len,
+                                      const float2* __restrict__ rope_tab, int max_pos, float eps,
+                                      T* dense, T* cache, int cap, int cache_batch, int* status) {
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= rows * heads) return;
+  const int64_t r = warp / heads;
+  const int hd = (int)(warp - r * heads);
+  int b, i;
+  if (!rm.map((int)r, b, i)) return;
+  const int pos = len[b] + i;
+  const float* src = in + r * (int64_t)(heads * d) + (int64_t)hd * d;
+  const int half = d >> 1;
+  const int P = half >> 5;           // pairs per lane: 1 (d = 64) or 2 (d = 128)
+  float x1[2], x2[2];
+  float ss = 0.f;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    if (p < P) {
+      const int j = lane + 32 * p;
+      x1[p] = src[j];
+      x2[p] = src[j + half];
+      ss += x1[p] * x1[p] + x2[p] * x2[p];
+    }
+  }
+  if (gain != nullptr) {
+    ss = warp_sum(ss);
+    const float rinv = 1.0f / sqrtf(ss / (float)d + eps);
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      if (p < P) {
+        const int j = lane + 32 * p;
+        x1[p] = x1[p] * rinv * gain[j];
+        x2[p] = x2[p] * rinv * gain[j + half];
+      }
+    }
+  }
+  if (use_rope) {
+    if (pos < 0 || pos >= max_pos) {
+      if (lane == 0) atomicOr(status, ST_BOUNDS);
+      return;
+    }
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      if (p < P) {
+        const int j = lane + 32 * p;
+        const float2 cs = rope_tab[(int64_t)pos * half + j];
+        const float y1 = x1[p] * cs.x - x2[p] * cs.y;
+        const float y2 = x2[p] * cs.x + x1[p] * cs.y;
+        x1[p] = y1;
+        x2[p] = y2;
+      }
+    }
+  }
+  T* dst;
+  if (cache != nullptr) {
+    if (b >= cache_batch || pos < 0 || pos >= cap) {
+      if (lane == 0) atomicOr(status, ST_CAPACITY);
+      return;
+    }
+    dst = cache + (((int64_t)b * heads + hd) * cap + pos) * d;
+  } else {
+    dst = dense + r * (int64_t)(heads * d) + (int64_t)hd * d;
+  }
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    if (p < P) {
+      const int j = lane + 32 * p;
+      dst[j] = from_f<T>(x1[p]);
+      dst[j + half] = from_f<T>(x2[p]);
+    }
+  }
+}
+
+// a = SiLU(g) * u, SiLU(x) = x / (1 + e^-x).
+template <typename T>
+__global__ void swiglu_kernel(const float* __restrict__ g, const float* __restrict__ u,
+                              T* __restrict__ a, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float x = g[i];
+    a[i] = from_f<T>(x / (1.0f + expf(-x)) * u[i]);
+  }
+}
+
+template <typename T>
+__global__ void cast_kernel(const float* __restrict__ in, T* __restrict__ out, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = from_f<T>(in[i]);
+}
+
+__global__ void advance_len_kernel(int32_t* len, const int32_t* nrows, int uniform, int batch,
+                                   int cap, int* status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const int n = nrows ? nrows[b] : uniform;
+  if (n < 0 || len[b] + n > cap) {
+    atomicOr(status, ST_CAPACITY);
+    return;
+  }
+  len[b] += n;
+}
+
+// ---------------------------------------------------------------------------
+int embed_block(dflash_handle* h, cudaStream_t s, int dtype, const void* E, const int32_t* anchor,
+                int mask_id, int batch, int B, int V, int D, float scale, float* x) {
+  Timer t;
+  launch_begin(h, DFLASH_K_ELEMENTWISE, s, &t);
+  if (dtype == DFLASH_BF16)
+    embed_block_kernel<bf16><<<batch * B, 256, 0, s>>>((const bf16*)E, anchor, mask_id, B, V, D,
+                                                       scale, x, h->d_status);
+  else
+    embed_block_kernel<float><<<batch * B, 256, 0, s>>>((const float*)E, anchor, mask_id, B, V, D,
+                                                        scale, x, h->d_status);
+  return launch_end(h, s, &t);
+}
+
+int embed_tokens(dflash_handle* h, cudaStream_t s, int dtype, const void* E, const int32_t* tok,
+                 int rows, int V, int D, float scale, float* x) {
+  Timer t;
+  launch_begin(h, DFLASH_K_ELEMENTWISE, s, &t);
+  if (dtype == DFLASH_BF16)
+    embed_tokens_kernel<bf16><<<rows, 256, 0, s>>>((const bf16*)E, tok, V, D, scale, x, h->d_status);
+  else
+    embed_tokens_kernel<float><<<rows, 256, 0, s>>>((const float*)E, tok, V, D, scale, x,
+                                                    h->d_status);
+  return launch_end(h, s, &t);
+}
+
+int rmsnorm_rows(dflash_handle* h, cudaStream_t s, int in_dtype, int out_dtype, const void* in,
+                 int64_t ld_in, void* out, int64_t ld_out, const float* g, int64_t rows, int D,
+                 float eps, int skip_first_of) {
+  if (rows <= 0) return DFLASH_OK;
+  Timer t;
+  launch_begin(h, DFLASH_K_ELEMENTWISE, s, &t);
+  const dim3 grid((unsigned)rows);
+  if (in_dtype == DFLASH_F32 && out_dtype == DFLASH_F32)
+    rmsnorm_kernel<float, float><<<grid, 256, 0, s>>>((const float*)in, ld_in, (float*)out, ld_out,
+                                                      g, D, eps, skip_first_of);
+  else if (in_dtype == DFLASH_F32 && out_dtype == DFLASH_BF16)
+    rmsnorm_kernel<float, bf16><<<grid, 256, 0, s>>>((const float*)in, ld_in, (bf16*)out, ld_out,
+                                                     g, D, eps, skip_first_of);
+  else if (in_dtype == DFLASH_BF16 && out_dtype == DFLASH_BF16)
+    rmsnorm_kernel<bf16, bf16><<<grid, 256, 0, s>>>((const bf16*)in, ld_in, (bf16*)out, ld_out, g,
+                                                    D, eps, skip_first_of);
+  else
+    rmsnorm_kernel<bf16, float><<<grid, 256, 0, s>>>((const bf16*)in, ld_in, (float*)out, ld_out,
+                                                     g, D, eps, skip_first_of);
+  return launch_end(h, s, &t);
+}
+
+int head_norm_rope(dflash_handle* h, cudaStream_t s, int dtype, const float* in, int64_t rows,
+                   int heads, int d, const float* gain, bool rope, const RowMap& rm,
+                   const int32_t* len, void* dense, void* cache, int cap, int cache_batch) {
+  if (rows <= 0) return DFLASH_OK;
+  const int64_t warps = rows * heads;
+  const unsigned blocks = (unsigned)((warps + 3) / 4);
+  Timer t;
+  launch_begin(h, DFLASH_K_ELEMENTWISE, s, &t);
+  if (dtype == DFLASH_BF16)
+    head_norm_rope_kernel<bf16><<<blocks, 128, 0, s>>>(
+        in, rows, heads, d, gain, rope ? 1 : 0, rm, len, h->d_rope, h->cfg.max_pos,
+        h->cfg.rms_eps, (bf16*)dense, (bf16*)cache, cap, cache_batch, h->d_status);
+  else
+    head_norm_rope_kernel<float><<<blocks, 128, 0, s>>>(
+        in, rows, heads, d, gain, rope ? 1 : 0, rm, len, h->d_rope, h->cfg.max_pos,
+        h->cfg.rms_eps, (float*)dense, (float*)cache, cap, cache_batch, h->d_status);
+  return launch_end(h, s, &t);
+}
+
+int swiglu(dflash_handle* h, cudaStream_t s, int dtype, const float* g, const float* u, void* a,
+           int64_t n) {
+  if (n <= 0) return DFLASH_OK;
+  const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 16);
+  Timer t;
+  launch_begin(h, DFLASH_K_ELEMENTWISE, s, &t);
+  if (dtype == DFLASH_BF16)
+    swiglu_kernel<bf16><<<blocks, 256, 0, s>>>(g, u, (bf16*)a, n);
+  else
+    swiglu_kernel<float><<<blocks, 256, 0, s>>>(g, u, (float*)a, n);
+  return launch_end(h, s, &t);
+}
+
+int cast_rows(dflash_handle* h, cudaStream_t s, int dtype, const float* in, void* out, int64_t n) {
+  if (n <= 0) return DFLASH_OK;
+  const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 16);
+  Timer t;
+  launch_begin(h, DFLASH_K_ELEMENTWISE, s, &t);
+  if (dtype == DFLASH_BF16)
+    cast_kernel<bf16><<<blocks, 256, 0, s>>>(in, (bf16*)out, n);
+  else
+    cast_kernel<float><<<blocks, 256, 0, s>>>(in, (float*)out, n);
+  return launch_end(h, s, &t);
+}
+
+int advance_len(dflash_handle* h, cudaStream_t s, int32_t* len, const int32_t* nrows, int uniform,
+                int batch, int cap) {
+  Timer t;
+  launch_begin(h, DFLASH_K_ELEMENTWISE, s, &t);
+  advance_len_kernel<<<(batch + 127) / 128, 128, 0, s>>>(len, nrows, uniform, batch, cap,
+                                                         h->d_status);
+  return launch_end(h, s, &t);
+}
+
+}  // namespace dflash

@@ -1,0 +1,101 @@
+"""Greedy DFlash speculative loop on one GPU, driven through the C ABI.
+
+Host-side orchestration only (txtmix source reading §9, steps 2-6): prefill
+the target, then per round fuse and inject the pending context rows, draft
+one block, verify it with one target forward, keep the accepted prefix plus
+the bonus token, trim the target cache, and carry the accepted positions'
+taps into the next round.  Every step runs in libdflash kernels; the host
+reads back the accepted length once per round (as the reference loop does).
+"""
+from __future__ import annotations
+
+from typing import List, Sequence, Tuple
+
+import torch
+
+from . import (KVCache, Model, dflash_build_target_layer_ids, dflash_draft_block,
+               dflash_fuse_context, dflash_inject_kv, dflash_target_forward, dflash_verify_greedy)
+
+
+class SpecDecoder:
+    def __init__(self, target: Model, draft: Model, *, t_layers: int, t_kv_heads: int,
+                 d_layers: int, d_kv_heads: int, head_dim: int, D: int, n_target_layers: int,
+                 n_pick: int, B: int, max_prompt: int, cap: int, device="cuda"):
+        self.target, self.draft, self.B, self.D = target, draft, B, D
+        self.device = device
+        self.dtype = target.dtype
+        td = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        self.tap_ids = dflash_build_target_layer_ids(n_target_layers, n_pick)
+        self.n_pick = n_pick
+        rows = max(max_prompt, B)
+        self.tkv = KVCache(t_layers, 1, t_kv_heads, cap, head_dim, self.dtype, device)
+        self.dkv = KVCache(d_layers, 1, d_kv_heads, cap, head_dim, self.dtype, device)
+        self.ws_t = target.workspace(rows, device)
+        self.ws_d = draft.workspace(rows, device)
+        self.h_t = torch.empty(rows, D, dtype=td, device=device)
+        self.draft_ids = torch.empty(1, B, dtype=torch.int32, device=device)
+        self.post = torch.empty(B, dtype=torch.int32, device=device)
+        self.start = torch.zeros(1, dtype=torch.int32, device=device)
+        self.accept = torch.zeros(1, dtype=torch.int32, device=device)
+        self.tau = torch.zeros(1, dtype=torch.int32, device=device)
+        self.bonus = torch.zeros(1, dtype=torch.int32, device=device)
+        self.out_tokens = torch.zeros(1, B, dtype=torch.int32, device=device)
+        self.row0 = torch.zeros(1, dtype=torch.int32, device=device)
+        self.taps_block = torch.empty(n_pick, B, D, dtype=td, device=device)
+
+    def reset(self):
+        self.tkv.len.zero_()
+        self.dkv.len.zero_()
+
+    def generate(self, prompt: Sequence[int], n_new: int) -> Tuple[List[int], List[int]]:
+        self.reset()
+        dev, B = self.device, self.B
+        P = len(prompt)
+        td = self.taps_block.dtype
+        taps_pre = torch.empty(self.n_pick, P, self.D, dtype=td, device=dev)
+        argmax_pre = torch.empty(P, dtype=torch.int32, device=dev)
+        tokens = torch.tensor(prompt, dtype=torch.int32, device=dev)[None]
+        dflash_target_forward(self.target.handle, tokens, 1, P, self.tkv.struct, self.tap_ids,
+                              taps_pre, argmax_pre, self.ws_t)
+        out = [int(argmax_pre[-1].item())]
+        pending, T = taps_pre, P
+        taus = []
+        while len(out) < n_new:
+            # inject the pending context rows at positions start - T .. start - 1
+            dflash_fuse_context(self.draft.handle, [pending[j] for j in range(self.n_pick)], T,
+                                self.h_t, self.ws_d)
+            nrows = torch.tensor([T], dtype=torch.int32, device=dev)
+            dflash_inject_kv(self.draft.handle, self.h_t, T, self.row0, nrows, 1,
+                             self.dkv.struct, self.ws_d)
+            anchor = torch.tensor([out[-1]], dtype=torch.int32, device=dev)
+            dflash_draft_block(self.draft.handle, anchor, 1, B, self.dkv.struct, self.draft_ids,
+                               None, None, self.ws_d)
+            # verify: one target forward over [anchor, d_1 .. d_{B-1}]
+            self.start.copy_(self.tkv.len[:1])
+            dflash_target_forward(self.target.handle, self.draft_ids, 1, B, self.tkv.struct,
+                                  self.tap_ids, self.taps_block, self.post, self.ws_t)
+            dflash_verify_greedy(self.draft_ids, self.post, 1, B, self.start, self.accept,
+                                 self.tau, self.bonus, self.out_tokens, self.tkv.len)
+            a = int(self.accept.item())
+            out.extend(int(t) for t in self.out_tokens[0, :a + 1].tolist())
+            pending, T = self.taps_block, a + 1
+            taus.append(a + 1)
+        return out[:n_new], taus
+
+    def ar_decode(self, prompt: Sequence[int], n_new: int) -> List[int]:
+        """The target's own greedy decode, one token per forward (M = 1)."""
+        self.reset()
+        dev = self.device
+        P = len(prompt)
+        argmax = torch.empty(P, dtype=torch.int32, device=dev)
+        tokens = torch.tensor(prompt, dtype=torch.int32, device=dev)[None]
+        dflash_target_forward(self.target.handle, tokens, 1, P, self.tkv.struct, [], None, argmax,
+                              self.ws_t)
+        out = [int(argmax[-1].item())]
+        one = torch.empty(1, dtype=torch.int32, device=dev)
+        while len(out) < n_new:
+            tok = torch.tensor([[out[-1]]], dtype=torch.int32, device=dev)
+            dflash_target_forward(self.target.handle, tok, 1, 1, self.tkv.struct, [], None, one,
+                                  self.ws_t)
+            out.append(int(one.item()))
+        return out

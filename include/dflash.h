@@ -1,0 +1,242 @@
+/*
+ * dflash.h — C ABI of libdflash: the DFlash block-diffusion draft path on
+ * one GB300 (sm_103a).
+ *
+ * The method (DFlash, "Block Diffusion for Flash Speculative Decoding"):
+ *   1. fuse:    H_t = RMSNorm(W_c [H^(l1); ...; H^(l5)])  — the hidden states of
+ *               five uniformly spaced target layers, concatenated on the hidden
+ *               axis and projected by W_c (D x 5D).  (A3-dflash tutorial
+ *               §2.1.1; txtmix source reading §5.)
+ *   2. inject:  every draft layer turns H_t into K/V entries through its own
+ *               k_proj (+ k_norm, RoPE) and v_proj, appended to that layer's
+ *               persistent draft KV cache; H_t never enters Q, o_proj or the
+ *               FFN.  (A3-dflash tutorial §2.1.2; txtmix §5.)
+ *   3. draft:   one forward pass of the block [anchor, mask x (B-1)] through
+ *               every draft layer, bidirectional attention over
+ *               [context KV ; block KV] with grouped K/V heads, SwiGLU FFN,
+ *               then the target's shared LM head with argmax on rows 1..B-1.
+ *               (txtmix §6 and §9.)
+ *   4. verify:  greedy longest matching prefix plus one bonus token; the
+ *               target cache is trimmed to start + accepted + 1.  (txtmix §8.)
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" are CUDA device pointers; "host" are host
+ *     memory.  All tensors are dense row-major with the stated shapes.
+ *   - Linear weights are stored out x in (y = x W^T).  RMSNorm gains are fp32.
+ *   - Weights, K/V caches, fused features and activations use the handle's
+ *     dtype (DFLASH_F32 or DFLASH_BF16); accumulation is always fp32.
+ *   - The library borrows every caller pointer (weights, caches, outputs,
+ *     workspace) and never frees them.  A handle owns only a device status
+ *     word and a RoPE cos/sin table, allocated in dflash_create.
+ *   - Calls are asynchronous on the given stream (NULL = legacy default
+ *     stream) and do not synchronise the host, except dflash_get_status.
+ *   - A handle must not be used from two streams at once.
+ *   - Return value: DFLASH_OK or an error code.  Argument errors are
+ *     detected on the host before anything is launched.  Errors only the
+ *     device can see (a sequence outgrowing its cache, a token id out of
+ *     range, a position beyond the RoPE table) skip the offending writes and
+ *     set the handle's device status word, read by dflash_get_status.
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* dflash_stream_t;
+
+enum dflash_status {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, negative size */
+  DFLASH_ERR_SHAPE = 2,         /* shape outside what the handle supports */
+  DFLASH_ERR_ALIGNMENT = 3,     /* a pointer is not 16-byte aligned */
+  DFLASH_ERR_CAPACITY = 4,      /* a K/V cache would overflow (device-detected) */
+  DFLASH_ERR_UNSUPPORTED = 5,   /* dtype / head_dim / device architecture */
+  DFLASH_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed */
+  DFLASH_ERR_DEVICE_TIMEOUT = 7,/* a bounded device-side wait gave up */
+  DFLASH_ERR_DEVICE_BOUNDS = 8, /* token id or position out of range (device-detected) */
+  DFLASH_ERR_WORKSPACE = 9      /* workspace smaller than dflash_workspace_bytes */
+};
+
+enum dflash_dtype { DFLASH_F32 = 0, DFLASH_BF16 = 1 };
+
+#define DFLASH_MAX_LAYERS 16
+#define DFLASH_MAX_PICK 8
+
+/* Model shape.  One struct serves the draft (qk_norm = 1, bidirectional
+ * block) and the small causal target used by the end-to-end loop
+ * (qk_norm = 0).  Fields follow the draft checkpoint's dflash_config
+ * (txtmix §11: block size, target_layer_ids, mask_token_id,
+ * input_embedding_scale) plus the Qwen3/Llama layer shape. */
+typedef struct dflash_config {
+  int32_t hidden;            /* D */
+  int32_t n_heads;           /* H query heads */
+  int32_t n_kv_heads;        /* G key/value heads; H % G == 0 */
+  int32_t head_dim;          /* d: 64 or 128 */
+  int32_t ffn;               /* F, SwiGLU intermediate size */
+  int32_t vocab;             /* V, shared embedding / LM head rows */
+  int32_t n_layers;          /* decoder layers, <= DFLASH_MAX_LAYERS */
+  int32_t n_target_layers;   /* depth of the target the features come from */
+  int32_t n_pick;            /* fused target layers (5), <= DFLASH_MAX_PICK */
+  int32_t target_layer_ids[DFLASH_MAX_PICK]; /* informational */
+  int32_t mask_token_id;
+  int32_t max_pos;           /* RoPE table covers positions 0 .. max_pos-1 */
+  int32_t qk_norm;           /* 1: per-head RMSNorm on q and k before RoPE */
+  int32_t dtype;             /* enum dflash_dtype */
+  float rope_theta;
+  float rms_eps;
+  float embed_scale;         /* input_embedding_scale */
+} dflash_config;
+
+/* One decoder layer's weights (device, borrowed). */
+typedef struct dflash_layer_weights {
+  const void* wq;            /* [H*d, D] */
+  const void* wk;            /* [G*d, D] */
+  const void* wv;            /* [G*d, D] */
+  const void* wo;            /* [D, H*d] */
+  const void* wg;            /* [F, D]  gate */
+  const void* wu;            /* [F, D]  up */
+  const void* wd;            /* [D, F]  down */
+  const float* g_in;         /* [D] input RMSNorm gain */
+  const float* g_post;       /* [D] post-attention RMSNorm gain */
+  const float* q_norm;       /* [d] (qk_norm only) */
+  const float* k_norm;       /* [d] (qk_norm only) */
+} dflash_layer_weights;
+
+typedef struct dflash_weights {
+  const void* wc;            /* [D, n_pick*D] fusion projection (draft only) */
+  const float* g_c;          /* [D] hidden_norm gain (draft only) */
+  const float* g_f;          /* [D] final RMSNorm gain before the LM head */
+  const void* embed;         /* [V, D] shared embedding */
+  const void* lm_head;       /* [V, D] shared LM head */
+  dflash_layer_weights layers[DFLASH_MAX_LAYERS];
+} dflash_weights;
+
+/* Per-layer K/V cache (device, borrowed).  k[l], v[l]: [batch_cap, G, cap, d]
+ * in the handle's dtype; len: device int32 [batch_cap], the number of filled
+ * positions of each sequence (entry t holds position t). */
+typedef struct dflash_kv {
+  void* k[DFLASH_MAX_LAYERS];
+  void* v[DFLASH_MAX_LAYERS];
+  int32_t* len;
+  int32_t cap;
+  int32_t batch_cap;
+} dflash_kv;
+
+typedef struct dflash_handle dflash_handle;
+
+/* Create a handle for one model.  Validates the shape, copies cfg and the
+ * weight pointers, allocates the device status word and a RoPE table of
+ * max_pos x d/2 (cos, sin) pairs computed on the host in double precision.
+ * Requires a device of compute capability 10.3. */
+int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out);
+int dflash_destroy(dflash_handle* h);
+
+/* Bytes of workspace any call of this handle needs for up to max_rows rows
+ * (rows = batch*B for draft/verify-forward calls, T for fuse/inject/prefill).
+ * The caller allocates it (256-byte aligned) and passes it with its size. */
+size_t dflash_workspace_bytes(const dflash_handle* h, int64_t max_rows);
+
+/* Target layers whose hidden states are fused (host, integer only):
+ * n_pick ids spread uniformly over 0-based [1, n_target_layers-3],
+ * rounding half up; n_pick == 1 takes the middle layer n_target_layers/2.
+ * (txtmix §5, build_target_layer_ids.)  ids_out: host int32[n_pick]. */
+int dflash_build_target_layer_ids(int32_t n_target_layers, int32_t n_pick, int32_t* ids_out);
+
+/* Step 1 — context fusion.  hidden: host array of n_pick device pointers,
+ * each [T, D] (handle dtype), in ascending layer order.  h_t_out: device
+ * [T, D] (handle dtype).  H_t = RMSNorm(concat(hidden) W_c^T; g_c). */
+int dflash_fuse_context(dflash_handle* h, const void* const* hidden, int64_t T,
+                        void* h_t_out, void* ws, size_t ws_bytes, dflash_stream_t s);
+
+/* Step 2 — K/V injection.  h_t: device [n_rows, D].  Rows
+ * seq_row0[b] .. seq_row0[b]+seq_rows[b]-1 of h_t belong to sequence b
+ * (device int32 [batch] each) and are appended to sequence b of every
+ * layer's cache at positions len[b] .. len[b]+seq_rows[b]-1:
+ *   K = RoPE(k_norm(h_t W_k^T), pos), V = h_t W_v^T.
+ * kv->len is advanced by seq_rows on the device.  A sequence that would
+ * exceed kv->cap is skipped and flags DFLASH_ERR_CAPACITY. */
+int dflash_inject_kv(dflash_handle* h, const void* h_t, int64_t n_rows,
+                     const int32_t* seq_row0, const int32_t* seq_rows, int32_t batch,
+                     const dflash_kv* kv, void* ws, size_t ws_bytes, dflash_stream_t s);
+
+/* Step 3 — one block draft forward.  anchor: device int32 [batch].  The
+ * block of sequence b is [anchor[b], mask x (B-1)] at positions
+ * len[b] .. len[b]+B-1 and attends (no mask) to its own B rows and to the
+ * len[b] cached context entries of each layer.  The cache is only read:
+ * the block's own K/V live in the workspace.
+ *   draft_ids: device int32 [batch, B]; column 0 = anchor, columns 1..B-1 =
+ *              argmax (lowest index on ties) of the fp32 logits.
+ *   top2_gap:  nullable device fp32 [batch, B-1], top-1 minus top-2 logit.
+ *   hidden_out: nullable device fp32 [batch*B, D], the residual stream after
+ *              the last layer (before the final norm). */
+int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, int32_t B,
+                       const dflash_kv* kv, int32_t* draft_ids, float* top2_gap,
+                       float* hidden_out, void* ws, size_t ws_bytes, dflash_stream_t s);
+
+/* Step 4 — greedy verification (integer only, no handle).
+ * draft, post: device int32 [batch, B]; post[b, j] is the target's argmax at
+ * block position j.  accept[b] = number of leading j in 1..B-1 with
+ * draft[b, j] == post[b, j-1]; bonus[b] = post[b, accept[b]];
+ * out_tokens[b] = draft[b, 1..accept], bonus, then -1 padding;
+ * tau[b] = accept[b] + 1 (nullable); new_len[b] = start[b] + accept[b] + 1,
+ * the trimmed target-cache length (nullable; may alias start). */
+int dflash_verify_greedy(const int32_t* draft, const int32_t* post, int32_t batch, int32_t B,
+                         const int32_t* start, int32_t* accept, int32_t* tau, int32_t* bonus,
+                         int32_t* out_tokens, int32_t* new_len, dflash_stream_t s);
+
+/* Final RMSNorm + shared LM head + fused argmax over rows of an fp32
+ * residual stream.  x: device fp32 [rows, D]; norm_gain: device fp32 [D];
+ * ids: device int32 [rows]; top2_gap: nullable device fp32 [rows]. */
+int dflash_lm_head_argmax(dflash_handle* h, const float* x, int32_t rows, const float* norm_gain,
+                          int32_t* ids, float* top2_gap, void* ws, size_t ws_bytes,
+                          dflash_stream_t s);
+
+/* Causal forward of a target model (qk_norm == 0 handle) over T new tokens
+ * per sequence, appended to its cache.  tokens: device int32 [batch, T] at
+ * positions len[b] .. len[b]+T-1; every row attends to cache entries
+ * 0 .. its own position.  kv->len advances by T.
+ *   tap_ids: host int32 [n_taps], 0-based layer ids; taps_out (nullable):
+ *            device [n_taps, batch*T, D] (handle dtype), the residual
+ *            stream after each listed layer.
+ *   argmax_out: device int32 [batch*T], greedy next token of every row
+ *            (final RMSNorm with g_f, shared LM head). */
+int dflash_target_forward(dflash_handle* h, const int32_t* tokens, int32_t batch, int32_t T,
+                          const dflash_kv* kv, const int32_t* tap_ids, int32_t n_taps,
+                          void* taps_out, int32_t* argmax_out, void* ws, size_t ws_bytes,
+                          dflash_stream_t s);
+
+/* Synchronise stream s, then read and clear the handle's device status word.
+ * Returns DFLASH_OK or the first device-detected error code. */
+int dflash_get_status(dflash_handle* h, dflash_stream_t s);
+
+const char* dflash_strerror(int code);
+
+/* Number of kernels this library has launched in this process. */
+int64_t dflash_launch_count(void);
+
+/* Per-kernel device timing.  While enabled, every launch of this handle is
+ * bracketed by CUDA events on its stream; dflash_timing_read synchronises,
+ * then returns for kernel class `kclass` the summed milliseconds and the
+ * launch count since the last reset (and resets that class). */
+enum dflash_kernel_class {
+  DFLASH_K_WEIGHT_GEMM = 0,   /* skinny weight-streaming projections */
+  DFLASH_K_ATTENTION = 1,
+  DFLASH_K_LM_HEAD = 2,
+  DFLASH_K_DENSE_GEMM = 3,    /* fuse / inject / prefill projections */
+  DFLASH_K_ELEMENTWISE = 4,   /* norms, embedding, RoPE, SwiGLU, bookkeeping */
+  DFLASH_K_VERIFY = 5,
+  DFLASH_K_NCLASS = 6
+};
+int dflash_timing_enable(dflash_handle* h, int on);
+int dflash_timing_read(dflash_handle* h, int32_t kclass, double* total_ms, int64_t* launches);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

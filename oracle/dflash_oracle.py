@@ -275,7 +275,8 @@ def top2_gap(z: np.ndarray) -> np.ndarray:
 
 def draft_block(shape, W: dict, ctx_K: List[List[np.ndarray]],
                 ctx_V: List[List[np.ndarray]], anchors: Sequence[int], B: int,
-                store=f32, return_logits: bool = False):
+                store=f32, return_logits: bool = False, lm_head: bool = True,
+                return_hidden: bool = False):
     """Single-pass draft of one block per sequence.
 
     ``shape`` has D, H, G, d, eps, rope_theta, mask_id, embed_scale.
@@ -287,11 +288,13 @@ def draft_block(shape, W: dict, ctx_K: List[List[np.ndarray]],
     each draft id is the argmax of its fp32 logits ([reading] §6, §14).
 
     Returns ids [batch, B] (column 0 = anchor), gap [batch, B-1] and,
-    if asked, logits [batch, B-1, V]."""
+    if asked, logits [batch, B-1, V] and the fp32 residual stream after the
+    last layer [batch, B, D].  With lm_head=False only the residual stream is
+    computed (ids and gaps are left zero)."""
     batch = len(anchors)
     ids = np.zeros((batch, B), dtype=np.int32)
     gaps = np.zeros((batch, B - 1), dtype=np.float64)
-    all_logits = []
+    all_logits, hidden = [], []
     for b in range(batch):
         L = ctx_K[0][b].shape[0]
         pos = np.arange(L, L + B)
@@ -299,16 +302,22 @@ def draft_block(shape, W: dict, ctx_K: List[List[np.ndarray]],
         for l, layer in enumerate(W["layers"]):
             x = draft_layer(x, layer, ctx_K[l][b], ctx_V[l][b], pos, shape.H,
                             shape.G, shape.d, shape.rope_theta, shape.eps, store)
+        hidden.append(x)
+        ids[b, 0] = anchors[b]
+        if not lm_head:
+            continue
         hf = store(rmsnorm(x[1:], W["g_f"], shape.eps))
         z = lm_head_logits(hf, W["lm_head"])
-        ids[b, 0] = anchors[b]
         ids[b, 1:] = argmax_lowest(z)
         gaps[b] = top2_gap(z)
         if return_logits:
             all_logits.append(z)
+    out = [ids, gaps]
     if return_logits:
-        return ids, gaps, np.stack(all_logits)
-    return ids, gaps
+        out.append(np.stack(all_logits))
+    if return_hidden:
+        out.append(np.stack(hidden))
+    return tuple(out)
 
 
 # ---------------------------------------------------------------------------

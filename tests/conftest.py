@@ -20,3 +20,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def dfl():
+    """The built CUDA binding (built in-tree on first use)."""
+    from block_diffusion_drafter_layer_gb300.build import build
+    build()
+    import block_diffusion_drafter_layer_gb300 as m
+    return m

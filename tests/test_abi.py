@@ -1,0 +1,66 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+symbol the header declares, and its host-only logic matches the oracle."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dflash.h")
+
+
+@pytest.fixture(scope="module")
+def dfl():
+    from block_diffusion_drafter_layer_gb300.build import build
+    build()
+    import block_diffusion_drafter_layer_gb300 as m
+    return m
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dflash_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("dflash_fuse_context", "dflash_inject_kv", "dflash_draft_block",
+              "dflash_verify_greedy", "dflash_create", "dflash_workspace_bytes"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(dfl):
+    lib = ctypes.CDLL(dfl.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(declared_functions()) == set(dfl.EXPORTED)
+
+
+@pytest.mark.parametrize("n_t", range(4, 70))
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8])
+def test_layer_ids_match_oracle(dfl, n_t, n):
+    try:
+        ref = O.build_target_layer_ids(n_t, n)
+    except ValueError:
+        with pytest.raises(dfl.DFlashError):
+            dfl.dflash_build_target_layer_ids(n_t, n)
+        return
+    assert dfl.dflash_build_target_layer_ids(n_t, n) == ref
+
+
+def test_strerror_and_argument_errors(dfl):
+    assert dfl.dflash_strerror(0) == "ok"
+    assert "capacity" in dfl.dflash_strerror(4)
+    with pytest.raises(dfl.DFlashError) as e:
+        dfl.dflash_build_target_layer_ids(36, 0)
+    assert e.value.code == 1
+    # null pointers are rejected on the host before any launch
+    lib = dfl._lib
+    assert lib.dflash_verify_greedy(None, None, 1, 4, None, None, None, None, None, None, None) == 1
+    assert lib.dflash_draft_block(None, None, 1, 4, None, None, None, None, None, 0, None) == 1
+    assert lib.dflash_fuse_context(None, None, 1, None, None, 0, None) == 1
+    assert lib.dflash_workspace_bytes(None, 16) == 0

@@ -1,0 +1,80 @@
+"""End-to-end greedy speculative loop on the GPU (fp32): losslessness.
+
+The loop's output must equal the oracle target's own greedy autoregressive
+output, token for token; the GPU's own autoregressive decode (one row per
+forward) must agree too, which checks that the kernels are row-invariant."""
+import collections
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from helpers import make_all_accept, to_np, to_np64
+
+pytestmark = pytest.mark.gpu
+
+
+def _upload(obj, dev="cuda"):
+    if isinstance(obj, np.ndarray):
+        return torch.from_numpy(np.ascontiguousarray(obj)).to(dev)
+    if isinstance(obj, dict):
+        return {k: _upload(v, dev) for k, v in obj.items()}
+    if isinstance(obj, list):
+        return [_upload(v, dev) for v in obj]
+    return obj
+
+
+def _run(dfl, w, TWn, DWn, prompt, n_new):
+    from synth.gpu import draft_model, spec_decoder, target_model
+    TW, DW = _upload(TWn), _upload(DWn)
+    DW["embed"], DW["lm_head"] = TW["embed"], TW["lm_head"]
+    cap = w.prompt_len + n_new + 2 * w.B
+    target = target_model(w.target, w.dtype, TW, max_pos=cap)
+    draft = draft_model(w.draft, w.dtype, DW, max_pos=cap)
+    dec = spec_decoder(w, target, draft, cap=cap)
+    spec, taus = dec.generate(prompt, n_new)
+    ar = dec.ar_decode(prompt, n_new)
+    assert dfl.dflash_get_status(target.handle) == 0
+    assert dfl.dflash_get_status(draft.handle) == 0
+    target.close()
+    draft.close()
+    return np.array(spec), np.array(ar), taus
+
+
+def _weights(w):
+    TW = to_np(synth.target_weights(w.target, w.dtype, w.seed))
+    DW = to_np(synth.draft_weights(w.draft, w.dtype, w.seed + 1,
+                                   shared={"embed": None, "lm_head": None}))
+    DW["embed"], DW["lm_head"] = TW["embed"], TW["lm_head"]
+    return TW, DW
+
+
+def test_e2e_lossless_256_tokens(dfl):
+    w = synth.WORKLOADS["e2e_f32"]
+    TW, DW = _weights(w)
+    prompt = synth.random_ids(w.prompt_len, w.target.V, seed=w.seed).tolist()
+    spec, ar_gpu, taus = _run(dfl, w, TW, DW, prompt, w.new_tokens)
+    ar_ref = O.ar_generate(w.target, to_np64(TW), prompt, w.new_tokens)
+    hist = collections.Counter(taus)
+    print(f"e2e: rounds {len(taus)}, mean tau {np.mean(taus):.3f}, "
+          f"tau histogram {dict(sorted(hist.items()))}")
+    np.testing.assert_array_equal(ar_gpu, ar_ref)
+    np.testing.assert_array_equal(spec, ar_ref)
+    assert all(1 <= t <= w.B for t in taus)
+
+
+def test_e2e_lossless_all_blocks_accepted(dfl):
+    """Every draft accepted (tau = B each round): exercises long accepted
+    prefixes, the cache trim and multi-row context injection per round."""
+    w = synth.with_(synth.WORKLOADS["e2e_f32"], new_tokens=96)
+    TW, DW = _weights(w)
+    c = 77
+    TW, DW = make_all_accept(TW, DW, w.target, c)
+    prompt = synth.random_ids(w.prompt_len - 1, w.target.V, seed=2).tolist() + [c]
+    spec, ar_gpu, taus = _run(dfl, w, TW, DW, prompt, w.new_tokens)
+    ar_ref = O.ar_generate(w.target, to_np64(TW), prompt, w.new_tokens)
+    np.testing.assert_array_equal(spec, ar_ref)
+    np.testing.assert_array_equal(ar_gpu, ar_ref)
+    assert taus == [w.B] * len(taus)

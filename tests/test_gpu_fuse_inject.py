@@ -1,0 +1,133 @@
+"""Context fusion and K/V injection on the GPU vs the oracle."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from helpers import TOL, float_parity, to_np, to_np64
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _models(dfl, w, weights, max_pos=4096):
+    from synth.gpu import draft_model
+    return draft_model(w.draft, w.dtype, weights, max_pos)
+
+
+def test_fuse_worked_example_gpu(dfl):
+    """The tutorial's printed context_feature[:3, :8], reproduced by the kernel."""
+    rows = [[float(v) for v in l.split()] for l in open(os.path.join(GOLDEN, "fuse_worked_example.txt"))
+            if l.strip() and not l.startswith("#")]
+    torch.manual_seed(42)
+    hs = [torch.randn(10, 64) for _ in range(5)]
+    lin = torch.nn.Linear(320, 64, bias=False)
+    dev = "cuda"
+    z = lambda *s: torch.zeros(*s, device=dev)
+    lay = {"wq": z(64, 64), "wk": z(64, 64), "wv": z(64, 64), "wo": z(64, 64), "wg": z(64, 64),
+           "wu": z(64, 64), "wd": z(64, 64), "g_in": z(64), "g_post": z(64), "q_norm": z(64),
+           "k_norm": z(64)}
+    weights = {"wc": lin.weight.detach().to(dev), "g_c": torch.ones(64, device=dev),
+               "g_f": torch.ones(64, device=dev), "embed": z(16, 64), "lm_head": z(16, 64),
+               "layers": [lay]}
+    m = dfl.Model(D=64, H=1, G=1, d=64, F=64, V=16, n_layers=1, dtype="f32", weights=weights,
+                  max_pos=16, qk_norm=True)
+    out = torch.empty(10, 64, device=dev)
+    dfl.dflash_fuse_context(m.handle, [h.to(dev) for h in hs], 10, out, m.workspace(10))
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    np.testing.assert_allclose(got[:3, :8], np.array(rows), atol=6e-5, rtol=0)
+    ref = O.fuse_context([h.numpy() for h in hs], lin.weight.detach().numpy(), np.ones(64), 1e-6)
+    np.testing.assert_allclose(got, ref, atol=1e-5, rtol=0)
+    m.close()
+
+
+@pytest.mark.parametrize("wname,T", [("tiny_f32", 64), ("tiny_f32", 4133), ("qwen3_8b_b1", 300)])
+def test_fuse_parity(dfl, wname, T):
+    w = synth.WORKLOADS[wname]
+    s = w.draft
+    weights = synth.draft_weights(s, w.dtype, w.seed, device="cuda")
+    hs = synth.target_hidden_states(T, s.D, s.n_pick, w.dtype, w.seed, device="cuda")
+    m = _models(dfl, w, weights)
+    out = torch.empty(T, s.D, dtype=synth.torch_dtype(w.dtype), device="cuda")
+    dfl.dflash_fuse_context(m.handle, hs, T, out, m.workspace(T))
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy()
+    hs_np, wc = [to_np(h) for h in hs], to_np(weights["wc"])
+    ref = O.fuse_context(hs_np, wc, np.ones(s.D), s.eps, O.storage(w.dtype))
+    err, exact = float_parity(got, ref, w.dtype, "H_t")
+    if w.dtype == "bf16":
+        ref32 = O.fuse_context(hs_np, wc, np.ones(s.D), s.eps, O.f32)
+        print(f"fuse {wname} T={T}: max|err| {err:.3e}, bit-equal {exact:.5f}; "
+              f"vs fp32-storage oracle {np.abs(got - ref32).max():.3e}")
+        assert exact > 0.99
+    m.close()
+
+
+@pytest.mark.parametrize("wname", ["tiny_f32", "qwen3_8b_b1", "qwen35_a3b_32k"])
+def test_inject_parity_ragged(dfl, wname):
+    w = synth.WORKLOADS[wname]
+    s = w.draft
+    dev = "cuda"
+    weights = synth.draft_weights(s, w.dtype, w.seed, device=dev)
+    m = _models(dfl, w, weights)
+    from synth.gpu import kv_cache
+    cap = 160
+    kv = kv_cache(s, 3, cap, w.dtype)
+    len0 = np.array([5, 0, 3], dtype=np.int32)
+    nrows = np.array([37, 27, 0], dtype=np.int32)
+    row0 = np.array([0, 37, 64], dtype=np.int32)
+    kv.len.copy_(torch.from_numpy(len0))
+    T = 64
+    H_t = synth.target_hidden_states(T, s.D, 1, w.dtype, w.seed + 3, device=dev)[0]
+    dfl.dflash_inject_kv(m.handle, H_t, T, torch.from_numpy(row0).to(dev),
+                         torch.from_numpy(nrows).to(dev), 3, kv.struct, m.workspace(T))
+    assert dfl.dflash_get_status(m.handle) == 0
+    np.testing.assert_array_equal(kv.len.cpu().numpy(), len0 + nrows)
+    Hn = to_np(H_t)
+    W64 = to_np64(weights)
+    store = O.storage(w.dtype)
+    for l in range(s.n_layers):
+        Kc, Vc = kv.k[l].float().cpu().numpy(), kv.v[l].float().cpu().numpy()
+        for b in range(3):
+            n, p0 = nrows[b], len0[b]
+            rows = Hn[row0[b]:row0[b] + n]
+            k, v = O.inject_kv(rows, W64["layers"][l], np.arange(p0, p0 + n), s.G, s.d,
+                               s.rope_theta, s.eps, store)
+            gk = Kc[b, :, p0:p0 + n, :].transpose(1, 0, 2)
+            gv = Vc[b, :, p0:p0 + n, :].transpose(1, 0, 2)
+            _, ek = float_parity(gk, k, w.dtype, f"K layer {l} seq {b}")
+            _, ev = float_parity(gv, v, w.dtype, f"V layer {l} seq {b}")
+            if n:
+                assert ek > 0.99 and ev > 0.99
+            # nothing outside the appended range was written
+            assert not Kc[b, :, :p0].any() and not Kc[b, :, p0 + n:].any()
+            assert not Vc[b, :, :p0].any() and not Vc[b, :, p0 + n:].any()
+    m.close()
+
+
+def test_fuse_sampled_rows_long_context(dfl):
+    """Full Qwen3.5-35B-A3B-shaped prefill (4 x 32768 rows): the kernel runs
+    on every row; the oracle recomputes a seeded sample of rows."""
+    w = synth.WORKLOADS["qwen35_a3b_32k"]
+    s = w.draft
+    T = w.batch * w.ctx_len
+    weights = synth.draft_weights(s, w.dtype, w.seed, device="cuda")
+    hs = synth.target_hidden_states(T, s.D, s.n_pick, w.dtype, w.seed, device="cuda")
+    m = _models(dfl, w, weights, max_pos=w.ctx_len + 64)
+    out = torch.empty(T, s.D, dtype=torch.bfloat16, device="cuda")
+    dfl.dflash_fuse_context(m.handle, hs, T, out, m.workspace(4096))
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(0).choice(T, 48, replace=False))
+    rows = np.concatenate([[0, T - 1], rows])
+    idx = torch.from_numpy(rows).cuda()
+    got = out[idx].float().cpu().numpy()
+    ref = O.fuse_context([h[idx].float().cpu().numpy() for h in hs], to_np(weights["wc"]),
+                         np.ones(s.D), s.eps, O.bf16)
+    _, exact = float_parity(got, ref, "bf16", "H_t sampled rows")
+    assert exact > 0.99
+    m.close()
