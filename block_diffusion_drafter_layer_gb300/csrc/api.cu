@@ -5,6 +5,8 @@
 #include <cstring>
 #include <vector>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace dflash {
@@ -53,12 +55,22 @@ constexpr int64_t kChunkRows = 4096;
 
 static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Scratch of the weight-streaming kernel: two fp32 partial tiles per CTA and
+// one top-2 record per (vocabulary tile, row).
+static size_t ws_partial_bytes(const dflash_handle* h) {
+  return round256((size_t)2 * std::max(h->num_sms, 1) * 64 * 128 * sizeof(float));
+}
+static size_t ws_amx_bytes(const dflash_handle* h) {
+  return round256((size_t)((h->cfg.vocab + 127) / 128) * 64 * sizeof(float4));
+}
+
 // Workspace of a forward pass (draft block, target forward, LM head) over R rows.
 static size_t forward_bytes(const dflash_config& c, int64_t R) {
   const size_t sz = esize(c.dtype);
   const int64_t D = c.hidden, Hd = (int64_t)c.n_heads * c.head_dim,
                 Gd = (int64_t)c.n_kv_heads * c.head_dim, F = c.ffn, V = c.vocab;
   size_t b = 0;
+  b += round256(R * F * sz);          // a (SwiGLU output)
   b += round256(R * D * 4);           // x
   b += round256(R * std::max(D, F) * sz);  // h / a
   b += round256(R * Hd * 4);          // qf
@@ -79,15 +91,20 @@ static size_t chunk_row_bytes(const dflash_config& c) {
 }
 
 struct Fwd {
-  float *x, *qf, *kf, *vf, *gf, *uf, *logits;
-  void *h, *q, *kb, *vb, *o, *hf;
+  float *x, *qf, *kf, *vf, *gf, *uf, *logits, *partial;
+  float4* amx;
+  void *h, *q, *kb, *vb, *o, *hf, *a;
 };
 
-static bool carve_forward(const dflash_config& c, int64_t R, void* ws, size_t ws_bytes, Fwd* f) {
+static bool carve_forward(const dflash_handle* h, int64_t R, void* ws, size_t ws_bytes, Fwd* f) {
+  const dflash_config& c = h->cfg;
   const size_t sz = esize(c.dtype);
   const int64_t D = c.hidden, Hd = (int64_t)c.n_heads * c.head_dim,
                 Gd = (int64_t)c.n_kv_heads * c.head_dim, F = c.ffn, V = c.vocab;
   Carve cv{(char*)ws, ws_bytes};
+  f->partial = cv.take<float>(ws_partial_bytes(h) / sizeof(float));
+  f->amx = cv.take<float4>(ws_amx_bytes(h) / sizeof(float4));
+  f->a = cv.take<char>(R * F * sz);
   f->x = cv.take<float>(R * D);
   f->h = cv.take<char>(R * std::max(D, F) * sz);
   f->qf = cv.take<float>(R * Hd);
@@ -138,6 +155,10 @@ static int mlp_tail(dflash_handle* h, cudaStream_t s, const dflash_layer_weights
   return gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, one_src(f.h, F, F), L.wd, F, f.x, D, R, D, F, true);
 }
 
+static bool streaming(const dflash_handle* h, int64_t M);
+static int lm_head_stream(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows, int32_t* ids,
+                          float* gap, int rps_out, const int32_t* anchor);
+
 static int lm_head(dflash_handle* h, cudaStream_t s, Fwd& f, const float* x, int64_t rows,
                    const float* gain, int skip_first_of, int32_t* ids, float* gap, int rps_out,
                    const int32_t* anchor) {
@@ -147,16 +168,161 @@ static int lm_head(dflash_handle* h, cudaStream_t s, Fwd& f, const float* x, int
   if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, x, D, f.hf, D, gain, rows, D, c.rms_eps,
                          skip_first_of)))
     return rc;
+  if (streaming(h, rows)) return lm_head_stream(h, s, f, rows, ids, gap, rps_out, anchor);
   if ((rc = gemm(h, s, DFLASH_K_LM_HEAD, dt, one_src(f.hf, D, D), h->w.lm_head, D, f.logits, V,
                  rows, V, D, false)))
     return rc;
   return argmax_rows(h, s, f.logits, rows, V, ids, gap, rps_out, anchor);
 }
 
+// ---- weight-streaming paths (bf16, at most 64 activation rows) -------------
+static bool streaming(const dflash_handle* h, int64_t M) {
+  return h->have_maps && M >= 1 && M <= 64;
+}
+
+static WSeg make_seg(int t0, int t1, int kind, int map, int n_valid, void* dst, int64_t ld) {
+  WSeg g{};
+  g.t0 = t0;
+  g.t1 = t1;
+  g.kind = kind;
+  g.map = map;
+  g.n_valid = n_valid;
+  g.dst = dst;
+  g.ld = ld;
+  return g;
+}
+
+static WSeg head_seg(int t0, int t1, int map, int n_valid, int d, int rope, const float* gain,
+                     void* dst, int64_t ld) {
+  WSeg g = make_seg(t0, t1, SK_HEAD, map, n_valid, dst, ld);
+  g.d = d;
+  g.rope = rope;
+  g.gain = gain;
+  return g;
+}
+
+// q, k, v of the block rows in one launch; the epilogue applies the per-head
+// q/k RMSNorm and RoPE and stores bf16 heads for the attention kernel.
+static int qkv_stream(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R, const RowMap& rm,
+                      const int32_t* len) {
+  const dflash_config& c = h->cfg;
+  const dflash_layer_weights& W = h->w.layers[l];
+  const int D = c.hidden, d = c.head_dim, Hd = c.n_heads * d, Gd = c.n_kv_heads * d;
+  const int tq = Hd / 128, tk = Gd / 128;
+  WLaunch L;
+  L.nmap = 3;
+  L.wmaps[0] = &h->maps[l].wq;
+  L.wmaps[1] = &h->maps[l].wk;
+  L.wmaps[2] = &h->maps[l].wv;
+  L.nseg = 3;
+  L.seg[0] = head_seg(0, tq, 0, Hd, d, 1, c.qk_norm ? W.q_norm : nullptr, f.q, Hd);
+  L.seg[1] = head_seg(tq, tq + tk, 1, Gd, d, 1, c.qk_norm ? W.k_norm : nullptr, f.kb, Gd);
+  L.seg[2] = head_seg(tq + tk, tq + 2 * tk, 2, Gd, d, 0, nullptr, f.vb, Gd);
+  L.nsrc = 1;
+  L.a_src[0] = f.h;
+  L.a_ld = D;
+  L.K = D;
+  L.M = (int)R;
+  L.rm = rm;
+  L.len = len;
+  return wstream(h, s, DFLASH_K_WEIGHT_GEMM, L, f.partial, f.amx);
+}
+
+// o_proj (+ residual), RMSNorm, gate/up with the SwiGLU epilogue, down (+ residual).
+static int mlp_stream(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R) {
+  const dflash_config& c = h->cfg;
+  const dflash_layer_weights& W = h->w.layers[l];
+  const int D = c.hidden, F = c.ffn, Hd = c.n_heads * c.head_dim, dt = c.dtype;
+  int rc;
+  WLaunch L;
+  L.nmap = 1;
+  L.wmaps[0] = &h->maps[l].wo;
+  L.nseg = 1;
+  L.seg[0] = make_seg(0, (D + 127) / 128, SK_RESID, 0, D, f.x, D);
+  L.nsrc = 1;
+  L.a_src[0] = f.o;
+  L.a_ld = Hd;
+  L.K = Hd;
+  L.M = (int)R;
+  if ((rc = wstream(h, s, DFLASH_K_WEIGHT_GEMM, L, f.partial, f.amx))) return rc;
+  if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, W.g_post, R, D, c.rms_eps, 0)))
+    return rc;
+  WLaunch G;
+  G.nmap = 2;
+  G.wmaps[0] = &h->maps[l].wg;
+  G.wmaps[1] = &h->maps[l].wu;
+  G.nseg = 1;
+  G.seg[0] = make_seg(0, (F + 63) / 64, SK_SWIGLU, 0, F, f.a, F);
+  G.seg[0].map2 = 1;
+  G.nsrc = 1;
+  G.a_src[0] = f.h;
+  G.a_ld = D;
+  G.K = D;
+  G.M = (int)R;
+  if ((rc = wstream(h, s, DFLASH_K_WEIGHT_GEMM, G, f.partial, f.amx))) return rc;
+  WLaunch Dn;
+  Dn.nmap = 1;
+  Dn.wmaps[0] = &h->maps[l].wd;
+  Dn.nseg = 1;
+  Dn.seg[0] = make_seg(0, (D + 127) / 128, SK_RESID, 0, D, f.x, D);
+  Dn.nsrc = 1;
+  Dn.a_src[0] = f.a;
+  Dn.a_ld = F;
+  Dn.K = F;
+  Dn.M = (int)R;
+  return wstream(h, s, DFLASH_K_WEIGHT_GEMM, Dn, f.partial, f.amx);
+}
+
+static int lm_head_stream(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows, int32_t* ids,
+                          float* gap, int rps_out, const int32_t* anchor) {
+  const dflash_config& c = h->cfg;
+  WLaunch L;
+  L.nmap = 1;
+  L.wmaps[0] = &h->map_lm;
+  L.nseg = 1;
+  L.seg[0] = make_seg(0, (c.vocab + 127) / 128, SK_ARGMAX, 0, c.vocab, nullptr, 0);
+  L.nsrc = 1;
+  L.a_src[0] = f.hf;
+  L.a_ld = c.hidden;
+  L.K = c.hidden;
+  L.M = (int)rows;
+  L.ids = ids;
+  L.gap = gap;
+  L.rps_out = rps_out;
+  L.anchor = anchor;
+  return wstream(h, s, DFLASH_K_LM_HEAD, L, f.partial, f.amx);
+}
+
 static bool kv_ok(const dflash_handle* h, const dflash_kv* kv, int batch) {
   if (!kv || !kv->len || kv->cap <= 0 || kv->batch_cap < batch) return false;
   for (int l = 0; l < h->cfg.n_layers; ++l)
     if (!kv->k[l] || !kv->v[l] || !aligned16(kv->k[l]) || !aligned16(kv->v[l])) return false;
+  return true;
+}
+
+// TMA descriptors of every bf16 weight, built once per handle.  Shapes that
+// do not tile into 128-row / 64-column blocks keep the portable kernels.
+static bool make_weight_maps(dflash_handle* h) {
+  const dflash_config& c = h->cfg;
+  const dflash_weights& w = h->w;
+  const int64_t D = c.hidden, d = c.head_dim, Hd = c.n_heads * d, Gd = c.n_kv_heads * d,
+                F = c.ffn, V = c.vocab;
+  if (c.dtype != DFLASH_BF16 || D % 128 || Hd % 128 || Gd % 128 || F % 64 || h->num_sms < 1)
+    return false;
+  auto mk = [](CUtensorMap* m, const void* p, int64_t rows, int64_t cols, uint32_t box_rows) {
+    return make_tmap_2d(m, p, (uint64_t)cols, (uint64_t)rows, (uint64_t)cols * 2, 64, box_rows);
+  };
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& L = w.layers[l];
+    LayerMaps& M = h->maps[l];
+    if (!mk(&M.wq, L.wq, Hd, D, 128) || !mk(&M.wk, L.wk, Gd, D, 128) ||
+        !mk(&M.wv, L.wv, Gd, D, 128) || !mk(&M.wo, L.wo, D, Hd, 128) ||
+        !mk(&M.wg, L.wg, F, D, 64) || !mk(&M.wu, L.wu, F, D, 64) || !mk(&M.wd, L.wd, D, F, 128))
+      return false;
+  }
+  if (w.wc && !mk(&h->map_wc, w.wc, D, c.n_pick * D, 128)) return false;
+  if (!mk(&h->map_lm, w.lm_head, V, D, 128)) return false;
+  h->have_maps = true;
   return true;
 }
 
@@ -233,11 +399,16 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   h->cfg = c;
   h->w = *w;
   h->device = dev;
-  if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess) {
+  cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess ||
+      cudaMalloc(&h->d_counters, (kMaxTiles + 1) * sizeof(int)) != cudaSuccess) {
+    cudaFree(h->d_status);
     delete h;
     return DFLASH_ERR_CUDA;
   }
   cudaMemset(h->d_status, 0, sizeof(int));
+  cudaMemset(h->d_counters, 0, (kMaxTiles + 1) * sizeof(int));
+  if (!make_weight_maps(h)) h->have_maps = false;
   // RoPE table: angle pos * theta^(-2i/d) in double precision, stored as fp32.
   const int half = c.head_dim / 2;
   std::vector<float2> tab((size_t)c.max_pos * half);
@@ -251,6 +422,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
       cudaMemcpy(h->d_rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
           cudaSuccess) {
     cudaFree(h->d_status);
+    cudaFree(h->d_counters);
     cudaFree(h->d_rope);
     delete h;
     return DFLASH_ERR_CUDA;
@@ -268,6 +440,7 @@ int dflash_destroy(dflash_handle* h) {
   }
   for (auto e : h->free_events) cudaEventDestroy(e);
   cudaFree(h->d_status);
+  cudaFree(h->d_counters);
   cudaFree(h->d_rope);
   delete h;
   return DFLASH_OK;
@@ -277,9 +450,10 @@ size_t dflash_workspace_bytes(const dflash_handle* h, int64_t max_rows) {
   if (!h || max_rows < 0) return 0;
   const int64_t R = std::max<int64_t>(max_rows, 1);
   // a forward pass over R rows, or fuse / inject in full kChunkRows passes
+  const size_t scratch = ws_partial_bytes(h) + ws_amx_bytes(h) + 512;
   const size_t fwd = forward_bytes(h->cfg, R);
   const size_t chunk = round256(kChunkRows * chunk_row_bytes(h->cfg)) + 1024;
-  return std::max(fwd, chunk);
+  return std::max(fwd, chunk) + scratch;
 }
 
 int dflash_fuse_context(dflash_handle* h, const void* const* hidden, int64_t T, void* h_t_out,
@@ -296,6 +470,25 @@ int dflash_fuse_context(dflash_handle* h, const void* const* hidden, int64_t T, 
   if (!aligned16(h_t_out) || !aligned16(ws)) return DFLASH_ERR_ALIGNMENT;
   cudaStream_t s = (cudaStream_t)st;
   const int D = c.hidden, dt = c.dtype;
+  if (streaming(h, T)) {
+    Carve cv{(char*)ws, ws_bytes};
+    float* partial = cv.take<float>(ws_partial_bytes(h) / sizeof(float));
+    float* Y = cv.take<float>(T * D);
+    if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+    WLaunch L;
+    L.nmap = 1;
+    L.wmaps[0] = &h->map_wc;
+    L.nseg = 1;
+    L.seg[0] = make_seg(0, (D + 127) / 128, SK_F32, 0, D, Y, D);
+    L.nsrc = c.n_pick;
+    for (int i = 0; i < c.n_pick; ++i) L.a_src[i] = hidden[i];
+    L.a_ld = D;
+    L.K = c.n_pick * D;
+    L.M = (int)T;
+    int rc = wstream(h, s, DFLASH_K_DENSE_GEMM, L, partial, nullptr);
+    if (rc) return rc;
+    return rmsnorm_rows(h, s, DFLASH_F32, dt, Y, D, h_t_out, D, h->w.g_c, T, D, c.rms_eps, 0);
+  }
   const int64_t chunk = std::min<int64_t>(kChunkRows, (int64_t)(ws_bytes / (D * 4 + 1)));
   if (chunk < 1) return DFLASH_ERR_WORKSPACE;
   float* Y = (float*)ws;
@@ -326,6 +519,44 @@ int dflash_inject_kv(dflash_handle* h, const void* h_t, int64_t n_rows, const in
   cudaStream_t s = (cudaStream_t)st;
   const dflash_config& c = h->cfg;
   const int D = c.hidden, G = c.n_kv_heads, d = c.head_dim, Gd = G * d, dt = c.dtype;
+  if (n_rows == 0) return advance_len(h, s, kv->len, seq_rows, 0, batch, kv->cap);
+  if (streaming(h, n_rows)) {
+    Carve cv{(char*)ws, ws_bytes};
+    float* partial = cv.take<float>(ws_partial_bytes(h) / sizeof(float));
+    if (!cv.ok) return DFLASH_ERR_WORKSPACE;
+    const int tk = Gd / 128;
+    const RowMap rm{1, 0, seq_row0, seq_rows, batch, 0};
+    for (int l0 = 0; l0 < c.n_layers; l0 += WS_MAXMAP / 2) {
+      const int nl = std::min(WS_MAXMAP / 2, c.n_layers - l0);
+      WLaunch L;
+      L.nmap = 2 * nl;
+      L.nseg = 2 * nl;
+      for (int j = 0; j < nl; ++j) {
+        const int l = l0 + j;
+        L.wmaps[2 * j] = &h->maps[l].wk;
+        L.wmaps[2 * j + 1] = &h->maps[l].wv;
+        WSeg gk = head_seg(2 * j * tk, (2 * j + 1) * tk, 2 * j, Gd, d, 1,
+                           c.qk_norm ? h->w.layers[l].k_norm : nullptr, kv->k[l], 0);
+        WSeg gv = head_seg((2 * j + 1) * tk, (2 * j + 2) * tk, 2 * j + 1, Gd, d, 0, nullptr,
+                           kv->v[l], 0);
+        gk.cache_cap = gv.cache_cap = kv->cap;
+        gk.cache_heads = gv.cache_heads = G;
+        gk.cache_batch = gv.cache_batch = kv->batch_cap;
+        L.seg[2 * j] = gk;
+        L.seg[2 * j + 1] = gv;
+      }
+      L.nsrc = 1;
+      L.a_src[0] = h_t;
+      L.a_ld = D;
+      L.K = D;
+      L.M = (int)n_rows;
+      L.rm = rm;
+      L.len = kv->len;
+      const int rc = wstream(h, s, DFLASH_K_DENSE_GEMM, L, partial, nullptr);
+      if (rc) return rc;
+    }
+    return advance_len(h, s, kv->len, seq_rows, 0, batch, kv->cap);
+  }
   const int64_t chunk = std::min<int64_t>(kChunkRows, (int64_t)(ws_bytes / (2 * Gd * 4 + 512)));
   if (chunk < 1) return DFLASH_ERR_WORKSPACE;
   Carve cv{(char*)ws, ws_bytes};
@@ -364,16 +595,25 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
   const int Hd = H * d, Gd = G * d;
   const int64_t R = (int64_t)batch * B;
   Fwd f;
-  if (!carve_forward(c, R, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
+  if (!carve_forward(h, R, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
   int rc;
   if ((rc = embed_block(h, s, dt, h->w.embed, anchor, c.mask_token_id, batch, B, c.vocab, D,
                         c.embed_scale, f.x)))
     return rc;
   const RowMap rm{0, B, nullptr, nullptr, batch, 0};
+  const bool stream = streaming(h, R);
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights& L = h->w.layers[l];
     if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, L.g_in, R, D, c.rms_eps, 0)))
       return rc;
+    if (stream) {
+      if ((rc = qkv_stream(h, s, l, f, R, rm, kv->len))) return rc;
+      if ((rc = attention(h, s, dt, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch,
+                          B, H, G, d, false, f.o)))
+        return rc;
+      if ((rc = mlp_stream(h, s, l, f, R))) return rc;
+      continue;
+    }
     const ASrc a = one_src(f.h, D, D);
     if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, a, L.wq, D, f.qf, Hd, R, Hd, D, false))) return rc;
     if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, a, L.wk, D, f.kf, Gd, R, Gd, D, false))) return rc;
@@ -420,7 +660,7 @@ int dflash_lm_head_argmax(dflash_handle* h, const float* x, int32_t rows, const 
   if (!h || !x || !norm_gain || !ids || !ws || rows < 0) return DFLASH_ERR_INVALID_ARG;
   if (rows == 0) return DFLASH_OK;
   Fwd f;
-  if (!carve_forward(h->cfg, rows, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
+  if (!carve_forward(h, rows, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
   return lm_head(h, (cudaStream_t)st, f, x, rows, norm_gain, 0, ids, top2_gap, 0, nullptr);
 }
 
@@ -440,7 +680,7 @@ int dflash_target_forward(dflash_handle* h, const int32_t* tokens, int32_t batch
   const int Hd = H * d, Gd = G * d;
   const int64_t R = (int64_t)batch * T;
   Fwd f;
-  if (!carve_forward(c, R, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
+  if (!carve_forward(h, R, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
   int rc;
   if ((rc = embed_tokens(h, s, dt, h->w.embed, tokens, (int)R, c.vocab, D, c.embed_scale, f.x)))
     return rc;
@@ -482,6 +722,8 @@ int dflash_get_status(dflash_handle* h, dflash_stream_t st) {
   if (cudaMemcpy(&v, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return DFLASH_ERR_CUDA;
   cudaMemset(h->d_status, 0, sizeof(int));
+  // a launch that gave up may have left tile counters mid-count
+  if (v & ST_TIMEOUT) cudaMemset(h->d_counters, 0, (kMaxTiles + 1) * sizeof(int));
   if (v & ST_CAPACITY) return DFLASH_ERR_CAPACITY;
   if (v & ST_BOUNDS) return DFLASH_ERR_DEVICE_BOUNDS;
   if (v & ST_TIMEOUT) return DFLASH_ERR_DEVICE_TIMEOUT;
@@ -517,3 +759,30 @@ int dflash_timing_read(dflash_handle* h, int32_t kclass, double* total_ms, int64
 }
 
 }  // extern "C"
+
+namespace dflash {
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+}  // namespace dflash

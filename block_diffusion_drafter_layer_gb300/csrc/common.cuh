@@ -1,6 +1,7 @@
 // Internal declarations shared by the libdflash translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -99,12 +100,26 @@ struct Timer {
 
 }  // namespace dflash
 
+namespace dflash {
+// TMA descriptors of one layer's bf16 weights (box 64 x 128 rows; SwiGLU
+// halves use 64 x 64 so a 128-row tile holds 64 gate + 64 up rows).
+struct LayerMaps {
+  CUtensorMap wq, wk, wv, wo, wg, wu, wd;
+};
+constexpr int kMaxTiles = 8192;   // 128-row weight tiles per projection launch
+}  // namespace dflash
+
 struct dflash_handle {
   dflash_config cfg;
   dflash_weights w;
   int device = 0;
+  int num_sms = 0;
   int* d_status = nullptr;
+  int* d_counters = nullptr;       // [kMaxTiles + 1] tile arrival counters, zero between launches
   float2* d_rope = nullptr;        // [max_pos, d/2] (cos, sin)
+  bool have_maps = false;
+  dflash::LayerMaps maps[DFLASH_MAX_LAYERS];
+  CUtensorMap map_wc, map_lm;
   bool timing = false;
   std::vector<cudaEvent_t> free_events;
   std::vector<dflash::Timer> pending;
@@ -132,6 +147,51 @@ struct Carve {
     return p;
   }
 };
+
+// ---- weight-streaming projection (k_wstream.cu) ----------------------------
+constexpr int WS_MAXMAP = 10;   // weight tensor maps per launch
+constexpr int WS_MAXSRC = 5;    // activation sources along K (fused context)
+enum SegKind : int { SK_F32 = 0, SK_RESID = 1, SK_HEAD = 2, SK_SWIGLU = 3, SK_ARGMAX = 4 };
+
+// One output segment: tiles [t0, t1) of the launch read weight map `map`
+// (and `map2`, the up projection, for SwiGLU) and finish with `kind`.
+struct WSeg {
+  int t0, t1;
+  int kind;
+  int map, map2;
+  int n_valid;          // valid output columns (features) of the segment
+  int d;                // SK_HEAD: head dim
+  int rope;             // SK_HEAD: rotate
+  const float* gain;    // SK_HEAD: per-head RMSNorm gain, or null
+  void* dst;            // output base
+  int64_t ld;           // dense output row stride (elements)
+  int cache_cap;        // SK_HEAD: > 0 appends into a [batch, heads, cap, d] cache
+  int cache_heads;
+  int cache_batch;
+};
+
+struct WLaunch {
+  int nseg = 0;
+  WSeg seg[WS_MAXMAP];
+  int nmap = 0;
+  const CUtensorMap* wmaps[WS_MAXMAP];
+  int nsrc = 0;
+  const void* a_src[WS_MAXSRC];
+  int64_t a_ld = 0;     // activation row stride (elements)
+  int K = 0, M = 0;
+  RowMap rm{};
+  const int32_t* len = nullptr;
+  int32_t* ids = nullptr;
+  float* gap = nullptr;
+  int rps_out = 0;
+  const int32_t* anchor = nullptr;
+};
+
+bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+size_t wstream_scratch_bytes(const dflash_handle* h, int M);
+int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float* partial,
+            float4* amx);
 
 // ---- kernel launchers (one translation unit each) --------------------------
 // A operand source: up to DFLASH_MAX_PICK column segments of width seg

@@ -1,0 +1,517 @@
+// Weight-streaming projection for few activation rows (M <= 64).
+//
+// At draft time every projection multiplies a handful of rows (the B block
+// rows of each sequence) by a large bf16 weight, so the work is bound by
+// reading the weight once from HBM.  The kernel therefore:
+//   * splits the weight into 128-row x 64-column tiles (16 KB) and hands
+//     every CTA (one per SM) an equal contiguous run of (tile, k-chunk)
+//     units, so all SMs stream the same number of bytes whatever the shape;
+//   * stages weight and activation chunks with TMA into an 8-deep
+//     shared-memory ring guarded by mbarriers (warp 0 produces, warps 1-4
+//     consume), prefetching the first weight chunks before waiting for the
+//     previous kernel (programmatic dependent launch);
+//   * multiplies with warp-level bf16 MMA (m16n8k16, fp32 accumulate);
+//   * combines the k-split partial sums of a tile in a fixed order in the
+//     CTA that finishes the tile last, then runs a fused epilogue: fp32
+//     store, residual add, SwiGLU, per-head RMSNorm + RoPE (+ cache append),
+//     or a top-2 argmax whose last tile merges the whole vocabulary.
+#include <string.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dflash {
+
+using namespace ptx;
+
+constexpr int WS_THREADS = 160;
+constexpr int WS_EPAD = 132;
+
+struct WParams {
+  CUtensorMap wmap[WS_MAXMAP];
+  CUtensorMap amap[WS_MAXSRC];
+  WSeg seg[WS_MAXMAP];
+  int nseg, n_tiles, kc, kc_per_src, M, grid, units;
+  float* partial;
+  int* counters;
+  int* status;
+  RowMap rm;
+  const int32_t* len;
+  const float2* rope_tab;
+  int max_pos;
+  float eps;
+  float4* amx;
+  int* amx_done;
+  int32_t* ids;
+  float* gap;
+  int rps_out;
+  const int32_t* anchor;
+};
+
+static_assert(sizeof(WParams) <= 4096, "kernel parameters must fit the 4 KB limit");
+
+template <int MT>
+struct WCfg {
+  static constexpr int STAGES = MT >= 4 ? 7 : 8;
+  static constexpr int W_BYTES = 128 * 64 * 2;
+  static constexpr int A_BYTES = MT * 16 * 64 * 2;
+  static constexpr int STAGE_TX = W_BYTES + A_BYTES;
+  static constexpr int OFF_A = STAGES * W_BYTES;
+  static constexpr int OFF_E = OFF_A + STAGES * A_BYTES;
+  static constexpr int E_FLOATS = MT * 16 * WS_EPAD;
+  static constexpr int OFF_BAR = OFF_E + E_FLOATS * 4;
+  static constexpr int OFF_MISC = OFF_BAR + 2 * STAGES * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+};
+
+__device__ __forceinline__ int seg_of(const WParams& p, int t) {
+  int s = 0;
+  while (s + 1 < p.nseg && t >= p.seg[s + 1].t0) ++s;
+  return s;
+}
+
+// CTA that owns unit u when U units are split evenly over G CTAs.
+__device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int64_t G) {
+  return (int)(((u + 1) * G + U - 1) / U) - 1;
+}
+__device__ __forceinline__ int first_unit(int64_t c, int64_t U, int64_t G) {
+  return (int)(c * U / G);
+}
+
+struct Top2 {
+  float t1;
+  int i1;
+  float t2;
+};
+__device__ __forceinline__ Top2 top2_merge(Top2 a, Top2 b) {
+  Top2 r;
+  if (b.t1 > a.t1 || (b.t1 == a.t1 && b.i1 < a.i1)) {
+    r.t1 = b.t1;
+    r.i1 = b.i1;
+  } else {
+    r.t1 = a.t1;
+    r.i1 = a.i1;
+  }
+  r.t2 = fmaxf(fminf(a.t1, b.t1), fmaxf(a.t2, b.t2));
+  return r;
+}
+__device__ __forceinline__ Top2 top2_warp(Top2 t) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Top2 u;
+    u.t1 = __shfl_xor_sync(0xffffffffu, t.t1, o);
+    u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
+    u.t2 = __shfl_xor_sync(0xffffffffu, t.t2, o);
+    t = top2_merge(t, u);
+  }
+  return t;
+}
+
+// ---- epilogues (128 consumer threads, final fp32 tile in E) ------------------
+template <int MT>
+__device__ void ws_epilogue(const WParams& p, int t, const float* E, volatile int* misc) {
+  const int tid = threadIdx.x - 32, cw = tid >> 5, lane = threadIdx.x & 31;
+  const WSeg& g = p.seg[seg_of(p, t)];
+  const int lt = t - g.t0;
+  const int M = p.M;
+  if (g.kind == SK_F32 || g.kind == SK_RESID) {
+    float* dst = (float*)g.dst;
+    for (int e = tid; e < M * 128; e += 128) {
+      const int r = e >> 7, c = e & 127;
+      const int n = lt * 128 + c;
+      if (n >= g.n_valid) continue;
+      float* o = dst + (int64_t)r * g.ld + n;
+      const float v = E[r * WS_EPAD + c];
+      *o = (g.kind == SK_RESID) ? (*o + v) : v;
+    }
+  } else if (g.kind == SK_SWIGLU) {
+    bf16* dst = (bf16*)g.dst;
+    for (int e = tid; e < M * 64; e += 128) {
+      const int r = e >> 6, c = e & 63;
+      const int f = lt * 64 + c;
+      if (f >= g.n_valid) continue;
+      const float gv = E[r * WS_EPAD + c], uv = E[r * WS_EPAD + 64 + c];
+      dst[(int64_t)r * g.ld + f] = __float2bfloat16_rn(gv / (1.0f + expf(-gv)) * uv);
+    }
+  } else if (g.kind == SK_HEAD) {
+    const int d = g.d, half = d >> 1, P = half >> 5, hpt = 128 / d;
+    for (int pi = cw; pi < M * hpt; pi += 4) {
+      const int r = pi / hpt, j = pi - r * hpt;
+      const int head = lt * hpt + j;
+      const float* src = E + r * WS_EPAD + j * d;
+      float x1[2], x2[2], ss = 0.f;
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        if (q < P) {
+          const int jj = lane + 32 * q;
+          x1[q] = src[jj];
+          x2[q] = src[jj + half];
+          ss += x1[q] * x1[q] + x2[q] * x2[q];
+        }
+      if (g.gain != nullptr) {
+        ss = warp_sum(ss);
+        const float rinv = 1.0f / sqrtf(ss / (float)d + p.eps);
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (q < P) {
+            const int jj = lane + 32 * q;
+            x1[q] = x1[q] * rinv * g.gain[jj];
+            x2[q] = x2[q] * rinv * g.gain[jj + half];
+          }
+      }
+      int b, i;
+      if (!p.rm.map(r, b, i)) continue;
+      const int pos = p.len[b] + i;
+      if (g.rope) {
+        if (pos < 0 || pos >= p.max_pos) {
+          if (lane == 0) atomicOr(p.status, ST_BOUNDS);
+          continue;
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (q < P) {
+            const int jj = lane + 32 * q;
+            const float2 cs = p.rope_tab[(int64_t)pos * half + jj];
+            const float y1 = x1[q] * cs.x - x2[q] * cs.y;
+            const float y2 = x2[q] * cs.x + x1[q] * cs.y;
+            x1[q] = y1;
+            x2[q] = y2;
+          }
+      }
+      bf16* o;
+      if (g.cache_cap > 0) {
+        if (b >= g.cache_batch || pos < 0 || pos >= g.cache_cap) {
+          if (lane == 0) atomicOr(p.status, ST_CAPACITY);
+          continue;
+        }
+        o = (bf16*)g.dst + (((int64_t)b * g.cache_heads + head) * g.cache_cap + pos) * d;
+      } else {
+        o = (bf16*)g.dst + (int64_t)r * g.ld + (int64_t)head * d;
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        if (q < P) {
+          const int jj = lane + 32 * q;
+          o[jj] = __float2bfloat16_rn(x1[q]);
+          o[jj + half] = __float2bfloat16_rn(x2[q]);
+        }
+    }
+  } else if (g.kind == SK_ARGMAX) {
+    for (int r = cw; r < M; r += 4) {
+      Top2 tt{-INFINITY, 0x7fffffff, -INFINITY};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = lane + 32 * q;
+        const int n = lt * 128 + c;
+        if (n >= g.n_valid) continue;
+        const float v = E[r * WS_EPAD + c];
+        Top2 u{v, n, -INFINITY};
+        tt = top2_merge(tt, u);
+      }
+      tt = top2_warp(tt);
+      if (lane == 0) p.amx[(int64_t)t * M + r] = make_float4(tt.t1, __int_as_float(tt.i1), tt.t2, 0.f);
+    }
+    __threadfence();
+    named_bar(1, 128);
+    if (tid == 0) {
+      const int old = atomicAdd(p.amx_done, 1);
+      const int last = (old == p.n_tiles - 1);
+      if (last) *p.amx_done = 0;
+      misc[1] = last;
+    }
+    named_bar(1, 128);
+    if (!misc[1]) return;
+    __threadfence();
+    for (int r = cw; r < M; r += 4) {
+      Top2 tt{-INFINITY, 0x7fffffff, -INFINITY};
+      for (int tt_i = lane; tt_i < p.n_tiles; tt_i += 32) {
+        const float4 rec = __ldcg(&p.amx[(int64_t)tt_i * M + r]);
+        Top2 u{rec.x, __float_as_int(rec.y), rec.z};
+        tt = top2_merge(tt, u);
+      }
+      tt = top2_warp(tt);
+      if (lane == 0) {
+        int64_t out = r, gout = r;
+        if (p.rps_out > 0) {
+          const int per = p.rps_out - 1;
+          const int64_t b = r / per, i = r % per + 1;
+          out = b * p.rps_out + i;
+          gout = b * per + (i - 1);
+          if (i == 1) p.ids[b * p.rps_out] = p.anchor[b];
+        }
+        p.ids[out] = tt.i1;
+        if (p.gap) p.gap[gout] = tt.t1 - tt.t2;
+      }
+    }
+  }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(WS_THREADS, 1) wstream_kernel(const __grid_constant__ WParams p) {
+  using C = WCfg<MT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + C::OFF_BAR, bar_empty = bar_full + 8 * C::STAGES;
+  volatile int* misc = (volatile int*)(smem + C::OFF_MISC);  // 0 abort, 1 last, 2 issued, 3 consumed
+  float* E = (float*)(smem + C::OFF_E);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t U = p.units, G = p.grid;
+  const int cta = blockIdx.x;
+  const int u0 = first_unit(cta, U, G), u1 = first_unit(cta + 1, U, G);
+  const int n = u1 - u0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 4);
+    }
+    misc[0] = misc[1] = misc[2] = misc[3] = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- producer: one lane issues every TMA load ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+      auto issue_w = [&](int u, int s) {
+        const int t = u / p.kc, kk = u - t * p.kc;
+        const WSeg& g = p.seg[seg_of(p, t)];
+        const int lt = t - g.t0;
+        const uint32_t dst = sbase + s * C::W_BYTES, bar = bar_full + 8 * s;
+        if (g.kind == SK_SWIGLU) {
+          tma_load_2d(dst, &p.wmap[g.map], bar, kk * 64, lt * 64, pol_w);
+          tma_load_2d(dst + C::W_BYTES / 2, &p.wmap[g.map2], bar, kk * 64, lt * 64, pol_w);
+        } else {
+          tma_load_2d(dst, &p.wmap[g.map], bar, kk * 64, lt * 128, pol_w);
+        }
+      };
+      auto issue_a = [&](int u, int s) {
+        const int kk = u % p.kc;
+        const int src = kk / p.kc_per_src, lk = kk - src * p.kc_per_src;
+        tma_load_2d(sbase + C::OFF_A + s * C::A_BYTES, &p.amap[src], bar_full + 8 * s, lk * 64, 0,
+                    pol_a);
+      };
+      const int pre = n < C::STAGES ? n : C::STAGES;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(bar_full + 8 * i, C::STAGE_TX);
+        issue_w(u0 + i, i);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) issue_a(u0 + i, i);
+      int issued = pre;
+      for (int i = pre; i < n; ++i) {
+        const int s = i % C::STAGES, use = i / C::STAGES;
+        if (misc[0]) break;
+        if (!mbar_wait(bar_empty + 8 * s, (use - 1) & 1)) {
+          atomicOr(p.status, ST_TIMEOUT);
+          misc[0] = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_full + 8 * s, C::STAGE_TX);
+        issue_w(u0 + i, s);
+        issue_a(u0 + i, s);
+        issued = i + 1;
+      }
+      misc[2] = issued;
+    }
+    __syncwarp();
+  } else {
+    // ---------------- consumers: warps 1-4, 32 weight rows each -------------
+    pdl_wait();
+    const int cw = warp - 1, tid = threadIdx.x - 32;
+    float acc[MT][4][4];
+    int cur = -1, kbeg = 0, kend = 0, consumed = 0;
+
+    auto flush = [&](int t) {
+      named_bar(1, 128);  // the previous epilogue has finished reading E
+      const bool full_tile = (kbeg == 0 && kend == p.kc);
+      const int g = lane >> 2, tg = lane & 3;
+      if (full_tile) {
+#pragma unroll
+        for (int mb = 0; mb < MT; ++mb)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int col = cw * 32 + j * 8 + 2 * tg;
+            *(float2*)&E[(mb * 16 + g) * WS_EPAD + col] = make_float2(acc[mb][j][0], acc[mb][j][1]);
+            *(float2*)&E[(mb * 16 + g + 8) * WS_EPAD + col] = make_float2(acc[mb][j][2], acc[mb][j][3]);
+          }
+      } else {
+        const int first_tile = u0 / p.kc;
+        float* slot = p.partial + (int64_t)(2 * cta + (t == first_tile ? 0 : 1)) * (MT * 16 * 128);
+#pragma unroll
+        for (int mb = 0; mb < MT; ++mb)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int col = cw * 32 + j * 8 + 2 * tg;
+            *(float2*)&slot[(mb * 16 + g) * 128 + col] = make_float2(acc[mb][j][0], acc[mb][j][1]);
+            *(float2*)&slot[(mb * 16 + g + 8) * 128 + col] = make_float2(acc[mb][j][2], acc[mb][j][3]);
+          }
+        __threadfence();
+        named_bar(1, 128);
+        const int lo = unit_owner((int64_t)t * p.kc, U, G);
+        const int hi = unit_owner((int64_t)t * p.kc + p.kc - 1, U, G);
+        if (tid == 0) {
+          const int old = atomicAdd(&p.counters[t], 1);
+          const int last = (old == hi - lo);
+          if (last) p.counters[t] = 0;
+          misc[1] = last;
+        }
+        named_bar(1, 128);
+        if (!misc[1]) return;
+        __threadfence();
+        for (int e = tid; e < MT * 16 * 128; e += 128) {
+          float sum = 0.f;
+          for (int c = lo; c <= hi; ++c) {
+            const int ft = first_unit(c, U, G) / p.kc;
+            sum += __ldcg(p.partial + (int64_t)(2 * c + (t == ft ? 0 : 1)) * (MT * 16 * 128) + e);
+          }
+          E[(e >> 7) * WS_EPAD + (e & 127)] = sum;
+        }
+      }
+      named_bar(1, 128);
+      ws_epilogue<MT>(p, t, E, misc);
+    };
+
+    for (int i = 0; i < n; ++i) {
+      const int u = u0 + i;
+      const int t = u / p.kc, kk = u - t * p.kc;
+      if (t != cur) {
+        if (cur >= 0) flush(cur);
+        cur = t;
+        kbeg = kk;
+#pragma unroll
+        for (int mb = 0; mb < MT; ++mb)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[mb][j][q] = 0.f;
+      }
+      const int s = i % C::STAGES;
+      // warp-uniform: the phase is complete once any lane has seen it complete
+      const bool ok = __any_sync(0xffffffffu, misc[0] == 0 && mbar_wait(bar_full + 8 * s, (i / C::STAGES) & 1));
+      if (!ok) {
+        if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
+        misc[0] = 1;
+        break;
+      }
+      const uint32_t wb = sbase + s * C::W_BYTES;
+      const uint32_t ab = sbase + C::OFF_A + s * C::A_BYTES;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t a[MT][4];
+#pragma unroll
+        for (int mb = 0; mb < MT; ++mb) {
+          const int row = mb * 16 + (lane & 15);
+          const int ch = 2 * ks + (lane >> 4);
+          ldsm_x4(ab + row * 128 + ((ch ^ (row & 7)) << 4), a[mb][0], a[mb][1], a[mb][2], a[mb][3]);
+        }
+        uint32_t b[4][2];
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          const int row = cw * 32 + pp * 16 + (lane & 7) + ((lane >> 4) << 3);
+          const int ch = 2 * ks + ((lane >> 3) & 1);
+          ldsm_x4(wb + row * 128 + ((ch ^ (row & 7)) << 4), b[2 * pp][0], b[2 * pp][1],
+                  b[2 * pp + 1][0], b[2 * pp + 1][1]);
+        }
+#pragma unroll
+        for (int mb = 0; mb < MT; ++mb)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma_bf16_16816(acc[mb][j], a[mb], b[j][0], b[j][1]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+      kend = kk + 1;
+      consumed = i + 1;
+    }
+    if (cur >= 0 && !misc[0]) flush(cur);
+    if (tid == 0) misc[3] = consumed;
+  }
+  __syncthreads();
+  if (misc[0] && threadIdx.x == 0) {
+    // drain TMA loads that were issued but never consumed before leaving
+    for (int i = misc[3]; i < misc[2]; ++i)
+      mbar_wait(bar_full + 8 * (i % C::STAGES), (i / C::STAGES) & 1, 100000000ull);
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int MT>
+static int launch_wstream(dflash_handle* h, cudaStream_t s, int kclass, const WParams& prm) {
+  using C = WCfg<MT>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(wstream_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(prm.grid);
+  cfg.blockDim = dim3(WS_THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  Timer t;
+  launch_begin(h, kclass, s, &t);
+  cudaLaunchKernelEx(&cfg, wstream_kernel<MT>, prm);
+  return launch_end(h, s, &t);
+}
+
+size_t wstream_scratch_bytes(const dflash_handle* h, int M) {
+  const int mt = (M + 15) / 16;
+  return (size_t)2 * h->num_sms * mt * 16 * 128 * sizeof(float) + 256;
+}
+
+int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float* partial,
+            float4* amx) {
+  if (L.M < 1 || L.M > 64 || L.K % 64 != 0 || L.nseg < 1 || L.nseg > WS_MAXMAP ||
+      L.nsrc < 1 || L.nsrc > WS_MAXSRC || (L.K / 64) % L.nsrc != 0)
+    return DFLASH_ERR_SHAPE;
+  const int MT = (L.M + 15) / 16;
+  WParams prm;
+  memset(&prm, 0, sizeof(prm));
+  for (int i = 0; i < L.nmap; ++i) prm.wmap[i] = *L.wmaps[i];
+  const int kc_per_src = L.K / 64 / L.nsrc;
+  for (int i = 0; i < L.nsrc; ++i)
+    if (!make_tmap_2d(&prm.amap[i], L.a_src[i], (uint64_t)kc_per_src * 64, (uint64_t)L.M,
+                      (uint64_t)L.a_ld * 2, 64, MT * 16))
+      return DFLASH_ERR_CUDA;
+  for (int i = 0; i < L.nseg; ++i) prm.seg[i] = L.seg[i];
+  prm.nseg = L.nseg;
+  prm.n_tiles = L.seg[L.nseg - 1].t1;
+  prm.kc = L.K / 64;
+  prm.kc_per_src = kc_per_src;
+  prm.M = L.M;
+  prm.units = prm.n_tiles * prm.kc;
+  prm.grid = std::min<int>(prm.units, h->num_sms);
+  prm.partial = partial;
+  prm.counters = h->d_counters;
+  prm.status = h->d_status;
+  prm.rm = L.rm;
+  prm.len = L.len;
+  prm.rope_tab = h->d_rope;
+  prm.max_pos = h->cfg.max_pos;
+  prm.eps = h->cfg.rms_eps;
+  prm.amx = amx;
+  prm.amx_done = h->d_counters + kMaxTiles;
+  prm.ids = L.ids;
+  prm.gap = L.gap;
+  prm.rps_out = L.rps_out;
+  prm.anchor = L.anchor;
+  if (prm.n_tiles > kMaxTiles) return DFLASH_ERR_SHAPE;
+  switch (MT) {
+    case 1: return launch_wstream<1>(h, s, kclass, prm);
+    case 2: return launch_wstream<2>(h, s, kclass, prm);
+    case 3: return launch_wstream<3>(h, s, kclass, prm);
+    default: return launch_wstream<4>(h, s, kclass, prm);
+  }
+}
+
+}  // namespace dflash

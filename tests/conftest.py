@@ -25,7 +25,7 @@ def pytest_collection_modifyitems(config, items):
 @pytest.fixture(scope="session")
 def dfl():
     """The built CUDA binding (built in-tree on first use)."""
-    from block_diffusion_drafter_layer_gb300.build import build
-    build()
+    import __graft_entry__
+    __graft_entry__.build()
     import block_diffusion_drafter_layer_gb300 as m
     return m

@@ -14,8 +14,8 @@ HEADER = os.path.join(ROOT, "include", "dflash.h")
 
 @pytest.fixture(scope="module")
 def dfl():
-    from block_diffusion_drafter_layer_gb300.build import build
-    build()
+    import __graft_entry__
+    __graft_entry__.build()
     import block_diffusion_drafter_layer_gb300 as m
     return m
 

@@ -33,15 +33,48 @@ def _oracle_ctx(kv, lens, seqs, n_layers):
     return K, V
 
 
-def _compare(w, ids, gap, hid, oids, ogap, ohid, label):
-    bad, near, n = id_parity(ids, oids, ogap)
-    print(f"{label}: ids compared {n}, mismatches {bad}, near-ties (<{NEAR_TIE}) {near}")
+def _compare(w, ids, gap, hid, oids, ogap, ohid, label, o32=None):
+    """fp32 path: ids bit-exact outside near-ties (oracle gap < 1e-3), floats
+    within 1e-4 of the oracle.
+
+    bf16 path: after N layers every value carries the rounding noise of the
+    bf16 storage points before it, amplified by each RMSNorm; the oracle run
+    with bf16 storage already differs from the same oracle with fp32 storage
+    by more than 2e-2 in the residual and in the logits.  So (1) ids must be
+    bit-exact at every position whose decision is not precision-sensitive in
+    the oracle itself: gap >= 1e-3 and gap >= 4x the change of that gap
+    between the oracle's bf16- and fp32-storage runs; (2) the GPU's residual
+    and gaps must be as close to the fp32-storage oracle as the bf16-storage
+    oracle is, within 25% plus 2e-2 (max) / 2e-3 (rms)."""
+    if w.dtype == "f32":
+        bad, near, n = id_parity(ids, oids, ogap)
+        print(f"{label}: ids compared {n}, mismatches {bad}, near-ties (<{NEAR_TIE}) {near}")
+        assert bad == 0
+        far = (ogap >= NEAR_TIE) & (np.asarray(ids)[:, 1:] == np.asarray(oids)[:, 1:])
+        e_h, _ = float_parity(hid, ohid, "f32", f"{label} residual")
+        e_g, _ = float_parity(gap[far], ogap[far], "f32", "gap")
+        print(f"{label}: residual max err {e_h:.3e}, gap max err {e_g:.3e}")
+        return
+    hid32, gap32 = o32
+    g, o = np.asarray(ids)[:, 1:], np.asarray(oids)[:, 1:]
+    sens = (ogap < NEAR_TIE) | (ogap < 4 * np.abs(ogap - gap32))
+    near = int((ogap < NEAR_TIE).sum())
+    bad = int(((g != o) & ~sens).sum())
+    print(f"{label}: ids compared {int((~sens).sum())}, mismatches {bad}, near-ties (<{NEAR_TIE}) "
+          f"{near}, precision-sensitive {int(sens.sum())} (of which differing {int(((g != o) & sens).sum())})")
     assert bad == 0
-    e_h, _ = float_parity(hid, ohid, w.dtype, f"{label} residual")
-    # gaps of near-tie rows depend on which of the tied logits won; compare the rest
-    far = ogap >= NEAR_TIE
-    e_g, _ = float_parity(gap[far], ogap[far], "f32" if w.dtype == "f32" else "bf16", "gap")
-    print(f"{label}: residual max err {e_h:.3e}, gap max err {e_g:.3e}")
+    rms = lambda a: float(np.sqrt(np.mean(np.square(a))))
+    e_gpu, e_ora = float(np.abs(hid - hid32).max()), float(np.abs(ohid - hid32).max())
+    r_gpu, r_ora = rms(hid - hid32), rms(ohid - hid32)
+    same = g == o
+    eg_gpu = float(np.abs(gap - gap32)[same].max()) if same.any() else 0.0
+    eg_ora = float(np.abs(ogap - gap32)[same].max()) if same.any() else 0.0
+    print(f"{label}: residual |gpu-fp32 oracle| max {e_gpu:.3e} rms {r_gpu:.3e} vs |bf16-fp32 oracle| "
+          f"max {e_ora:.3e} rms {r_ora:.3e}; gap |gpu-fp32 oracle| {eg_gpu:.3e} vs {eg_ora:.3e}; "
+          f"|gpu-bf16 oracle| residual {float(np.abs(hid - ohid).max()):.3e}")
+    assert np.isfinite(hid).all()
+    assert e_gpu <= 1.25 * e_ora + 2e-2 and r_gpu <= 1.25 * r_ora + 2e-3
+    assert eg_gpu <= 1.25 * eg_ora + 2e-2
 
 
 def test_draft_chain_tiny(dfl):
@@ -97,8 +130,12 @@ def _random_cache_case(dfl, w, B, lens, sample, weights=None):
     cK, cV = _oracle_ctx(kv, lens, sample, s.n_layers)
     oids, ogap, ohid = O.draft_block(s, W, cK, cV, anchors[sample], B, O.storage(w.dtype),
                                      return_hidden=True)
+    o32 = None
+    if w.dtype == "bf16":
+        _, g32, h32 = O.draft_block(s, W, cK, cV, anchors[sample], B, O.f32, return_hidden=True)
+        o32 = (h32, g32)
     _compare(w, ids[sample], gap[sample], hid[sample], oids, ogap, ohid,
-             f"{w.name} B={B} seqs={list(sample)}")
+             f"{w.name} B={B} seqs={list(sample)}", o32)
     m.close()
     return weights
 
@@ -142,21 +179,23 @@ def test_draft_block_size_one(dfl):
     m.close()
 
 
-def test_lm_head_argmax_ties_and_gap(dfl):
+@pytest.mark.parametrize("wname", ["tiny_f32", "qwen3_8b_b1"])
+def test_lm_head_argmax_ties_and_gap(dfl, wname):
     """Duplicate LM-head rows make exact logit ties: the lowest index wins
-    and the gap is zero; elsewhere ids and gaps match the oracle."""
+    (33 and 700 sit in different 128-row vocabulary tiles, 900 and 901 in
+    the same one) and the gap is zero; elsewhere ids and gaps match."""
     from synth.gpu import draft_model
-    w = synth.WORKLOADS["tiny_f32"]
+    w = synth.WORKLOADS[wname]
     s = w.draft
     weights = synth.draft_weights(s, w.dtype, w.seed, device="cuda")
     rows = 6
     x = torch.randn(rows, s.D, generator=torch.Generator().manual_seed(3)).cuda()
     hf = x / torch.sqrt((x * x).mean(1, keepdim=True) + s.eps)
     lm = weights["lm_head"]
-    lm[700] = hf[0] * 0.5
-    lm[33] = hf[0] * 0.5                    # same row twice: exact tie, 33 < 700
-    lm[900] = hf[1] * 0.5
-    lm[901] = hf[1] * 0.5
+    lm[700] = (hf[0] * 0.5).to(lm.dtype)
+    lm[33] = (hf[0] * 0.5).to(lm.dtype)    # same row twice: exact tie, 33 < 700
+    lm[900] = (hf[1] * 0.5).to(lm.dtype)
+    lm[901] = (hf[1] * 0.5).to(lm.dtype)
     m = draft_model(s, w.dtype, weights, max_pos=64)
     ids = torch.empty(rows, dtype=torch.int32, device="cuda")
     gap = torch.empty(rows, device="cuda")
@@ -164,7 +203,10 @@ def test_lm_head_argmax_ties_and_gap(dfl):
     torch.cuda.synchronize()
     ids, gap = ids.cpu().numpy(), gap.cpu().numpy()
     assert ids[0] == 33 and ids[1] == 900 and gap[0] == 0 and gap[1] == 0
-    z = O.lm_head_logits(O.f32(O.rmsnorm(x.cpu().numpy(), np.ones(s.D), s.eps)), to_np(lm))
-    np.testing.assert_array_equal(ids[2:], O.argmax_lowest(z)[2:])
-    np.testing.assert_allclose(gap, O.top2_gap(z), atol=1e-4)
+    st = O.storage(w.dtype)
+    z = O.lm_head_logits(st(O.rmsnorm(x.cpu().numpy(), np.ones(s.D), s.eps)), to_np(lm))
+    og = O.top2_gap(z)
+    far = og >= NEAR_TIE
+    np.testing.assert_array_equal(ids[2:][far[2:]], O.argmax_lowest(z)[2:][far[2:]])
+    np.testing.assert_allclose(gap, og, atol=1e-4 if w.dtype == "f32" else 2e-3)
     m.close()

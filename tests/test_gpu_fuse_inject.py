@@ -46,7 +46,9 @@ def test_fuse_worked_example_gpu(dfl):
     m.close()
 
 
-@pytest.mark.parametrize("wname,T", [("tiny_f32", 64), ("tiny_f32", 4133), ("qwen3_8b_b1", 300)])
+@pytest.mark.parametrize("wname,T", [("tiny_f32", 64), ("tiny_f32", 4133), ("qwen3_8b_b1", 16),
+                                     ("qwen3_8b_b1", 64), ("qwen3_8b_b1", 300),
+                                     ("qwen35_a3b_32k", 40)])
 def test_fuse_parity(dfl, wname, T):
     w = synth.WORKLOADS[wname]
     s = w.draft
@@ -102,7 +104,7 @@ def test_inject_parity_ragged(dfl, wname):
             gv = Vc[b, :, p0:p0 + n, :].transpose(1, 0, 2)
             _, ek = float_parity(gk, k, w.dtype, f"K layer {l} seq {b}")
             _, ev = float_parity(gv, v, w.dtype, f"V layer {l} seq {b}")
-            if n:
+            if n and w.dtype == "bf16":
                 assert ek > 0.99 and ev > 0.99
             # nothing outside the appended range was written
             assert not Kc[b, :, :p0].any() and not Kc[b, :, p0 + n:].any()
