@@ -146,7 +146,7 @@ class Draft:
         cap = self.L_max + 2 * self.B + 8
         self.model = draft_model(s, w.dtype, self.weights, max_pos=cap + 8)
         self.kv = kv_cache(s, self.batch, cap, w.dtype)
-        self.ws = self.model.workspace(rows)
+        self.ws = self.model.workspace(rows, max_batch=self.batch, max_block=self.B)
         # prefill context: fuse + inject every sequence's L_b rows
         self.T_pre = sum(self.lens)
         self.pre_hidden = synth.target_hidden_states(self.T_pre, s.D, s.n_pick, w.dtype, seed,

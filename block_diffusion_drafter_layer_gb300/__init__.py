@@ -66,7 +66,7 @@ _P = C.c_void_p
 _sig = {
     "dflash_create": (C.c_int, [C.POINTER(dflash_config), C.POINTER(dflash_weights), C.POINTER(_P)]),
     "dflash_destroy": (C.c_int, [_P]),
-    "dflash_workspace_bytes": (C.c_size_t, [_P, C.c_int64]),
+    "dflash_workspace_bytes": (C.c_size_t, [_P, C.c_int32, C.c_int32, C.c_int64]),
     "dflash_build_target_layer_ids": (C.c_int, [C.c_int32, C.c_int32, C.POINTER(C.c_int32)]),
     "dflash_fuse_context": (C.c_int, [_P, C.POINTER(_P), C.c_int64, _P, _P, C.c_size_t, _P]),
     "dflash_inject_kv": (C.c_int, [_P, _P, C.c_int64, _P, _P, C.c_int32, C.POINTER(dflash_kv),
@@ -138,8 +138,8 @@ def dflash_destroy(h: int):
     _check(_lib.dflash_destroy(h), "dflash_destroy")
 
 
-def dflash_workspace_bytes(h: int, max_rows: int) -> int:
-    return int(_lib.dflash_workspace_bytes(h, max_rows))
+def dflash_workspace_bytes(h: int, max_batch: int, max_block: int, max_rows: int) -> int:
+    return int(_lib.dflash_workspace_bytes(h, max_batch, max_block, max_rows))
 
 
 def dflash_fuse_context(h: int, hidden: Sequence[torch.Tensor], T: int, h_t_out: torch.Tensor,
@@ -238,8 +238,13 @@ class Model:
         self.dtype = dtype
         self.handle = dflash_create(cfg, w)
 
-    def workspace(self, max_rows: int, device="cuda") -> torch.Tensor:
-        n = dflash_workspace_bytes(self.handle, max_rows)
+    def workspace(self, max_rows: int, device="cuda", max_batch: int = 0,
+                  max_block: int = 0) -> torch.Tensor:
+        """Workspace for calls of up to max_rows rows and draft blocks of up to
+        max_batch x max_block rows (default: one sequence of max_rows rows)."""
+        if max_batch == 0:
+            max_batch, max_block = 1, max_rows
+        n = dflash_workspace_bytes(self.handle, max_batch, max_block, max_rows)
         return torch.empty(n, dtype=torch.uint8, device=device)
 
     def close(self):

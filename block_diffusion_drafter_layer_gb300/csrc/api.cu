@@ -58,7 +58,7 @@ static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 // Scratch of the weight-streaming kernel: two fp32 partial tiles per CTA and
 // one top-2 record per (vocabulary tile, row).
 static size_t ws_partial_bytes(const dflash_handle* h) {
-  return round256((size_t)2 * std::max(h->num_sms, 1) * 64 * 128 * sizeof(float));
+  return round256(wstream_scratch_bytes(h, 64));
 }
 static size_t ws_amx_bytes(const dflash_handle* h) {
   return round256((size_t)((h->cfg.vocab + 127) / 128) * 64 * sizeof(float4));
@@ -91,18 +91,20 @@ static size_t chunk_row_bytes(const dflash_config& c) {
 }
 
 struct Fwd {
-  float *x, *qf, *kf, *vf, *gf, *uf, *logits, *partial;
+  float *x, *qf, *kf, *vf, *gf, *uf, *logits, *partial, *attn;
   float4* amx;
   void *h, *q, *kb, *vb, *o, *hf, *a;
 };
 
-static bool carve_forward(const dflash_handle* h, int64_t R, void* ws, size_t ws_bytes, Fwd* f) {
+static bool carve_forward(const dflash_handle* h, int64_t R, void* ws, size_t ws_bytes, Fwd* f,
+                          int batch = 0, int B = 0) {
   const dflash_config& c = h->cfg;
   const size_t sz = esize(c.dtype);
   const int64_t D = c.hidden, Hd = (int64_t)c.n_heads * c.head_dim,
                 Gd = (int64_t)c.n_kv_heads * c.head_dim, F = c.ffn, V = c.vocab;
   Carve cv{(char*)ws, ws_bytes};
   f->partial = cv.take<float>(ws_partial_bytes(h) / sizeof(float));
+  f->attn = batch > 0 ? cv.take<float>(attn_scratch_bytes(h, batch, B) / sizeof(float)) : nullptr;
   f->amx = cv.take<float4>(ws_amx_bytes(h) / sizeof(float4));
   f->a = cv.take<char>(R * F * sz);
   f->x = cv.take<float>(R * D);
@@ -446,11 +448,14 @@ int dflash_destroy(dflash_handle* h) {
   return DFLASH_OK;
 }
 
-size_t dflash_workspace_bytes(const dflash_handle* h, int64_t max_rows) {
-  if (!h || max_rows < 0) return 0;
-  const int64_t R = std::max<int64_t>(max_rows, 1);
+size_t dflash_workspace_bytes(const dflash_handle* h, int32_t max_batch, int32_t max_block,
+                              int64_t max_rows) {
+  if (!h || max_batch < 0 || max_block < 0 || max_rows < 0) return 0;
+  const int64_t R = std::max<int64_t>({(int64_t)max_batch * max_block, max_rows, 1});
   // a forward pass over R rows, or fuse / inject in full kChunkRows passes
-  const size_t scratch = ws_partial_bytes(h) + ws_amx_bytes(h) + 512;
+  const size_t scratch = ws_partial_bytes(h) + ws_amx_bytes(h) + 1024 +
+                         (max_batch > 0 && max_block > 0
+                              ? attn_scratch_bytes(h, max_batch, max_block) : 0);
   const size_t fwd = forward_bytes(h->cfg, R);
   const size_t chunk = round256(kChunkRows * chunk_row_bytes(h->cfg)) + 1024;
   return std::max(fwd, chunk) + scratch;
@@ -595,7 +600,7 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
   const int Hd = H * d, Gd = G * d;
   const int64_t R = (int64_t)batch * B;
   Fwd f;
-  if (!carve_forward(h, R, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
+  if (!carve_forward(h, R, ws, ws_bytes, &f, batch, B)) return DFLASH_ERR_WORKSPACE;
   int rc;
   if ((rc = embed_block(h, s, dt, h->w.embed, anchor, c.mask_token_id, batch, B, c.vocab, D,
                         c.embed_scale, f.x)))
@@ -608,9 +613,13 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
       return rc;
     if (stream) {
       if ((rc = qkv_stream(h, s, l, f, R, rm, kv->len))) return rc;
-      if ((rc = attention(h, s, dt, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch,
-                          B, H, G, d, false, f.o)))
-        return rc;
+      if (attn_fast_ok(h, B))
+        rc = attention_fast(h, s, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch, B,
+                            f.o, f.attn);
+      else
+        rc = attention(h, s, dt, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch, B,
+                       H, G, d, false, f.o);
+      if (rc) return rc;
       if ((rc = mlp_stream(h, s, l, f, R))) return rc;
       continue;
     }

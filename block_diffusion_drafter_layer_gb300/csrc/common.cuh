@@ -193,6 +193,14 @@ size_t wstream_scratch_bytes(const dflash_handle* h, int M);
 int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float* partial,
             float4* amx);
 
+// ---- split-K attention of the draft block (k_attention.cu) ------------------
+int attn_split_keys(const dflash_handle* h, int batch, int B, int cap);
+size_t attn_scratch_bytes(const dflash_handle* h, int batch, int B);
+bool attn_fast_ok(const dflash_handle* h, int B);
+int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* kc, const void* vc,
+                   int cap, const int32_t* len, const void* kb, const void* vb, int batch, int B,
+                   void* o, float* scratch);
+
 // ---- kernel launchers (one translation unit each) --------------------------
 // A operand source: up to DFLASH_MAX_PICK column segments of width seg
 // (column k of row m is seg_ptr[k / seg][m * ld + k % seg]).

@@ -42,11 +42,16 @@ __global__ void embed_tokens_kernel(const T* __restrict__ E, const int32_t* __re
 // out[r] = in[r'] / sqrt(mean(in[r']^2) + eps) * g, fp32 arithmetic.
 // skip_first_of > 1 maps output row r to input row r' that skips the first
 // row of every group of skip_first_of rows (the anchor rows of a block).
+// Each thread first loads all of its elements (up to RN_CACHE) into registers
+// so the loads are in flight together, then reduces, then writes.
+constexpr int RN_CACHE = 32;
 template <typename TI, typename TO>
-__global__ void rmsnorm_kernel(const TI* __restrict__ in, int64_t ld_in, TO* __restrict__ out,
-                               int64_t ld_out, const float* __restrict__ g, int D, float eps,
-                               int skip_first_of) {
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const TI* __restrict__ in, int64_t ld_in,
+                                                      TO* __restrict__ out, int64_t ld_out,
+                                                      const float* __restrict__ g, int D, float eps,
+                                                      int skip_first_of) {
   __shared__ float red[33];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int64_t r = blockIdx.x;
   int64_t ri = r;
   if (skip_first_of > 1) {
@@ -54,15 +59,29 @@ __global__ void rmsnorm_kernel(const TI* __restrict__ in, int64_t ld_in, TO* __r
     ri = (r / per) * skip_first_of + (r % per) + 1;
   }
   const TI* src = in + ri * ld_in;
+  float v[RN_CACHE];
   float ss = 0.f;
-  for (int k = threadIdx.x; k < D; k += blockDim.x) {
-    const float v = to_f(src[k]);
-    ss += v * v;
+#pragma unroll
+  for (int q = 0; q < RN_CACHE; ++q) {
+    const int k = threadIdx.x + q * blockDim.x;
+    v[q] = (k < D) ? to_f(src[k]) : 0.f;
+  }
+#pragma unroll
+  for (int q = 0; q < RN_CACHE; ++q) ss += v[q] * v[q];
+  for (int k = threadIdx.x + RN_CACHE * blockDim.x; k < D; k += blockDim.x) {
+    const float x = to_f(src[k]);
+    ss += x * x;
   }
   ss = block_sum(ss, red);
   const float rinv = 1.0f / sqrtf(ss / (float)D + eps);
   TO* dst = out + r * ld_out;
-  for (int k = threadIdx.x; k < D; k += blockDim.x) dst[k] = from_f<TO>(to_f(src[k]) * rinv * g[k]);
+#pragma unroll
+  for (int q = 0; q < RN_CACHE; ++q) {
+    const int k = threadIdx.x + q * blockDim.x;
+    if (k < D) dst[k] = from_f<TO>(v[q] * rinv * g[k]);
+  }
+  for (int k = threadIdx.x + RN_CACHE * blockDim.x; k < D; k += blockDim.x)
+    dst[k] = from_f<TO>(to_f(src[k]) * rinv * g[k]);
 }
 
 // One warp per (row, head): optional per-head RMSNorm, optional RoPE with

@@ -7,8 +7,8 @@
 //     every CTA (one per SM) an equal contiguous run of (tile, k-chunk)
 //     units, so all SMs stream the same number of bytes whatever the shape;
 //   * stages weight and activation chunks with TMA into an 8-deep
-//     shared-memory ring guarded by mbarriers (warp 0 produces, warps 1-4
-//     consume), prefetching the first weight chunks before waiting for the
+//     shared-memory ring guarded by mbarriers (warp 0 produces, warps 1-8
+//     consume: 4 weight-row quarters x 2 k-halves), prefetching the first weight chunks before waiting for the
 //     previous kernel (programmatic dependent launch);
 //   * multiplies with warp-level bf16 MMA (m16n8k16, fp32 accumulate);
 //   * combines the k-split partial sums of a tile in a fixed order in the
@@ -24,7 +24,20 @@ namespace dflash {
 
 using namespace ptx;
 
-constexpr int WS_THREADS = 160;
+// Consumer layout: 4 weight-row quarters x WS_KSPLIT slices of each 64-wide
+// k-chunk (compile-time tuning), plus one producer warp whose first
+// WS_NPROD lanes each issue every WS_NPROD-th stage.
+#ifndef DFLASH_WS_KSPLIT
+#define DFLASH_WS_KSPLIT 1
+#endif
+#ifndef DFLASH_WS_NPROD
+#define DFLASH_WS_NPROD 1
+#endif
+constexpr int WS_KSPLIT = DFLASH_WS_KSPLIT;
+constexpr int WS_NPROD = DFLASH_WS_NPROD;
+constexpr int WS_CW = 4 * WS_KSPLIT;
+constexpr int WS_CT = WS_CW * 32;
+constexpr int WS_THREADS = 32 + WS_CT;
 constexpr int WS_EPAD = 132;
 
 struct WParams {
@@ -50,18 +63,32 @@ struct WParams {
 
 static_assert(sizeof(WParams) <= 4096, "kernel parameters must fit the 4 KB limit");
 
+// Ring depth and resident CTAs per SM (compile-time tuning; shared memory per
+// CTA must fit 227 KB / WS_MINBLOCKS).
+#ifndef DFLASH_WS_STAGES
+#define DFLASH_WS_STAGES 8
+#endif
+#ifndef DFLASH_WS_MINBLOCKS
+#define DFLASH_WS_MINBLOCKS 2
+#endif
+
 template <int MT>
 struct WCfg {
-  static constexpr int STAGES = MT >= 4 ? 7 : 8;
   static constexpr int W_BYTES = 128 * 64 * 2;
   static constexpr int A_BYTES = MT * 16 * 64 * 2;
   static constexpr int STAGE_TX = W_BYTES + A_BYTES;
+  // deepest ring that fits the shared memory of one of WS_MINBLOCKS CTAs per SM
+  static constexpr int BUDGET = DFLASH_WS_MINBLOCKS == 1 ? 232448 : 233472 / DFLASH_WS_MINBLOCKS - 1024;
+  static constexpr int FIXED = MT * 16 * WS_EPAD * 4 + 2 * 16 * 8 + 64 + 64 * 8 + 1024;
+  static constexpr int FIT = (BUDGET - FIXED) / STAGE_TX;
+  static constexpr int STAGES = FIT < DFLASH_WS_STAGES ? FIT : DFLASH_WS_STAGES;
+  static_assert(STAGES >= 2, "ring too shallow");
   static constexpr int OFF_A = STAGES * W_BYTES;
   static constexpr int OFF_E = OFF_A + STAGES * A_BYTES;
   static constexpr int E_FLOATS = MT * 16 * WS_EPAD;
   static constexpr int OFF_BAR = OFF_E + E_FLOATS * 4;
   static constexpr int OFF_MISC = OFF_BAR + 2 * STAGES * 8;
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;
+  static constexpr int SMEM = OFF_MISC + 64 + 64 * 8 + 1024;
 };
 
 __device__ __forceinline__ int seg_of(const WParams& p, int t) {
@@ -109,24 +136,36 @@ __device__ __forceinline__ Top2 top2_warp(Top2 t) {
 
 // ---- epilogues (128 consumer threads, final fp32 tile in E) ------------------
 template <int MT>
-__device__ void ws_epilogue(const WParams& p, int t, const float* E, volatile int* misc) {
+__device__ void ws_epilogue(const WParams& p, int t, const float* E, volatile int* misc,
+                            const int* rowpos) {
   const int tid = threadIdx.x - 32, cw = tid >> 5, lane = threadIdx.x & 31;
   const WSeg& g = p.seg[seg_of(p, t)];
   const int lt = t - g.t0;
   const int M = p.M;
   if (g.kind == SK_F32 || g.kind == SK_RESID) {
+    // float4 per thread-iteration; the residual loads of all iterations are
+    // issued before any is used (n_valid and ld are multiples of 4 here)
     float* dst = (float*)g.dst;
-    for (int e = tid; e < M * 128; e += 128) {
-      const int r = e >> 7, c = e & 127;
-      const int n = lt * 128 + c;
-      if (n >= g.n_valid) continue;
-      float* o = dst + (int64_t)r * g.ld + n;
-      const float v = E[r * WS_EPAD + c];
-      *o = (g.kind == SK_RESID) ? (*o + v) : v;
+    constexpr int IT = MT * 512 / WS_CT;  // (MT*16 rows * 32 float4) / consumer threads
+    float4 old[IT];
+#pragma unroll
+    for (int q = 0; q < IT; ++q) {
+      const int e = tid + q * WS_CT, r = e >> 5, c = (e & 31) * 4, n = lt * 128 + c;
+      old[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g.kind == SK_RESID && r < M && n < g.n_valid)
+        old[q] = *(const float4*)(dst + (int64_t)r * g.ld + n);
+    }
+#pragma unroll
+    for (int q = 0; q < IT; ++q) {
+      const int e = tid + q * WS_CT, r = e >> 5, c = (e & 31) * 4, n = lt * 128 + c;
+      if (r >= M || n >= g.n_valid) continue;
+      const float* ev = E + r * WS_EPAD + c;
+      *(float4*)(dst + (int64_t)r * g.ld + n) =
+          make_float4(old[q].x + ev[0], old[q].y + ev[1], old[q].z + ev[2], old[q].w + ev[3]);
     }
   } else if (g.kind == SK_SWIGLU) {
     bf16* dst = (bf16*)g.dst;
-    for (int e = tid; e < M * 64; e += 128) {
+    for (int e = tid; e < M * 64; e += WS_CT) {
       const int r = e >> 6, c = e & 63;
       const int f = lt * 64 + c;
       if (f >= g.n_valid) continue;
@@ -135,9 +174,25 @@ __device__ void ws_epilogue(const WParams& p, int t, const float* E, volatile in
     }
   } else if (g.kind == SK_HEAD) {
     const int d = g.d, half = d >> 1, P = half >> 5, hpt = 128 / d;
-    for (int pi = cw; pi < M * hpt; pi += 4) {
+    float gn1[2] = {1.f, 1.f}, gn2[2] = {1.f, 1.f};
+    if (g.gain != nullptr) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        if (q < P) {
+          gn1[q] = g.gain[lane + 32 * q];
+          gn2[q] = g.gain[lane + 32 * q + half];
+        }
+    }
+    for (int pi = cw; pi < M * hpt; pi += WS_CW) {
       const int r = pi / hpt, j = pi - r * hpt;
       const int head = lt * hpt + j;
+      const int pb = rowpos[2 * r], pos = rowpos[2 * r + 1];   // sequence, position (-1: skip)
+      float2 cs[2] = {make_float2(1.f, 0.f), make_float2(1.f, 0.f)};
+      if (g.rope && pos >= 0 && pos < p.max_pos) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (q < P) cs[q] = p.rope_tab[(int64_t)pos * half + lane + 32 * q];
+      }
       const float* src = E + r * WS_EPAD + j * d;
       float x1[2], x2[2], ss = 0.f;
 #pragma unroll
@@ -154,14 +209,12 @@ __device__ void ws_epilogue(const WParams& p, int t, const float* E, volatile in
 #pragma unroll
         for (int q = 0; q < 2; ++q)
           if (q < P) {
-            const int jj = lane + 32 * q;
-            x1[q] = x1[q] * rinv * g.gain[jj];
-            x2[q] = x2[q] * rinv * g.gain[jj + half];
+            x1[q] = x1[q] * rinv * gn1[q];
+            x2[q] = x2[q] * rinv * gn2[q];
           }
       }
-      int b, i;
-      if (!p.rm.map(r, b, i)) continue;
-      const int pos = p.len[b] + i;
+      if (pb < 0) continue;                  // row not appended by this call
+      const int b = pb;
       if (g.rope) {
         if (pos < 0 || pos >= p.max_pos) {
           if (lane == 0) atomicOr(p.status, ST_BOUNDS);
@@ -170,10 +223,8 @@ __device__ void ws_epilogue(const WParams& p, int t, const float* E, volatile in
 #pragma unroll
         for (int q = 0; q < 2; ++q)
           if (q < P) {
-            const int jj = lane + 32 * q;
-            const float2 cs = p.rope_tab[(int64_t)pos * half + jj];
-            const float y1 = x1[q] * cs.x - x2[q] * cs.y;
-            const float y2 = x2[q] * cs.x + x1[q] * cs.y;
+            const float y1 = x1[q] * cs[q].x - x2[q] * cs[q].y;
+            const float y2 = x2[q] * cs[q].x + x1[q] * cs[q].y;
             x1[q] = y1;
             x2[q] = y2;
           }
@@ -197,7 +248,7 @@ __device__ void ws_epilogue(const WParams& p, int t, const float* E, volatile in
         }
     }
   } else if (g.kind == SK_ARGMAX) {
-    for (int r = cw; r < M; r += 4) {
+    for (int r = cw; r < M; r += WS_CW) {
       Top2 tt{-INFINITY, 0x7fffffff, -INFINITY};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -212,22 +263,31 @@ __device__ void ws_epilogue(const WParams& p, int t, const float* E, volatile in
       if (lane == 0) p.amx[(int64_t)t * M + r] = make_float4(tt.t1, __int_as_float(tt.i1), tt.t2, 0.f);
     }
     __threadfence();
-    named_bar(1, 128);
+    named_bar(1, WS_CT);
     if (tid == 0) {
       const int old = atomicAdd(p.amx_done, 1);
       const int last = (old == p.n_tiles - 1);
       if (last) *p.amx_done = 0;
       misc[1] = last;
     }
-    named_bar(1, 128);
+    named_bar(1, WS_CT);
     if (!misc[1]) return;
     __threadfence();
-    for (int r = cw; r < M; r += 4) {
+    for (int r = cw; r < M; r += WS_CW) {
       Top2 tt{-INFINITY, 0x7fffffff, -INFINITY};
-      for (int tt_i = lane; tt_i < p.n_tiles; tt_i += 32) {
-        const float4 rec = __ldcg(&p.amx[(int64_t)tt_i * M + r]);
-        Top2 u{rec.x, __float_as_int(rec.y), rec.z};
-        tt = top2_merge(tt, u);
+      for (int t0 = 0; t0 < p.n_tiles; t0 += 32 * 8) {
+        float4 rec[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int ti = t0 + lane + 32 * q;
+          rec[q] = ti < p.n_tiles ? __ldcg(&p.amx[(int64_t)ti * M + r])
+                                  : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          Top2 u{rec[q].x, __float_as_int(rec[q].y), rec[q].z};
+          tt = top2_merge(tt, u);
+        }
       }
       tt = top2_warp(tt);
       if (lane == 0) {
@@ -247,7 +307,7 @@ __device__ void ws_epilogue(const WParams& p, int t, const float* E, volatile in
 }
 
 template <int MT>
-__global__ void __launch_bounds__(WS_THREADS, 1) wstream_kernel(const __grid_constant__ WParams p) {
+__global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kernel(const __grid_constant__ WParams p) {
   using C = WCfg<MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -264,7 +324,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1) wstream_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 4);
+      mbar_init(bar_empty + 8 * s, WS_CW);
     }
     misc[0] = misc[1] = misc[2] = misc[3] = 0;
     fence_barrier_init();
@@ -273,8 +333,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1) wstream_kernel(const __grid_con
   if (threadIdx.x == 0) pdl_launch_dependents();
 
   if (warp == 0) {
-    // ---------------- producer: one lane issues every TMA load ----------------
-    if (lane == 0) {
+    // ---------------- producer: lanes < WS_NPROD issue the TMA loads ---------
+    if (lane < WS_NPROD) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
       auto issue_w = [&](int u, int s) {
         const int t = u / p.kc, kk = u - t * p.kc;
@@ -295,14 +355,14 @@ __global__ void __launch_bounds__(WS_THREADS, 1) wstream_kernel(const __grid_con
                     pol_a);
       };
       const int pre = n < C::STAGES ? n : C::STAGES;
-      for (int i = 0; i < pre; ++i) {
+      for (int i = lane; i < pre; i += WS_NPROD) {
         mbar_arrive_expect_tx(bar_full + 8 * i, C::STAGE_TX);
         issue_w(u0 + i, i);
       }
       pdl_wait();
-      for (int i = 0; i < pre; ++i) issue_a(u0 + i, i);
+      for (int i = lane; i < pre; i += WS_NPROD) issue_a(u0 + i, i);
       int issued = pre;
-      for (int i = pre; i < n; ++i) {
+      for (int i = pre + lane; i < n; i += WS_NPROD) {
         const int s = i % C::STAGES, use = i / C::STAGES;
         if (misc[0]) break;
         if (!mbar_wait(bar_empty + 8 * s, (use - 1) & 1)) {
@@ -315,42 +375,66 @@ __global__ void __launch_bounds__(WS_THREADS, 1) wstream_kernel(const __grid_con
         issue_a(u0 + i, s);
         issued = i + 1;
       }
-      misc[2] = issued;
+      atomicMax((int*)&misc[2], issued);   // highest stage index issued, for the drain
     }
     __syncwarp();
   } else {
     // ---------------- consumers: warps 1-4, 32 weight rows each -------------
     pdl_wait();
     const int cw = warp - 1, tid = threadIdx.x - 32;
+    const int nq = cw & 3, kh = cw >> 2;   // weight-row quarter, k-slice of each chunk
+    // sequence and cache position of each activation row (head epilogues)
+    int* rowpos = (int*)(smem + C::OFF_MISC + 64);
+    if (tid < MT * 16) {
+      int b = -1, i = 0, pos = -1;
+      if (tid < p.M && p.len != nullptr && p.rm.map(tid, b, i)) pos = p.len[b] + i;
+      else b = -1;
+      rowpos[2 * tid] = b;
+      rowpos[2 * tid + 1] = pos;
+    }
+    named_bar(1, WS_CT);
     float acc[MT][4][4];
     int cur = -1, kbeg = 0, kend = 0, consumed = 0;
 
     auto flush = [&](int t) {
-      named_bar(1, 128);  // the previous epilogue has finished reading E
+      named_bar(1, WS_CT);  // the previous epilogue has finished reading E
       const bool full_tile = (kbeg == 0 && kend == p.kc);
       const int g = lane >> 2, tg = lane & 3;
-      if (full_tile) {
+      // the two k-halves of the tile meet in E in a fixed order: half 0 stores,
+      // half 1 adds
 #pragma unroll
-        for (int mb = 0; mb < MT; ++mb)
+      for (int half = 0; half < WS_KSPLIT; ++half) {
+        if (kh == half) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int col = cw * 32 + j * 8 + 2 * tg;
-            *(float2*)&E[(mb * 16 + g) * WS_EPAD + col] = make_float2(acc[mb][j][0], acc[mb][j][1]);
-            *(float2*)&E[(mb * 16 + g + 8) * WS_EPAD + col] = make_float2(acc[mb][j][2], acc[mb][j][3]);
-          }
-      } else {
+          for (int mb = 0; mb < MT; ++mb)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int col = nq * 32 + j * 8 + 2 * tg;
+              float2* e0 = (float2*)&E[(mb * 16 + g) * WS_EPAD + col];
+              float2* e1 = (float2*)&E[(mb * 16 + g + 8) * WS_EPAD + col];
+              if (half == 0) {
+                *e0 = make_float2(acc[mb][j][0], acc[mb][j][1]);
+                *e1 = make_float2(acc[mb][j][2], acc[mb][j][3]);
+              } else {
+                const float2 a0 = *e0, a1 = *e1;
+                *e0 = make_float2(a0.x + acc[mb][j][0], a0.y + acc[mb][j][1]);
+                *e1 = make_float2(a1.x + acc[mb][j][2], a1.y + acc[mb][j][3]);
+              }
+            }
+        }
+        named_bar(1, WS_CT);
+      }
+      if (!full_tile) {
+        constexpr int IT = MT * 512 / WS_CT;   // float4s of a tile per consumer thread
         const int first_tile = u0 / p.kc;
-        float* slot = p.partial + (int64_t)(2 * cta + (t == first_tile ? 0 : 1)) * (MT * 16 * 128);
+        float4* slot = (float4*)(p.partial + (int64_t)(2 * cta + (t == first_tile ? 0 : 1)) * (MT * 16 * 128));
 #pragma unroll
-        for (int mb = 0; mb < MT; ++mb)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int col = cw * 32 + j * 8 + 2 * tg;
-            *(float2*)&slot[(mb * 16 + g) * 128 + col] = make_float2(acc[mb][j][0], acc[mb][j][1]);
-            *(float2*)&slot[(mb * 16 + g + 8) * 128 + col] = make_float2(acc[mb][j][2], acc[mb][j][3]);
-          }
+        for (int q = 0; q < IT; ++q) {
+          const int e4 = tid + q * WS_CT, e = e4 * 4;
+          slot[e4] = *(const float4*)&E[(e >> 7) * WS_EPAD + (e & 127)];
+        }
         __threadfence();
-        named_bar(1, 128);
+        named_bar(1, WS_CT);
         const int lo = unit_owner((int64_t)t * p.kc, U, G);
         const int hi = unit_owner((int64_t)t * p.kc + p.kc - 1, U, G);
         if (tid == 0) {
@@ -359,20 +443,45 @@ __global__ void __launch_bounds__(WS_THREADS, 1) wstream_kernel(const __grid_con
           if (last) p.counters[t] = 0;
           misc[1] = last;
         }
-        named_bar(1, 128);
+        named_bar(1, WS_CT);
         if (!misc[1]) return;
         __threadfence();
-        for (int e = tid; e < MT * 16 * 128; e += 128) {
-          float sum = 0.f;
-          for (int c = lo; c <= hi; ++c) {
+        // sum the contributors' partial tiles in CTA (= k) order; the loads of
+        // up to 8 contributors x all of a thread's float4s are issued first
+        float4 sum[IT];
+#pragma unroll
+        for (int q = 0; q < IT; ++q) sum[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = lo; c0 <= hi; c0 += 8) {
+          const float4* src[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int c = min(c0 + k, hi);
             const int ft = first_unit(c, U, G) / p.kc;
-            sum += __ldcg(p.partial + (int64_t)(2 * c + (t == ft ? 0 : 1)) * (MT * 16 * 128) + e);
+            src[k] = (const float4*)(p.partial + (int64_t)(2 * c + (t == ft ? 0 : 1)) * (MT * 16 * 128));
           }
-          E[(e >> 7) * WS_EPAD + (e & 127)] = sum;
+#pragma unroll
+          for (int q = 0; q < IT; ++q) {
+            float4 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __ldcg(src[k] + tid + q * WS_CT);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (c0 + k <= hi) {
+                sum[q].x += v[k].x;
+                sum[q].y += v[k].y;
+                sum[q].z += v[k].z;
+                sum[q].w += v[k].w;
+              }
+          }
         }
+#pragma unroll
+        for (int q = 0; q < IT; ++q) {
+          const int e = (tid + q * WS_CT) * 4;
+          *(float4*)&E[(e >> 7) * WS_EPAD + (e & 127)] = sum[q];
+        }
+        named_bar(1, WS_CT);
       }
-      named_bar(1, 128);
-      ws_epilogue<MT>(p, t, E, misc);
+      ws_epilogue<MT>(p, t, E, misc, rowpos);
     };
 
     for (int i = 0; i < n; ++i) {
@@ -400,7 +509,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1) wstream_kernel(const __grid_con
       const uint32_t wb = sbase + s * C::W_BYTES;
       const uint32_t ab = sbase + C::OFF_A + s * C::A_BYTES;
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
+      for (int kk = 0; kk < 4 / WS_KSPLIT; ++kk) {
+        const int ks = (4 / WS_KSPLIT) * kh + kk;
         uint32_t a[MT][4];
 #pragma unroll
         for (int mb = 0; mb < MT; ++mb) {
@@ -411,7 +521,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1) wstream_kernel(const __grid_con
         uint32_t b[4][2];
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
-          const int row = cw * 32 + pp * 16 + (lane & 7) + ((lane >> 4) << 3);
+          const int row = nq * 32 + pp * 16 + (lane & 7) + ((lane >> 4) << 3);
           const int ch = 2 * ks + ((lane >> 3) & 1);
           ldsm_x4(wb + row * 128 + ((ch ^ (row & 7)) << 4), b[2 * pp][0], b[2 * pp][1],
                   b[2 * pp + 1][0], b[2 * pp + 1][1]);
@@ -431,9 +541,11 @@ __global__ void __launch_bounds__(WS_THREADS, 1) wstream_kernel(const __grid_con
   }
   __syncthreads();
   if (misc[0] && threadIdx.x == 0) {
-    // drain TMA loads that were issued but never consumed before leaving
-    for (int i = misc[3]; i < misc[2]; ++i)
-      mbar_wait(bar_full + 8 * (i % C::STAGES), (i / C::STAGES) & 1, 100000000ull);
+    // drain TMA loads that were issued but never consumed before leaving (at
+    // most one ring's worth; each wait is bounded)
+    const int hi = min(misc[2], misc[3] + C::STAGES);
+    for (int i = misc[3]; i < hi; ++i)
+      if (!mbar_wait(bar_full + 8 * (i % C::STAGES), (i / C::STAGES) & 1, 20000000ull)) break;
   }
 }
 
@@ -466,7 +578,7 @@ static int launch_wstream(dflash_handle* h, cudaStream_t s, int kclass, const WP
 
 size_t wstream_scratch_bytes(const dflash_handle* h, int M) {
   const int mt = (M + 15) / 16;
-  return (size_t)2 * h->num_sms * mt * 16 * 128 * sizeof(float) + 256;
+  return (size_t)2 * h->num_sms * DFLASH_WS_MINBLOCKS * mt * 16 * 128 * sizeof(float) + 256;
 }
 
 int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float* partial,
@@ -490,7 +602,7 @@ int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
   prm.kc_per_src = kc_per_src;
   prm.M = L.M;
   prm.units = prm.n_tiles * prm.kc;
-  prm.grid = std::min<int>(prm.units, h->num_sms);
+  prm.grid = std::min<int>(prm.units, h->num_sms * DFLASH_WS_MINBLOCKS);
   prm.partial = partial;
   prm.counters = h->d_counters;
   prm.status = h->d_status;

@@ -137,10 +137,13 @@ typedef struct dflash_handle dflash_handle;
 int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_handle** out);
 int dflash_destroy(dflash_handle* h);
 
-/* Bytes of workspace any call of this handle needs for up to max_rows rows
- * (rows = batch*B for draft/verify-forward calls, T for fuse/inject/prefill).
- * The caller allocates it (256-byte aligned) and passes it with its size. */
-size_t dflash_workspace_bytes(const dflash_handle* h, int64_t max_rows);
+/* Bytes of workspace any call of this handle needs: draft blocks of up to
+ * max_batch sequences of max_block rows, and fuse / inject / target-forward
+ * calls of up to max_rows rows (a forward pass over batch*T rows counts as
+ * batch*T).  The caller allocates it (256-byte aligned) and passes it with
+ * its size; a call given less returns DFLASH_ERR_WORKSPACE. */
+size_t dflash_workspace_bytes(const dflash_handle* h, int32_t max_batch, int32_t max_block,
+                              int64_t max_rows);
 
 /* Target layers whose hidden states are fused (host, integer only):
  * n_pick ids spread uniformly over 0-based [1, n_target_layers-3],

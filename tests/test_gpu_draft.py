@@ -20,7 +20,8 @@ def _gpu_draft(dfl, m, anchors, batch, B, kv, D):
     ids = torch.full((batch, B), -5, dtype=torch.int32, device=dev)
     gap = torch.empty(batch, max(B - 1, 1), device=dev)
     hid = torch.empty(batch * B, D, device=dev)
-    dfl.dflash_draft_block(m.handle, a, batch, B, kv.struct, ids, gap, hid, m.workspace(batch * B))
+    dfl.dflash_draft_block(m.handle, a, batch, B, kv.struct, ids, gap, hid,
+                           m.workspace(batch * B, max_batch=batch, max_block=B))
     assert dfl.dflash_get_status(m.handle) == 0
     return ids.cpu().numpy(), gap.cpu().numpy(), hid.cpu().numpy().reshape(batch, B, D)
 
