@@ -78,6 +78,7 @@ _sig = {
     "dflash_target_forward": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.POINTER(dflash_kv),
                                         C.POINTER(C.c_int32), C.c_int32, _P, _P, _P, C.c_size_t,
                                         _P]),
+    "dflash_lm_head_argmax_noalloc": (C.c_int, [_P, _P, C.c_int32, _P, _P, _P, _P]),
     "dflash_get_status": (C.c_int, [_P, _P]),
     "dflash_strerror": (C.c_char_p, [C.c_int]),
     "dflash_launch_count": (C.c_int64, []),
@@ -191,6 +192,15 @@ def dflash_target_forward(h: int, tokens: torch.Tensor, batch: int, T: int, kv: 
                                       _ptr(taps_out), _ptr(argmax_out), _ptr(ws),
                                       ws.numel() * ws.element_size(), _stream(stream)),
            "dflash_target_forward")
+
+
+def dflash_lm_head_argmax_noalloc(h: int, x: torch.Tensor, rows: int, norm_gain: torch.Tensor,
+                                  ids: torch.Tensor, top2_gap: Optional[torch.Tensor], stream=None):
+    """LM-head argmax with the library's fixed internal scratch (no workspace),
+    for callers that cannot provide device memory at call time."""
+    _check(_lib.dflash_lm_head_argmax_noalloc(h, _ptr(x), rows, _ptr(norm_gain), _ptr(ids),
+                                              _ptr(top2_gap), _stream(stream)),
+           "dflash_lm_head_argmax_noalloc")
 
 
 def dflash_get_status(h: int, stream=None) -> int:

@@ -346,6 +346,7 @@ const char* dflash_strerror(int code) {
     case DFLASH_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case DFLASH_ERR_DEVICE_BOUNDS: return "token id or position out of range";
     case DFLASH_ERR_WORKSPACE: return "workspace too small";
+    case DFLASH_ERR_STATIC_LIMIT: return "request exceeds the fixed internal scratch limits";
     default: return "unknown error";
   }
 }

@@ -60,7 +60,8 @@ enum dflash_status {
   DFLASH_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed */
   DFLASH_ERR_DEVICE_TIMEOUT = 7,/* a bounded device-side wait gave up */
   DFLASH_ERR_DEVICE_BOUNDS = 8, /* token id or position out of range (device-detected) */
-  DFLASH_ERR_WORKSPACE = 9      /* workspace smaller than dflash_workspace_bytes */
+  DFLASH_ERR_WORKSPACE = 9,     /* workspace smaller than dflash_workspace_bytes */
+  DFLASH_ERR_STATIC_LIMIT = 10  /* request larger than a fixed internal scratch array */
 };
 
 enum dflash_dtype { DFLASH_F32 = 0, DFLASH_BF16 = 1 };
@@ -213,6 +214,30 @@ int dflash_target_forward(dflash_handle* h, const int32_t* tokens, int32_t batch
                           const dflash_kv* kv, const int32_t* tap_ids, int32_t n_taps,
                           void* taps_out, int32_t* argmax_out, void* ws, size_t ws_bytes,
                           dflash_stream_t s);
+
+/* LM-head argmax that allocates nothing and takes no workspace.
+ * The paper has no counterpart to this call: it exists for callers that cannot
+ * give the library device memory at call time, such as a serving loop whose
+ * device memory is entirely reserved up front by its own pool, or a
+ * latency-critical path that must not call cudaMalloc (which may synchronise
+ * the device and has no latency bound).  Same result as dflash_lm_head_argmax
+ * (final RMSNorm with norm_gain, shared LM head, lowest-index argmax and
+ * top-2 gap per row); same arguments minus the workspace.
+ *   - Scratch lives in one file-scope device array of about 5.8 MB that every
+ *     GPU which loads the library keeps until the process exits.  Limits:
+ *     rows <= 16, hidden <= 8192, vocab <= 262144, and the handle must be a
+ *     bf16 handle whose weights tile for the streaming kernel (otherwise
+ *     DFLASH_ERR_UNSUPPORTED); larger requests return DFLASH_ERR_STATIC_LIMIT.
+ *   - The first call on a device looks up the array's device address (set-up,
+ *     once per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls that overlap on the GPU
+ *     (different streams, or different handles at once) race on it: order
+ *     them. */
+int dflash_lm_head_argmax_noalloc(dflash_handle* h, const float* x, int32_t rows,
+                                  const float* norm_gain, int32_t* ids, float* top2_gap,
+                                  dflash_stream_t s);
 
 /* Synchronise stream s, then read and clear the handle's device status word.
  * Returns DFLASH_OK or the first device-detected error code. */
