@@ -325,8 +325,19 @@ static bool make_weight_maps(dflash_handle* h) {
   if (w.wc && !mk(&h->map_wc, w.wc, D, c.n_pick * D, 128)) return false;
   if (!mk(&h->map_lm, w.lm_head, V, D, 128)) return false;
   h->have_maps = true;
+  // 256-row boxes for the tensor-core projection of long prefixes
+  if (d == 128 && D % 256 == 0 && Gd % 256 == 0 && w.wc) {
+    bool ok = mk(&h->map_tc_wc, w.wc, D, c.n_pick * D, 256);
+    for (int l = 0; ok && l < c.n_layers; ++l)
+      ok = mk(&h->maps[l].tk, w.layers[l].wk, Gd, D, 256) &&
+           mk(&h->maps[l].tv, w.layers[l].wv, Gd, D, 256);
+    h->have_tc = ok;
+  }
   return true;
 }
+
+// Long prefixes (>= 128 rows) of a bf16 handle go to the tensor-core kernel.
+static bool dense_tc(const dflash_handle* h, int64_t M) { return h->have_tc && M >= 128; }
 
 }  // namespace dflash
 
@@ -495,6 +506,32 @@ int dflash_fuse_context(dflash_handle* h, const void* const* hidden, int64_t T, 
     if (rc) return rc;
     return rmsnorm_rows(h, s, DFLASH_F32, dt, Y, D, h_t_out, D, h->w.g_c, T, D, c.rms_eps, 0);
   }
+  if (dense_tc(h, T)) {
+    // tensor-core projection in row chunks staged as fp32 in the workspace,
+    // each followed by the row RMSNorm
+    const int64_t chunk = std::min<int64_t>(T, (int64_t)(ws_bytes / ((size_t)D * 4 + 1)) / 128 * 128);
+    if (chunk < 128) return DFLASH_ERR_WORKSPACE;
+    float* Yc = (float*)ws;
+    for (int64_t r0 = 0; r0 < T; r0 += chunk) {
+      const int64_t n = std::min(chunk, T - r0);
+      WLaunch L;
+      L.nmap = 1;
+      L.wmaps[0] = &h->map_tc_wc;
+      L.nseg = 1;
+      L.seg[0] = make_seg(0, D / 256, SK_F32, 0, D, Yc, D);
+      L.nsrc = c.n_pick;
+      for (int i = 0; i < c.n_pick; ++i) L.a_src[i] = byte_off(hidden[i], r0 * D, dt);
+      L.a_ld = D;
+      L.K = c.n_pick * D;
+      L.M = (int)n;
+      int rc = tc_gemm(h, s, DFLASH_K_DENSE_GEMM, L);
+      if (rc) return rc;
+      rc = rmsnorm_rows(h, s, DFLASH_F32, dt, Yc, D, (void*)byte_off(h_t_out, r0 * D, dt), D,
+                        h->w.g_c, n, D, c.rms_eps, 0);
+      if (rc) return rc;
+    }
+    return DFLASH_OK;
+  }
   const int64_t chunk = std::min<int64_t>(kChunkRows, (int64_t)(ws_bytes / (D * 4 + 1)));
   if (chunk < 1) return DFLASH_ERR_WORKSPACE;
   float* Y = (float*)ws;
@@ -559,6 +596,42 @@ int dflash_inject_kv(dflash_handle* h, const void* h_t, int64_t n_rows, const in
       L.rm = rm;
       L.len = kv->len;
       const int rc = wstream(h, s, DFLASH_K_DENSE_GEMM, L, partial, nullptr);
+      if (rc) return rc;
+    }
+    return advance_len(h, s, kv->len, seq_rows, 0, batch, kv->cap);
+  }
+  if (dense_tc(h, n_rows) && n_rows <= 0x7fffffff) {
+    // one tensor-core launch for every layer's k and v; the epilogue applies
+    // k_norm and RoPE and appends to the caches
+    const int tk = Gd / 256;
+    const RowMap rm{1, 0, seq_row0, seq_rows, batch, 0};
+    for (int l0 = 0; l0 < c.n_layers; l0 += WS_MAXMAP / 2) {
+      const int nl = std::min(WS_MAXMAP / 2, c.n_layers - l0);
+      WLaunch L;
+      L.nmap = 2 * nl;
+      L.nseg = 2 * nl;
+      for (int j = 0; j < nl; ++j) {
+        const int l = l0 + j;
+        L.wmaps[2 * j] = &h->maps[l].tk;
+        L.wmaps[2 * j + 1] = &h->maps[l].tv;
+        WSeg gk = head_seg(2 * j * tk, (2 * j + 1) * tk, 2 * j, Gd, d, 1,
+                           c.qk_norm ? h->w.layers[l].k_norm : nullptr, kv->k[l], 0);
+        WSeg gv = head_seg((2 * j + 1) * tk, (2 * j + 2) * tk, 2 * j + 1, Gd, d, 0, nullptr,
+                           kv->v[l], 0);
+        gk.cache_cap = gv.cache_cap = kv->cap;
+        gk.cache_heads = gv.cache_heads = G;
+        gk.cache_batch = gv.cache_batch = kv->batch_cap;
+        L.seg[2 * j] = gk;
+        L.seg[2 * j + 1] = gv;
+      }
+      L.nsrc = 1;
+      L.a_src[0] = h_t;
+      L.a_ld = D;
+      L.K = D;
+      L.M = (int)n_rows;
+      L.rm = rm;
+      L.len = kv->len;
+      const int rc = tc_gemm(h, s, DFLASH_K_DENSE_GEMM, L);
       if (rc) return rc;
     }
     return advance_len(h, s, kv->len, seq_rows, 0, batch, kv->cap);

@@ -105,6 +105,7 @@ namespace dflash {
 // halves use 64 x 64 so a 128-row tile holds 64 gate + 64 up rows).
 struct LayerMaps {
   CUtensorMap wq, wk, wv, wo, wg, wu, wd;
+  CUtensorMap tk, tv;   // 64 x 256-row boxes for the tensor-core (tcgen05) projection
 };
 constexpr int kMaxTiles = 8192;   // 128-row weight tiles per projection launch
 }  // namespace dflash
@@ -118,8 +119,9 @@ struct dflash_handle {
   int* d_counters = nullptr;       // [kMaxTiles + 1] tile arrival counters, zero between launches
   float2* d_rope = nullptr;        // [max_pos, d/2] (cos, sin)
   bool have_maps = false;
+  bool have_tc = false;
   dflash::LayerMaps maps[DFLASH_MAX_LAYERS];
-  CUtensorMap map_wc, map_lm;
+  CUtensorMap map_wc, map_lm, map_tc_wc;
   bool timing = false;
   std::vector<cudaEvent_t> free_events;
   std::vector<dflash::Timer> pending;
@@ -192,6 +194,11 @@ bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
 size_t wstream_scratch_bytes(const dflash_handle* h, int M);
 int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float* partial,
             float4* amx);
+
+// ---- tensor-core (tcgen05 / TMEM) dense projection (k_tcgemm.cu) ----------
+// Same launch description as wstream; 128 x 256 output tiles, SK_F32 and
+// SK_HEAD (d = 128) epilogues; segments are in units of 256 columns.
+int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L);
 
 // ---- split-K attention of the draft block (k_attention.cu) ------------------
 int attn_split_keys(const dflash_handle* h, int batch, int B, int cap);

@@ -24,7 +24,8 @@ using namespace ptx;
 constexpr int AT_THREADS = 128;
 constexpr int AT_KSUB = 64;   // keys per sub-chunk
 constexpr int AT_MAX_SPLITS = 128;   // splits per (b, g); bounds the combine's shared memory
-constexpr int AT_MIN_SPLIT = 512;    // keys per split unless that leaves too few CTAs
+constexpr int AT_MIN_SPLIT = 256;    // keys per split unless that leaves too few CTAs
+constexpr int AT_STAGES = 3;         // cp.async pipeline depth of K/V sub-chunks
 
 struct AttnParams {
   const bf16* q;       // [batch*B, H*d]
@@ -36,7 +37,7 @@ struct AttnParams {
   const int32_t* len;  // [batch]
   int cap, B, H, G, rep, split;
   float scale_log2;    // log2(e) / sqrt(d)
-  float* part;         // [batch, G, qgroups, nsplit_max, 64, d + 2]
+  float* part;         // [batch, G, qgroups, nsplit_max, 64, d + 4]
   int* counters;       // [batch * G * qgroups]
   int nsplit_max, qgroups;
   int* status;
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_split_kernel(const AttnPar
   uint8_t* smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sK0 = sQ + 64 * DH * 2;
-  const uint32_t sV0 = sK0 + 2 * AT_KSUB * DH * 2;
+  const uint32_t sV0 = sK0 + AT_STAGES * AT_KSUB * DH * 2;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, g = blockIdx.y;
   const int b = blockIdx.z / p.qgroups, qg = blockIdx.z - b * p.qgroups;
@@ -131,8 +132,12 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_split_kernel(const AttnPar
     }
   };
   const int nsub = (k_end - k_begin + AT_KSUB - 1) / AT_KSUB;
-  load_kv(k_begin, 0);
-  cp_async_commit();
+  // prologue: the first AT_STAGES-1 sub-chunks (the Q tile rides in group 0)
+#pragma unroll
+  for (int st = 0; st < AT_STAGES - 1; ++st) {
+    if (st < nsub) load_kv(k_begin + st * AT_KSUB, st);
+    cp_async_commit();
+  }
 
   const int gq = lane >> 2, tg = lane & 3;
   const bool active = warp * 16 < qrows;
@@ -143,10 +148,11 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_split_kernel(const AttnPar
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
 
   for (int sc = 0; sc < nsub; ++sc) {
-    const int stage = sc & 1;
-    if (sc + 1 < nsub) load_kv(k_begin + (sc + 1) * AT_KSUB, stage ^ 1);
+    const int stage = sc % AT_STAGES;
+    const int pre = sc + AT_STAGES - 1;
+    if (pre < nsub) load_kv(k_begin + pre * AT_KSUB, pre % AT_STAGES);
     cp_async_commit();
-    cp_async_wait<1>();
+    cp_async_wait<AT_STAGES - 1>();
     __syncthreads();
     if (sc == 0 && active) {
 #pragma unroll
@@ -252,7 +258,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_split_kernel(const AttnPar
   cp_async_wait<0>();
 
   // ---- partial of this split: per query row (max, sum, unnormalised O) ------
-  const int DP = DH + 2;
+  const int DP = DH + 4;   // (max, sum, 2 pad, output) keeps the output 16-byte aligned
   const int bgq = (b * p.G + g) * p.qgroups + qg;
   float* part = p.part + ((int64_t)bgq * p.nsplit_max + split) * 64 * DP;
   if (active) {
@@ -265,8 +271,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_split_kernel(const AttnPar
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       const int col = j * 8 + 2 * tg;
-      *(float2*)&part[r0 * DP + 2 + col] = make_float2(acc[j][0], acc[j][1]);
-      *(float2*)&part[r1 * DP + 2 + col] = make_float2(acc[j][2], acc[j][3]);
+      *(float2*)&part[r0 * DP + 4 + col] = make_float2(acc[j][0], acc[j][1]);
+      *(float2*)&part[r1 * DP + 4 + col] = make_float2(acc[j][2], acc[j][3]);
     }
     if (tg == 0) {
       part[r0 * DP] = mrow[0];
@@ -314,24 +320,50 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_split_kernel(const AttnPar
     inv[tid] = 1.0f / lt;
   }
   __syncthreads();
-  for (int c = tid; c < DH; c += AT_THREADS) {
-    float o[64];
+  // each warp owns 16 query rows; its lanes cover one row's DH columns with
+  // one float4 each (a coalesced 512-byte row read); 8 rows x 2 splits of
+  // loads are in flight together and the splits are added in order
+  static_assert(DH == 128, "combine maps 32 lanes x float4 onto a 128-wide row");
+  for (int rc = warp * 16; rc < warp * 16 + 16 && rc < qrows; rc += 8) {
+    float4 o[8];
 #pragma unroll
-    for (int r = 0; r < 64; ++r) o[r] = 0.f;
-    for (int s2 = 0; s2 < nsplit; ++s2) {
-      const float* pr = base + (int64_t)s2 * 64 * DP + 2 + c;
-      float v[64];
+    for (int rr = 0; rr < 8; ++rr) o[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nsplit; s0 += 2) {
+      float4 v[2][8];
+      float w[2][8];
 #pragma unroll
-      for (int r = 0; r < 64; ++r) v[r] = (r < qrows) ? __ldcg(&pr[(int64_t)r * DP]) : 0.f;
+      for (int u = 0; u < 2; ++u) {
+        const int s2 = min(s0 + u, nsplit - 1);
 #pragma unroll
-      for (int r = 0; r < 64; ++r) o[r] += v[r] * ml[2 * (s2 * 64 + r)];
+        for (int rr = 0; rr < 8; ++rr) {
+          const int r = min(rc + rr, qrows - 1);
+          v[u][rr] = __ldcg((const float4*)(base + ((int64_t)s2 * 64 + r) * DP + 4) + lane);
+          w[u][rr] = (s0 + u < nsplit) ? ml[2 * (s2 * 64 + r)] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          o[rr].x += v[u][rr].x * w[u][rr];
+          o[rr].y += v[u][rr].y * w[u][rr];
+          o[rr].z += v[u][rr].z * w[u][rr];
+          o[rr].w += v[u][rr].w * w[u][rr];
+        }
     }
 #pragma unroll
-    for (int r = 0; r < 64; ++r) {
+    for (int rr = 0; rr < 8; ++rr) {
+      const int r = rc + rr;
       if (r >= qrows) break;
       const int qr = q0 + r, hh = qr / p.B, i = qr - hh * p.B;
-      p.o[(int64_t)(b * p.B + i) * (p.H * DH) + (int64_t)(g * p.rep + hh) * DH + c] =
-          __float2bfloat16_rn(o[r] * inv[r]);
+      bf16* dst = p.o + (int64_t)(b * p.B + i) * (p.H * DH) + (int64_t)(g * p.rep + hh) * DH + 4 * lane;
+      const float iv = inv[r];
+      __nv_bfloat162 t0 = __floats2bfloat162_rn(o[rr].x * iv, o[rr].y * iv);
+      __nv_bfloat162 t1 = __floats2bfloat162_rn(o[rr].z * iv, o[rr].w * iv);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&t0);
+      pk.y = *reinterpret_cast<uint32_t*>(&t1);
+      *reinterpret_cast<uint2*>(dst) = pk;
     }
   }
 }
@@ -361,7 +393,7 @@ size_t attn_scratch_bytes(const dflash_handle* h, int batch, int B) {
   const dflash_config& c = h->cfg;
   const int rep = c.n_heads / c.n_kv_heads, qgroups = (B * rep + 63) / 64;
   return (size_t)batch * c.n_kv_heads * qgroups * attn_nsplit_target(h, batch, B) * 64 *
-             (c.head_dim + 2) * sizeof(float) + 256;
+             (c.head_dim + 4) * sizeof(float) + 256;
 }
 
 bool attn_fast_ok(const dflash_handle* h, int B) {
@@ -395,9 +427,9 @@ int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* 
   p.counters = h->d_counters;
   p.status = h->d_status;
   if ((int64_t)batch * p.G * p.qgroups > kMaxTiles) return DFLASH_ERR_SHAPE;
-  // main loop: Q + 2 x (K, V) sub-chunks; combine: Q region + (max, sum) per
-  // (split, row) + 64 inverse sums
-  const size_t smem = std::max<size_t>((size_t)(64 + 4 * AT_KSUB) * DH * 2,
+  // main loop: Q + AT_STAGES x (K, V) sub-chunks; combine: Q region + (max,
+  // sum) per (split, row) + 64 inverse sums
+  const size_t smem = std::max<size_t>((size_t)(64 + 2 * AT_STAGES * AT_KSUB) * DH * 2,
                                        (size_t)64 * DH * 2 + (2 * 64 * AT_MAX_SPLITS + 64) * 4) +
                       128;
   static bool attr_set = false;

@@ -6,11 +6,15 @@
 namespace dflash {
 
 // Block input rows [anchor, mask x (B-1)] through the shared embedding, times
-// input_embedding_scale, into the fp32 residual stream (txtmix §6, §9).
+// input_embedding_scale, into the fp32 residual stream (txtmix §6, §9).  All
+// of a thread's loads are issued before the stores.
 template <typename T>
-__global__ void embed_block_kernel(const T* __restrict__ E, const int32_t* __restrict__ anchor,
-                                   int mask_id, int B, int V, int D, float scale,
-                                   float* __restrict__ x, int* status) {
+__global__ void __launch_bounds__(256) embed_block_kernel(const T* __restrict__ E,
+                                                          const int32_t* __restrict__ anchor,
+                                                          int mask_id, int B, int V, int D,
+                                                          float scale, float* __restrict__ x,
+                                                          int* status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int r = blockIdx.x;
   const int b = r / B, i = r - b * B;
   const int id = (i == 0) ? anchor[b] : mask_id;
@@ -21,7 +25,19 @@ __global__ void embed_block_kernel(const T* __restrict__ E, const int32_t* __res
     return;
   }
   const T* src = E + (int64_t)id * D;
-  for (int k = threadIdx.x; k < D; k += blockDim.x) dst[k] = to_f(src[k]) * scale;
+  constexpr int C = 32;
+  float v[C];
+#pragma unroll
+  for (int q = 0; q < C; ++q) {
+    const int k = threadIdx.x + q * blockDim.x;
+    v[q] = k < D ? to_f(src[k]) : 0.f;
+  }
+#pragma unroll
+  for (int q = 0; q < C; ++q) {
+    const int k = threadIdx.x + q * blockDim.x;
+    if (k < D) dst[k] = v[q] * scale;
+  }
+  for (int k = threadIdx.x + C * blockDim.x; k < D; k += blockDim.x) dst[k] = to_f(src[k]) * scale;
 }
 
 template <typename T>

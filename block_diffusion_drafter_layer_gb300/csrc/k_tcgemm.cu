@@ -1,0 +1,342 @@
+// Dense projection on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// Used where a projection multiplies many rows (the context prefill: fusing
+// and injecting thousands of target positions at once), so the work is a
+// dense contraction.  One CTA computes a 128-row x 256-column output tile:
+//   warp 0    one lane streams 64-wide K slices of the activations (A, 16 KB)
+//             and of the weight (B, 32 KB) with TMA into a 4-deep ring;
+//   warp 1    allocates the 256-column TMEM accumulator; one lane issues
+//             tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate) and
+//             releases each ring stage with tcgen05.commit;
+//   warps 2-5 wait for the final commit, read their 32-lane quarter of the
+//             accumulator with tcgen05.ld and run the epilogue: fp32 store,
+//             or per-head RMSNorm + RoPE + store into a K/V cache.
+// Every wait is bounded; on timeout the CTA flags the status word, drains,
+// frees its TMEM and returns.
+#include <string.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dflash {
+
+using namespace ptx;
+
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
+constexpr int TC_THREADS = 192;
+constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;   // 16 KB
+constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;   // 32 KB
+constexpr int TC_STAGE_TX = TC_A_BYTES + TC_B_BYTES;
+constexpr int TC_OFF_B = TC_STAGES * TC_A_BYTES;
+constexpr int TC_OFF_GUARD = TC_OFF_B + TC_STAGES * TC_B_BYTES;
+constexpr int TC_GUARD = 16384;                 // slack after the ring
+constexpr int TC_OFF_BAR = TC_OFF_GUARD + TC_GUARD;
+constexpr int TC_SMEM = TC_OFF_BAR + 128 + 1024;
+constexpr uint32_t TC_TMEM_COLS = 256;
+
+struct TcParams {
+  CUtensorMap amap[WS_MAXSRC];
+  CUtensorMap bmap[WS_MAXMAP];
+  WSeg seg[WS_MAXMAP];
+  int nseg, M, K, kc_per_src, n_mtiles, n_ntiles;
+  RowMap rm;
+  const int32_t* len;
+  const float2* rope_tab;
+  int max_pos;
+  float eps;
+  int* status;
+};
+static_assert(sizeof(TcParams) <= 4096, "kernel parameters must fit the 4 KB limit");
+
+// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
+// the 128-byte swizzle: rows of 128 B, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);        // start address
+  d |= (uint64_t)1u << 16;                          // leading byte offset (unused here)
+  d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1u << 46;                          // descriptor version
+  d |= (uint64_t)2u << 61;                          // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16, bf16 A and B (K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+// 32 lanes x 32 consecutive fp32 columns: thread t gets lane (base lane + t).
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ int tc_seg_of(const TcParams& p, int t) {
+  int s = 0;
+  while (s + 1 < p.nseg && t >= p.seg[s + 1].t0) ++s;
+  return s;
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + TC_OFF_BAR, bar_empty = bar_full + 8 * TC_STAGES,
+                 bar_done = bar_empty + 8 * TC_STAGES;
+  volatile uint32_t* tmem_slot = (volatile uint32_t*)(smem + TC_OFF_BAR + 8 * (2 * TC_STAGES + 1));
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x / p.n_ntiles, nt = blockIdx.x - mt * p.n_ntiles;
+  const int nk = p.K / TC_BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < TC_STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32((const void*)tmem_slot)),
+                 "r"(TC_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) pdl_launch_dependents();
+
+  const WSeg& g = p.seg[tc_seg_of(p, nt)];
+  const int lt = nt - g.t0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer -------------------------------------------------------------
+      const uint64_t pol_w = policy_evict_last(), pol_a = policy_evict_last();
+      pdl_wait();
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % TC_STAGES, use = kb / TC_STAGES;
+        if (use > 0 && !mbar_wait(bar_empty + 8 * s, (use - 1) & 1)) {
+          atomicOr(p.status, ST_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        if (*abort_flag) break;
+        mbar_arrive_expect_tx(bar_full + 8 * s, TC_STAGE_TX);
+        const int src = kb / p.kc_per_src, lk = kb - src * p.kc_per_src;
+        tma_load_2d(sbase + s * TC_A_BYTES, &p.amap[src], bar_full + 8 * s, lk * TC_BK,
+                    mt * TC_BM, pol_a);
+        tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES, &p.bmap[g.map], bar_full + 8 * s,
+                    kb * TC_BK, lt * TC_BN, pol_w);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ---------------------------------------------------------------
+      const uint32_t idesc = idesc_bf16_f32(TC_BM, TC_BN);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % TC_STAGES, use = kb / TC_STAGES;
+        if (*abort_flag || !mbar_wait(bar_full + 8 * s, use & 1)) {
+          atomicOr(p.status, ST_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = sbase + s * TC_A_BYTES, b0 = sbase + TC_OFF_B + s * TC_B_BYTES;
+#pragma unroll
+        for (int j = 0; j < TC_BK / 16; ++j)
+          tc_mma(tmem, sdesc_sw128(a0 + j * 32), sdesc_sw128(b0 + j * 32), idesc,
+                 (kb > 0 || j > 0) ? 1u : 0u);
+        tc_commit(bar_empty + 8 * s);
+      }
+      tc_commit(bar_done);
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: warps 2-5, TMEM lane quarter (warp % 4) -----------------------
+    pdl_wait();                                     // cache lengths come from earlier kernels
+    const int q = warp & 3;
+    const int r = q * 32 + lane;                    // row within the tile
+    const int row = mt * TC_BM + r;
+    const bool ok = mbar_wait(bar_done, 0, 4000000000ull) && !*abort_flag;
+    tc_fence_after();
+    if (ok) {
+      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+      if (g.kind == SK_F32) {
+        float* dst = (float*)g.dst;
+        for (int c = 0; c < TC_BN / 32; ++c) {
+          float v[32];
+          tc_ld32(trow + c * 32, v);
+          const int n = lt * TC_BN + c * 32;
+          if (row < p.M && n < g.n_valid) {
+            float4* o = (float4*)(dst + (int64_t)row * g.ld + n);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+        }
+      } else if (g.kind == SK_HEAD && g.d == 128) {
+        int b = -1, i = 0;
+        const bool mapped = row < p.M && p.rm.map(row, b, i);
+        const int pos = mapped ? p.len[b] + i : -1;
+        for (int hh = 0; hh < TC_BN / 128; ++hh) {
+          float x[128];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tc_ld32(trow + hh * 128 + c * 32, x + 32 * c);
+          if (!mapped) continue;
+          const int head = lt * (TC_BN / 128) + hh;
+          if (g.gain != nullptr) {
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < 128; ++e) ss += x[e] * x[e];
+            const float rinv = 1.0f / sqrtf(ss / 128.0f + p.eps);
+#pragma unroll
+            for (int e = 0; e < 128; ++e) x[e] = x[e] * rinv * g.gain[e];
+          }
+          if (g.rope) {
+            if (pos < 0 || pos >= p.max_pos) {
+              atomicOr(p.status, ST_BOUNDS);
+              continue;
+            }
+            const float2* cs = p.rope_tab + (int64_t)pos * 64;
+#pragma unroll
+            for (int e = 0; e < 64; ++e) {
+              const float2 t = cs[e];
+              const float y1 = x[e] * t.x - x[e + 64] * t.y;
+              const float y2 = x[e + 64] * t.x + x[e] * t.y;
+              x[e] = y1;
+              x[e + 64] = y2;
+            }
+          }
+          bf16* o;
+          if (g.cache_cap > 0) {
+            if (b >= g.cache_batch || pos < 0 || pos >= g.cache_cap) {
+              atomicOr(p.status, ST_CAPACITY);
+              continue;
+            }
+            o = (bf16*)g.dst + (((int64_t)b * g.cache_heads + head) * g.cache_cap + pos) * 128;
+          } else {
+            o = (bf16*)g.dst + (int64_t)row * g.ld + (int64_t)head * 128;
+          }
+#pragma unroll
+          for (int e = 0; e < 128; e += 8) {
+            uint4 w;
+            __nv_bfloat162 t0 = __floats2bfloat162_rn(x[e], x[e + 1]);
+            __nv_bfloat162 t1 = __floats2bfloat162_rn(x[e + 2], x[e + 3]);
+            __nv_bfloat162 t2 = __floats2bfloat162_rn(x[e + 4], x[e + 5]);
+            __nv_bfloat162 t3 = __floats2bfloat162_rn(x[e + 6], x[e + 7]);
+            w.x = *reinterpret_cast<uint32_t*>(&t0);
+            w.y = *reinterpret_cast<uint32_t*>(&t1);
+            w.z = *reinterpret_cast<uint32_t*>(&t2);
+            w.w = *reinterpret_cast<uint32_t*>(&t3);
+            *reinterpret_cast<uint4*>(o + e) = w;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && threadIdx.x == 0) {
+    // let any TMA loads still in flight land before the shared memory is released
+    for (int s = 0; s < TC_STAGES; ++s) mbar_wait(bar_full + 8 * s, 0, 20000000ull);
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TC_TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L) {
+  if (L.M < 1 || L.K % TC_BK != 0 || L.nseg < 1 || L.nseg > WS_MAXMAP || L.nsrc < 1 ||
+      L.nsrc > WS_MAXSRC || (L.K / TC_BK) % L.nsrc != 0)
+    return DFLASH_ERR_SHAPE;
+  for (int i = 0; i < L.nseg; ++i)
+    if (L.seg[i].kind != SK_F32 && !(L.seg[i].kind == SK_HEAD && L.seg[i].d == 128))
+      return DFLASH_ERR_SHAPE;
+  TcParams prm;
+  memset(&prm, 0, sizeof(prm));
+  const int kc_per_src = L.K / TC_BK / L.nsrc;
+  for (int i = 0; i < L.nsrc; ++i)
+    if (!make_tmap_2d(&prm.amap[i], L.a_src[i], (uint64_t)kc_per_src * TC_BK, (uint64_t)L.M,
+                      (uint64_t)L.a_ld * 2, TC_BK, TC_BM))
+      return DFLASH_ERR_CUDA;
+  for (int i = 0; i < L.nmap; ++i) prm.bmap[i] = *L.wmaps[i];
+  for (int i = 0; i < L.nseg; ++i) prm.seg[i] = L.seg[i];
+  prm.nseg = L.nseg;
+  prm.M = L.M;
+  prm.K = L.K;
+  prm.kc_per_src = kc_per_src;
+  prm.n_ntiles = L.seg[L.nseg - 1].t1;
+  prm.n_mtiles = (L.M + TC_BM - 1) / TC_BM;
+  prm.rm = L.rm;
+  prm.len = L.len;
+  prm.rope_tab = h->d_rope;
+  prm.max_pos = h->cfg.max_pos;
+  prm.eps = h->cfg.rms_eps;
+  prm.status = h->d_status;
+  const int64_t tiles = (int64_t)prm.n_mtiles * prm.n_ntiles;
+  if (tiles > 0x7fffffff) return DFLASH_ERR_SHAPE;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TC_SMEM) != cudaSuccess)
+      return DFLASH_ERR_CUDA;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = TC_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  Timer t;
+  launch_begin(h, kclass, s, &t);
+  cudaLaunchKernelEx(&cfg, tc_gemm_kernel, prm);
+  return launch_end(h, s, &t);
+}
+
+}  // namespace dflash

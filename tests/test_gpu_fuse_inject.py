@@ -70,21 +70,27 @@ def test_fuse_parity(dfl, wname, T):
     m.close()
 
 
-@pytest.mark.parametrize("wname", ["tiny_f32", "qwen3_8b_b1", "qwen35_a3b_32k"])
-def test_inject_parity_ragged(dfl, wname):
+@pytest.mark.parametrize("wname,rows", [("tiny_f32", (37, 27)), ("qwen3_8b_b1", (37, 27)),
+                                        ("qwen35_a3b_32k", (37, 27)),
+                                        ("qwen3_8b_b1", (150, 117)),
+                                        ("qwen35_a3b_32k", (211, 300))])
+def test_inject_parity_ragged(dfl, wname, rows):
+    """Ragged rows of two sequences appended after existing entries, a third
+    sequence with no rows; 64 rows take the streaming path, more rows the
+    tensor-core path."""
     w = synth.WORKLOADS[wname]
     s = w.draft
     dev = "cuda"
     weights = synth.draft_weights(s, w.dtype, w.seed, device=dev)
     m = _models(dfl, w, weights)
     from synth.gpu import kv_cache
-    cap = 160
+    cap = 320
     kv = kv_cache(s, 3, cap, w.dtype)
     len0 = np.array([5, 0, 3], dtype=np.int32)
-    nrows = np.array([37, 27, 0], dtype=np.int32)
-    row0 = np.array([0, 37, 64], dtype=np.int32)
+    nrows = np.array([rows[0], rows[1], 0], dtype=np.int32)
+    T = rows[0] + rows[1]
+    row0 = np.array([0, rows[0], T], dtype=np.int32)
     kv.len.copy_(torch.from_numpy(len0))
-    T = 64
     H_t = synth.target_hidden_states(T, s.D, 1, w.dtype, w.seed + 3, device=dev)[0]
     dfl.dflash_inject_kv(m.handle, H_t, T, torch.from_numpy(row0).to(dev),
                          torch.from_numpy(nrows).to(dev), 3, kv.struct, m.workspace(T))
