@@ -60,8 +60,10 @@ static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 static size_t ws_partial_bytes(const dflash_handle* h) {
   return round256(wstream_scratch_bytes(h, 64));
 }
-static size_t ws_amx_bytes(const dflash_handle* h) {
-  return round256((size_t)((h->cfg.vocab + 127) / 128) * 64 * sizeof(float4));
+static size_t ws_amx_bytes(const dflash_handle* h, int64_t R = 64) {
+  const size_t a = (size_t)((h->cfg.vocab + 127) / 128) * 64;        // streaming kernel
+  const size_t b = (size_t)((h->cfg.vocab + 255) / 256) * std::max<int64_t>(R, 64);  // tcgen05
+  return round256(std::max(a, b) * sizeof(float4));
 }
 
 // Workspace of a forward pass (draft block, target forward, LM head) over R rows.
@@ -105,7 +107,7 @@ static bool carve_forward(const dflash_handle* h, int64_t R, void* ws, size_t ws
   Carve cv{(char*)ws, ws_bytes};
   f->partial = cv.take<float>(ws_partial_bytes(h) / sizeof(float));
   f->attn = batch > 0 ? cv.take<float>(attn_scratch_bytes(h, batch, B) / sizeof(float)) : nullptr;
-  f->amx = cv.take<float4>(ws_amx_bytes(h) / sizeof(float4));
+  f->amx = cv.take<float4>(ws_amx_bytes(h, R) / sizeof(float4));
   f->a = cv.take<char>(R * F * sz);
   f->x = cv.take<float>(R * D);
   f->h = cv.take<char>(R * std::max(D, F) * sz);
@@ -158,6 +160,9 @@ static int mlp_tail(dflash_handle* h, cudaStream_t s, const dflash_layer_weights
 }
 
 static bool streaming(const dflash_handle* h, int64_t M);
+static bool dense_tc(const dflash_handle* h, int64_t M);
+static int lm_head_tc(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows, int32_t* ids,
+                      float* gap, int rps_out, const int32_t* anchor);
 static int lm_head_stream(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows, int32_t* ids,
                           float* gap, int rps_out, const int32_t* anchor);
 
@@ -171,6 +176,7 @@ static int lm_head(dflash_handle* h, cudaStream_t s, Fwd& f, const float* x, int
                          skip_first_of)))
     return rc;
   if (streaming(h, rows)) return lm_head_stream(h, s, f, rows, ids, gap, rps_out, anchor);
+  if (dense_tc(h, rows)) return lm_head_tc(h, s, f, rows, ids, gap, rps_out, anchor);
   if ((rc = gemm(h, s, DFLASH_K_LM_HEAD, dt, one_src(f.hf, D, D), h->w.lm_head, D, f.logits, V,
                  rows, V, D, false)))
     return rc;
@@ -295,6 +301,96 @@ static int lm_head_stream(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows
   return wstream(h, s, DFLASH_K_LM_HEAD, L, f.partial, f.amx);
 }
 
+// ---- tensor-core paths for blocks of >= 128 rows (e.g. batch 32 x B 16) -----
+static int qkv_tc(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R, const RowMap& rm,
+                  const int32_t* len) {
+  const dflash_config& c = h->cfg;
+  const dflash_layer_weights& W = h->w.layers[l];
+  const int D = c.hidden, d = c.head_dim, Hd = c.n_heads * d, Gd = c.n_kv_heads * d;
+  const int tq = Hd / 256, tk = Gd / 256;
+  WLaunch L;
+  L.nmap = 3;
+  L.wmaps[0] = &h->maps[l].tq;
+  L.wmaps[1] = &h->maps[l].tk;
+  L.wmaps[2] = &h->maps[l].tv;
+  L.nseg = 3;
+  L.seg[0] = head_seg(0, tq, 0, Hd, d, 1, c.qk_norm ? W.q_norm : nullptr, f.q, Hd);
+  L.seg[1] = head_seg(tq, tq + tk, 1, Gd, d, 1, c.qk_norm ? W.k_norm : nullptr, f.kb, Gd);
+  L.seg[2] = head_seg(tq + tk, tq + 2 * tk, 2, Gd, d, 0, nullptr, f.vb, Gd);
+  L.nsrc = 1;
+  L.a_src[0] = f.h;
+  L.a_ld = D;
+  L.K = D;
+  L.M = (int)R;
+  L.rm = rm;
+  L.len = len;
+  return tc_gemm(h, s, DFLASH_K_WEIGHT_GEMM, L);
+}
+
+static int mlp_tc(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R) {
+  const dflash_config& c = h->cfg;
+  const dflash_layer_weights& W = h->w.layers[l];
+  const int D = c.hidden, F = c.ffn, Hd = c.n_heads * c.head_dim, dt = c.dtype;
+  int rc;
+  WLaunch L;
+  L.nmap = 1;
+  L.wmaps[0] = &h->maps[l].to;
+  L.nseg = 1;
+  L.seg[0] = make_seg(0, D / 256, SK_RESID, 0, D, f.x, D);
+  L.nsrc = 1;
+  L.a_src[0] = f.o;
+  L.a_ld = Hd;
+  L.K = Hd;
+  L.M = (int)R;
+  if ((rc = tc_gemm(h, s, DFLASH_K_WEIGHT_GEMM, L))) return rc;
+  if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, W.g_post, R, D, c.rms_eps, 0)))
+    return rc;
+  WLaunch G;
+  G.nmap = 2;
+  G.wmaps[0] = &h->maps[l].tg;
+  G.wmaps[1] = &h->maps[l].tu;
+  G.nseg = 1;
+  G.seg[0] = make_seg(0, F / 128, SK_SWIGLU, 0, F, f.a, F);
+  G.seg[0].map2 = 1;
+  G.nsrc = 1;
+  G.a_src[0] = f.h;
+  G.a_ld = D;
+  G.K = D;
+  G.M = (int)R;
+  if ((rc = tc_gemm(h, s, DFLASH_K_WEIGHT_GEMM, G))) return rc;
+  WLaunch Dn;
+  Dn.nmap = 1;
+  Dn.wmaps[0] = &h->maps[l].td;
+  Dn.nseg = 1;
+  Dn.seg[0] = make_seg(0, D / 256, SK_RESID, 0, D, f.x, D);
+  Dn.nsrc = 1;
+  Dn.a_src[0] = f.a;
+  Dn.a_ld = F;
+  Dn.K = F;
+  Dn.M = (int)R;
+  return tc_gemm(h, s, DFLASH_K_WEIGHT_GEMM, Dn);
+}
+
+static int lm_head_tc(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows, int32_t* ids,
+                      float* gap, int rps_out, const int32_t* anchor) {
+  const dflash_config& c = h->cfg;
+  WLaunch L;
+  L.nmap = 1;
+  L.wmaps[0] = &h->map_tc_lm;
+  L.nseg = 1;
+  L.seg[0] = make_seg(0, (c.vocab + 255) / 256, SK_ARGMAX, 0, c.vocab, nullptr, 0);
+  L.nsrc = 1;
+  L.a_src[0] = f.hf;
+  L.a_ld = c.hidden;
+  L.K = c.hidden;
+  L.M = (int)rows;
+  L.ids = ids;
+  L.gap = gap;
+  L.rps_out = rps_out;
+  L.anchor = anchor;
+  return tc_gemm(h, s, DFLASH_K_LM_HEAD, L, f.amx);
+}
+
 static bool kv_ok(const dflash_handle* h, const dflash_kv* kv, int batch) {
   if (!kv || !kv->len || kv->cap <= 0 || kv->batch_cap < batch) return false;
   for (int l = 0; l < h->cfg.n_layers; ++l)
@@ -326,11 +422,17 @@ static bool make_weight_maps(dflash_handle* h) {
   if (!mk(&h->map_lm, w.lm_head, V, D, 128)) return false;
   h->have_maps = true;
   // 256-row boxes for the tensor-core projection of long prefixes
-  if (d == 128 && D % 256 == 0 && Gd % 256 == 0 && w.wc) {
-    bool ok = mk(&h->map_tc_wc, w.wc, D, c.n_pick * D, 256);
-    for (int l = 0; ok && l < c.n_layers; ++l)
-      ok = mk(&h->maps[l].tk, w.layers[l].wk, Gd, D, 256) &&
-           mk(&h->maps[l].tv, w.layers[l].wv, Gd, D, 256);
+  if (d == 128 && D % 256 == 0 && Hd % 256 == 0 && Gd % 256 == 0 && F % 128 == 0) {
+    bool ok = mk(&h->map_tc_lm, w.lm_head, V, D, 256);
+    if (ok && w.wc) ok = mk(&h->map_tc_wc, w.wc, D, c.n_pick * D, 256);
+    for (int l = 0; ok && l < c.n_layers; ++l) {
+      const dflash_layer_weights& L = w.layers[l];
+      LayerMaps& M = h->maps[l];
+      ok = mk(&M.tq, L.wq, Hd, D, 256) && mk(&M.tk, L.wk, Gd, D, 256) &&
+           mk(&M.tv, L.wv, Gd, D, 256) && mk(&M.to, L.wo, D, Hd, 256) &&
+           mk(&M.tg, L.wg, F, D, 128) && mk(&M.tu, L.wu, F, D, 128) &&
+           mk(&M.td, L.wd, D, F, 256);
+    }
     h->have_tc = ok;
   }
   return true;
@@ -465,7 +567,7 @@ size_t dflash_workspace_bytes(const dflash_handle* h, int32_t max_batch, int32_t
   if (!h || max_batch < 0 || max_block < 0 || max_rows < 0) return 0;
   const int64_t R = std::max<int64_t>({(int64_t)max_batch * max_block, max_rows, 1});
   // a forward pass over R rows, or fuse / inject in full kChunkRows passes
-  const size_t scratch = ws_partial_bytes(h) + ws_amx_bytes(h) + 1024 +
+  const size_t scratch = ws_partial_bytes(h) + ws_amx_bytes(h, R) + 1024 +
                          (max_batch > 0 && max_block > 0
                               ? attn_scratch_bytes(h, max_batch, max_block) : 0);
   const size_t fwd = forward_bytes(h->cfg, R);
@@ -681,10 +783,19 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
     return rc;
   const RowMap rm{0, B, nullptr, nullptr, batch, 0};
   const bool stream = streaming(h, R);
+  const bool tcore = !stream && dense_tc(h, R) && attn_fast_ok(h, B);
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights& L = h->w.layers[l];
     if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, L.g_in, R, D, c.rms_eps, 0)))
       return rc;
+    if (tcore) {
+      if ((rc = qkv_tc(h, s, l, f, R, rm, kv->len))) return rc;
+      if ((rc = attention_fast(h, s, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch,
+                               B, f.o, f.attn)))
+        return rc;
+      if ((rc = mlp_tc(h, s, l, f, R))) return rc;
+      continue;
+    }
     if (stream) {
       if ((rc = qkv_stream(h, s, l, f, R, rm, kv->len))) return rc;
       if (attn_fast_ok(h, B))

@@ -105,7 +105,9 @@ namespace dflash {
 // halves use 64 x 64 so a 128-row tile holds 64 gate + 64 up rows).
 struct LayerMaps {
   CUtensorMap wq, wk, wv, wo, wg, wu, wd;
-  CUtensorMap tk, tv;   // 64 x 256-row boxes for the tensor-core (tcgen05) projection
+  // boxes for the tensor-core (tcgen05) projection: 64 x 256 rows, and
+  // 64 x 128 rows for the SwiGLU gate / up halves
+  CUtensorMap tq, tk, tv, to, tg, tu, td;
 };
 constexpr int kMaxTiles = 8192;   // 128-row weight tiles per projection launch
 }  // namespace dflash
@@ -121,7 +123,7 @@ struct dflash_handle {
   bool have_maps = false;
   bool have_tc = false;
   dflash::LayerMaps maps[DFLASH_MAX_LAYERS];
-  CUtensorMap map_wc, map_lm, map_tc_wc;
+  CUtensorMap map_wc, map_lm, map_tc_wc, map_tc_lm;
   bool timing = false;
   std::vector<cudaEvent_t> free_events;
   std::vector<dflash::Timer> pending;
@@ -198,7 +200,7 @@ int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
 // ---- tensor-core (tcgen05 / TMEM) dense projection (k_tcgemm.cu) ----------
 // Same launch description as wstream; 128 x 256 output tiles, SK_F32 and
 // SK_HEAD (d = 128) epilogues; segments are in units of 256 columns.
-int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L);
+int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float4* amx = nullptr);
 
 // ---- split-K attention of the draft block (k_attention.cu) ------------------
 int attn_split_keys(const dflash_handle* h, int batch, int B, int cap);

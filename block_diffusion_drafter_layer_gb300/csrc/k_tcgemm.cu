@@ -10,7 +10,9 @@
 //             releases each ring stage with tcgen05.commit;
 //   warps 2-5 wait for the final commit, read their 32-lane quarter of the
 //             accumulator with tcgen05.ld and run the epilogue: fp32 store,
-//             or per-head RMSNorm + RoPE + store into a K/V cache.
+//             residual add, SwiGLU (gate and up rows paired in one tile),
+//             per-head RMSNorm + RoPE + store (dense or into a K/V cache), or a
+//             per-row top-2 whose last column tile merges the vocabulary.
 // Every wait is bounded; on timeout the CTA flags the status word, drains,
 // frees its TMEM and returns.
 #include <string.h>
@@ -45,6 +47,12 @@ struct TcParams {
   int max_pos;
   float eps;
   int* status;
+  float4* amx;          // SK_ARGMAX: top-2 record per (column tile, row)
+  int* counters;        // SK_ARGMAX: column tiles finished per row tile
+  int32_t* ids;
+  float* gap;
+  int rps_out;
+  const int32_t* anchor;
 };
 static_assert(sizeof(TcParams) <= 4096, "kernel parameters must fit the 4 KB limit");
 
@@ -162,8 +170,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         const int src = kb / p.kc_per_src, lk = kb - src * p.kc_per_src;
         tma_load_2d(sbase + s * TC_A_BYTES, &p.amap[src], bar_full + 8 * s, lk * TC_BK,
                     mt * TC_BM, pol_a);
-        tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES, &p.bmap[g.map], bar_full + 8 * s,
-                    kb * TC_BK, lt * TC_BN, pol_w);
+        if (g.kind == SK_SWIGLU) {   // 128 gate rows then the same 128 up rows
+          tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES, &p.bmap[g.map], bar_full + 8 * s,
+                      kb * TC_BK, lt * (TC_BN / 2), pol_w);
+          tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES + TC_B_BYTES / 2, &p.bmap[g.map2],
+                      bar_full + 8 * s, kb * TC_BK, lt * (TC_BN / 2), pol_w);
+        } else {
+          tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES, &p.bmap[g.map], bar_full + 8 * s,
+                      kb * TC_BK, lt * TC_BN, pol_w);
+        }
       }
     }
     __syncwarp();
@@ -195,7 +210,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     const int q = warp & 3;
     const int r = q * 32 + lane;                    // row within the tile
     const int row = mt * TC_BM + r;
-    const bool ok = mbar_wait(bar_done, 0, 4000000000ull) && !*abort_flag;
+    const bool ok = mbar_wait(bar_done, 0, 4000000000ull) && !(*abort_flag & 1);
     tc_fence_after();
     if (ok) {
       const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
@@ -211,6 +226,75 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           }
         }
+      } else if (g.kind == SK_RESID) {
+        float* dst = (float*)g.dst;
+        for (int c = 0; c < TC_BN / 32; ++c) {
+          float v[32];
+          tc_ld32(trow + c * 32, v);
+          const int n = lt * TC_BN + c * 32;
+          if (row < p.M && n < g.n_valid) {
+            float4* o = (float4*)(dst + (int64_t)row * g.ld + n);
+            float4 old[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) old[i] = o[i];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o[i] = make_float4(old[i].x + v[4 * i], old[i].y + v[4 * i + 1], old[i].z + v[4 * i + 2],
+                                 old[i].w + v[4 * i + 3]);
+          }
+        }
+      } else if (g.kind == SK_SWIGLU) {
+        bf16* dst = (bf16*)g.dst;
+        for (int c = 0; c < TC_BN / 64; ++c) {
+          float gv[32], uv[32];
+          tc_ld32(trow + c * 32, gv);
+          tc_ld32(trow + TC_BN / 2 + c * 32, uv);
+          const int f = lt * (TC_BN / 2) + c * 32;
+          if (row < p.M && f < g.n_valid) {
+            uint4* o = (uint4*)(dst + (int64_t)row * g.ld + f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float a[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float x = gv[8 * i + k];
+                a[k] = x / (1.0f + expf(-x)) * uv[8 * i + k];
+              }
+              __nv_bfloat162 t0 = __floats2bfloat162_rn(a[0], a[1]);
+              __nv_bfloat162 t1 = __floats2bfloat162_rn(a[2], a[3]);
+              __nv_bfloat162 t2 = __floats2bfloat162_rn(a[4], a[5]);
+              __nv_bfloat162 t3 = __floats2bfloat162_rn(a[6], a[7]);
+              uint4 w;
+              w.x = *reinterpret_cast<uint32_t*>(&t0);
+              w.y = *reinterpret_cast<uint32_t*>(&t1);
+              w.z = *reinterpret_cast<uint32_t*>(&t2);
+              w.w = *reinterpret_cast<uint32_t*>(&t3);
+              o[i] = w;
+            }
+          }
+        }
+      } else if (g.kind == SK_ARGMAX) {
+        // top-2 of this row over the tile's columns (lowest index on ties)
+        float t1 = -INFINITY, t2 = -INFINITY;
+        int i1 = 0x7fffffff;
+        for (int c = 0; c < TC_BN / 32; ++c) {
+          float v[32];
+          tc_ld32(trow + c * 32, v);
+          const int n0 = lt * TC_BN + c * 32;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            if (n0 + k >= g.n_valid) break;
+            const float x = v[k];
+            if (x > t1) {
+              t2 = t1;
+              t1 = x;
+              i1 = n0 + k;
+            } else if (x > t2) {
+              t2 = x;
+            }
+          }
+        }
+        if (row < p.M) p.amx[(int64_t)nt * p.M + row] = make_float4(t1, __int_as_float(i1), t2, 0.f);
       } else if (g.kind == SK_HEAD && g.d == 128) {
         int b = -1, i = 0;
         const bool mapped = row < p.M && p.rm.map(row, b, i);
@@ -271,9 +355,58 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
       }
     }
   }
+  if (g.kind == SK_ARGMAX) {
+    // the CTA that finishes the last column tile of this row tile merges the
+    // records of its 128 rows over all column tiles, in column-tile order
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int old = atomicAdd(&p.counters[mt], 1);
+      const int last = (old == p.n_ntiles - 1);
+      if (last) p.counters[mt] = 0;
+      *abort_flag = *abort_flag | (last ? 2 : 0);
+    }
+    __syncthreads();
+    if ((*abort_flag & 2) && warp >= 2) {
+      __threadfence();
+      const int r = (warp & 3) * 32 + lane, row = mt * TC_BM + r;
+      if (row < p.M) {
+        float t1 = -INFINITY, t2 = -INFINITY;
+        int i1 = 0x7fffffff;
+        for (int n0 = 0; n0 < p.n_ntiles; n0 += 8) {
+          float4 rec[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            rec[k] = (n0 + k < p.n_ntiles) ? __ldcg(&p.amx[(int64_t)(n0 + k) * p.M + row])
+                                           : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY, 0.f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float a1 = rec[k].x, a2 = rec[k].z;
+            const int ai = __float_as_int(rec[k].y);
+            const float lo = fminf(t1, a1);
+            if (a1 > t1 || (a1 == t1 && ai < i1)) {
+              t1 = a1;
+              i1 = ai;
+            }
+            t2 = fmaxf(lo, fmaxf(t2, a2));
+          }
+        }
+        int64_t out = row, gout = row;
+        if (p.rps_out > 0) {
+          const int per = p.rps_out - 1;
+          const int64_t b = row / per, i = row % per + 1;
+          out = b * p.rps_out + i;
+          gout = b * per + (i - 1);
+          if (i == 1) p.ids[b * p.rps_out] = p.anchor[b];
+        }
+        p.ids[out] = i1;
+        if (p.gap) p.gap[gout] = t1 - t2;
+      }
+    }
+  }
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag && threadIdx.x == 0) {
+  if ((*abort_flag & 1) && threadIdx.x == 0) {
     // let any TMA loads still in flight land before the shared memory is released
     for (int s = 0; s < TC_STAGES; ++s) mbar_wait(bar_full + 8 * s, 0, 20000000ull);
   }
@@ -286,13 +419,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------------------
-int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L) {
+int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float4* amx) {
   if (L.M < 1 || L.K % TC_BK != 0 || L.nseg < 1 || L.nseg > WS_MAXMAP || L.nsrc < 1 ||
       L.nsrc > WS_MAXSRC || (L.K / TC_BK) % L.nsrc != 0)
     return DFLASH_ERR_SHAPE;
   for (int i = 0; i < L.nseg; ++i)
-    if (L.seg[i].kind != SK_F32 && !(L.seg[i].kind == SK_HEAD && L.seg[i].d == 128))
-      return DFLASH_ERR_SHAPE;
+    if (L.seg[i].kind == SK_HEAD && L.seg[i].d != 128) return DFLASH_ERR_SHAPE;
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
   const int kc_per_src = L.K / TC_BK / L.nsrc;
@@ -314,7 +446,14 @@ int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L) {
   prm.max_pos = h->cfg.max_pos;
   prm.eps = h->cfg.rms_eps;
   prm.status = h->d_status;
+  prm.amx = amx;
+  prm.counters = h->d_counters;
+  prm.ids = L.ids;
+  prm.gap = L.gap;
+  prm.rps_out = L.rps_out;
+  prm.anchor = L.anchor;
   const int64_t tiles = (int64_t)prm.n_mtiles * prm.n_ntiles;
+  if (L.seg[0].kind == SK_ARGMAX && (prm.n_mtiles > kMaxTiles || !amx)) return DFLASH_ERR_SHAPE;
   if (tiles > 0x7fffffff) return DFLASH_ERR_SHAPE;
   static bool attr_set = false;
   if (!attr_set) {
