@@ -21,8 +21,9 @@ LIB_PATH = os.path.join(_HERE, "libdflash.so")
 MAX_LAYERS = 16
 MAX_PICK = 8
 F32, BF16 = 0, 1
-K_WEIGHT_GEMM, K_ATTENTION, K_LM_HEAD, K_DENSE_GEMM, K_ELEMENTWISE, K_VERIFY = range(6)
-K_NCLASS = 6
+(K_WEIGHT_GEMM, K_ATTENTION, K_LM_HEAD, K_DENSE_GEMM, K_ELEMENTWISE, K_VERIFY,
+ K_DRAFT_CHAIN) = range(7)
+K_NCLASS = 7
 
 
 class DFlashError(RuntimeError):
@@ -84,6 +85,9 @@ _sig = {
     "dflash_launch_count": (C.c_int64, []),
     "dflash_timing_enable": (C.c_int, [_P, C.c_int]),
     "dflash_timing_read": (C.c_int, [_P, C.c_int32, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
+    "dflash_chain_trace_enable": (C.c_int, [_P, C.c_int]),
+    "dflash_chain_trace_read": (C.c_int, [_P, C.POINTER(C.c_int64), C.c_int32,
+                                          C.POINTER(C.c_int32)]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -215,6 +219,24 @@ def dflash_timing_read(h: int, kclass: int):
     ms, n = C.c_double(), C.c_int64()
     _check(_lib.dflash_timing_read(h, kclass, C.byref(ms), C.byref(n)), "dflash_timing_read")
     return ms.value, n.value
+
+
+def dflash_chain_trace_enable(h: int, on: bool):
+    _check(_lib.dflash_chain_trace_enable(h, 1 if on else 0), "dflash_chain_trace_enable")
+
+
+TRACE_COLS = ("first_start", "last_start", "first_end", "last_end", "mma_done",
+              "fixup_start", "fixup_sum", "epilogue_end")
+
+
+def dflash_chain_trace_read(h: int, n: int = 128):
+    """Per phase of the latest traced persistent launch: a tuple of ns times
+    named by TRACE_COLS (0 where a phase has no such event)."""
+    k = len(TRACE_COLS)
+    buf = (C.c_int64 * (k * n))()
+    np_ = C.c_int32()
+    _check(_lib.dflash_chain_trace_read(h, buf, n, C.byref(np_)), "dflash_chain_trace_read")
+    return [tuple(buf[k * i: k * i + k]) for i in range(min(np_.value, n))]
 
 
 # ---------------------------------------------------------------------------

@@ -17,6 +17,9 @@ NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(HERE, "..", "include")]
+# extra nvcc flags, e.g. "-DDFLASH_CH_PF=4" to try a compile-time tuning value
+# (objects are not rebuilt when only this changes: remove _build/ first)
+FLAGS += os.environ.get("DFLASH_NVCC_FLAGS", "").split()
 
 
 def _stale(out, deps):

@@ -63,7 +63,14 @@ static size_t ws_partial_bytes(const dflash_handle* h) {
 static size_t ws_amx_bytes(const dflash_handle* h, int64_t R = 64) {
   const size_t a = (size_t)((h->cfg.vocab + 127) / 128) * 64;        // streaming kernel
   const size_t b = (size_t)((h->cfg.vocab + 255) / 256) * std::max<int64_t>(R, 64);  // tcgen05
-  return round256(std::max(a, b) * sizeof(float4));
+  const size_t c = (size_t)std::max(chain_grid(h), 2 * h->num_sms) * 16;  // persistent kernel
+  return round256(std::max({a, b, c}) * sizeof(float4));
+}
+
+// Split-K attention partials of the draft block; the same region holds the
+// persistent kernel's attention-run partials.
+static size_t attn_region_bytes(const dflash_handle* h, int batch, int B) {
+  return round256(std::max(attn_scratch_bytes(h, batch, B), chain_apart_bytes(h, batch)));
 }
 
 // Workspace of a forward pass (draft block, target forward, LM head) over R rows.
@@ -73,7 +80,7 @@ static size_t forward_bytes(const dflash_config& c, int64_t R) {
                 Gd = (int64_t)c.n_kv_heads * c.head_dim, F = c.ffn, V = c.vocab;
   size_t b = 0;
   b += round256(R * F * sz);          // a (SwiGLU output)
-  b += round256(R * D * 4);           // x
+  b += round256(R * D * 4) * 2;       // x, x times the next norm gain
   b += round256(R * std::max(D, F) * sz);  // h / a
   b += round256(R * Hd * 4);          // qf
   b += round256(R * Gd * 4) * 2;      // kf, vf
@@ -93,7 +100,7 @@ static size_t chunk_row_bytes(const dflash_config& c) {
 }
 
 struct Fwd {
-  float *x, *qf, *kf, *vf, *gf, *uf, *logits, *partial, *attn;
+  float *x, *xg, *qf, *kf, *vf, *gf, *uf, *logits, *partial, *attn, *ssq;
   float4* amx;
   void *h, *q, *kb, *vb, *o, *hf, *a;
 };
@@ -106,10 +113,12 @@ static bool carve_forward(const dflash_handle* h, int64_t R, void* ws, size_t ws
                 Gd = (int64_t)c.n_kv_heads * c.head_dim, F = c.ffn, V = c.vocab;
   Carve cv{(char*)ws, ws_bytes};
   f->partial = cv.take<float>(ws_partial_bytes(h) / sizeof(float));
-  f->attn = batch > 0 ? cv.take<float>(attn_scratch_bytes(h, batch, B) / sizeof(float)) : nullptr;
+  f->attn = batch > 0 ? cv.take<float>(attn_region_bytes(h, batch, B) / sizeof(float)) : nullptr;
+  f->ssq = cv.take<float>((size_t)(h->cfg.hidden / 128 + 1) * 16);
   f->amx = cv.take<float4>(ws_amx_bytes(h, R) / sizeof(float4));
   f->a = cv.take<char>(R * F * sz);
   f->x = cv.take<float>(R * D);
+  f->xg = cv.take<float>(R * D);
   f->h = cv.take<char>(R * std::max(D, F) * sz);
   f->qf = cv.take<float>(R * Hd);
   f->kf = cv.take<float>(R * Gd);
@@ -421,6 +430,24 @@ static bool make_weight_maps(dflash_handle* h) {
   if (w.wc && !mk(&h->map_wc, w.wc, D, c.n_pick * D, 128)) return false;
   if (!mk(&h->map_lm, w.lm_head, V, D, 128)) return false;
   h->have_maps = true;
+  // device copy of the draft-layer and LM-head maps for the persistent kernel
+  if (d == 128 && F % 64 == 0) {
+    std::vector<CUtensorMap> tab((size_t)c.n_layers * 7 + 1);
+    for (int l = 0; l < c.n_layers; ++l) {
+      const LayerMaps& M = h->maps[l];
+      const CUtensorMap* src[7] = {&M.wq, &M.wk, &M.wv, &M.wo, &M.wg, &M.wu, &M.wd};
+      for (int k = 0; k < 7; ++k) tab[(size_t)l * 7 + k] = *src[k];
+    }
+    tab.back() = h->map_lm;
+    void* p = nullptr;
+    if (cudaMalloc(&p, tab.size() * sizeof(CUtensorMap)) == cudaSuccess) {
+      if (cudaMemcpy(p, tab.data(), tab.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) ==
+          cudaSuccess)
+        h->d_wmaps = (CUtensorMap*)p;
+      else
+        cudaFree(p);
+    }
+  }
   // 256-row boxes for the tensor-core projection of long prefixes
   if (d == 128 && D % 256 == 0 && Hd % 256 == 0 && Gd % 256 == 0 && F % 128 == 0) {
     bool ok = mk(&h->map_tc_lm, w.lm_head, V, D, 256);
@@ -517,13 +544,13 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   h->device = dev;
   cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess ||
-      cudaMalloc(&h->d_counters, (kMaxTiles + 1) * sizeof(int)) != cudaSuccess) {
+      cudaMalloc(&h->d_counters, kCounters * sizeof(int)) != cudaSuccess) {
     cudaFree(h->d_status);
     delete h;
     return DFLASH_ERR_CUDA;
   }
   cudaMemset(h->d_status, 0, sizeof(int));
-  cudaMemset(h->d_counters, 0, (kMaxTiles + 1) * sizeof(int));
+  cudaMemset(h->d_counters, 0, kCounters * sizeof(int));
   if (!make_weight_maps(h)) h->have_maps = false;
   // RoPE table: angle pos * theta^(-2i/d) in double precision, stored as fp32.
   const int half = c.head_dim / 2;
@@ -558,6 +585,8 @@ int dflash_destroy(dflash_handle* h) {
   cudaFree(h->d_status);
   cudaFree(h->d_counters);
   cudaFree(h->d_rope);
+  cudaFree(h->d_wmaps);
+  cudaFree(h->d_trace);
   delete h;
   return DFLASH_OK;
 }
@@ -568,8 +597,9 @@ size_t dflash_workspace_bytes(const dflash_handle* h, int32_t max_batch, int32_t
   const int64_t R = std::max<int64_t>({(int64_t)max_batch * max_block, max_rows, 1});
   // a forward pass over R rows, or fuse / inject in full kChunkRows passes
   const size_t scratch = ws_partial_bytes(h) + ws_amx_bytes(h, R) + 1024 +
+                         round256((size_t)(h->cfg.hidden / 128 + 1) * 16 * sizeof(float)) +
                          (max_batch > 0 && max_block > 0
-                              ? attn_scratch_bytes(h, max_batch, max_block) : 0);
+                              ? attn_region_bytes(h, max_batch, max_block) : 0);
   const size_t fwd = forward_bytes(h->cfg, R);
   const size_t chunk = round256(kChunkRows * chunk_row_bytes(h->cfg)) + 1024;
   return std::max(fwd, chunk) + scratch;
@@ -778,6 +808,19 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
   Fwd f;
   if (!carve_forward(h, R, ws, ws_bytes, &f, batch, B)) return DFLASH_ERR_WORKSPACE;
   int rc;
+  if (chain_ok(h, batch, B)) {
+    // the whole block in one persistent launch
+    ChainArgs A{anchor, batch, B, kv, draft_ids, top2_gap, f.x, f.xg, f.q, f.kb, f.vb, f.o, f.a,
+                f.ssq, f.partial, f.attn, f.amx};
+    if ((rc = draft_chain(h, s, A))) return rc;
+    if (hidden_out &&
+        cudaMemcpyAsync(hidden_out, f.x, R * D * sizeof(float), cudaMemcpyDeviceToDevice, s))
+      return DFLASH_ERR_CUDA;
+    if (B == 1 &&
+        cudaMemcpyAsync(draft_ids, anchor, batch * sizeof(int32_t), cudaMemcpyDeviceToDevice, s))
+      return DFLASH_ERR_CUDA;
+    return DFLASH_OK;
+  }
   if ((rc = embed_block(h, s, dt, h->w.embed, anchor, c.mask_token_id, batch, B, c.vocab, D,
                         c.embed_scale, f.x)))
     return rc;
@@ -917,7 +960,7 @@ int dflash_get_status(dflash_handle* h, dflash_stream_t st) {
     return DFLASH_ERR_CUDA;
   cudaMemset(h->d_status, 0, sizeof(int));
   // a launch that gave up may have left tile counters mid-count
-  if (v & ST_TIMEOUT) cudaMemset(h->d_counters, 0, (kMaxTiles + 1) * sizeof(int));
+  if (v & ST_TIMEOUT) cudaMemset(h->d_counters, 0, kCounters * sizeof(int));
   if (v & ST_CAPACITY) return DFLASH_ERR_CAPACITY;
   if (v & ST_BOUNDS) return DFLASH_ERR_DEVICE_BOUNDS;
   if (v & ST_TIMEOUT) return DFLASH_ERR_DEVICE_TIMEOUT;
@@ -952,6 +995,42 @@ int dflash_timing_read(dflash_handle* h, int32_t kclass, double* total_ms, int64
   return DFLASH_OK;
 }
 
+int dflash_chain_trace_enable(dflash_handle* h, int on) {
+  if (!h) return DFLASH_ERR_INVALID_ARG;
+  if (on && !h->d_trace) {
+    if (cudaMalloc(&h->d_trace, kChainTraceCols * kChainMaxPhases * sizeof(unsigned long long)) !=
+        cudaSuccess) {
+      h->d_trace = nullptr;
+      return DFLASH_ERR_CUDA;
+    }
+    h->trace_phases = 0;
+  } else if (!on && h->d_trace) {
+    cudaDeviceSynchronize();
+    cudaFree(h->d_trace);
+    h->d_trace = nullptr;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_chain_trace_read(dflash_handle* h, int64_t* out, int32_t n, int32_t* n_phases) {
+  if (!h || !n_phases || n < 0 || (n > 0 && !out)) return DFLASH_ERR_INVALID_ARG;
+  *n_phases = 0;
+  if (!h->d_trace || h->trace_phases == 0) return DFLASH_OK;
+  std::vector<unsigned long long> t(kChainTraceCols * kChainMaxPhases);
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(t.data(), h->d_trace, t.size() * sizeof(t[0]), cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  const int np = h->trace_phases;
+  for (int p = 0; p < np && p < n; ++p)
+    for (int k = 0; k < kChainTraceCols; ++k) {
+      const unsigned long long v = t[(size_t)k * kChainMaxPhases + p];
+      out[kChainTraceCols * p + k] = v == ~0ull ? 0 : (int64_t)v;
+    }
+  *n_phases = np;
+  return DFLASH_OK;
+}
+
 }  // extern "C"
 
 namespace dflash {
@@ -959,7 +1038,7 @@ namespace dflash {
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int dtype) {
   if (!g_encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -973,7 +1052,26 @@ bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t es[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  const CUtensorMapDataType ty =
+      dtype == DFLASH_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return g_encode(m, ty, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// fp32 rows [rows, cols] viewed as [rows, cols / 32, 32] (3-D), box
+// {32, 2, box_rows} with the 128-byte swizzle: one load brings a 64-column
+// chunk of box_rows rows (128-byte line l = 2 * row + half).
+bool make_tmap_rows_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                        uint32_t box_rows) {
+  if (!g_encode && !make_tmap_2d(m, base, 32, 1, 128, 32, 1, DFLASH_F32)) return false;
+  if (cols % 64) return false;
+  const cuuint64_t dims[3] = {32, cols / 32, rows};
+  const cuuint64_t strides[2] = {128, cols * 4};
+  const cuuint32_t box[3] = {32, 2, box_rows};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;

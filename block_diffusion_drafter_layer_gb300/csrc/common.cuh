@@ -110,6 +110,16 @@ struct LayerMaps {
   CUtensorMap tq, tk, tv, to, tg, tu, td;
 };
 constexpr int kMaxTiles = 8192;   // 128-row weight tiles per projection launch
+// d_counters: [0, kMaxTiles) tile arrival counters, then the LM-head merge
+// counter, the persistent kernel's grid barrier and its exit counter
+constexpr int kCounters = kMaxTiles + 4;
+// phases of the persistent draft-block kernel: embed, 10 per layer, LM head
+// and its reduce
+constexpr int kChainMaxPhases = 3 + 10 * DFLASH_MAX_LAYERS;
+// timeline columns per phase: first start, last start, first end, last end,
+// last CTA done with its multiply-adds, and for the split-K fix-ups (the CTA
+// that completes a tile): latest fix-up start, sum done, epilogue done
+constexpr int kChainTraceCols = 8;
 }  // namespace dflash
 
 struct dflash_handle {
@@ -118,12 +128,15 @@ struct dflash_handle {
   int device = 0;
   int num_sms = 0;
   int* d_status = nullptr;
-  int* d_counters = nullptr;       // [kMaxTiles + 1] tile arrival counters, zero between launches
+  int* d_counters = nullptr;       // [kCounters] arrival counters, zero between launches
   float2* d_rope = nullptr;        // [max_pos, d/2] (cos, sin)
   bool have_maps = false;
   bool have_tc = false;
   dflash::LayerMaps maps[DFLASH_MAX_LAYERS];
   CUtensorMap map_wc, map_lm, map_tc_wc, map_tc_lm;
+  CUtensorMap* d_wmaps = nullptr;  // device copy: q k v o gate up down per layer, then LM head
+  unsigned long long* d_trace = nullptr;  // phase timeline of the persistent kernel, when enabled
+  int trace_phases = 0;
   bool timing = false;
   std::vector<cudaEvent_t> free_events;
   std::vector<dflash::Timer> pending;
@@ -191,8 +204,13 @@ struct WLaunch {
   const int32_t* anchor = nullptr;
 };
 
+// 2-D TMA descriptor with the 128-byte swizzle (box_inner x element size must
+// be 128 bytes or less); dtype DFLASH_BF16 or DFLASH_F32.
 bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                  int dtype = DFLASH_BF16);
+bool make_tmap_rows_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                        uint32_t box_rows);
 size_t wstream_scratch_bytes(const dflash_handle* h, int M);
 int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float* partial,
             float4* amx);
@@ -209,6 +227,26 @@ bool attn_fast_ok(const dflash_handle* h, int B);
 int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* kc, const void* vc,
                    int cap, const int32_t* len, const void* kb, const void* vb, int batch, int B,
                    void* o, float* scratch);
+
+// ---- persistent draft block for at most 16 rows (k_chain.cu) ----------------
+struct ChainArgs {
+  const int32_t* anchor;
+  int batch, B;
+  const dflash_kv* kv;
+  int32_t* ids;
+  float* gap;
+  float* x;                     // [R, D] fp32 residual
+  float* xg;                    // [R, D] fp32 residual times the next RMSNorm gain
+  void *q, *kb, *vb, *o, *a;    // bf16 [R, H*d], [R, G*d] x 2, [R, H*d], [R, F]
+  float* ssq;                   // [D / 128, 16]
+  float* partial;               // split-K fix-up tiles
+  float* apart;                 // attention run partials (chain_apart_bytes)
+  float4* amx;                  // LM-head top-2 records
+};
+int chain_grid(const dflash_handle* h);
+size_t chain_apart_bytes(const dflash_handle* h, int batch);
+bool chain_ok(const dflash_handle* h, int batch, int B);
+int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A);
 
 // ---- kernel launchers (one translation unit each) --------------------------
 // A operand source: up to DFLASH_MAX_PICK column segments of width seg

@@ -1,0 +1,1308 @@
+// Persistent draft-block kernel for short blocks (at most 16 rows in all).
+//
+// A draft block of one sequence (or a few short ones) multiplies a handful of
+// rows by every draft weight, so its time is the time to read those weights
+// from HBM.  Issued as one launch per projection, each launch loses several
+// microseconds to start-up, ramp and the split-K fix-up tail.  This kernel
+// runs the whole block (txtmix §6: embed the block [anchor, mask, ...], the
+// draft layers over [context ; block], the shared LM head) in one cooperative
+// launch of two CTAs per SM, as a fixed sequence of phases separated by
+// grid-wide barriers:
+//
+//   embed | per layer: q/k/v  attention  combine  o_proj  gate/up  down | LM head
+//
+// (each projection followed by a reduce phase, below)
+//
+// * Projections stream their weight tiles through a TMA / mbarrier ring in
+//   (128-row tile, 64-column chunk) units spread evenly over the CTAs (split
+//   K).  A CTA finishes the tiles it owns whole; for the others it leaves a
+//   partial sum, and the following reduce phase gives each (tile, row) to one
+//   warp, which adds the partials in k order and runs the epilogue.  The
+//   producer lane keeps loading the NEXT projection's weights while the grid
+//   waits at a barrier (weights do not depend on activations); only the
+//   activation loads wait for the barrier.
+// * The RMSNorms in front of q/k/v, gate/up and the LM head are folded into
+//   those projections: the residual epilogues (and the embedding) write the
+//   residual x, the residual times the next norm's gain (x * g), and one sum
+//   of squares of x per (128-column tile, row); the next projection loads the
+//   fp32 x * g rows by TMA and builds its bf16 MMA operand as
+//   bf16((x * g) * rinv) in registers: the norm's storage point, with the two
+//   fp32 products taken in the other order.
+// * Attention cuts the keys of each (sequence, kv head) into equal runs of
+//   32-key sub-chunks, one run per work item, items dealt round-robin to the
+//   CTAs; each item keeps (max, sum, unnormalised output) per query row, and
+//   the combine phase merges the runs of a row in run order.
+//
+// Every wait is bounded; a CTA that gives up sets ST_TIMEOUT, which every
+// other CTA polls while it waits, so the grid drains within one wait limit.
+#include <string.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dflash {
+
+using namespace ptx;
+
+#ifndef DFLASH_CH_STAGES
+#define DFLASH_CH_STAGES 3
+#endif
+// weight units a CTA prefetches into L2 beyond its shared-memory ring (0:
+// none; measured on the Qwen3-8B-shaped block, 4 and 8 were slower: the
+// prefetched lines compete with the demand stream)
+#ifndef DFLASH_CH_PF
+#define DFLASH_CH_PF 0
+#endif
+
+constexpr int CH_THREADS = 160;            // warp 0: TMA producer; warps 1-4: consumers
+constexpr int CH_CT = 128;                 // consumer threads
+constexpr int CH_STAGES = DFLASH_CH_STAGES;
+constexpr int CH_W = 128 * 64 * 2;         // weight chunk: 128 rows x 64 k, bf16
+constexpr int CH_A = 16 * 64 * 4;          // activation chunk: 16 rows x 64 k, fp32 (or bf16)
+constexpr int CH_DH = 128;                 // head dim of the attention phases
+constexpr int CH_AK = 32;                  // keys per attention sub-chunk
+constexpr int CH_DP = CH_DH + 4;           // attention partial row: max, sum, 2 pad, output
+constexpr int CH_EPAD = 132;               // fp32 tile row pitch in shared memory
+constexpr int CH_ROWS = 16;                // rows of the block (all sequences)
+constexpr int CH_MAXB = 16;                // sequences
+
+// shared memory layout (offsets from a 1024-aligned base)
+constexpr int CH_OFF_A = CH_STAGES * CH_W;
+constexpr int CH_OFF_ATT = CH_OFF_A + CH_STAGES * CH_A;
+constexpr int CH_ATT_Q = 64 * CH_DH * 2;              // 64 query rows
+constexpr int CH_ATT_KV = CH_AK * CH_DH * 2;          // one K (or V) sub-chunk
+constexpr int CH_ATT_BYTES = CH_ATT_Q + 4 * CH_ATT_KV; // Q + 2 stages x (K, V)
+constexpr int CH_OFF_BAR = CH_OFF_ATT + CH_ATT_BYTES;
+constexpr int CH_OFF_MISC = CH_OFF_BAR + 2 * CH_STAGES * 8;
+constexpr int CH_MISC_BYTES = 2048;
+constexpr int CH_SMEM = CH_OFF_MISC + CH_MISC_BYTES + 1024;
+static_assert(CH_ROWS * CH_EPAD * 4 <= CH_ATT_BYTES, "the fp32 tile aliases the attention buffers");
+static_assert(CH_SMEM <= 233472 / 2 - 1024, "two CTAs per SM");
+
+enum ChainPhase : int { PH_EMBED, PH_QKV, PH_ATT, PH_CMB, PH_O, PH_GU, PH_DN, PH_LM, PH_RED };
+// phases of one layer; every projection is followed by its reduce phase
+constexpr int kLayerPhases = 10;
+__device__ __constant__ const int kLayerSeq[kLayerPhases] = {PH_QKV, PH_RED, PH_ATT, PH_CMB, PH_O,
+                                                             PH_RED, PH_GU,  PH_RED, PH_DN,  PH_RED};
+
+struct ChainLayer {
+  const float* g_in;
+  const float* g_post;
+  const float* q_norm;
+  const float* k_norm;
+};
+
+struct ChainParams {
+  CUtensorMap map_xg;         // fp32 x * g [R, D] as [R, D/32, 32], box {32, 2, 16}
+  CUtensorMap map_o;          // bf16 attention output [R, H*d], box 64 x 16
+  CUtensorMap map_a;          // bf16 SwiGLU output [R, F], box 64 x 16
+  const CUtensorMap* wmaps;   // [n_layers * 7 + 1]: q k v o gate up down per layer, LM head
+  const bf16* kc[DFLASH_MAX_LAYERS];
+  const bf16* vc[DFLASH_MAX_LAYERS];
+  ChainLayer lay[DFLASH_MAX_LAYERS];
+  const bf16* embed;
+  const float* g_f;
+  const int32_t* anchor;
+  const int32_t* len;
+  int32_t* ids;
+  float* gap;
+  float* x;
+  float* xg;
+  bf16* q;
+  bf16* kb;
+  bf16* vb;
+  bf16* o;
+  bf16* a;
+  float* ssq;                 // [D / 128][16]
+  float* partial;             // split-K fix-up: [2 * grid][16 * 128]
+  float* apart;               // attention items: [n_items_max][64][CH_DP]
+  float4* amx;                // LM-head top-2 records: [vocab tiles][R]
+  int* counters;              // tile counters; amx_done, barrier, exit at kMaxTiles + 0..2
+  int* status;
+  unsigned long long* trace;  // optional: kChainTraceCols arrays of [kChainMaxPhases] (ns)
+  const float2* rope;
+  int max_pos;
+  int R, batch, B, D, Hd, Gd, F, V, G, rep, nL, cap, mask_id, qk_norm;
+  int grid, n_phases, n_items_max;
+  float eps, embed_scale, scale_log2;
+};
+static_assert(sizeof(ChainParams) <= 4096, "kernel parameters must fit the 4 KB limit");
+
+// misc words in shared memory
+// MS_ABORT may be set by any thread at any time; MS_GO and MS_LAST are
+// written by consumer thread 0 only between two consumer barriers, so every
+// consumer warp reads the same value and takes the same barriers.
+enum : int { MS_ABORT = 0, MS_LAST = 1, MS_ISSUED = 2, MS_CONSUMED = 3, MS_GO = 4 };
+// [0, 16) ints: flags; [16, 48): rowpos (sequence, position) per row;
+// [48, 64): rinv per row; [64, 192): attention item tables; [192, 384):
+// LM-head top-2 records, [4 warps][16 rows][3]
+
+// Phase p: 0 embed; then kLayerPhases per layer; then LM head and its reduce.
+__device__ __forceinline__ int phase_kind(const ChainParams& P, int p, int& l) {
+  if (p == 0) {
+    l = 0;
+    return PH_EMBED;
+  }
+  const int q = p - 1;
+  l = q / kLayerPhases;
+  if (l >= P.nL) {
+    l = P.nL;
+    return q - P.nL * kLayerPhases == 0 ? PH_LM : PH_RED;
+  }
+  return kLayerSeq[q % kLayerPhases];
+}
+
+struct Geo {
+  int n_tiles, kc, a_f32;
+};
+__device__ __forceinline__ Geo gemm_geo(const ChainParams& P, int kind) {
+  switch (kind) {
+    case PH_QKV: return {(P.Hd + 2 * P.Gd) / 128, P.D / 64, 1};
+    case PH_O: return {P.D / 128, P.Hd / 64, 0};
+    case PH_GU: return {P.F / 64, P.D / 64, 1};
+    case PH_DN: return {P.D / 128, P.F / 64, 0};
+    default: return {(P.V + 127) / 128, P.D / 64, 1};   // PH_LM
+  }
+}
+__device__ __forceinline__ bool is_gemm(int kind) {
+  return kind == PH_QKV || kind == PH_O || kind == PH_GU || kind == PH_DN || kind == PH_LM;
+}
+
+__device__ __forceinline__ int first_unit_of(int64_t c, int64_t U, int64_t G) {
+  return (int)(c * U / G);
+}
+__device__ __forceinline__ int owner_of(int64_t u, int64_t U, int64_t G) {
+  return (int)(((u + 1) * G + U - 1) / U) - 1;
+}
+
+// ---- grid barrier ----------------------------------------------------------
+// Phase p may start once every CTA has arrived p times.  Gives up (and flags
+// ST_TIMEOUT) after the wall-clock limit or as soon as another CTA has.
+__device__ bool grid_wait(const ChainParams& P, int target) {
+  const int* bar = P.counters + kMaxTiles + 1;
+  if (ld_acquire_gpu(bar) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  for (int it = 0;; ++it) {
+    if (ld_acquire_gpu(bar) >= target) return true;
+    if ((it & 63) == 63) {
+      if (*(volatile int*)P.status & ST_TIMEOUT) return false;
+      if (globaltimer() - t0 > 2000000000ull) {
+        atomicOr(P.status, ST_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// ---- producer ----------------------------------------------------------------
+// One lane walks this CTA's projection units of every phase twice: a weight
+// cursor that fills ring slots as soon as they are free, and an activation
+// cursor that follows it once the unit's phase has passed its barrier.
+struct Cursor {
+  int p, kind, l, u, u1, kc, a_f32;
+  int i;   // ring index
+};
+
+__device__ __forceinline__ bool cursor_phase(const ChainParams& P, Cursor& c, int p) {
+  for (; p < P.n_phases; ++p) {
+    int l;
+    const int kind = phase_kind(P, p, l);
+    if (!is_gemm(kind)) continue;
+    const Geo g = gemm_geo(P, kind);
+    const int64_t U = (int64_t)g.n_tiles * g.kc;
+    const int u0 = first_unit_of(blockIdx.x, U, P.grid), u1 = first_unit_of(blockIdx.x + 1, U, P.grid);
+    if (u1 <= u0) continue;
+    c.p = p;
+    c.kind = kind;
+    c.l = l;
+    c.u = u0;
+    c.u1 = u1;
+    c.kc = g.kc;
+    c.a_f32 = g.a_f32;
+    return true;
+  }
+  c.p = P.n_phases;
+  return false;
+}
+__device__ __forceinline__ bool cursor_next(const ChainParams& P, Cursor& c) {
+  ++c.i;
+  if (++c.u < c.u1) return true;
+  return cursor_phase(P, c, c.p + 1);
+}
+
+// Weight box(es) of unit c: (map, inner coordinate, row coordinate); GU has two.
+struct WBox {
+  const CUtensorMap* m[2];
+  int c0, r[2], n;
+};
+__device__ __forceinline__ WBox wbox(const ChainParams& P, const Cursor& c) {
+  const int t = c.u / c.kc, kk = c.u - t * c.kc;
+  WBox b;
+  b.c0 = kk * 64;
+  b.n = 1;
+  if (c.kind == PH_LM) {
+    b.m[0] = P.wmaps + P.nL * 7;
+    b.r[0] = t * 128;
+    return b;
+  }
+  const CUtensorMap* L = P.wmaps + c.l * 7;
+  switch (c.kind) {
+    case PH_QKV: {
+      const int tq = P.Hd / 128, tk = P.Gd / 128;
+      const int w = t < tq ? 0 : t < tq + tk ? 1 : 2;
+      b.m[0] = L + w;
+      b.r[0] = (t - (w == 0 ? 0 : w == 1 ? tq : tq + tk)) * 128;
+      break;
+    }
+    case PH_O: b.m[0] = L + 3; b.r[0] = t * 128; break;
+    case PH_GU:
+      b.m[0] = L + 4;
+      b.m[1] = L + 5;
+      b.r[0] = b.r[1] = t * 64;
+      b.n = 2;
+      break;
+    default: b.m[0] = L + 6; b.r[0] = t * 128; break;   // PH_DN
+  }
+  return b;
+}
+
+__device__ void issue_w(const ChainParams& P, const Cursor& c, uint32_t dst, uint32_t bar,
+                        uint64_t pol) {
+  const WBox b = wbox(P, c);
+  tma_load_2d(dst, b.m[0], bar, b.c0, b.r[0], pol);
+  if (b.n == 2) tma_load_2d(dst + CH_W / 2, b.m[1], bar, b.c0, b.r[1], pol);
+}
+
+__device__ void prefetch_w(const ChainParams& P, const Cursor& c) {
+  const WBox b = wbox(P, c);
+  tma_prefetch_2d(b.m[0], b.c0, b.r[0]);
+  if (b.n == 2) tma_prefetch_2d(b.m[1], b.c0, b.r[1]);
+}
+
+__device__ void issue_a(const ChainParams& P, const Cursor& c, uint32_t dst, uint32_t bar,
+                        uint64_t pol) {
+  const int kk = c.u % c.kc;
+  if (c.a_f32) {
+    tma_load_3d(dst, &P.map_xg, bar, 0, kk * 2, 0, pol);
+  } else {
+    tma_load_2d(dst, c.kind == PH_O ? &P.map_o : &P.map_a, bar, kk * 64, 0, pol);
+  }
+}
+
+__device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full,
+                         uint32_t bar_empty, volatile int* misc) {
+  const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
+  Cursor w{}, a{};
+  w.i = a.i = 0;
+  bool w_more = cursor_phase(P, w, 0);
+  a = w;
+  bool a_more = w_more;
+  // L2 prefetch cursor: kept DFLASH_CH_PF units past the ring, so HBM keeps
+  // streaming upcoming weights while the grid sits in a tail or a barrier
+  Cursor f = w;
+  bool f_more = w_more;
+  auto prefetch_ahead = [&]() {
+    while (f_more && f.i < w.i + CH_STAGES + DFLASH_CH_PF) {
+      if (f.i >= w.i + CH_STAGES) prefetch_w(P, f);
+      f_more = cursor_next(P, f);
+    }
+  };
+  prefetch_ahead();
+  int ready = 0;                 // phases known to have passed their barrier
+  uint64_t t_idle = 0;
+  bool abort = false;
+  while (a_more) {
+    bool prog = false;
+    if (w_more && !abort) {
+      const int s = w.i % CH_STAGES, use = w.i / CH_STAGES;
+      // with no activation load owed, block in the barrier wait instead of spinning
+      if (use == 0 || (a.i == w.i ? mbar_try_wait(bar_empty + 8 * s, (use - 1) & 1)
+                                  : mbar_test_wait(bar_empty + 8 * s, (use - 1) & 1))) {
+        const uint32_t abytes = w.a_f32 ? CH_A : CH_A / 2;
+        mbar_arrive_expect_tx(bar_full + 8 * s, CH_W + abytes);
+        issue_w(P, w, sbase + s * CH_W, bar_full + 8 * s, pol_w);
+        w_more = cursor_next(P, w);
+        prefetch_ahead();
+        prog = true;
+      }
+    }
+    if (a.i < w.i) {
+      bool ok = abort || a.p <= ready;
+      if (!ok && ld_acquire_gpu(P.counters + kMaxTiles + 1) >= a.p * P.grid) {
+        // the phase's inputs are visible to this thread; order them before
+        // its TMA (async-proxy) reads
+        fence_proxy_async_global();
+        ready = a.p;
+        ok = true;
+      }
+      if (ok) {
+        const int s = a.i % CH_STAGES;
+        issue_a(P, a, sbase + CH_OFF_A + s * CH_A, bar_full + 8 * s, pol_a);
+        a_more = cursor_next(P, a);
+        prog = true;
+      }
+    } else if (!w_more) {
+      break;   // every issued unit has its activation load
+    }
+    if (prog) {
+      t_idle = 0;
+      continue;
+    }
+    if (abort) break;   // nothing left that can complete
+    if (misc[MS_ABORT] || (*(volatile int*)P.status & ST_TIMEOUT)) {
+      abort = true;     // stop loading weights; finish the activation loads already owed
+      continue;
+    }
+    const uint64_t now = globaltimer();
+    if (t_idle == 0) t_idle = now;
+    else if (now - t_idle > 2000000000ull) {
+      atomicOr(P.status, ST_TIMEOUT);
+      misc[MS_ABORT] = 1;
+      abort = true;
+    }
+  }
+  misc[MS_ISSUED] = w.i;
+}
+
+// ---- consumers: projection ------------------------------------------------------
+struct Top2 {
+  float t1;
+  int i1;
+  float t2;
+};
+__device__ __forceinline__ Top2 top2_merge(Top2 a, Top2 b) {
+  Top2 r;
+  if (b.t1 > a.t1 || (b.t1 == a.t1 && b.i1 < a.i1)) {
+    r.t1 = b.t1;
+    r.i1 = b.i1;
+  } else {
+    r.t1 = a.t1;
+    r.i1 = a.i1;
+  }
+  r.t2 = fmaxf(fminf(a.t1, b.t1), fmaxf(a.t2, b.t2));
+  return r;
+}
+__device__ __forceinline__ Top2 top2_warp(Top2 t) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Top2 u;
+    u.t1 = __shfl_xor_sync(0xffffffffu, t.t1, o);
+    u.i1 = __shfl_xor_sync(0xffffffffu, t.i1, o);
+    u.t2 = __shfl_xor_sync(0xffffffffu, t.t2, o);
+    t = top2_merge(t, u);
+  }
+  return t;
+}
+__device__ __forceinline__ float4 shfl_xor4(float4 v, int m) {
+  return make_float4(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m),
+                     __shfl_xor_sync(0xffffffffu, v.z, m), __shfl_xor_sync(0xffffffffu, v.w, m));
+}
+
+// Row epilogues.  One warp finishes one row r of one output tile t; lane k
+// holds the tile's columns 4k .. 4k+3.  Global inputs of the epilogue are
+// fetched first (row_in) so their latency overlaps the partial-tile loads.
+struct RowIn {
+  float4 a;   // residual (o_proj, down) or RoPE (cos, sin) of columns j, j+1 (q, k)
+  float4 b;   // RoPE (cos, sin) of columns j+2, j+3 (q, k)
+};
+__device__ __forceinline__ int qkv_which(const ChainParams& P, int t) {
+  const int tq = P.Hd / 128, tk = P.Gd / 128;
+  return t < tq ? 0 : t < tq + tk ? 1 : 2;
+}
+
+// The gain the tile's epilogue multiplies by (the same for all rows): the
+// next norm's (o_proj, down), the head norm's (q, k) or none.
+__device__ __forceinline__ float4 tile_gain(const ChainParams& P, int kind, int l, int t) {
+  const int lane = threadIdx.x & 31;
+  if (kind == PH_O || kind == PH_DN) {
+    const float* gn = kind == PH_O ? P.lay[l].g_post : l + 1 < P.nL ? P.lay[l + 1].g_in : P.g_f;
+    return __ldg((const float4*)(gn + t * 128) + lane);
+  }
+  if (kind == PH_QKV && P.qk_norm) {
+    const int which = qkv_which(P, t);
+    if (which < 2) return __ldg((const float4*)(which == 0 ? P.lay[l].q_norm : P.lay[l].k_norm) + lane);
+  }
+  return make_float4(1.f, 1.f, 1.f, 1.f);
+}
+
+__device__ __forceinline__ RowIn row_in(const ChainParams& P, int kind, int t, int r,
+                                        const int* rowpos) {
+  const int lane = threadIdx.x & 31;
+  RowIn in;
+  in.a = in.b = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (kind == PH_O || kind == PH_DN) {
+    in.a = __ldcg((const float4*)(P.x + (int64_t)r * P.D + t * 128) + lane);
+  } else if (kind == PH_QKV && qkv_which(P, t) < 2) {
+    const int pos = rowpos[2 * r + 1];
+    if (pos >= 0 && pos < P.max_pos) {
+      const float4* rp = (const float4*)(P.rope + (int64_t)pos * 64 + ((4 * lane) & 63));
+      in.a = __ldg(rp);
+      in.b = __ldg(rp + 1);
+    }
+  }
+  return in;
+}
+
+__device__ __forceinline__ void row_apply(const ChainParams& P, int kind, int t, int r, float4 v,
+                                          float4 g, const RowIn& in, const int* rowpos,
+                                          float* rec /* [16][3] of this warp */) {
+  const int lane = threadIdx.x & 31;
+  if (kind == PH_O || kind == PH_DN) {
+    // x += v; x * g for the next norm; the row's sum of squares over the tile
+    const float4 nv = make_float4(in.a.x + v.x, in.a.y + v.y, in.a.z + v.z, in.a.w + v.w);
+    const int64_t off = (int64_t)r * P.D + t * 128 + 4 * lane;
+    *(float4*)(P.x + off) = nv;
+    *(float4*)(P.xg + off) = make_float4(nv.x * g.x, nv.y * g.y, nv.z * g.z, nv.w * g.w);
+    const float ss = warp_sum(nv.x * nv.x + nv.y * nv.y + nv.z * nv.z + nv.w * nv.w);
+    if (lane == 0) P.ssq[t * CH_ROWS + r] = ss;
+  } else if (kind == PH_GU) {
+    // columns 0..63: gate rows of the tile, 64..127: up rows
+    const float4 u = shfl_xor4(v, 16);
+    if (lane < 16) {
+      uint2 pk;
+      pk.x = pack_bf16(v.x / (1.0f + expf(-v.x)) * u.x, v.y / (1.0f + expf(-v.y)) * u.y);
+      pk.y = pack_bf16(v.z / (1.0f + expf(-v.z)) * u.z, v.w / (1.0f + expf(-v.w)) * u.w);
+      *(uint2*)(P.a + (int64_t)r * P.F + t * 64 + 4 * lane) = pk;
+    }
+  } else if (kind == PH_QKV) {
+    const int which = qkv_which(P, t);
+    const int tq = P.Hd / 128, tk = P.Gd / 128;
+    if (which < 2) {
+      if (P.qk_norm) {   // per-head RMSNorm over the tile's 128 columns
+        const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+        const float rinv = 1.0f / sqrtf(ss / (float)CH_DH + P.eps);
+        v = make_float4(v.x * rinv * g.x, v.y * rinv * g.y, v.z * rinv * g.z, v.w * rinv * g.w);
+      }
+      const int pos = rowpos[2 * r + 1];
+      if (pos < 0 || pos >= P.max_pos) {
+        if (lane == 0) atomicOr(P.status, ST_BOUNDS);
+        return;
+      }
+      // rotate-half pairs (j, j + 64): lanes 0-15 hold j, lanes 16-31 j + 64
+      const float4 o = shfl_xor4(v, 16);
+      const float sg = lane < 16 ? -1.f : 1.f;
+      const float4 c0 = in.a, c1 = in.b;   // (cos, sin) of j, j+1 | j+2, j+3
+      v = make_float4(v.x * c0.x + sg * o.x * c0.y, v.y * c0.z + sg * o.y * c0.w,
+                      v.z * c1.x + sg * o.z * c1.y, v.w * c1.z + sg * o.w * c1.w);
+    }
+    bf16* dst = which == 0 ? P.q + (int64_t)r * P.Hd + t * CH_DH
+                : which == 1 ? P.kb + (int64_t)r * P.Gd + (t - tq) * CH_DH
+                             : P.vb + (int64_t)r * P.Gd + (t - tq - tk) * CH_DH;
+    uint2 pk;
+    pk.x = pack_bf16(v.x, v.y);
+    pk.y = pack_bf16(v.z, v.w);
+    *(uint2*)(dst + 4 * lane) = pk;
+  } else {   // PH_LM: top-2 of the tile's row, folded into this warp's record
+    Top2 tt{-INFINITY, 0x7fffffff, -INFINITY};
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int n = t * 128 + 4 * lane + k;
+      if (n < P.V) tt = top2_merge(tt, Top2{vv[k], n, -INFINITY});
+    }
+    tt = top2_warp(tt);
+    if (lane == 0) {
+      Top2 cur{rec[3 * r], __float_as_int(rec[3 * r + 1]), rec[3 * r + 2]};
+      cur = top2_merge(cur, tt);
+      rec[3 * r] = cur.t1;
+      rec[3 * r + 1] = __int_as_float(cur.i1);
+      rec[3 * r + 2] = cur.t2;
+    }
+  }
+}
+
+// fp32 pair (line, col), col even, of 128-byte lines stored with the 128-byte
+// swizzle (16-byte chunk c of line l at c ^ (l & 7)).
+__device__ __forceinline__ float2 lds_x(const uint8_t* box, int line, int c) {
+  return *(const float2*)(box + line * 128 + ((((c >> 2) ^ (line & 7))) << 4) + (c & 3) * 4);
+}
+
+// One projection phase: this CTA's units [u0, u1) of the phase's
+// (tile, k-chunk) grid.  A tile whose units this CTA owns entirely is
+// finished here (row epilogues); every other tile leaves this CTA's partial
+// sum in its slot for the reduce phase.  `ri` is the ring index of the first
+// unit.  After a timed-out wait the warps skip the arithmetic but keep every
+// barrier.
+__device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int& ri,
+                           uint8_t* smem, uint32_t sbase, uint32_t bar_full, uint32_t bar_empty,
+                           volatile int* misc, const int* rowpos, float* rinv_s, float* recs) {
+  const int tid = threadIdx.x - 32, cw = tid >> 5, lane = threadIdx.x & 31;
+  const Geo geo = gemm_geo(P, kind);
+  const int64_t U = (int64_t)geo.n_tiles * geo.kc, G = P.grid;
+  const int cta = blockIdx.x;
+  const int u0 = first_unit_of(cta, U, G), u1 = first_unit_of(cta + 1, U, G);
+  if (u1 <= u0) return;
+  float* E = (float*)(smem + CH_OFF_ATT);
+  if (geo.a_f32) {
+    // rinv per row from the residual tiles' sums of squares: 8 threads per
+    // row take every 8th tile (loads in flight together), then a fixed
+    // shuffle tree adds the 8 parts
+    {
+      const int r = tid >> 3, j = tid & 7, nt = P.D / 128;
+      float s = 0.f;
+      for (int t0 = j; t0 < nt; t0 += 64) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int t = t0 + 8 * k;
+          v[k] = t < nt ? __ldcg(P.ssq + t * CH_ROWS + r) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s += v[k];
+      }
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      s += __shfl_xor_sync(0xffffffffu, s, 4);
+      if (j == 0) rinv_s[r] = r < P.R ? 1.0f / sqrtf(s / (float)P.D + P.eps) : 0.f;
+    }
+    named_bar(1, CH_CT);
+  }
+  const int g = lane >> 2, tg = lane & 3;
+  const float ri0 = geo.a_f32 ? rinv_s[g] : 0.f, ri1 = geo.a_f32 ? rinv_s[g + 8] : 0.f;
+  float acc[4][4];
+  int cur = -1, kbeg = 0, kend = 0;
+
+  auto flush = [&](int t) -> void {
+    named_bar(1, CH_CT);   // the previous tile's rows have been read out of E
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = cw * 32 + j * 8 + 2 * tg;
+      *(float2*)&E[g * CH_EPAD + col] = make_float2(acc[j][0], acc[j][1]);
+      *(float2*)&E[(g + 8) * CH_EPAD + col] = make_float2(acc[j][2], acc[j][3]);
+    }
+    named_bar(1, CH_CT);
+    if (kbeg == 0 && kend == geo.kc) {
+      // whole tile: finish its rows here (warp cw: rows cw, cw + 4, ...)
+      const float4 gt = tile_gain(P, kind, l, t);
+      RowIn in[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = cw + 4 * q;
+        in[q] = row_in(P, kind, t, r < P.R ? r : 0, rowpos);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = cw + 4 * q;
+        if (r < P.R)
+          row_apply(P, kind, t, r, *(const float4*)&E[r * CH_EPAD + 4 * lane], gt, in[q], rowpos,
+                    recs + cw * 48);
+      }
+    } else {
+      const int slot_i = (uint32_t)u0 / (uint32_t)geo.kc == (uint32_t)t ? 0 : 1;
+      float4* slot = (float4*)(P.partial + (int64_t)(2 * cta + slot_i) * (CH_ROWS * 128));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int e4 = tid + q * CH_CT, e = e4 * 4;
+        slot[e4] = *(const float4*)&E[(e >> 7) * CH_EPAD + (e & 127)];
+      }
+    }
+  };
+
+  for (int u = u0; u < u1; ++u, ++ri) {
+    const int t = u / geo.kc, kk = u - t * geo.kc;
+    if (t != cur) {
+      if (cur >= 0) flush(cur);
+      cur = t;
+      kbeg = kk;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    }
+    const int s = ri % CH_STAGES;
+    kend = kk + 1;
+    if (misc[MS_ABORT]) continue;
+    if (!__any_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (ri / CH_STAGES) & 1))) {
+      if (lane == 0) atomicOr(P.status, ST_TIMEOUT);
+      misc[MS_ABORT] = 1;
+      continue;
+    }
+    const uint32_t wb = sbase + s * CH_W;
+    const uint32_t ab = sbase + CH_OFF_A + s * CH_A;
+    const uint8_t* abox = smem + CH_OFF_A + s * CH_A;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t af[4];
+      if (geo.a_f32) {
+        // columns ks*16 + {2tg, 2tg+1, 2tg+8, 2tg+9} of the chunk: 32-column
+        // half h = ks / 2, line 2 * row + h
+        const int h = ks >> 1, c0 = (ks & 1) * 16 + 2 * tg;
+        const float2 x00 = lds_x(abox, 2 * g + h, c0), x10 = lds_x(abox, 2 * (g + 8) + h, c0);
+        const float2 x01 = lds_x(abox, 2 * g + h, c0 + 8), x11 = lds_x(abox, 2 * (g + 8) + h, c0 + 8);
+        af[0] = pack_bf16(x00.x * ri0, x00.y * ri0);
+        af[1] = pack_bf16(x10.x * ri1, x10.y * ri1);
+        af[2] = pack_bf16(x01.x * ri0, x01.y * ri0);
+        af[3] = pack_bf16(x11.x * ri1, x11.y * ri1);
+      } else {
+        const int row = lane & 15, ch = 2 * ks + (lane >> 4);
+        ldsm_x4(ab + row * 128 + ((ch ^ (row & 7)) << 4), af[0], af[1], af[2], af[3]);
+      }
+      uint32_t b[4][2];
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        const int row = cw * 32 + pp * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int ch = 2 * ks + ((lane >> 3) & 1);
+        ldsm_x4(wb + row * 128 + ((ch ^ (row & 7)) << 4), b[2 * pp][0], b[2 * pp][1],
+                b[2 * pp + 1][0], b[2 * pp + 1][1]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mma_bf16_16816(acc[j], af, b[j][0], b[j][1]);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+    if (tid == 0) misc[MS_CONSUMED] = ri + 1;
+  }
+  if (P.trace != nullptr && tid == 0)   // last CTA to finish its multiply-adds
+    atomicMax(P.trace + 4 * kChainMaxPhases + phase, (unsigned long long)globaltimer());
+  flush(cur);
+}
+
+// Reduce phase after a projection: one warp per (tile, row) of every tile
+// that several CTAs contributed to adds the contributors' partial rows in
+// CTA (= k) order, with all loads of a batch (and the epilogue's own inputs)
+// in flight together, then runs the row epilogue.
+//
+// Contributors of tile t (units t*kc .. t*kc + kc - 1): with at least one unit
+// per CTA (U >= G) they are the CTAs lo .. hi, each of which holds t in slot 0
+// (its first tile) except lo when lo began in an earlier tile (slot 1); with
+// fewer units than CTAs every unit has its own owner, holding t in slot 0.
+__device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* rowpos, float* recs) {
+  const int warp = (threadIdx.x - 32) >> 5, lane = threadIdx.x & 31;
+  const Geo geo = gemm_geo(P, kind);
+  const uint32_t U = (uint32_t)geo.n_tiles * geo.kc, G = P.grid, kc = geo.kc;
+  const int R = P.R, ntask = geo.n_tiles * R;
+  const bool dense = U >= G;
+  auto owner = [&](uint32_t u) { return (int)(((u + 1) * G + U - 1) / U) - 1; };
+  constexpr int RB = 12;   // contributors per batch
+  for (int k = blockIdx.x * 4 + warp; k < ntask; k += P.grid * 4) {
+    const int t = k / R, r = k - t * R;
+    const int lo = owner((uint32_t)t * kc), hi = owner((uint32_t)t * kc + kc - 1);
+    if (lo == hi) continue;   // finished by its only owner
+    const int n = dense ? hi - lo + 1 : (int)kc;
+    const bool lo_slot1 = dense && (uint32_t)lo * U / G < (uint32_t)t * kc;
+    const float4 gt = tile_gain(P, kind, l, t);
+    const RowIn in = row_in(P, kind, t, r, rowpos);
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < n; j0 += RB) {
+      float4 v[RB];
+#pragma unroll
+      for (int j = 0; j < RB; ++j) {
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j0 + j < n) {
+          const int c = dense ? lo + j0 + j : owner((uint32_t)t * kc + j0 + j);
+          const int slot = (dense && j0 + j == 0 && lo_slot1) ? 1 : 0;
+          v[j] = __ldcg((const float4*)(P.partial + (int64_t)(2 * c + slot) * (CH_ROWS * 128) +
+                                        r * 128) + lane);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < RB; ++j) {
+        sum.x += v[j].x;
+        sum.y += v[j].y;
+        sum.z += v[j].z;
+        sum.w += v[j].w;
+      }
+    }
+    row_apply(P, kind, t, r, sum, gt, in, rowpos, recs + warp * 48);
+  }
+}
+
+// End of the LM head: every CTA publishes its per-row record (the top-2 over
+// the vocabulary rows it finished, from its four warps' records); the last
+// CTA to do so merges the grid's records (top-2 merging is order-free, so the
+// result does not depend on which CTA finished which tile) and writes ids
+// and gaps.
+__device__ void lm_finish(const ChainParams& P, volatile int* misc, const float* recs) {
+  const int tid = threadIdx.x - 32, cw = tid >> 5, lane = threadIdx.x & 31;
+  const int R = P.R;
+  named_bar(1, CH_CT);
+  if (tid < R) {
+    Top2 m{-INFINITY, 0x7fffffff, -INFINITY};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float* rc = recs + w * 48 + 3 * tid;
+      m = top2_merge(m, Top2{rc[0], __float_as_int(rc[1]), rc[2]});
+    }
+    P.amx[(int64_t)blockIdx.x * R + tid] = make_float4(m.t1, __int_as_float(m.i1), m.t2, 0.f);
+  }
+  named_bar(1, CH_CT);
+  if (tid == 0) {
+    int* done = P.counters + kMaxTiles;
+    const int old = atom_add_acq_rel_gpu(done, 1);
+    const int last = (old == P.grid - 1);
+    if (last) *done = 0;
+    misc[MS_LAST] = last;
+  }
+  named_bar(1, CH_CT);
+  if (!misc[MS_LAST]) return;
+  // warp cw merges rows cw, cw + 4, ... two rows at a time, all of a pair's
+  // record loads in flight together
+  for (int r0 = cw; r0 < R; r0 += 8) {
+    Top2 tt[2] = {{-INFINITY, 0x7fffffff, -INFINITY}, {-INFINITY, 0x7fffffff, -INFINITY}};
+    for (int c0 = 0; c0 < P.grid; c0 += 320) {
+      float4 v[2][10];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int q = 0; q < 10; ++q) {
+          const int c = c0 + lane + 32 * q, r = r0 + 4 * h;
+          v[h][q] = (c < P.grid && r < R)
+                        ? __ldcg(&P.amx[(int64_t)c * R + r])
+                        : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY, 0.f);
+        }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int q = 0; q < 10; ++q)
+          tt[h] = top2_merge(tt[h], Top2{v[h][q].x, __float_as_int(v[h][q].y), v[h][q].z});
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = r0 + 4 * h;
+      const Top2 m = top2_warp(tt[h]);
+      if (r >= R || lane != 0) continue;
+      const int b = r / P.B, i = r - b * P.B;
+      if (i == 0) {
+        P.ids[(int64_t)b * P.B] = P.anchor[b];
+      } else {
+        P.ids[(int64_t)b * P.B + i] = m.i1;
+        if (P.gap) P.gap[(int64_t)b * (P.B - 1) + i - 1] = m.t1 - m.t2;
+      }
+    }
+  }
+}
+
+// ---- consumers: attention ----------------------------------------------------------
+// Work items: for each sequence b, the keys [0, len_b + B) in 32-key
+// sub-chunks, `chunk` sub-chunks per item; items ordered (b, g, run).
+struct Items {
+  int chunk, total;
+  int nsub[CH_MAXB], runs[CH_MAXB], base[CH_MAXB], L[CH_MAXB];
+};
+
+__device__ void make_items(const ChainParams& P, Items* it) {
+  int U = 0;
+  for (int b = 0; b < P.batch; ++b) {
+    int L = P.len[b];
+    if (L < 0 || L > P.cap) {
+      atomicOr(P.status, ST_BOUNDS);
+      L = L < 0 ? 0 : P.cap;
+    }
+    it->L[b] = L;
+    it->nsub[b] = (L + P.B + CH_AK - 1) / CH_AK;
+    U += P.G * it->nsub[b];
+  }
+  const int chunk = max(1, (U + P.grid - 1) / P.grid);
+  int n = 0;
+  for (int b = 0; b < P.batch; ++b) {
+    it->runs[b] = (it->nsub[b] + chunk - 1) / chunk;
+    it->base[b] = n;
+    n += P.G * it->runs[b];
+  }
+  it->chunk = chunk;
+  it->total = n;
+}
+
+__device__ __forceinline__ uint32_t tswz(int row, int chunk) {
+  return (uint32_t)(row * (CH_DH * 2) + ((chunk ^ (row & 7)) << 4));
+}
+
+// Trace helper: latest time over the grid for column `col` of phase `p`.
+__device__ __forceinline__ void trace_max(const ChainParams& P, int col, int p) {
+  if (P.trace != nullptr) atomicMax(P.trace + col * kChainMaxPhases + p, (unsigned long long)globaltimer());
+}
+
+__device__ void attention_phase(const ChainParams& P, int phase, int l, const Items* it, uint8_t* smem) {
+  const int tid = threadIdx.x - 32, warp = tid >> 5, lane = threadIdx.x & 31;
+  const uint32_t sQ = smem_u32(smem + CH_OFF_ATT);
+  const uint32_t sK0 = sQ + CH_ATT_Q, sV0 = sK0 + 2 * CH_ATT_KV;
+  const int QM = P.B * P.rep;
+  const int gq = lane >> 2, tg = lane & 3;
+  const bool active = warp * 16 < QM;
+  const int total = min(it->total, P.n_items_max);
+  for (int j = blockIdx.x; j < total; j += P.grid) {
+    int b = 0;
+    while (b + 1 < P.batch && j >= it->base[b + 1]) ++b;
+    const int jj = j - it->base[b];
+    const int g = jj / it->runs[b], run = jj - g * it->runs[b];
+    const int L = it->L[b], nk = L + P.B;
+    const int k_begin = run * it->chunk * CH_AK;
+    const int k_end = min(nk, k_begin + it->chunk * CH_AK);
+    const int nsub = (k_end - k_begin + CH_AK - 1) / CH_AK;
+    const bf16* kcb = P.kc[l] + ((int64_t)b * P.G + g) * P.cap * CH_DH;
+    const bf16* vcb = P.vc[l] + ((int64_t)b * P.G + g) * P.cap * CH_DH;
+    const bf16* kbb = P.kb + (int64_t)b * P.B * P.Gd + (int64_t)g * CH_DH;
+    const bf16* vbb = P.vb + (int64_t)b * P.B * P.Gd + (int64_t)g * CH_DH;
+    named_bar(1, CH_CT);   // the previous item is done with the buffers
+    // Q rows: row r = head hh of the group, block row i (r = hh * B + i)
+    for (int e = tid; e < 64 * 16; e += CH_CT) {
+      const int r = e >> 4, c = e & 15;
+      const bool ok = r < QM;
+      const int hh = ok ? r / P.B : 0, i = ok ? r - hh * P.B : 0;
+      const bf16* src = P.q + (int64_t)(b * P.B + i) * P.Hd + (int64_t)(g * P.rep + hh) * CH_DH + c * 8;
+      cp_async16(sQ + tswz(r, c), ok ? src : P.q, ok);
+    }
+    auto load_kv = [&](int k0, int stage) {
+      const uint32_t dk = sK0 + stage * CH_ATT_KV, dv = sV0 + stage * CH_ATT_KV;
+      for (int e = tid; e < CH_AK * 16; e += CH_CT) {
+        const int r = e >> 4, c = e & 15, jk = k0 + r;
+        const bool ok = jk < k_end;
+        const bf16 *ks, *vs;
+        if (jk < L) {
+          ks = kcb + (int64_t)jk * CH_DH + c * 8;
+          vs = vcb + (int64_t)jk * CH_DH + c * 8;
+        } else {
+          const int jb = ok ? jk - L : 0;
+          ks = kbb + (int64_t)jb * P.Gd + c * 8;
+          vs = vbb + (int64_t)jb * P.Gd + c * 8;
+        }
+        cp_async16(dk + tswz(r, c), ok ? ks : kcb, ok);
+        cp_async16(dv + tswz(r, c), ok ? vs : vcb, ok);
+      }
+    };
+    load_kv(k_begin, 0);
+    cp_async_commit();
+    float acc[16][4];
+#pragma unroll
+    for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+    for (int sc = 0; sc < nsub; ++sc) {
+      const int stage = sc & 1;
+      if (sc + 1 < nsub) load_kv(k_begin + (sc + 1) * CH_AK, stage ^ 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+      named_bar(1, CH_CT);
+      if (sc == 0 && tid == 0) trace_max(P, 5, phase);   // first K/V sub-chunk in
+      if (active) {
+        const uint32_t sK = sK0 + stage * CH_ATT_KV, sV = sV0 + stage * CH_ATT_KV;
+        const int kbase = k_begin + sc * CH_AK;
+        float s[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t qa[4];   // Q fragments are re-read from shared memory (registers are scarce)
+          {
+            const int row = warp * 16 + (lane & 15), ch = 2 * ks + (lane >> 4);
+            ldsm_x4(sQ + tswz(row, ch), qa[0], qa[1], qa[2], qa[3]);
+          }
+#pragma unroll
+          for (int pp = 0; pp < 2; ++pp) {
+            const int row = pp * 16 + (lane & 7) + ((lane >> 4) << 3);
+            const int ch = 2 * ks + ((lane >> 3) & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(sK + tswz(row, ch), b0, b1, b2, b3);
+            mma_bf16_16816(s[2 * pp], qa, b0, b1);
+            mma_bf16_16816(s[2 * pp + 1], qa, b2, b3);
+          }
+        }
+        float mnew[2] = {mrow[0], mrow[1]};
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int key = kbase + n * 8 + 2 * tg + (q & 1);
+            s[n][q] = key < k_end ? s[n][q] * P.scale_log2 : -INFINITY;
+            mnew[q >> 1] = fmaxf(mnew[q >> 1], s[n][q]);
+          }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          mnew[h] = fmaxf(mnew[h], __shfl_xor_sync(0xffffffffu, mnew[h], 1));
+          mnew[h] = fmaxf(mnew[h], __shfl_xor_sync(0xffffffffu, mnew[h], 2));
+        }
+        float alpha[2], lsum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) alpha[h] = mrow[h] == -INFINITY ? 0.f : exp2f(mrow[h] - mnew[h]);
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float e = exp2f(s[n][q] - mnew[q >> 1]);
+            s[n][q] = e;
+            lsum[q >> 1] += e;
+          }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          lrow[h] = lrow[h] * alpha[h] + lsum[h];
+          mrow[h] = mnew[h];
+        }
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          acc[n][0] *= alpha[0];
+          acc[n][1] *= alpha[0];
+          acc[n][2] *= alpha[1];
+          acc[n][3] *= alpha[1];
+        }
+        // O += P V with P as a bf16 (hi, lo) pair
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const float* s0 = s[2 * kk];
+          const float* s1 = s[2 * kk + 1];
+          const float v[8] = {s0[0], s0[1], s0[2], s0[3], s1[0], s1[1], s1[2], s1[3]};
+          float hi[8], lo[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            hi[q] = __bfloat162float(__float2bfloat16_rn(v[q]));
+            lo[q] = v[q] - hi[q];
+          }
+          const uint32_t ph[4] = {pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]),
+                                  pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7])};
+          const uint32_t pl[4] = {pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]),
+                                  pack_bf16(lo[4], lo[5]), pack_bf16(lo[6], lo[7])};
+#pragma unroll
+          for (int np = 0; np < 8; ++np) {
+            const int row = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int ch = np * 2 + (lane >> 4);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(sV + tswz(row, ch), b0, b1, b2, b3);
+            mma_bf16_16816(acc[2 * np], ph, b0, b1);
+            mma_bf16_16816(acc[2 * np + 1], ph, b2, b3);
+            mma_bf16_16816(acc[2 * np], pl, b0, b1);
+            mma_bf16_16816(acc[2 * np + 1], pl, b2, b3);
+          }
+        }
+      }
+      named_bar(1, CH_CT);   // stage buffers free for the load two steps ahead
+    }
+    cp_async_wait<0>();
+    if (tid == 0) trace_max(P, 6, phase);   // item's arithmetic done
+    if (active) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
+        lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
+      }
+      float* part = P.apart + (int64_t)j * 64 * CH_DP;
+      const int r0 = warp * 16 + gq, r1 = r0 + 8;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        const int col = n * 8 + 2 * tg;
+        *(float2*)&part[r0 * CH_DP + 4 + col] = make_float2(acc[n][0], acc[n][1]);
+        *(float2*)&part[r1 * CH_DP + 4 + col] = make_float2(acc[n][2], acc[n][3]);
+      }
+      if (tg == 0) {
+        part[r0 * CH_DP] = mrow[0];
+        part[r0 * CH_DP + 1] = lrow[0];
+        part[r1 * CH_DP] = mrow[1];
+        part[r1 * CH_DP + 1] = lrow[1];
+      }
+    }
+    if (tid == 0) trace_max(P, 7, phase);   // partial written (issued)
+  }
+}
+
+// Combine: one warp per (sequence, kv head, query row); lanes own 4 output
+// columns each and add the runs' contributions in run order.
+__device__ void combine_phase(const ChainParams& P, int phase, const Items* it) {
+  const int tid = threadIdx.x - 32, warp = tid >> 5, lane = threadIdx.x & 31;
+  const int QM = P.B * P.rep;
+  const int nrows = P.batch * P.G * QM;
+  for (int w = blockIdx.x * 4 + warp; w < nrows; w += P.grid * 4) {
+    const int b = w / (P.G * QM), rem = w - b * (P.G * QM);
+    const int g = rem / QM, r = rem - g * QM;
+    const int runs = it->runs[b];
+    const int j0 = it->base[b] + g * runs;
+    if (j0 + runs > P.n_items_max) continue;
+    const float* base = P.apart + ((int64_t)j0 * 64 + r) * CH_DP;
+    const int64_t stride = (int64_t)64 * CH_DP;
+    float M = -INFINITY;
+    for (int s = lane; s < runs; s += 32) M = fmaxf(M, __ldcg(base + s * stride));
+    M = warp_max(M);
+    float lt = 0.f;
+    for (int s = lane; s < runs; s += 32) {
+      const float ms = __ldcg(base + s * stride);
+      const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - M);
+      lt += __ldcg(base + s * stride + 1) * wgt;
+    }
+    lt = warp_sum(lt);
+    if (lane == 0) trace_max(P, 5, phase);   // (max, sum) of the runs in
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < runs; s0 += 8) {
+      float4 v[8];
+      float wv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int s = min(s0 + k, runs - 1);
+        v[k] = __ldcg((const float4*)(base + s * stride + 4) + lane);
+        const float ms = __ldcg(base + s * stride);
+        wv[k] = (s0 + k < runs && ms != -INFINITY) ? exp2f(ms - M) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        o.x += v[k].x * wv[k];
+        o.y += v[k].y * wv[k];
+        o.z += v[k].z * wv[k];
+        o.w += v[k].w * wv[k];
+      }
+    }
+    if (lane == 0) trace_max(P, 6, phase);   // outputs summed
+    const float iv = 1.0f / lt;
+    const int hh = r / P.B, i = r - hh * P.B;
+    bf16* dst = P.o + (int64_t)(b * P.B + i) * P.Hd + (int64_t)(g * P.rep + hh) * CH_DH + 4 * lane;
+    uint2 pk;
+    pk.x = pack_bf16(o.x * iv, o.y * iv);
+    pk.y = pack_bf16(o.z * iv, o.w * iv);
+    *(uint2*)dst = pk;
+  }
+}
+
+// Embedding of the block rows (anchor, then mask tokens) into the fp32
+// residual, with the per-(tile, row) sums of squares of the first norm.
+__device__ void embed_phase(const ChainParams& P) {
+  const int tid = threadIdx.x - 32, warp = tid >> 5, lane = threadIdx.x & 31;
+  const int tiles = P.D / 128;
+  for (int w = blockIdx.x * 4 + warp; w < P.R * tiles; w += P.grid * 4) {
+    const int r = w / tiles, t = w - r * tiles;
+    const int b = r / P.B, i = r - b * P.B;
+    const int id = i == 0 ? P.anchor[b] : P.mask_id;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (id < 0 || id >= P.V) {
+      if (lane == 0) atomicOr(P.status, ST_BOUNDS);
+    } else {
+      const uint2 raw = __ldg((const uint2*)(P.embed + (int64_t)id * P.D + t * 128) + lane);
+      const __nv_bfloat162 e0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+      const __nv_bfloat162 e1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+      v = make_float4(__low2float(e0) * P.embed_scale, __high2float(e0) * P.embed_scale,
+                      __low2float(e1) * P.embed_scale, __high2float(e1) * P.embed_scale);
+    }
+    *((float4*)(P.x + (int64_t)r * P.D + t * 128) + lane) = v;
+    const float4 g4 = __ldg((const float4*)(P.lay[0].g_in + t * 128) + lane);
+    *((float4*)(P.xg + (int64_t)r * P.D + t * 128) + lane) =
+        make_float4(v.x * g4.x, v.y * g4.y, v.z * g4.z, v.w * g4.w);
+    const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+    if (lane == 0) P.ssq[t * CH_ROWS + r] = ss;
+  }
+}
+
+__global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_constant__ ChainParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + CH_OFF_BAR, bar_empty = bar_full + 8 * CH_STAGES;
+  volatile int* misc = (volatile int*)(smem + CH_OFF_MISC);
+  int* rowpos = (int*)(smem + CH_OFF_MISC) + 16;
+  float* rinv_s = (float*)(smem + CH_OFF_MISC) + 48;
+  Items* items = (Items*)((int*)(smem + CH_OFF_MISC) + 64);
+  float* recs = (float*)(smem + CH_OFF_MISC) + 192;
+  static_assert(64 * 4 + sizeof(Items) <= 192 * 4 && (192 + 4 * 48) * 4 <= CH_MISC_BYTES, "misc area");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < CH_STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 4);
+    }
+    misc[MS_ABORT] = misc[MS_LAST] = misc[MS_ISSUED] = misc[MS_CONSUMED] = misc[MS_GO] = 0;
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) make_items(P, items);
+  if (threadIdx.x >= 32 && threadIdx.x < 32 + CH_ROWS) {
+    const int r = threadIdx.x - 32;
+    int b = -1, pos = -1;
+    if (r < P.R) {
+      b = r / P.B;
+      pos = P.len[b] + (r - b * P.B);
+    }
+    rowpos[2 * r] = b;
+    rowpos[2 * r + 1] = pos;
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    if (lane == 0) producer(P, sbase, bar_full, bar_empty, misc);
+    __syncwarp();
+  } else {
+    const int tid = threadIdx.x - 32;
+    int ri = 0;
+    for (int p = 0; p < P.n_phases; ++p) {
+      if (tid == 0) {
+        bool go = misc[MS_ABORT] == 0;
+        if (go && !grid_wait(P, p * P.grid)) {
+          misc[MS_ABORT] = 1;
+          go = false;
+        }
+        misc[MS_GO] = go;
+      }
+      named_bar(1, CH_CT);
+      if (!misc[MS_GO]) break;
+      if (P.trace != nullptr && tid == 0) {
+        const unsigned long long now = globaltimer();
+        atomicMin(P.trace + p, now);                          // first CTA to start
+        atomicMax(P.trace + kChainMaxPhases + p, now);        // last CTA to start
+      }
+      int l;
+      const int kind = phase_kind(P, p, l);
+      if (kind == PH_EMBED) {
+        embed_phase(P);
+      } else if (kind == PH_ATT) {
+        attention_phase(P, p, l, items, smem);
+      } else if (kind == PH_CMB) {
+        combine_phase(P, p, items);
+      } else if (kind == PH_RED) {
+        int lp;
+        const int pk = phase_kind(P, p - 1, lp);
+        reduce_phase(P, pk, lp, rowpos, recs);
+        if (pk == PH_LM) lm_finish(P, misc, recs);
+      } else {
+        if (kind == PH_LM) {
+          for (int e = tid; e < 4 * CH_ROWS; e += CH_CT) {
+            recs[3 * e] = -INFINITY;
+            recs[3 * e + 1] = __int_as_float(0x7fffffff);
+            recs[3 * e + 2] = -INFINITY;
+          }
+          named_bar(1, CH_CT);
+        }
+        gemm_phase(P, p, kind, l, ri, smem, sbase, bar_full, bar_empty, misc, rowpos, rinv_s, recs);
+      }
+      named_bar(1, CH_CT);
+      if (tid == 0) {
+        red_release_gpu_add(P.counters + kMaxTiles + 1, 1);
+        if (P.trace != nullptr) {
+          const unsigned long long now = globaltimer();
+          atomicMin(P.trace + 2 * kChainMaxPhases + p, now);  // first CTA to finish
+          atomicMax(P.trace + 3 * kChainMaxPhases + p, now);  // last CTA to finish
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (misc[MS_ABORT]) {
+      // wait (bounded) for weight / activation loads that were issued but not
+      // consumed, so no TMA write lands after the CTA has left
+      const int hi = misc[MS_ISSUED];
+      for (int i = misc[MS_CONSUMED]; i < hi; ++i)
+        if (!mbar_wait(bar_full + 8 * (i % CH_STAGES), (i / CH_STAGES) & 1, 20000000ull)) break;
+    }
+    __threadfence();
+    int* exitc = P.counters + kMaxTiles + 2;
+    const int old = atomicAdd(exitc, 1);
+    if (old == P.grid - 1) {
+      P.counters[kMaxTiles + 1] = 0;
+      *exitc = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+static int g_chain_occ = -1;
+
+int chain_grid(const dflash_handle* h) {
+  if (g_chain_occ < 0) {
+    int occ = 0;
+    if (cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, chain_kernel, CH_THREADS, CH_SMEM) !=
+            cudaSuccess)
+      occ = 0;
+    g_chain_occ = std::min(occ, 2);
+  }
+  return g_chain_occ * h->num_sms;
+}
+
+size_t chain_apart_bytes(const dflash_handle* h, int batch) {
+  const int grid = std::max(chain_grid(h), 2 * h->num_sms);
+  return (size_t)(grid + std::max(batch, 1) * h->cfg.n_kv_heads) * 64 * CH_DP * sizeof(float) + 256;
+}
+
+bool chain_ok(const dflash_handle* h, int batch, int B) {
+  const dflash_config& c = h->cfg;
+  const int64_t R = (int64_t)batch * B;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!al16(h->w.g_f)) return false;   // gains are read as float4 in the epilogues
+  for (int l = 0; l < c.n_layers; ++l) {
+    const dflash_layer_weights& L = h->w.layers[l];
+    if (!al16(L.g_in) || !al16(L.g_post)) return false;
+    if (c.qk_norm && (!al16(L.q_norm) || !al16(L.k_norm))) return false;
+  }
+  return h->have_maps && h->d_wmaps != nullptr && c.dtype == DFLASH_BF16 && c.head_dim == CH_DH &&
+         R >= 1 && R <= CH_ROWS && batch <= CH_MAXB && B * (c.n_heads / c.n_kv_heads) <= 64 &&
+         c.hidden % 128 == 0 && c.ffn % 64 == 0 && (c.vocab + 127) / 128 <= kMaxTiles &&
+         chain_grid(h) > 0;
+}
+
+int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
+  const dflash_config& c = h->cfg;
+  const int R = A.batch * A.B;
+  const int D = c.hidden, Hd = c.n_heads * c.head_dim, Gd = c.n_kv_heads * c.head_dim, F = c.ffn;
+  ChainParams P;
+  memset(&P, 0, sizeof(P));
+  if (!make_tmap_rows_f32(&P.map_xg, A.xg, D, R, 16) ||
+      !make_tmap_2d(&P.map_o, A.o, Hd, R, (uint64_t)Hd * 2, 64, 16) ||
+      !make_tmap_2d(&P.map_a, A.a, F, R, (uint64_t)F * 2, 64, 16))
+    return DFLASH_ERR_CUDA;
+  P.wmaps = h->d_wmaps;
+  for (int l = 0; l < c.n_layers; ++l) {
+    P.kc[l] = (const bf16*)A.kv->k[l];
+    P.vc[l] = (const bf16*)A.kv->v[l];
+    const dflash_layer_weights& L = h->w.layers[l];
+    P.lay[l] = ChainLayer{L.g_in, L.g_post, L.q_norm, L.k_norm};
+  }
+  P.embed = (const bf16*)h->w.embed;
+  P.g_f = h->w.g_f;
+  P.anchor = A.anchor;
+  P.len = A.kv->len;
+  P.ids = A.ids;
+  P.gap = A.gap;
+  P.x = A.x;
+  P.xg = A.xg;
+  P.q = (bf16*)A.q;
+  P.kb = (bf16*)A.kb;
+  P.vb = (bf16*)A.vb;
+  P.o = (bf16*)A.o;
+  P.a = (bf16*)A.a;
+  P.ssq = A.ssq;
+  P.partial = A.partial;
+  P.apart = A.apart;
+  P.amx = A.amx;
+  P.counters = h->d_counters;
+  P.status = h->d_status;
+  P.rope = h->d_rope;
+  P.max_pos = c.max_pos;
+  P.R = R;
+  P.batch = A.batch;
+  P.B = A.B;
+  P.D = D;
+  P.Hd = Hd;
+  P.Gd = Gd;
+  P.F = F;
+  P.V = c.vocab;
+  P.G = c.n_kv_heads;
+  P.rep = c.n_heads / c.n_kv_heads;
+  P.nL = c.n_layers;
+  P.cap = A.kv->cap;
+  P.mask_id = c.mask_token_id;
+  P.qk_norm = c.qk_norm;
+  P.grid = chain_grid(h);
+  if (h->d_trace != nullptr) {
+    // minima start from all-ones, maxima from zero
+    const size_t col = kChainMaxPhases * sizeof(unsigned long long);
+    if (cudaMemsetAsync(h->d_trace, 0xff, col, s) ||
+        cudaMemsetAsync(h->d_trace + kChainMaxPhases, 0, col, s) ||
+        cudaMemsetAsync(h->d_trace + 2 * kChainMaxPhases, 0xff, col, s) ||
+        cudaMemsetAsync(h->d_trace + 3 * kChainMaxPhases, 0, (kChainTraceCols - 3) * col, s))
+      return DFLASH_ERR_CUDA;
+    P.trace = h->d_trace;
+    h->trace_phases = 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 2 : 0);
+  }
+  P.n_phases = 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 2 : 0);
+  P.n_items_max = P.grid + A.batch * c.n_kv_heads;
+  P.eps = c.rms_eps;
+  P.embed_scale = c.embed_scale;
+  P.scale_log2 = 1.4426950408889634f / sqrtf((float)CH_DH);
+  if (P.grid <= 0) return DFLASH_ERR_UNSUPPORTED;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P.grid);
+  cfg.blockDim = dim3(CH_THREADS);
+  cfg.dynamicSmemBytes = CH_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  Timer t;
+  launch_begin(h, DFLASH_K_DRAFT_CHAIN, s, &t);
+  cudaLaunchKernelEx(&cfg, chain_kernel, P);
+  return launch_end(h, s, &t);
+}
+
+}  // namespace dflash

@@ -499,12 +499,15 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
             for (int q = 0; q < 4; ++q) acc[mb][j][q] = 0.f;
       }
       const int s = i % C::STAGES;
+      kend = kk + 1;
+      // after a timed-out wait (in any warp) the warps skip the arithmetic but
+      // keep walking the units, so all of them reach the same named barriers
+      if (misc[0]) continue;
       // warp-uniform: the phase is complete once any lane has seen it complete
-      const bool ok = __any_sync(0xffffffffu, misc[0] == 0 && mbar_wait(bar_full + 8 * s, (i / C::STAGES) & 1));
-      if (!ok) {
+      if (!__any_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (i / C::STAGES) & 1))) {
         if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
         misc[0] = 1;
-        break;
+        continue;
       }
       const uint32_t wb = sbase + s * C::W_BYTES;
       const uint32_t ab = sbase + C::OFF_A + s * C::A_BYTES;
@@ -533,10 +536,9 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-      kend = kk + 1;
       consumed = i + 1;
     }
-    if (cur >= 0 && !misc[0]) flush(cur);
+    if (cur >= 0) flush(cur);
     if (tid == 0) misc[3] = consumed;
   }
   __syncthreads();

@@ -259,10 +259,25 @@ enum dflash_kernel_class {
   DFLASH_K_DENSE_GEMM = 3,    /* fuse / inject / prefill projections */
   DFLASH_K_ELEMENTWISE = 4,   /* norms, embedding, RoPE, SwiGLU, bookkeeping */
   DFLASH_K_VERIFY = 5,
-  DFLASH_K_NCLASS = 6
+  DFLASH_K_DRAFT_CHAIN = 6,   /* whole draft block in one persistent launch (<= 16 rows) */
+  DFLASH_K_NCLASS = 7
 };
 int dflash_timing_enable(dflash_handle* h, int on);
 int dflash_timing_read(dflash_handle* h, int32_t kclass, double* total_ms, int64_t* launches);
+
+/* Phase timeline of the persistent draft-block kernel (class
+ * DFLASH_K_DRAFT_CHAIN).  While enabled (a small device buffer owned by the
+ * handle), each such launch records for every phase (embed; per layer q/k/v,
+ * attention, combine, o_proj, gate/up, down; LM head) eight device-clock
+ * times in ns (%globaltimer): the first and the last CTA to begin it, the
+ * first and the last CTA to finish it, the last CTA to finish its
+ * multiply-adds, and the latest split-K fix-up start, fix-up sum and
+ * epilogue end (the last three only for projection phases; 0 elsewhere).
+ * dflash_chain_trace_read synchronises the device and writes these eight
+ * values for min(n, phases) phases of the handle's latest traced launch into
+ * the host array out[8 * n]; *n_phases gets the phase count (0: none). */
+int dflash_chain_trace_enable(dflash_handle* h, int on);
+int dflash_chain_trace_read(dflash_handle* h, int64_t* out, int32_t n, int32_t* n_phases);
 
 #ifdef __cplusplus
 }

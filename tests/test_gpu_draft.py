@@ -34,19 +34,23 @@ def _oracle_ctx(kv, lens, seqs, n_layers):
     return K, V
 
 
-def _compare(w, ids, gap, hid, oids, ogap, ohid, label, o32=None):
+def _compare(w, ids, gap, hid, oids, ogap, ohid, label, o32=None, W=None):
     """fp32 path: ids bit-exact outside near-ties (oracle gap < 1e-3), floats
     within 1e-4 of the oracle.
 
     bf16 path: after N layers every value carries the rounding noise of the
     bf16 storage points before it, amplified by each RMSNorm; the oracle run
     with bf16 storage already differs from the same oracle with fp32 storage
-    by more than 2e-2 in the residual and in the logits.  So (1) ids must be
-    bit-exact at every position whose decision is not precision-sensitive in
-    the oracle itself: gap >= 1e-3 and gap >= 4x the change of that gap
-    between the oracle's bf16- and fp32-storage runs; (2) the GPU's residual
-    and gaps must be as close to the fp32-storage oracle as the bf16-storage
-    oracle is, within 25% plus 2e-2 (max) / 2e-3 (rms)."""
+    by more than 2e-2 in the residual and in the logits.  So (1) ids must
+    equal the oracle's, except that where they differ the GPU's id must be a
+    near-maximiser of the oracle's own logits: its oracle logit within
+    max(1e-3, 4 x rms) of the oracle's best, rms being the root mean square
+    change of the top-2 gap between the oracle's bf16- and fp32-storage runs
+    over the case (the logit noise the storage points cause; one position's
+    own change is a single draw of that noise and can be much smaller);
+    (2) the GPU's residual and gaps must be as close to the fp32-storage
+    oracle as the bf16-storage oracle is, within 25% plus 2e-2 (max) /
+    2e-3 (rms)."""
     if w.dtype == "f32":
         bad, near, n = id_parity(ids, oids, ogap)
         print(f"{label}: ids compared {n}, mismatches {bad}, near-ties (<{NEAR_TIE}) {near}")
@@ -58,12 +62,22 @@ def _compare(w, ids, gap, hid, oids, ogap, ohid, label, o32=None):
         return
     hid32, gap32 = o32
     g, o = np.asarray(ids)[:, 1:], np.asarray(oids)[:, 1:]
-    sens = (ogap < NEAR_TIE) | (ogap < 4 * np.abs(ogap - gap32))
-    near = int((ogap < NEAR_TIE).sum())
-    bad = int(((g != o) & ~sens).sum())
-    print(f"{label}: ids compared {int((~sens).sum())}, mismatches {bad}, near-ties (<{NEAR_TIE}) "
-          f"{near}, precision-sensitive {int(sens.sum())} (of which differing {int(((g != o) & sens).sum())})")
-    assert bad == 0
+    noise = float(np.sqrt(np.mean(np.square(ogap - gap32))))
+    tol = max(NEAR_TIE, 4.0 * noise)
+    diff = list(zip(*np.nonzero(g != o)))
+    worst = 0.0
+    for b, i in diff:
+        # the oracle's logits of this row, from its own final residual
+        hf = O.bf16(O.rmsnorm(ohid[b, i + 1][None, :], W["g_f"], w.draft.eps))
+        z = O.lm_head_logits(hf, W["lm_head"])[0]
+        deficit = float(z[o[b, i]] - z[g[b, i]])
+        worst = max(worst, deficit)
+        print(f"  differing id seq {b} pos {i + 1}: gpu {g[b, i]} (gap {gap[b, i]:.3e}), oracle "
+              f"{o[b, i]} (gap bf16 {ogap[b, i]:.3e}, fp32 {gap32[b, i]:.3e}); oracle logit "
+              f"deficit of the gpu id {deficit:.3e} vs noise bound {tol:.3e}")
+    print(f"{label}: ids {g.size}, equal {g.size - len(diff)}, differing {len(diff)} (worst oracle "
+          f"logit deficit {worst:.3e}, bound {tol:.3e} = max(1e-3, 4 x gap noise rms {noise:.3e}))")
+    assert worst <= tol
     rms = lambda a: float(np.sqrt(np.mean(np.square(a))))
     e_gpu, e_ora = float(np.abs(hid - hid32).max()), float(np.abs(ohid - hid32).max())
     r_gpu, r_ora = rms(hid - hid32), rms(ohid - hid32)
@@ -136,7 +150,7 @@ def _random_cache_case(dfl, w, B, lens, sample, weights=None):
         _, g32, h32 = O.draft_block(s, W, cK, cV, anchors[sample], B, O.f32, return_hidden=True)
         o32 = (h32, g32)
     _compare(w, ids[sample], gap[sample], hid[sample], oids, ogap, ohid,
-             f"{w.name} B={B} seqs={list(sample)}", o32)
+             f"{w.name} B={B} seqs={list(sample)}", o32, W)
     m.close()
     return weights
 
@@ -211,3 +225,63 @@ def test_lm_head_argmax_ties_and_gap(dfl, wname):
     np.testing.assert_array_equal(ids[2:][far[2:]], O.argmax_lowest(z)[2:][far[2:]])
     np.testing.assert_allclose(gap, og, atol=1e-4 if w.dtype == "f32" else 2e-3)
     m.close()
+
+
+# ---- short blocks (at most 16 rows): the single persistent launch ----------
+# A small bf16 shape that the persistent kernel accepts (head dim 128, D a
+# multiple of 128): its projections have fewer (tile, k-chunk) units than the
+# kernel has CTAs, so most CTAs own no unit of a phase.
+SMALL_BF16 = synth.Workload(
+    name="small_bf16", dtype="bf16",
+    draft=synth.DraftShape(n_layers=2, D=256, H=4, G=2, d=128, F=768, V=2048, mask_id=2047,
+                           n_target_layers=12),
+    batch=1, B=16, ctx_len=64, seed=1005)
+
+
+@pytest.mark.parametrize("B,lens", [
+    (16, [64]),                  # one sequence, 16 rows
+    (5, [37]),                   # 5 rows: a partial 16-row tile
+    (8, [0, 37]),                # two sequences, one with an empty context
+    (4, [5, 100, 0, 64]),        # four ragged sequences
+])
+def test_draft_short_block_small_bf16(dfl, B, lens):
+    _random_cache_case(dfl, SMALL_BF16, B, lens, np.arange(len(lens)))
+
+
+def test_draft_short_block_b1_batch16(dfl):
+    """16 sequences of block size 1: the block is the anchors; the final
+    residual still matches the oracle and the ids are the anchors."""
+    from synth.gpu import draft_model, kv_cache
+    w, s = SMALL_BF16, SMALL_BF16.draft
+    lens = [int(x) for x in np.random.default_rng(5).integers(0, 70, 16)]
+    weights = synth.draft_weights(s, w.dtype, w.seed, device="cuda")
+    K, V = synth.random_kv_cache(16, s.G, 70, s.d, s.n_layers, 0.02 * np.sqrt(s.D), w.dtype,
+                                 w.seed, device="cuda")
+    kv = kv_cache(s, 16, 70, w.dtype, k=K, v=V)
+    kv.len.copy_(torch.tensor(lens, dtype=torch.int32))
+    m = draft_model(s, w.dtype, weights, max_pos=128)
+    anchors = synth.anchors(16, s.V, s.mask_id, w.seed)
+    ids, _, hid = _gpu_draft(dfl, m, anchors, 16, 1, kv, s.D)
+    np.testing.assert_array_equal(ids[:, 0], anchors)
+    W = to_np(weights)
+    cK, cV = _oracle_ctx(kv, lens, range(16), s.n_layers)
+    _, _, ohid = O.draft_block(s, W, cK, cV, anchors, 1, O.storage(w.dtype), return_hidden=True)
+    _, _, h32 = O.draft_block(s, W, cK, cV, anchors, 1, O.f32, return_hidden=True)
+    e_gpu, e_ora = float(np.abs(hid - h32).max()), float(np.abs(ohid - h32).max())
+    print(f"B=1 x 16: residual |gpu-fp32 oracle| {e_gpu:.3e} vs |bf16-fp32 oracle| {e_ora:.3e}")
+    assert np.isfinite(hid).all() and e_gpu <= 1.25 * e_ora + 2e-2
+    m.close()
+
+
+def test_draft_qwen3_8b_two_sequences(dfl):
+    """Qwen3-8B-shaped draft, two sequences of 8 rows (16 rows: one launch)
+    with contexts of 2048 and 300."""
+    w = synth.WORKLOADS["qwen3_8b_b1"]
+    _random_cache_case(dfl, w, 8, [2048, 300], np.array([0, 1]))
+
+
+def test_draft_qwen3_8b_batch2_rows32(dfl):
+    """32 rows: above the persistent kernel's limit, the per-projection
+    streaming launches run."""
+    w = synth.WORKLOADS["qwen3_8b_b1"]
+    _random_cache_case(dfl, w, 16, [1500, 2048], np.array([0, 1]))
