@@ -45,7 +45,7 @@ namespace dflash {
 using namespace ptx;
 
 #ifndef DFLASH_CH_STAGES
-#define DFLASH_CH_STAGES 3
+#define DFLASH_CH_STAGES 5
 #endif
 // weight units a CTA prefetches into L2 beyond its shared-memory ring (0:
 // none; measured on the Qwen3-8B-shaped block, 4 and 8 were slower: the
@@ -66,17 +66,22 @@ constexpr int CH_EPAD = 132;               // fp32 tile row pitch in shared memo
 constexpr int CH_ROWS = 16;                // rows of the block (all sequences)
 constexpr int CH_MAXB = 16;                // sequences
 
-// shared memory layout (offsets from a 1024-aligned base)
+// shared memory layout (offsets from a 1024-aligned base).  The attention
+// phases use the ring's memory: the producer loads no weight unit of a phase
+// after attention(l) until this CTA has finished attention(l), and every
+// earlier ring entry has been consumed before attention(l) starts.
 constexpr int CH_OFF_A = CH_STAGES * CH_W;
-constexpr int CH_OFF_ATT = CH_OFF_A + CH_STAGES * CH_A;
+constexpr int CH_RING_BYTES = CH_OFF_A + CH_STAGES * CH_A;
+constexpr int CH_OFF_ATT = 0;
 constexpr int CH_ATT_Q = 64 * CH_DH * 2;              // 64 query rows
 constexpr int CH_ATT_KV = CH_AK * CH_DH * 2;          // one K (or V) sub-chunk
 constexpr int CH_ATT_BYTES = CH_ATT_Q + 4 * CH_ATT_KV; // Q + 2 stages x (K, V)
-constexpr int CH_OFF_BAR = CH_OFF_ATT + CH_ATT_BYTES;
+constexpr int CH_OFF_E = CH_RING_BYTES;               // fp32 output tile [16][CH_EPAD]
+constexpr int CH_OFF_BAR = CH_OFF_E + CH_ROWS * CH_EPAD * 4;
 constexpr int CH_OFF_MISC = CH_OFF_BAR + 2 * CH_STAGES * 8;
 constexpr int CH_MISC_BYTES = 2048;
 constexpr int CH_SMEM = CH_OFF_MISC + CH_MISC_BYTES + 1024;
-static_assert(CH_ROWS * CH_EPAD * 4 <= CH_ATT_BYTES, "the fp32 tile aliases the attention buffers");
+static_assert(CH_ATT_BYTES <= CH_RING_BYTES, "the attention buffers alias the ring");
 static_assert(CH_SMEM <= 233472 / 2 - 1024, "two CTAs per SM");
 
 enum ChainPhase : int { PH_EMBED, PH_QKV, PH_ATT, PH_CMB, PH_O, PH_GU, PH_DN, PH_LM, PH_RED };
@@ -132,7 +137,9 @@ static_assert(sizeof(ChainParams) <= 4096, "kernel parameters must fit the 4 KB 
 // MS_ABORT may be set by any thread at any time; MS_GO and MS_LAST are
 // written by consumer thread 0 only between two consumer barriers, so every
 // consumer warp reads the same value and takes the same barriers.
-enum : int { MS_ABORT = 0, MS_LAST = 1, MS_ISSUED = 2, MS_CONSUMED = 3, MS_GO = 4 };
+// MS_ATT_DONE: layers whose attention phase this CTA has finished (written by
+// consumer thread 0, read by the producer).
+enum : int { MS_ABORT = 0, MS_LAST = 1, MS_ISSUED = 2, MS_CONSUMED = 3, MS_GO = 4, MS_ATT_DONE = 5 };
 // [0, 16) ints: flags; [16, 48): rowpos (sequence, position) per row;
 // [48, 64): rinv per row; [64, 192): attention item tables; [192, 384):
 // LM-head top-2 records, [4 warps][16 rows][3]
@@ -313,7 +320,13 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
   bool abort = false;
   while (a_more) {
     bool prog = false;
-    if (w_more && !abort) {
+    // ring memory doubles as the attention buffers: a weight unit may be
+    // loaded only once this CTA has finished every attention phase before
+    // the unit's phase (q/k/v(l) follows attention(l-1); o_proj(l) onward
+    // follows attention(l); the LM head follows them all)
+    const int att_need = w.kind == PH_QKV ? w.l : w.kind == PH_LM ? P.nL : w.l + 1;
+    const bool w_held = w_more && misc[MS_ATT_DONE] < att_need;
+    if (w_more && !abort && !w_held) {
       const int s = w.i % CH_STAGES, use = w.i / CH_STAGES;
       // with no activation load owed, block in the barrier wait instead of spinning
       if (use == 0 || (a.i == w.i ? mbar_try_wait(bar_empty + 8 * s, (use - 1) & 1)
@@ -349,6 +362,7 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
       continue;
     }
     if (abort) break;   // nothing left that can complete
+    if (w_held && a.i == w.i) __nanosleep(256);   // attention is running: stay off the issue slots
     if (misc[MS_ABORT] || (*(volatile int*)P.status & ST_TIMEOUT)) {
       abort = true;     // stop loading weights; finish the activation loads already owed
       continue;
@@ -532,7 +546,7 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
   const int cta = blockIdx.x;
   const int u0 = first_unit_of(cta, U, G), u1 = first_unit_of(cta + 1, U, G);
   if (u1 <= u0) return;
-  float* E = (float*)(smem + CH_OFF_ATT);
+  float* E = (float*)(smem + CH_OFF_E);
   if (geo.a_f32) {
     // rinv per row from the residual tiles' sums of squares: 8 threads per
     // row take every 8th tile (loads in flight together), then a fixed
@@ -989,58 +1003,63 @@ __device__ void attention_phase(const ChainParams& P, int phase, int l, const It
   }
 }
 
-// Combine: one warp per (sequence, kv head, query row); lanes own 4 output
-// columns each and add the runs' contributions in run order.
+// Combine: two warps per (sequence, kv head, query row), each owning 64 of
+// the row's 128 output columns (two per lane).  The runs' (max, sum) pairs
+// come in one batch of loads, the runs' outputs in batches of 32 runs; the
+// runs are added in run order.
 __device__ void combine_phase(const ChainParams& P, int phase, const Items* it) {
   const int tid = threadIdx.x - 32, warp = tid >> 5, lane = threadIdx.x & 31;
   const int QM = P.B * P.rep;
-  const int nrows = P.batch * P.G * QM;
-  for (int w = blockIdx.x * 4 + warp; w < nrows; w += P.grid * 4) {
-    const int b = w / (P.G * QM), rem = w - b * (P.G * QM);
+  const int ntask = 2 * P.batch * P.G * QM;
+  const int64_t stride = (int64_t)64 * CH_DP;
+  for (int w = blockIdx.x * 4 + warp; w < ntask; w += P.grid * 4) {
+    const int half = w & 1, row = w >> 1;
+    const int b = row / (P.G * QM), rem = row - b * (P.G * QM);
     const int g = rem / QM, r = rem - g * QM;
     const int runs = it->runs[b];
     const int j0 = it->base[b] + g * runs;
     if (j0 + runs > P.n_items_max) continue;
     const float* base = P.apart + ((int64_t)j0 * 64 + r) * CH_DP;
-    const int64_t stride = (int64_t)64 * CH_DP;
-    float M = -INFINITY;
-    for (int s = lane; s < runs; s += 32) M = fmaxf(M, __ldcg(base + s * stride));
+    // (max, sum) of runs lane and lane + 32 stay in registers (at most 64
+    // runs); longer lists re-read theirs per group of 32
+    float2 ml0 = make_float2(-INFINITY, 0.f), ml1 = make_float2(-INFINITY, 0.f);
+    if (lane < runs) ml0 = __ldcg((const float2*)(base + lane * stride));
+    if (lane + 32 < runs) ml1 = __ldcg((const float2*)(base + (lane + 32) * stride));
+    float M = fmaxf(ml0.x, ml1.x);
+    for (int s0 = 64; s0 < runs; s0 += 32)
+      if (s0 + lane < runs) M = fmaxf(M, __ldcg(base + (s0 + lane) * stride));
     M = warp_max(M);
-    float lt = 0.f;
-    for (int s = lane; s < runs; s += 32) {
-      const float ms = __ldcg(base + s * stride);
-      const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - M);
-      lt += __ldcg(base + s * stride + 1) * wgt;
+    const float w0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - M);
+    const float w1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
+    float lt = ml0.y * w0 + ml1.y * w1;
+    float2 o = make_float2(0.f, 0.f);
+    for (int s0 = 0; s0 < runs; s0 += 32) {
+      float wl = s0 == 0 ? w0 : w1;
+      if (s0 >= 64) {
+        const float2 ml = s0 + lane < runs ? __ldcg((const float2*)(base + (s0 + lane) * stride))
+                                           : make_float2(-INFINITY, 0.f);
+        wl = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+        lt += ml.y * wl;
+      }
+      float2 v[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        v[k] = s0 + k < runs ? __ldcg((const float2*)(base + (s0 + k) * stride + 4 + half * 64) + lane)
+                             : make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, wl, k);
+        o.x += v[k].x * wk;
+        o.y += v[k].y * wk;
+      }
     }
     lt = warp_sum(lt);
-    if (lane == 0) trace_max(P, 5, phase);   // (max, sum) of the runs in
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < runs; s0 += 8) {
-      float4 v[8];
-      float wv[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int s = min(s0 + k, runs - 1);
-        v[k] = __ldcg((const float4*)(base + s * stride + 4) + lane);
-        const float ms = __ldcg(base + s * stride);
-        wv[k] = (s0 + k < runs && ms != -INFINITY) ? exp2f(ms - M) : 0.f;
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        o.x += v[k].x * wv[k];
-        o.y += v[k].y * wv[k];
-        o.z += v[k].z * wv[k];
-        o.w += v[k].w * wv[k];
-      }
-    }
-    if (lane == 0) trace_max(P, 6, phase);   // outputs summed
+    if (lane == 0) trace_max(P, 5, phase);   // weights and outputs in
     const float iv = 1.0f / lt;
     const int hh = r / P.B, i = r - hh * P.B;
-    bf16* dst = P.o + (int64_t)(b * P.B + i) * P.Hd + (int64_t)(g * P.rep + hh) * CH_DH + 4 * lane;
-    uint2 pk;
-    pk.x = pack_bf16(o.x * iv, o.y * iv);
-    pk.y = pack_bf16(o.z * iv, o.w * iv);
-    *(uint2*)dst = pk;
+    bf16* dst = P.o + (int64_t)(b * P.B + i) * P.Hd + (int64_t)(g * P.rep + hh) * CH_DH +
+                half * 64 + 2 * lane;
+    *(uint32_t*)dst = pack_bf16(o.x * iv, o.y * iv);
   }
 }
 
@@ -1091,6 +1110,7 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
       mbar_init(bar_empty + 8 * s, 4);
     }
     misc[MS_ABORT] = misc[MS_LAST] = misc[MS_ISSUED] = misc[MS_CONSUMED] = misc[MS_GO] = 0;
+    misc[MS_ATT_DONE] = 0;
     fence_barrier_init();
   }
   if (threadIdx.x == 32) make_items(P, items);
@@ -1134,6 +1154,8 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
         embed_phase(P);
       } else if (kind == PH_ATT) {
         attention_phase(P, p, l, items, smem);
+        named_bar(1, CH_CT);   // every warp is done with the ring memory
+        if (tid == 0) misc[MS_ATT_DONE] = l + 1;
       } else if (kind == PH_CMB) {
         combine_phase(P, p, items);
       } else if (kind == PH_RED) {
