@@ -88,6 +88,8 @@ _sig = {
     "dflash_chain_trace_enable": (C.c_int, [_P, C.c_int]),
     "dflash_chain_trace_read": (C.c_int, [_P, C.POINTER(C.c_int64), C.c_int32,
                                           C.POINTER(C.c_int32)]),
+    "dflash_chain_trace_events": (C.c_int, [_P, C.POINTER(C.c_int64), C.c_int64,
+                                            C.POINTER(C.c_int64)]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -237,6 +239,22 @@ def dflash_chain_trace_read(h: int, n: int = 128):
     np_ = C.c_int32()
     _check(_lib.dflash_chain_trace_read(h, buf, n, C.byref(np_)), "dflash_chain_trace_read")
     return [tuple(buf[k * i: k * i + k]) for i in range(min(np_.value, n))]
+
+
+EV_CTAS, EV_PHASES, EV_UNITS = 4, 164, 12
+EV_SLOTS = 2 + 4 * EV_UNITS
+
+
+def dflash_chain_trace_events(h: int):
+    """Raw event log [EV_CTAS][EV_PHASES][EV_SLOTS] (SM cycles, comparable
+    within one CTA) of the latest traced launch (zeros unless the library was
+    built with -DDFLASH_CH_EVLOG=1)."""
+    n = EV_CTAS * EV_PHASES * EV_SLOTS
+    buf = (C.c_int64 * n)()
+    cnt = C.c_int64()
+    _check(_lib.dflash_chain_trace_events(h, buf, n, C.byref(cnt)), "dflash_chain_trace_events")
+    return [[list(buf[(c * EV_PHASES + p) * EV_SLOTS:(c * EV_PHASES + p + 1) * EV_SLOTS])
+             for p in range(EV_PHASES)] for c in range(EV_CTAS)]
 
 
 # ---------------------------------------------------------------------------

@@ -114,7 +114,7 @@ static bool carve_forward(const dflash_handle* h, int64_t R, void* ws, size_t ws
   Carve cv{(char*)ws, ws_bytes};
   f->partial = cv.take<float>(ws_partial_bytes(h) / sizeof(float));
   f->attn = batch > 0 ? cv.take<float>(attn_region_bytes(h, batch, B) / sizeof(float)) : nullptr;
-  f->ssq = cv.take<float>((size_t)(h->cfg.hidden / 128 + 1) * 16);
+  f->ssq = cv.take<float>((size_t)(h->cfg.hidden / 128 + 1) * 16 * 8);
   f->amx = cv.take<float4>(ws_amx_bytes(h, R) / sizeof(float4));
   f->a = cv.take<char>(R * F * sz);
   f->x = cv.take<float>(R * D);
@@ -597,7 +597,7 @@ size_t dflash_workspace_bytes(const dflash_handle* h, int32_t max_batch, int32_t
   const int64_t R = std::max<int64_t>({(int64_t)max_batch * max_block, max_rows, 1});
   // a forward pass over R rows, or fuse / inject in full kChunkRows passes
   const size_t scratch = ws_partial_bytes(h) + ws_amx_bytes(h, R) + 1024 +
-                         round256((size_t)(h->cfg.hidden / 128 + 1) * 16 * sizeof(float)) +
+                         round256((size_t)(h->cfg.hidden / 128 + 1) * 16 * 8 * sizeof(float)) +
                          (max_batch > 0 && max_block > 0
                               ? attn_region_bytes(h, max_batch, max_block) : 0);
   const size_t fwd = forward_bytes(h->cfg, R);
@@ -998,8 +998,8 @@ int dflash_timing_read(dflash_handle* h, int32_t kclass, double* total_ms, int64
 int dflash_chain_trace_enable(dflash_handle* h, int on) {
   if (!h) return DFLASH_ERR_INVALID_ARG;
   if (on && !h->d_trace) {
-    if (cudaMalloc(&h->d_trace, kChainTraceCols * kChainMaxPhases * sizeof(unsigned long long)) !=
-        cudaSuccess) {
+    if (cudaMalloc(&h->d_trace, (kChainTraceCols * kChainMaxPhases + kEvWords) *
+                                    sizeof(unsigned long long)) != cudaSuccess) {
       h->d_trace = nullptr;
       return DFLASH_ERR_CUDA;
     }
@@ -1028,6 +1028,19 @@ int dflash_chain_trace_read(dflash_handle* h, int64_t* out, int32_t n, int32_t* 
       out[kChainTraceCols * p + k] = v == ~0ull ? 0 : (int64_t)v;
     }
   *n_phases = np;
+  return DFLASH_OK;
+}
+
+int dflash_chain_trace_events(dflash_handle* h, int64_t* out, int64_t n, int64_t* count) {
+  if (!h || !count || n < 0 || (n > 0 && !out)) return DFLASH_ERR_INVALID_ARG;
+  *count = 0;
+  if (!h->d_trace || h->trace_phases == 0) return DFLASH_OK;
+  const int64_t m = std::min<int64_t>(n, (int64_t)kEvWords);
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(out, h->d_trace + kChainTraceCols * kChainMaxPhases, m * sizeof(int64_t),
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DFLASH_ERR_CUDA;
+  *count = m;
   return DFLASH_OK;
 }
 

@@ -110,16 +110,22 @@ struct LayerMaps {
   CUtensorMap tq, tk, tv, to, tg, tu, td;
 };
 constexpr int kMaxTiles = 8192;   // 128-row weight tiles per projection launch
-// d_counters: [0, kMaxTiles) tile arrival counters, then the LM-head merge
-// counter, the persistent kernel's grid barrier and its exit counter
+// d_counters: [0, kMaxTiles) tile arrival counters, then the streaming
+// kernel's LM-head merge counter and the persistent kernel's grid barrier
 constexpr int kCounters = kMaxTiles + 4;
 // phases of the persistent draft-block kernel: embed, 10 per layer, LM head
 // and its reduce
-constexpr int kChainMaxPhases = 3 + 10 * DFLASH_MAX_LAYERS;
+constexpr int kChainMaxPhases = 4 + 10 * DFLASH_MAX_LAYERS;
 // timeline columns per phase: first start, last start, first end, last end,
 // last CTA done with its multiply-adds, and for the split-K fix-ups (the CTA
 // that completes a tile): latest fix-up start, sum done, epilogue done
 constexpr int kChainTraceCols = 8;
+// per-CTA event log of the persistent kernel (compiled in with
+// -DDFLASH_CH_EVLOG=1): kEvCtas sampled CTAs x kChainMaxPhases phases x
+// kEvSlots times (ns): 0 start, 1 end, 2.. unit k ready, .. unit k done,
+// .. weight load k issued, .. activation load k issued (k < kEvUnits)
+constexpr int kEvCtas = 4, kEvUnits = 12, kEvSlots = 2 + 4 * kEvUnits;
+constexpr size_t kEvWords = (size_t)kEvCtas * kChainMaxPhases * kEvSlots;
 }  // namespace dflash
 
 struct dflash_handle {
@@ -238,7 +244,7 @@ struct ChainArgs {
   float* x;                     // [R, D] fp32 residual
   float* xg;                    // [R, D] fp32 residual times the next RMSNorm gain
   void *q, *kb, *vb, *o, *a;    // bf16 [R, H*d], [R, G*d] x 2, [R, H*d], [R, F]
-  float* ssq;                   // [D / 128, 16]
+  float* ssq;                   // [D / 128, 16] sums of squares, 8 floats apart
   float* partial;               // split-K fix-up tiles
   float* apart;                 // attention run partials (chain_apart_bytes)
   float4* amx;                  // LM-head top-2 records

@@ -47,11 +47,9 @@ using namespace ptx;
 #ifndef DFLASH_CH_STAGES
 #define DFLASH_CH_STAGES 5
 #endif
-// weight units a CTA prefetches into L2 beyond its shared-memory ring (0:
-// none; measured on the Qwen3-8B-shaped block, 4 and 8 were slower: the
-// prefetched lines compete with the demand stream)
-#ifndef DFLASH_CH_PF
-#define DFLASH_CH_PF 0
+// pause of the producer lane between polls when nothing can be issued (ns)
+#ifndef DFLASH_CH_IDLE_NS
+#define DFLASH_CH_IDLE_NS 64
 #endif
 
 constexpr int CH_THREADS = 160;            // warp 0: TMA producer; warps 1-4: consumers
@@ -65,6 +63,12 @@ constexpr int CH_DP = CH_DH + 4;           // attention partial row: max, sum, 2
 constexpr int CH_EPAD = 132;               // fp32 tile row pitch in shared memory
 constexpr int CH_ROWS = 16;                // rows of the block (all sequences)
 constexpr int CH_MAXB = 16;                // sequences
+// floats between consecutive sums of squares: each (tile, row) value is
+// written by a different warp, so each gets a 32-byte sector of its own
+#ifndef DFLASH_CH_SSQ_STRIDE
+#define DFLASH_CH_SSQ_STRIDE 8
+#endif
+constexpr int CH_SSQ = DFLASH_CH_SSQ_STRIDE;
 
 // shared memory layout (offsets from a 1024-aligned base).  The attention
 // phases use the ring's memory: the producer loads no weight unit of a phase
@@ -84,7 +88,7 @@ constexpr int CH_SMEM = CH_OFF_MISC + CH_MISC_BYTES + 1024;
 static_assert(CH_ATT_BYTES <= CH_RING_BYTES, "the attention buffers alias the ring");
 static_assert(CH_SMEM <= 233472 / 2 - 1024, "two CTAs per SM");
 
-enum ChainPhase : int { PH_EMBED, PH_QKV, PH_ATT, PH_CMB, PH_O, PH_GU, PH_DN, PH_LM, PH_RED };
+enum ChainPhase : int { PH_EMBED, PH_QKV, PH_ATT, PH_CMB, PH_O, PH_GU, PH_DN, PH_LM, PH_RED, PH_LMFIN };
 // phases of one layer; every projection is followed by its reduce phase
 constexpr int kLayerPhases = 10;
 __device__ __constant__ const int kLayerSeq[kLayerPhases] = {PH_QKV, PH_RED, PH_ATT, PH_CMB, PH_O,
@@ -118,11 +122,11 @@ struct ChainParams {
   bf16* vb;
   bf16* o;
   bf16* a;
-  float* ssq;                 // [D / 128][16]
+  float* ssq;                 // [D / 128][16] rows, CH_SSQ floats apart
   float* partial;             // split-K fix-up: [2 * grid][16 * 128]
   float* apart;               // attention items: [n_items_max][64][CH_DP]
   float4* amx;                // LM-head top-2 records: [vocab tiles][R]
-  int* counters;              // tile counters; amx_done, barrier, exit at kMaxTiles + 0..2
+  int* counters;              // grid barrier at kMaxTiles + 1
   int* status;
   unsigned long long* trace;  // optional: kChainTraceCols arrays of [kChainMaxPhases] (ns)
   const float2* rope;
@@ -144,7 +148,8 @@ enum : int { MS_ABORT = 0, MS_LAST = 1, MS_ISSUED = 2, MS_CONSUMED = 3, MS_GO = 
 // [48, 64): rinv per row; [64, 192): attention item tables; [192, 384):
 // LM-head top-2 records, [4 warps][16 rows][3]
 
-// Phase p: 0 embed; then kLayerPhases per layer; then LM head and its reduce.
+// Phase p: 0 embed; then kLayerPhases per layer; then the LM head, its
+// reduce (which also publishes each CTA's top-2 records) and the final merge.
 __device__ __forceinline__ int phase_kind(const ChainParams& P, int p, int& l) {
   if (p == 0) {
     l = 0;
@@ -154,7 +159,8 @@ __device__ __forceinline__ int phase_kind(const ChainParams& P, int p, int& l) {
   l = q / kLayerPhases;
   if (l >= P.nL) {
     l = P.nL;
-    return q - P.nL * kLayerPhases == 0 ? PH_LM : PH_RED;
+    const int k = q - P.nL * kLayerPhases;
+    return k == 0 ? PH_LM : k == 1 ? PH_RED : PH_LMFIN;
   }
   return kLayerSeq[q % kLayerPhases];
 }
@@ -182,6 +188,26 @@ __device__ __forceinline__ int owner_of(int64_t u, int64_t U, int64_t G) {
   return (int)(((u + 1) * G + U - 1) / U) - 1;
 }
 
+// Trace helper: latest time over the grid for column `col` of phase `p`.
+__device__ __forceinline__ void trace_max(const ChainParams& P, int col, int p) {
+  if (P.trace != nullptr) atomicMax(P.trace + col * kChainMaxPhases + p, (unsigned long long)globaltimer());
+}
+
+#ifndef DFLASH_CH_EVLOG
+#define DFLASH_CH_EVLOG 0
+#endif
+// Event log of sampled CTAs (every grid/4-th), compiled in on request only.
+// Times are the SM's cycle counter (exact within one CTA; %globaltimer ticks
+// too coarsely for sub-microsecond steps), so compare events of one CTA only.
+__device__ __forceinline__ void ev(const ChainParams& P, int p, int slot) {
+  if (DFLASH_CH_EVLOG && P.trace != nullptr) {
+    const int q = P.grid / kEvCtas;
+    if (q > 0 && blockIdx.x % q == 0 && blockIdx.x / q < kEvCtas && slot < kEvSlots)
+      P.trace[(size_t)kChainTraceCols * kChainMaxPhases +
+              ((size_t)(blockIdx.x / q) * kChainMaxPhases + p) * kEvSlots + slot] = clock64();
+  }
+}
+
 // ---- grid barrier ----------------------------------------------------------
 // Phase p may start once every CTA has arrived p times.  Gives up (and flags
 // ST_TIMEOUT) after the wall-clock limit or as soon as another CTA has.
@@ -207,8 +233,39 @@ __device__ bool grid_wait(const ChainParams& P, int target) {
 // cursor that follows it once the unit's phase has passed its barrier.
 struct Cursor {
   int p, kind, l, u, u1, kc, a_f32;
-  int i;   // ring index
+  int i;        // ring index
+  int t, kk;    // tile and k-chunk of unit u
+  const CUtensorMap* wm0;   // weight box(es) of tile t (gate / up: two)
+  const CUtensorMap* wm1;
+  int wrow;     // row coordinate of tile t in its weight
 };
+
+// Weight map(s) and row of the cursor's tile.
+__device__ __forceinline__ void cursor_tile(const ChainParams& P, Cursor& c) {
+  c.wm1 = nullptr;
+  if (c.kind == PH_LM) {
+    c.wm0 = P.wmaps + P.nL * 7;
+    c.wrow = c.t * 128;
+    return;
+  }
+  const CUtensorMap* L = P.wmaps + c.l * 7;
+  switch (c.kind) {
+    case PH_QKV: {
+      const int tq = P.Hd / 128, tk = P.Gd / 128;
+      const int w = c.t < tq ? 0 : c.t < tq + tk ? 1 : 2;
+      c.wm0 = L + w;
+      c.wrow = (c.t - (w == 0 ? 0 : w == 1 ? tq : tq + tk)) * 128;
+      break;
+    }
+    case PH_O: c.wm0 = L + 3; c.wrow = c.t * 128; break;
+    case PH_GU:
+      c.wm0 = L + 4;
+      c.wm1 = L + 5;
+      c.wrow = c.t * 64;
+      break;
+    default: c.wm0 = L + 6; c.wrow = c.t * 128; break;   // PH_DN
+  }
+}
 
 __device__ __forceinline__ bool cursor_phase(const ChainParams& P, Cursor& c, int p) {
   for (; p < P.n_phases; ++p) {
@@ -226,6 +283,9 @@ __device__ __forceinline__ bool cursor_phase(const ChainParams& P, Cursor& c, in
     c.u1 = u1;
     c.kc = g.kc;
     c.a_f32 = g.a_f32;
+    c.t = u0 / g.kc;
+    c.kk = u0 - c.t * g.kc;
+    cursor_tile(P, c);
     return true;
   }
   c.p = P.n_phases;
@@ -233,67 +293,25 @@ __device__ __forceinline__ bool cursor_phase(const ChainParams& P, Cursor& c, in
 }
 __device__ __forceinline__ bool cursor_next(const ChainParams& P, Cursor& c) {
   ++c.i;
-  if (++c.u < c.u1) return true;
-  return cursor_phase(P, c, c.p + 1);
-}
-
-// Weight box(es) of unit c: (map, inner coordinate, row coordinate); GU has two.
-struct WBox {
-  const CUtensorMap* m[2];
-  int c0, r[2], n;
-};
-__device__ __forceinline__ WBox wbox(const ChainParams& P, const Cursor& c) {
-  const int t = c.u / c.kc, kk = c.u - t * c.kc;
-  WBox b;
-  b.c0 = kk * 64;
-  b.n = 1;
-  if (c.kind == PH_LM) {
-    b.m[0] = P.wmaps + P.nL * 7;
-    b.r[0] = t * 128;
-    return b;
+  if (++c.u >= c.u1) return cursor_phase(P, c, c.p + 1);
+  if (++c.kk == c.kc) {
+    c.kk = 0;
+    ++c.t;
+    cursor_tile(P, c);
   }
-  const CUtensorMap* L = P.wmaps + c.l * 7;
-  switch (c.kind) {
-    case PH_QKV: {
-      const int tq = P.Hd / 128, tk = P.Gd / 128;
-      const int w = t < tq ? 0 : t < tq + tk ? 1 : 2;
-      b.m[0] = L + w;
-      b.r[0] = (t - (w == 0 ? 0 : w == 1 ? tq : tq + tk)) * 128;
-      break;
-    }
-    case PH_O: b.m[0] = L + 3; b.r[0] = t * 128; break;
-    case PH_GU:
-      b.m[0] = L + 4;
-      b.m[1] = L + 5;
-      b.r[0] = b.r[1] = t * 64;
-      b.n = 2;
-      break;
-    default: b.m[0] = L + 6; b.r[0] = t * 128; break;   // PH_DN
-  }
-  return b;
+  return true;
 }
 
-__device__ void issue_w(const ChainParams& P, const Cursor& c, uint32_t dst, uint32_t bar,
-                        uint64_t pol) {
-  const WBox b = wbox(P, c);
-  tma_load_2d(dst, b.m[0], bar, b.c0, b.r[0], pol);
-  if (b.n == 2) tma_load_2d(dst + CH_W / 2, b.m[1], bar, b.c0, b.r[1], pol);
+__device__ __forceinline__ void issue_w(const ChainParams& P, const Cursor& c, uint32_t dst,
+                                        uint32_t bar, uint64_t pol) {
+  tma_load_2d(dst, c.wm0, bar, c.kk * 64, c.wrow, pol);
+  if (c.wm1 != nullptr) tma_load_2d(dst + CH_W / 2, c.wm1, bar, c.kk * 64, c.wrow, pol);
 }
 
-__device__ void prefetch_w(const ChainParams& P, const Cursor& c) {
-  const WBox b = wbox(P, c);
-  tma_prefetch_2d(b.m[0], b.c0, b.r[0]);
-  if (b.n == 2) tma_prefetch_2d(b.m[1], b.c0, b.r[1]);
-}
-
-__device__ void issue_a(const ChainParams& P, const Cursor& c, uint32_t dst, uint32_t bar,
-                        uint64_t pol) {
-  const int kk = c.u % c.kc;
-  if (c.a_f32) {
-    tma_load_3d(dst, &P.map_xg, bar, 0, kk * 2, 0, pol);
-  } else {
-    tma_load_2d(dst, c.kind == PH_O ? &P.map_o : &P.map_a, bar, kk * 64, 0, pol);
-  }
+__device__ __forceinline__ void issue_a(const ChainParams& P, const Cursor& c, uint32_t dst,
+                                        uint32_t bar, uint64_t pol) {
+  if (c.a_f32) tma_load_3d(dst, &P.map_xg, bar, 0, c.kk * 2, 0, pol);
+  else tma_load_2d(dst, c.kind == PH_O ? &P.map_o : &P.map_a, bar, c.kk * 64, 0, pol);
 }
 
 __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full,
@@ -304,19 +322,9 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
   bool w_more = cursor_phase(P, w, 0);
   a = w;
   bool a_more = w_more;
-  // L2 prefetch cursor: kept DFLASH_CH_PF units past the ring, so HBM keeps
-  // streaming upcoming weights while the grid sits in a tail or a barrier
-  Cursor f = w;
-  bool f_more = w_more;
-  auto prefetch_ahead = [&]() {
-    while (f_more && f.i < w.i + CH_STAGES + DFLASH_CH_PF) {
-      if (f.i >= w.i + CH_STAGES) prefetch_w(P, f);
-      f_more = cursor_next(P, f);
-    }
-  };
-  prefetch_ahead();
   int ready = 0;                 // phases known to have passed their barrier
   uint64_t t_idle = 0;
+  uint32_t idle = 0;
   bool abort = false;
   while (a_more) {
     bool prog = false;
@@ -334,8 +342,11 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
         const uint32_t abytes = w.a_f32 ? CH_A : CH_A / 2;
         mbar_arrive_expect_tx(bar_full + 8 * s, CH_W + abytes);
         issue_w(P, w, sbase + s * CH_W, bar_full + 8 * s, pol_w);
+        if (DFLASH_CH_EVLOG) {
+          const int k = w.u - first_unit_of(blockIdx.x, (int64_t)gemm_geo(P, w.kind).n_tiles * w.kc, P.grid);
+          if (k < kEvUnits) ev(P, w.p, 2 + 2 * kEvUnits + k);
+        }
         w_more = cursor_next(P, w);
-        prefetch_ahead();
         prog = true;
       }
     }
@@ -351,6 +362,10 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
       if (ok) {
         const int s = a.i % CH_STAGES;
         issue_a(P, a, sbase + CH_OFF_A + s * CH_A, bar_full + 8 * s, pol_a);
+        if (DFLASH_CH_EVLOG) {
+          const int k = a.u - first_unit_of(blockIdx.x, (int64_t)gemm_geo(P, a.kind).n_tiles * a.kc, P.grid);
+          if (k < kEvUnits) ev(P, a.p, 2 + 3 * kEvUnits + k);
+        }
         a_more = cursor_next(P, a);
         prog = true;
       }
@@ -359,10 +374,15 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
     }
     if (prog) {
       t_idle = 0;
+      idle = 0;
       continue;
     }
     if (abort) break;   // nothing left that can complete
-    if (w_held && a.i == w.i) __nanosleep(256);   // attention is running: stay off the issue slots
+    // idle: give the issue slots to the consumer warps sharing this SM sub-partition
+    __nanosleep(w_held && a.i == w.i ? 256 : DFLASH_CH_IDLE_NS);
+    // the abort flags and the clock are checked every 64th idle turn only:
+    // a global load here would hold the lane for a microsecond each turn
+    if ((++idle & 63) != 0) continue;
     if (misc[MS_ABORT] || (*(volatile int*)P.status & ST_TIMEOUT)) {
       abort = true;     // stop loading weights; finish the activation loads already owed
       continue;
@@ -468,7 +488,7 @@ __device__ __forceinline__ void row_apply(const ChainParams& P, int kind, int t,
     *(float4*)(P.x + off) = nv;
     *(float4*)(P.xg + off) = make_float4(nv.x * g.x, nv.y * g.y, nv.z * g.z, nv.w * g.w);
     const float ss = warp_sum(nv.x * nv.x + nv.y * nv.y + nv.z * nv.z + nv.w * nv.w);
-    if (lane == 0) P.ssq[t * CH_ROWS + r] = ss;
+    if (lane == 0) P.ssq[(t * CH_ROWS + r) * CH_SSQ] = ss;
   } else if (kind == PH_GU) {
     // columns 0..63: gate rows of the tile, 64..127: up rows
     const float4 u = shfl_xor4(v, 16);
@@ -559,7 +579,7 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int t = t0 + 8 * k;
-          v[k] = t < nt ? __ldcg(P.ssq + t * CH_ROWS + r) : 0.f;
+          v[k] = t < nt ? __ldcg(P.ssq + (t * CH_ROWS + r) * CH_SSQ) : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) s += v[k];
@@ -570,6 +590,7 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
       if (j == 0) rinv_s[r] = r < P.R ? 1.0f / sqrtf(s / (float)P.D + P.eps) : 0.f;
     }
     named_bar(1, CH_CT);
+    if (tid == 0) trace_max(P, 7, phase);   // rinv ready
   }
   const int g = lane >> 2, tg = lane & 3;
   const float ri0 = geo.a_f32 ? rinv_s[g] : 0.f, ri1 = geo.a_f32 ? rinv_s[g + 8] : 0.f;
@@ -612,8 +633,12 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
     }
   };
 
+  int t = u0 / geo.kc, kk = u0 - t * geo.kc - 1;   // advanced at the top of each turn
   for (int u = u0; u < u1; ++u, ++ri) {
-    const int t = u / geo.kc, kk = u - t * geo.kc;
+    if (++kk == geo.kc) {
+      kk = 0;
+      ++t;
+    }
     if (t != cur) {
       if (cur >= 0) flush(cur);
       cur = t;
@@ -629,6 +654,7 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
       misc[MS_ABORT] = 1;
       continue;
     }
+    if (DFLASH_CH_EVLOG && tid == 0 && u - u0 < kEvUnits) ev(P, phase, 2 + (u - u0));
     const uint32_t wb = sbase + s * CH_W;
     const uint32_t ab = sbase + CH_OFF_A + s * CH_A;
     const uint8_t* abox = smem + CH_OFF_A + s * CH_A;
@@ -662,7 +688,12 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-    if (tid == 0) misc[MS_CONSUMED] = ri + 1;
+    if (tid == 0) {
+      if (DFLASH_CH_EVLOG && u - u0 < kEvUnits) ev(P, phase, 2 + kEvUnits + (u - u0));
+      misc[MS_CONSUMED] = ri + 1;
+      if (u == u0) trace_max(P, 5, phase);                  // first unit ready and done
+      if (u == u0 + (u1 - u0) / 2) trace_max(P, 6, phase);  // half of the units done
+    }
   }
   if (P.trace != nullptr && tid == 0)   // last CTA to finish its multiply-adds
     atomicMax(P.trace + 4 * kChainMaxPhases + phase, (unsigned long long)globaltimer());
@@ -686,7 +717,8 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
   const bool dense = U >= G;
   auto owner = [&](uint32_t u) { return (int)(((u + 1) * G + U - 1) / U) - 1; };
   constexpr int RB = 12;   // contributors per batch
-  for (int k = blockIdx.x * 4 + warp; k < ntask; k += P.grid * 4) {
+  const int W = P.grid * 4, k_first = blockIdx.x * 4 + warp;
+  for (int k = k_first; k < ntask; k += W) {
     const int t = k / R, r = k - t * R;
     const int lo = owner((uint32_t)t * kc), hi = owner((uint32_t)t * kc + kc - 1);
     if (lo == hi) continue;   // finished by its only owner
@@ -719,67 +751,50 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
   }
 }
 
-// End of the LM head: every CTA publishes its per-row record (the top-2 over
-// the vocabulary rows it finished, from its four warps' records); the last
-// CTA to do so merges the grid's records (top-2 merging is order-free, so the
-// result does not depend on which CTA finished which tile) and writes ids
-// and gaps.
-__device__ void lm_finish(const ChainParams& P, volatile int* misc, const float* recs) {
-  const int tid = threadIdx.x - 32, cw = tid >> 5, lane = threadIdx.x & 31;
-  const int R = P.R;
+// End of the LM head's reduce phase: each CTA publishes one top-2 record per
+// row (over the vocabulary tiles it finished, from its four warps' records).
+__device__ void lm_publish(const ChainParams& P, const float* recs) {
+  const int tid = threadIdx.x - 32;
   named_bar(1, CH_CT);
-  if (tid < R) {
+  if (tid < P.R) {
     Top2 m{-INFINITY, 0x7fffffff, -INFINITY};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const float* rc = recs + w * 48 + 3 * tid;
       m = top2_merge(m, Top2{rc[0], __float_as_int(rc[1]), rc[2]});
     }
-    P.amx[(int64_t)blockIdx.x * R + tid] = make_float4(m.t1, __int_as_float(m.i1), m.t2, 0.f);
+    P.amx[(int64_t)blockIdx.x * P.R + tid] = make_float4(m.t1, __int_as_float(m.i1), m.t2, 0.f);
   }
-  named_bar(1, CH_CT);
-  if (tid == 0) {
-    int* done = P.counters + kMaxTiles;
-    const int old = atom_add_acq_rel_gpu(done, 1);
-    const int last = (old == P.grid - 1);
-    if (last) *done = 0;
-    misc[MS_LAST] = last;
-  }
-  named_bar(1, CH_CT);
-  if (!misc[MS_LAST]) return;
-  // warp cw merges rows cw, cw + 4, ... two rows at a time, all of a pair's
-  // record loads in flight together
-  for (int r0 = cw; r0 < R; r0 += 8) {
-    Top2 tt[2] = {{-INFINITY, 0x7fffffff, -INFINITY}, {-INFINITY, 0x7fffffff, -INFINITY}};
-    for (int c0 = 0; c0 < P.grid; c0 += 320) {
-      float4 v[2][10];
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int q = 0; q < 10; ++q) {
-          const int c = c0 + lane + 32 * q, r = r0 + 4 * h;
-          v[h][q] = (c < P.grid && r < R)
-                        ? __ldcg(&P.amx[(int64_t)c * R + r])
-                        : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY, 0.f);
-        }
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int q = 0; q < 10; ++q)
-          tt[h] = top2_merge(tt[h], Top2{v[h][q].x, __float_as_int(v[h][q].y), v[h][q].z});
+}
+
+// Final merge (after a grid barrier): one warp per row merges the grid's
+// records (top-2 merging is order-free, so the result does not depend on
+// which CTA finished which tile) and writes the id and the gap.
+__device__ void lm_merge(const ChainParams& P) {
+  const int warp = (threadIdx.x - 32) >> 5, lane = threadIdx.x & 31;
+  const int R = P.R;
+  for (int r = blockIdx.x * 4 + warp; r < R; r += P.grid * 4) {
+    const int b = r / P.B, i = r - b * P.B;
+    if (i == 0) {
+      if (lane == 0) P.ids[(int64_t)b * P.B] = P.anchor[b];
+      continue;
     }
+    Top2 tt{-INFINITY, 0x7fffffff, -INFINITY};
+    for (int c0 = 0; c0 < P.grid; c0 += 32 * 12) {
+      float4 v[12];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = r0 + 4 * h;
-      const Top2 m = top2_warp(tt[h]);
-      if (r >= R || lane != 0) continue;
-      const int b = r / P.B, i = r - b * P.B;
-      if (i == 0) {
-        P.ids[(int64_t)b * P.B] = P.anchor[b];
-      } else {
-        P.ids[(int64_t)b * P.B + i] = m.i1;
-        if (P.gap) P.gap[(int64_t)b * (P.B - 1) + i - 1] = m.t1 - m.t2;
+      for (int q = 0; q < 12; ++q) {
+        const int c = c0 + lane + 32 * q;
+        v[q] = c < P.grid ? __ldcg(&P.amx[(int64_t)c * R + r])
+                          : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY, 0.f);
       }
+#pragma unroll
+      for (int q = 0; q < 12; ++q) tt = top2_merge(tt, Top2{v[q].x, __float_as_int(v[q].y), v[q].z});
+    }
+    tt = top2_warp(tt);
+    if (lane == 0) {
+      P.ids[(int64_t)b * P.B + i] = tt.i1;
+      if (P.gap) P.gap[(int64_t)b * (P.B - 1) + i - 1] = tt.t1 - tt.t2;
     }
   }
 }
@@ -819,9 +834,20 @@ __device__ __forceinline__ uint32_t tswz(int row, int chunk) {
   return (uint32_t)(row * (CH_DH * 2) + ((chunk ^ (row & 7)) << 4));
 }
 
-// Trace helper: latest time over the grid for column `col` of phase `p`.
-__device__ __forceinline__ void trace_max(const ChainParams& P, int col, int p) {
-  if (P.trace != nullptr) atomicMax(P.trace + col * kChainMaxPhases + p, (unsigned long long)globaltimer());
+struct ItemGeo {
+  int b, g, L, k_begin, k_end;
+};
+__device__ __forceinline__ ItemGeo item_geo(const ChainParams& P, const Items* it, int j) {
+  ItemGeo q;
+  q.b = 0;
+  while (q.b + 1 < P.batch && j >= it->base[q.b + 1]) ++q.b;
+  const int jj = j - it->base[q.b];
+  q.g = jj / it->runs[q.b];
+  const int run = jj - q.g * it->runs[q.b];
+  q.L = it->L[q.b];
+  q.k_begin = run * it->chunk * CH_AK;
+  q.k_end = min(q.L + P.B, q.k_begin + it->chunk * CH_AK);
+  return q;
 }
 
 __device__ void attention_phase(const ChainParams& P, int phase, int l, const Items* it, uint8_t* smem) {
@@ -833,13 +859,8 @@ __device__ void attention_phase(const ChainParams& P, int phase, int l, const It
   const bool active = warp * 16 < QM;
   const int total = min(it->total, P.n_items_max);
   for (int j = blockIdx.x; j < total; j += P.grid) {
-    int b = 0;
-    while (b + 1 < P.batch && j >= it->base[b + 1]) ++b;
-    const int jj = j - it->base[b];
-    const int g = jj / it->runs[b], run = jj - g * it->runs[b];
-    const int L = it->L[b], nk = L + P.B;
-    const int k_begin = run * it->chunk * CH_AK;
-    const int k_end = min(nk, k_begin + it->chunk * CH_AK);
+    const ItemGeo ig = item_geo(P, it, j);
+    const int b = ig.b, g = ig.g, L = ig.L, k_begin = ig.k_begin, k_end = ig.k_end;
     const int nsub = (k_end - k_begin + CH_AK - 1) / CH_AK;
     const bf16* kcb = P.kc[l] + ((int64_t)b * P.G + g) * P.cap * CH_DH;
     const bf16* vcb = P.vc[l] + ((int64_t)b * P.G + g) * P.cap * CH_DH;
@@ -1087,7 +1108,7 @@ __device__ void embed_phase(const ChainParams& P) {
     *((float4*)(P.xg + (int64_t)r * P.D + t * 128) + lane) =
         make_float4(v.x * g4.x, v.y * g4.y, v.z * g4.z, v.w * g4.w);
     const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
-    if (lane == 0) P.ssq[t * CH_ROWS + r] = ss;
+    if (lane == 0) P.ssq[(t * CH_ROWS + r) * CH_SSQ] = ss;
   }
 }
 
@@ -1145,6 +1166,7 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
       if (!misc[MS_GO]) break;
       if (P.trace != nullptr && tid == 0) {
         const unsigned long long now = globaltimer();
+        ev(P, p, 0);
         atomicMin(P.trace + p, now);                          // first CTA to start
         atomicMax(P.trace + kChainMaxPhases + p, now);        // last CTA to start
       }
@@ -1162,7 +1184,9 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
         int lp;
         const int pk = phase_kind(P, p - 1, lp);
         reduce_phase(P, pk, lp, rowpos, recs);
-        if (pk == PH_LM) lm_finish(P, misc, recs);
+        if (pk == PH_LM) lm_publish(P, recs);
+      } else if (kind == PH_LMFIN) {
+        lm_merge(P);
       } else {
         if (kind == PH_LM) {
           for (int e = tid; e < 4 * CH_ROWS; e += CH_CT) {
@@ -1179,6 +1203,7 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
         red_release_gpu_add(P.counters + kMaxTiles + 1, 1);
         if (P.trace != nullptr) {
           const unsigned long long now = globaltimer();
+          ev(P, p, 1);
           atomicMin(P.trace + 2 * kChainMaxPhases + p, now);  // first CTA to finish
           atomicMax(P.trace + 3 * kChainMaxPhases + p, now);  // last CTA to finish
         }
@@ -1193,13 +1218,10 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
       const int hi = misc[MS_ISSUED];
       for (int i = misc[MS_CONSUMED]; i < hi; ++i)
         if (!mbar_wait(bar_full + 8 * (i % CH_STAGES), (i / CH_STAGES) & 1, 20000000ull)) break;
-    }
-    __threadfence();
-    int* exitc = P.counters + kMaxTiles + 2;
-    const int old = atomicAdd(exitc, 1);
-    if (old == P.grid - 1) {
+    } else if (blockIdx.x == 0 && grid_wait(P, P.n_phases * P.grid)) {
+      // every CTA has passed its last phase (and polls no more): the barrier
+      // counter starts the next launch from zero
       P.counters[kMaxTiles + 1] = 0;
-      *exitc = 0;
     }
   }
 }
@@ -1300,12 +1322,13 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
     if (cudaMemsetAsync(h->d_trace, 0xff, col, s) ||
         cudaMemsetAsync(h->d_trace + kChainMaxPhases, 0, col, s) ||
         cudaMemsetAsync(h->d_trace + 2 * kChainMaxPhases, 0xff, col, s) ||
-        cudaMemsetAsync(h->d_trace + 3 * kChainMaxPhases, 0, (kChainTraceCols - 3) * col, s))
+        cudaMemsetAsync(h->d_trace + 3 * kChainMaxPhases, 0,
+                        (kChainTraceCols - 3) * col + kEvWords * sizeof(unsigned long long), s))
       return DFLASH_ERR_CUDA;
     P.trace = h->d_trace;
-    h->trace_phases = 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 2 : 0);
+    h->trace_phases = 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 3 : 0);
   }
-  P.n_phases = 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 2 : 0);
+  P.n_phases = 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 3 : 0);
   P.n_items_max = P.grid + A.batch * c.n_kv_heads;
   P.eps = c.rms_eps;
   P.embed_scale = c.embed_scale;

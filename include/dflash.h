@@ -278,6 +278,14 @@ int dflash_timing_read(dflash_handle* h, int32_t kclass, double* total_ms, int64
  * the host array out[8 * n]; *n_phases gets the phase count (0: none). */
 int dflash_chain_trace_enable(dflash_handle* h, int on);
 int dflash_chain_trace_read(dflash_handle* h, int64_t* out, int32_t n, int32_t* n_phases);
+/* Raw per-CTA event log of the latest traced launch: 4 sampled CTAs x 164
+ * phases x 50 words (times are the CTA's SM cycle counter, comparable within
+ * one CTA only; 0 = no event): phase start, phase end, then for the CTA's
+ * first 12 projection units: data ready, multiply done, weight load issued,
+ * activation load issued.  Recorded only by builds compiled with
+ * -DDFLASH_CH_EVLOG=1 (a profiling build); otherwise all zero.  Copies
+ * min(n, total) words to the host array out; *count gets the number copied. */
+int dflash_chain_trace_events(dflash_handle* h, int64_t* out, int64_t n, int64_t* count);
 
 #ifdef __cplusplus
 }
