@@ -332,6 +332,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace", action="store_true",
+                    help="print the persistent kernel's per-phase timeline of one step "
+                         "(a table, not the JSON line) and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -345,10 +348,77 @@ def main():
         if args.impl == "reference":
             run_reference(args, rank, world)
             return
+        if args.trace:
+            if rank == 0:
+                run_trace(args)
+            return
         run_ours(args, rank, world, local)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()
+
+
+PHASE_NAMES = ("q/k/v", "q/k/v reduce", "attention", "combine", "o_proj", "o_proj reduce",
+               "gate/up", "gate/up reduce", "down", "down reduce")
+
+
+def run_trace(args):
+    """Per-phase device timeline of the draft block in one bench step."""
+    import block_diffusion_drafter_layer_gb300 as dfl
+    w = synth.WORKLOADS[args.workload]
+    st = Draft(w, 0, 8)
+    st.prefill()
+    for _ in range(max(args.warmup, 3)):
+        st.step()
+    dfl.dflash_chain_trace_enable(st.model.handle, True)
+    st.step()
+    tr = dfl.dflash_chain_trace_read(st.model.handle)
+    dfl.dflash_chain_trace_enable(st.model.handle, False)
+    torch.cuda.synchronize()
+    if not tr:
+        print(f"{w.name}: the draft block did not run as one persistent launch (no timeline)")
+        return
+    names = ["embed"]
+    for l in range(w.draft.n_layers):
+        names += [f"layer {l} {n}" for n in PHASE_NAMES]
+    names += ["LM head", "LM head reduce", "LM head merge"][:len(tr) - len(names)]
+    t0 = tr[0][0]
+    print(f"# {w.name}: persistent draft-block launch, {len(tr)} phases; times in us from the "
+          f"first CTA's start (device %globaltimer, ~1 us resolution)")
+    print("| phase | start | first CTA in -> last CTA done | gap after previous |")
+    print("|---|---|---|---|")
+    prev = t0
+    tot = {}
+    for nm, row in zip(names, tr):
+        s0, e1 = row[0], row[3]
+        print(f"| {nm} | {(s0 - t0) / 1e3:.1f} | {(e1 - s0) / 1e3:.2f} | {(s0 - prev) / 1e3:.2f} |")
+        key = nm.split(" ", 2)[-1] if nm.startswith("layer") else nm
+        tot[key] = tot.get(key, 0.0) + (e1 - prev) / 1e3
+        prev = e1
+    print(f"\ntotal {(prev - t0) / 1e3:.1f} us; per phase kind (incl. the barrier before it): " +
+          ", ".join(f"{k} {v:.1f}" for k, v in tot.items()))
+
+
+def _traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, if that
+    record was taken on the current source of the kernel (else None)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    r = rec.get(kernel)
+    if not r or r.get("workload") != workload:
+        return None
+    h = hashlib.sha256()
+    for rel in r.get("sources", []):
+        try:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+        except OSError:
+            return None
+    return r.get("dram_bytes_per_launch") if h.hexdigest() == r.get("sha256") else None
 
 
 def run_ours(args, rank, world, local):
@@ -411,7 +481,7 @@ def run_ours(args, rank, world, local):
     ach = nbytes[dom] / (cls[dom][0] / 1e3) / 1e9
     roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
             "frac": ach / hbm, "peak_kind": peak_kind,
-            "traffic": None, "launches_per_step": cls[dom][1],
+            "traffic": _traffic(dom, w.name), "launches_per_step": cls[dom][1],
             "algorithmic_bytes_per_step": nbytes[dom],
             "class_ms_per_step": {k: round(v[0], 4) for k, v in cls.items()}}
     total_bytes = sum(nbytes[k] for k in ("weight_gemm", "lm_head", "attention", "dense_gemm"))
