@@ -1073,21 +1073,4 @@ bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
          CUDA_SUCCESS;
 }
 
-// fp32 rows [rows, cols] viewed as [rows, cols / 32, 32] (3-D), box
-// {32, 2, box_rows} with the 128-byte swizzle: one load brings a 64-column
-// chunk of box_rows rows (128-byte line l = 2 * row + half).
-bool make_tmap_rows_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
-                        uint32_t box_rows) {
-  if (!g_encode && !make_tmap_2d(m, base, 32, 1, 128, 32, 1, DFLASH_F32)) return false;
-  if (cols % 64) return false;
-  const cuuint64_t dims[3] = {32, cols / 32, rows};
-  const cuuint64_t strides[2] = {128, cols * 4};
-  const cuuint32_t box[3] = {32, 2, box_rows};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
 }  // namespace dflash

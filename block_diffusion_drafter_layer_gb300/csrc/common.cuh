@@ -215,8 +215,6 @@ struct WLaunch {
 bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                   int dtype = DFLASH_BF16);
-bool make_tmap_rows_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
-                        uint32_t box_rows);
 size_t wstream_scratch_bytes(const dflash_handle* h, int M);
 int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float* partial,
             float4* amx);
@@ -242,7 +240,7 @@ struct ChainArgs {
   int32_t* ids;
   float* gap;
   float* x;                     // [R, D] fp32 residual
-  float* xg;                    // [R, D] fp32 residual times the next RMSNorm gain
+  float* xg;                    // [R, D] space for bf16 residual x next RMSNorm gain
   void *q, *kb, *vb, *o, *a;    // bf16 [R, H*d], [R, G*d] x 2, [R, H*d], [R, F]
   float* ssq;                   // [D / 128, 16] sums of squares, 8 floats apart
   float* partial;               // split-K fix-up tiles

@@ -22,12 +22,12 @@
 //   waits at a barrier (weights do not depend on activations); only the
 //   activation loads wait for the barrier.
 // * The RMSNorms in front of q/k/v, gate/up and the LM head are folded into
-//   those projections: the residual epilogues (and the embedding) write the
-//   residual x, the residual times the next norm's gain (x * g), and one sum
-//   of squares of x per (128-column tile, row); the next projection loads the
-//   fp32 x * g rows by TMA and builds its bf16 MMA operand as
-//   bf16((x * g) * rinv) in registers: the norm's storage point, with the two
-//   fp32 products taken in the other order.
+//   those projections.  RMSNorm scales each row by one number, 1 / rms(x), so
+//   W (x g / rms) = (W (x g)) / rms: the residual epilogues (and the
+//   embedding) write the residual x, bf16(x * g) for the next norm's gain g,
+//   and one sum of squares of x per (128-column tile, row); the next
+//   projection multiplies bf16(x * g) like any other operand and its
+//   epilogue scales the fp32 rows by 1 / rms from those sums.
 // * Attention cuts the keys of each (sequence, kv head) into equal runs of
 //   32-key sub-chunks, one run per work item, items dealt round-robin to the
 //   CTAs; each item keeps (max, sum, unnormalised output) per query row, and
@@ -56,7 +56,7 @@ constexpr int CH_THREADS = 160;            // warp 0: TMA producer; warps 1-4: c
 constexpr int CH_CT = 128;                 // consumer threads
 constexpr int CH_STAGES = DFLASH_CH_STAGES;
 constexpr int CH_W = 128 * 64 * 2;         // weight chunk: 128 rows x 64 k, bf16
-constexpr int CH_A = 16 * 64 * 4;          // activation chunk: 16 rows x 64 k, fp32 (or bf16)
+constexpr int CH_A = 16 * 64 * 2;          // activation chunk: 16 rows x 64 k, bf16
 constexpr int CH_DH = 128;                 // head dim of the attention phases
 constexpr int CH_AK = 32;                  // keys per attention sub-chunk
 constexpr int CH_DP = CH_DH + 4;           // attention partial row: max, sum, 2 pad, output
@@ -102,7 +102,7 @@ struct ChainLayer {
 };
 
 struct ChainParams {
-  CUtensorMap map_xg;         // fp32 x * g [R, D] as [R, D/32, 32], box {32, 2, 16}
+  CUtensorMap map_xg;         // bf16 x * g [R, D], box 64 x 16
   CUtensorMap map_o;          // bf16 attention output [R, H*d], box 64 x 16
   CUtensorMap map_a;          // bf16 SwiGLU output [R, F], box 64 x 16
   const CUtensorMap* wmaps;   // [n_layers * 7 + 1]: q k v o gate up down per layer, LM head
@@ -116,7 +116,7 @@ struct ChainParams {
   int32_t* ids;
   float* gap;
   float* x;
-  float* xg;
+  bf16* xg;
   bf16* q;
   bf16* kb;
   bf16* vb;
@@ -165,8 +165,10 @@ __device__ __forceinline__ int phase_kind(const ChainParams& P, int p, int& l) {
   return kLayerSeq[q % kLayerPhases];
 }
 
+// nin: the phase's input RMSNorm is folded in (its operand is bf16(x * g);
+// the epilogue scales the fp32 result rows by 1 / rms(x))
 struct Geo {
-  int n_tiles, kc, a_f32;
+  int n_tiles, kc, nin;
 };
 __device__ __forceinline__ Geo gemm_geo(const ChainParams& P, int kind) {
   switch (kind) {
@@ -232,7 +234,7 @@ __device__ bool grid_wait(const ChainParams& P, int target) {
 // cursor that fills ring slots as soon as they are free, and an activation
 // cursor that follows it once the unit's phase has passed its barrier.
 struct Cursor {
-  int p, kind, l, u, u1, kc, a_f32;
+  int p, kind, l, u, u1, kc;
   int i;        // ring index
   int t, kk;    // tile and k-chunk of unit u
   const CUtensorMap* wm0;   // weight box(es) of tile t (gate / up: two)
@@ -282,7 +284,6 @@ __device__ __forceinline__ bool cursor_phase(const ChainParams& P, Cursor& c, in
     c.u = u0;
     c.u1 = u1;
     c.kc = g.kc;
-    c.a_f32 = g.a_f32;
     c.t = u0 / g.kc;
     c.kk = u0 - c.t * g.kc;
     cursor_tile(P, c);
@@ -310,8 +311,8 @@ __device__ __forceinline__ void issue_w(const ChainParams& P, const Cursor& c, u
 
 __device__ __forceinline__ void issue_a(const ChainParams& P, const Cursor& c, uint32_t dst,
                                         uint32_t bar, uint64_t pol) {
-  if (c.a_f32) tma_load_3d(dst, &P.map_xg, bar, 0, c.kk * 2, 0, pol);
-  else tma_load_2d(dst, c.kind == PH_O ? &P.map_o : &P.map_a, bar, c.kk * 64, 0, pol);
+  const CUtensorMap* m = c.kind == PH_O ? &P.map_o : c.kind == PH_DN ? &P.map_a : &P.map_xg;
+  tma_load_2d(dst, m, bar, c.kk * 64, 0, pol);
 }
 
 __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full,
@@ -339,8 +340,7 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
       // with no activation load owed, block in the barrier wait instead of spinning
       if (use == 0 || (a.i == w.i ? mbar_try_wait(bar_empty + 8 * s, (use - 1) & 1)
                                   : mbar_test_wait(bar_empty + 8 * s, (use - 1) & 1))) {
-        const uint32_t abytes = w.a_f32 ? CH_A : CH_A / 2;
-        mbar_arrive_expect_tx(bar_full + 8 * s, CH_W + abytes);
+        mbar_arrive_expect_tx(bar_full + 8 * s, CH_W + CH_A);
         issue_w(P, w, sbase + s * CH_W, bar_full + 8 * s, pol_w);
         if (DFLASH_CH_EVLOG) {
           const int k = w.u - first_unit_of(blockIdx.x, (int64_t)gemm_geo(P, w.kind).n_tiles * w.kc, P.grid);
@@ -477,16 +477,23 @@ __device__ __forceinline__ RowIn row_in(const ChainParams& P, int kind, int t, i
   return in;
 }
 
+// ri: 1 / rms of row r where the phase's input norm is folded in (q/k/v,
+// gate/up, LM head: the operand was bf16(x * g), so the row of the product is
+// scaled here), else 1.
 __device__ __forceinline__ void row_apply(const ChainParams& P, int kind, int t, int r, float4 v,
-                                          float4 g, const RowIn& in, const int* rowpos,
+                                          float ri, float4 g, const RowIn& in, const int* rowpos,
                                           float* rec /* [16][3] of this warp */) {
   const int lane = threadIdx.x & 31;
+  v = make_float4(v.x * ri, v.y * ri, v.z * ri, v.w * ri);
   if (kind == PH_O || kind == PH_DN) {
     // x += v; x * g for the next norm; the row's sum of squares over the tile
     const float4 nv = make_float4(in.a.x + v.x, in.a.y + v.y, in.a.z + v.z, in.a.w + v.w);
     const int64_t off = (int64_t)r * P.D + t * 128 + 4 * lane;
     *(float4*)(P.x + off) = nv;
-    *(float4*)(P.xg + off) = make_float4(nv.x * g.x, nv.y * g.y, nv.z * g.z, nv.w * g.w);
+    uint2 pk;
+    pk.x = pack_bf16(nv.x * g.x, nv.y * g.y);
+    pk.y = pack_bf16(nv.z * g.z, nv.w * g.w);
+    *(uint2*)(P.xg + off) = pk;
     const float ss = warp_sum(nv.x * nv.x + nv.y * nv.y + nv.z * nv.z + nv.w * nv.w);
     if (lane == 0) P.ssq[(t * CH_ROWS + r) * CH_SSQ] = ss;
   } else if (kind == PH_GU) {
@@ -545,10 +552,29 @@ __device__ __forceinline__ void row_apply(const ChainParams& P, int kind, int t,
   }
 }
 
-// fp32 pair (line, col), col even, of 128-byte lines stored with the 128-byte
-// swizzle (16-byte chunk c of line l at c ^ (l & 7)).
-__device__ __forceinline__ float2 lds_x(const uint8_t* box, int line, int c) {
-  return *(const float2*)(box + line * 128 + ((((c >> 2) ^ (line & 7))) << 4) + (c & 3) * 4);
+// 1 / rms of every row of the residual from its per-(tile, row) sums of
+// squares, into rinv_s (all consumer threads; 8 per row take every 8th tile,
+// loads in flight together, then a fixed shuffle tree adds the 8 parts).
+__device__ void rinv_rows(const ChainParams& P, float* rinv_s) {
+  const int tid = threadIdx.x - 32;
+  const int r = tid >> 3, j = tid & 7, nt = P.D / 128;
+  float s = 0.f;
+  for (int t0 = j; t0 < nt; t0 += 64) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int t = t0 + 8 * k;
+      v[k] = t < nt ? __ldcg(P.ssq + (t * CH_ROWS + r) * CH_SSQ) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s += v[k];
+  }
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  s += __shfl_xor_sync(0xffffffffu, s, 4);
+  named_bar(1, CH_CT);   // the previous readers of rinv_s are done
+  if (j == 0) rinv_s[r] = r < P.R ? 1.0f / sqrtf(s / (float)P.D + P.eps) : 0.f;
+  named_bar(1, CH_CT);
 }
 
 // One projection phase: this CTA's units [u0, u1) of the phase's
@@ -567,33 +593,8 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
   const int u0 = first_unit_of(cta, U, G), u1 = first_unit_of(cta + 1, U, G);
   if (u1 <= u0) return;
   float* E = (float*)(smem + CH_OFF_E);
-  if (geo.a_f32) {
-    // rinv per row from the residual tiles' sums of squares: 8 threads per
-    // row take every 8th tile (loads in flight together), then a fixed
-    // shuffle tree adds the 8 parts
-    {
-      const int r = tid >> 3, j = tid & 7, nt = P.D / 128;
-      float s = 0.f;
-      for (int t0 = j; t0 < nt; t0 += 64) {
-        float v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int t = t0 + 8 * k;
-          v[k] = t < nt ? __ldcg(P.ssq + (t * CH_ROWS + r) * CH_SSQ) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) s += v[k];
-      }
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      s += __shfl_xor_sync(0xffffffffu, s, 4);
-      if (j == 0) rinv_s[r] = r < P.R ? 1.0f / sqrtf(s / (float)P.D + P.eps) : 0.f;
-    }
-    named_bar(1, CH_CT);
-    if (tid == 0) trace_max(P, 7, phase);   // rinv ready
-  }
   const int g = lane >> 2, tg = lane & 3;
-  const float ri0 = geo.a_f32 ? rinv_s[g] : 0.f, ri1 = geo.a_f32 ? rinv_s[g + 8] : 0.f;
+  bool have_rinv = false;   // 1 / rms of the rows, computed when a first tile finishes here
   float acc[4][4];
   int cur = -1, kbeg = 0, kend = 0;
 
@@ -608,6 +609,10 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
     named_bar(1, CH_CT);
     if (kbeg == 0 && kend == geo.kc) {
       // whole tile: finish its rows here (warp cw: rows cw, cw + 4, ...)
+      if (geo.nin && !have_rinv) {
+        rinv_rows(P, rinv_s);
+        have_rinv = true;
+      }
       const float4 gt = tile_gain(P, kind, l, t);
       RowIn in[4];
 #pragma unroll
@@ -619,8 +624,8 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
       for (int q = 0; q < 4; ++q) {
         const int r = cw + 4 * q;
         if (r < P.R)
-          row_apply(P, kind, t, r, *(const float4*)&E[r * CH_EPAD + 4 * lane], gt, in[q], rowpos,
-                    recs + cw * 48);
+          row_apply(P, kind, t, r, *(const float4*)&E[r * CH_EPAD + 4 * lane],
+                    geo.nin ? rinv_s[r] : 1.f, gt, in[q], rowpos, recs + cw * 48);
       }
     } else {
       const int slot_i = (uint32_t)u0 / (uint32_t)geo.kc == (uint32_t)t ? 0 : 1;
@@ -657,21 +662,10 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
     if (DFLASH_CH_EVLOG && tid == 0 && u - u0 < kEvUnits) ev(P, phase, 2 + (u - u0));
     const uint32_t wb = sbase + s * CH_W;
     const uint32_t ab = sbase + CH_OFF_A + s * CH_A;
-    const uint8_t* abox = smem + CH_OFF_A + s * CH_A;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       uint32_t af[4];
-      if (geo.a_f32) {
-        // columns ks*16 + {2tg, 2tg+1, 2tg+8, 2tg+9} of the chunk: 32-column
-        // half h = ks / 2, line 2 * row + h
-        const int h = ks >> 1, c0 = (ks & 1) * 16 + 2 * tg;
-        const float2 x00 = lds_x(abox, 2 * g + h, c0), x10 = lds_x(abox, 2 * (g + 8) + h, c0);
-        const float2 x01 = lds_x(abox, 2 * g + h, c0 + 8), x11 = lds_x(abox, 2 * (g + 8) + h, c0 + 8);
-        af[0] = pack_bf16(x00.x * ri0, x00.y * ri0);
-        af[1] = pack_bf16(x10.x * ri1, x10.y * ri1);
-        af[2] = pack_bf16(x01.x * ri0, x01.y * ri0);
-        af[3] = pack_bf16(x11.x * ri1, x11.y * ri1);
-      } else {
+      {
         const int row = lane & 15, ch = 2 * ks + (lane >> 4);
         ldsm_x4(ab + row * 128 + ((ch ^ (row & 7)) << 4), af[0], af[1], af[2], af[3]);
       }
@@ -709,9 +703,11 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
 // per CTA (U >= G) they are the CTAs lo .. hi, each of which holds t in slot 0
 // (its first tile) except lo when lo began in an earlier tile (slot 1); with
 // fewer units than CTAs every unit has its own owner, holding t in slot 0.
-__device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* rowpos, float* recs) {
+__device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* rowpos, float* recs,
+                             float* rinv_s) {
   const int warp = (threadIdx.x - 32) >> 5, lane = threadIdx.x & 31;
   const Geo geo = gemm_geo(P, kind);
+  if (geo.nin) rinv_rows(P, rinv_s);   // 1 / rms of each row, once per CTA
   const uint32_t U = (uint32_t)geo.n_tiles * geo.kc, G = P.grid, kc = geo.kc;
   const int R = P.R, ntask = geo.n_tiles * R;
   const bool dense = U >= G;
@@ -747,7 +743,7 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
         sum.w += v[j].w;
       }
     }
-    row_apply(P, kind, t, r, sum, gt, in, rowpos, recs + warp * 48);
+    row_apply(P, kind, t, r, sum, geo.nin ? rinv_s[r] : 1.f, gt, in, rowpos, recs + warp * 48);
   }
 }
 
@@ -1105,8 +1101,10 @@ __device__ void embed_phase(const ChainParams& P) {
     }
     *((float4*)(P.x + (int64_t)r * P.D + t * 128) + lane) = v;
     const float4 g4 = __ldg((const float4*)(P.lay[0].g_in + t * 128) + lane);
-    *((float4*)(P.xg + (int64_t)r * P.D + t * 128) + lane) =
-        make_float4(v.x * g4.x, v.y * g4.y, v.z * g4.z, v.w * g4.w);
+    uint2 pk;
+    pk.x = pack_bf16(v.x * g4.x, v.y * g4.y);
+    pk.y = pack_bf16(v.z * g4.z, v.w * g4.w);
+    *((uint2*)(P.xg + (int64_t)r * P.D + t * 128) + lane) = pk;
     const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
     if (lane == 0) P.ssq[(t * CH_ROWS + r) * CH_SSQ] = ss;
   }
@@ -1183,7 +1181,7 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
       } else if (kind == PH_RED) {
         int lp;
         const int pk = phase_kind(P, p - 1, lp);
-        reduce_phase(P, pk, lp, rowpos, recs);
+        reduce_phase(P, pk, lp, rowpos, recs, rinv_s);
         if (pk == PH_LM) lm_publish(P, recs);
       } else if (kind == PH_LMFIN) {
         lm_merge(P);
@@ -1269,7 +1267,7 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
   const int D = c.hidden, Hd = c.n_heads * c.head_dim, Gd = c.n_kv_heads * c.head_dim, F = c.ffn;
   ChainParams P;
   memset(&P, 0, sizeof(P));
-  if (!make_tmap_rows_f32(&P.map_xg, A.xg, D, R, 16) ||
+  if (!make_tmap_2d(&P.map_xg, A.xg, D, R, (uint64_t)D * 2, 64, 16) ||
       !make_tmap_2d(&P.map_o, A.o, Hd, R, (uint64_t)Hd * 2, 64, 16) ||
       !make_tmap_2d(&P.map_a, A.a, F, R, (uint64_t)F * 2, 64, 16))
     return DFLASH_ERR_CUDA;
@@ -1287,7 +1285,7 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
   P.ids = A.ids;
   P.gap = A.gap;
   P.x = A.x;
-  P.xg = A.xg;
+  P.xg = (bf16*)A.xg;
   P.q = (bf16*)A.q;
   P.kb = (bf16*)A.kb;
   P.vb = (bf16*)A.vb;

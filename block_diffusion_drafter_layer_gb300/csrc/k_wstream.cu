@@ -35,6 +35,7 @@ using namespace ptx;
 #endif
 constexpr int WS_KSPLIT = DFLASH_WS_KSPLIT;
 constexpr int WS_NPROD = DFLASH_WS_NPROD;
+static_assert(WS_NPROD == 1, "the producer steps one cursor per lane");
 constexpr int WS_CW = 4 * WS_KSPLIT;
 constexpr int WS_CT = WS_CW * 32;
 constexpr int WS_THREADS = 32 + WS_CT;
@@ -336,44 +337,85 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
     // ---------------- producer: lanes < WS_NPROD issue the TMA loads ---------
     if (lane < WS_NPROD) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
-      auto issue_w = [&](int u, int s) {
-        const int t = u / p.kc, kk = u - t * p.kc;
-        const WSeg& g = p.seg[seg_of(p, t)];
-        const int lt = t - g.t0;
-        const uint32_t dst = sbase + s * C::W_BYTES, bar = bar_full + 8 * s;
-        if (g.kind == SK_SWIGLU) {
-          tma_load_2d(dst, &p.wmap[g.map], bar, kk * 64, lt * 64, pol_w);
-          tma_load_2d(dst + C::W_BYTES / 2, &p.wmap[g.map2], bar, kk * 64, lt * 64, pol_w);
-        } else {
-          tma_load_2d(dst, &p.wmap[g.map], bar, kk * 64, lt * 128, pol_w);
+      // (tile, k-chunk, activation source) of the next unit, stepped without
+      // divisions; the tile's weight box is resolved once per tile
+      struct Cur {
+        int t, kk, src, lk, seg;
+        const CUtensorMap* m0;
+        const CUtensorMap* m1;   // SwiGLU up half
+        int row;
+      };
+      auto tile = [&](Cur& c) {
+        while (c.seg + 1 < p.nseg && c.t >= p.seg[c.seg + 1].t0) ++c.seg;
+        const WSeg& g = p.seg[c.seg];
+        const int lt = c.t - g.t0;
+        c.m0 = &p.wmap[g.map];
+        c.m1 = g.kind == SK_SWIGLU ? &p.wmap[g.map2] : nullptr;
+        c.row = lt * (g.kind == SK_SWIGLU ? 64 : 128);
+      };
+      auto start = [&](Cur& c, int u) {
+        c.t = u / p.kc;
+        c.kk = u - c.t * p.kc;
+        c.src = c.kk / p.kc_per_src;
+        c.lk = c.kk - c.src * p.kc_per_src;
+        c.seg = 0;
+        tile(c);
+      };
+      auto step = [&](Cur& c) {
+        if (++c.lk == p.kc_per_src) {
+          c.lk = 0;
+          ++c.src;
+        }
+        if (++c.kk == p.kc) {
+          c.kk = c.src = c.lk = 0;
+          ++c.t;
+          tile(c);
         }
       };
-      auto issue_a = [&](int u, int s) {
-        const int kk = u % p.kc;
-        const int src = kk / p.kc_per_src, lk = kk - src * p.kc_per_src;
-        tma_load_2d(sbase + C::OFF_A + s * C::A_BYTES, &p.amap[src], bar_full + 8 * s, lk * 64, 0,
+      auto issue_w = [&](const Cur& c, int s) {
+        const uint32_t dst = sbase + s * C::W_BYTES, bar = bar_full + 8 * s;
+        tma_load_2d(dst, c.m0, bar, c.kk * 64, c.row, pol_w);
+        if (c.m1 != nullptr) tma_load_2d(dst + C::W_BYTES / 2, c.m1, bar, c.kk * 64, c.row, pol_w);
+      };
+      auto issue_a = [&](const Cur& c, int s) {
+        tma_load_2d(sbase + C::OFF_A + s * C::A_BYTES, &p.amap[c.src], bar_full + 8 * s, c.lk * 64, 0,
                     pol_a);
       };
+      Cur wc, ac;
+      start(wc, u0);
+      ac = wc;
       const int pre = n < C::STAGES ? n : C::STAGES;
-      for (int i = lane; i < pre; i += WS_NPROD) {
+      for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(bar_full + 8 * i, C::STAGE_TX);
-        issue_w(u0 + i, i);
+        issue_w(wc, i);
+        step(wc);
       }
       pdl_wait();
-      for (int i = lane; i < pre; i += WS_NPROD) issue_a(u0 + i, i);
+      for (int i = 0; i < pre; ++i) {
+        issue_a(ac, i);
+        step(ac);
+      }
       int issued = pre;
-      for (int i = pre + lane; i < n; i += WS_NPROD) {
-        const int s = i % C::STAGES, use = i / C::STAGES;
+      // unit i reuses slot i % STAGES after the consumers' release of use
+      // i / STAGES - 1, whose phase parity is (i / STAGES - 1) & 1
+      int s = pre % C::STAGES;
+      uint32_t par = (pre / C::STAGES + 1) & 1;
+      for (int i = pre; i < n; ++i) {
         if (misc[0]) break;
-        if (!mbar_wait(bar_empty + 8 * s, (use - 1) & 1)) {
+        if (!mbar_wait(bar_empty + 8 * s, par)) {
           atomicOr(p.status, ST_TIMEOUT);
           misc[0] = 1;
           break;
         }
         mbar_arrive_expect_tx(bar_full + 8 * s, C::STAGE_TX);
-        issue_w(u0 + i, s);
-        issue_a(u0 + i, s);
+        issue_w(wc, s);
+        issue_a(wc, s);
+        step(wc);
         issued = i + 1;
+        if (++s == C::STAGES) {
+          s = 0;
+          par ^= 1;
+        }
       }
       atomicMax((int*)&misc[2], issued);   // highest stage index issued, for the drain
     }
@@ -484,9 +526,17 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
       ws_epilogue<MT>(p, t, E, misc, rowpos);
     };
 
+    // tile / k-chunk of the unit and its ring slot / phase parity, stepped
+    // at the top of each turn
+    int t = u0 / p.kc, kk = u0 - t * p.kc - 1, s = -1;
+    uint32_t fpar = 1;
     for (int i = 0; i < n; ++i) {
-      const int u = u0 + i;
-      const int t = u / p.kc, kk = u - t * p.kc;
+      if (++kk == p.kc) {
+        kk = 0;
+        ++t;
+      }
+      if (++s == C::STAGES) s = 0;
+      if (s == 0) fpar ^= 1;
       if (t != cur) {
         if (cur >= 0) flush(cur);
         cur = t;
@@ -498,13 +548,12 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[mb][j][q] = 0.f;
       }
-      const int s = i % C::STAGES;
       kend = kk + 1;
       // after a timed-out wait (in any warp) the warps skip the arithmetic but
       // keep walking the units, so all of them reach the same named barriers
       if (misc[0]) continue;
       // warp-uniform: the phase is complete once any lane has seen it complete
-      if (!__any_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (i / C::STAGES) & 1))) {
+      if (!__any_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, fpar))) {
         if (lane == 0) atomicOr(p.status, ST_TIMEOUT);
         misc[0] = 1;
         continue;
@@ -512,8 +561,8 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
       const uint32_t wb = sbase + s * C::W_BYTES;
       const uint32_t ab = sbase + C::OFF_A + s * C::A_BYTES;
 #pragma unroll
-      for (int kk = 0; kk < 4 / WS_KSPLIT; ++kk) {
-        const int ks = (4 / WS_KSPLIT) * kh + kk;
+      for (int kq = 0; kq < 4 / WS_KSPLIT; ++kq) {
+        const int ks = (4 / WS_KSPLIT) * kh + kq;
         uint32_t a[MT][4];
 #pragma unroll
         for (int mb = 0; mb < MT; ++mb) {
