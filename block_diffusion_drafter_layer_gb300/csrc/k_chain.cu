@@ -210,6 +210,16 @@ __device__ __forceinline__ void ev(const ChainParams& P, int p, int slot) {
   }
 }
 
+// This CTA's units [u0, u1) of a projection phase: an even share of all
+// (tile, k-chunk) units (split K).  (Dealing the LM head's 1187 tiles out
+// whole instead, to leave nothing to reduce, made that phase 12% slower.)
+__device__ __forceinline__ void unit_range(const ChainParams& P, int kind, int cta, int& u0, int& u1) {
+  const Geo g = gemm_geo(P, kind);
+  const int64_t U = (int64_t)g.n_tiles * g.kc;
+  u0 = first_unit_of(cta, U, P.grid);
+  u1 = first_unit_of(cta + 1, U, P.grid);
+}
+
 // ---- grid barrier ----------------------------------------------------------
 // Phase p may start once every CTA has arrived p times.  Gives up (and flags
 // ST_TIMEOUT) after the wall-clock limit or as soon as another CTA has.
@@ -275,8 +285,8 @@ __device__ __forceinline__ bool cursor_phase(const ChainParams& P, Cursor& c, in
     const int kind = phase_kind(P, p, l);
     if (!is_gemm(kind)) continue;
     const Geo g = gemm_geo(P, kind);
-    const int64_t U = (int64_t)g.n_tiles * g.kc;
-    const int u0 = first_unit_of(blockIdx.x, U, P.grid), u1 = first_unit_of(blockIdx.x + 1, U, P.grid);
+    int u0, u1;
+    unit_range(P, kind, blockIdx.x, u0, u1);
     if (u1 <= u0) continue;
     c.p = p;
     c.kind = kind;
@@ -343,7 +353,9 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
         mbar_arrive_expect_tx(bar_full + 8 * s, CH_W + CH_A);
         issue_w(P, w, sbase + s * CH_W, bar_full + 8 * s, pol_w);
         if (DFLASH_CH_EVLOG) {
-          const int k = w.u - first_unit_of(blockIdx.x, (int64_t)gemm_geo(P, w.kind).n_tiles * w.kc, P.grid);
+          int e0, e1;
+          unit_range(P, w.kind, blockIdx.x, e0, e1);
+          const int k = w.u - e0;
           if (k < kEvUnits) ev(P, w.p, 2 + 2 * kEvUnits + k);
         }
         w_more = cursor_next(P, w);
@@ -363,7 +375,9 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
         const int s = a.i % CH_STAGES;
         issue_a(P, a, sbase + CH_OFF_A + s * CH_A, bar_full + 8 * s, pol_a);
         if (DFLASH_CH_EVLOG) {
-          const int k = a.u - first_unit_of(blockIdx.x, (int64_t)gemm_geo(P, a.kind).n_tiles * a.kc, P.grid);
+          int e0, e1;
+          unit_range(P, a.kind, blockIdx.x, e0, e1);
+          const int k = a.u - e0;
           if (k < kEvUnits) ev(P, a.p, 2 + 3 * kEvUnits + k);
         }
         a_more = cursor_next(P, a);
@@ -588,9 +602,9 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
                            volatile int* misc, const int* rowpos, float* rinv_s, float* recs) {
   const int tid = threadIdx.x - 32, cw = tid >> 5, lane = threadIdx.x & 31;
   const Geo geo = gemm_geo(P, kind);
-  const int64_t U = (int64_t)geo.n_tiles * geo.kc, G = P.grid;
   const int cta = blockIdx.x;
-  const int u0 = first_unit_of(cta, U, G), u1 = first_unit_of(cta + 1, U, G);
+  int u0, u1;
+  unit_range(P, kind, cta, u0, u1);
   if (u1 <= u0) return;
   float* E = (float*)(smem + CH_OFF_E);
   const int g = lane >> 2, tg = lane & 3;
@@ -708,6 +722,83 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
   const int warp = (threadIdx.x - 32) >> 5, lane = threadIdx.x & 31;
   const Geo geo = gemm_geo(P, kind);
   if (geo.nin) rinv_rows(P, rinv_s);   // 1 / rms of each row, once per CTA
+  const uint32_t Uu = (uint32_t)geo.n_tiles * geo.kc;
+  if (kind == PH_LM && Uu >= 2u * geo.kc * P.grid) {
+    // At least two whole tiles' units per CTA: a split tile contains exactly
+    // one CTA boundary, so its contributors are CTA c - 1 (slot 1) and CTA c
+    // (slot 0).  One warp per (boundary, 4 rows): 8 loads in one batch.
+    const int nq = (P.R + 3) / 4;
+    const RowIn none{make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int k = blockIdx.x * 4 + warp; k < (P.grid - 1) * nq; k += P.grid * 4) {
+      const int c = 1 + k / nq, r0 = (k - (c - 1) * nq) * 4;
+      const uint32_t fu = (uint32_t)c * Uu / (uint32_t)P.grid;
+      if (fu % geo.kc == 0) continue;   // boundary between tiles: nothing split
+      const int t = fu / geo.kc;
+      const float* pa = P.partial + (int64_t)(2 * (c - 1) + 1) * (CH_ROWS * 128);
+      const float* pb = P.partial + (int64_t)(2 * c) * (CH_ROWS * 128);
+      float4 va[4], vb[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = min(r0 + q, P.R - 1);
+        va[q] = __ldcg((const float4*)(pa + r * 128) + lane);
+        vb[q] = __ldcg((const float4*)(pb + r * 128) + lane);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = r0 + q;
+        if (r >= P.R) break;
+        const float4 sum = make_float4(0.f + va[q].x + vb[q].x, 0.f + va[q].y + vb[q].y,
+                                       0.f + va[q].z + vb[q].z, 0.f + va[q].w + vb[q].w);
+        row_apply(P, kind, t, r, sum, rinv_s[r], make_float4(1.f, 1.f, 1.f, 1.f), none, rowpos,
+                  recs + warp * 48);
+      }
+    }
+    return;
+  }
+  if (kind == PH_GU && Uu >= (uint32_t)P.grid && 3u * (Uu / P.grid) >= geo.kc) {
+    // gate/up (an epilogue that reads nothing per row) with at least kc / 3
+    // units per CTA: a split tile has at most 3 contributors (CTAs lo .. hi,
+    // lo in slot 1 when it began in an earlier tile).  One warp per (tile,
+    // 4 rows): all of a task's loads in one batch, one task per warp.
+    constexpr int CB = 3;
+    const uint32_t G = P.grid;
+    auto owner = [&](uint32_t u) { return (int)(((u + 1) * G + Uu - 1) / Uu) - 1; };
+    const int nq = (P.R + 3) / 4;
+    const RowIn none{make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int k = blockIdx.x * 4 + warp; k < geo.n_tiles * nq; k += P.grid * 4) {
+      const int t = k / nq, r0 = (k - t * nq) * 4;
+      const int lo = owner((uint32_t)t * geo.kc), hi = owner((uint32_t)t * geo.kc + geo.kc - 1);
+      if (lo == hi) continue;   // finished by its only owner
+      const int n = hi - lo + 1;
+      const bool lo1 = (uint32_t)lo * Uu / G < (uint32_t)t * geo.kc;
+      float4 v[CB][4];
+#pragma unroll
+      for (int j = 0; j < CB; ++j) {
+        const float* pj = P.partial + (int64_t)(2 * (lo + j) + (j == 0 && lo1 ? 1 : 0)) * (CH_ROWS * 128);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = min(r0 + q, P.R - 1);
+          v[j][q] = j < n ? __ldcg((const float4*)(pj + r * 128) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int r = r0 + q;
+        if (r >= P.R) break;
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < CB; ++j) {
+          sum.x += v[j][q].x;
+          sum.y += v[j][q].y;
+          sum.z += v[j][q].z;
+          sum.w += v[j][q].w;
+        }
+        row_apply(P, kind, t, r, sum, rinv_s[r], make_float4(1.f, 1.f, 1.f, 1.f), none, rowpos,
+                  recs + warp * 48);
+      }
+    }
+    return;
+  }
   const uint32_t U = (uint32_t)geo.n_tiles * geo.kc, G = P.grid, kc = geo.kc;
   const int R = P.R, ntask = geo.n_tiles * R;
   const bool dense = U >= G;
