@@ -47,6 +47,10 @@ using namespace ptx;
 #ifndef DFLASH_CH_STAGES
 #define DFLASH_CH_STAGES 5
 #endif
+// attention probabilities enter P V as a bf16 (hi, lo) pair (1) or as bf16 (0)
+#ifndef DFLASH_CH_PLO
+#define DFLASH_CH_PLO 1
+#endif
 // pause of the producer lane between polls when nothing can be issued (ns)
 #ifndef DFLASH_CH_IDLE_NS
 #define DFLASH_CH_IDLE_NS 64
@@ -721,7 +725,11 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
                              float* rinv_s) {
   const int warp = (threadIdx.x - 32) >> 5, lane = threadIdx.x & 31;
   const Geo geo = gemm_geo(P, kind);
-  if (geo.nin) rinv_rows(P, rinv_s);   // 1 / rms of each row, once per CTA
+  // 1 / rms of each row: once per CTA where a warp may take several tasks;
+  // with at most one task per warp (q/k/v) it comes from the task's own load
+  // batch instead (one round trip fewer)
+  const bool rinv_in_task = geo.nin && geo.n_tiles * P.R <= P.grid * 4;
+  if (geo.nin && !rinv_in_task) rinv_rows(P, rinv_s);
   const uint32_t Uu = (uint32_t)geo.n_tiles * geo.kc;
   if (kind == PH_LM && Uu >= 2u * geo.kc * P.grid) {
     // At least two whole tiles' units per CTA: a split tile contains exactly
@@ -813,6 +821,9 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
     const bool lo_slot1 = dense && (uint32_t)lo * U / G < (uint32_t)t * kc;
     const float4 gt = tile_gain(P, kind, l, t);
     const RowIn in = row_in(P, kind, t, r, rowpos);
+    float ss = 0.f;
+    if (rinv_in_task)
+      for (int tt = lane; tt < P.D / 128; tt += 32) ss += __ldcg(P.ssq + (tt * CH_ROWS + r) * CH_SSQ);
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j0 = 0; j0 < n; j0 += RB) {
       float4 v[RB];
@@ -834,7 +845,9 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
         sum.w += v[j].w;
       }
     }
-    row_apply(P, kind, t, r, sum, geo.nin ? rinv_s[r] : 1.f, gt, in, rowpos, recs + warp * 48);
+    const float ri = !geo.nin ? 1.f
+                     : rinv_in_task ? 1.0f / sqrtf(warp_sum(ss) / (float)P.D + P.eps) : rinv_s[r];
+    row_apply(P, kind, t, r, sum, ri, gt, in, rowpos, recs + warp * 48);
   }
 }
 
@@ -1077,8 +1090,10 @@ __device__ void attention_phase(const ChainParams& P, int phase, int l, const It
             ldsm_x4_t(sV + tswz(row, ch), b0, b1, b2, b3);
             mma_bf16_16816(acc[2 * np], ph, b0, b1);
             mma_bf16_16816(acc[2 * np + 1], ph, b2, b3);
-            mma_bf16_16816(acc[2 * np], pl, b0, b1);
-            mma_bf16_16816(acc[2 * np + 1], pl, b2, b3);
+            if (DFLASH_CH_PLO) {
+              mma_bf16_16816(acc[2 * np], pl, b0, b1);
+              mma_bf16_16816(acc[2 * np + 1], pl, b2, b3);
+            }
           }
         }
       }
