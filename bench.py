@@ -69,11 +69,17 @@ def step_bytes(w, lens, esz):
 
 # ---------------------------------------------------------------------------
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling during the timed region.
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    The sampler is started first and waited on until it writes its first
+    line, then `mark()` brackets the timed region; only samples whose
+    timestamp falls inside that bracket count (if the region is shorter than
+    the sampling period, the first sample after its start stands in)."""
+
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, index):
         try:
@@ -83,18 +89,37 @@ class Clocks:
             self.index = str(index)
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.p = None
+        self.t = [None, None]
 
     def start(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                       "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.p = None
+            return
+        t_end = time.time() + 10.0
+        while time.time() < t_end and self.p.poll() is None:
+            if os.path.getsize(self.f.name) > 0:
+                break
+            time.sleep(0.01)
+
+    def mark(self, i):
+        self.t[i] = time.time()
+
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def stop(self):
         if self.p is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(2.0 * self.PERIOD_MS / 1e3)
         self.p.terminate()
         try:
             self.p.wait(timeout=5)
@@ -105,18 +130,23 @@ class Clocks:
         with open(self.f.name) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) >= 10:
+                    rows.append((self._when(parts[0]), parts[1:]))
         os.unlink(self.f.name)
-        if not rows:
+        t0, t1 = self.t
+        inside = [r for w, r in rows if w is not None and t0 is not None and t0 <= w <= t1]
+        if not inside:
+            after = [r for w, r in rows if w is not None and t0 is not None and w >= t0]
+            inside = after[:1]
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        sm = [float(r[1]) for r in inside if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": float(np.median(sm)) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(inside), "period_ms": self.PERIOD_MS}
 
 
 # ---------------------------------------------------------------------------
@@ -454,7 +484,9 @@ def run_ours(args, rank, world, local):
     n0 = dfl.dflash_launch_count()
     clocks = Clocks(local)
     clocks.start()
+    clocks.mark(0)
     t = time_steps(st.step, args.steps, world)
+    clocks.mark(1)
     clk = clocks.stop()
     launches = dfl.dflash_launch_count() - n0
     t = _max_over_ranks(t, world)
