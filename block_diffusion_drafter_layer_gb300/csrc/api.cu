@@ -827,6 +827,9 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
   const RowMap rm{0, B, nullptr, nullptr, batch, 0};
   const bool stream = streaming(h, R);
   const bool tcore = !stream && dense_tc(h, R) && attn_fast_ok(h, B);
+  if ((tcore || stream) && attn_fast_ok(h, B) &&
+      (rc = attn_plan(h, s, kv->len, kv->cap, batch, B, f.attn)))
+    return rc;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights& L = h->w.layers[l];
     if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, L.g_in, R, D, c.rms_eps, 0)))

@@ -110,8 +110,9 @@ struct LayerMaps {
   CUtensorMap tq, tk, tv, to, tg, tu, td;
 };
 constexpr int kMaxTiles = 8192;   // 128-row weight tiles per projection launch
-// d_counters: [0, kMaxTiles) tile arrival counters, then the streaming
-// kernel's LM-head merge counter and the persistent kernel's grid barrier
+// d_counters: [0, kMaxTiles) tile arrival counters (tensor-core LM head),
+// then the persistent kernel's grid barrier (kMaxTiles + 1) and the
+// streaming kernel's grid barrier (kMaxTiles + 2)
 constexpr int kCounters = kMaxTiles + 4;
 // phases of the persistent draft-block kernel: embed, 10 per layer, LM head
 // and its reduce
@@ -225,8 +226,11 @@ int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
 int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float4* amx = nullptr);
 
 // ---- split-K attention of the draft block (k_attention.cu) ------------------
-int attn_split_keys(const dflash_handle* h, int batch, int B, int cap);
 size_t attn_scratch_bytes(const dflash_handle* h, int batch, int B);
+// Cut the batch's keys into attention items (reads the lengths on the device);
+// run once per draft block before the layers' attention_fast calls.
+int attn_plan(dflash_handle* h, cudaStream_t s, const int32_t* len, int cap, int batch, int B,
+              float* scratch);
 bool attn_fast_ok(const dflash_handle* h, int B);
 int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* kc, const void* vc,
                    int cap, const int32_t* len, const void* kb, const void* vb, int batch, int B,

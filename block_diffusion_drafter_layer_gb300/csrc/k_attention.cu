@@ -1,19 +1,27 @@
 // Split-K attention of the draft block over [context cache ; block] (bf16).
 //
-// For one sequence b and one key/value head g, the queries are the block's
-// B rows of the H/G query heads that share g (B * H/G <= 64 rows per CTA
-// group); the keys are the L_b cached context entries followed by the
-// block's own B rows, all visible (txtmix §6: full-attention draft layers
-// are non-causal).  The key axis is cut into fixed splits by absolute key
-// index, one CTA per (split, g, b): the CTA streams its keys in 64-key
-// sub-chunks (cp.async, double-buffered), computes S = Q K^T and P V with
-// warp-level bf16 MMA (fp32 accumulate), and keeps a running max and sum
-// per query row (online softmax, row max / sum reduced with quad shuffles).
-// The probabilities enter the PV product as a bf16 pair (hi + lo) so they
-// carry ~16 bits.  Each CTA writes (max, sum, unnormalised output) per row;
-// the CTA that finishes a (b, g) last combines the splits in split order.
-// Splits depend only on key positions, so a row's result does not depend on
-// the batch or block size around it.
+// For one sequence b and one key/value head g the queries are the block's B
+// rows of the H/G query heads that share g (at most 64 rows per query group);
+// the keys are the L_b cached context entries followed by the block's own B
+// rows, all visible (txtmix §6: full-attention draft layers are non-causal).
+// A (b, g, query group) is a "unit".  Three launches:
+//   attn_plan_kernel     reads the context lengths on the device and cuts
+//                        every unit's keys into items of one common length (a
+//                        multiple of 64 keys) chosen so that about AT_WAVES
+//                        items fall on each resident CTA; it runs once per
+//                        draft block, since the lengths do not change between
+//                        layers;
+//   attn_split_kernel    persistent CTAs (2 per SM) take the items
+//                        round-robin: stream the item's keys in 64-key
+//                        sub-chunks (cp.async, 3 stages), S = Q K^T and P V
+//                        with warp-level bf16 MMA (fp32 accumulate), online
+//                        softmax with the row max and sum reduced over quad
+//                        shuffles, and write (max, sum, unnormalised output)
+//                        per query row;
+//   attn_combine_kernel  one warp per (unit, query row) merges the unit's
+//                        items in key order and writes the bf16 output.
+// Items depend only on the lengths of the batch, so results are
+// deterministic.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -22,10 +30,18 @@ namespace dflash {
 using namespace ptx;
 
 constexpr int AT_THREADS = 128;
-constexpr int AT_KSUB = 64;   // keys per sub-chunk
-constexpr int AT_MAX_SPLITS = 128;   // splits per (b, g); bounds the combine's shared memory
-constexpr int AT_MIN_SPLIT = 256;    // keys per split unless that leaves too few CTAs
-constexpr int AT_STAGES = 3;         // cp.async pipeline depth of K/V sub-chunks
+constexpr int AT_KSUB = 64;              // keys per sub-chunk
+constexpr int AT_STAGES = 3;             // cp.async pipeline depth of K/V sub-chunks
+constexpr int AT_CTAS_PER_SM = 2;
+constexpr int AT_WAVES = 3;              // items per persistent CTA, as a target
+constexpr int AT_MIN_SUB = 4;            // sub-chunks per item, at least
+constexpr int AT_MAX_ITEMS_UNIT = 128;   // items per unit, at most
+constexpr int AT_DP = 132;               // floats per partial row: max, sum, 2 pad, 128 outputs
+constexpr int AT_COMB_WARPS = 8;         // query rows per combine CTA
+
+struct AttnItem {
+  int unit, k0, k1, pad;   // keys [k0, k1) of the unit
+};
 
 struct AttnParams {
   const bf16* q;       // [batch*B, H*d]
@@ -35,13 +51,135 @@ struct AttnParams {
   const bf16* vb;
   bf16* o;             // [batch*B, H*d]
   const int32_t* len;  // [batch]
-  int cap, B, H, G, rep, split;
+  int cap, B, H, G, rep, qgroups, units;
   float scale_log2;    // log2(e) / sqrt(d)
-  float* part;         // [batch, G, qgroups, nsplit_max, 64, d + 4]
-  int* counters;       // [batch * G * qgroups]
-  int nsplit_max, qgroups;
+  const int* n_items;  // number of items (written by the plan)
+  const AttnItem* items;
+  const int* unit_begin;   // [units + 1] first item of each unit
+  float* part;         // [max_items][64][AT_DP]
   int* status;
 };
+
+// Scratch region layout: header, unit offsets, items, partials.
+struct AttnScratch {
+  int* hdr;
+  int* unit_begin;
+  AttnItem* items;
+  float* part;
+};
+
+static size_t r256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static int attn_units(const dflash_handle* h, int batch, int B) {
+  const dflash_config& c = h->cfg;
+  const int rep = c.n_heads / c.n_kv_heads, qgroups = (B * rep + 63) / 64;
+  return batch * c.n_kv_heads * qgroups;
+}
+static int attn_slots(const dflash_handle* h) { return AT_CTAS_PER_SM * std::max(1, h->num_sms); }
+// The plan cuts T sub-chunks into items of C >= T / (AT_WAVES * slots)
+// sub-chunks each, so the items number at most AT_WAVES * slots + units.
+static int64_t attn_max_items(const dflash_handle* h, int batch, int B) {
+  return (int64_t)AT_WAVES * attn_slots(h) + attn_units(h, batch, B);
+}
+static AttnScratch attn_carve(float* scratch, int units, int64_t max_items) {
+  char* p = reinterpret_cast<char*>(scratch);
+  AttnScratch s;
+  s.hdr = reinterpret_cast<int*>(p);
+  p += 256;
+  s.unit_begin = reinterpret_cast<int*>(p);
+  p += r256((size_t)(units + 1) * sizeof(int));
+  s.items = reinterpret_cast<AttnItem*>(p);
+  p += r256((size_t)max_items * sizeof(AttnItem));
+  s.part = reinterpret_cast<float*>(p);
+  return s;
+}
+
+size_t attn_scratch_bytes(const dflash_handle* h, int batch, int B) {
+  const int units = attn_units(h, batch, B);
+  const int64_t mi = attn_max_items(h, batch, B);
+  return 256 + r256((size_t)(units + 1) * sizeof(int)) + r256((size_t)mi * sizeof(AttnItem)) +
+         (size_t)mi * 64 * AT_DP * sizeof(float) + 256;
+}
+
+// ---- plan: items of equal length over all units ----------------------------
+__global__ void __launch_bounds__(256) attn_plan_kernel(const int32_t* len, int batch, int B,
+                                                        int cap, int per_b, int slots,
+                                                        int max_items, int* hdr, int* unit_begin,
+                                                        AttnItem* items, int* status) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ long long s_t[8];
+  __shared__ int s_m[8], s_c, s_n;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  long long t = 0;
+  int mx = 0;
+  for (int b = tid; b < batch; b += blockDim.x) {
+    const int L = len[b];
+    if (L < 0 || L > cap) {
+      atomicOr(status, ST_BOUNDS);
+      continue;
+    }
+    const int ns = (L + B + AT_KSUB - 1) / AT_KSUB;
+    t += ns;
+    mx = max(mx, ns);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    t += __shfl_xor_sync(0xffffffffu, t, o);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    s_t[warp] = t;
+    s_m[warp] = mx;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    long long T = 0;
+    int M = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      T += s_t[w];
+      M = max(M, s_m[w]);
+    }
+    T *= per_b;
+    const long long cw = (T + (long long)AT_WAVES * slots - 1) / ((long long)AT_WAVES * slots);
+    long long c = cw > AT_MIN_SUB ? cw : AT_MIN_SUB;
+    const long long cm = (M + AT_MAX_ITEMS_UNIT - 1) / AT_MAX_ITEMS_UNIT;
+    if (cm > c) c = cm;
+    const int C = (int)c;
+    int n = 0;
+    for (int b = 0; b < batch; ++b) {
+      const int L = len[b];
+      const bool ok = L >= 0 && L <= cap;
+      const int ns = ok ? (L + B + AT_KSUB - 1) / AT_KSUB : 0;
+      const int per = (ns + C - 1) / C;
+      for (int j = 0; j < per_b; ++j) {
+        unit_begin[b * per_b + j] = n;
+        n += per;
+      }
+    }
+    unit_begin[batch * per_b] = n;
+    if (n > max_items) {   // cannot happen: C bounds the count
+      atomicOr(status, ST_BOUNDS);
+      n = 0;
+    }
+    hdr[0] = n;
+    s_c = C;
+    s_n = n;
+  }
+  __syncthreads();
+  if (s_n == 0) return;
+  const int C = s_c, units = batch * per_b;
+  for (int u = tid; u < units; u += blockDim.x) {
+    const int L = len[u / per_b];
+    if (L < 0 || L > cap) continue;
+    const int keys = L + B;
+    const int i0 = unit_begin[u], i1 = unit_begin[u + 1];
+    for (int i = i0; i < i1; ++i) {
+      const int k0 = (i - i0) * C * AT_KSUB;
+      items[i] = AttnItem{u, k0, min(keys, k0 + C * AT_KSUB), 0};
+    }
+  }
+}
 
 // smem tile of rows x DH bf16 (row = 2*DH bytes), 16-byte chunks XOR-swizzled
 // by (row & 7) so 8 rows of one chunk column hit distinct banks.
@@ -50,8 +188,9 @@ __device__ __forceinline__ uint32_t tile_off(int row, int chunk) {
   return (uint32_t)(row * (DH * 2) + ((chunk ^ (row & 7)) << 4));
 }
 
+// ---- the items: one partial softmax per (item, query row) --------------------
 template <int DH>
-__global__ void __launch_bounds__(AT_THREADS, 2) attn_split_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(const AttnParams p) {
   constexpr int CH = DH / 8;               // 16-byte chunks per row
   constexpr int NT = DH / 8;               // n8 tiles of the output
   extern __shared__ uint8_t smem_raw[];
@@ -60,319 +199,250 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_split_kernel(const AttnPar
   const uint32_t sK0 = sQ + 64 * DH * 2;
   const uint32_t sV0 = sK0 + AT_STAGES * AT_KSUB * DH * 2;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, g = blockIdx.y;
-  const int b = blockIdx.z / p.qgroups, qg = blockIdx.z - b * p.qgroups;
+  const int gq = lane >> 2, tg = lane & 3;
   pdl_launch_dependents();
   pdl_wait();
+  const int n_items = *p.n_items;
+  const int QM = p.B * p.rep;
 
-  const int L = p.len[b];
-  const int nk = L + p.B;
-  const int nsplit = (nk + p.split - 1) / p.split;
-  if (split >= nsplit) return;
-  if (L < 0 || L > p.cap || nsplit > p.nsplit_max) {
-    if (tid == 0) atomicOr(p.status, ST_BOUNDS);
-    return;
-  }
-  const int QM = p.B * p.rep;                 // query rows of this (b, g)
-  const int q0 = qg * 64;
-  const int qrows = min(64, QM - q0);
-  const int k_begin = split * p.split, k_end = min(nk, k_begin + p.split);
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const AttnItem item = p.items[it];
+    const int u = item.unit;
+    const int qg = u % p.qgroups, bg = u / p.qgroups;
+    const int g = bg % p.G, b = bg / p.G;
+    const int L = p.len[b];
+    const int q0 = qg * 64;
+    const int qrows = min(64, QM - q0);
+    const int k_begin = item.k0, k_end = item.k1;
 
-  // ---- Q tile: row r = query (q0 + r) = head hh of the group, block row i
-  for (int e = tid; e < 64 * CH; e += AT_THREADS) {
-    const int r = e / CH, c = e - r * CH;
-    const int qr = q0 + r;
-    const bool ok = r < qrows;
-    const int hh = ok ? qr / p.B : 0, i = ok ? qr - hh * p.B : 0;
-    const bf16* src = p.q + (int64_t)(b * p.B + i) * (p.H * DH) + (int64_t)(g * p.rep + hh) * DH + c * 8;
-    cp_async16(sQ + tile_off<DH>(r, c), ok ? src : p.q, ok);
-  }
-  const bf16* kcb = p.kc + ((int64_t)b * p.G + g) * p.cap * DH;
-  const bf16* vcb = p.vc + ((int64_t)b * p.G + g) * p.cap * DH;
-  const bf16* kbb = p.kb + (int64_t)b * p.B * (p.G * DH) + (int64_t)g * DH;
-  const bf16* vbb = p.vb + (int64_t)b * p.B * (p.G * DH) + (int64_t)g * DH;
-  auto load_kv = [&](int k0, int stage) {
-    const uint32_t dk = sK0 + stage * AT_KSUB * DH * 2, dv = sV0 + stage * AT_KSUB * DH * 2;
-    for (int e = tid; e < AT_KSUB * CH; e += AT_THREADS) {
+    // ---- Q tile: row r = query (q0 + r) = head hh of the group, block row i
+    for (int e = tid; e < 64 * CH; e += AT_THREADS) {
       const int r = e / CH, c = e - r * CH;
-      const int j = k0 + r;
-      const bool ok = j < k_end;
-      const bf16 *ks, *vs;
-      if (j < L) {
-        ks = kcb + (int64_t)j * DH + c * 8;
-        vs = vcb + (int64_t)j * DH + c * 8;
-      } else {
-        const int jb = ok ? j - L : 0;
-        ks = kbb + (int64_t)jb * (p.G * DH) + c * 8;
-        vs = vbb + (int64_t)jb * (p.G * DH) + c * 8;
-      }
-      cp_async16(dk + tile_off<DH>(r, c), ok ? ks : kcb, ok);
-      cp_async16(dv + tile_off<DH>(r, c), ok ? vs : vcb, ok);
+      const int qr = q0 + r;
+      const bool ok = r < qrows;
+      const int hh = ok ? qr / p.B : 0, i = ok ? qr - hh * p.B : 0;
+      const bf16* src =
+          p.q + (int64_t)(b * p.B + i) * (p.H * DH) + (int64_t)(g * p.rep + hh) * DH + c * 8;
+      cp_async16(sQ + tile_off<DH>(r, c), ok ? src : p.q, ok);
     }
-  };
-  const int nsub = (k_end - k_begin + AT_KSUB - 1) / AT_KSUB;
-  // prologue: the first AT_STAGES-1 sub-chunks (the Q tile rides in group 0)
-#pragma unroll
-  for (int st = 0; st < AT_STAGES - 1; ++st) {
-    if (st < nsub) load_kv(k_begin + st * AT_KSUB, st);
-    cp_async_commit();
-  }
-
-  const int gq = lane >> 2, tg = lane & 3;
-  const bool active = warp * 16 < qrows;
-  uint32_t qa[DH / 16][4];
-  float acc[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-
-  for (int sc = 0; sc < nsub; ++sc) {
-    const int stage = sc % AT_STAGES;
-    const int pre = sc + AT_STAGES - 1;
-    if (pre < nsub) load_kv(k_begin + pre * AT_KSUB, pre % AT_STAGES);
-    cp_async_commit();
-    cp_async_wait<AT_STAGES - 1>();
-    __syncthreads();
-    if (sc == 0 && active) {
-#pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks) {
-        const int row = warp * 16 + (lane & 15);
-        const int ch = 2 * ks + (lane >> 4);
-        ldsm_x4(sQ + tile_off<DH>(row, ch), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+    const bf16* kcb = p.kc + ((int64_t)b * p.G + g) * p.cap * DH;
+    const bf16* vcb = p.vc + ((int64_t)b * p.G + g) * p.cap * DH;
+    const bf16* kbb = p.kb + (int64_t)b * p.B * (p.G * DH) + (int64_t)g * DH;
+    const bf16* vbb = p.vb + (int64_t)b * p.B * (p.G * DH) + (int64_t)g * DH;
+    auto load_kv = [&](int k0, int stage) {
+      const uint32_t dk = sK0 + stage * AT_KSUB * DH * 2, dv = sV0 + stage * AT_KSUB * DH * 2;
+      for (int e = tid; e < AT_KSUB * CH; e += AT_THREADS) {
+        const int r = e / CH, c = e - r * CH;
+        const int j = k0 + r;
+        const bool ok = j < k_end;
+        const bf16 *ks, *vs;
+        if (j < L) {
+          ks = kcb + (int64_t)j * DH + c * 8;
+          vs = vcb + (int64_t)j * DH + c * 8;
+        } else {
+          const int jb = ok ? j - L : 0;
+          ks = kbb + (int64_t)jb * (p.G * DH) + c * 8;
+          vs = vbb + (int64_t)jb * (p.G * DH) + c * 8;
+        }
+        cp_async16(dk + tile_off<DH>(r, c), ok ? ks : kcb, ok);
+        cp_async16(dv + tile_off<DH>(r, c), ok ? vs : vcb, ok);
       }
+    };
+    const int nsub = (k_end - k_begin + AT_KSUB - 1) / AT_KSUB;
+    // prologue: the first AT_STAGES-1 sub-chunks (the Q tile rides in group 0)
+#pragma unroll
+    for (int st = 0; st < AT_STAGES - 1; ++st) {
+      if (st < nsub) load_kv(k_begin + st * AT_KSUB, st);
+      cp_async_commit();
     }
+
+    const bool active = warp * 16 < qrows;
+    uint32_t qa[DH / 16][4];
+    float acc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+
+    for (int sc = 0; sc < nsub; ++sc) {
+      const int stage = sc % AT_STAGES;
+      const int pre = sc + AT_STAGES - 1;
+      if (pre < nsub) load_kv(k_begin + pre * AT_KSUB, pre % AT_STAGES);
+      cp_async_commit();
+      cp_async_wait<AT_STAGES - 1>();
+      __syncthreads();
+      if (sc == 0 && active) {
+#pragma unroll
+        for (int ks = 0; ks < DH / 16; ++ks) {
+          const int row = warp * 16 + (lane & 15);
+          const int ch = 2 * ks + (lane >> 4);
+          ldsm_x4(sQ + tile_off<DH>(row, ch), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+        }
+      }
+      if (active) {
+        const uint32_t sK = sK0 + stage * AT_KSUB * DH * 2, sV = sV0 + stage * AT_KSUB * DH * 2;
+        const int kbase = k_begin + sc * AT_KSUB;
+        // S = Q K^T for 64 keys: 8 n8 tiles
+        float s[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < DH / 16; ++ks) {
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            const int row = pp * 16 + (lane & 7) + ((lane >> 4) << 3);
+            const int ch = 2 * ks + ((lane >> 3) & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(sK + tile_off<DH>(row, ch), b0, b1, b2, b3);
+            mma_bf16_16816(s[2 * pp], qa[ks], b0, b1);
+            mma_bf16_16816(s[2 * pp + 1], qa[ks], b2, b3);
+          }
+        }
+        // online softmax over this sub-chunk (base-2 exponent, scale folded in)
+        float mnew[2] = {mrow[0], mrow[1]};
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int key = kbase + j * 8 + 2 * tg + (q & 1);
+            s[j][q] = (key < k_end) ? s[j][q] * p.scale_log2 : -INFINITY;
+            mnew[q >> 1] = fmaxf(mnew[q >> 1], s[j][q]);
+          }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          mnew[h] = fmaxf(mnew[h], __shfl_xor_sync(0xffffffffu, mnew[h], 1));
+          mnew[h] = fmaxf(mnew[h], __shfl_xor_sync(0xffffffffu, mnew[h], 2));
+        }
+        float alpha[2], lsum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) alpha[h] = (mrow[h] == -INFINITY) ? 0.f : exp2f(mrow[h] - mnew[h]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float e = exp2f(s[j][q] - mnew[q >> 1]);
+            s[j][q] = e;
+            lsum[q >> 1] += e;
+          }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          lrow[h] = lrow[h] * alpha[h] + lsum[h];
+          mrow[h] = mnew[h];
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          acc[j][0] *= alpha[0];
+          acc[j][1] *= alpha[0];
+          acc[j][2] *= alpha[1];
+          acc[j][3] *= alpha[1];
+        }
+        // O += P V with P rounded to bf16 (the row sum above keeps fp32 P)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t ph[4];
+          const float* s0 = s[2 * kk];
+          const float* s1 = s[2 * kk + 1];
+          ph[0] = pack_bf16(s0[0], s0[1]);
+          ph[1] = pack_bf16(s0[2], s0[3]);
+          ph[2] = pack_bf16(s1[0], s1[1]);
+          ph[3] = pack_bf16(s1[2], s1[3]);
+#pragma unroll
+          for (int np = 0; np < NT / 2; ++np) {
+            const int row = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int ch = np * 2 + (lane >> 4);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(sV + tile_off<DH>(row, ch), b0, b1, b2, b3);
+            mma_bf16_16816(acc[2 * np], ph, b0, b1);
+            mma_bf16_16816(acc[2 * np + 1], ph, b2, b3);
+          }
+        }
+      }
+      __syncthreads();
+    }
+    cp_async_wait<0>();
+
+    // ---- partial of this item: per query row (max, sum, unnormalised O) ----
+    float* part = p.part + (int64_t)it * 64 * AT_DP;
     if (active) {
-      const uint32_t sK = sK0 + stage * AT_KSUB * DH * 2, sV = sV0 + stage * AT_KSUB * DH * 2;
-      const int kbase = k_begin + sc * AT_KSUB;
-      // S = Q K^T for 64 keys: 8 n8 tiles
-      float s[8][4];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < DH / 16; ++ks) {
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-          const int row = pp * 16 + (lane & 7) + ((lane >> 4) << 3);
-          const int ch = 2 * ks + ((lane >> 3) & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(sK + tile_off<DH>(row, ch), b0, b1, b2, b3);
-          mma_bf16_16816(s[2 * pp], qa[ks], b0, b1);
-          mma_bf16_16816(s[2 * pp + 1], qa[ks], b2, b3);
-        }
-      }
-      // online softmax over this sub-chunk (base-2 exponent, scale folded in)
-      float mnew[2] = {mrow[0], mrow[1]};
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int key = kbase + j * 8 + 2 * tg + (q & 1);
-          s[j][q] = (key < k_end) ? s[j][q] * p.scale_log2 : -INFINITY;
-          mnew[q >> 1] = fmaxf(mnew[q >> 1], s[j][q]);
-        }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        mnew[h] = fmaxf(mnew[h], __shfl_xor_sync(0xffffffffu, mnew[h], 1));
-        mnew[h] = fmaxf(mnew[h], __shfl_xor_sync(0xffffffffu, mnew[h], 2));
+        lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
+        lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
       }
-      float alpha[2], lsum[2] = {0.f, 0.f};
-#pragma unroll
-      for (int h = 0; h < 2; ++h) alpha[h] = (mrow[h] == -INFINITY) ? 0.f : exp2f(mrow[h] - mnew[h]);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float e = exp2f(s[j][q] - mnew[q >> 1]);
-          s[j][q] = e;
-          lsum[q >> 1] += e;
-        }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        lrow[h] = lrow[h] * alpha[h] + lsum[h];
-        mrow[h] = mnew[h];
-      }
+      const int r0 = warp * 16 + gq, r1 = r0 + 8;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        acc[j][0] *= alpha[0];
-        acc[j][1] *= alpha[0];
-        acc[j][2] *= alpha[1];
-        acc[j][3] *= alpha[1];
+        const int col = j * 8 + 2 * tg;
+        __stcg((float2*)&part[r0 * AT_DP + 4 + col], make_float2(acc[j][0], acc[j][1]));
+        __stcg((float2*)&part[r1 * AT_DP + 4 + col], make_float2(acc[j][2], acc[j][3]));
       }
-      // O += P V, P as bf16 hi + lo
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t ph[4], pl[4];
-        const float* s0 = s[2 * kk];
-        const float* s1 = s[2 * kk + 1];
-        const float v[8] = {s0[0], s0[1], s0[2], s0[3], s1[0], s1[1], s1[2], s1[3]};
-        float hi[8], lo[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          hi[q] = __bfloat162float(__float2bfloat16_rn(v[q]));
-          lo[q] = v[q] - hi[q];
-        }
-        ph[0] = pack_bf16(hi[0], hi[1]);
-        ph[1] = pack_bf16(hi[2], hi[3]);
-        ph[2] = pack_bf16(hi[4], hi[5]);
-        ph[3] = pack_bf16(hi[6], hi[7]);
-        pl[0] = pack_bf16(lo[0], lo[1]);
-        pl[1] = pack_bf16(lo[2], lo[3]);
-        pl[2] = pack_bf16(lo[4], lo[5]);
-        pl[3] = pack_bf16(lo[6], lo[7]);
-#pragma unroll
-        for (int np = 0; np < NT / 2; ++np) {
-          const int row = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-          const int ch = np * 2 + (lane >> 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(sV + tile_off<DH>(row, ch), b0, b1, b2, b3);
-          mma_bf16_16816(acc[2 * np], ph, b0, b1);
-          mma_bf16_16816(acc[2 * np + 1], ph, b2, b3);
-          mma_bf16_16816(acc[2 * np], pl, b0, b1);
-          mma_bf16_16816(acc[2 * np + 1], pl, b2, b3);
-        }
+      if (tg == 0) {
+        __stcg((float2*)&part[r0 * AT_DP], make_float2(mrow[0], lrow[0]));
+        __stcg((float2*)&part[r1 * AT_DP], make_float2(mrow[1], lrow[1]));
       }
     }
     __syncthreads();
   }
-  cp_async_wait<0>();
-
-  // ---- partial of this split: per query row (max, sum, unnormalised O) ------
-  const int DP = DH + 4;   // (max, sum, 2 pad, output) keeps the output 16-byte aligned
-  const int bgq = (b * p.G + g) * p.qgroups + qg;
-  float* part = p.part + ((int64_t)bgq * p.nsplit_max + split) * 64 * DP;
-  if (active) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
-      lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
-    }
-    const int r0 = warp * 16 + gq, r1 = r0 + 8;
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int col = j * 8 + 2 * tg;
-      *(float2*)&part[r0 * DP + 4 + col] = make_float2(acc[j][0], acc[j][1]);
-      *(float2*)&part[r1 * DP + 4 + col] = make_float2(acc[j][2], acc[j][3]);
-    }
-    if (tg == 0) {
-      part[r0 * DP] = mrow[0];
-      part[r0 * DP + 1] = lrow[0];
-      part[r1 * DP] = mrow[1];
-      part[r1 * DP + 1] = lrow[1];
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  __shared__ int is_last;
-  if (tid == 0) {
-    const int old = atomicAdd(&p.counters[bgq], 1);
-    is_last = (old == nsplit - 1);
-    if (is_last) p.counters[bgq] = 0;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // ---- combine the splits of (b, g, q-group) in split order ------------------
-  // (max, sum) of every (split, row) go to shared memory (the K/V buffers are
-  // free now); each row's split weights are formed there; then thread c owns
-  // output column c of every row and accumulates the splits in order, with
-  // the loads of all rows of one split in flight together.
-  const float* base = p.part + (int64_t)bgq * p.nsplit_max * 64 * DP;
-  float* ml = reinterpret_cast<float*>(smem + 64 * DH * 2);        // [nsplit][64][2]
-  float* inv = ml + 2 * 64 * AT_MAX_SPLITS;                         // [64]
-  for (int e = tid; e < nsplit * 64; e += AT_THREADS) {
-    const int s2 = e >> 6, r = e & 63;
-    const float* pr = base + ((int64_t)s2 * 64 + r) * DP;
-    ml[2 * e] = r < qrows ? __ldcg(&pr[0]) : 0.f;
-    ml[2 * e + 1] = r < qrows ? __ldcg(&pr[1]) : 0.f;
-  }
-  __syncthreads();
-  if (tid < 64) {
-    float M = -INFINITY;
-    for (int s2 = 0; s2 < nsplit; ++s2) M = fmaxf(M, ml[2 * (s2 * 64 + tid)]);
-    float lt = 0.f;
-    for (int s2 = 0; s2 < nsplit; ++s2) {
-      const float ms = ml[2 * (s2 * 64 + tid)];
-      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      lt += ml[2 * (s2 * 64 + tid) + 1] * w;
-      ml[2 * (s2 * 64 + tid)] = w;
-    }
-    inv[tid] = 1.0f / lt;
-  }
-  __syncthreads();
-  // each warp owns 16 query rows; its lanes cover one row's DH columns with
-  // one float4 each (a coalesced 512-byte row read); 8 rows x 2 splits of
-  // loads are in flight together and the splits are added in order
-  static_assert(DH == 128, "combine maps 32 lanes x float4 onto a 128-wide row");
-  for (int rc = warp * 16; rc < warp * 16 + 16 && rc < qrows; rc += 8) {
-    float4 o[8];
-#pragma unroll
-    for (int rr = 0; rr < 8; ++rr) o[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < nsplit; s0 += 2) {
-      float4 v[2][8];
-      float w[2][8];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int s2 = min(s0 + u, nsplit - 1);
-#pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          const int r = min(rc + rr, qrows - 1);
-          v[u][rr] = __ldcg((const float4*)(base + ((int64_t)s2 * 64 + r) * DP + 4) + lane);
-          w[u][rr] = (s0 + u < nsplit) ? ml[2 * (s2 * 64 + r)] : 0.f;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          o[rr].x += v[u][rr].x * w[u][rr];
-          o[rr].y += v[u][rr].y * w[u][rr];
-          o[rr].z += v[u][rr].z * w[u][rr];
-          o[rr].w += v[u][rr].w * w[u][rr];
-        }
-    }
-#pragma unroll
-    for (int rr = 0; rr < 8; ++rr) {
-      const int r = rc + rr;
-      if (r >= qrows) break;
-      const int qr = q0 + r, hh = qr / p.B, i = qr - hh * p.B;
-      bf16* dst = p.o + (int64_t)(b * p.B + i) * (p.H * DH) + (int64_t)(g * p.rep + hh) * DH + 4 * lane;
-      const float iv = inv[r];
-      __nv_bfloat162 t0 = __floats2bfloat162_rn(o[rr].x * iv, o[rr].y * iv);
-      __nv_bfloat162 t1 = __floats2bfloat162_rn(o[rr].z * iv, o[rr].w * iv);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&t0);
-      pk.y = *reinterpret_cast<uint32_t*>(&t1);
-      *reinterpret_cast<uint2*>(dst) = pk;
-    }
-  }
 }
 
-// Splits per (b, g, q-group): about two CTAs per SM over the whole batch.
-static int attn_nsplit_target(const dflash_handle* h, int batch, int B) {
-  const dflash_config& c = h->cfg;
-  const int rep = c.n_heads / c.n_kv_heads, qgroups = (B * rep + 63) / 64;
-  const int64_t units = (int64_t)batch * c.n_kv_heads * qgroups;
-  return (int)std::min<int64_t>(AT_MAX_SPLITS,
-                                std::max<int64_t>(1, (2 * h->num_sms + units - 1) / units));
-}
-
-// Keys per split: the longest sequence divided over at most the target split
-// count, using splits of at least AT_MIN_SPLIT keys (fewer, longer splits for
-// short contexts), rounded up to a multiple of 64.  Splits start at fixed key
-// positions, so a key's split does not depend on the other sequences.
-int attn_split_keys(const dflash_handle* h, int batch, int B, int cap) {
-  const int64_t keys = (int64_t)cap + B;
-  int64_t t = attn_nsplit_target(h, batch, B);
-  t = std::max<int64_t>(1, std::min<int64_t>(t, (keys + AT_MIN_SPLIT - 1) / AT_MIN_SPLIT));
-  int64_t s = (keys + t - 1) / t;
-  return (int)(((s + 63) / 64) * 64);
-}
-
-size_t attn_scratch_bytes(const dflash_handle* h, int batch, int B) {
-  const dflash_config& c = h->cfg;
-  const int rep = c.n_heads / c.n_kv_heads, qgroups = (B * rep + 63) / 64;
-  return (size_t)batch * c.n_kv_heads * qgroups * attn_nsplit_target(h, batch, B) * 64 *
-             (c.head_dim + 4) * sizeof(float) + 256;
+// ---- combine: one warp per (unit, query row), items added in key order ------
+template <int DH>
+__global__ void __launch_bounds__(AT_COMB_WARPS * 32) attn_combine_kernel(const AttnParams p) {
+  static_assert(DH == 128, "the combine maps 32 lanes x float4 onto a 128-wide row");
+  __shared__ float wsm[AT_COMB_WARPS][AT_MAX_ITEMS_UNIT];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gr = blockIdx.x * AT_COMB_WARPS + warp;
+  const int u = gr >> 6, r = gr & 63;
+  if (u >= p.units) return;
+  const int qg = u % p.qgroups, bg = u / p.qgroups;
+  const int g = bg % p.G, b = bg / p.G;
+  const int q0 = qg * 64, qrows = min(64, p.B * p.rep - q0);
+  if (r >= qrows) return;
+  const int i0 = p.unit_begin[u], ns = p.unit_begin[u + 1] - i0;
+  if (ns <= 0 || ns > AT_MAX_ITEMS_UNIT) return;   // no items: the plan flagged a bad length
+  const float* base = p.part + ((int64_t)i0 * 64 + r) * AT_DP;
+  const int64_t stride = 64 * AT_DP;
+  float M = -INFINITY;
+  for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(base + s * stride));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float lt = 0.f;
+  for (int s = lane; s < ns; s += 32) {
+    const float2 ml = __ldcg((const float2*)(base + s * stride));
+    const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+    wsm[warp][s] = w;
+    lt += ml.y * w;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, o);
+  __syncwarp();
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int s = min(s0 + k, ns - 1);
+      v[k] = __ldcg((const float4*)(base + s * stride + 4) + lane);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float w = (s0 + k < ns) ? wsm[warp][s0 + k] : 0.f;
+      acc.x += v[k].x * w;
+      acc.y += v[k].y * w;
+      acc.z += v[k].z * w;
+      acc.w += v[k].w * w;
+    }
+  }
+  const float iv = 1.0f / lt;
+  const int qr = q0 + r, hh = qr / p.B, i = qr - hh * p.B;
+  bf16* dst = p.o + (int64_t)(b * p.B + i) * (p.H * DH) + (int64_t)(g * p.rep + hh) * DH + 4 * lane;
+  __nv_bfloat162 t0 = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
+  __nv_bfloat162 t1 = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&t0);
+  pk.y = *reinterpret_cast<uint32_t*>(&t1);
+  *reinterpret_cast<uint2*>(dst) = pk;
 }
 
 bool attn_fast_ok(const dflash_handle* h, int B) {
@@ -380,11 +450,45 @@ bool attn_fast_ok(const dflash_handle* h, int B) {
   return c.dtype == DFLASH_BF16 && c.head_dim == 128 && h->num_sms > 0 && B >= 1;
 }
 
+static void pdl_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, dim3 grid, dim3 block,
+                       size_t smem, cudaStream_t s) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->gridDim = grid;
+  cfg->blockDim = block;
+  cfg->dynamicSmemBytes = smem;
+  cfg->stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
+
+int attn_plan(dflash_handle* h, cudaStream_t s, const int32_t* len, int cap, int batch, int B,
+              float* scratch) {
+  const dflash_config& c = h->cfg;
+  const int rep = c.n_heads / c.n_kv_heads, qgroups = (B * rep + 63) / 64;
+  const int units = attn_units(h, batch, B);
+  const int64_t mi = attn_max_items(h, batch, B);
+  if (mi > 0x7fffffff || (int64_t)units * 64 > 0x7fffffff) return DFLASH_ERR_SHAPE;
+  const AttnScratch sc = attn_carve(scratch, units, mi);
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  pdl_config(&cfg, attr, dim3(1), dim3(256), 0, s);
+  Timer t;
+  launch_begin(h, DFLASH_K_ATTENTION, s, &t);
+  cudaLaunchKernelEx(&cfg, attn_plan_kernel, len, batch, B, cap, c.n_kv_heads * qgroups,
+                     attn_slots(h), (int)mi, sc.hdr, sc.unit_begin, sc.items, h->d_status);
+  return launch_end(h, s, &t);
+}
+
 int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* kc, const void* vc,
                    int cap, const int32_t* len, const void* kb, const void* vb, int batch, int B,
                    void* o, float* scratch) {
   const dflash_config& c = h->cfg;
   constexpr int DH = 128;
+  const int units = attn_units(h, batch, B);
+  const int64_t mi = attn_max_items(h, batch, B);
+  const AttnScratch sc = attn_carve(scratch, units, mi);
   AttnParams p;
   p.q = (const bf16*)q;
   p.kc = (const bf16*)kc;
@@ -398,19 +502,16 @@ int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* 
   p.H = c.n_heads;
   p.G = c.n_kv_heads;
   p.rep = c.n_heads / c.n_kv_heads;
-  p.split = attn_split_keys(h, batch, B, cap);
-  p.scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
-  p.part = scratch;
   p.qgroups = (B * p.rep + 63) / 64;
-  p.nsplit_max = (cap + B + p.split - 1) / p.split;
-  p.counters = h->d_counters;
+  p.units = units;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
+  p.n_items = sc.hdr;
+  p.items = sc.items;
+  p.unit_begin = sc.unit_begin;
+  p.part = sc.part;
   p.status = h->d_status;
-  if ((int64_t)batch * p.G * p.qgroups > kMaxTiles) return DFLASH_ERR_SHAPE;
-  // main loop: Q + AT_STAGES x (K, V) sub-chunks; combine: Q region + (max,
-  // sum) per (split, row) + 64 inverse sums
-  const size_t smem = std::max<size_t>((size_t)(64 + 2 * AT_STAGES * AT_KSUB) * DH * 2,
-                                       (size_t)64 * DH * 2 + (2 * 64 * AT_MAX_SPLITS + 64) * 4) +
-                      128;
+  // Q + AT_STAGES x (K, V) sub-chunks
+  const size_t smem = (size_t)(64 + 2 * AT_STAGES * AT_KSUB) * DH * 2 + 128;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_split_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -418,19 +519,19 @@ int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* 
       return DFLASH_ERR_CUDA;
     attr_set = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.nsplit_max, p.G, batch * p.qgroups);
-  cfg.blockDim = dim3(AT_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
+  const int grid = (int)std::min<int64_t>(mi, attn_slots(h));
+  cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  pdl_config(&cfg, attr, dim3(grid), dim3(AT_THREADS), smem, s);
   Timer t;
   launch_begin(h, DFLASH_K_ATTENTION, s, &t);
   cudaLaunchKernelEx(&cfg, attn_split_kernel<DH>, p);
+  int rc = launch_end(h, s, &t);
+  if (rc) return rc;
+  const int cgrid = (units * 64 + AT_COMB_WARPS - 1) / AT_COMB_WARPS;
+  pdl_config(&cfg, attr, dim3(cgrid), dim3(AT_COMB_WARPS * 32), 0, s);
+  launch_begin(h, DFLASH_K_ATTENTION, s, &t);
+  cudaLaunchKernelEx(&cfg, attn_combine_kernel<DH>, p);
   return launch_end(h, s, &t);
 }
 

@@ -11,10 +11,16 @@
 //     consume: 4 weight-row quarters x 2 k-halves), prefetching the first weight chunks before waiting for the
 //     previous kernel (programmatic dependent launch);
 //   * multiplies with warp-level bf16 MMA (m16n8k16, fp32 accumulate);
-//   * combines the k-split partial sums of a tile in a fixed order in the
-//     CTA that finishes the tile last, then runs a fused epilogue: fp32
-//     store, residual add, SwiGLU, per-head RMSNorm + RoPE (+ cache append),
-//     or a top-2 argmax whose last tile merges the whole vocabulary.
+//   * finishes a tile it owns whole with a fused epilogue (fp32 store,
+//     residual add, SwiGLU, per-head RMSNorm + RoPE (+ cache append), or
+//     per-row top-2 records of an LM-head tile) and writes the partial sums
+//     of the (at most two) tiles it shares with neighbours;
+//   * after a bounded grid barrier (the grid is co-resident: a cooperative
+//     launch of at most two CTAs per SM) gives every (shared tile, row
+//     block) to one warp of the grid, which adds the contributors' partials
+//     in k order and runs the same epilogue per row;
+//   * for the LM head, after a second barrier, merges each row's top-2
+//     records over the vocabulary (one warp per row).
 #include <string.h>
 
 #include "common.cuh"
@@ -40,6 +46,7 @@ constexpr int WS_CW = 4 * WS_KSPLIT;
 constexpr int WS_CT = WS_CW * 32;
 constexpr int WS_THREADS = 32 + WS_CT;
 constexpr int WS_EPAD = 132;
+constexpr int WS_MAXLIST = 1024;   // CTAs per launch at most (one shared tile per CTA boundary)
 
 struct WParams {
   CUtensorMap wmap[WS_MAXMAP];
@@ -47,7 +54,9 @@ struct WParams {
   WSeg seg[WS_MAXMAP];
   int nseg, n_tiles, kc, kc_per_src, M, grid, units;
   float* partial;
-  int* counters;
+  int* counters;        // arrival count per tile (last-arriver fix-up)
+  int* bar;             // grid barrier word (zero between launches)
+  int row_batch;        // rows per reduce task: 4 when tiles have few contributors, else 1
   int* status;
   RowMap rm;
   const int32_t* len;
@@ -55,7 +64,6 @@ struct WParams {
   int max_pos;
   float eps;
   float4* amx;
-  int* amx_done;
   int32_t* ids;
   float* gap;
   int rps_out;
@@ -80,7 +88,7 @@ struct WCfg {
   static constexpr int STAGE_TX = W_BYTES + A_BYTES;
   // deepest ring that fits the shared memory of one of WS_MINBLOCKS CTAs per SM
   static constexpr int BUDGET = DFLASH_WS_MINBLOCKS == 1 ? 232448 : 233472 / DFLASH_WS_MINBLOCKS - 1024;
-  static constexpr int FIXED = MT * 16 * WS_EPAD * 4 + 2 * 16 * 8 + 64 + 64 * 8 + 1024;
+  static constexpr int FIXED = MT * 16 * WS_EPAD * 4 + 2 * 16 * 8 + 64 + 64 * 8 + 4 * (WS_MAXLIST + 4) + 1024;
   static constexpr int FIT = (BUDGET - FIXED) / STAGE_TX;
   static constexpr int STAGES = FIT < DFLASH_WS_STAGES ? FIT : DFLASH_WS_STAGES;
   static_assert(STAGES >= 2, "ring too shallow");
@@ -89,7 +97,8 @@ struct WCfg {
   static constexpr int E_FLOATS = MT * 16 * WS_EPAD;
   static constexpr int OFF_BAR = OFF_E + E_FLOATS * 4;
   static constexpr int OFF_MISC = OFF_BAR + 2 * STAGES * 8;
-  static constexpr int SMEM = OFF_MISC + 64 + 64 * 8 + 1024;
+  static constexpr int OFF_LIST = OFF_MISC + 64 + 64 * 8;   // shared tiles, then their count
+  static constexpr int SMEM = OFF_LIST + 4 * (WS_MAXLIST + 4) + 1024;
 };
 
 __device__ __forceinline__ int seg_of(const WParams& p, int t) {
@@ -263,51 +272,214 @@ __device__ void ws_epilogue(const WParams& p, int t, const float* E, volatile in
       tt = top2_warp(tt);
       if (lane == 0) p.amx[(int64_t)t * M + r] = make_float4(tt.t1, __int_as_float(tt.i1), tt.t2, 0.f);
     }
-    __threadfence();
-    named_bar(1, WS_CT);
-    if (tid == 0) {
-      const int old = atomicAdd(p.amx_done, 1);
-      const int last = (old == p.n_tiles - 1);
-      if (last) *p.amx_done = 0;
-      misc[1] = last;
-    }
-    named_bar(1, WS_CT);
-    if (!misc[1]) return;
-    __threadfence();
-    for (int r = cw; r < M; r += WS_CW) {
-      Top2 tt{-INFINITY, 0x7fffffff, -INFINITY};
-      for (int t0 = 0; t0 < p.n_tiles; t0 += 32 * 8) {
-        float4 rec[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int ti = t0 + lane + 32 * q;
-          rec[q] = ti < p.n_tiles ? __ldcg(&p.amx[(int64_t)ti * M + r])
-                                  : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY, 0.f);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          Top2 u{rec[q].x, __float_as_int(rec[q].y), rec[q].z};
-          tt = top2_merge(tt, u);
-        }
+  }
+}
+
+// ---- per-row epilogue of a reduced tile row (one warp, lane = 4 columns) -----
+__device__ void ws_row(const WParams& p, int t, int r, float4 v, const int* rowpos) {
+  const int lane = threadIdx.x & 31;
+  const WSeg& g = p.seg[seg_of(p, t)];
+  const int lt = t - g.t0;
+  float x[4] = {v.x, v.y, v.z, v.w};
+  if (g.kind == SK_F32 || g.kind == SK_RESID) {
+    const int n = lt * 128 + 4 * lane;
+    if (n < g.n_valid) {   // n_valid and ld are multiples of 4 here
+      float4* o = (float4*)((float*)g.dst + (int64_t)r * g.ld + n);
+      if (g.kind == SK_RESID) {
+        const float4 a = *o;
+        x[0] += a.x;
+        x[1] += a.y;
+        x[2] += a.z;
+        x[3] += a.w;
       }
-      tt = top2_warp(tt);
-      if (lane == 0) {
-        int64_t out = r, gout = r;
-        if (p.rps_out > 0) {
-          const int per = p.rps_out - 1;
-          const int64_t b = r / per, i = r % per + 1;
-          out = b * p.rps_out + i;
-          gout = b * per + (i - 1);
-          if (i == 1) p.ids[b * p.rps_out] = p.anchor[b];
-        }
-        p.ids[out] = tt.i1;
-        if (p.gap) p.gap[gout] = tt.t1 - tt.t2;
+      *o = make_float4(x[0], x[1], x[2], x[3]);
+    }
+  } else if (g.kind == SK_SWIGLU) {
+    // columns 0-63 of the tile are gate rows, 64-127 the matching up rows
+    float u[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) u[q] = __shfl_xor_sync(0xffffffffu, x[q], 16);
+    if (lane < 16) {
+      bf16* dst = (bf16*)g.dst + (int64_t)r * g.ld;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int f = lt * 64 + 4 * lane + q;
+        if (f < g.n_valid) dst[f] = __float2bfloat16_rn(x[q] / (1.0f + expf(-x[q])) * u[q]);
+      }
+    }
+  } else if (g.kind == SK_HEAD) {
+    // d = 128: one head per tile row; d = 64: two, one per half-warp
+    const int d = g.d, half = d >> 1;
+    const int hl = d == 128 ? lane : (lane & 15);
+    const int head = lt * (128 / d) + (d == 128 ? 0 : (lane >> 4));
+    if (g.gain != nullptr) {
+      float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+      if (d == 128) ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float rinv = 1.0f / sqrtf(ss / (float)d + p.eps);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) x[q] = x[q] * rinv * g.gain[4 * hl + q];
+    }
+    float px[4];   // the element half a head away (the other RoPE operand)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) px[q] = __shfl_xor_sync(0xffffffffu, x[q], d == 128 ? 16 : 8);
+    const int b = rowpos[2 * r], pos = rowpos[2 * r + 1];   // sequence, position (-1: skip)
+    if (b < 0) return;                                      // row not appended by this call
+    if (g.rope) {
+      if (pos < 0 || pos >= p.max_pos) {
+        if (lane == 0) atomicOr(p.status, ST_BOUNDS);
+        return;
+      }
+      const bool lo_half = 4 * hl < half;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = (4 * hl + q) - (lo_half ? 0 : half);
+        const float2 cs = p.rope_tab[(int64_t)pos * half + i];
+        x[q] = lo_half ? x[q] * cs.x - px[q] * cs.y : x[q] * cs.x + px[q] * cs.y;
+      }
+    }
+    bf16* o;
+    if (g.cache_cap > 0) {
+      if (b >= g.cache_batch || pos < 0 || pos >= g.cache_cap) {
+        if (lane == 0) atomicOr(p.status, ST_CAPACITY);
+        return;
+      }
+      o = (bf16*)g.dst + (((int64_t)b * g.cache_heads + head) * g.cache_cap + pos) * d;
+    } else {
+      o = (bf16*)g.dst + (int64_t)r * g.ld + (int64_t)head * d;
+    }
+    __nv_bfloat162 t0 = __floats2bfloat162_rn(x[0], x[1]);
+    __nv_bfloat162 t1 = __floats2bfloat162_rn(x[2], x[3]);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&t0);
+    pk.y = *reinterpret_cast<uint32_t*>(&t1);
+    *reinterpret_cast<uint2*>(o + 4 * hl) = pk;
+  } else if (g.kind == SK_ARGMAX) {
+    Top2 tt{-INFINITY, 0x7fffffff, -INFINITY};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int n = lt * 128 + 4 * lane + q;
+      if (n < g.n_valid) tt = top2_merge(tt, Top2{x[q], n, -INFINITY});
+    }
+    tt = top2_warp(tt);
+    if (lane == 0) p.amx[(int64_t)t * p.M + r] = make_float4(tt.t1, __int_as_float(tt.i1), tt.t2, 0.f);
+  }
+}
+
+// ---- grid barrier (bounded; every CTA of the grid is resident) ---------------
+__device__ bool ws_grid_wait(const WParams& p, int target) {
+  if (ld_acquire_gpu(p.bar) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  for (int it = 0;; ++it) {
+    if (ld_acquire_gpu(p.bar) >= target) return true;
+    if ((it & 63) == 63) {
+      if (*(volatile int*)p.status & ST_TIMEOUT) return false;
+      if (globaltimer() - t0 > 2000000000ull) {
+        atomicOr(p.status, ST_TIMEOUT);
+        return false;
       }
     }
   }
 }
+// Consumers of every CTA arrive; true once all CTAs have arrived k times.
+// After a timeout (here or in another CTA) the CTA stops taking part.
+__device__ bool ws_grid_sync(const WParams& p, int k, volatile int* misc, int tid) {
+  named_bar(1, WS_CT);
+  if (tid == 0) {
+    bool go = misc[0] == 0;
+    red_release_gpu_add(p.bar, 1);
+    if (go && !ws_grid_wait(p, k * p.grid)) {
+      misc[0] = 1;
+      go = false;
+    }
+    misc[4] = go;
+  }
+  named_bar(1, WS_CT);
+  return misc[4] != 0;
+}
 
-template <int MT>
+// ---- shared tiles: one warp per (tile, block of RB rows) over the grid -------
+// A tile is shared when a CTA boundary falls strictly inside it (every CTA
+// lists these tiles at its start).  Contributor c's partial of tile t is its
+// first slot if t is c's first tile, else its second.
+template <int MT, int RB>
+__device__ void ws_reduce(const WParams& p, const int* rowpos, const int* list) {
+  constexpr int CB = 16 / RB;   // contributors whose loads are in flight together
+  const int cw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
+  const int64_t U = p.units, G = p.grid;
+  const int nwarps = p.grid * WS_CW, gw = blockIdx.x * WS_CW + cw;
+  const int rblocks = (p.M + RB - 1) / RB;
+  const int ntask = list[WS_MAXLIST] * rblocks;
+  for (int k = gw; k < ntask; k += nwarps) {
+    const int t = list[k / rblocks], r0 = (k - (k / rblocks) * rblocks) * RB;
+    const int lo = unit_owner((int64_t)t * p.kc, U, G);
+    const int hi = unit_owner((int64_t)t * p.kc + p.kc - 1, U, G);
+    float4 sum[RB];
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr) sum[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = lo; c0 <= hi; c0 += CB) {
+      float4 v[CB][RB];
+#pragma unroll
+      for (int j = 0; j < CB; ++j) {
+        const int cc = min(c0 + j, hi);
+        const int slot = 2 * cc + (first_unit(cc, U, G) / p.kc == t ? 0 : 1);
+        const float* base = p.partial + (int64_t)slot * (MT * 16 * 128) + 4 * lane;
+#pragma unroll
+        for (int rr = 0; rr < RB; ++rr)
+          v[j][rr] = __ldcg((const float4*)(base + min(r0 + rr, p.M - 1) * 128));
+      }
+#pragma unroll
+      for (int j = 0; j < CB; ++j)
+        if (c0 + j <= hi)
+#pragma unroll
+          for (int rr = 0; rr < RB; ++rr) {
+            sum[rr].x += v[j][rr].x;
+            sum[rr].y += v[j][rr].y;
+            sum[rr].z += v[j][rr].z;
+            sum[rr].w += v[j][rr].w;
+          }
+    }
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr)
+      if (r0 + rr < p.M) ws_row(p, t, r0 + rr, sum[rr], rowpos);
+  }
+}
+
+// ---- LM head: each row's top-2 over all vocabulary tiles (one warp per row) --
+__device__ void ws_merge(const WParams& p) {
+  const int cw = (threadIdx.x >> 5) - 1, lane = threadIdx.x & 31;
+  const int nwarps = p.grid * WS_CW, gw = blockIdx.x * WS_CW + cw;
+  for (int r = gw; r < p.M; r += nwarps) {
+    Top2 tt{-INFINITY, 0x7fffffff, -INFINITY};
+    for (int t0 = 0; t0 < p.n_tiles; t0 += 32 * 16) {
+      float4 rec[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int ti = t0 + lane + 32 * q;
+        rec[q] = ti < p.n_tiles ? __ldcg(&p.amx[(int64_t)ti * p.M + r])
+                                : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) tt = top2_merge(tt, Top2{rec[q].x, __float_as_int(rec[q].y), rec[q].z});
+    }
+    tt = top2_warp(tt);
+    if (lane == 0) {
+      int64_t out = r, gout = r;
+      if (p.rps_out > 0) {
+        const int per = p.rps_out - 1;
+        const int64_t b = r / per, i = r % per + 1;
+        out = b * p.rps_out + i;
+        gout = b * per + (i - 1);
+        if (i == 1) p.ids[b * p.rps_out] = p.anchor[b];
+      }
+      p.ids[out] = tt.i1;
+      if (p.gap) p.gap[gout] = tt.t1 - tt.t2;
+    }
+  }
+}
+
+template <int MT, bool GB>
 __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kernel(const __grid_constant__ WParams p) {
   using C = WCfg<MT>;
   extern __shared__ uint8_t smem_raw[];
@@ -422,8 +594,30 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
     __syncwarp();
   } else {
     // ---------------- consumers: warps 1-4, 32 weight rows each -------------
-    pdl_wait();
     const int cw = warp - 1, tid = threadIdx.x - 32;
+    if (GB && cw == 0) {
+      // the shared tiles (a CTA boundary strictly inside), each listed once
+      // at its first such boundary; depends on the launch shape only
+      int* list = (int*)(smem + C::OFF_LIST);
+      int n_shared = 0;
+      for (int c0 = 1; c0 < p.grid; c0 += 32) {
+        const int c = c0 + lane;
+        int t = -1;
+        if (c < p.grid) {
+          const int fb = first_unit(c, U, G);
+          if (fb % p.kc != 0) {
+            const int fp = first_unit(c - 1, U, G);
+            t = fb / p.kc;
+            if (c > 1 && fp % p.kc != 0 && fp / p.kc == t) t = -1;
+          }
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, t >= 0);
+        if (t >= 0) list[n_shared + __popc(m & ((1u << lane) - 1u))] = t;
+        n_shared += __popc(m);
+      }
+      if (lane == 0) list[WS_MAXLIST] = n_shared;
+    }
+    pdl_wait();
     const int nq = cw & 3, kh = cw >> 2;   // weight-row quarter, k-slice of each chunk
     // sequence and cache position of each activation row (head epilogues)
     int* rowpos = (int*)(smem + C::OFF_MISC + 64);
@@ -467,14 +661,20 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
         named_bar(1, WS_CT);
       }
       if (!full_tile) {
+        // a tile shared with neighbouring CTAs: its partial goes to this
+        // CTA's first or second slot
         constexpr int IT = MT * 512 / WS_CT;   // float4s of a tile per consumer thread
         const int first_tile = u0 / p.kc;
         float4* slot = (float4*)(p.partial + (int64_t)(2 * cta + (t == first_tile ? 0 : 1)) * (MT * 16 * 128));
 #pragma unroll
         for (int q = 0; q < IT; ++q) {
           const int e4 = tid + q * WS_CT, e = e4 * 4;
-          slot[e4] = *(const float4*)&E[(e >> 7) * WS_EPAD + (e & 127)];
+          __stcg(slot + e4, *(const float4*)&E[(e >> 7) * WS_EPAD + (e & 127)]);
         }
+        if (GB) return;   // finished after the grid barrier
+        // otherwise the contributor that arrives last sums the partials in CTA
+        // (= k) order, with the loads of up to 8 contributors x all of a
+        // thread's float4s issued first, and runs the epilogue
         __threadfence();
         named_bar(1, WS_CT);
         const int lo = unit_owner((int64_t)t * p.kc, U, G);
@@ -488,8 +688,6 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
         named_bar(1, WS_CT);
         if (!misc[1]) return;
         __threadfence();
-        // sum the contributors' partial tiles in CTA (= k) order; the loads of
-        // up to 8 contributors x all of a thread's float4s are issued first
         float4 sum[IT];
 #pragma unroll
         for (int q = 0; q < IT; ++q) sum[q] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -589,6 +787,24 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
     }
     if (cur >= 0) flush(cur);
     if (tid == 0) misc[3] = consumed;
+    // ---- shared tiles, then (LM head) the vocabulary merge ------------------
+    if (GB) {
+    const bool argmax = p.seg[0].kind == SK_ARGMAX;
+    if (ws_grid_sync(p, 1, misc, tid)) {
+      const int* list = (const int*)(smem + C::OFF_LIST);
+      if (p.row_batch == 4)
+        ws_reduce<MT, 4>(p, rowpos, list);
+      else
+        ws_reduce<MT, 1>(p, rowpos, list);
+    }
+    if (argmax && ws_grid_sync(p, 2, misc, tid)) ws_merge(p);
+    named_bar(1, WS_CT);
+    if (tid == 0) {
+      red_release_gpu_add(p.bar, 1);   // this CTA polls the barrier no more
+      // once every CTA has left, the first one clears the word for the next launch
+      if (blockIdx.x == 0 && !misc[0] && ws_grid_wait(p, (argmax ? 3 : 2) * p.grid)) *p.bar = 0;
+    }
+    }
   }
   __syncthreads();
   if (misc[0] && threadIdx.x == 0) {
@@ -601,29 +817,47 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
 }
 
 // ---------------------------------------------------------------------------
-template <int MT>
-static int launch_wstream(dflash_handle* h, cudaStream_t s, int kclass, const WParams& prm) {
+// GB: the LM head (top-2 records, then a merge over the vocabulary) runs
+// with grid barriers and is launched cooperatively; the other projections
+// finish shared tiles in the contributor that arrives last.  Both may start
+// early (programmatic dependent launch).
+template <int MT, bool GB>
+static int launch_wstream(dflash_handle* h, cudaStream_t s, int kclass, WParams prm) {
   using C = WCfg<MT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(wstream_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM) != cudaSuccess)
+  static int occ = -1;
+  if (occ < 0) {
+    int o = 0;
+    if (cudaFuncSetAttribute(wstream_kernel<MT, GB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, wstream_kernel<MT, GB>, WS_THREADS,
+                                                      C::SMEM) != cudaSuccess)
       return DFLASH_ERR_CUDA;
-    attr_set = true;
+    occ = std::min(o, DFLASH_WS_MINBLOCKS);
   }
+  if (occ < 1 || (int64_t)occ * h->num_sms > WS_MAXLIST) return DFLASH_ERR_UNSUPPORTED;
+  // every CTA resident at once (a grid barrier waits for all of them)
+  prm.grid = (int)std::min<int64_t>(prm.units, (int64_t)occ * h->num_sms);
+  const int64_t per = prm.units / prm.grid;                 // units of the smallest CTA
+  const int64_t contributors = (prm.kc + per - 1) / per + 1;  // at most, per shared tile
+  prm.row_batch = contributors <= 4 ? 4 : 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(prm.grid);
   cfg.blockDim = dim3(WS_THREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na++].val.programmaticStreamSerializationAllowed = 1;
+  if (GB) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na++].val.cooperative = 1;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   Timer t;
   launch_begin(h, kclass, s, &t);
-  cudaLaunchKernelEx(&cfg, wstream_kernel<MT>, prm);
+  cudaLaunchKernelEx(&cfg, wstream_kernel<MT, GB>, prm);
   return launch_end(h, s, &t);
 }
 
@@ -653,9 +887,9 @@ int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
   prm.kc_per_src = kc_per_src;
   prm.M = L.M;
   prm.units = prm.n_tiles * prm.kc;
-  prm.grid = std::min<int>(prm.units, h->num_sms * DFLASH_WS_MINBLOCKS);
   prm.partial = partial;
   prm.counters = h->d_counters;
+  prm.bar = h->d_counters + kMaxTiles + 2;
   prm.status = h->d_status;
   prm.rm = L.rm;
   prm.len = L.len;
@@ -663,17 +897,24 @@ int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
   prm.max_pos = h->cfg.max_pos;
   prm.eps = h->cfg.rms_eps;
   prm.amx = amx;
-  prm.amx_done = h->d_counters + kMaxTiles;
   prm.ids = L.ids;
   prm.gap = L.gap;
   prm.rps_out = L.rps_out;
   prm.anchor = L.anchor;
   if (prm.n_tiles > kMaxTiles) return DFLASH_ERR_SHAPE;
+  if (L.seg[0].kind == SK_ARGMAX) {
+    switch (MT) {
+      case 1: return launch_wstream<1, true>(h, s, kclass, prm);
+      case 2: return launch_wstream<2, true>(h, s, kclass, prm);
+      case 3: return launch_wstream<3, true>(h, s, kclass, prm);
+      default: return launch_wstream<4, true>(h, s, kclass, prm);
+    }
+  }
   switch (MT) {
-    case 1: return launch_wstream<1>(h, s, kclass, prm);
-    case 2: return launch_wstream<2>(h, s, kclass, prm);
-    case 3: return launch_wstream<3>(h, s, kclass, prm);
-    default: return launch_wstream<4>(h, s, kclass, prm);
+    case 1: return launch_wstream<1, false>(h, s, kclass, prm);
+    case 2: return launch_wstream<2, false>(h, s, kclass, prm);
+    case 3: return launch_wstream<3, false>(h, s, kclass, prm);
+    default: return launch_wstream<4, false>(h, s, kclass, prm);
   }
 }
 

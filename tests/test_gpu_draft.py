@@ -248,6 +248,16 @@ def test_draft_short_block_small_bf16(dfl, B, lens):
     _random_cache_case(dfl, SMALL_BF16, B, lens, np.arange(len(lens)))
 
 
+@pytest.mark.parametrize("B,lens", [
+    (16, [0, 3000, 17, 700]),    # 64 rows: streaming launches, ragged split-attention items
+    (48, [1000]),                # 96 query rows per kv head: two query groups
+])
+def test_draft_split_attention_small_bf16(dfl, B, lens):
+    """Blocks above 16 rows run the per-projection launches and the planned
+    split attention (items cut from the device-side lengths)."""
+    _random_cache_case(dfl, SMALL_BF16, B, lens, np.arange(len(lens)))
+
+
 def test_draft_short_block_b1_batch16(dfl):
     """16 sequences of block size 1: the block is the anchors; the final
     residual still matches the oracle and the ids are the anchors."""
