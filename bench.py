@@ -166,9 +166,19 @@ class Draft:
         seed = w.seed + 100 * rank
         self.weights = synth.draft_weights(s, w.dtype, seed, device=dev)
         self.len0 = torch.tensor(self.lens, dtype=torch.int32, device=dev)
-        self.hidden = synth.target_hidden_states(rows, s.D, s.n_pick, w.dtype, seed + 1, device=dev)
-        self.anchor = torch.from_numpy(synth.anchors(self.batch, s.V, s.mask_id, seed)).to(dev)
-        self.post = torch.from_numpy(synth.random_ids((self.batch, self.B), s.V, seed + 2)).to(dev)
+        # a step's inputs (the 5 target feature slices, anchors, posterior) and
+        # results (ids, accepted, tau, bonus, tokens) each live in one buffer,
+        # so the end-to-end run moves them with one copy per direction
+        hid = synth.target_hidden_states(rows, s.D, s.n_pick, w.dtype, seed + 1, device=dev)
+        self.hidden_all = torch.stack(hid)
+        del hid
+        self.hidden = [self.hidden_all[i] for i in range(s.n_pick)]
+        nb, bb = self.batch, self.batch * self.B
+        self.ints_in = torch.empty(nb + bb, dtype=torch.int32, device=dev)
+        self.anchor = self.ints_in[:nb]
+        self.post = self.ints_in[nb:].view(nb, self.B)
+        self.anchor.copy_(torch.from_numpy(synth.anchors(nb, s.V, s.mask_id, seed)))
+        self.post.copy_(torch.from_numpy(synth.random_ids((nb, self.B), s.V, seed + 2)))
         self.start = torch.tensor(self.lens, dtype=torch.int32, device=dev)
         if not with_model:
             return
@@ -191,10 +201,14 @@ class Draft:
         self.Ht = torch.empty(rows, s.D, dtype=td, device=dev)
         self.row0 = torch.arange(0, rows, self.B, dtype=torch.int32, device=dev)
         self.nrow = torch.full((self.batch,), self.B, dtype=torch.int32, device=dev)
-        i32 = lambda *sh: torch.empty(*sh, dtype=torch.int32, device=dev)
-        self.ids, self.acc, self.tau, self.bonus = i32(self.batch, self.B), i32(self.batch), \
-            i32(self.batch), i32(self.batch)
-        self.out_tokens = i32(self.batch, self.B)
+        # results: ids and tokens [batch, B], then accepted, tau, bonus [batch],
+        # each view starting on a 16-byte boundary
+        pad = lambda n: (n + 3) // 4 * 4
+        offs = np.cumsum([0, bb, bb, pad(nb), pad(nb), pad(nb)])
+        self.ints_out = torch.empty(int(offs[-1]), dtype=torch.int32, device=dev)
+        view = lambda i, *sh: self.ints_out[int(offs[i]):int(offs[i]) + int(np.prod(sh))].view(*sh)
+        self.ids, self.out_tokens = view(0, nb, self.B), view(1, nb, self.B)
+        self.acc, self.tau, self.bonus = view(2, nb), view(3, nb), view(4, nb)
 
     def prefill(self):
         d, m = self.dfl, self.model
@@ -519,29 +533,21 @@ def run_ours(args, rank, world, local):
     total_bytes = sum(nbytes[k] for k in ("weight_gemm", "lm_head", "attention", "dense_gemm"))
     step_frac = total_bytes / (ms_step / 1e3) / 1e9 / hbm
 
-    # end to end through the C ABI from pinned host memory
-    h_hidden = [torch.empty_like(h, device="cpu").pin_memory() for h in st.hidden]
-    for hh, hd in zip(h_hidden, st.hidden):
-        hh.copy_(hd)
-    h_anchor = st.anchor.cpu().pin_memory()
-    h_post = st.post.cpu().pin_memory()
-    h_ids = torch.empty(st.batch, st.B, dtype=torch.int32).pin_memory()
-    h_acc = torch.empty(st.batch, dtype=torch.int32).pin_memory()
-    h_bonus = torch.empty(st.batch, dtype=torch.int32).pin_memory()
-    h_out = torch.empty(st.batch, st.B, dtype=torch.int32).pin_memory()
-    h2d = sum(h.numel() * h.element_size() for h in h_hidden) + h_anchor.numel() * 4 + h_post.numel() * 4
-    d2h = (h_ids.numel() + h_acc.numel() + h_bonus.numel() + h_out.numel()) * 4
+    # end to end through the C ABI from pinned host memory: every step copies
+    # its inputs in (features, anchors, posterior: one buffer each) and its
+    # results out (one buffer), then waits for them
+    h_hidden = torch.empty_like(st.hidden_all, device="cpu").pin_memory()
+    h_hidden.copy_(st.hidden_all)
+    h_ints_in = st.ints_in.cpu().pin_memory()
+    h_ints_out = torch.empty_like(st.ints_out, device="cpu").pin_memory()
+    h2d = h_hidden.numel() * h_hidden.element_size() + h_ints_in.numel() * 4
+    d2h = h_ints_out.numel() * 4
 
     def e2e_step():
-        for hh, hd in zip(h_hidden, st.hidden):
-            hd.copy_(hh, non_blocking=True)
-        st.anchor.copy_(h_anchor, non_blocking=True)
-        st.post.copy_(h_post, non_blocking=True)
+        st.hidden_all.copy_(h_hidden, non_blocking=True)
+        st.ints_in.copy_(h_ints_in, non_blocking=True)
         st.step()
-        h_ids.copy_(st.ids, non_blocking=True)
-        h_acc.copy_(st.acc, non_blocking=True)
-        h_bonus.copy_(st.bonus, non_blocking=True)
-        h_out.copy_(st.out_tokens, non_blocking=True)
+        h_ints_out.copy_(st.ints_out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for _ in range(args.warmup):

@@ -49,7 +49,7 @@ using namespace ptx;
 #endif
 // attention probabilities enter P V as a bf16 (hi, lo) pair (1) or as bf16 (0)
 #ifndef DFLASH_CH_PLO
-#define DFLASH_CH_PLO 1
+#define DFLASH_CH_PLO 0
 #endif
 // pause of the producer lane between polls when nothing can be issued (ns)
 #ifndef DFLASH_CH_IDLE_NS
@@ -1066,7 +1066,7 @@ __device__ void attention_phase(const ChainParams& P, int phase, int l, const It
           acc[n][2] *= alpha[1];
           acc[n][3] *= alpha[1];
         }
-        // O += P V with P as a bf16 (hi, lo) pair
+        // O += P V with P rounded to bf16 (plus its bf16 remainder when DFLASH_CH_PLO)
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
           const float* s0 = s[2 * kk];
