@@ -193,8 +193,17 @@ static int lm_head(dflash_handle* h, cudaStream_t s, Fwd& f, const float* x, int
 }
 
 // ---- weight-streaming paths (bf16, at most 64 activation rows) -------------
+// Row counts (compile-time tuning): the weight-streaming kernel takes
+// projections of at most DFLASH_STREAM_MAX_ROWS rows, the tensor-core kernel
+// those of at least DFLASH_TC_MIN_ROWS rows (when both apply, streaming).
+#ifndef DFLASH_STREAM_MAX_ROWS
+#define DFLASH_STREAM_MAX_ROWS 64
+#endif
+#ifndef DFLASH_TC_MIN_ROWS
+#define DFLASH_TC_MIN_ROWS 128
+#endif
 static bool streaming(const dflash_handle* h, int64_t M) {
-  return h->have_maps && M >= 1 && M <= 64;
+  return h->have_maps && M >= 1 && M <= DFLASH_STREAM_MAX_ROWS;
 }
 
 static WSeg make_seg(int t0, int t1, int kind, int map, int n_valid, void* dst, int64_t ld) {
@@ -466,7 +475,9 @@ static bool make_weight_maps(dflash_handle* h) {
 }
 
 // Long prefixes (>= 128 rows) of a bf16 handle go to the tensor-core kernel.
-static bool dense_tc(const dflash_handle* h, int64_t M) { return h->have_tc && M >= 128; }
+static bool dense_tc(const dflash_handle* h, int64_t M) {
+  return h->have_tc && M >= DFLASH_TC_MIN_ROWS;
+}
 
 }  // namespace dflash
 
@@ -641,8 +652,9 @@ int dflash_fuse_context(dflash_handle* h, const void* const* hidden, int64_t T, 
   if (dense_tc(h, T)) {
     // tensor-core projection in row chunks staged as fp32 in the workspace,
     // each followed by the row RMSNorm
-    const int64_t chunk = std::min<int64_t>(T, (int64_t)(ws_bytes / ((size_t)D * 4 + 1)) / 128 * 128);
-    if (chunk < 128) return DFLASH_ERR_WORKSPACE;
+    const int64_t fit = (int64_t)(ws_bytes / ((size_t)D * 4 + 1)) / 128 * 128;
+    const int64_t chunk = std::min<int64_t>(T, fit);
+    if (fit < std::min<int64_t>(T, 128)) return DFLASH_ERR_WORKSPACE;
     float* Yc = (float*)ws;
     for (int64_t r0 = 0; r0 < T; r0 += chunk) {
       const int64_t n = std::min(chunk, T - r0);
