@@ -62,8 +62,9 @@ def step_bytes(w, lens, esz):
     out["attention"] = ctx * s.G * s.d * 2 * esz * s.n_layers
     out["dense_gemm"] = (s.D * s.n_pick * s.D + 2 * s.G * s.d * s.D * s.n_layers) * esz + \
         rows * s.n_pick * s.D * esz
-    # the persistent kernel runs the whole block: layer weights, LM head, context K/V
-    out["draft_chain"] = out["weight_gemm"] + out["lm_head"] + out["attention"]
+    # the persistent kernel runs the whole round: the fusion and injection
+    # weights, the layer weights, the LM head and the context K/V
+    out["draft_chain"] = out["weight_gemm"] + out["lm_head"] + out["attention"] + out["dense_gemm"]
     return out
 
 
@@ -218,13 +219,14 @@ class Draft:
                            self.batch, self.kv.struct, self.ws)
 
     def step(self):
+        """One round: fusion + injection of the B pending rows per sequence and
+        the block draft (dflash_draft_round: one persistent launch for blocks
+        of at most 16 rows), then greedy verification."""
         d, m = self.dfl, self.model
         self.kv.len.copy_(self.len0)
-        d.dflash_fuse_context(m.handle, self.hidden, self.rows, self.Ht, self.ws)
-        d.dflash_inject_kv(m.handle, self.Ht, self.rows, self.row0, self.nrow, self.batch,
-                           self.kv.struct, self.ws)
-        d.dflash_draft_block(m.handle, self.anchor, self.batch, self.B, self.kv.struct, self.ids,
-                             None, None, self.ws)
+        d.dflash_draft_round(m.handle, self.hidden, self.rows, self.row0, self.nrow, self.Ht,
+                             self.anchor, self.batch, self.B, self.kv.struct, self.ids, None,
+                             None, self.ws)
         d.dflash_verify_greedy(self.ids, self.post, self.batch, self.B, self.start, self.acc,
                                self.tau, self.bonus, self.out_tokens, None)
 
@@ -422,7 +424,9 @@ def run_trace(args):
     if not tr:
         print(f"{w.name}: the draft block did not run as one persistent launch (no timeline)")
         return
-    names = ["embed"]
+    names = ["fuse", "fuse reduce", "fuse norm", "inject", "inject reduce", "embed"]
+    if len(tr) < len(names) + PHASE_NAMES.__len__() * w.draft.n_layers:
+        names = ["embed"]   # a draft block without the round's phases
     for l in range(w.draft.n_layers):
         names += [f"layer {l} {n}" for n in PHASE_NAMES]
     names += ["LM head", "LM head reduce", "LM head merge"][:len(tr) - len(names)]

@@ -74,6 +74,9 @@ _sig = {
                                    _P, C.c_size_t, _P]),
     "dflash_draft_block": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.POINTER(dflash_kv), _P, _P,
                                      _P, _P, C.c_size_t, _P]),
+    "dflash_draft_round": (C.c_int, [_P, C.POINTER(_P), C.c_int32, _P, _P, _P, _P, C.c_int32,
+                                     C.c_int32, C.POINTER(dflash_kv), _P, _P, _P, _P, C.c_size_t,
+                                     _P]),
     "dflash_verify_greedy": (C.c_int, [_P, _P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_lm_head_argmax": (C.c_int, [_P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
     "dflash_target_forward": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.POINTER(dflash_kv),
@@ -171,6 +174,20 @@ def dflash_draft_block(h: int, anchor: torch.Tensor, batch: int, B: int, kv: dfl
                                    _ptr(top2_gap), _ptr(hidden_out), _ptr(ws),
                                    ws.numel() * ws.element_size(), _stream(stream)),
            "dflash_draft_block")
+
+
+def dflash_draft_round(h: int, hidden: Sequence[torch.Tensor], n_rows: int,
+                       seq_row0: torch.Tensor, seq_rows: torch.Tensor, h_t_out: torch.Tensor,
+                       anchor: torch.Tensor, batch: int, B: int, kv: dflash_kv,
+                       draft_ids: torch.Tensor, top2_gap: Optional[torch.Tensor],
+                       hidden_out: Optional[torch.Tensor], ws: torch.Tensor, stream=None):
+    """Fusion + injection of the n_rows pending features, then the block draft."""
+    arr = (_P * len(hidden))(*[_ptr(x) for x in hidden])
+    _check(_lib.dflash_draft_round(h, arr, n_rows, _ptr(seq_row0), _ptr(seq_rows), _ptr(h_t_out),
+                                   _ptr(anchor), batch, B, C.byref(kv), _ptr(draft_ids),
+                                   _ptr(top2_gap), _ptr(hidden_out), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream)),
+           "dflash_draft_round")
 
 
 def dflash_verify_greedy(draft: torch.Tensor, post: torch.Tensor, batch: int, B: int,

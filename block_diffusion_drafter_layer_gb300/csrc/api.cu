@@ -441,20 +441,23 @@ static bool make_weight_maps(dflash_handle* h) {
   h->have_maps = true;
   // device copy of the draft-layer and LM-head maps for the persistent kernel
   if (d == 128 && F % 64 == 0) {
-    std::vector<CUtensorMap> tab((size_t)c.n_layers * 7 + 1);
+    std::vector<CUtensorMap> tab((size_t)c.n_layers * 7 + 2);
     for (int l = 0; l < c.n_layers; ++l) {
       const LayerMaps& M = h->maps[l];
       const CUtensorMap* src[7] = {&M.wq, &M.wk, &M.wv, &M.wo, &M.wg, &M.wu, &M.wd};
       for (int k = 0; k < 7; ++k) tab[(size_t)l * 7 + k] = *src[k];
     }
-    tab.back() = h->map_lm;
+    tab[(size_t)c.n_layers * 7] = h->map_lm;
+    tab[(size_t)c.n_layers * 7 + 1] = w.wc ? h->map_wc : h->map_lm;
     void* p = nullptr;
     if (cudaMalloc(&p, tab.size() * sizeof(CUtensorMap)) == cudaSuccess) {
       if (cudaMemcpy(p, tab.data(), tab.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) ==
-          cudaSuccess)
+          cudaSuccess) {
         h->d_wmaps = (CUtensorMap*)p;
-      else
+        h->have_wc_map = w.wc != nullptr && c.hidden % 128 == 0;
+      } else {
         cudaFree(p);
+      }
     }
   }
   // 256-row boxes for the tensor-core projection of long prefixes
@@ -894,6 +897,58 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
   }
   return lm_head(h, s, f, f.x, (int64_t)batch * (B - 1), h->w.g_f, B, draft_ids, top2_gap, B,
                  anchor);
+}
+
+int dflash_draft_round(dflash_handle* h, const void* const* hidden, int32_t n_rows,
+                       const int32_t* seq_row0, const int32_t* seq_rows, void* h_t_out,
+                       const int32_t* anchor, int32_t batch, int32_t B, const dflash_kv* kv,
+                       int32_t* draft_ids, float* top2_gap, float* hidden_out, void* ws,
+                       size_t ws_bytes, dflash_stream_t st) {
+  if (!h || n_rows < 0) return DFLASH_ERR_INVALID_ARG;
+  if (n_rows == 0)
+    return dflash_draft_block(h, anchor, batch, B, kv, draft_ids, top2_gap, hidden_out, ws,
+                              ws_bytes, st);
+  if (!hidden || !seq_row0 || !seq_rows || !h_t_out || !anchor || !draft_ids || !ws ||
+      batch < 1 || B < 1)
+    return DFLASH_ERR_INVALID_ARG;
+  if (!kv_ok(h, kv, batch)) return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = h->cfg;
+  for (int i = 0; i < c.n_pick; ++i) {
+    if (!hidden[i]) return DFLASH_ERR_INVALID_ARG;
+    if (!aligned16(hidden[i])) return DFLASH_ERR_ALIGNMENT;
+  }
+  if (!aligned16(h_t_out) || !aligned16(ws)) return DFLASH_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)st;
+  if (chain_ok(h, batch, B) && n_rows <= 16 && h->have_wc_map && h->w.g_c &&
+      aligned16(h->w.g_c)) {
+    // fusion, injection and the block in one persistent launch
+    const int64_t R = (int64_t)batch * B;
+    Fwd f;
+    if (!carve_forward(h, std::max<int64_t>(R, n_rows), ws, ws_bytes, &f, batch, B))
+      return DFLASH_ERR_WORKSPACE;
+    ChainArgs A{anchor, batch, B, kv, draft_ids, top2_gap, f.x, f.xg, f.q, f.kb, f.vb, f.o, f.a,
+                f.ssq, f.partial, f.attn, f.amx};
+    A.n_in = n_rows;
+    A.hidden = hidden;
+    A.row0 = seq_row0;
+    A.nrow = seq_rows;
+    A.ht = h_t_out;
+    int rc = draft_chain(h, s, A);
+    if (rc) return rc;
+    if (hidden_out &&
+        cudaMemcpyAsync(hidden_out, f.x, R * c.hidden * sizeof(float), cudaMemcpyDeviceToDevice, s))
+      return DFLASH_ERR_CUDA;
+    if (B == 1 &&
+        cudaMemcpyAsync(draft_ids, anchor, batch * sizeof(int32_t), cudaMemcpyDeviceToDevice, s))
+      return DFLASH_ERR_CUDA;
+    return DFLASH_OK;
+  }
+  int rc = dflash_fuse_context(h, hidden, n_rows, h_t_out, ws, ws_bytes, st);
+  if (!rc) rc = dflash_inject_kv(h, h_t_out, n_rows, seq_row0, seq_rows, batch, kv, ws, ws_bytes, st);
+  if (!rc)
+    rc = dflash_draft_block(h, anchor, batch, B, kv, draft_ids, top2_gap, hidden_out, ws, ws_bytes,
+                            st);
+  return rc;
 }
 
 int dflash_verify_greedy(const int32_t* draft, const int32_t* post, int32_t batch, int32_t B,

@@ -116,7 +116,7 @@ constexpr int kMaxTiles = 8192;   // 128-row weight tiles per projection launch
 constexpr int kCounters = kMaxTiles + 4;
 // phases of the persistent draft-block kernel: embed, 10 per layer, LM head
 // and its reduce
-constexpr int kChainMaxPhases = 4 + 10 * DFLASH_MAX_LAYERS;
+constexpr int kChainMaxPhases = 9 + 10 * DFLASH_MAX_LAYERS;   // 5 round phases, embed, layers, LM head
 // timeline columns per phase: first start, last start, first end, last end,
 // last CTA done with its multiply-adds, and for the split-K fix-ups (the CTA
 // that completes a tile): latest fix-up start, sum done, epilogue done
@@ -139,6 +139,7 @@ struct dflash_handle {
   float2* d_rope = nullptr;        // [max_pos, d/2] (cos, sin)
   bool have_maps = false;
   bool have_tc = false;
+  bool have_wc_map = false;        // d_wmaps holds W_c after the LM head (the round's fusion)
   dflash::LayerMaps maps[DFLASH_MAX_LAYERS];
   CUtensorMap map_wc, map_lm, map_tc_wc, map_tc_lm;
   CUtensorMap* d_wmaps = nullptr;  // device copy: q k v o gate up down per layer, then LM head
@@ -250,6 +251,12 @@ struct ChainArgs {
   float* partial;               // split-K fix-up tiles
   float* apart;                 // attention run partials (chain_apart_bytes)
   float4* amx;                  // LM-head top-2 records
+  // a round (n_in > 0): fuse + inject the pending rows before the block
+  int n_in = 0;
+  const void* const* hidden = nullptr;   // n_pick device pointers [n_in, D]
+  const int32_t* row0 = nullptr;         // device [batch]
+  const int32_t* nrow = nullptr;         // device [batch]
+  void* ht = nullptr;                    // device bf16 [n_in, D]
 };
 int chain_grid(const dflash_handle* h);
 size_t chain_apart_bytes(const dflash_handle* h, int batch);

@@ -92,11 +92,18 @@ constexpr int CH_SMEM = CH_OFF_MISC + CH_MISC_BYTES + 1024;
 static_assert(CH_ATT_BYTES <= CH_RING_BYTES, "the attention buffers alias the ring");
 static_assert(CH_SMEM <= 233472 / 2 - 1024, "two CTAs per SM");
 
-enum ChainPhase : int { PH_EMBED, PH_QKV, PH_ATT, PH_CMB, PH_O, PH_GU, PH_DN, PH_LM, PH_RED, PH_LMFIN };
+enum ChainPhase : int {
+  PH_EMBED, PH_QKV, PH_ATT, PH_CMB, PH_O, PH_GU, PH_DN, PH_LM, PH_RED, PH_LMFIN,
+  PH_FUSE, PH_FNORM, PH_INJ   // the round's context projection, its norm, the K/V injection
+};
 // phases of one layer; every projection is followed by its reduce phase
 constexpr int kLayerPhases = 10;
 __device__ __constant__ const int kLayerSeq[kLayerPhases] = {PH_QKV, PH_RED, PH_ATT, PH_CMB, PH_O,
                                                              PH_RED, PH_GU,  PH_RED, PH_DN,  PH_RED};
+// phases a round runs before the draft block: fuse the pending target
+// features, normalise them, inject their K/V into every layer's cache
+constexpr int kRoundPhases = 5;
+__device__ __constant__ const int kRoundSeq[kRoundPhases] = {PH_FUSE, PH_RED, PH_FNORM, PH_INJ, PH_RED};
 
 struct ChainLayer {
   const float* g_in;
@@ -106,17 +113,23 @@ struct ChainLayer {
 };
 
 struct ChainParams {
+  CUtensorMap map_hid[DFLASH_MAX_PICK];   // round: the pending target features [n_in, D], box 64 x 16
+  CUtensorMap map_ht;         // round: the fused context feature H_t [n_in, D], box 64 x 16
   CUtensorMap map_xg;         // bf16 x * g [R, D], box 64 x 16
   CUtensorMap map_o;          // bf16 attention output [R, H*d], box 64 x 16
   CUtensorMap map_a;          // bf16 SwiGLU output [R, F], box 64 x 16
-  const CUtensorMap* wmaps;   // [n_layers * 7 + 1]: q k v o gate up down per layer, LM head
+  const CUtensorMap* wmaps;   // [n_layers * 7 + 2]: q k v o gate up down per layer, LM head, W_c
   const bf16* kc[DFLASH_MAX_LAYERS];
   const bf16* vc[DFLASH_MAX_LAYERS];
   ChainLayer lay[DFLASH_MAX_LAYERS];
   const bf16* embed;
   const float* g_f;
+  const float* g_c;           // round: the fused context's RMSNorm gain
+  bf16* ht;                   // round: H_t out [n_in, D]
+  const int32_t* row0;        // round: first pending row of each sequence
+  const int32_t* nrow;        // round: pending rows of each sequence (appended to its cache)
   const int32_t* anchor;
-  const int32_t* len;
+  int32_t* len;               // cache lengths (a round advances them)
   int32_t* ids;
   float* gap;
   float* x;
@@ -136,6 +149,7 @@ struct ChainParams {
   const float2* rope;
   int max_pos;
   int R, batch, B, D, Hd, Gd, F, V, G, rep, nL, cap, mask_id, qk_norm;
+  int pre, n_in, n_pick, kv_batch;   // round phases (0 or kRoundPhases), pending rows, sources, cache batch
   int grid, n_phases, n_items_max;
   float eps, embed_scale, scale_log2;
 };
@@ -150,11 +164,19 @@ static_assert(sizeof(ChainParams) <= 4096, "kernel parameters must fit the 4 KB 
 enum : int { MS_ABORT = 0, MS_LAST = 1, MS_ISSUED = 2, MS_CONSUMED = 3, MS_GO = 4, MS_ATT_DONE = 5 };
 // [0, 16) ints: flags; [16, 48): rowpos (sequence, position) per row;
 // [48, 64): rinv per row; [64, 192): attention item tables; [192, 384):
-// LM-head top-2 records, [4 warps][16 rows][3]
+// LM-head top-2 records, [4 warps][16 rows][3]; [384, 416): injpos
+// (sequence, cache position) per pending row of a round
 
-// Phase p: 0 embed; then kLayerPhases per layer; then the LM head, its
-// reduce (which also publishes each CTA's top-2 records) and the final merge.
+// Phase p: the round's phases (p < P.pre), then embed; kLayerPhases per
+// layer; the LM head, its reduce (which also publishes each CTA's top-2
+// records) and the final merge.
+template <bool RD>
 __device__ __forceinline__ int phase_kind(const ChainParams& P, int p, int& l) {
+  if (RD && p < P.pre) {
+    l = 0;
+    return kRoundSeq[p];
+  }
+  if (RD) p -= P.pre;
   if (p == 0) {
     l = 0;
     return PH_EMBED;
@@ -180,11 +202,20 @@ __device__ __forceinline__ Geo gemm_geo(const ChainParams& P, int kind) {
     case PH_O: return {P.D / 128, P.Hd / 64, 0};
     case PH_GU: return {P.F / 64, P.D / 64, 1};
     case PH_DN: return {P.D / 128, P.F / 64, 0};
+    case PH_FUSE: return {P.D / 128, P.n_pick * (P.D / 64), 0};
+    case PH_INJ: return {P.nL * 2 * (P.Gd / 128), P.D / 64, 0};   // per layer: k tiles, v tiles
     default: return {(P.V + 127) / 128, P.D / 64, 1};   // PH_LM
   }
 }
+template <bool RD>
 __device__ __forceinline__ bool is_gemm(int kind) {
-  return kind == PH_QKV || kind == PH_O || kind == PH_GU || kind == PH_DN || kind == PH_LM;
+  return kind == PH_QKV || kind == PH_O || kind == PH_GU || kind == PH_DN || kind == PH_LM ||
+         (RD && (kind == PH_FUSE || kind == PH_INJ));
+}
+// rows of a phase's activations: the round's pending rows or the block rows
+template <bool RD>
+__device__ __forceinline__ int rows_of(const ChainParams& P, int kind) {
+  return RD && (kind == PH_FUSE || kind == PH_INJ) ? P.n_in : P.R;
 }
 
 __device__ __forceinline__ int first_unit_of(int64_t c, int64_t U, int64_t G) {
@@ -254,14 +285,31 @@ struct Cursor {
   const CUtensorMap* wm0;   // weight box(es) of tile t (gate / up: two)
   const CUtensorMap* wm1;
   int wrow;     // row coordinate of tile t in its weight
+  // set when the cursor enters a phase: the activation map of k-chunk kk is
+  // amap[asrc] at column alk * 64 (asrc steps every aper k-chunks: the
+  // fusion's sources), and the attention phases the unit's weights wait for
+  const CUtensorMap* amap;
+  int aper, asrc, alk, att_need;
 };
 
 // Weight map(s) and row of the cursor's tile.
+template <bool RD>
 __device__ __forceinline__ void cursor_tile(const ChainParams& P, Cursor& c) {
   c.wm1 = nullptr;
   if (c.kind == PH_LM) {
     c.wm0 = P.wmaps + P.nL * 7;
     c.wrow = c.t * 128;
+    return;
+  }
+  if (RD && c.kind == PH_FUSE) {
+    c.wm0 = P.wmaps + P.nL * 7 + 1;
+    c.wrow = c.t * 128;
+    return;
+  }
+  if (RD && c.kind == PH_INJ) {   // layer t / 2tk; its k tiles, then its v tiles
+    const int tk = P.Gd / 128, li = c.t / (2 * tk), w = (c.t - li * 2 * tk) / tk;
+    c.wm0 = P.wmaps + li * 7 + 1 + w;
+    c.wrow = (c.t - li * 2 * tk - w * tk) * 128;
     return;
   }
   const CUtensorMap* L = P.wmaps + c.l * 7;
@@ -283,11 +331,12 @@ __device__ __forceinline__ void cursor_tile(const ChainParams& P, Cursor& c) {
   }
 }
 
+template <bool RD>
 __device__ __forceinline__ bool cursor_phase(const ChainParams& P, Cursor& c, int p) {
   for (; p < P.n_phases; ++p) {
     int l;
-    const int kind = phase_kind(P, p, l);
-    if (!is_gemm(kind)) continue;
+    const int kind = phase_kind<RD>(P, p, l);
+    if (!is_gemm<RD>(kind)) continue;
     const Geo g = gemm_geo(P, kind);
     int u0, u1;
     unit_range(P, kind, blockIdx.x, u0, u1);
@@ -300,19 +349,41 @@ __device__ __forceinline__ bool cursor_phase(const ChainParams& P, Cursor& c, in
     c.kc = g.kc;
     c.t = u0 / g.kc;
     c.kk = u0 - c.t * g.kc;
-    cursor_tile(P, c);
+    cursor_tile<RD>(P, c);
+    if (RD && kind == PH_FUSE) {
+      c.amap = P.map_hid;
+      c.aper = P.D / 64;
+    } else {
+      c.amap = kind == PH_O ? &P.map_o : kind == PH_DN ? &P.map_a
+               : RD && kind == PH_INJ ? &P.map_ht : &P.map_xg;
+      c.aper = g.kc;
+    }
+    c.asrc = c.kk / c.aper;
+    c.alk = c.kk - c.asrc * c.aper;
+    // ring memory doubles as the attention buffers: a weight unit may be
+    // loaded only once this CTA has finished every attention phase before
+    // the unit's phase (q/k/v(l) follows attention(l-1); o_proj(l) onward
+    // follows attention(l); the LM head follows them all)
+    c.att_need = kind == PH_QKV || (RD && (kind == PH_FUSE || kind == PH_INJ)) ? l
+                 : kind == PH_LM ? P.nL : l + 1;
     return true;
   }
   c.p = P.n_phases;
   return false;
 }
+template <bool RD>
 __device__ __forceinline__ bool cursor_next(const ChainParams& P, Cursor& c) {
   ++c.i;
-  if (++c.u >= c.u1) return cursor_phase(P, c, c.p + 1);
+  if (++c.u >= c.u1) return cursor_phase<RD>(P, c, c.p + 1);
+  if (++c.alk == c.aper) {
+    c.alk = 0;
+    ++c.asrc;
+  }
   if (++c.kk == c.kc) {
     c.kk = 0;
+    c.asrc = c.alk = 0;
     ++c.t;
-    cursor_tile(P, c);
+    cursor_tile<RD>(P, c);
   }
   return true;
 }
@@ -325,16 +396,16 @@ __device__ __forceinline__ void issue_w(const ChainParams& P, const Cursor& c, u
 
 __device__ __forceinline__ void issue_a(const ChainParams& P, const Cursor& c, uint32_t dst,
                                         uint32_t bar, uint64_t pol) {
-  const CUtensorMap* m = c.kind == PH_O ? &P.map_o : c.kind == PH_DN ? &P.map_a : &P.map_xg;
-  tma_load_2d(dst, m, bar, c.kk * 64, 0, pol);
+  tma_load_2d(dst, c.amap + c.asrc, bar, c.alk * 64, 0, pol);
 }
 
+template <bool RD>
 __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full,
                          uint32_t bar_empty, volatile int* misc) {
   const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
   Cursor w{}, a{};
   w.i = a.i = 0;
-  bool w_more = cursor_phase(P, w, 0);
+  bool w_more = cursor_phase<RD>(P, w, 0);
   a = w;
   bool a_more = w_more;
   int ready = 0;                 // phases known to have passed their barrier
@@ -343,12 +414,7 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
   bool abort = false;
   while (a_more) {
     bool prog = false;
-    // ring memory doubles as the attention buffers: a weight unit may be
-    // loaded only once this CTA has finished every attention phase before
-    // the unit's phase (q/k/v(l) follows attention(l-1); o_proj(l) onward
-    // follows attention(l); the LM head follows them all)
-    const int att_need = w.kind == PH_QKV ? w.l : w.kind == PH_LM ? P.nL : w.l + 1;
-    const bool w_held = w_more && misc[MS_ATT_DONE] < att_need;
+    const bool w_held = w_more && misc[MS_ATT_DONE] < w.att_need;
     if (w_more && !abort && !w_held) {
       const int s = w.i % CH_STAGES, use = w.i / CH_STAGES;
       // with no activation load owed, block in the barrier wait instead of spinning
@@ -362,7 +428,7 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
           const int k = w.u - e0;
           if (k < kEvUnits) ev(P, w.p, 2 + 2 * kEvUnits + k);
         }
-        w_more = cursor_next(P, w);
+        w_more = cursor_next<RD>(P, w);
         prog = true;
       }
     }
@@ -384,7 +450,7 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
           const int k = a.u - e0;
           if (k < kEvUnits) ev(P, a.p, 2 + 3 * kEvUnits + k);
         }
-        a_more = cursor_next(P, a);
+        a_more = cursor_next<RD>(P, a);
         prog = true;
       }
     } else if (!w_more) {
@@ -570,6 +636,48 @@ __device__ __forceinline__ void row_apply(const ChainParams& P, int kind, int t,
   }
 }
 
+// Row epilogues of the round's projections: the fusion (the row and its sum of squares over the tile) and
+// the injection (k: per-head RMSNorm + RoPE; k and v appended to layer li's
+// cache at the row's position).  injpos: (sequence, position) per pending row.
+__device__ __forceinline__ void row_round(const ChainParams& P, int kind, int t, int r, float4 v,
+                                       const int* injpos) {
+  const int lane = threadIdx.x & 31;
+  if (kind == PH_FUSE) {
+    *(float4*)(P.x + (int64_t)r * P.D + t * 128 + 4 * lane) = v;
+    const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+    if (lane == 0) P.ssq[(t * CH_ROWS + r) * CH_SSQ] = ss;
+    return;
+  }
+  const int tk = P.Gd / 128, li = t / (2 * tk), w = (t - li * 2 * tk) / tk;
+  const int head = t - li * 2 * tk - w * tk;
+  if (w == 0 && P.qk_norm) {
+    const float4 g = __ldg((const float4*)P.lay[li].k_norm + lane);
+    const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
+    const float rinv = 1.0f / sqrtf(ss / (float)CH_DH + P.eps);
+    v = make_float4(v.x * rinv * g.x, v.y * rinv * g.y, v.z * rinv * g.z, v.w * rinv * g.w);
+  }
+  const int b = injpos[2 * r], pos = injpos[2 * r + 1];
+  if (b < 0) return;   // not a pending row of any sequence
+  if (pos < 0 || pos >= P.cap || b >= P.kv_batch || (w == 0 && pos >= P.max_pos)) {
+    if (lane == 0) atomicOr(P.status, ST_CAPACITY);
+    return;
+  }
+  if (w == 0) {   // rotate-half pairs (j, j + 64): lanes 0-15 hold j, lanes 16-31 j + 64
+    const float4* rp = (const float4*)(P.rope + (int64_t)pos * 64 + ((4 * lane) & 63));
+    const float4 c0 = __ldg(rp), c1 = __ldg(rp + 1);
+    const float4 o = shfl_xor4(v, 16);
+    const float sg = lane < 16 ? -1.f : 1.f;
+    v = make_float4(v.x * c0.x + sg * o.x * c0.y, v.y * c0.z + sg * o.y * c0.w,
+                    v.z * c1.x + sg * o.z * c1.y, v.w * c1.z + sg * o.w * c1.w);
+  }
+  bf16* dst = const_cast<bf16*>(w == 0 ? P.kc[li] : P.vc[li]) +
+              (((int64_t)b * P.G + head) * P.cap + pos) * CH_DH;
+  uint2 pk;
+  pk.x = pack_bf16(v.x, v.y);
+  pk.y = pack_bf16(v.z, v.w);
+  *(uint2*)(dst + 4 * lane) = pk;
+}
+
 // 1 / rms of every row of the residual from its per-(tile, row) sums of
 // squares, into rinv_s (all consumer threads; 8 per row take every 8th tile,
 // loads in flight together, then a fixed shuffle tree adds the 8 parts).
@@ -601,6 +709,7 @@ __device__ void rinv_rows(const ChainParams& P, float* rinv_s) {
 // sum in its slot for the reduce phase.  `ri` is the ring index of the first
 // unit.  After a timed-out wait the warps skip the arithmetic but keep every
 // barrier.
+template <bool RD>
 __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int& ri,
                            uint8_t* smem, uint32_t sbase, uint32_t bar_full, uint32_t bar_empty,
                            volatile int* misc, const int* rowpos, float* rinv_s, float* recs) {
@@ -612,6 +721,7 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
   if (u1 <= u0) return;
   float* E = (float*)(smem + CH_OFF_E);
   const int g = lane >> 2, tg = lane & 3;
+  const int nrows = rows_of<RD>(P, kind);
   bool have_rinv = false;   // 1 / rms of the rows, computed when a first tile finishes here
   float acc[4][4];
   int cur = -1, kbeg = 0, kend = 0;
@@ -636,12 +746,15 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int r = cw + 4 * q;
-        in[q] = row_in(P, kind, t, r < P.R ? r : 0, rowpos);
+        in[q] = row_in(P, kind, t, r < nrows ? r : 0, rowpos);
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int r = cw + 4 * q;
-        if (r < P.R)
+        if (r >= nrows) continue;
+        if (RD && (kind == PH_FUSE || kind == PH_INJ))
+          row_round(P, kind, t, r, *(const float4*)&E[r * CH_EPAD + 4 * lane], rowpos);
+        else
           row_apply(P, kind, t, r, *(const float4*)&E[r * CH_EPAD + 4 * lane],
                     geo.nin ? rinv_s[r] : 1.f, gt, in[q], rowpos, recs + cw * 48);
       }
@@ -721,6 +834,7 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
 // per CTA (U >= G) they are the CTAs lo .. hi, each of which holds t in slot 0
 // (its first tile) except lo when lo began in an earlier tile (slot 1); with
 // fewer units than CTAs every unit has its own owner, holding t in slot 0.
+template <bool RD>
 __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* rowpos, float* recs,
                              float* rinv_s) {
   const int warp = (threadIdx.x - 32) >> 5, lane = threadIdx.x & 31;
@@ -808,7 +922,7 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
     return;
   }
   const uint32_t U = (uint32_t)geo.n_tiles * geo.kc, G = P.grid, kc = geo.kc;
-  const int R = P.R, ntask = geo.n_tiles * R;
+  const int R = rows_of<RD>(P, kind), ntask = geo.n_tiles * R;
   const bool dense = U >= G;
   auto owner = [&](uint32_t u) { return (int)(((u + 1) * G + U - 1) / U) - 1; };
   constexpr int RB = 12;   // contributors per batch
@@ -847,7 +961,10 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
     }
     const float ri = !geo.nin ? 1.f
                      : rinv_in_task ? 1.0f / sqrtf(warp_sum(ss) / (float)P.D + P.eps) : rinv_s[r];
-    row_apply(P, kind, t, r, sum, ri, gt, in, rowpos, recs + warp * 48);
+    if (RD && (kind == PH_FUSE || kind == PH_INJ))
+      row_round(P, kind, t, r, sum, rowpos);
+    else
+      row_apply(P, kind, t, r, sum, ri, gt, in, rowpos, recs + warp * 48);
   }
 }
 
@@ -907,10 +1024,11 @@ struct Items {
   int nsub[CH_MAXB], runs[CH_MAXB], base[CH_MAXB], L[CH_MAXB];
 };
 
+template <bool RD>
 __device__ void make_items(const ChainParams& P, Items* it) {
   int U = 0;
   for (int b = 0; b < P.batch; ++b) {
-    int L = P.len[b];
+    int L = P.len[b] + (RD && P.pre ? P.nrow[b] : 0);   // a round's appended rows count
     if (L < 0 || L > P.cap) {
       atomicOr(P.status, ST_BOUNDS);
       L = L < 0 ? 0 : P.cap;
@@ -1186,6 +1304,28 @@ __device__ void combine_phase(const ChainParams& P, int phase, const Items* it) 
   }
 }
 
+// The round's fused context feature: each pending row of the projection
+// (fp32 in x) through RMSNorm with gain g_c, H_t = bf16(y / rms(y) * g_c);
+// one warp per (row, 128-column tile).  CTA 0 then advances the cache
+// lengths by the appended rows (every CTA read them before its first phase).
+__device__ void fnorm_phase(const ChainParams& P) {
+  const int tid = threadIdx.x - 32, warp = tid >> 5, lane = threadIdx.x & 31;
+  const int tiles = P.D / 128;
+  for (int w = blockIdx.x * 4 + warp; w < P.n_in * tiles; w += P.grid * 4) {
+    const int r = w / tiles, t = w - r * tiles;
+    float ss = 0.f;
+    for (int tt = lane; tt < tiles; tt += 32) ss += __ldcg(P.ssq + (tt * CH_ROWS + r) * CH_SSQ);
+    const float4 y = __ldcg((const float4*)(P.x + (int64_t)r * P.D + t * 128) + lane);
+    const float4 g = __ldg((const float4*)(P.g_c + t * 128) + lane);
+    const float rinv = 1.0f / sqrtf(warp_sum(ss) / (float)P.D + P.eps);
+    uint2 pk;
+    pk.x = pack_bf16(y.x * rinv * g.x, y.y * rinv * g.y);
+    pk.y = pack_bf16(y.z * rinv * g.z, y.w * rinv * g.w);
+    *((uint2*)(P.ht + (int64_t)r * P.D + t * 128) + lane) = pk;
+  }
+  if (blockIdx.x == 0 && tid < P.batch) P.len[tid] += P.nrow[tid];
+}
+
 // Embedding of the block rows (anchor, then mask tokens) into the fp32
 // residual, with the per-(tile, row) sums of squares of the first norm.
 __device__ void embed_phase(const ChainParams& P) {
@@ -1216,6 +1356,7 @@ __device__ void embed_phase(const ChainParams& P) {
   }
 }
 
+template <bool RD>
 __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_constant__ ChainParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -1226,7 +1367,9 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
   float* rinv_s = (float*)(smem + CH_OFF_MISC) + 48;
   Items* items = (Items*)((int*)(smem + CH_OFF_MISC) + 64);
   float* recs = (float*)(smem + CH_OFF_MISC) + 192;
-  static_assert(64 * 4 + sizeof(Items) <= 192 * 4 && (192 + 4 * 48) * 4 <= CH_MISC_BYTES, "misc area");
+  int* injpos = (int*)(smem + CH_OFF_MISC) + 384;
+  static_assert(64 * 4 + sizeof(Items) <= 192 * 4 && (192 + 4 * 48) * 4 <= 384 * 4 &&
+                    (384 + 2 * CH_ROWS) * 4 <= CH_MISC_BYTES, "misc area");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -1238,21 +1381,37 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
     misc[MS_ATT_DONE] = 0;
     fence_barrier_init();
   }
-  if (threadIdx.x == 32) make_items(P, items);
+  if (threadIdx.x == 32) make_items<RD>(P, items);
   if (threadIdx.x >= 32 && threadIdx.x < 32 + CH_ROWS) {
     const int r = threadIdx.x - 32;
     int b = -1, pos = -1;
     if (r < P.R) {
       b = r / P.B;
-      pos = P.len[b] + (r - b * P.B);
+      pos = P.len[b] + (RD && P.pre ? P.nrow[b] : 0) + (r - b * P.B);
     }
     rowpos[2 * r] = b;
     rowpos[2 * r + 1] = pos;
   }
+  if (RD && threadIdx.x >= 64 && threadIdx.x < 64 + CH_ROWS) {
+    // a round's pending rows: the sequence whose row range holds the row,
+    // and the cache position it is appended at
+    const int r = threadIdx.x - 64;
+    int b = -1, pos = -1;
+    for (int s = 0; P.pre && r < P.n_in && s < P.batch; ++s) {
+      const int r0 = P.row0[s], n = P.nrow[s];
+      if (r >= r0 && r < r0 + n) {
+        b = s;
+        pos = P.len[s] + (r - r0);
+        break;
+      }
+    }
+    injpos[2 * r] = b;
+    injpos[2 * r + 1] = pos;
+  }
   __syncthreads();
 
   if (warp == 0) {
-    if (lane == 0) producer(P, sbase, bar_full, bar_empty, misc);
+    if (lane == 0) producer<RD>(P, sbase, bar_full, bar_empty, misc);
     __syncwarp();
   } else {
     const int tid = threadIdx.x - 32;
@@ -1275,7 +1434,7 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
         atomicMax(P.trace + kChainMaxPhases + p, now);        // last CTA to start
       }
       int l;
-      const int kind = phase_kind(P, p, l);
+      const int kind = phase_kind<RD>(P, p, l);
       if (kind == PH_EMBED) {
         embed_phase(P);
       } else if (kind == PH_ATT) {
@@ -1284,10 +1443,12 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
         if (tid == 0) misc[MS_ATT_DONE] = l + 1;
       } else if (kind == PH_CMB) {
         combine_phase(P, p, items);
+      } else if (RD && kind == PH_FNORM) {
+        fnorm_phase(P);
       } else if (kind == PH_RED) {
         int lp;
-        const int pk = phase_kind(P, p - 1, lp);
-        reduce_phase(P, pk, lp, rowpos, recs, rinv_s);
+        const int pk = phase_kind<RD>(P, p - 1, lp);
+        reduce_phase<RD>(P, pk, lp, RD && pk == PH_INJ ? injpos : rowpos, recs, rinv_s);
         if (pk == PH_LM) lm_publish(P, recs);
       } else if (kind == PH_LMFIN) {
         lm_merge(P);
@@ -1300,7 +1461,8 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
           }
           named_bar(1, CH_CT);
         }
-        gemm_phase(P, p, kind, l, ri, smem, sbase, bar_full, bar_empty, misc, rowpos, rinv_s, recs);
+        gemm_phase<RD>(P, p, kind, l, ri, smem, sbase, bar_full, bar_empty, misc,
+                   RD && kind == PH_INJ ? injpos : rowpos, rinv_s, recs);
       }
       named_bar(1, CH_CT);
       if (tid == 0) {
@@ -1336,12 +1498,19 @@ static int g_chain_occ = -1;
 int chain_grid(const dflash_handle* h) {
   if (g_chain_occ < 0) {
     int occ = 0;
-    if (cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CH_SMEM) !=
-            cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, chain_kernel, CH_THREADS, CH_SMEM) !=
-            cudaSuccess)
-      occ = 0;
-    g_chain_occ = std::min(occ, 2);
+    // both variants (the block alone, and a round before it) share the
+    // launch shape; the grid is what both can keep resident
+    int occ1 = 0;
+    if (cudaFuncSetAttribute(chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             CH_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             CH_SMEM) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, chain_kernel<false>, CH_THREADS,
+                                                      CH_SMEM) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ1, chain_kernel<true>, CH_THREADS,
+                                                      CH_SMEM) != cudaSuccess)
+      occ = occ1 = 0;
+    g_chain_occ = std::min(std::min(occ, occ1), 2);
   }
   return g_chain_occ * h->num_sms;
 }
@@ -1377,6 +1546,24 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
       !make_tmap_2d(&P.map_o, A.o, Hd, R, (uint64_t)Hd * 2, 64, 16) ||
       !make_tmap_2d(&P.map_a, A.a, F, R, (uint64_t)F * 2, 64, 16))
     return DFLASH_ERR_CUDA;
+  if (A.n_in > 0) {
+    // the round's phases: the pending features and H_t as TMA sources
+    if (A.n_in > CH_ROWS || !A.hidden || !A.row0 || !A.nrow || !A.ht || !h->w.g_c ||
+        !h->have_wc_map)
+      return DFLASH_ERR_INVALID_ARG;
+    for (int i = 0; i < c.n_pick; ++i)
+      if (!make_tmap_2d(&P.map_hid[i], A.hidden[i], D, A.n_in, (uint64_t)D * 2, 64, 16))
+        return DFLASH_ERR_CUDA;
+    if (!make_tmap_2d(&P.map_ht, A.ht, D, A.n_in, (uint64_t)D * 2, 64, 16)) return DFLASH_ERR_CUDA;
+    P.pre = kRoundPhases;
+    P.n_in = A.n_in;
+    P.n_pick = c.n_pick;
+    P.row0 = A.row0;
+    P.nrow = A.nrow;
+    P.ht = (bf16*)A.ht;
+    P.g_c = h->w.g_c;
+  }
+  P.kv_batch = A.kv->batch_cap;
   P.wmaps = h->d_wmaps;
   for (int l = 0; l < c.n_layers; ++l) {
     P.kc[l] = (const bf16*)A.kv->k[l];
@@ -1387,7 +1574,7 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
   P.embed = (const bf16*)h->w.embed;
   P.g_f = h->w.g_f;
   P.anchor = A.anchor;
-  P.len = A.kv->len;
+  P.len = A.kv->len;   // advanced in place by a round
   P.ids = A.ids;
   P.gap = A.gap;
   P.x = A.x;
@@ -1430,9 +1617,9 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
                         (kChainTraceCols - 3) * col + kEvWords * sizeof(unsigned long long), s))
       return DFLASH_ERR_CUDA;
     P.trace = h->d_trace;
-    h->trace_phases = 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 3 : 0);
+    h->trace_phases = P.pre + 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 3 : 0);
   }
-  P.n_phases = 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 3 : 0);
+  P.n_phases = P.pre + 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 3 : 0);
   P.n_items_max = P.grid + A.batch * c.n_kv_heads;
   P.eps = c.rms_eps;
   P.embed_scale = c.embed_scale;
@@ -1450,7 +1637,7 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
   cfg.numAttrs = 1;
   Timer t;
   launch_begin(h, DFLASH_K_DRAFT_CHAIN, s, &t);
-  cudaLaunchKernelEx(&cfg, chain_kernel, P);
+  cudaLaunchKernelEx(&cfg, P.pre ? chain_kernel<true> : chain_kernel<false>, P);
   return launch_end(h, s, &t);
 }
 

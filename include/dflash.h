@@ -183,6 +183,20 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
                        const dflash_kv* kv, int32_t* draft_ids, float* top2_gap,
                        float* hidden_out, void* ws, size_t ws_bytes, dflash_stream_t s);
 
+/* Steps 1-3 of one speculative round in one call: context fusion of the
+ * n_rows pending target features (hidden, as for dflash_fuse_context, into
+ * h_t_out), their K/V injection (seq_row0 / seq_rows as for
+ * dflash_inject_kv; kv->len advances by seq_rows), then the block draft of
+ * dflash_draft_block over the grown caches.  The result equals the three
+ * calls in that order.  Blocks of at most 16 rows with at most 16 pending
+ * rows (bf16, head dim 128) run as one persistent launch; other shapes run
+ * the three calls.  n_rows == 0 skips fusion and injection. */
+int dflash_draft_round(dflash_handle* h, const void* const* hidden, int32_t n_rows,
+                       const int32_t* seq_row0, const int32_t* seq_rows, void* h_t_out,
+                       const int32_t* anchor, int32_t batch, int32_t B, const dflash_kv* kv,
+                       int32_t* draft_ids, float* top2_gap, float* hidden_out, void* ws,
+                       size_t ws_bytes, dflash_stream_t s);
+
 /* Step 4 — greedy verification (integer only, no handle).
  * draft, post: device int32 [batch, B]; post[b, j] is the target's argmax at
  * block position j.  accept[b] = number of leading j in 1..B-1 with

@@ -63,4 +63,6 @@ def test_strerror_and_argument_errors(dfl):
     assert lib.dflash_verify_greedy(None, None, 1, 4, None, None, None, None, None, None, None) == 1
     assert lib.dflash_draft_block(None, None, 1, 4, None, None, None, None, None, 0, None) == 1
     assert lib.dflash_fuse_context(None, None, 1, None, None, 0, None) == 1
+    assert lib.dflash_draft_round(None, None, 4, None, None, None, None, 1, 4, None, None, None,
+                                  None, None, 0, None) == 1
     assert lib.dflash_workspace_bytes(None, 1, 16, 16) == 0
