@@ -78,6 +78,8 @@ _sig = {
                                      C.c_int32, C.POINTER(dflash_kv), _P, _P, _P, _P, C.c_size_t,
                                      _P]),
     "dflash_verify_greedy": (C.c_int, [_P, _P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
+    "dflash_emit_tokens": (C.c_int, [_P, _P, _P, C.c_int32, C.c_int32, _P, C.c_int32, _P, _P,
+                                     C.c_int32, _P, _P]),
     "dflash_lm_head_argmax": (C.c_int, [_P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
     "dflash_target_forward": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.POINTER(dflash_kv),
                                         C.POINTER(C.c_int32), C.c_int32, _P, _P, _P, C.c_size_t,
@@ -188,6 +190,17 @@ def dflash_draft_round(h: int, hidden: Sequence[torch.Tensor], n_rows: int,
                                    _ptr(top2_gap), _ptr(hidden_out), _ptr(ws),
                                    ws.numel() * ws.element_size(), _stream(stream)),
            "dflash_draft_round")
+
+
+def dflash_emit_tokens(h: int, out_tokens: torch.Tensor, tau: torch.Tensor, batch: int, B: int,
+                       out_buf: torch.Tensor, out_len: torch.Tensor,
+                       tau_log: Optional[torch.Tensor] = None,
+                       n_rounds: Optional[torch.Tensor] = None, stream=None):
+    """Append a round's emitted tokens (and its tau) on the device."""
+    log_cap = tau_log.shape[-1] if tau_log is not None else 0
+    _check(_lib.dflash_emit_tokens(h, _ptr(out_tokens), _ptr(tau), batch, B, _ptr(out_buf),
+                                   out_buf.shape[-1], _ptr(out_len), _ptr(tau_log), log_cap,
+                                   _ptr(n_rounds), _stream(stream)), "dflash_emit_tokens")
 
 
 def dflash_verify_greedy(draft: torch.Tensor, post: torch.Tensor, batch: int, B: int,

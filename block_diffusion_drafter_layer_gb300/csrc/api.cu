@@ -961,6 +961,17 @@ int dflash_verify_greedy(const int32_t* draft, const int32_t* post, int32_t batc
                        out_tokens, new_len);
 }
 
+int dflash_emit_tokens(dflash_handle* h, const int32_t* out_tokens, const int32_t* tau,
+                       int32_t batch, int32_t B, int32_t* out_buf, int32_t out_cap,
+                       int32_t* out_len, int32_t* tau_log, int32_t log_cap, int32_t* n_rounds,
+                       dflash_stream_t st) {
+  if (!h || !out_tokens || !tau || !out_buf || !out_len || batch < 1 || B < 1 || out_cap < 1 ||
+      (tau_log && (!n_rounds || log_cap < 1)))
+    return DFLASH_ERR_INVALID_ARG;
+  return emit_tokens((cudaStream_t)st, out_tokens, tau, batch, B, out_buf, out_cap, out_len,
+                     tau_log, log_cap, n_rounds, h->d_status);
+}
+
 int dflash_lm_head_argmax(dflash_handle* h, const float* x, int32_t rows, const float* norm_gain,
                           int32_t* ids, float* top2_gap, void* ws, size_t ws_bytes,
                           dflash_stream_t st) {

@@ -305,5 +305,8 @@ int argmax_rows(dflash_handle* h, cudaStream_t s, const float* logits, int64_t r
 int verify_greedy(cudaStream_t s, const int32_t* draft, const int32_t* post, int batch, int B,
                   const int32_t* start, int32_t* accept, int32_t* tau, int32_t* bonus,
                   int32_t* out_tokens, int32_t* new_len);
+int emit_tokens(cudaStream_t s, const int32_t* out_tokens, const int32_t* tau, int batch, int B,
+                int32_t* out_buf, int out_cap, int32_t* out_len, int32_t* tau_log, int log_cap,
+                int32_t* n_rounds, int* status);
 
 }  // namespace dflash

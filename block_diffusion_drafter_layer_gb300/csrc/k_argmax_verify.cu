@@ -110,4 +110,41 @@ int verify_greedy(cudaStream_t s, const int32_t* draft, const int32_t* post, int
   return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }
 
+// Device-side bookkeeping of a round (one thread per sequence): the round's
+// emitted tokens (the accepted drafts and the bonus, tau[b] of them) are
+// appended to the sequence's output at out_len[b], and tau is logged, so a
+// loop of rounds needs no host read in between.  A tau outside [1, B] flags
+// ST_BOUNDS and emits nothing; tokens past out_cap are counted, not stored.
+__global__ void emit_tokens_kernel(const int32_t* __restrict__ out_tokens,
+                                   const int32_t* __restrict__ tau, int batch, int B,
+                                   int32_t* out_buf, int out_cap, int32_t* out_len,
+                                   int32_t* tau_log, int log_cap, int32_t* n_rounds,
+                                   int* status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const int n = tau[b];
+  if (n < 1 || n > B) {
+    atomicOr(status, ST_BOUNDS);
+    return;
+  }
+  const int at = out_len[b];
+  for (int j = 0; j < n; ++j)
+    if (at + j < out_cap) out_buf[(int64_t)b * out_cap + at + j] = out_tokens[(int64_t)b * B + j];
+  out_len[b] = at + n;
+  if (tau_log && n_rounds) {
+    const int r = n_rounds[b];
+    if (r < log_cap) tau_log[(int64_t)b * log_cap + r] = n;
+    n_rounds[b] = r + 1;
+  }
+}
+
+int emit_tokens(cudaStream_t s, const int32_t* out_tokens, const int32_t* tau, int batch, int B,
+                int32_t* out_buf, int out_cap, int32_t* out_len, int32_t* tau_log, int log_cap,
+                int32_t* n_rounds, int* status) {
+  emit_tokens_kernel<<<(batch + 127) / 128, 128, 0, s>>>(out_tokens, tau, batch, B, out_buf, out_cap,
+                                                         out_len, tau_log, log_cap, n_rounds, status);
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
+}
+
 }  // namespace dflash

@@ -14,7 +14,8 @@ from typing import List, Sequence, Tuple
 import torch
 
 from . import (KVCache, Model, dflash_build_target_layer_ids, dflash_draft_block,
-               dflash_fuse_context, dflash_inject_kv, dflash_target_forward, dflash_verify_greedy)
+               dflash_draft_round, dflash_emit_tokens, dflash_fuse_context, dflash_inject_kv,
+               dflash_target_forward, dflash_verify_greedy)
 
 
 class SpecDecoder:
@@ -81,6 +82,71 @@ class SpecDecoder:
             pending, T = self.taps_block, a + 1
             taus.append(a + 1)
         return out[:n_new], taus
+
+    def generate_resident(self, prompt: Sequence[int], n_new: int, check_every: int = 8,
+                          block_sizes: Sequence[int] = ()) -> Tuple[List[int], List[int]]:
+        """The same loop with every round's state on the device: the round's
+        fusion + injection + draft is one dflash_draft_round call whose
+        pending rows are the previous round's tau (device) and whose anchor
+        is its bonus (device); dflash_emit_tokens appends the emitted tokens
+        and tau on the device.  The host reads the output length only every
+        `check_every` rounds (it may then run a few rounds past n_new, whose
+        tokens are dropped).
+
+        block_sizes: block sizes to schedule between (e.g. (16, 8)); at each
+        check the next rounds use the smallest listed size that still covers
+        the longest tau of the last window plus one (a block that is never
+        filled costs target rows and draft rows for nothing), and the largest
+        once a window's longest tau reaches the current size.  Empty: the
+        decoder's own B throughout.  Returns (tokens, tau per round)."""
+        self.reset()
+        dev = self.device
+        sizes = sorted(set(block_sizes)) or [self.B]
+        if sizes[-1] > self.B:
+            raise ValueError("block sizes above the decoder's B")
+        P = len(prompt)
+        td = self.taps_block.dtype
+        taps_pre = torch.empty(self.n_pick, P, self.D, dtype=td, device=dev)
+        argmax_pre = torch.empty(P, dtype=torch.int32, device=dev)
+        tokens = torch.tensor(prompt, dtype=torch.int32, device=dev)[None]
+        dflash_target_forward(self.target.handle, tokens, 1, P, self.tkv.struct, self.tap_ids,
+                              taps_pre, argmax_pre, self.ws_t)
+        cap = n_new + (check_every + 1) * self.B
+        out_buf = torch.zeros(1, cap, dtype=torch.int32, device=dev)
+        out_buf[0, 0] = argmax_pre[-1]
+        out_len = torch.ones(1, dtype=torch.int32, device=dev)
+        max_rounds = n_new + check_every
+        tau_log = torch.zeros(1, max_rounds, dtype=torch.int32, device=dev)
+        n_rounds = torch.zeros(1, dtype=torch.int32, device=dev)
+        anchor = argmax_pre[-1:]
+        pending, n_rows = taps_pre, P
+        seq_rows = torch.tensor([P], dtype=torch.int32, device=dev)
+        B = sizes[-1]
+        rounds = 0
+        while True:
+            dflash_draft_round(self.draft.handle, [pending[j] for j in range(self.n_pick)],
+                               n_rows, self.row0, seq_rows, self.h_t, anchor, 1, B,
+                               self.dkv.struct, self.draft_ids, None, None, self.ws_d)
+            self.start.copy_(self.tkv.len[:1])
+            dflash_target_forward(self.target.handle, self.draft_ids, 1, B, self.tkv.struct,
+                                  self.tap_ids, self.taps_block, self.post, self.ws_t)
+            dflash_verify_greedy(self.draft_ids, self.post, 1, B, self.start, self.accept,
+                                 self.tau, self.bonus, self.out_tokens, self.tkv.len)
+            dflash_emit_tokens(self.draft.handle, self.out_tokens, self.tau, 1, B, out_buf,
+                               out_len, tau_log, n_rounds)
+            anchor, pending, n_rows, seq_rows = self.bonus, self.taps_block, B, self.tau
+            rounds += 1
+            if rounds % check_every == 0 or rounds >= max_rounds:
+                if int(out_len.item()) >= n_new or rounds >= max_rounds:
+                    break
+                if len(sizes) > 1:
+                    recent = tau_log[0, rounds - check_every:rounds]
+                    longest = int(recent.max().item())
+                    fit = [b for b in sizes if b >= longest + 1]
+                    B = sizes[-1] if longest >= B else (fit[0] if fit else sizes[-1])
+        taus = tau_log[0, :int(n_rounds.item())].tolist()
+        n = min(int(out_len.item()), cap)
+        return out_buf[0, :n].tolist()[:n_new], taus
 
     def ar_decode(self, prompt: Sequence[int], n_new: int) -> List[int]:
         """The target's own greedy decode, one token per forward (M = 1)."""

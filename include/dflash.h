@@ -208,6 +208,21 @@ int dflash_verify_greedy(const int32_t* draft, const int32_t* post, int32_t batc
                          const int32_t* start, int32_t* accept, int32_t* tau, int32_t* bonus,
                          int32_t* out_tokens, int32_t* new_len, dflash_stream_t s);
 
+/* Device-side bookkeeping of a round, so a loop of rounds needs no host read
+ * in between (txtmix §9: the emitted tokens of a round are the accepted
+ * drafts and the bonus).  out_tokens, tau: device int32 [batch, B] and
+ * [batch] as written by dflash_verify_greedy.  For each sequence b the first
+ * tau[b] tokens are appended to out_buf[b, out_len[b] ..] (device int32
+ * [batch, out_cap]; tokens past out_cap are counted but not stored) and
+ * out_len[b] (device int32 [batch]) advances by tau[b].  tau_log (nullable,
+ * device int32 [batch, log_cap]) records tau at index n_rounds[b] (device
+ * int32 [batch], advanced by one).  The handle only supplies the status word:
+ * a tau outside [1, B] flags DFLASH_ERR_DEVICE_BOUNDS and emits nothing. */
+int dflash_emit_tokens(dflash_handle* h, const int32_t* out_tokens, const int32_t* tau,
+                       int32_t batch, int32_t B, int32_t* out_buf, int32_t out_cap,
+                       int32_t* out_len, int32_t* tau_log, int32_t log_cap, int32_t* n_rounds,
+                       dflash_stream_t s);
+
 /* Final RMSNorm + shared LM head + fused argmax over rows of an fp32
  * residual stream.  x: device fp32 [rows, D]; norm_gain: device fp32 [D];
  * ids: device int32 [rows]; top2_gap: nullable device fp32 [rows]. */

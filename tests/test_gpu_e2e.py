@@ -4,6 +4,7 @@ The loop's output must equal the oracle target's own greedy autoregressive
 output, token for token; the GPU's own autoregressive decode (one row per
 forward) must agree too, which checks that the kernels are row-invariant."""
 import collections
+import time
 
 import numpy as np
 import pytest
@@ -78,3 +79,80 @@ def test_e2e_lossless_all_blocks_accepted(dfl):
     np.testing.assert_array_equal(spec, ar_ref)
     np.testing.assert_array_equal(ar_gpu, ar_ref)
     assert taus == [w.B] * len(taus)
+
+
+def _run_both(dfl, w, TWn, DWn, prompt, n_new, **kw):
+    """The host-synchronised loop and the device-resident loop on the same
+    models, each timed (after a warm-up of both)."""
+    from synth.gpu import draft_model, spec_decoder, target_model
+    TW, DW = _upload(TWn), _upload(DWn)
+    DW["embed"], DW["lm_head"] = TW["embed"], TW["lm_head"]
+    cap = w.prompt_len + n_new + 12 * w.B
+    target = target_model(w.target, w.dtype, TW, max_pos=cap)
+    draft = draft_model(w.draft, w.dtype, DW, max_pos=cap)
+    dec = spec_decoder(w, target, draft, cap=cap)
+    dec.generate(prompt, 8)
+    dec.generate_resident(prompt, 8, **kw)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    host, host_taus = dec.generate(prompt, n_new)
+    t1 = time.perf_counter()
+    res, res_taus = dec.generate_resident(prompt, n_new, **kw)
+    torch.cuda.synchronize()
+    t2 = time.perf_counter()
+    assert dfl.dflash_get_status(target.handle) == 0
+    assert dfl.dflash_get_status(draft.handle) == 0
+    print(f"host-synchronised loop {n_new / (t1 - t0):.0f} tokens/s ({len(host_taus)} rounds), "
+          f"device-resident loop {n_new / (t2 - t1):.0f} tokens/s ({len(res_taus)} rounds, {kw})")
+    target.close()
+    draft.close()
+    return np.array(host), host_taus, np.array(res), res_taus
+
+
+def test_e2e_resident_loop_matches_host_loop(dfl):
+    """Device-resident rounds (dflash_draft_round, state on the device, a
+    host read every 4 rounds): the same tokens and the same tau per round as
+    the host-synchronised loop, and lossless."""
+    w = synth.WORKLOADS["e2e_f32"]
+    TW, DW = _weights(w)
+    prompt = synth.random_ids(w.prompt_len, w.target.V, seed=w.seed).tolist()
+    host, host_taus, res, res_taus = _run_both(dfl, w, TW, DW, prompt, w.new_tokens,
+                                               check_every=4)
+    ar_ref = O.ar_generate(w.target, to_np64(TW), prompt, w.new_tokens)
+    np.testing.assert_array_equal(host, ar_ref)
+    np.testing.assert_array_equal(res, ar_ref)
+    # the resident loop may run a few rounds past the end before its check
+    assert res_taus[:len(host_taus)] == host_taus
+    assert all(1 <= t <= w.B for t in res_taus)
+
+
+def test_e2e_resident_loop_block_schedule(dfl):
+    """Block sizes scheduled between 8 and 16 from the last window's taus:
+    still the target's own greedy output (any B is lossless)."""
+    w = synth.WORKLOADS["e2e_f32"]
+    TW, DW = _weights(w)
+    prompt = synth.random_ids(w.prompt_len, w.target.V, seed=w.seed + 5).tolist()
+    _, _, res, res_taus = _run_both(dfl, w, TW, DW, prompt, w.new_tokens, check_every=4,
+                                    block_sizes=(8, 16))
+    ar_ref = O.ar_generate(w.target, to_np64(TW), prompt, w.new_tokens)
+    np.testing.assert_array_equal(res, ar_ref)
+    hist = collections.Counter(res_taus)
+    print(f"scheduled blocks: rounds {len(res_taus)}, tau histogram {dict(sorted(hist.items()))}")
+    # short accepted prefixes move the schedule to 8-row blocks after the first window
+    if max(res_taus[:4]) < 8:
+        assert max(res_taus[4:8]) <= 8
+
+
+def test_e2e_resident_loop_all_accepted(dfl):
+    """Every draft accepted: tau = B every round, and the schedule stays at
+    the largest block."""
+    w = synth.with_(synth.WORKLOADS["e2e_f32"], new_tokens=96)
+    TW, DW = _weights(w)
+    c = 77
+    TW, DW = make_all_accept(TW, DW, w.target, c)
+    prompt = synth.random_ids(w.prompt_len - 1, w.target.V, seed=2).tolist() + [c]
+    _, _, res, res_taus = _run_both(dfl, w, TW, DW, prompt, w.new_tokens, check_every=2,
+                                    block_sizes=(8, 16))
+    ar_ref = O.ar_generate(w.target, to_np64(TW), prompt, w.new_tokens)
+    np.testing.assert_array_equal(res, ar_ref)
+    assert res_taus == [w.B] * len(res_taus)
