@@ -37,6 +37,14 @@ What pins each function (tests/test_oracle_*.py):
                            Geometric acceptance (Monte Carlo)
   target_forward + loops   losslessness: speculative output equals the
                            target's own greedy autoregressive output
+  sample_from              hand-computed inverse-CDF buckets (zero weights
+                           skipped, scale invariance), Monte Carlo frequencies
+  verify_rejection         the speculative-sampling theorem (chi-square: the
+                           emitted token follows p whatever q is), acceptance
+                           rate sum_x min(p, q), p = q accepts everything,
+                           one-hot p and q reduce to verify_greedy
+                           (exhaustive on tiny B and V)
+  speculative_sample_generate  T -> 0 limit equals the greedy loop
 """
 from __future__ import annotations
 
@@ -51,6 +59,8 @@ __all__ = [
     "embed_block", "draft_layer", "draft_block", "lm_head_logits",
     "argmax_lowest", "top2_gap", "verify_greedy", "expected_tau_from_prefix",
     "TargetCache", "target_forward", "ar_generate", "speculative_generate",
+    "softmax_t", "sample_from", "verify_rejection", "acceptance_probability",
+    "speculative_sample_generate",
 ]
 
 
@@ -363,6 +373,78 @@ def expected_tau_from_prefix(prefix_match_prob: Sequence[float]) -> float:
 
 
 # ---------------------------------------------------------------------------
+# sampling verification, T > 0 ([reading] §8: the acceptance probability is
+# p/q, the prefix ends at the first rejection, and the token after it is
+# drawn from max(p - q, 0) normalised; [translation] T = 1 experiments)
+# ---------------------------------------------------------------------------
+def softmax_t(z: np.ndarray, T: float) -> np.ndarray:
+    """softmax(z / T) over the last axis in fp64, T > 0."""
+    if not T > 0:
+        raise ValueError("temperature must be positive")
+    a = np.asarray(z, dtype=np.float64) / T
+    a = a - a.max(axis=-1, keepdims=True)
+    e = np.exp(a)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def sample_from(weights: np.ndarray, u: float) -> int:
+    """Inverse-CDF draw from non-negative weights (need not sum to 1): the
+    smallest index i whose running sum (fp64, in index order) exceeds
+    u * total, u in [0, 1).  An index of zero weight is never drawn."""
+    w = np.asarray(weights, dtype=np.float64)
+    c = np.cumsum(w)
+    i = int(np.searchsorted(c, u * c[-1], side="right"))
+    return min(i, len(w) - 1)
+
+
+def verify_rejection(draft: np.ndarray, q: np.ndarray, p: np.ndarray,
+                     u_accept: np.ndarray, u_sample: np.ndarray, start: np.ndarray):
+    """Speculative sampling verification per sequence.
+
+    draft[b] = [anchor, d_1 .. d_{B-1}], d_j drawn from q[b, j-1], the
+    draft's distribution at block position j.  p[b, j] (j = 0 .. B-1) is the
+    target's distribution of the token that follows block position j.  d_j
+    is accepted when u_accept[b, j-1] * q[b, j-1][d_j] < p[b, j-1][d_j]
+    (probability min(1, p/q)); the first rejection ends the prefix, a_b
+    drafts accepted.  The token after the prefix is drawn with u_sample[b]:
+    from max(p[b, a] - q[b, a], 0) renormalised when d_{a+1} was rejected,
+    from p[b, B-1] when every draft was accepted.  tau_b = a_b + 1.
+
+    Returns (accept, token, out_tokens [batch, B] padded with -1, new_len),
+    shaped like verify_greedy's result (token in the bonus's place)."""
+    draft = np.asarray(draft)
+    batch, B = draft.shape
+    accept = np.zeros(batch, dtype=np.int32)
+    token = np.zeros(batch, dtype=np.int32)
+    out = np.full((batch, B), -1, dtype=np.int32)
+    new_len = np.zeros(batch, dtype=np.int32)
+    for b in range(batch):
+        a = 0
+        while a < B - 1:
+            d = int(draft[b, a + 1])
+            if u_accept[b, a] * q[b, a][d] < p[b, a][d]:
+                a += 1
+            else:
+                break
+        if a < B - 1:
+            res = np.maximum(np.asarray(p[b, a], np.float64) - np.asarray(q[b, a], np.float64), 0.0)
+            tok = sample_from(res if res.sum() > 0 else p[b, a], float(u_sample[b]))
+        else:
+            tok = sample_from(p[b, B - 1], float(u_sample[b]))
+        accept[b] = a
+        token[b] = tok
+        out[b, :a] = draft[b, 1:a + 1]
+        out[b, a] = tok
+        new_len[b] = int(start[b]) + a + 1
+    return accept, token, out, new_len
+
+
+def acceptance_probability(p: np.ndarray, q: np.ndarray) -> float:
+    """P(a draft drawn from q is accepted against p) = sum_x min(p(x), q(x))."""
+    return float(np.minimum(np.asarray(p, np.float64), np.asarray(q, np.float64)).sum())
+
+
+# ---------------------------------------------------------------------------
 # end-to-end check: Llama-style causal target and the two decoders
 # ([reading] §9; [tutorial] data-flow section)
 # ---------------------------------------------------------------------------
@@ -384,13 +466,14 @@ class TargetCache:
 
 
 def target_forward(tshape, TW: dict, cache: TargetCache, tokens: Sequence[int],
-                   tap_ids: Sequence[int], store=f32):
+                   tap_ids: Sequence[int], store=f32, logits_out: list = None):
     """Causal forward of the target over ``tokens`` appended to ``cache``.
 
     One row at a time (row i at position len(cache) sees keys 0..pos), so a
     row's result does not depend on how many rows are processed together.
     Returns (argmax ids per row, taps [n_pick, n, D] fp32): a tap is the
-    residual stream after 0-based decoder layer ``id``."""
+    residual stream after 0-based decoder layer ``id``.  ``logits_out``
+    (a list), when given, receives each row's fp32 logits."""
     D, H, G, d = tshape.D, tshape.H, tshape.G, tshape.d
     ids_out, taps = [], [[] for _ in tap_ids]
     for tok in tokens:
@@ -418,6 +501,8 @@ def target_forward(tshape, TW: dict, cache: TargetCache, tokens: Sequence[int],
                     taps[j].append(x[0].copy())
         hf = store(rmsnorm(x, TW["g_final"], tshape.eps))
         z = lm_head_logits(hf, TW["lm_head"])
+        if logits_out is not None:
+            logits_out.append(z[0])
         ids_out.append(int(argmax_lowest(z)[0]))
     return np.array(ids_out, dtype=np.int32), np.array(taps, dtype=np.float64)
 
@@ -477,4 +562,56 @@ def speculative_generate(tshape, TW: dict, dshape, DW: dict,
         pending = vtaps[:, :a + 1, :]
         start = int(new_len[0])
         taus.append(a + 1)
+    return np.array(out[:n_new], dtype=np.int32), taus
+
+
+def speculative_sample_generate(tshape, TW: dict, dshape, DW: dict,
+                                prompt: Sequence[int], n_new: int, B: int, T: float,
+                                uniforms, store=f32):
+    """The DFlash loop at temperature T > 0 ([reading] §8, §9): drafts drawn
+    from the draft's softmax(z / T), verification by verify_rejection
+    against the target's softmax(z / T).  ``uniforms(round)`` returns that
+    round's (u_first, u_draft [B-1], u_accept [B-1], u_sample) draws; u_first
+    (round 0 only) draws the first token from the prefill's last row.
+
+    Returns (tokens [n_new], list of tau per round)."""
+    tap_ids = build_target_layer_ids(dshape.n_target_layers, dshape.n_pick)
+    cache = TargetCache(tshape.n_layers)
+    z_pre = []
+    _, taps = target_forward(tshape, TW, cache, prompt, tap_ids, store, z_pre)
+    u_first, _, _, _ = uniforms(0)
+    out = [sample_from(softmax_t(z_pre[-1], T), u_first)]
+    start = len(prompt)
+    ctx_K = [np.zeros((0, dshape.G, dshape.d)) for _ in DW["layers"]]
+    ctx_V = [np.zeros((0, dshape.G, dshape.d)) for _ in DW["layers"]]
+    pending = taps
+    taus = []
+    r = 0
+    while len(out) < n_new:
+        _, u_draft, u_accept, u_sample = uniforms(r)
+        Tn = pending.shape[1]
+        H_t = fuse_context(list(pending), DW["wc"], DW["g_c"], dshape.eps, store)
+        pos = np.arange(start - Tn, start)
+        for l, layer in enumerate(DW["layers"]):
+            k, v = inject_kv(H_t, layer, pos, dshape.G, dshape.d,
+                             dshape.rope_theta, dshape.eps, store)
+            ctx_K[l] = np.concatenate([ctx_K[l], k], axis=0)
+            ctx_V[l] = np.concatenate([ctx_V[l], v], axis=0)
+        _, _, z = draft_block(dshape, DW, [[k] for k in ctx_K], [[v] for v in ctx_V],
+                              [out[-1]], B, store, return_logits=True)
+        q = softmax_t(z[0], T)                                       # [B-1, V]
+        draft = np.array([[out[-1]] + [sample_from(q[j], u_draft[j]) for j in range(B - 1)]])
+        z_ver = []
+        _, vtaps = target_forward(tshape, TW, cache, draft[0], tap_ids, store, z_ver)
+        pv = softmax_t(np.array(z_ver), T)                           # [B, V]
+        accept, _, toks, new_len = verify_rejection(draft, q[None], pv[None],
+                                                    np.asarray(u_accept)[None],
+                                                    np.array([u_sample]), np.array([start]))
+        a = int(accept[0])
+        out.extend(int(t) for t in toks[0, :a + 1])
+        cache.crop(int(new_len[0]))
+        pending = vtaps[:, :a + 1, :]
+        start = int(new_len[0])
+        taus.append(a + 1)
+        r += 1
     return np.array(out[:n_new], dtype=np.int32), taus

@@ -255,3 +255,16 @@ def planted_posterior(draft: np.ndarray, p: float, V: int, seed: int):
             r = int(rng.integers(0, V - 1))
             post[b, kb] = (int(draft[b, kb + 1]) + 1 + r) % V
     return post.astype(np.int32), k.astype(np.int32)
+
+
+def round_uniforms(seed: int, B: int):
+    """Seeded uniform [0, 1) draws of a sampling loop (T > 0), as a function
+    of the round r: (u_first, u_draft [B-1], u_accept [B-1], u_sample).
+    u_first draws the first token from the prefill's last row (round 0);
+    u_draft draws the B-1 drafts, u_accept decides each draft's acceptance
+    and u_sample draws the token after the accepted prefix.  Both the GPU
+    loop and the oracle's loop consume these same numbers."""
+    def draws(r: int):
+        g = np.random.default_rng([seed, r])
+        return (float(g.random()), g.random(B - 1), g.random(B - 1), float(g.random()))
+    return draws

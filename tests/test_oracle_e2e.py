@@ -48,6 +48,32 @@ def test_speculative_all_accepted_blocks():
     assert taus == [B] * len(taus)
 
 
+def test_sampling_loop_low_temperature_is_the_greedy_loop():
+    """T -> 0: every softmax is one-hot at the argmax, so the sampling loop
+    draws the argmax drafts and verification reduces to the greedy rule:
+    the same tokens and taus as the greedy loop, whatever the uniforms."""
+    tshape, dshape = tiny_e2e()
+    TW, DW = _weights(tshape, dshape, 60)
+    prompt = synth.random_ids(11, tshape.V, seed=6).tolist()
+    B, n_new = 4, 16
+    greedy, gt = O.speculative_generate(tshape, TW, dshape, DW, prompt, n_new, B)
+    samp, st = O.speculative_sample_generate(tshape, TW, dshape, DW, prompt, n_new, B, 1e-6,
+                                             synth.round_uniforms(1, B))
+    np.testing.assert_array_equal(samp, greedy)
+    assert st == gt
+
+
+def test_sampling_loop_taus_in_range():
+    tshape, dshape = tiny_e2e()
+    TW, DW = _weights(tshape, dshape, 61)
+    prompt = synth.random_ids(11, tshape.V, seed=7).tolist()
+    B, n_new = 5, 16
+    out, taus = O.speculative_sample_generate(tshape, TW, dshape, DW, prompt, n_new, B, 1.0,
+                                              synth.round_uniforms(2, B))
+    assert len(out) == n_new and all(0 <= t < tshape.V for t in out)
+    assert all(1 <= t <= B for t in taus) and sum(taus) + 1 >= n_new
+
+
 def test_speculative_equals_autoregressive_bf16_storage():
     tshape, dshape = tiny_e2e()
     TW, DW = _weights(tshape, dshape, 91)
