@@ -81,6 +81,12 @@ _sig = {
     "dflash_emit_tokens": (C.c_int, [_P, _P, _P, C.c_int32, C.c_int32, _P, C.c_int32, _P, _P,
                                      C.c_int32, _P, _P]),
     "dflash_lm_head_argmax": (C.c_int, [_P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
+    "dflash_lm_head_logits": (C.c_int, [_P, _P, C.c_int32, _P, C.c_int32, _P, _P, C.c_size_t,
+                                        _P]),
+    "dflash_sample_rows": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.c_float, _P, _P, C.c_int32,
+                                     _P, _P]),
+    "dflash_verify_rejection": (C.c_int, [_P, _P, _P, _P, C.c_int32, _P, _P, C.c_int32,
+                                          C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_target_forward": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.POINTER(dflash_kv),
                                         C.POINTER(C.c_int32), C.c_int32, _P, _P, _P, C.c_size_t,
                                         _P]),
@@ -203,6 +209,33 @@ def dflash_emit_tokens(h: int, out_tokens: torch.Tensor, tau: torch.Tensor, batc
                                    _ptr(n_rounds), _stream(stream)), "dflash_emit_tokens")
 
 
+def dflash_lm_head_logits(h: int, x: torch.Tensor, rows: int, norm_gain: torch.Tensor,
+                          logits: torch.Tensor, ws: torch.Tensor, skip_first_of: int = 0,
+                          stream=None):
+    _check(_lib.dflash_lm_head_logits(h, _ptr(x), rows, _ptr(norm_gain), skip_first_of,
+                                      _ptr(logits), _ptr(ws), ws.numel() * ws.element_size(),
+                                      _stream(stream)), "dflash_lm_head_logits")
+
+
+def dflash_sample_rows(h: int, logits: torch.Tensor, rows: int, vocab: int, temperature: float,
+                       u: Optional[torch.Tensor], ids: Optional[torch.Tensor],
+                       probs: Optional[torch.Tensor] = None, ids_stride: int = 1, stream=None):
+    _check(_lib.dflash_sample_rows(h, _ptr(logits), rows, vocab, temperature, _ptr(u), _ptr(ids),
+                                   ids_stride, _ptr(probs), _stream(stream)), "dflash_sample_rows")
+
+
+def dflash_verify_rejection(h: int, draft: torch.Tensor, q_probs: torch.Tensor,
+                            p_probs: torch.Tensor, vocab: int, u_accept: torch.Tensor,
+                            u_sample: torch.Tensor, batch: int, B: int, start: torch.Tensor,
+                            accept: torch.Tensor, tau: Optional[torch.Tensor],
+                            token: Optional[torch.Tensor], out_tokens: torch.Tensor,
+                            new_len: Optional[torch.Tensor], stream=None):
+    _check(_lib.dflash_verify_rejection(h, _ptr(draft), _ptr(q_probs), _ptr(p_probs), vocab,
+                                        _ptr(u_accept), _ptr(u_sample), batch, B, _ptr(start),
+                                        _ptr(accept), _ptr(tau), _ptr(token), _ptr(out_tokens),
+                                        _ptr(new_len), _stream(stream)), "dflash_verify_rejection")
+
+
 def dflash_verify_greedy(draft: torch.Tensor, post: torch.Tensor, batch: int, B: int,
                          start: torch.Tensor, accept: torch.Tensor, tau: Optional[torch.Tensor],
                          bonus: torch.Tensor, out_tokens: torch.Tensor,
@@ -316,6 +349,8 @@ class Model:
                 setattr(w.layers[l], name, _ptr(lay.get(name)))
         self.cfg, self.w, self.weights = cfg, w, weights
         self.dtype = dtype
+        self.vocab, self.n_layers = V, n_layers
+        self.final_gain = weights.get("g_f", weights.get("g_final"))   # the final RMSNorm's gain
         self.handle = dflash_create(cfg, w)
 
     def workspace(self, max_rows: int, device="cuda", max_batch: int = 0,

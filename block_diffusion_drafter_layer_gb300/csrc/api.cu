@@ -409,6 +409,46 @@ static int lm_head_tc(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows, in
   return tc_gemm(h, s, DFLASH_K_LM_HEAD, L, f.amx);
 }
 
+// fp32 logits of rows through the final RMSNorm (gain) and the shared LM
+// head: the same projections as lm_head with the fp32-store epilogue.
+static int lm_logits(dflash_handle* h, cudaStream_t s, Fwd& f, const float* x, int64_t rows,
+                     const float* gain, int skip_first_of, float* logits) {
+  const dflash_config& c = h->cfg;
+  const int D = c.hidden, V = c.vocab, dt = c.dtype;
+  int rc;
+  if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, x, D, f.hf, D, gain, rows, D, c.rms_eps,
+                         skip_first_of)))
+    return rc;
+  if (streaming(h, rows) && V % 4 == 0) {
+    WLaunch L;
+    L.nmap = 1;
+    L.wmaps[0] = &h->map_lm;
+    L.nseg = 1;
+    L.seg[0] = make_seg(0, (V + 127) / 128, SK_F32, 0, V, logits, V);
+    L.nsrc = 1;
+    L.a_src[0] = f.hf;
+    L.a_ld = D;
+    L.K = D;
+    L.M = (int)rows;
+    return wstream(h, s, DFLASH_K_LM_HEAD, L, f.partial, nullptr);
+  }
+  if (dense_tc(h, rows) && V % 32 == 0) {
+    WLaunch L;
+    L.nmap = 1;
+    L.wmaps[0] = &h->map_tc_lm;
+    L.nseg = 1;
+    L.seg[0] = make_seg(0, (V + 255) / 256, SK_F32, 0, V, logits, V);
+    L.nsrc = 1;
+    L.a_src[0] = f.hf;
+    L.a_ld = D;
+    L.K = D;
+    L.M = (int)rows;
+    return tc_gemm(h, s, DFLASH_K_LM_HEAD, L);
+  }
+  return gemm(h, s, DFLASH_K_LM_HEAD, dt, one_src(f.hf, D, D), h->w.lm_head, D, logits, V, rows,
+              V, D, false);
+}
+
 static bool kv_ok(const dflash_handle* h, const dflash_kv* kv, int batch) {
   if (!kv || !kv->len || kv->cap <= 0 || kv->batch_cap < batch) return false;
   for (int l = 0; l < h->cfg.n_layers; ++l)
@@ -812,7 +852,8 @@ int dflash_inject_kv(dflash_handle* h, const void* h_t, int64_t n_rows, const in
 int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, int32_t B,
                        const dflash_kv* kv, int32_t* draft_ids, float* top2_gap, float* hidden_out,
                        void* ws, size_t ws_bytes, dflash_stream_t st) {
-  if (!h || !anchor || !draft_ids || !ws || batch < 1 || B < 1) return DFLASH_ERR_INVALID_ARG;
+  if (!h || !anchor || (!draft_ids && !hidden_out) || !ws || batch < 1 || B < 1)
+    return DFLASH_ERR_INVALID_ARG;
   if (!kv_ok(h, kv, batch)) return DFLASH_ERR_INVALID_ARG;
   if (!aligned16(ws)) return DFLASH_ERR_ALIGNMENT;
   cudaStream_t s = (cudaStream_t)st;
@@ -831,7 +872,7 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
     if (hidden_out &&
         cudaMemcpyAsync(hidden_out, f.x, R * D * sizeof(float), cudaMemcpyDeviceToDevice, s))
       return DFLASH_ERR_CUDA;
-    if (B == 1 &&
+    if (B == 1 && draft_ids &&
         cudaMemcpyAsync(draft_ids, anchor, batch * sizeof(int32_t), cudaMemcpyDeviceToDevice, s))
       return DFLASH_ERR_CUDA;
     return DFLASH_OK;
@@ -890,6 +931,7 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
   if (hidden_out &&
       cudaMemcpyAsync(hidden_out, f.x, R * D * sizeof(float), cudaMemcpyDeviceToDevice, s))
     return DFLASH_ERR_CUDA;
+  if (!draft_ids) return DFLASH_OK;   // the residual only (the caller samples)
   if (B == 1) {
     if (cudaMemcpyAsync(draft_ids, anchor, batch * sizeof(int32_t), cudaMemcpyDeviceToDevice, s))
       return DFLASH_ERR_CUDA;
@@ -980,6 +1022,42 @@ int dflash_lm_head_argmax(dflash_handle* h, const float* x, int32_t rows, const 
   Fwd f;
   if (!carve_forward(h, rows, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
   return lm_head(h, (cudaStream_t)st, f, x, rows, norm_gain, 0, ids, top2_gap, 0, nullptr);
+}
+
+int dflash_lm_head_logits(dflash_handle* h, const float* x, int32_t rows, const float* norm_gain,
+                          int32_t skip_first_of, float* logits, void* ws, size_t ws_bytes,
+                          dflash_stream_t st) {
+  if (!h || !x || !norm_gain || !logits || !ws || rows < 0 || skip_first_of < 0 ||
+      skip_first_of == 1)
+    return DFLASH_ERR_INVALID_ARG;
+  if (rows == 0) return DFLASH_OK;
+  if (!aligned16(logits) || !aligned16(ws)) return DFLASH_ERR_ALIGNMENT;
+  Fwd f;
+  if (!carve_forward(h, rows, ws, ws_bytes, &f)) return DFLASH_ERR_WORKSPACE;
+  return lm_logits(h, (cudaStream_t)st, f, x, rows, norm_gain, skip_first_of, logits);
+}
+
+int dflash_sample_rows(dflash_handle* h, const float* logits, int32_t rows, int32_t vocab,
+                       float temperature, const double* u, int32_t* ids, int32_t ids_stride,
+                       float* probs, dflash_stream_t st) {
+  if (!h || !logits || rows < 0 || vocab < 1 || !(temperature > 0.f) || (!ids && !probs) ||
+      (ids && (!u || ids_stride < 1)))
+    return DFLASH_ERR_INVALID_ARG;
+  if (rows == 0) return DFLASH_OK;
+  return sample_rows(h, (cudaStream_t)st, logits, rows, vocab, temperature, u, ids, ids_stride,
+                     probs);
+}
+
+int dflash_verify_rejection(dflash_handle* h, const int32_t* draft, const float* q_probs,
+                            const float* p_probs, int32_t vocab, const double* u_accept,
+                            const double* u_sample, int32_t batch, int32_t B,
+                            const int32_t* start, int32_t* accept, int32_t* tau, int32_t* token,
+                            int32_t* out_tokens, int32_t* new_len, dflash_stream_t st) {
+  if (!h || !draft || !q_probs || !p_probs || vocab < 1 || !u_sample || batch < 1 || B < 1 ||
+      (B > 1 && !u_accept) || !start || !accept || !out_tokens)
+    return DFLASH_ERR_INVALID_ARG;
+  return verify_rejection(h, (cudaStream_t)st, draft, q_probs, p_probs, vocab, u_accept, u_sample,
+                          batch, B, start, accept, tau, token, out_tokens, new_len);
 }
 
 int dflash_target_forward(dflash_handle* h, const int32_t* tokens, int32_t batch, int32_t T,

@@ -1617,9 +1617,10 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
                         (kChainTraceCols - 3) * col + kEvWords * sizeof(unsigned long long), s))
       return DFLASH_ERR_CUDA;
     P.trace = h->d_trace;
-    h->trace_phases = P.pre + 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 3 : 0);
+    h->trace_phases = P.pre + 1 + kLayerPhases * c.n_layers + (A.B > 1 && A.ids ? 3 : 0);
   }
-  P.n_phases = P.pre + 1 + kLayerPhases * c.n_layers + (A.B > 1 ? 3 : 0);
+  // no LM-head phases when the caller takes the residual only (B = 1, or no ids)
+  P.n_phases = P.pre + 1 + kLayerPhases * c.n_layers + (A.B > 1 && A.ids ? 3 : 0);
   P.n_items_max = P.grid + A.batch * c.n_kv_heads;
   P.eps = c.rms_eps;
   P.embed_scale = c.embed_scale;

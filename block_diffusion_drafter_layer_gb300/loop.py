@@ -15,7 +15,8 @@ import torch
 
 from . import (KVCache, Model, dflash_build_target_layer_ids, dflash_draft_block,
                dflash_draft_round, dflash_emit_tokens, dflash_fuse_context, dflash_inject_kv,
-               dflash_target_forward, dflash_verify_greedy)
+               dflash_lm_head_logits, dflash_sample_rows, dflash_target_forward,
+               dflash_verify_greedy, dflash_verify_rejection)
 
 
 class SpecDecoder:
@@ -147,6 +148,78 @@ class SpecDecoder:
         taus = tau_log[0, :int(n_rounds.item())].tolist()
         n = min(int(out_len.item()), cap)
         return out_buf[0, :n].tolist()[:n_new], taus
+
+    def generate_sampled(self, prompt: Sequence[int], n_new: int, temperature: float,
+                         uniforms) -> Tuple[List[int], List[int]]:
+        """The loop at temperature T > 0 (txtmix §8): each draft is drawn
+        from the draft's softmax(z / T) (dflash_draft_block without its LM
+        head, dflash_lm_head_logits, dflash_sample_rows), verified against
+        the target's softmax(z / T) by dflash_verify_rejection.  The target's
+        final hidden rows come from a tap at its last layer.  ``uniforms(r)``
+        gives round r's (u_first, u_draft [B-1], u_accept [B-1], u_sample).
+        Returns (tokens, tau per round)."""
+        self.reset()
+        dev, B, D = self.device, self.B, self.D
+        T = float(temperature)
+        V = self.target.vocab
+        L = self.target.n_layers
+        taps_ids = list(self.tap_ids) + [L - 1]
+        n_t = len(taps_ids)
+        P = len(prompt)
+        td = self.taps_block.dtype
+        taps_pre = torch.empty(n_t, P, D, dtype=td, device=dev)
+        argmax_pre = torch.empty(P, dtype=torch.int32, device=dev)
+        tokens = torch.tensor(prompt, dtype=torch.int32, device=dev)[None]
+        dflash_target_forward(self.target.handle, tokens, 1, P, self.tkv.struct, taps_ids,
+                              taps_pre, argmax_pre, self.ws_t)
+        f64 = lambda a: torch.as_tensor(a, dtype=torch.float64).reshape(-1).to(dev)
+        g_t, g_d = self.target.final_gain, self.draft.final_gain
+        z_t = torch.empty(B, V, dtype=torch.float32, device=dev)
+        p_t = torch.empty(1, B, V, dtype=torch.float32, device=dev)
+        z_d = torch.empty(B - 1, V, dtype=torch.float32, device=dev)
+        q_d = torch.empty(1, B - 1, V, dtype=torch.float32, device=dev)
+        hid = torch.empty(B, D, dtype=torch.float32, device=dev)
+        first = torch.empty(1, dtype=torch.int32, device=dev)
+        u_first, _, _, _ = uniforms(0)
+        last = taps_pre[n_t - 1, P - 1:P].float()
+        dflash_lm_head_logits(self.target.handle, last, 1, g_t, z_t, self.ws_t)
+        dflash_sample_rows(self.target.handle, z_t, 1, V, T, f64([u_first]), first)
+        out = [int(first.item())]
+        taps_blk = torch.empty(n_t, B, D, dtype=td, device=dev)
+        pending, Tn = taps_pre, P
+        taus = []
+        r = 0
+        while len(out) < n_new:
+            _, u_draft, u_accept, u_sample = uniforms(r)
+            dflash_fuse_context(self.draft.handle, [pending[j] for j in range(self.n_pick)], Tn,
+                                self.h_t, self.ws_d)
+            nrows = torch.tensor([Tn], dtype=torch.int32, device=dev)
+            dflash_inject_kv(self.draft.handle, self.h_t, Tn, self.row0, nrows, 1,
+                             self.dkv.struct, self.ws_d)
+            self.draft_ids[0, 0] = out[-1]
+            anchor = self.draft_ids[0, :1].clone()
+            dflash_draft_block(self.draft.handle, anchor, 1, B, self.dkv.struct, None, None,
+                               hid, self.ws_d)
+            dflash_lm_head_logits(self.draft.handle, hid, B - 1, g_d, z_d, self.ws_d,
+                                  skip_first_of=B)
+            dflash_sample_rows(self.draft.handle, z_d, B - 1, V, T, f64(u_draft),
+                               self.draft_ids[0, 1:], q_d[0])
+            self.start.copy_(self.tkv.len[:1])
+            dflash_target_forward(self.target.handle, self.draft_ids, 1, B, self.tkv.struct,
+                                  taps_ids, taps_blk, self.post, self.ws_t)
+            dflash_lm_head_logits(self.target.handle, taps_blk[n_t - 1].float().contiguous(), B,
+                                  g_t, z_t, self.ws_t)
+            dflash_sample_rows(self.target.handle, z_t, B, V, T, None, None, p_t[0])
+            dflash_verify_rejection(self.target.handle, self.draft_ids, q_d, p_t, V,
+                                    f64(u_accept), f64([u_sample]), 1, B, self.start,
+                                    self.accept, self.tau, self.bonus, self.out_tokens,
+                                    self.tkv.len)
+            a = int(self.accept.item())
+            out.extend(int(t) for t in self.out_tokens[0, :a + 1].tolist())
+            pending, Tn = taps_blk, a + 1
+            taus.append(a + 1)
+            r += 1
+        return out[:n_new], taus
 
     def ar_decode(self, prompt: Sequence[int], n_new: int) -> List[int]:
         """The target's own greedy decode, one token per forward (M = 1)."""

@@ -175,7 +175,10 @@ int dflash_inject_kv(dflash_handle* h, const void* h_t, int64_t n_rows,
  * len[b] cached context entries of each layer.  The cache is only read:
  * the block's own K/V live in the workspace.
  *   draft_ids: device int32 [batch, B]; column 0 = anchor, columns 1..B-1 =
- *              argmax (lowest index on ties) of the fp32 logits.
+ *              argmax (lowest index on ties) of the fp32 logits.  May be
+ *              NULL when hidden_out is given: the LM head is skipped (a
+ *              caller that samples at T > 0 takes the residual, then
+ *              dflash_lm_head_logits and dflash_sample_rows).
  *   top2_gap:  nullable device fp32 [batch, B-1], top-1 minus top-2 logit.
  *   hidden_out: nullable device fp32 [batch*B, D], the residual stream after
  *              the last layer (before the final norm). */
@@ -229,6 +232,44 @@ int dflash_emit_tokens(dflash_handle* h, const int32_t* out_tokens, const int32_
 int dflash_lm_head_argmax(dflash_handle* h, const float* x, int32_t rows, const float* norm_gain,
                           int32_t* ids, float* top2_gap, void* ws, size_t ws_bytes,
                           dflash_stream_t s);
+
+/* fp32 logits of rows of an fp32 residual stream through the final RMSNorm
+ * (norm_gain, device fp32 [D]) and the shared LM head.  x: device fp32;
+ * logits: device fp32 [rows, V] (16-byte aligned).  skip_first_of = 0 reads
+ * x as [rows, D]; skip_first_of = B > 1 reads x as blocks of B rows and
+ * skips the first row of each (the anchors), so rows = batch * (B - 1). */
+int dflash_lm_head_logits(dflash_handle* h, const float* x, int32_t rows, const float* norm_gain,
+                          int32_t skip_first_of, float* logits, void* ws, size_t ws_bytes,
+                          dflash_stream_t s);
+
+/* Sampling at temperature T > 0 (txtmix §8, the T = 1 setting of the
+ * paper's experiments).  For each row of logits (device fp32 [rows, vocab])
+ * p = softmax(logits / T); probs (nullable, device fp32 [rows, vocab])
+ * receives p; ids (nullable, device int32, row r at ids[r * ids_stride])
+ * receives the inverse-CDF draw with u[r] (device fp64 [rows], uniform in
+ * [0, 1)): the smallest index whose running sum of p in index order exceeds
+ * u[r] times the total.  At least one of ids and probs is required. */
+int dflash_sample_rows(dflash_handle* h, const float* logits, int32_t rows, int32_t vocab,
+                       float temperature, const double* u, int32_t* ids, int32_t ids_stride,
+                       float* probs, dflash_stream_t s);
+
+/* Speculative sampling verification (txtmix §8: acceptance probability p/q,
+ * the prefix ends at the first rejection, the token after it is drawn from
+ * max(p - q, 0) renormalised).  draft: device int32 [batch, B] =
+ * [anchor, d_1 .. d_{B-1}]; q_probs: device fp32 [batch, B-1, vocab], the
+ * draft's distribution at block positions 1..B-1 (d_j was drawn from row
+ * j-1); p_probs: device fp32 [batch, B, vocab], the target's distribution of
+ * the token after block position j.  d_j is accepted when
+ * u_accept[b, j-1] * q(d_j) < p(d_j) (device fp64 [batch, B-1]); with a
+ * drafts accepted, the token after them is drawn with u_sample[b] (device
+ * fp64 [batch]) from max(p[a] - q[a], 0) when d_{a+1} was rejected, from
+ * p[B-1] when all were accepted.  Outputs as dflash_verify_greedy
+ * (token: nullable device int32 [batch], the drawn token). */
+int dflash_verify_rejection(dflash_handle* h, const int32_t* draft, const float* q_probs,
+                            const float* p_probs, int32_t vocab, const double* u_accept,
+                            const double* u_sample, int32_t batch, int32_t B,
+                            const int32_t* start, int32_t* accept, int32_t* tau, int32_t* token,
+                            int32_t* out_tokens, int32_t* new_len, dflash_stream_t s);
 
 /* Causal forward of a target model (qk_norm == 0 handle) over T new tokens
  * per sequence, appended to its cache.  tokens: device int32 [batch, T] at
