@@ -83,10 +83,12 @@ _sig = {
     "dflash_lm_head_argmax": (C.c_int, [_P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
     "dflash_lm_head_logits": (C.c_int, [_P, _P, C.c_int32, _P, C.c_int32, _P, _P, C.c_size_t,
                                         _P]),
+    "dflash_sampling_ws_bytes": (C.c_size_t, [C.c_int32, C.c_int32]),
     "dflash_sample_rows": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.c_float, _P, _P, C.c_int32,
-                                     _P, _P]),
+                                     _P, _P, C.c_size_t, _P]),
     "dflash_verify_rejection": (C.c_int, [_P, _P, _P, _P, C.c_int32, _P, _P, C.c_int32,
-                                          C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
+                                          C.c_int32, _P, _P, _P, _P, _P, _P, _P, C.c_size_t,
+                                          _P]),
     "dflash_target_forward": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.POINTER(dflash_kv),
                                         C.POINTER(C.c_int32), C.c_int32, _P, _P, _P, C.c_size_t,
                                         _P]),
@@ -217,11 +219,26 @@ def dflash_lm_head_logits(h: int, x: torch.Tensor, rows: int, norm_gain: torch.T
                                       _stream(stream)), "dflash_lm_head_logits")
 
 
+def dflash_sampling_ws_bytes(rows: int, vocab: int) -> int:
+    return int(_lib.dflash_sampling_ws_bytes(rows, vocab))
+
+
+def _sampling_ws(ws, rows, vocab, like):
+    if ws is None:   # scratch from torch's caching allocator
+        ws = torch.empty(dflash_sampling_ws_bytes(rows, vocab), dtype=torch.uint8,
+                         device=like.device)
+    return ws
+
+
 def dflash_sample_rows(h: int, logits: torch.Tensor, rows: int, vocab: int, temperature: float,
                        u: Optional[torch.Tensor], ids: Optional[torch.Tensor],
-                       probs: Optional[torch.Tensor] = None, ids_stride: int = 1, stream=None):
+                       probs: Optional[torch.Tensor] = None, ids_skip_first_of: int = 0,
+                       ws: Optional[torch.Tensor] = None, stream=None):
+    ws = _sampling_ws(ws, rows, vocab, logits)
     _check(_lib.dflash_sample_rows(h, _ptr(logits), rows, vocab, temperature, _ptr(u), _ptr(ids),
-                                   ids_stride, _ptr(probs), _stream(stream)), "dflash_sample_rows")
+                                   ids_skip_first_of, _ptr(probs), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream)),
+           "dflash_sample_rows")
 
 
 def dflash_verify_rejection(h: int, draft: torch.Tensor, q_probs: torch.Tensor,
@@ -229,11 +246,14 @@ def dflash_verify_rejection(h: int, draft: torch.Tensor, q_probs: torch.Tensor,
                             u_sample: torch.Tensor, batch: int, B: int, start: torch.Tensor,
                             accept: torch.Tensor, tau: Optional[torch.Tensor],
                             token: Optional[torch.Tensor], out_tokens: torch.Tensor,
-                            new_len: Optional[torch.Tensor], stream=None):
+                            new_len: Optional[torch.Tensor], ws: Optional[torch.Tensor] = None,
+                            stream=None):
+    ws = _sampling_ws(ws, batch, vocab, p_probs)
     _check(_lib.dflash_verify_rejection(h, _ptr(draft), _ptr(q_probs), _ptr(p_probs), vocab,
                                         _ptr(u_accept), _ptr(u_sample), batch, B, _ptr(start),
                                         _ptr(accept), _ptr(tau), _ptr(token), _ptr(out_tokens),
-                                        _ptr(new_len), _stream(stream)), "dflash_verify_rejection")
+                                        _ptr(new_len), _ptr(ws), ws.numel() * ws.element_size(),
+                                        _stream(stream)), "dflash_verify_rejection")
 
 
 def dflash_verify_greedy(draft: torch.Tensor, post: torch.Tensor, batch: int, B: int,

@@ -1037,27 +1037,38 @@ int dflash_lm_head_logits(dflash_handle* h, const float* x, int32_t rows, const 
   return lm_logits(h, (cudaStream_t)st, f, x, rows, norm_gain, skip_first_of, logits);
 }
 
+size_t dflash_sampling_ws_bytes(int32_t rows, int32_t vocab) {
+  if (rows < 0 || vocab < 1) return 0;
+  return sampling_ws_bytes(rows, vocab);
+}
+
 int dflash_sample_rows(dflash_handle* h, const float* logits, int32_t rows, int32_t vocab,
-                       float temperature, const double* u, int32_t* ids, int32_t ids_stride,
-                       float* probs, dflash_stream_t st) {
+                       float temperature, const double* u, int32_t* ids,
+                       int32_t ids_skip_first_of, float* probs, void* ws, size_t ws_bytes,
+                       dflash_stream_t st) {
   if (!h || !logits || rows < 0 || vocab < 1 || !(temperature > 0.f) || (!ids && !probs) ||
-      (ids && (!u || ids_stride < 1)))
+      (ids && !u) || ids_skip_first_of < 0 || ids_skip_first_of == 1 || !ws)
     return DFLASH_ERR_INVALID_ARG;
+  if (((uintptr_t)ws & 255) != 0) return DFLASH_ERR_ALIGNMENT;
+  if (ws_bytes < sampling_ws_bytes(rows, vocab)) return DFLASH_ERR_WORKSPACE;
   if (rows == 0) return DFLASH_OK;
-  return sample_rows(h, (cudaStream_t)st, logits, rows, vocab, temperature, u, ids, ids_stride,
-                     probs);
+  return sample_rows(h, (cudaStream_t)st, logits, rows, vocab, temperature, u, ids,
+                     ids_skip_first_of, probs, ws);
 }
 
 int dflash_verify_rejection(dflash_handle* h, const int32_t* draft, const float* q_probs,
                             const float* p_probs, int32_t vocab, const double* u_accept,
                             const double* u_sample, int32_t batch, int32_t B,
                             const int32_t* start, int32_t* accept, int32_t* tau, int32_t* token,
-                            int32_t* out_tokens, int32_t* new_len, dflash_stream_t st) {
+                            int32_t* out_tokens, int32_t* new_len, void* ws, size_t ws_bytes,
+                            dflash_stream_t st) {
   if (!h || !draft || !q_probs || !p_probs || vocab < 1 || !u_sample || batch < 1 || B < 1 ||
-      (B > 1 && !u_accept) || !start || !accept || !out_tokens)
+      (B > 1 && !u_accept) || !start || !accept || !out_tokens || !ws)
     return DFLASH_ERR_INVALID_ARG;
+  if (((uintptr_t)ws & 255) != 0) return DFLASH_ERR_ALIGNMENT;
+  if (ws_bytes < sampling_ws_bytes(batch, vocab)) return DFLASH_ERR_WORKSPACE;
   return verify_rejection(h, (cudaStream_t)st, draft, q_probs, p_probs, vocab, u_accept, u_sample,
-                          batch, B, start, accept, tau, token, out_tokens, new_len);
+                          batch, B, start, accept, tau, token, out_tokens, new_len, ws);
 }
 
 int dflash_target_forward(dflash_handle* h, const int32_t* tokens, int32_t batch, int32_t T,

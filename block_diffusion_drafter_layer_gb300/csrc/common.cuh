@@ -310,11 +310,12 @@ int emit_tokens(cudaStream_t s, const int32_t* out_tokens, const int32_t* tau, i
                 int32_t* n_rounds, int* status);
 
 // ---- sampling at T > 0 (k_sampling.cu) ------------------------------------
+size_t sampling_ws_bytes(int rows, int V);
 int sample_rows(dflash_handle* h, cudaStream_t s, const float* logits, int rows, int V, float T,
-                const double* u, int32_t* ids, int ids_stride, float* probs);
+                const double* u, int32_t* ids, int ids_skip_first_of, float* probs, void* ws);
 int verify_rejection(dflash_handle* h, cudaStream_t s, const int32_t* draft, const float* q,
                      const float* p, int V, const double* u_acc, const double* u_smp, int batch,
                      int B, const int32_t* start, int32_t* accept, int32_t* tau, int32_t* token,
-                     int32_t* out_tokens, int32_t* new_len);
+                     int32_t* out_tokens, int32_t* new_len, void* ws);
 
 }  // namespace dflash

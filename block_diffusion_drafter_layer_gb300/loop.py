@@ -15,7 +15,8 @@ import torch
 
 from . import (KVCache, Model, dflash_build_target_layer_ids, dflash_draft_block,
                dflash_draft_round, dflash_emit_tokens, dflash_fuse_context, dflash_inject_kv,
-               dflash_lm_head_logits, dflash_sample_rows, dflash_target_forward,
+               dflash_lm_head_logits, dflash_sample_rows, dflash_sampling_ws_bytes,
+               dflash_target_forward,
                dflash_verify_greedy, dflash_verify_rejection)
 
 
@@ -180,10 +181,11 @@ class SpecDecoder:
         q_d = torch.empty(1, B - 1, V, dtype=torch.float32, device=dev)
         hid = torch.empty(B, D, dtype=torch.float32, device=dev)
         first = torch.empty(1, dtype=torch.int32, device=dev)
+        ws_s = torch.empty(dflash_sampling_ws_bytes(B, V), dtype=torch.uint8, device=dev)
         u_first, _, _, _ = uniforms(0)
         last = taps_pre[n_t - 1, P - 1:P].float()
         dflash_lm_head_logits(self.target.handle, last, 1, g_t, z_t, self.ws_t)
-        dflash_sample_rows(self.target.handle, z_t, 1, V, T, f64([u_first]), first)
+        dflash_sample_rows(self.target.handle, z_t, 1, V, T, f64([u_first]), first, ws=ws_s)
         out = [int(first.item())]
         taps_blk = torch.empty(n_t, B, D, dtype=td, device=dev)
         pending, Tn = taps_pre, P
@@ -203,17 +205,17 @@ class SpecDecoder:
             dflash_lm_head_logits(self.draft.handle, hid, B - 1, g_d, z_d, self.ws_d,
                                   skip_first_of=B)
             dflash_sample_rows(self.draft.handle, z_d, B - 1, V, T, f64(u_draft),
-                               self.draft_ids[0, 1:], q_d[0])
+                               self.draft_ids[0, 1:], q_d[0], ws=ws_s)
             self.start.copy_(self.tkv.len[:1])
             dflash_target_forward(self.target.handle, self.draft_ids, 1, B, self.tkv.struct,
                                   taps_ids, taps_blk, self.post, self.ws_t)
             dflash_lm_head_logits(self.target.handle, taps_blk[n_t - 1].float().contiguous(), B,
                                   g_t, z_t, self.ws_t)
-            dflash_sample_rows(self.target.handle, z_t, B, V, T, None, None, p_t[0])
+            dflash_sample_rows(self.target.handle, z_t, B, V, T, None, None, p_t[0], ws=ws_s)
             dflash_verify_rejection(self.target.handle, self.draft_ids, q_d, p_t, V,
                                     f64(u_accept), f64([u_sample]), 1, B, self.start,
                                     self.accept, self.tau, self.bonus, self.out_tokens,
-                                    self.tkv.len)
+                                    self.tkv.len, ws=ws_s)
             a = int(self.accept.item())
             out.extend(int(t) for t in self.out_tokens[0, :a + 1].tolist())
             pending, Tn = taps_blk, a + 1

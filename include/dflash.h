@@ -242,16 +242,31 @@ int dflash_lm_head_logits(dflash_handle* h, const float* x, int32_t rows, const 
                           int32_t skip_first_of, float* logits, void* ws, size_t ws_bytes,
                           dflash_stream_t s);
 
+/* Bytes of device scratch dflash_sample_rows needs for rows rows of the
+ * vocabulary (and dflash_verify_rejection for batch = rows sequences):
+ * per row 16 bytes for each chunk of 2048 vocabulary entries plus 48, and
+ * 512 more.  0 for a negative rows or vocab < 1.  Host only. */
+size_t dflash_sampling_ws_bytes(int32_t rows, int32_t vocab);
+
 /* Sampling at temperature T > 0 (txtmix §8, the T = 1 setting of the
  * paper's experiments).  For each row of logits (device fp32 [rows, vocab])
  * p = softmax(logits / T); probs (nullable, device fp32 [rows, vocab])
- * receives p; ids (nullable, device int32, row r at ids[r * ids_stride])
- * receives the inverse-CDF draw with u[r] (device fp64 [rows], uniform in
- * [0, 1)): the smallest index whose running sum of p in index order exceeds
- * u[r] times the total.  At least one of ids and probs is required. */
+ * receives p; ids (nullable, device int32) receives the inverse-CDF draw
+ * with u[r] (device fp64 [rows], uniform in [0, 1)): the smallest index
+ * whose running sum of p in index order exceeds u[r] times the total.  Row r
+ * goes to ids[r]; ids_skip_first_of = k > 1 reads ids as blocks of k and
+ * fills their slots 1..k-1 in order (row r at block r / (k-1), slot
+ * 1 + r % (k-1)), so the draws of dflash_lm_head_logits(skip_first_of = B)
+ * land in draft_ids[batch, B] behind the anchors; 1 or negative is
+ * DFLASH_ERR_INVALID_ARG.  At least one of ids and probs is required; probs
+ * may be the logits buffer itself (the softmax is then taken in place).
+ * ws: device scratch of dflash_sampling_ws_bytes(rows, vocab) bytes,
+ * 256-byte aligned (DFLASH_ERR_ALIGNMENT, DFLASH_ERR_WORKSPACE otherwise);
+ * the call owns it until it completes on s. */
 int dflash_sample_rows(dflash_handle* h, const float* logits, int32_t rows, int32_t vocab,
-                       float temperature, const double* u, int32_t* ids, int32_t ids_stride,
-                       float* probs, dflash_stream_t s);
+                       float temperature, const double* u, int32_t* ids,
+                       int32_t ids_skip_first_of, float* probs, void* ws, size_t ws_bytes,
+                       dflash_stream_t s);
 
 /* Speculative sampling verification (txtmix §8: acceptance probability p/q,
  * the prefix ends at the first rejection, the token after it is drawn from
@@ -264,12 +279,15 @@ int dflash_sample_rows(dflash_handle* h, const float* logits, int32_t rows, int3
  * drafts accepted, the token after them is drawn with u_sample[b] (device
  * fp64 [batch]) from max(p[a] - q[a], 0) when d_{a+1} was rejected, from
  * p[B-1] when all were accepted.  Outputs as dflash_verify_greedy
- * (token: nullable device int32 [batch], the drawn token). */
+ * (token: nullable device int32 [batch], the drawn token).  ws: device
+ * scratch of dflash_sampling_ws_bytes(batch, vocab) bytes, 256-byte
+ * aligned. */
 int dflash_verify_rejection(dflash_handle* h, const int32_t* draft, const float* q_probs,
                             const float* p_probs, int32_t vocab, const double* u_accept,
                             const double* u_sample, int32_t batch, int32_t B,
                             const int32_t* start, int32_t* accept, int32_t* tau, int32_t* token,
-                            int32_t* out_tokens, int32_t* new_len, dflash_stream_t s);
+                            int32_t* out_tokens, int32_t* new_len, void* ws, size_t ws_bytes,
+                            dflash_stream_t s);
 
 /* Causal forward of a target model (qk_norm == 0 handle) over T new tokens
  * per sequence, appended to its cache.  tokens: device int32 [batch, T] at

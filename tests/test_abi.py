@@ -66,3 +66,19 @@ def test_strerror_and_argument_errors(dfl):
     assert lib.dflash_draft_round(None, None, 4, None, None, None, None, 1, 4, None, None, None,
                                   None, None, 0, None) == 1
     assert lib.dflash_workspace_bytes(None, 1, 16, 16) == 0
+
+
+def test_sampling_scratch_and_argument_errors(dfl):
+    """The sampling calls' scratch size (per row 16 bytes per 2048-entry
+    vocabulary chunk plus 48, and 512) and their host-side argument checks."""
+    assert dfl.dflash_sampling_ws_bytes(15, 151936) == 15 * (75 * 16 + 48) + 512
+    assert dfl.dflash_sampling_ws_bytes(1, 2048) == 16 + 48 + 512
+    assert dfl.dflash_sampling_ws_bytes(1, 2049) == 32 + 48 + 512
+    assert dfl.dflash_sampling_ws_bytes(0, 10) == 512
+    assert dfl.dflash_sampling_ws_bytes(-1, 10) == 0
+    assert dfl.dflash_sampling_ws_bytes(3, 0) == 0
+    lib = dfl._lib
+    assert lib.dflash_sample_rows(None, None, 1, 16, 1.0, None, None, 0, None, None, 0, None) == 1
+    assert lib.dflash_verify_rejection(None, None, None, None, 16, None, None, 1, 4, None, None,
+                                       None, None, None, None, None, 0, None) == 1
+    assert lib.dflash_lm_head_logits(None, None, 1, None, 0, None, None, 0, None) == 1

@@ -35,22 +35,36 @@ def _near_boundary(weights, u, a, b):
     return bool(np.any(np.abs(c[lo:hi] - t) <= BOUNDARY * c[-1]))
 
 
-@pytest.mark.parametrize("V,T", [(1024, 1.0), (151936, 1.0), (2048, 0.5), (4096, 2.0)])
-def test_sample_rows_matches_oracle(dfl, V, T):
+@pytest.mark.parametrize("V,T,skip", [(1024, 1.0, 0), (151936, 1.0, 16), (2048, 0.5, 0),
+                                      (4096, 2.0, 5)])
+def test_sample_rows_matches_oracle(dfl, V, T, skip):
+    """skip > 1: the draws land in the draft slots of [batch, skip] blocks
+    (slot 0, the anchor, untouched)."""
     _, _, m = _handle(dfl)
     rng = np.random.default_rng(V + int(10 * T))
-    rows = 24
+    rows = 24 if skip != 16 else 30
     z = (rng.standard_normal((rows, V)) * 3).astype(np.float32)
     u = rng.random(rows)
     dev = "cuda"
-    ids = torch.full((rows,), -1, dtype=torch.int32, device=dev)
+    n_ids = rows if skip < 2 else rows // (skip - 1) * skip
+    ids = torch.full((n_ids,), -1, dtype=torch.int32, device=dev)
     probs = torch.empty(rows, V, device=dev)
     dfl.dflash_sample_rows(m.handle, torch.from_numpy(z).to(dev), rows, V, T,
-                           torch.from_numpy(u).to(dev), ids, probs)
+                           torch.from_numpy(u).to(dev), ids, probs, ids_skip_first_of=skip)
     assert dfl.dflash_get_status(m.handle) == 0
     p = O.softmax_t(z, T)
     np.testing.assert_allclose(probs.cpu().numpy(), p, rtol=2e-5, atol=1e-12)
+    # in place (probs is the logits buffer): the same bits and draws
+    zin = torch.from_numpy(z).to(dev)
+    ids2 = torch.full_like(ids, -1)
+    dfl.dflash_sample_rows(m.handle, zin, rows, V, T, torch.from_numpy(u).to(dev), ids2, zin,
+                           ids_skip_first_of=skip)
+    assert torch.equal(zin, probs) and torch.equal(ids2, ids)
     got = ids.cpu().numpy()
+    if skip > 1:
+        blk = got.reshape(-1, skip)
+        assert (blk[:, 0] == -1).all()
+        got = blk[:, 1:].reshape(-1)
     want = np.array([O.sample_from(p[r], u[r]) for r in range(rows)])
     flips = [r for r in range(rows) if got[r] != want[r]]
     assert all(_near_boundary(p[r], u[r], got[r], want[r]) for r in flips), flips
@@ -195,3 +209,126 @@ def test_e2e_sampling_loop_matches_oracle(dfl):
     assert taus == rtaus
     target.close()
     draft.close()
+
+
+def _chi2_ok(counts, probs, label, alpha=1e-5):
+    """Pearson chi-squared of observed counts against n * probs: bins of zero
+    probability must stay empty, and the p-value of the rest exceed alpha."""
+    stats = pytest.importorskip("scipy.stats")
+    counts, probs = np.asarray(counts, np.float64), np.asarray(probs, np.float64)
+    n = counts.sum()
+    zero = probs == 0
+    assert counts[zero].sum() == 0, f"{label}: drew a token of zero probability"
+    e = n * probs[~zero]
+    x2 = float(((counts[~zero] - e) ** 2 / e).sum())
+    pv = float(stats.chi2.sf(x2, int((~zero).sum()) - 1))
+    print(f"{label}: n={int(n)} chi2={x2:.1f} p={pv:.3g}")
+    assert pv > alpha, label
+
+
+def _dist(rng, V, zeros):
+    w = rng.gamma(0.7, size=V)
+    w[zeros] = 0.0
+    return (w / w.sum()).astype(np.float32)
+
+
+def test_verify_rejection_is_lossless_chi2(dfl):
+    """The speculative-sampling guarantee on the GPU verifier: with draft
+    tokens drawn from q_j, the token emitted at block position j (whenever
+    the round reaches it) is distributed as the target's p_j, whatever q is.
+    p and q are fixed per position (so the target's next-token law does not
+    depend on the earlier tokens) and each has tokens of zero probability
+    the other favours.  Also the acceptance rate of the first draft equals
+    sum_x min(p_0, q_0)."""
+    _, _, m = _handle(dfl)
+    dev = "cuda"
+    rng = np.random.default_rng(2024)
+    V, B, n = 12, 4, 60000
+    p = np.stack([_dist(rng, V, [j % V, 5]) for j in range(B)])
+    q = np.stack([_dist(rng, V, [(j + 3) % V]) for j in range(B - 1)])
+    cq = np.cumsum(q.astype(np.float64), axis=1)
+    draft = np.zeros((n, B), dtype=np.int32)
+    draft[:, 0] = rng.integers(0, V, n)
+    for j in range(1, B):   # d_j drawn from q_{j-1} by inverse CDF
+        t = rng.random(n) * cq[j - 1, -1]
+        draft[:, j] = np.minimum(np.searchsorted(cq[j - 1], t, side="right"), V - 1)
+    qq = np.ascontiguousarray(np.broadcast_to(q, (n, B - 1, V)))
+    pp = np.ascontiguousarray(np.broadcast_to(p, (n, B, V)))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    u_acc, u_smp = rng.random((n, B - 1)), rng.random(n)
+    start = np.zeros(n, dtype=np.int32)
+    acc = torch.empty(n, dtype=torch.int32, device=dev)
+    out = torch.empty(n, B, dtype=torch.int32, device=dev)
+    dfl.dflash_verify_rejection(m.handle, t(draft), t(qq), t(pp), V, t(u_acc), t(u_smp), n, B,
+                                t(start), acc, None, None, out, None)
+    assert dfl.dflash_get_status(m.handle) == 0
+    out, acc = out.cpu().numpy(), acc.cpu().numpy()
+    for j in range(B):
+        col = out[:, j]
+        col = col[col >= 0]
+        assert len(col) == (acc >= j).sum()
+        _chi2_ok(np.bincount(col, minlength=V), p[j], f"position {j}")
+    r = float(np.minimum(p[0].astype(np.float64), q[0]).sum())
+    z = ((acc >= 1).mean() - r) / np.sqrt(r * (1 - r) / n)
+    print(f"first-draft acceptance {(acc >= 1).mean():.4f} vs {r:.4f} (z = {z:.2f})")
+    assert abs(z) < 5
+    m.close()
+
+
+def test_sample_rows_chi2(dfl):
+    """Draws from one row's softmax(z / T) (T = 0.7) with independent
+    uniforms follow that distribution."""
+    _, _, m = _handle(dfl)
+    dev = "cuda"
+    rng = np.random.default_rng(7)
+    V, n, T = 24, 60000, 0.7
+    z = (rng.standard_normal(V) * 1.5).astype(np.float32)
+    zz = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(z, (n, V)))).to(dev)
+    ids = torch.empty(n, dtype=torch.int32, device=dev)
+    dfl.dflash_sample_rows(m.handle, zz, n, V, T, torch.from_numpy(rng.random(n)).to(dev), ids)
+    assert dfl.dflash_get_status(m.handle) == 0
+    _chi2_ok(np.bincount(ids.cpu().numpy(), minlength=V), O.softmax_t(z, T), "softmax draws")
+    m.close()
+
+
+def test_verify_rejection_zero_residual(dfl):
+    """p_a == q_a and a draft of zero probability under both: the draft is
+    rejected (u * 0 < 0 fails), the residual max(p - q, 0) is all zero, and
+    the token is drawn from p_a itself; also a draft id out of range fails
+    its test and sets the status word."""
+    _, _, m = _handle(dfl)
+    dev = "cuda"
+    rng = np.random.default_rng(99)
+    V, B, batch = 5000, 4, 3
+    q = O.softmax_t(rng.standard_normal((batch, B - 1, V)) * 2, 1.0).astype(np.float32)
+    p = np.concatenate([q, O.softmax_t(rng.standard_normal((batch, 1, V)), 1.0)
+                        .astype(np.float32)], axis=1)
+    draft = np.zeros((batch, B), dtype=np.int32)
+    for b in range(batch):
+        for j in range(1, B):
+            draft[b, j] = O.sample_from(q[b, j - 1], rng.random())
+    for b, j in [(0, 1), (1, 2)]:   # rejection at position j-1, p == q there
+        z = int(draft[b, j])
+        q[b, j - 1, z] = p[b, j - 1, z] = 0.0
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    u_acc, u_smp = rng.random((batch, B - 1)), rng.random(batch)
+    start = np.full(batch, 7, dtype=np.int32)
+    acc = torch.empty(batch, dtype=torch.int32, device=dev)
+    tok = torch.empty(batch, dtype=torch.int32, device=dev)
+    out = torch.empty(batch, B, dtype=torch.int32, device=dev)
+    dfl.dflash_verify_rejection(m.handle, t(draft), t(q), t(p), V, t(u_acc), t(u_smp), batch, B,
+                                t(start), acc, None, tok, out, None)
+    assert dfl.dflash_get_status(m.handle) == 0
+    oa, ot, oo, _ = O.verify_rejection(draft, q.astype(np.float64), p.astype(np.float64), u_acc,
+                                       u_smp, start)
+    assert list(oa[:2]) == [0, 1] and oa[2] == B - 1
+    np.testing.assert_array_equal(acc.cpu().numpy(), oa)
+    np.testing.assert_array_equal(tok.cpu().numpy(), ot)
+    np.testing.assert_array_equal(out.cpu().numpy(), oo)
+    # an out-of-range draft id: rejected there, ST_BOUNDS reported
+    draft[2, 2] = V + 3
+    dfl.dflash_verify_rejection(m.handle, t(draft), t(q), t(p), V, t(u_acc), t(u_smp), batch, B,
+                                t(start), acc, None, tok, out, None)
+    assert acc.cpu().numpy()[2] == 1
+    assert dfl.dflash_get_status(m.handle) == 8   # DFLASH_ERR_DEVICE_BOUNDS
+    m.close()
