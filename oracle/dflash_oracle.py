@@ -11,7 +11,8 @@ Pages cited (by title and section):
   [reading]   txtmix "DFlash：把扩散模型关进草稿阶段…" source reading, §5 target
               feature KV injection, §6 one-step denoising, §8 losslessness
               from the verification rule, §9 one request through the system,
-              §11 dflash_config fields.
+              §11 dflash_config fields, §13-§14 DFlash 2 (the candidate
+              selector).
 
 Arithmetic: every dot product and reduction in fp64.  Values are then
 rounded at the "storage points" where the GPU path stores a tensor, using
@@ -45,6 +46,13 @@ What pins each function (tests/test_oracle_*.py):
                            one-hot p and q reduce to verify_greedy
                            (exhaustive on tiny B and V)
   speculative_sample_generate  T -> 0 limit equals the greedy loop
+  topk_lowest              brute force by repeated argmax on tiny rows with
+                           planted ties
+  select_candidates        k = 1 and a zero codebook reduce the walk to the
+                           argmax; a planted bigram chain (pair term on the
+                           predecessor's and successor's own codebooks) is
+                           followed from the anchor; relabelling the
+                           vocabulary relabels the path
 """
 from __future__ import annotations
 
@@ -60,7 +68,7 @@ __all__ = [
     "argmax_lowest", "top2_gap", "verify_greedy", "expected_tau_from_prefix",
     "TargetCache", "target_forward", "ar_generate", "speculative_generate",
     "softmax_t", "sample_from", "verify_rejection", "acceptance_probability",
-    "speculative_sample_generate",
+    "speculative_sample_generate", "topk_lowest", "select_candidates",
 ]
 
 
@@ -442,6 +450,56 @@ def verify_rejection(draft: np.ndarray, q: np.ndarray, p: np.ndarray,
 def acceptance_probability(p: np.ndarray, q: np.ndarray) -> float:
     """P(a draft drawn from q is accepted against p) = sum_x min(p(x), q(x))."""
     return float(np.minimum(np.asarray(p, np.float64), np.asarray(q, np.float64)).sum())
+
+
+# ---------------------------------------------------------------------------
+# DFlash 2 candidate selection  ([reading] §13, §14)
+# ---------------------------------------------------------------------------
+def topk_lowest(z: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest values of each row of z, ordered by value
+    (descending) and, among equal values, by index (ascending)."""
+    z = np.asarray(z)
+    out = np.empty(z.shape[:-1] + (k,), dtype=np.int32)
+    for idx in np.ndindex(*z.shape[:-1]):
+        row = z[idx]
+        order = np.lexsort((np.arange(row.shape[0]), -row))
+        out[idx] = order[:k]
+    return out
+
+
+def select_candidates(logits: np.ndarray, hidden: np.ndarray, anchor: int,
+                      W_h: np.ndarray, code_pred: np.ndarray, code_succ: np.ndarray,
+                      top_k: int):
+    """The DFlash 2 candidate selector on one block, greedy.
+
+    logits: [n, V], the draft's logits at block positions 1..n (the anchor
+    makes none); hidden: [n, D], the final-normed rows that produced them.
+    Each position keeps its top_k tokens (topk_lowest) with their logits as
+    unary scores U_t.  The context gate is H_t = W_h hidden_t (W_h [r, D],
+    no bias).  Starting from the anchor, the walk scores every candidate b
+    of position t after the chosen predecessor a as
+        S_t(a, b) = U_t(b) + sum_r code_pred[a, r] * H_t[r] * code_succ[b, r]
+    and keeps the best (the earlier candidate on a tie); the kept token is
+    the next predecessor.  Returns (path [n], candidates [n, top_k],
+    chosen scores [n])."""
+    logits = np.asarray(logits, np.float64)
+    n = logits.shape[0]
+    cand = topk_lowest(logits, top_k)
+    unary = np.take_along_axis(logits, cand, axis=-1)
+    H = np.asarray(hidden, np.float64) @ np.asarray(W_h, np.float64).T
+    A = np.asarray(code_pred, np.float64)
+    Bc = np.asarray(code_succ, np.float64)
+    path = np.zeros(n, dtype=np.int32)
+    best = np.zeros(n)
+    pred = int(anchor)
+    for t in range(n):
+        gate = A[pred] * H[t]
+        scores = unary[t] + Bc[cand[t]] @ gate
+        j = int(np.argmax(scores))
+        path[t] = cand[t, j]
+        best[t] = scores[j]
+        pred = int(path[t])
+    return path, cand, best
 
 
 # ---------------------------------------------------------------------------
