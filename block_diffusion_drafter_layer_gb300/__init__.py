@@ -89,6 +89,10 @@ _sig = {
     "dflash_verify_rejection": (C.c_int, [_P, _P, _P, _P, C.c_int32, _P, _P, C.c_int32,
                                           C.c_int32, _P, _P, _P, _P, _P, _P, _P, C.c_size_t,
                                           _P]),
+    "dflash_select_ws_bytes": (C.c_size_t, [_P, C.c_int32, C.c_int32, C.c_int32, C.c_int32]),
+    "dflash_select_candidates": (C.c_int, [_P, _P, _P, _P, _P, C.c_int32, C.c_int32, C.c_int32,
+                                           _P, C.c_int32, _P, _P, C.c_int32, _P, _P, _P, _P,
+                                           C.c_size_t, _P]),
     "dflash_target_forward": (C.c_int, [_P, _P, C.c_int32, C.c_int32, C.POINTER(dflash_kv),
                                         C.POINTER(C.c_int32), C.c_int32, _P, _P, _P, C.c_size_t,
                                         _P]),
@@ -254,6 +258,29 @@ def dflash_verify_rejection(h: int, draft: torch.Tensor, q_probs: torch.Tensor,
                                         _ptr(accept), _ptr(tau), _ptr(token), _ptr(out_tokens),
                                         _ptr(new_len), _ptr(ws), ws.numel() * ws.element_size(),
                                         _stream(stream)), "dflash_verify_rejection")
+
+
+def dflash_select_ws_bytes(h: int, batch: int, B: int, top_k: int, rank: int) -> int:
+    return int(_lib.dflash_select_ws_bytes(h, batch, B, top_k, rank))
+
+
+def dflash_select_candidates(h: int, logits: torch.Tensor, hidden: torch.Tensor,
+                             norm_gain: torch.Tensor, anchor: torch.Tensor, batch: int, B: int,
+                             top_k: int, w_h: torch.Tensor, code_pred: torch.Tensor,
+                             code_succ: torch.Tensor, draft_ids: torch.Tensor,
+                             candidates: Optional[torch.Tensor] = None,
+                             scores: Optional[torch.Tensor] = None,
+                             ws: Optional[torch.Tensor] = None, stream=None):
+    rank, n_codes = int(w_h.shape[0]), int(code_pred.shape[0])
+    if ws is None:   # scratch from torch's caching allocator
+        ws = torch.empty(dflash_select_ws_bytes(h, batch, B, top_k, rank), dtype=torch.uint8,
+                         device=logits.device)
+    _check(_lib.dflash_select_candidates(h, _ptr(logits), _ptr(hidden), _ptr(norm_gain),
+                                         _ptr(anchor), batch, B, top_k, _ptr(w_h), rank,
+                                         _ptr(code_pred), _ptr(code_succ), n_codes,
+                                         _ptr(draft_ids), _ptr(candidates), _ptr(scores),
+                                         _ptr(ws), ws.numel() * ws.element_size(),
+                                         _stream(stream)), "dflash_select_candidates")
 
 
 def dflash_verify_greedy(draft: torch.Tensor, post: torch.Tensor, batch: int, B: int,

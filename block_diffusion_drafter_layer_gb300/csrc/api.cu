@@ -950,8 +950,8 @@ int dflash_draft_round(dflash_handle* h, const void* const* hidden, int32_t n_ro
   if (n_rows == 0)
     return dflash_draft_block(h, anchor, batch, B, kv, draft_ids, top2_gap, hidden_out, ws,
                               ws_bytes, st);
-  if (!hidden || !seq_row0 || !seq_rows || !h_t_out || !anchor || !draft_ids || !ws ||
-      batch < 1 || B < 1)
+  if (!hidden || !seq_row0 || !seq_rows || !h_t_out || !anchor || (!draft_ids && !hidden_out) ||
+      !ws || batch < 1 || B < 1)
     return DFLASH_ERR_INVALID_ARG;
   if (!kv_ok(h, kv, batch)) return DFLASH_ERR_INVALID_ARG;
   const dflash_config& c = h->cfg;
@@ -980,7 +980,7 @@ int dflash_draft_round(dflash_handle* h, const void* const* hidden, int32_t n_ro
     if (hidden_out &&
         cudaMemcpyAsync(hidden_out, f.x, R * c.hidden * sizeof(float), cudaMemcpyDeviceToDevice, s))
       return DFLASH_ERR_CUDA;
-    if (B == 1 &&
+    if (B == 1 && draft_ids &&
         cudaMemcpyAsync(draft_ids, anchor, batch * sizeof(int32_t), cudaMemcpyDeviceToDevice, s))
       return DFLASH_ERR_CUDA;
     return DFLASH_OK;
@@ -1069,6 +1069,32 @@ int dflash_verify_rejection(dflash_handle* h, const int32_t* draft, const float*
   if (ws_bytes < sampling_ws_bytes(batch, vocab)) return DFLASH_ERR_WORKSPACE;
   return verify_rejection(h, (cudaStream_t)st, draft, q_probs, p_probs, vocab, u_accept, u_sample,
                           batch, B, start, accept, tau, token, out_tokens, new_len, ws);
+}
+
+size_t dflash_select_ws_bytes(const dflash_handle* h, int32_t batch, int32_t B, int32_t top_k,
+                              int32_t rank) {
+  if (!h || batch < 1 || B < 2 || top_k < 1 || rank < 1) return 0;
+  return select_ws_bytes(batch, B, h->cfg.vocab, h->cfg.hidden, top_k, rank);
+}
+
+int dflash_select_candidates(dflash_handle* h, const float* logits, const float* hidden,
+                             const float* norm_gain, const int32_t* anchor, int32_t batch,
+                             int32_t B, int32_t top_k, const void* w_h, int32_t rank,
+                             const void* code_pred, const void* code_succ, int32_t n_codes,
+                             int32_t* draft_ids, int32_t* candidates, float* scores, void* ws,
+                             size_t ws_bytes, dflash_stream_t st) {
+  if (!h || !logits || !hidden || !norm_gain || !anchor || !w_h || !code_pred || !code_succ ||
+      !draft_ids || !ws || batch < 1 || n_codes < h->cfg.vocab ||
+      !select_shape_ok(B, h->cfg.vocab, h->cfg.hidden, top_k, rank))
+    return DFLASH_ERR_INVALID_ARG;
+  if (((uintptr_t)ws & 255) != 0 || !aligned16(hidden) || !aligned16(norm_gain) ||
+      !aligned16(w_h))
+    return DFLASH_ERR_ALIGNMENT;
+  if (ws_bytes < select_ws_bytes(batch, B, h->cfg.vocab, h->cfg.hidden, top_k, rank))
+    return DFLASH_ERR_WORKSPACE;
+  return select_candidates(h, (cudaStream_t)st, logits, hidden, norm_gain, anchor, batch, B, top_k,
+                           w_h, rank, code_pred, code_succ, n_codes, draft_ids, candidates,
+                           scores, ws);
 }
 
 int dflash_target_forward(dflash_handle* h, const int32_t* tokens, int32_t batch, int32_t T,

@@ -317,5 +317,12 @@ int verify_rejection(dflash_handle* h, cudaStream_t s, const int32_t* draft, con
                      const float* p, int V, const double* u_acc, const double* u_smp, int batch,
                      int B, const int32_t* start, int32_t* accept, int32_t* tau, int32_t* token,
                      int32_t* out_tokens, int32_t* new_len, void* ws);
+size_t select_ws_bytes(int batch, int B, int V, int D, int K, int rank);
+bool select_shape_ok(int B, int V, int D, int K, int rank);
+int select_candidates(dflash_handle* h, cudaStream_t s, const float* logits, const float* x,
+                      const float* gain, const int32_t* anchor, int batch, int B, int K,
+                      const void* w_h, int rank, const void* code_pred, const void* code_succ,
+                      int n_codes, int32_t* draft_ids, int32_t* cand_out, float* scores,
+                      void* ws);
 
 }  // namespace dflash

@@ -68,6 +68,7 @@ enum dflash_dtype { DFLASH_F32 = 0, DFLASH_BF16 = 1 };
 
 #define DFLASH_MAX_LAYERS 16
 #define DFLASH_MAX_PICK 8
+#define DFLASH_SEL_KMAX 16   /* candidates per position of dflash_select_candidates */
 
 /* Model shape.  One struct serves the draft (qk_norm = 1, bidirectional
  * block) and the small causal target used by the end-to-end loop
@@ -193,7 +194,9 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
  * dflash_draft_block over the grown caches.  The result equals the three
  * calls in that order.  Blocks of at most 16 rows with at most 16 pending
  * rows (bf16, head dim 128) run as one persistent launch; other shapes run
- * the three calls.  n_rows == 0 skips fusion and injection. */
+ * the three calls.  n_rows == 0 skips fusion and injection.  draft_ids may
+ * be NULL when hidden_out is given, as for dflash_draft_block (a round that
+ * samples or selects its drafts from the residual). */
 int dflash_draft_round(dflash_handle* h, const void* const* hidden, int32_t n_rows,
                        const int32_t* seq_row0, const int32_t* seq_rows, void* h_t_out,
                        const int32_t* anchor, int32_t batch, int32_t B, const dflash_kv* kv,
@@ -288,6 +291,38 @@ int dflash_verify_rejection(dflash_handle* h, const int32_t* draft, const float*
                             const int32_t* start, int32_t* accept, int32_t* tau, int32_t* token,
                             int32_t* out_tokens, int32_t* new_len, void* ws, size_t ws_bytes,
                             dflash_stream_t s);
+
+/* DFlash 2 candidate selection, greedy (txtmix §13-§14: top-k candidates
+ * per draft position, an adjacent-pair score, a greedy walk from the
+ * anchor).  Rows are block positions 1..B-1 of each sequence.
+ *   logits:    device fp32 [batch*(B-1), vocab], the draft's LM-head logits
+ *              (dflash_lm_head_logits with skip_first_of = B).
+ *   hidden:    device fp32 [batch*B, D], the residual stream after the last
+ *              layer (dflash_draft_block's hidden_out); rows 1..B-1 of each
+ *              block pass the final RMSNorm with norm_gain (device fp32 [D]).
+ *   Each position t keeps its top_k tokens (largest logit first, the lower
+ *   id first among equal logits) with unary score U_t = their logit.  The
+ *   context gate is H_t = W_h xhat_t (w_h: device [rank, D], handle dtype,
+ *   no bias).  From a = anchor[b] the walk takes, at every position, the
+ *   candidate c maximising U_t(c) + sum_r code_pred[a, r] H_t[r]
+ *   code_succ[c, r] (the earlier candidate on a tie) and continues from it.
+ *   code_pred, code_succ: device [n_codes, rank] (handle dtype), n_codes >=
+ *   vocab.  1 <= top_k <= DFLASH_SEL_KMAX and top_k <= vocab; rank a positive
+ *   multiple of 32.
+ *   draft_ids: device int32 [batch, B] = [anchor, path].  candidates
+ *   (nullable): device int32 [batch*(B-1), top_k] in that order.  scores
+ *   (nullable): device fp32 [batch*(B-1)], the chosen pair scores.
+ *   ws: device scratch of dflash_select_ws_bytes(h, batch, B, top_k, rank)
+ *   bytes, 256-byte aligned.  An anchor id outside [0, n_codes) reads code
+ *   row 0 and sets DFLASH_ERR_DEVICE_BOUNDS. */
+size_t dflash_select_ws_bytes(const dflash_handle* h, int32_t batch, int32_t B, int32_t top_k,
+                              int32_t rank);
+int dflash_select_candidates(dflash_handle* h, const float* logits, const float* hidden,
+                             const float* norm_gain, const int32_t* anchor, int32_t batch,
+                             int32_t B, int32_t top_k, const void* w_h, int32_t rank,
+                             const void* code_pred, const void* code_succ, int32_t n_codes,
+                             int32_t* draft_ids, int32_t* candidates, float* scores, void* ws,
+                             size_t ws_bytes, dflash_stream_t s);
 
 /* Causal forward of a target model (qk_norm == 0 handle) over T new tokens
  * per sequence, appended to its cache.  tokens: device int32 [batch, T] at

@@ -268,3 +268,17 @@ def round_uniforms(seed: int, B: int):
         g = np.random.default_rng([seed, r])
         return (float(g.random()), g.random(B - 1), g.random(B - 1), float(g.random()))
     return draws
+
+
+def selector_weights(D: int, V: int, dtype: str, seed: int, rank: int = 256,
+                     device="cpu") -> dict:
+    """Random-init weights of a DFlash 2 candidate selector: the context-gate
+    projection w_h [rank, D] with N(0, 1/D) entries (unit-scale gates from
+    unit-RMS rows) and two codebooks [V, rank] with N(0, rank^-1/2) entries,
+    so that a pair term summed over the rank has unit scale, comparable to
+    the draft logits' gaps."""
+    td = torch_dtype(dtype)
+    g = _gen(seed, device)
+    return {"w_h": _normal((rank, D), D ** -0.5, g, device, td),
+            "code_pred": _normal((V, rank), rank ** -0.25, g, device, td),
+            "code_succ": _normal((V, rank), rank ** -0.25, g, device, td)}
