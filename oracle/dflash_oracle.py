@@ -29,6 +29,11 @@ What pins each function (tests/test_oracle_*.py):
                            invariance, identity at position 0, norm kept
   attention                torch scaled_dot_product_attention (fp64) with
                            grouped K/V heads, uniform-score closed form
+  draft_key_visible        causal window of one: each row's own value
+                           exactly; causal rows ignore later rows; a window
+                           ignores older context; the anchor's causal output
+                           equals full attention over explicitly sliced keys;
+                           a window covering all keys changes nothing
   draft_layer/draft_block  reductions: zero W_o and W_d give the identity;
                            zero W_q gives uniform attention (closed form);
                            context enters only through K/V
@@ -68,7 +73,7 @@ __all__ = [
     "argmax_lowest", "top2_gap", "verify_greedy", "expected_tau_from_prefix",
     "TargetCache", "target_forward", "ar_generate", "speculative_generate",
     "softmax_t", "sample_from", "verify_rejection", "acceptance_probability",
-    "speculative_sample_generate", "topk_lowest", "select_candidates",
+    "speculative_sample_generate", "topk_lowest", "select_candidates", "draft_key_visible",
 ]
 
 
@@ -248,16 +253,34 @@ def embed_block(embed: np.ndarray, anchor: int, mask_id: int, B: int,
     return f32(np.asarray(embed[ids], dtype=np.float64) * scale)
 
 
+def draft_key_visible(L: int, B: int, causal: bool, window: int) -> np.ndarray:
+    """Which keys each block row sees in a draft layer ([reading] §6: a
+    sliding_attention layer is causal unless configured otherwise, and its
+    visible range is cut to the sliding window; a full_attention layer is
+    bidirectional).  Keys are [context ; block] at positions 0 .. L+B-1,
+    block row i at position p = L + i.  A causal row sees keys at or before
+    p; a window of W keeps keys after p - W.  Returns [B, L + B] bool."""
+    p = np.arange(L, L + B)[:, None]
+    j = np.arange(L + B)[None, :]
+    vis = np.ones((B, L + B), dtype=bool)
+    if causal:
+        vis &= j <= p
+    if window > 0:
+        vis &= j > p - window
+    return vis
+
+
 def draft_layer(x: np.ndarray, layer: dict, ctx_K: np.ndarray, ctx_V: np.ndarray,
                 pos: np.ndarray, H: int, G: int, d: int, theta: float, eps: float,
-                store=f32) -> np.ndarray:
+                store=f32, mask: Optional[np.ndarray] = None) -> np.ndarray:
     """One Qwen3-style draft decoder layer over one sequence's block.
 
     x: [B, D] fp32 residual.  ctx_K, ctx_V: [L, G, d] injected context.
     Queries come from the block only; keys/values are [context ; block]
     concatenated along the sequence ([tutorial] §2.1.2; [reading] §5);
-    attention is bidirectional (no mask).  Then o_proj + residual and a
-    SwiGLU FFN + residual, each sublayer pre-normalised."""
+    attention is bidirectional unless ``mask`` (draft_key_visible) says
+    otherwise.  Then o_proj + residual and a SwiGLU FFN + residual, each
+    sublayer pre-normalised."""
     B = x.shape[0]
     h = store(rmsnorm(x, layer["g_in"], eps))
     q = linear(h, layer["wq"]).reshape(B, H, d)
@@ -268,7 +291,7 @@ def draft_layer(x: np.ndarray, layer: dict, ctx_K: np.ndarray, ctx_V: np.ndarray
     v = store(v)
     K = np.concatenate([ctx_K, k], axis=0)
     Vv = np.concatenate([ctx_V, v], axis=0)
-    o = store(attention(q, K, Vv).reshape(B, H * d))
+    o = store(attention(q, K, Vv, mask).reshape(B, H * d))
     x = f32(x + linear(o, layer["wo"]))
     h2 = store(rmsnorm(x, layer["g_post"], eps))
     a = store(silu(linear(h2, layer["wg"])) * linear(h2, layer["wu"]))
@@ -302,6 +325,9 @@ def draft_block(shape, W: dict, ctx_K: List[List[np.ndarray]],
     layer l, sequence b.  The block [anchor, mask x (B-1)] sits at positions
     L_b .. L_b + B - 1 ([reading] §9: positions run from start - ctx_len).
     Every row goes through every layer (the anchor's K/V feed the others);
+    layer l is causal when bit l of shape.causal_layers is set and keeps a
+    window of shape.sliding_window keys when bit l of shape.window_layers is
+    (draft_key_visible; both default to none: bidirectional layers);
     the final RMSNorm and the shared LM head run on rows 1..B-1 only, and
     each draft id is the argmax of its fp32 logits ([reading] §6, §14).
 
@@ -318,8 +344,12 @@ def draft_block(shape, W: dict, ctx_K: List[List[np.ndarray]],
         pos = np.arange(L, L + B)
         x = embed_block(W["embed"], anchors[b], shape.mask_id, B, shape.embed_scale)
         for l, layer in enumerate(W["layers"]):
+            causal = bool((getattr(shape, "causal_layers", 0) >> l) & 1)
+            window = (getattr(shape, "sliding_window", 0)
+                      if (getattr(shape, "window_layers", 0) >> l) & 1 else 0)
+            mask = draft_key_visible(L, B, causal, window) if causal or window else None
             x = draft_layer(x, layer, ctx_K[l][b], ctx_V[l][b], pos, shape.H,
-                            shape.G, shape.d, shape.rope_theta, shape.eps, store)
+                            shape.G, shape.d, shape.rope_theta, shape.eps, store, mask)
         hidden.append(x)
         ids[b, 0] = anchors[b]
         if not lm_head:

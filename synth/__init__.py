@@ -41,6 +41,9 @@ class DraftShape:
     rope_theta: float = 1e6
     eps: float = 1e-6
     embed_scale: float = 1.0
+    causal_layers: int = 0    # bit l: layer l is causal (a sliding_attention layer)
+    window_layers: int = 0    # bit l: layer l keeps sliding_window keys
+    sliding_window: int = 0
 
 
 @dataclass(frozen=True)
