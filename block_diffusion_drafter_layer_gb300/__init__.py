@@ -44,7 +44,9 @@ class dflash_config(C.Structure):
                 ("n_layers", C.c_int32), ("n_target_layers", C.c_int32), ("n_pick", C.c_int32),
                 ("target_layer_ids", C.c_int32 * MAX_PICK), ("mask_token_id", C.c_int32),
                 ("max_pos", C.c_int32), ("qk_norm", C.c_int32), ("dtype", C.c_int32),
-                ("rope_theta", C.c_float), ("rms_eps", C.c_float), ("embed_scale", C.c_float)]
+                ("rope_theta", C.c_float), ("rms_eps", C.c_float), ("embed_scale", C.c_float),
+                ("causal_layers", C.c_int32), ("window_layers", C.c_int32),
+                ("sliding_window", C.c_int32)]
 
 
 class dflash_layer_weights(C.Structure):
@@ -376,7 +378,7 @@ class Model:
     def __init__(self, *, D, H, G, d, F, V, n_layers, dtype: str, weights: dict, max_pos: int,
                  qk_norm: bool, mask_id: int = 0, n_target_layers: int = 0, n_pick: int = 5,
                  target_layer_ids: Sequence[int] = (), rope_theta=1e6, eps=1e-6,
-                 embed_scale=1.0):
+                 embed_scale=1.0, causal_layers=0, window_layers=0, sliding_window=0):
         cfg = dflash_config()
         cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim = D, H, G, d
         cfg.ffn, cfg.vocab, cfg.n_layers = F, V, n_layers
@@ -386,6 +388,8 @@ class Model:
         cfg.mask_token_id, cfg.max_pos, cfg.qk_norm = mask_id, max_pos, 1 if qk_norm else 0
         cfg.dtype = BF16 if dtype == "bf16" else F32
         cfg.rope_theta, cfg.rms_eps, cfg.embed_scale = rope_theta, eps, embed_scale
+        cfg.causal_layers, cfg.window_layers = causal_layers, window_layers
+        cfg.sliding_window = sliding_window
         w = dflash_weights()
         w.wc, w.g_c = _ptr(weights.get("wc")), _ptr(weights.get("g_c"))
         w.g_f = _ptr(weights.get("g_f", weights.get("g_final")))

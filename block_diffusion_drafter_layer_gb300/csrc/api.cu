@@ -46,6 +46,13 @@ int launch_end(dflash_handle* h, cudaStream_t s, Timer* t) {
   return e == cudaSuccess ? DFLASH_OK : DFLASH_ERR_CUDA;
 }
 
+// A draft layer's mask (txtmix §6): causal rows, and the window of keys
+// (0: none).
+static int layer_causal(const dflash_config& c, int l) { return (c.causal_layers >> l) & 1; }
+static int layer_window(const dflash_config& c, int l) {
+  return ((c.window_layers >> l) & 1) ? c.sliding_window : 0;
+}
+
 static size_t esize(int dtype) { return dtype == DFLASH_BF16 ? 2 : 4; }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -573,6 +580,10 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
       c.max_pos <= 0 || c.mask_token_id < 0 || c.mask_token_id >= c.vocab || !(c.rms_eps > 0.f))
     return DFLASH_ERR_SHAPE;
   if (!w->embed || !w->lm_head || !w->g_f) return DFLASH_ERR_INVALID_ARG;
+  if (c.causal_layers < 0 || c.window_layers < 0 || c.sliding_window < 0 ||
+      (c.window_layers != 0 && c.sliding_window < 1) ||
+      ((c.causal_layers | c.window_layers) >> c.n_layers) != 0)
+    return DFLASH_ERR_SHAPE;
   const void* al[] = {w->embed, w->lm_head, w->wc};
   for (const void* p : al)
     if (p && !aligned16(p)) return DFLASH_ERR_ALIGNMENT;
@@ -893,7 +904,7 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
     if (tcore) {
       if ((rc = qkv_tc(h, s, l, f, R, rm, kv->len))) return rc;
       if ((rc = attention_fast(h, s, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch,
-                               B, f.o, f.attn)))
+                               B, f.o, f.attn, layer_causal(c, l), layer_window(c, l))))
         return rc;
       if ((rc = mlp_tc(h, s, l, f, R))) return rc;
       continue;
@@ -902,10 +913,10 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
       if ((rc = qkv_stream(h, s, l, f, R, rm, kv->len))) return rc;
       if (attn_fast_ok(h, B))
         rc = attention_fast(h, s, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch, B,
-                            f.o, f.attn);
+                            f.o, f.attn, layer_causal(c, l), layer_window(c, l));
       else
         rc = attention(h, s, dt, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch, B,
-                       H, G, d, false, f.o);
+                       H, G, d, false, f.o, layer_causal(c, l), layer_window(c, l));
       if (rc) return rc;
       if ((rc = mlp_stream(h, s, l, f, R))) return rc;
       continue;
@@ -924,7 +935,7 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
                              0)))
       return rc;
     if ((rc = attention(h, s, dt, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch, B,
-                        H, G, d, false, f.o)))
+                        H, G, d, false, f.o, layer_causal(c, l), layer_window(c, l))))
       return rc;
     if ((rc = mlp_tail(h, s, L, f, R))) return rc;
   }

@@ -235,7 +235,7 @@ int attn_plan(dflash_handle* h, cudaStream_t s, const int32_t* len, int cap, int
 bool attn_fast_ok(const dflash_handle* h, int B);
 int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* kc, const void* vc,
                    int cap, const int32_t* len, const void* kb, const void* vb, int batch, int B,
-                   void* o, float* scratch);
+                   void* o, float* scratch, int causal, int window);
 
 // ---- persistent draft block for at most 16 rows (k_chain.cu) ----------------
 struct ChainArgs {
@@ -299,7 +299,8 @@ int advance_len(dflash_handle* h, cudaStream_t s, int32_t* len, const int32_t* n
 // Attention of block rows over [cache(0..len) ; block] (draft) or cache(0..pos) (causal target).
 int attention(dflash_handle* h, cudaStream_t s, int dtype, const void* q, const void* kc,
               const void* vc, int cap, const int32_t* len, const void* kb, const void* vb,
-              int batch, int rows_per_seq, int H, int G, int d, bool causal_in_cache, void* o);
+              int batch, int rows_per_seq, int H, int G, int d, bool causal_in_cache, void* o,
+              int causal = 0, int window = 0);
 int argmax_rows(dflash_handle* h, cudaStream_t s, const float* logits, int64_t rows, int V,
                 int32_t* ids, float* gap, int rows_per_seq_out, const int32_t* anchor);
 int verify_greedy(cudaStream_t s, const int32_t* draft, const int32_t* post, int batch, int B,

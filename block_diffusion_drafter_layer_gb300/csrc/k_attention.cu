@@ -53,6 +53,7 @@ struct AttnParams {
   const int32_t* len;  // [batch]
   int cap, B, H, G, rep, qgroups, units;
   float scale_log2;    // log2(e) / sqrt(d)
+  int causal, window;  // the layer's mask: causal rows, a window of keys (0: none)
   const int* n_items;  // number of items (written by the plan)
   const AttnItem* items;
   const int* unit_begin;   // [units + 1] first item of each unit
@@ -214,6 +215,16 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
     const int q0 = qg * 64;
     const int qrows = min(64, QM - q0);
     const int k_begin = item.k0, k_end = item.k1;
+    // this thread's two query rows (tile rows warp * 16 + gq and + 8; block
+    // row i at position L + i): keys [klo, khi) visible
+    int klo[2], khi[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int qr = q0 + warp * 16 + gq + 8 * h;
+      const int pq = L + (qr < QM ? qr % p.B : 0);
+      klo[h] = p.window > 0 ? max(0, pq - p.window + 1) : 0;
+      khi[h] = p.causal ? pq + 1 : k_end;
+    }
 
     // ---- Q tile: row r = query (q0 + r) = head hh of the group, block row i
     for (int e = tid; e < 64 * CH; e += AT_THREADS) {
@@ -304,7 +315,8 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int key = kbase + j * 8 + 2 * tg + (q & 1);
-            s[j][q] = (key < k_end) ? s[j][q] * p.scale_log2 : -INFINITY;
+            const bool vis = key < k_end && key >= klo[q >> 1] && key < khi[q >> 1];
+            s[j][q] = vis ? s[j][q] * p.scale_log2 : -INFINITY;
             mnew[q >> 1] = fmaxf(mnew[q >> 1], s[j][q]);
           }
 #pragma unroll
@@ -319,7 +331,8 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
         for (int j = 0; j < 8; ++j)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float e = exp2f(s[j][q] - mnew[q >> 1]);
+            // a row may see no key of this item yet (masked layers): weight 0
+            const float e = mnew[q >> 1] == -INFINITY ? 0.f : exp2f(s[j][q] - mnew[q >> 1]);
             s[j][q] = e;
             lsum[q >> 1] += e;
           }
@@ -483,7 +496,7 @@ int attn_plan(dflash_handle* h, cudaStream_t s, const int32_t* len, int cap, int
 
 int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* kc, const void* vc,
                    int cap, const int32_t* len, const void* kb, const void* vb, int batch, int B,
-                   void* o, float* scratch) {
+                   void* o, float* scratch, int causal, int window) {
   const dflash_config& c = h->cfg;
   constexpr int DH = 128;
   const int units = attn_units(h, batch, B);
@@ -499,6 +512,7 @@ int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* 
   p.len = len;
   p.cap = cap;
   p.B = B;
+  p.causal = causal, p.window = window;
   p.H = c.n_heads;
   p.G = c.n_kv_heads;
   p.rep = c.n_heads / c.n_kv_heads;

@@ -152,6 +152,7 @@ struct ChainParams {
   int pre, n_in, n_pick, kv_batch;   // round phases (0 or kRoundPhases), pending rows, sources, cache batch
   int grid, n_phases, n_items_max;
   float eps, embed_scale, scale_log2;
+  int causal_layers, window_layers, window;   // draft layer types (bit l: layer l)
 };
 static_assert(sizeof(ChainParams) <= 4096, "kernel parameters must fit the 4 KB limit");
 
@@ -1068,7 +1069,8 @@ __device__ __forceinline__ ItemGeo item_geo(const ChainParams& P, const Items* i
   return q;
 }
 
-__device__ void attention_phase(const ChainParams& P, int phase, int l, const Items* it, uint8_t* smem) {
+__device__ void attention_phase(const ChainParams& P, int phase, int l, const Items* it, uint8_t* smem,
+                                const int* rowpos) {
   const int tid = threadIdx.x - 32, warp = tid >> 5, lane = threadIdx.x & 31;
   const uint32_t sQ = smem_u32(smem + CH_OFF_ATT);
   const uint32_t sK0 = sQ + CH_ATT_Q, sV0 = sK0 + 2 * CH_ATT_KV;
@@ -1080,6 +1082,9 @@ __device__ void attention_phase(const ChainParams& P, int phase, int l, const It
     const ItemGeo ig = item_geo(P, it, j);
     const int b = ig.b, g = ig.g, L = ig.L, k_begin = ig.k_begin, k_end = ig.k_end;
     const int nsub = (k_end - k_begin + CH_AK - 1) / CH_AK;
+    // a causal or windowed layer (CTA-uniform): each query row sees keys
+    // [klo, khi) only; the other layers run the unmasked code as it is
+    const bool masked = ((P.causal_layers | P.window_layers) >> l) & 1;
     const bf16* kcb = P.kc[l] + ((int64_t)b * P.G + g) * P.cap * CH_DH;
     const bf16* vcb = P.vc[l] + ((int64_t)b * P.G + g) * P.cap * CH_DH;
     const bf16* kbb = P.kb + (int64_t)b * P.B * P.Gd + (int64_t)g * CH_DH;
@@ -1148,14 +1153,39 @@ __device__ void attention_phase(const ChainParams& P, int phase, int l, const It
           }
         }
         float mnew[2] = {mrow[0], mrow[1]};
+        if (!masked) {
 #pragma unroll
-        for (int n = 0; n < 4; ++n)
+          for (int n = 0; n < 4; ++n)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int key = kbase + n * 8 + 2 * tg + (q & 1);
-            s[n][q] = key < k_end ? s[n][q] * P.scale_log2 : -INFINITY;
-            mnew[q >> 1] = fmaxf(mnew[q >> 1], s[n][q]);
+            for (int q = 0; q < 4; ++q) {
+              const int key = kbase + n * 8 + 2 * tg + (q & 1);
+              s[n][q] = key < k_end ? s[n][q] * P.scale_log2 : -INFINITY;
+              mnew[q >> 1] = fmaxf(mnew[q >> 1], s[n][q]);
+            }
+        } else {
+          // this thread's rows r (= hh * B + i) and r + 8: block row i at
+          // position rowpos; causal keeps keys up to it, a window of W the
+          // last W positions
+          const int win = ((P.window_layers >> l) & 1) ? P.window : 0;
+          const bool causal = (P.causal_layers >> l) & 1;
+          int klo[2], khi[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int r = warp * 16 + gq + 8 * h;
+            const int pq = rowpos[2 * (b * P.B + (r < QM ? r % P.B : 0)) + 1];
+            klo[h] = win > 0 ? max(0, pq - win + 1) : 0;
+            khi[h] = causal ? pq + 1 : k_end;
           }
+#pragma unroll
+          for (int n = 0; n < 4; ++n)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int key = kbase + n * 8 + 2 * tg + (q & 1);
+              const bool vis = key < k_end && key >= klo[q >> 1] && key < khi[q >> 1];
+              s[n][q] = vis ? s[n][q] * P.scale_log2 : -INFINITY;
+              mnew[q >> 1] = fmaxf(mnew[q >> 1], s[n][q]);
+            }
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           mnew[h] = fmaxf(mnew[h], __shfl_xor_sync(0xffffffffu, mnew[h], 1));
@@ -1168,7 +1198,8 @@ __device__ void attention_phase(const ChainParams& P, int phase, int l, const It
         for (int n = 0; n < 4; ++n)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float e = exp2f(s[n][q] - mnew[q >> 1]);
+            // a masked row may see no key of this item yet: weight 0
+            const float e = masked && mnew[q >> 1] == -INFINITY ? 0.f : exp2f(s[n][q] - mnew[q >> 1]);
             s[n][q] = e;
             lsum[q >> 1] += e;
           }
@@ -1438,7 +1469,7 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
       if (kind == PH_EMBED) {
         embed_phase(P);
       } else if (kind == PH_ATT) {
-        attention_phase(P, p, l, items, smem);
+        attention_phase(P, p, l, items, smem, rowpos);
         named_bar(1, CH_CT);   // every warp is done with the ring memory
         if (tid == 0) misc[MS_ATT_DONE] = l + 1;
       } else if (kind == PH_CMB) {
@@ -1625,6 +1656,7 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
   P.eps = c.rms_eps;
   P.embed_scale = c.embed_scale;
   P.scale_log2 = 1.4426950408889634f / sqrtf((float)CH_DH);
+  P.causal_layers = c.causal_layers, P.window_layers = c.window_layers, P.window = c.sliding_window;
   if (P.grid <= 0) return DFLASH_ERR_UNSUPPORTED;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(P.grid);

@@ -93,6 +93,15 @@ typedef struct dflash_config {
   float rope_theta;
   float rms_eps;
   float embed_scale;         /* input_embedding_scale */
+  /* Draft layer types (txtmix §6): a sliding_attention layer is causal and
+   * keeps a window of sliding_window keys, a full_attention layer is
+   * bidirectional.  Block row i sits at position p = L + i after the L
+   * context entries; a causal layer's row sees keys at positions <= p, a
+   * windowed layer's row keys at positions > p - sliding_window (context
+   * included).  0 everywhere: every layer bidirectional over all keys. */
+  int32_t causal_layers;     /* bit l: layer l is causal */
+  int32_t window_layers;     /* bit l: layer l keeps sliding_window keys */
+  int32_t sliding_window;    /* >= 1 when window_layers != 0 */
 } dflash_config;
 
 /* One decoder layer's weights (device, borrowed). */

@@ -18,7 +18,9 @@ def draft_model(s: DraftShape, dtype: str, weights: dict, max_pos: int) -> dfl.M
     return dfl.Model(D=s.D, H=s.H, G=s.G, d=s.d, F=s.F, V=s.V, n_layers=s.n_layers, dtype=dtype,
                      weights=weights, max_pos=max_pos, qk_norm=True, mask_id=s.mask_id,
                      n_target_layers=s.n_target_layers, n_pick=s.n_pick, target_layer_ids=ids,
-                     rope_theta=s.rope_theta, eps=s.eps, embed_scale=s.embed_scale)
+                     rope_theta=s.rope_theta, eps=s.eps, embed_scale=s.embed_scale,
+                     causal_layers=s.causal_layers, window_layers=s.window_layers,
+                     sliding_window=s.sliding_window)
 
 
 def target_model(t: TargetShape, dtype: str, weights: dict, max_pos: int) -> dfl.Model:
