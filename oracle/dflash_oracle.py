@@ -34,6 +34,11 @@ What pins each function (tests/test_oracle_*.py):
                            ignores older context; the anchor's causal output
                            equals full attention over explicitly sliced keys;
                            a window covering all keys changes nothing
+  dynamic_conv             taps (1, 0) are the identity and (0, 1) a shift
+                           by one row; one correction per channel group;
+                           causal (a row ignores later rows); in a layer,
+                           identity convs change nothing and a shifting
+                           finish conv shifts the sublayer's increment
   draft_layer/draft_block  reductions: zero W_o and W_d give the identity;
                            zero W_q gives uniform attention (closed form);
                            context enters only through K/V
@@ -74,6 +79,7 @@ __all__ = [
     "TargetCache", "target_forward", "ar_generate", "speculative_generate",
     "softmax_t", "sample_from", "verify_rejection", "acceptance_probability",
     "speculative_sample_generate", "topk_lowest", "select_candidates", "draft_key_visible",
+    "dynamic_conv",
 ]
 
 
@@ -270,9 +276,39 @@ def draft_key_visible(L: int, B: int, causal: bool, window: int) -> np.ndarray:
     return vis
 
 
+def dynamic_conv(x: np.ndarray, corr: np.ndarray, base: np.ndarray, group: int) -> np.ndarray:
+    """DFlash 2's two-tap grouped dynamic causal conv over one block
+    ([reading] §13, §14): out_t = k_t0 * x_t + k_t1 * x_(t-1), depthwise,
+    with each coefficient the learned base kernel plus a correction computed
+    from the row's hidden state, one correction per group of ``group``
+    channels.  The block's first row has no predecessor (zero: the module
+    keeps no state across steps; every later row reads the one before it,
+    so the first mask position reads the anchor).
+
+    x: [B, D]; corr: [B, 2, D // group] (tap, group); base: [2, D] (tap,
+    channel).  Returns [B, D] fp64."""
+    x = np.asarray(x, np.float64)
+    k = np.asarray(base, np.float64)[None] + np.repeat(np.asarray(corr, np.float64), group, axis=-1)
+    prev = np.concatenate([np.zeros((1, x.shape[1])), x[:-1]], axis=0)
+    return k[:, 0] * x + k[:, 1] * prev
+
+
+def _conv_pair(x: np.ndarray, kp: np.ndarray, base: np.ndarray, group: int):
+    """The corrections of a conv module's two calls from the rows x:
+    kernel_projection kp [2 * 2 * (D // group), D] (no bias), read as
+    [call, tap, group]; base [2 (call), 2 (tap), D].  Returns the prepare
+    and finish functions (y -> conv of y with that call's coefficients; the
+    prepared rows are stored in fp32, and the sublayer output y is stored in
+    fp32 before its finish conv)."""
+    B, D = x.shape
+    corr = linear(x, kp).reshape(B, 2, 2, D // group)
+    return (lambda y: f32(dynamic_conv(y, corr[:, 0], base[0], group)),
+            lambda y: dynamic_conv(f32(y), corr[:, 1], base[1], group))
+
+
 def draft_layer(x: np.ndarray, layer: dict, ctx_K: np.ndarray, ctx_V: np.ndarray,
                 pos: np.ndarray, H: int, G: int, d: int, theta: float, eps: float,
-                store=f32, mask: Optional[np.ndarray] = None) -> np.ndarray:
+                store=f32, mask: Optional[np.ndarray] = None, conv_group: int = 0) -> np.ndarray:
     """One Qwen3-style draft decoder layer over one sequence's block.
 
     x: [B, D] fp32 residual.  ctx_K, ctx_V: [L, G, d] injected context.
@@ -280,9 +316,19 @@ def draft_layer(x: np.ndarray, layer: dict, ctx_K: np.ndarray, ctx_V: np.ndarray
     concatenated along the sequence ([tutorial] §2.1.2; [reading] §5);
     attention is bidirectional unless ``mask`` (draft_key_visible) says
     otherwise.  Then o_proj + residual and a SwiGLU FFN + residual, each
-    sublayer pre-normalised."""
+    sublayer pre-normalised.
+
+    conv_group > 0 (DFlash 2, [reading] §13, §14): each sublayer has its own
+    conv module (layer["conv_att_kp"] / ["conv_att_base"] and the "mlp"
+    pair).  Its corrections come from the residual entering the sublayer;
+    the prepare call convolves that residual before the sublayer's norm and
+    the finish call convolves the sublayer's output before the residual
+    add (x + finish(f(norm(prepare(x)))))."""
     B = x.shape[0]
-    h = store(rmsnorm(x, layer["g_in"], eps))
+    prep = fin = lambda y: y
+    if conv_group:
+        prep, fin = _conv_pair(x, layer["conv_att_kp"], layer["conv_att_base"], conv_group)
+    h = store(rmsnorm(prep(x), layer["g_in"], eps))
     q = linear(h, layer["wq"]).reshape(B, H, d)
     k = linear(h, layer["wk"]).reshape(B, G, d)
     v = linear(h, layer["wv"]).reshape(B, G, d)
@@ -292,10 +338,12 @@ def draft_layer(x: np.ndarray, layer: dict, ctx_K: np.ndarray, ctx_V: np.ndarray
     K = np.concatenate([ctx_K, k], axis=0)
     Vv = np.concatenate([ctx_V, v], axis=0)
     o = store(attention(q, K, Vv, mask).reshape(B, H * d))
-    x = f32(x + linear(o, layer["wo"]))
-    h2 = store(rmsnorm(x, layer["g_post"], eps))
+    x = f32(x + fin(linear(o, layer["wo"])))
+    if conv_group:
+        prep, fin = _conv_pair(x, layer["conv_mlp_kp"], layer["conv_mlp_base"], conv_group)
+    h2 = store(rmsnorm(prep(x), layer["g_post"], eps))
     a = store(silu(linear(h2, layer["wg"])) * linear(h2, layer["wu"]))
-    return f32(x + linear(a, layer["wd"]))
+    return f32(x + fin(linear(a, layer["wd"])))
 
 
 def lm_head_logits(hf: np.ndarray, W_lm: np.ndarray) -> np.ndarray:
@@ -349,7 +397,8 @@ def draft_block(shape, W: dict, ctx_K: List[List[np.ndarray]],
                       if (getattr(shape, "window_layers", 0) >> l) & 1 else 0)
             mask = draft_key_visible(L, B, causal, window) if causal or window else None
             x = draft_layer(x, layer, ctx_K[l][b], ctx_V[l][b], pos, shape.H,
-                            shape.G, shape.d, shape.rope_theta, shape.eps, store, mask)
+                            shape.G, shape.d, shape.rope_theta, shape.eps, store, mask,
+                            getattr(shape, "conv_group", 0))
         hidden.append(x)
         ids[b, 0] = anchors[b]
         if not lm_head:

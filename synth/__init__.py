@@ -44,6 +44,7 @@ class DraftShape:
     causal_layers: int = 0    # bit l: layer l is causal (a sliding_attention layer)
     window_layers: int = 0    # bit l: layer l keeps sliding_window keys
     sliding_window: int = 0
+    conv_group: int = 0       # channels per conv correction (0: no conv modules)
 
 
 @dataclass(frozen=True)
@@ -285,3 +286,22 @@ def selector_weights(D: int, V: int, dtype: str, seed: int, rank: int = 256,
     return {"w_h": _normal((rank, D), D ** -0.5, g, device, td),
             "code_pred": _normal((V, rank), rank ** -0.25, g, device, td),
             "code_succ": _normal((V, rank), rank ** -0.25, g, device, td)}
+
+
+def add_conv_weights(weights: dict, shape: DraftShape, dtype: str, seed: int,
+                     device="cpu") -> dict:
+    """Random-init conv modules (one around attention, one around the FFN)
+    added to each layer of ``weights``: kernel projections [2 * 2 * (D //
+    conv_group), D] with N(0, 0.1^2 / D) entries (corrections of about 0.1
+    from unit-RMS rows) and fp32 base kernels [2 (call), 2 (tap), D] near
+    the identity (tap 0 about 1, tap 1 about 0.3 in size)."""
+    td = torch_dtype(dtype)
+    g = _gen(seed, device)
+    D, ng = shape.D, shape.D // shape.conv_group
+    for lay in weights["layers"]:
+        for k in ("att", "mlp"):
+            lay[f"conv_{k}_kp"] = _normal((4 * ng, D), 0.1 * D ** -0.5, g, device, td)
+            base = _normal((2, 2, D), 0.3, g, device, torch.float32)
+            base[:, 0] += 1.0
+            lay[f"conv_{k}_base"] = base
+    return weights
