@@ -46,12 +46,14 @@ class dflash_config(C.Structure):
                 ("max_pos", C.c_int32), ("qk_norm", C.c_int32), ("dtype", C.c_int32),
                 ("rope_theta", C.c_float), ("rms_eps", C.c_float), ("embed_scale", C.c_float),
                 ("causal_layers", C.c_int32), ("window_layers", C.c_int32),
-                ("sliding_window", C.c_int32)]
+                ("sliding_window", C.c_int32), ("conv_group", C.c_int32)]
 
 
 class dflash_layer_weights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in ("wq", "wk", "wv", "wo", "wg", "wu", "wd",
-                                          "g_in", "g_post", "q_norm", "k_norm")]
+                                          "g_in", "g_post", "q_norm", "k_norm",
+                                          "conv_att_kp", "conv_att_base", "conv_mlp_kp",
+                                          "conv_mlp_base")]
 
 
 class dflash_weights(C.Structure):
@@ -378,7 +380,8 @@ class Model:
     def __init__(self, *, D, H, G, d, F, V, n_layers, dtype: str, weights: dict, max_pos: int,
                  qk_norm: bool, mask_id: int = 0, n_target_layers: int = 0, n_pick: int = 5,
                  target_layer_ids: Sequence[int] = (), rope_theta=1e6, eps=1e-6,
-                 embed_scale=1.0, causal_layers=0, window_layers=0, sliding_window=0):
+                 embed_scale=1.0, causal_layers=0, window_layers=0, sliding_window=0,
+                 conv_group=0):
         cfg = dflash_config()
         cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim = D, H, G, d
         cfg.ffn, cfg.vocab, cfg.n_layers = F, V, n_layers
@@ -389,14 +392,15 @@ class Model:
         cfg.dtype = BF16 if dtype == "bf16" else F32
         cfg.rope_theta, cfg.rms_eps, cfg.embed_scale = rope_theta, eps, embed_scale
         cfg.causal_layers, cfg.window_layers = causal_layers, window_layers
-        cfg.sliding_window = sliding_window
+        cfg.sliding_window, cfg.conv_group = sliding_window, conv_group
         w = dflash_weights()
         w.wc, w.g_c = _ptr(weights.get("wc")), _ptr(weights.get("g_c"))
         w.g_f = _ptr(weights.get("g_f", weights.get("g_final")))
         w.embed, w.lm_head = _ptr(weights["embed"]), _ptr(weights["lm_head"])
         for l, lay in enumerate(weights["layers"]):
             for name in ("wq", "wk", "wv", "wo", "wg", "wu", "wd", "g_in", "g_post",
-                         "q_norm", "k_norm"):
+                         "q_norm", "k_norm", "conv_att_kp", "conv_att_base", "conv_mlp_kp",
+                         "conv_mlp_base"):
                 setattr(w.layers[l], name, _ptr(lay.get(name)))
         self.cfg, self.w, self.weights = cfg, w, weights
         self.dtype = dtype

@@ -97,6 +97,10 @@ static size_t forward_bytes(const dflash_config& c, int64_t R) {
   b += round256(R * F * 4) * 2;       // gf, uf
   b += round256(R * D * sz);          // hf
   b += round256(R * V * 4);           // logits
+  if (c.conv_group > 0) {             // conv: prepared rows / sublayer outputs, corrections
+    b += round256(R * D * 4);
+    b += round256(R * (4 * D / c.conv_group) * 4);
+  }
   return b + 1024;
 }
 
@@ -108,6 +112,7 @@ static size_t chunk_row_bytes(const dflash_config& c) {
 
 struct Fwd {
   float *x, *xg, *qf, *kf, *vf, *gf, *uf, *logits, *partial, *attn, *ssq;
+  float *cu, *cc;   // conv: prepared rows / sublayer outputs [R, D], corrections [R, 4 D / group]
   float4* amx;
   void *h, *q, *kb, *vb, *o, *hf, *a;
 };
@@ -138,6 +143,11 @@ static bool carve_forward(const dflash_handle* h, int64_t R, void* ws, size_t ws
   f->uf = cv.take<float>(R * F);
   f->hf = cv.take<char>(R * D * sz);
   f->logits = cv.take<float>(R * V);
+  f->cu = f->cc = nullptr;
+  if (c.conv_group > 0) {
+    f->cu = cv.take<float>(R * D);
+    f->cc = cv.take<float>(R * (4 * D / c.conv_group));
+  }
   return cv.ok;
 }
 
@@ -173,6 +183,37 @@ static int mlp_tail(dflash_handle* h, cudaStream_t s, const dflash_layer_weights
     return rc;
   if ((rc = swiglu(h, s, dt, f.gf, f.uf, f.h, R * F))) return rc;
   return gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, one_src(f.h, F, F), L.wd, F, f.x, D, R, D, F, true);
+}
+
+// mlp_tail with the conv modules (txtmix §13-§14): x += finish(o W_o^T);
+// then h = norm(prepare(x)) with the FFN module's corrections and
+// x += finish(SwiGLU FFN of h).  Each finish call convolves the sublayer
+// output across adjacent rows of a block, so it follows the projection
+// instead of being its epilogue.
+static int conv_mlp_tail(dflash_handle* h, cudaStream_t s, const dflash_layer_weights& L, Fwd& f,
+                         int64_t R, int B) {
+  const dflash_config& c = h->cfg;
+  const int D = c.hidden, F = c.ffn, Hd = c.n_heads * c.head_dim, dt = c.dtype;
+  int rc;
+  if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, one_src(f.o, Hd, Hd), L.wo, Hd, f.cu, D, R, D, Hd,
+                 false)))
+    return rc;
+  if ((rc = conv_apply(h, s, f.cu, f.cc, L.conv_att_base, 1, R, B, f.x, true))) return rc;
+  if ((rc = conv_corr(h, s, f.x, L.conv_mlp_kp, R, f.cc))) return rc;
+  if ((rc = conv_apply(h, s, f.x, f.cc, L.conv_mlp_base, 0, R, B, f.cu, false))) return rc;
+  if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.cu, D, f.h, D, L.g_post, R, D, c.rms_eps, 0)))
+    return rc;
+  if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, one_src(f.h, D, D), L.wg, D, f.gf, F, R, F, D,
+                 false)))
+    return rc;
+  if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, one_src(f.h, D, D), L.wu, D, f.uf, F, R, F, D,
+                 false)))
+    return rc;
+  if ((rc = swiglu(h, s, dt, f.gf, f.uf, f.h, R * F))) return rc;
+  if ((rc = gemm(h, s, DFLASH_K_WEIGHT_GEMM, dt, one_src(f.h, F, F), L.wd, F, f.cu, D, R, D, F,
+                 false)))
+    return rc;
+  return conv_apply(h, s, f.cu, f.cc, L.conv_mlp_base, 1, R, B, f.x, true);
 }
 
 static bool streaming(const dflash_handle* h, int64_t M);
@@ -582,7 +623,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
   if (!w->embed || !w->lm_head || !w->g_f) return DFLASH_ERR_INVALID_ARG;
   if (c.causal_layers < 0 || c.window_layers < 0 || c.sliding_window < 0 ||
       (c.window_layers != 0 && c.sliding_window < 1) ||
-      ((c.causal_layers | c.window_layers) >> c.n_layers) != 0)
+      ((c.causal_layers | c.window_layers) >> c.n_layers) != 0 || c.conv_group < 0 ||
+      (c.conv_group > 0 && c.hidden % c.conv_group != 0))
     return DFLASH_ERR_SHAPE;
   const void* al[] = {w->embed, w->lm_head, w->wc};
   for (const void* p : al)
@@ -596,6 +638,9 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, dflash_hand
     }
     if (!L.g_in || !L.g_post) return DFLASH_ERR_INVALID_ARG;
     if (c.qk_norm && (!L.q_norm || !L.k_norm)) return DFLASH_ERR_INVALID_ARG;
+    if (c.conv_group > 0 &&
+        (!L.conv_att_kp || !L.conv_att_base || !L.conv_mlp_kp || !L.conv_mlp_base))
+      return DFLASH_ERR_INVALID_ARG;
   }
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DFLASH_ERR_CUDA;
@@ -892,14 +937,20 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
                         c.embed_scale, f.x)))
     return rc;
   const RowMap rm{0, B, nullptr, nullptr, batch, 0};
-  const bool stream = streaming(h, R);
-  const bool tcore = !stream && dense_tc(h, R) && attn_fast_ok(h, B);
+  const bool conv = c.conv_group > 0;   // conv modules: the per-projection path below
+  const bool stream = !conv && streaming(h, R);
+  const bool tcore = !conv && !stream && dense_tc(h, R) && attn_fast_ok(h, B);
   if ((tcore || stream) && attn_fast_ok(h, B) &&
       (rc = attn_plan(h, s, kv->len, kv->cap, batch, B, f.attn)))
     return rc;
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights& L = h->w.layers[l];
-    if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, L.g_in, R, D, c.rms_eps, 0)))
+    if (conv) {   // the attention module's corrections and prepare call: h = norm(prepare(x))
+      if ((rc = conv_corr(h, s, f.x, L.conv_att_kp, R, f.cc))) return rc;
+      if ((rc = conv_apply(h, s, f.x, f.cc, L.conv_att_base, 0, R, B, f.cu, false))) return rc;
+    }
+    if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, conv ? f.cu : f.x, D, f.h, D, L.g_in, R, D,
+                           c.rms_eps, 0)))
       return rc;
     if (tcore) {
       if ((rc = qkv_tc(h, s, l, f, R, rm, kv->len))) return rc;
@@ -937,7 +988,7 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
     if ((rc = attention(h, s, dt, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch, B,
                         H, G, d, false, f.o, layer_causal(c, l), layer_window(c, l))))
       return rc;
-    if ((rc = mlp_tail(h, s, L, f, R))) return rc;
+    if ((rc = conv ? conv_mlp_tail(h, s, L, f, R, B) : mlp_tail(h, s, L, f, R))) return rc;
   }
   if (hidden_out &&
       cudaMemcpyAsync(hidden_out, f.x, R * D * sizeof(float), cudaMemcpyDeviceToDevice, s))

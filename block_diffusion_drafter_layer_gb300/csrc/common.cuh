@@ -318,6 +318,10 @@ int verify_rejection(dflash_handle* h, cudaStream_t s, const int32_t* draft, con
                      const float* p, int V, const double* u_acc, const double* u_smp, int batch,
                      int B, const int32_t* start, int32_t* accept, int32_t* tau, int32_t* token,
                      int32_t* out_tokens, int32_t* new_len, void* ws);
+int conv_corr(dflash_handle* h, cudaStream_t s, const float* x, const void* kp, int64_t R,
+              float* corr);
+int conv_apply(dflash_handle* h, cudaStream_t s, const float* y, const float* corr,
+               const float* base, int call, int64_t R, int B, float* out, bool accumulate);
 size_t select_ws_bytes(int batch, int B, int V, int D, int K, int rank);
 bool select_shape_ok(int B, int V, int D, int K, int rank);
 int select_candidates(dflash_handle* h, cudaStream_t s, const float* logits, const float* x,

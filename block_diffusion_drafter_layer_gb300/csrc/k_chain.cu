@@ -1556,6 +1556,7 @@ bool chain_ok(const dflash_handle* h, int batch, int B) {
   const int64_t R = (int64_t)batch * B;
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   if (!al16(h->w.g_f)) return false;   // gains are read as float4 in the epilogues
+  if (c.conv_group > 0) return false;   // conv modules run in the per-projection path
   for (int l = 0; l < c.n_layers; ++l) {
     const dflash_layer_weights& L = h->w.layers[l];
     if (!al16(L.g_in) || !al16(L.g_post)) return false;

@@ -102,6 +102,11 @@ typedef struct dflash_config {
   int32_t causal_layers;     /* bit l: layer l is causal */
   int32_t window_layers;     /* bit l: layer l keeps sliding_window keys */
   int32_t sliding_window;    /* >= 1 when window_layers != 0 */
+  /* DFlash 2's grouped dynamic causal conv (txtmix §13-§14): > 0 gives
+   * every draft layer two conv modules (around attention and around the
+   * FFN; weights in dflash_layer_weights), one dynamic correction per
+   * conv_group channels (16 in DFlash 2); D % conv_group == 0.  0: none. */
+  int32_t conv_group;
 } dflash_config;
 
 /* One decoder layer's weights (device, borrowed). */
@@ -117,6 +122,19 @@ typedef struct dflash_layer_weights {
   const float* g_post;       /* [D] post-attention RMSNorm gain */
   const float* q_norm;       /* [d] (qk_norm only) */
   const float* k_norm;       /* [d] (qk_norm only) */
+  /* conv modules (conv_group > 0 only), one per sublayer.  A module's
+   * kernel projection kp [2*2*(D/conv_group), D] (handle dtype, no bias)
+   * maps the residual entering the sublayer to corrections read as
+   * [call, tap, group]; base [2 (call), 2 (tap), D] fp32.  Coefficient of
+   * channel c, tap k, call n at row t: base[n][k][c] + corr_t[n][k][c /
+   * conv_group]; conv_t(y) = coef_0 * y_t + coef_1 * y_(t-1), with no
+   * predecessor for a block's first row.  Call 0 (prepare) convolves the
+   * residual before the sublayer's norm, call 1 (finish) the sublayer's
+   * output before the residual add. */
+  const void* conv_att_kp;
+  const float* conv_att_base;
+  const void* conv_mlp_kp;
+  const float* conv_mlp_base;
 } dflash_layer_weights;
 
 typedef struct dflash_weights {

@@ -20,7 +20,7 @@ def draft_model(s: DraftShape, dtype: str, weights: dict, max_pos: int) -> dfl.M
                      n_target_layers=s.n_target_layers, n_pick=s.n_pick, target_layer_ids=ids,
                      rope_theta=s.rope_theta, eps=s.eps, embed_scale=s.embed_scale,
                      causal_layers=s.causal_layers, window_layers=s.window_layers,
-                     sliding_window=s.sliding_window)
+                     sliding_window=s.sliding_window, conv_group=s.conv_group)
 
 
 def target_model(t: TargetShape, dtype: str, weights: dict, max_pos: int) -> dfl.Model:
