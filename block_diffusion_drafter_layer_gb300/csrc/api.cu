@@ -303,7 +303,11 @@ static int qkv_stream(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R
 }
 
 // o_proj (+ residual), RMSNorm, gate/up with the SwiGLU epilogue, down (+ residual).
-static int mlp_stream(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R) {
+// With the conv modules (conv): o_proj and down store plain rows into f.cu
+// and their finish convs add them into x; the FFN's norm reads the rows of
+// its prepare conv.
+static int mlp_stream(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R, bool conv,
+                      int B) {
   const dflash_config& c = h->cfg;
   const dflash_layer_weights& W = h->w.layers[l];
   const int D = c.hidden, F = c.ffn, Hd = c.n_heads * c.head_dim, dt = c.dtype;
@@ -312,14 +316,21 @@ static int mlp_stream(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R
   L.nmap = 1;
   L.wmaps[0] = &h->maps[l].wo;
   L.nseg = 1;
-  L.seg[0] = make_seg(0, (D + 127) / 128, SK_RESID, 0, D, f.x, D);
+  L.seg[0] = conv ? make_seg(0, (D + 127) / 128, SK_F32, 0, D, f.cu, D)
+                  : make_seg(0, (D + 127) / 128, SK_RESID, 0, D, f.x, D);
   L.nsrc = 1;
   L.a_src[0] = f.o;
   L.a_ld = Hd;
   L.K = Hd;
   L.M = (int)R;
   if ((rc = wstream(h, s, DFLASH_K_WEIGHT_GEMM, L, f.partial, f.amx))) return rc;
-  if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, W.g_post, R, D, c.rms_eps, 0)))
+  if (conv) {
+    if ((rc = conv_apply(h, s, f.cu, f.cc, W.conv_att_base, 1, R, B, f.x, true))) return rc;
+    if ((rc = conv_corr(h, s, f.x, W.conv_mlp_kp, R, f.cc))) return rc;
+    if ((rc = conv_apply(h, s, f.x, f.cc, W.conv_mlp_base, 0, R, B, f.cu, false))) return rc;
+  }
+  if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, conv ? f.cu : f.x, D, f.h, D, W.g_post, R, D,
+                         c.rms_eps, 0)))
     return rc;
   WLaunch G;
   G.nmap = 2;
@@ -338,13 +349,15 @@ static int mlp_stream(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R
   Dn.nmap = 1;
   Dn.wmaps[0] = &h->maps[l].wd;
   Dn.nseg = 1;
-  Dn.seg[0] = make_seg(0, (D + 127) / 128, SK_RESID, 0, D, f.x, D);
+  Dn.seg[0] = conv ? make_seg(0, (D + 127) / 128, SK_F32, 0, D, f.cu, D)
+                   : make_seg(0, (D + 127) / 128, SK_RESID, 0, D, f.x, D);
   Dn.nsrc = 1;
   Dn.a_src[0] = f.a;
   Dn.a_ld = F;
   Dn.K = F;
   Dn.M = (int)R;
-  return wstream(h, s, DFLASH_K_WEIGHT_GEMM, Dn, f.partial, f.amx);
+  if ((rc = wstream(h, s, DFLASH_K_WEIGHT_GEMM, Dn, f.partial, f.amx))) return rc;
+  return conv ? conv_apply(h, s, f.cu, f.cc, W.conv_mlp_base, 1, R, B, f.x, true) : DFLASH_OK;
 }
 
 static int lm_head_stream(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows, int32_t* ids,
@@ -937,8 +950,8 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
                         c.embed_scale, f.x)))
     return rc;
   const RowMap rm{0, B, nullptr, nullptr, batch, 0};
-  const bool conv = c.conv_group > 0;   // conv modules: the per-projection path below
-  const bool stream = !conv && streaming(h, R);
+  const bool conv = c.conv_group > 0;   // conv modules: streaming or SIMT projections
+  const bool stream = streaming(h, R);
   const bool tcore = !conv && !stream && dense_tc(h, R) && attn_fast_ok(h, B);
   if ((tcore || stream) && attn_fast_ok(h, B) &&
       (rc = attn_plan(h, s, kv->len, kv->cap, batch, B, f.attn)))
@@ -969,7 +982,7 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
         rc = attention(h, s, dt, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch, B,
                        H, G, d, false, f.o, layer_causal(c, l), layer_window(c, l));
       if (rc) return rc;
-      if ((rc = mlp_stream(h, s, l, f, R))) return rc;
+      if ((rc = mlp_stream(h, s, l, f, R, conv, B))) return rc;
       continue;
     }
     const ASrc a = one_src(f.h, D, D);
