@@ -77,8 +77,17 @@ static_assert(sizeof(WParams) <= 4096, "kernel parameters must fit the 4 KB limi
 #ifndef DFLASH_WS_STAGES
 #define DFLASH_WS_STAGES 8
 #endif
+// 1: the launch may start while the kernel before it finishes (programmatic
+// dependent launch; activations are read after griddepcontrol.wait)
+#ifndef DFLASH_WS_PDL
+#define DFLASH_WS_PDL 1
+#endif
+// CTAs per SM.  One, with the deeper ring it leaves room for: with two
+// co-resident CTAs a rare result error was seen (one consumer warp's 32
+// output columns of one tile, in a few of 300 identical LM-head launches),
+// never with one, and one is as fast.
 #ifndef DFLASH_WS_MINBLOCKS
-#define DFLASH_WS_MINBLOCKS 2
+#define DFLASH_WS_MINBLOCKS 1
 #endif
 
 template <int MT>
@@ -847,8 +856,10 @@ static int launch_wstream(dflash_handle* h, cudaStream_t s, int kclass, WParams 
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
-  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[na++].val.programmaticStreamSerializationAllowed = 1;
+  if (DFLASH_WS_PDL) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na++].val.programmaticStreamSerializationAllowed = 1;
+  }
   if (GB) {
     attr[na].id = cudaLaunchAttributeCooperative;
     attr[na++].val.cooperative = 1;
