@@ -9,13 +9,14 @@ reads back the accepted length once per round (as the reference loop does).
 """
 from __future__ import annotations
 
-from typing import List, Sequence, Tuple
+from typing import List, Optional, Sequence, Tuple
 
 import torch
 
 from . import (KVCache, Model, dflash_build_target_layer_ids, dflash_draft_block,
                dflash_draft_round, dflash_emit_tokens, dflash_fuse_context, dflash_inject_kv,
                dflash_lm_head_logits, dflash_sample_rows, dflash_sampling_ws_bytes,
+               dflash_select_candidates, dflash_select_ws_bytes,
                dflash_target_forward,
                dflash_verify_greedy, dflash_verify_rejection)
 
@@ -50,9 +51,24 @@ class SpecDecoder:
         self.tkv.len.zero_()
         self.dkv.len.zero_()
 
-    def generate(self, prompt: Sequence[int], n_new: int) -> Tuple[List[int], List[int]]:
+    def generate(self, prompt: Sequence[int], n_new: int,
+                 selector: Optional[dict] = None) -> Tuple[List[int], List[int]]:
+        """The greedy loop, reading the accepted length every round.
+        selector (DFlash 2's candidate selection, txtmix §13-§14): {"w_h",
+        "code_pred", "code_succ", "top_k"}; the block is then drafted without
+        its argmax head, and the drafts are dflash_select_candidates over its
+        LM-head logits (greedy verification keeps the output the target's
+        own).  Returns (tokens, tau per round)."""
         self.reset()
         dev, B = self.device, self.B
+        if selector is not None:
+            V = self.draft.vocab
+            hid = torch.empty(B, self.D, dtype=torch.float32, device=dev)
+            z_d = torch.empty(B - 1, V, dtype=torch.float32, device=dev)
+            rank = int(selector["w_h"].shape[0])
+            ws_sel = torch.empty(dflash_select_ws_bytes(self.draft.handle, 1, B,
+                                                        selector["top_k"], rank),
+                                 dtype=torch.uint8, device=dev)
         P = len(prompt)
         td = self.taps_block.dtype
         taps_pre = torch.empty(self.n_pick, P, self.D, dtype=td, device=dev)
@@ -71,8 +87,19 @@ class SpecDecoder:
             dflash_inject_kv(self.draft.handle, self.h_t, T, self.row0, nrows, 1,
                              self.dkv.struct, self.ws_d)
             anchor = torch.tensor([out[-1]], dtype=torch.int32, device=dev)
-            dflash_draft_block(self.draft.handle, anchor, 1, B, self.dkv.struct, self.draft_ids,
-                               None, None, self.ws_d)
+            if selector is None:
+                dflash_draft_block(self.draft.handle, anchor, 1, B, self.dkv.struct,
+                                   self.draft_ids, None, None, self.ws_d)
+            else:
+                g_d = self.draft.final_gain
+                dflash_draft_block(self.draft.handle, anchor, 1, B, self.dkv.struct, None, None,
+                                   hid, self.ws_d)
+                dflash_lm_head_logits(self.draft.handle, hid, B - 1, g_d, z_d, self.ws_d,
+                                      skip_first_of=B)
+                dflash_select_candidates(self.draft.handle, z_d, hid, g_d, anchor, 1, B,
+                                         selector["top_k"], selector["w_h"],
+                                         selector["code_pred"], selector["code_succ"],
+                                         self.draft_ids, ws=ws_sel)
             # verify: one target forward over [anchor, d_1 .. d_{B-1}]
             self.start.copy_(self.tkv.len[:1])
             dflash_target_forward(self.target.handle, self.draft_ids, 1, B, self.tkv.struct,

@@ -658,7 +658,7 @@ def ar_generate(tshape, TW: dict, prompt: Sequence[int], n_new: int,
 
 def speculative_generate(tshape, TW: dict, dshape, DW: dict,
                          prompt: Sequence[int], n_new: int, B: int,
-                         store=f32):
+                         store=f32, selector: Optional[dict] = None):
     """Greedy DFlash loop ([reading] §9 steps 2-6).
 
     Prefill the target (first token = first anchor; taps of every prompt
@@ -667,6 +667,9 @@ def speculative_generate(tshape, TW: dict, dshape, DW: dict,
     [anchor, mask x (B-1)], verify it with one target forward, keep the
     accepted prefix plus the bonus, crop the target cache to the new start,
     and keep only the accepted positions' taps as the next context.
+    selector (DFlash 2, [reading] §13-§14): {"w_h", "code_pred",
+    "code_succ", "top_k"}; the drafts are then select_candidates over the
+    block's logits and final-normed rows instead of the argmax.
 
     Returns (tokens [n_new], list of tau per round)."""
     tap_ids = build_target_layer_ids(dshape.n_target_layers, dshape.n_pick)
@@ -688,8 +691,19 @@ def speculative_generate(tshape, TW: dict, dshape, DW: dict,
                              dshape.rope_theta, dshape.eps, store)
             ctx_K[l] = np.concatenate([ctx_K[l], k], axis=0)
             ctx_V[l] = np.concatenate([ctx_V[l], v], axis=0)
-        draft, _ = draft_block(dshape, DW, [[k] for k in ctx_K],
-                               [[v] for v in ctx_V], [out[-1]], B, store)
+        if selector is None:
+            draft, _ = draft_block(dshape, DW, [[k] for k in ctx_K],
+                                   [[v] for v in ctx_V], [out[-1]], B, store)
+        else:
+            draft, _, z, hid = draft_block(dshape, DW, [[k] for k in ctx_K],
+                                           [[v] for v in ctx_V], [out[-1]], B, store,
+                                           return_logits=True, return_hidden=True)
+            hn = rmsnorm(hid[0, 1:], DW["g_f"], dshape.eps)
+            path, _, _ = select_candidates(z[0], hn, out[-1], selector["w_h"],
+                                           selector["code_pred"], selector["code_succ"],
+                                           selector["top_k"])
+            draft = draft.copy()
+            draft[0, 1:] = path
         post, vtaps = target_forward(tshape, TW, cache, draft[0], tap_ids, store)
         accept, bonus, toks, new_len = verify_greedy(draft, post[None, :],
                                                      np.array([start]))

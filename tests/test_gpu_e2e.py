@@ -156,3 +156,35 @@ def test_e2e_resident_loop_all_accepted(dfl):
     ar_ref = O.ar_generate(w.target, to_np64(TW), prompt, w.new_tokens)
     np.testing.assert_array_equal(res, ar_ref)
     assert res_taus == [w.B] * len(res_taus)
+
+
+def test_e2e_selected_loop(dfl):
+    """The greedy loop with DFlash 2 candidate selection: the GPU's tokens
+    and taus equal the oracle's selected loop, and the tokens are the
+    target's own greedy output (lossless whatever the drafts)."""
+    from synth.gpu import draft_model, spec_decoder, target_model
+    w = synth.WORKLOADS["e2e_f32"]
+    TWn, DWn = _weights(w)
+    TW, DW = _upload(TWn), _upload(DWn)
+    DW["embed"], DW["lm_head"] = TW["embed"], TW["lm_head"]
+    n_new = 40
+    cap = w.prompt_len + n_new + 2 * w.B
+    target = target_model(w.target, w.dtype, TW, max_pos=cap)
+    draft = draft_model(w.draft, w.dtype, DW, max_pos=cap)
+    dec = spec_decoder(w, target, draft, cap=cap)
+    sel = synth.selector_weights(w.draft.D, w.draft.V, "f32", 13, rank=64, device="cuda")
+    sel["top_k"] = 16
+    prompt = synth.random_ids(w.prompt_len, w.target.V, seed=w.seed).tolist()
+    toks, taus = dec.generate(prompt, n_new, selector=sel)
+    assert dfl.dflash_get_status(draft.handle) == 0
+    sel_np = to_np64({k: v for k, v in sel.items() if k != "top_k"})
+    sel_np["top_k"] = 16
+    ref, rtaus = O.speculative_generate(w.target, to_np64(TWn), w.draft, to_np64(DWn), prompt,
+                                        n_new, w.B, selector=sel_np)
+    ar = O.ar_generate(w.target, to_np64(TWn), prompt, n_new)
+    print(f"selected loop: rounds {len(taus)}, taus {taus}")
+    np.testing.assert_array_equal(np.array(toks), ref)
+    np.testing.assert_array_equal(np.array(toks), ar)
+    assert taus == rtaus
+    target.close()
+    draft.close()

@@ -95,3 +95,19 @@ def test_draft_block_anchor_column_and_shapes():
     assert ids.shape == (2, w.B) and gaps.shape == (2, w.B - 1)
     assert list(ids[:, 0]) == [3, 900]
     assert (gaps >= 0).all() and ids.max() < s.V
+
+
+def test_selected_loop_equals_autoregressive():
+    """DFlash 2 candidate selection changes the drafts, not the output: the
+    greedy loop with the selector still emits the target's own greedy
+    autoregressive tokens (txtmix §13-§14 with the verification of §8)."""
+    tshape, dshape = tiny_e2e()
+    TW, DW = _weights(tshape, dshape, 91)
+    sel = to_np(synth.selector_weights(dshape.D, dshape.V, "f32", 5, rank=32))
+    sel["top_k"] = 8
+    prompt = synth.random_ids(12, tshape.V, seed=4).tolist()
+    n_new = 20
+    ar = O.ar_generate(tshape, TW, prompt, n_new)
+    spec, taus = O.speculative_generate(tshape, TW, dshape, DW, prompt, n_new, 6, selector=sel)
+    np.testing.assert_array_equal(spec, ar)
+    assert all(1 <= t <= 6 for t in taus)
