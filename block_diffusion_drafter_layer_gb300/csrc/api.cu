@@ -381,17 +381,26 @@ static int lm_head_stream(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows
 }
 
 // ---- tensor-core paths for blocks of >= 128 rows (e.g. batch 32 x B 16) -----
+// Output tile width of a tcgen05 projection with N output columns: 128 where
+// 128-column tiles still fit in one wave (256-column tiles would leave more
+// than half of the SMs idle: o_proj and down at batch 32 x B 16), else 256.
+static int tc_width(const dflash_handle* h, int64_t M, int64_t N) {
+  return 2 * ((M + 127) / 128) * (N / 256) <= h->num_sms ? 128 : 256;
+}
+
 static int qkv_tc(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R, const RowMap& rm,
                   const int32_t* len) {
   const dflash_config& c = h->cfg;
   const dflash_layer_weights& W = h->w.layers[l];
   const int D = c.hidden, d = c.head_dim, Hd = c.n_heads * d, Gd = c.n_kv_heads * d;
-  const int tq = Hd / 256, tk = Gd / 256;
   WLaunch L;
+  L.bn = tc_width(h, R, Hd + 2 * Gd);
+  const int tq = Hd / L.bn, tk = Gd / L.bn;
+  const bool narrow = L.bn == 128;
   L.nmap = 3;
-  L.wmaps[0] = &h->maps[l].tq;
-  L.wmaps[1] = &h->maps[l].tk;
-  L.wmaps[2] = &h->maps[l].tv;
+  L.wmaps[0] = narrow ? &h->maps[l].wq : &h->maps[l].tq;
+  L.wmaps[1] = narrow ? &h->maps[l].wk : &h->maps[l].tk;
+  L.wmaps[2] = narrow ? &h->maps[l].wv : &h->maps[l].tv;
   L.nseg = 3;
   L.seg[0] = head_seg(0, tq, 0, Hd, d, 1, c.qk_norm ? W.q_norm : nullptr, f.q, Hd);
   L.seg[1] = head_seg(tq, tq + tk, 1, Gd, d, 1, c.qk_norm ? W.k_norm : nullptr, f.kb, Gd);
@@ -412,10 +421,11 @@ static int mlp_tc(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R) {
   const int D = c.hidden, F = c.ffn, Hd = c.n_heads * c.head_dim, dt = c.dtype;
   int rc;
   WLaunch L;
+  L.bn = tc_width(h, R, D);
   L.nmap = 1;
-  L.wmaps[0] = &h->maps[l].to;
+  L.wmaps[0] = L.bn == 128 ? &h->maps[l].wo : &h->maps[l].to;
   L.nseg = 1;
-  L.seg[0] = make_seg(0, D / 256, SK_RESID, 0, D, f.x, D);
+  L.seg[0] = make_seg(0, D / L.bn, SK_RESID, 0, D, f.x, D);
   L.nsrc = 1;
   L.a_src[0] = f.o;
   L.a_ld = Hd;
@@ -425,11 +435,12 @@ static int mlp_tc(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R) {
   if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, f.x, D, f.h, D, W.g_post, R, D, c.rms_eps, 0)))
     return rc;
   WLaunch G;
+  G.bn = tc_width(h, R, 2 * (int64_t)F);
   G.nmap = 2;
-  G.wmaps[0] = &h->maps[l].tg;
-  G.wmaps[1] = &h->maps[l].tu;
+  G.wmaps[0] = G.bn == 128 ? &h->maps[l].wg : &h->maps[l].tg;   // gate / up boxes of bn / 2 rows
+  G.wmaps[1] = G.bn == 128 ? &h->maps[l].wu : &h->maps[l].tu;
   G.nseg = 1;
-  G.seg[0] = make_seg(0, F / 128, SK_SWIGLU, 0, F, f.a, F);
+  G.seg[0] = make_seg(0, F / (G.bn / 2), SK_SWIGLU, 0, F, f.a, F);
   G.seg[0].map2 = 1;
   G.nsrc = 1;
   G.a_src[0] = f.h;
@@ -438,10 +449,11 @@ static int mlp_tc(dflash_handle* h, cudaStream_t s, int l, Fwd& f, int64_t R) {
   G.M = (int)R;
   if ((rc = tc_gemm(h, s, DFLASH_K_WEIGHT_GEMM, G))) return rc;
   WLaunch Dn;
+  Dn.bn = tc_width(h, R, D);
   Dn.nmap = 1;
-  Dn.wmaps[0] = &h->maps[l].td;
+  Dn.wmaps[0] = Dn.bn == 128 ? &h->maps[l].wd : &h->maps[l].td;
   Dn.nseg = 1;
-  Dn.seg[0] = make_seg(0, D / 256, SK_RESID, 0, D, f.x, D);
+  Dn.seg[0] = make_seg(0, D / Dn.bn, SK_RESID, 0, D, f.x, D);
   Dn.nsrc = 1;
   Dn.a_src[0] = f.a;
   Dn.a_ld = F;

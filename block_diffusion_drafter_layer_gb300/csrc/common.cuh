@@ -210,6 +210,7 @@ struct WLaunch {
   float* gap = nullptr;
   int rps_out = 0;
   const int32_t* anchor = nullptr;
+  int bn = 256;         // tcgen05 kernel: output tile width (segment tiles and weight boxes match it)
 };
 
 // 2-D TMA descriptor with the 128-byte swizzle (box_inner x element size must

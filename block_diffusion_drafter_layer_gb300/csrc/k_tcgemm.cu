@@ -2,11 +2,13 @@
 //
 // Used where a projection multiplies many rows (the context prefill: fusing
 // and injecting thousands of target positions at once), so the work is a
-// dense contraction.  One CTA computes a 128-row x 256-column output tile:
+// dense contraction.  One CTA computes a 128-row x BN-column output tile
+// (BN = 256, or 128 where 256-column tiles would leave most SMs idle):
 //   warp 0    one lane streams 64-wide K slices of the activations (A, 16 KB)
-//             and of the weight (B, 32 KB) with TMA into a 4-deep ring;
-//   warp 1    allocates the 256-column TMEM accumulator; one lane issues
-//             tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate) and
+//             and of the weight (B, BN x 128 B) with TMA into a 4-deep
+//             (BN = 256) or 6-deep (BN = 128) ring;
+//   warp 1    allocates the BN-column TMEM accumulator; one lane issues
+//             tcgen05.mma (M=128, N=BN, K=16, bf16 in, fp32 accumulate) and
 //             releases each ring stage with tcgen05.commit;
 //   warps 2-5 wait for the final commit, read their 32-lane quarter of the
 //             accumulator with tcgen05.ld and run the epilogue: fp32 store,
@@ -24,23 +26,42 @@ namespace dflash {
 
 using namespace ptx;
 
-constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
+// Tile order.  With few row tiles (a block of drafted rows: 4 at batch 32 x
+// B 16) consecutive CTAs take the row tiles of one weight column tile, so
+// each weight tile is read from HBM once (column-first order re-read the
+// 1.2 GB LM head from HBM once per row tile: 817 -> 560 us at 480 rows);
+// with many (a long
+// prefix) consecutive CTAs share a row tile of activations instead, which
+// measured faster there.  0 keeps column-first order everywhere.
+#ifndef DFLASH_TC_MFAST
+#define DFLASH_TC_MFAST 1
+#endif
+
+constexpr int TC_BM = 128, TC_BK = 64;
 constexpr int TC_THREADS = 192;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;   // 16 KB
-constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;   // 32 KB
-constexpr int TC_STAGE_TX = TC_A_BYTES + TC_B_BYTES;
-constexpr int TC_OFF_B = TC_STAGES * TC_A_BYTES;
-constexpr int TC_OFF_GUARD = TC_OFF_B + TC_STAGES * TC_B_BYTES;
-constexpr int TC_GUARD = 16384;                 // slack after the ring
-constexpr int TC_OFF_BAR = TC_OFF_GUARD + TC_GUARD;
-constexpr int TC_SMEM = TC_OFF_BAR + 128 + 1024;
-constexpr uint32_t TC_TMEM_COLS = 256;
+
+// Shared-memory layout of the ring for a BN-column tile.
+template <int BN>
+struct TcCfg {
+  static_assert(BN == 128 || BN == 256, "tile width");
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int B_BYTES = BN * TC_BK * 2;   // 32 KB or 16 KB
+  static constexpr int STAGE_TX = TC_A_BYTES + B_BYTES;
+  static constexpr int OFF_B = STAGES * TC_A_BYTES;
+  static constexpr int OFF_GUARD = OFF_B + STAGES * B_BYTES;
+  static constexpr int GUARD = 16384;              // slack after the ring
+  static constexpr int OFF_BAR = OFF_GUARD + GUARD;
+  static constexpr int SMEM = OFF_BAR + 8 * (2 * STAGES + 1) + 64 + 1024;
+  static constexpr uint32_t TMEM_COLS = BN;
+};
+static_assert(TcCfg<256>::SMEM <= 232448 && TcCfg<128>::SMEM <= 232448, "shared memory per CTA");
 
 struct TcParams {
   CUtensorMap amap[WS_MAXSRC];
   CUtensorMap bmap[WS_MAXMAP];
   WSeg seg[WS_MAXMAP];
-  int nseg, M, K, kc_per_src, n_mtiles, n_ntiles;
+  int nseg, M, K, kc_per_src, n_mtiles, n_ntiles, m_fast;
   RowMap rm;
   const int32_t* len;
   const float2* rope_tab;
@@ -116,7 +137,12 @@ __device__ __forceinline__ int tc_seg_of(const TcParams& p, int t) {
   return s;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using C = TcCfg<BN>;
+  constexpr int TC_BN = BN, TC_STAGES = C::STAGES, TC_B_BYTES = C::B_BYTES;
+  constexpr int TC_STAGE_TX = C::STAGE_TX, TC_OFF_B = C::OFF_B, TC_OFF_BAR = C::OFF_BAR;
+  constexpr uint32_t TC_TMEM_COLS = C::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
@@ -125,7 +151,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
   volatile uint32_t* tmem_slot = (volatile uint32_t*)(smem + TC_OFF_BAR + 8 * (2 * TC_STAGES + 1));
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x / p.n_ntiles, nt = blockIdx.x - mt * p.n_ntiles;
+  // m_fast: the row tiles that share a weight column tile run side by side,
+  // so the column comes from HBM once and from L2 for the others
+  const int mt = p.m_fast ? blockIdx.x % p.n_mtiles : blockIdx.x / p.n_ntiles;
+  const int nt = p.m_fast ? blockIdx.x / p.n_mtiles : blockIdx.x - mt * p.n_ntiles;
   const int nk = p.K / TC_BK;
 
   if (threadIdx.x == 0) {
@@ -420,7 +449,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 
 // ---------------------------------------------------------------------------
 int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float4* amx) {
-  if (L.M < 1 || L.K % TC_BK != 0 || L.nseg < 1 || L.nseg > WS_MAXMAP || L.nsrc < 1 ||
+  if ((L.bn != 128 && L.bn != 256) || L.M < 1 || L.K % TC_BK != 0 || L.nseg < 1 || L.nseg > WS_MAXMAP || L.nsrc < 1 ||
       L.nsrc > WS_MAXSRC || (L.K / TC_BK) % L.nsrc != 0)
     return DFLASH_ERR_SHAPE;
   for (int i = 0; i < L.nseg; ++i)
@@ -440,6 +469,7 @@ int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
   prm.kc_per_src = kc_per_src;
   prm.n_ntiles = L.seg[L.nseg - 1].t1;
   prm.n_mtiles = (L.M + TC_BM - 1) / TC_BM;
+  prm.m_fast = DFLASH_TC_MFAST && prm.n_mtiles * 8 <= h->num_sms;
   prm.rm = L.rm;
   prm.len = L.len;
   prm.rope_tab = h->d_rope;
@@ -455,17 +485,19 @@ int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
   const int64_t tiles = (int64_t)prm.n_mtiles * prm.n_ntiles;
   if (L.seg[0].kind == SK_ARGMAX && (prm.n_mtiles > kMaxTiles || !amx)) return DFLASH_ERR_SHAPE;
   if (tiles > 0x7fffffff) return DFLASH_ERR_SHAPE;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TC_SMEM) != cudaSuccess)
+  static bool attr_set[2] = {false, false};
+  const int bi = L.bn == 128 ? 1 : 0;
+  auto kern = bi ? tc_gemm_kernel<128> : tc_gemm_kernel<256>;
+  const int smem = bi ? TcCfg<128>::SMEM : TcCfg<256>::SMEM;
+  if (!attr_set[bi]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return DFLASH_ERR_CUDA;
-    attr_set = true;
+    attr_set[bi] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)tiles);
   cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = TC_SMEM;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -474,7 +506,7 @@ int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
   cfg.numAttrs = 1;
   Timer t;
   launch_begin(h, kclass, s, &t);
-  cudaLaunchKernelEx(&cfg, tc_gemm_kernel, prm);
+  cudaLaunchKernelEx(&cfg, kern, prm);
   return launch_end(h, s, &t);
 }
 

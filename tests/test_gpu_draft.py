@@ -175,6 +175,16 @@ def test_draft_qwen3_8b_batch32_ragged(dfl):
     _random_cache_case(dfl, w, w.B, lens, sample)
 
 
+def test_draft_35b_batch8_narrow_tiles(dfl):
+    """35B-A3B-shaped draft, 8 sequences x 16 rows = 128 rows: every layer
+    projection runs on the tensor-core kernel with 128-column tiles (the
+    head-norm + RoPE, SwiGLU and residual epilogues at that width)."""
+    w = synth.with_(synth.WORKLOADS["qwen35_a3b_32k"], batch=8)
+    lens = [int(x) for x in np.random.default_rng(8).integers(1, 1500, 8)]
+    lens[5] = 0
+    _random_cache_case(dfl, w, w.B, lens, np.array([2, 5]))
+
+
 @pytest.mark.parametrize("B", [8, 16])
 def test_draft_long_context_32k(dfl, B):
     w = synth.WORKLOADS["qwen35_a3b_32k"]
