@@ -381,6 +381,10 @@ def main():
     ap.add_argument("--trace", action="store_true",
                     help="print the persistent kernel's per-phase timeline of one step "
                          "(a table, not the JSON line) and exit")
+    ap.add_argument("--lm-head", type=int, default=0, metavar="ROWS",
+                    help="time the LM head + argmax alone on ROWS rows of the workload's "
+                         "shape (a one-layer draft, so a profiler capture stays small), "
+                         "print one line and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -398,10 +402,47 @@ def main():
             if rank == 0:
                 run_trace(args)
             return
+        if args.lm_head > 0:
+            if rank == 0:
+                run_lm_head(args)
+            return
         run_ours(args, rank, world, local)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()
+
+
+def run_lm_head(args):
+    """CUDA-event time of one LM head + argmax call (final RMSNorm, the
+    vocabulary projection and the per-row top-2) on args.lm_head rows."""
+    import dataclasses
+    import block_diffusion_drafter_layer_gb300 as dfl
+    from synth.gpu import draft_model
+    w = synth.WORKLOADS[args.workload]
+    s = dataclasses.replace(w.draft, n_layers=1)
+    weights = synth.draft_weights(s, w.dtype, w.seed, device="cuda")
+    m = draft_model(s, w.dtype, weights, max_pos=64)
+    rows = args.lm_head
+    x = torch.randn(rows, s.D, device="cuda", generator=torch.Generator("cuda").manual_seed(w.seed))
+    ids = torch.empty(rows, dtype=torch.int32, device="cuda")
+    gap = torch.empty(rows, device="cuda")
+    ws = m.workspace(rows)
+    for _ in range(args.warmup):
+        dfl.dflash_lm_head_argmax(m.handle, x, rows, weights["g_f"], ids, gap, ws)
+    torch.cuda.synchronize()
+    if dfl.dflash_get_status(m.handle) != 0:
+        raise RuntimeError("device status %d" % dfl.dflash_get_status(m.handle))
+    st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    st.record()
+    for _ in range(args.steps):
+        dfl.dflash_lm_head_argmax(m.handle, x, rows, weights["g_f"], ids, gap, ws)
+    en.record()
+    torch.cuda.synchronize()
+    us = st.elapsed_time(en) / args.steps * 1000
+    flops = 2.0 * rows * s.V * s.D
+    print(json.dumps({"lm_head_rows": rows, "workload": w.name, "us_per_call": round(us, 2),
+                      "tflops": round(flops / us / 1e6, 1)}))
+    m.close()
 
 
 PHASE_NAMES = ("q/k/v", "q/k/v reduce", "attention", "combine", "o_proj", "o_proj reduce",
