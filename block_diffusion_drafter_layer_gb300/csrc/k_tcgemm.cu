@@ -2,16 +2,17 @@
 //
 // Used where a projection multiplies many rows (the context prefill: fusing
 // and injecting thousands of target positions at once), so the work is a
-// dense contraction.  One CTA computes a 128-row x BN-column output tile
+// dense contraction.  One CTA per SM walks 128-row x BN-column output tiles
 // (BN = 256, or 128 where 256-column tiles would leave most SMs idle):
 //   warp 0    one lane streams 64-wide K slices of the activations (A, 16 KB)
 //             and of the weight (B, BN x 128 B) with TMA into a 4-deep
 //             (BN = 256) or 6-deep (BN = 128) ring;
-//   warp 1    allocates the BN-column TMEM accumulator; one lane issues
-//             tcgen05.mma (M=128, N=BN, K=16, bf16 in, fp32 accumulate) and
-//             releases each ring stage with tcgen05.commit;
-//   warps 2-5 wait for the final commit, read their 32-lane quarter of the
-//             accumulator with tcgen05.ld and run the epilogue: fp32 store,
+//   warp 1    allocates two BN-column TMEM accumulators; one lane issues
+//             tcgen05.mma (M=128, N=BN, K=16, bf16 in, fp32 accumulate) into
+//             the tile's buffer, releases each ring stage with tcgen05.commit
+//             and commits the buffer after the tile's last K slice;
+//   warps 2-5 wait for a buffer's commit, read their 32-lane quarter with
+//             tcgen05.ld, release the buffer and run the epilogue: fp32 store,
 //             residual add, SwiGLU (gate and up rows paired in one tile),
 //             per-head RMSNorm + RoPE + store (dense or into a K/V cache), or a
 //             per-row top-2 whose last column tile merges the vocabulary.
@@ -52,8 +53,8 @@ struct TcCfg {
   static constexpr int OFF_GUARD = OFF_B + STAGES * B_BYTES;
   static constexpr int GUARD = 16384;              // slack after the ring
   static constexpr int OFF_BAR = OFF_GUARD + GUARD;
-  static constexpr int SMEM = OFF_BAR + 8 * (2 * STAGES + 1) + 64 + 1024;
-  static constexpr uint32_t TMEM_COLS = BN;
+  static constexpr int SMEM = OFF_BAR + 8 * (2 * STAGES + 4) + 64 + 1024;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;   // two accumulators
 };
 static_assert(TcCfg<256>::SMEM <= 232448 && TcCfg<128>::SMEM <= 232448, "shared memory per CTA");
 
@@ -137,33 +138,231 @@ __device__ __forceinline__ int tc_seg_of(const TcParams& p, int t) {
   return s;
 }
 
+// Epilogue of one output tile for the row this thread owns; trow addresses
+// the row's TMEM lane in the tile's accumulator.
+template <int BN>
+__device__ __forceinline__ void tc_tile_epilogue(const TcParams& p, const WSeg& g, int lt, int nt,
+                                                 int row, uint32_t trow) {
+  constexpr int TC_BN = BN;
+  if (g.kind == SK_F32) {
+    float* dst = (float*)g.dst;
+    for (int c = 0; c < TC_BN / 32; ++c) {
+      float v[32];
+      tc_ld32(trow + c * 32, v);
+      const int n = lt * TC_BN + c * 32;
+      if (row < p.M && n < g.n_valid) {
+        float4* o = (float4*)(dst + (int64_t)row * g.ld + n);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+    }
+  } else if (g.kind == SK_RESID) {
+    float* dst = (float*)g.dst;
+    for (int c = 0; c < TC_BN / 32; ++c) {
+      float v[32];
+      tc_ld32(trow + c * 32, v);
+      const int n = lt * TC_BN + c * 32;
+      if (row < p.M && n < g.n_valid) {
+        float4* o = (float4*)(dst + (int64_t)row * g.ld + n);
+        float4 old[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) old[i] = o[i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          o[i] = make_float4(old[i].x + v[4 * i], old[i].y + v[4 * i + 1], old[i].z + v[4 * i + 2],
+                             old[i].w + v[4 * i + 3]);
+      }
+    }
+  } else if (g.kind == SK_SWIGLU) {
+    bf16* dst = (bf16*)g.dst;
+    for (int c = 0; c < TC_BN / 64; ++c) {
+      float gv[32], uv[32];
+      tc_ld32(trow + c * 32, gv);
+      tc_ld32(trow + TC_BN / 2 + c * 32, uv);
+      const int f = lt * (TC_BN / 2) + c * 32;
+      if (row < p.M && f < g.n_valid) {
+        uint4* o = (uint4*)(dst + (int64_t)row * g.ld + f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float a[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float x = gv[8 * i + k];
+            a[k] = x / (1.0f + expf(-x)) * uv[8 * i + k];
+          }
+          __nv_bfloat162 t0 = __floats2bfloat162_rn(a[0], a[1]);
+          __nv_bfloat162 t1 = __floats2bfloat162_rn(a[2], a[3]);
+          __nv_bfloat162 t2 = __floats2bfloat162_rn(a[4], a[5]);
+          __nv_bfloat162 t3 = __floats2bfloat162_rn(a[6], a[7]);
+          uint4 w;
+          w.x = *reinterpret_cast<uint32_t*>(&t0);
+          w.y = *reinterpret_cast<uint32_t*>(&t1);
+          w.z = *reinterpret_cast<uint32_t*>(&t2);
+          w.w = *reinterpret_cast<uint32_t*>(&t3);
+          o[i] = w;
+        }
+      }
+    }
+  } else if (g.kind == SK_ARGMAX) {
+    // top-2 of this row over the tile's columns (lowest index on ties)
+    float t1 = -INFINITY, t2 = -INFINITY;
+    int i1 = 0x7fffffff;
+    for (int c = 0; c < TC_BN / 32; ++c) {
+      float v[32];
+      tc_ld32(trow + c * 32, v);
+      const int n0 = lt * TC_BN + c * 32;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        if (n0 + k >= g.n_valid) break;
+        const float x = v[k];
+        if (x > t1) {
+          t2 = t1;
+          t1 = x;
+          i1 = n0 + k;
+        } else if (x > t2) {
+          t2 = x;
+        }
+      }
+    }
+    if (row < p.M) p.amx[(int64_t)nt * p.M + row] = make_float4(t1, __int_as_float(i1), t2, 0.f);
+  } else if (g.kind == SK_HEAD && g.d == 128) {
+    int b = -1, i = 0;
+    const bool mapped = row < p.M && p.rm.map(row, b, i);
+    const int pos = mapped ? p.len[b] + i : -1;
+    for (int hh = 0; hh < TC_BN / 128; ++hh) {
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc_ld32(trow + hh * 128 + c * 32, x + 32 * c);
+      if (!mapped) continue;
+      const int head = lt * (TC_BN / 128) + hh;
+      if (g.gain != nullptr) {
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 128; ++e) ss += x[e] * x[e];
+        const float rinv = 1.0f / sqrtf(ss / 128.0f + p.eps);
+#pragma unroll
+        for (int e = 0; e < 128; ++e) x[e] = x[e] * rinv * g.gain[e];
+      }
+      if (g.rope) {
+        if (pos < 0 || pos >= p.max_pos) {
+          atomicOr(p.status, ST_BOUNDS);
+          continue;
+        }
+        const float2* cs = p.rope_tab + (int64_t)pos * 64;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const float2 t = cs[e];
+          const float y1 = x[e] * t.x - x[e + 64] * t.y;
+          const float y2 = x[e + 64] * t.x + x[e] * t.y;
+          x[e] = y1;
+          x[e + 64] = y2;
+        }
+      }
+      bf16* o;
+      if (g.cache_cap > 0) {
+        if (b >= g.cache_batch || pos < 0 || pos >= g.cache_cap) {
+          atomicOr(p.status, ST_CAPACITY);
+          continue;
+        }
+        o = (bf16*)g.dst + (((int64_t)b * g.cache_heads + head) * g.cache_cap + pos) * 128;
+      } else {
+        o = (bf16*)g.dst + (int64_t)row * g.ld + (int64_t)head * 128;
+      }
+#pragma unroll
+      for (int e = 0; e < 128; e += 8) {
+        uint4 w;
+        __nv_bfloat162 t0 = __floats2bfloat162_rn(x[e], x[e + 1]);
+        __nv_bfloat162 t1 = __floats2bfloat162_rn(x[e + 2], x[e + 3]);
+        __nv_bfloat162 t2 = __floats2bfloat162_rn(x[e + 4], x[e + 5]);
+        __nv_bfloat162 t3 = __floats2bfloat162_rn(x[e + 6], x[e + 7]);
+        w.x = *reinterpret_cast<uint32_t*>(&t0);
+        w.y = *reinterpret_cast<uint32_t*>(&t1);
+        w.z = *reinterpret_cast<uint32_t*>(&t2);
+        w.w = *reinterpret_cast<uint32_t*>(&t3);
+        *reinterpret_cast<uint4*>(o + e) = w;
+      }
+    }
+  }
+}
+
+// Top-2 of one row over every column tile's record, in column-tile order
+// (lowest index on ties), written as the row's draft id and top-2 gap.
+__device__ __forceinline__ void tc_merge_row(const TcParams& p, int row) {
+  float t1 = -INFINITY, t2 = -INFINITY;
+  int i1 = 0x7fffffff;
+  for (int n0 = 0; n0 < p.n_ntiles; n0 += 8) {
+    float4 rec[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      rec[k] = (n0 + k < p.n_ntiles) ? __ldcg(&p.amx[(int64_t)(n0 + k) * p.M + row])
+                                     : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY, 0.f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float a1 = rec[k].x, a2 = rec[k].z;
+      const int ai = __float_as_int(rec[k].y);
+      const float lo = fminf(t1, a1);
+      if (a1 > t1 || (a1 == t1 && ai < i1)) {
+        t1 = a1;
+        i1 = ai;
+      }
+      t2 = fmaxf(lo, fmaxf(t2, a2));
+    }
+  }
+  int64_t out = row, gout = row;
+  if (p.rps_out > 0) {
+    const int per = p.rps_out - 1;
+    const int64_t b = row / per, i = row % per + 1;
+    out = b * p.rps_out + i;
+    gout = b * per + (i - 1);
+    if (i == 1) p.ids[b * p.rps_out] = p.anchor[b];
+  }
+  p.ids[out] = i1;
+  if (p.gap) p.gap[gout] = t1 - t2;
+}
+
+// Persistent: CTA c takes tiles c, c + grid, ... in launch order; the ring
+// runs on across its tiles and two TMEM accumulators let the epilogue of
+// one tile overlap the MMAs of the next.
 template <int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<BN>;
-  constexpr int TC_BN = BN, TC_STAGES = C::STAGES, TC_B_BYTES = C::B_BYTES;
+  constexpr int TC_STAGES = C::STAGES, TC_B_BYTES = C::B_BYTES;
   constexpr int TC_STAGE_TX = C::STAGE_TX, TC_OFF_B = C::OFF_B, TC_OFF_BAR = C::OFF_BAR;
   constexpr uint32_t TC_TMEM_COLS = C::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
+  // ring full / empty per stage; accumulator full (MMA commit) / empty (the
+  // four epilogue warps) per TMEM buffer
   const uint32_t bar_full = sbase + TC_OFF_BAR, bar_empty = bar_full + 8 * TC_STAGES,
-                 bar_done = bar_empty + 8 * TC_STAGES;
-  volatile uint32_t* tmem_slot = (volatile uint32_t*)(smem + TC_OFF_BAR + 8 * (2 * TC_STAGES + 1));
+                 bar_tfull = bar_empty + 8 * TC_STAGES, bar_tempty = bar_tfull + 16;
+  volatile uint32_t* tmem_slot = (volatile uint32_t*)(smem + TC_OFF_BAR + 8 * (2 * TC_STAGES + 4));
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  volatile int* last_flag = (volatile int*)(tmem_slot + 2);
+  volatile int* kcount = (volatile int*)(tmem_slot + 3);   // k-blocks issued, consumed
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = p.K / TC_BK;
+  const int tiles = p.n_mtiles * p.n_ntiles;
+  const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   // m_fast: the row tiles that share a weight column tile run side by side,
   // so the column comes from HBM once and from L2 for the others
-  const int mt = p.m_fast ? blockIdx.x % p.n_mtiles : blockIdx.x / p.n_ntiles;
-  const int nt = p.m_fast ? blockIdx.x / p.n_mtiles : blockIdx.x - mt * p.n_ntiles;
-  const int nk = p.K / TC_BK;
+  auto tile_of = [&](int j, int& mt, int& nt) {
+    const int t = (int)blockIdx.x + j * (int)gridDim.x;
+    mt = p.m_fast ? t % p.n_mtiles : t / p.n_ntiles;
+    nt = p.m_fast ? t / p.n_mtiles : t - mt * p.n_ntiles;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < TC_STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_tfull + 8 * b, 1);
+      mbar_init(bar_tempty + 8 * b, 4);
+    }
     *abort_flag = 0;
+    kcount[0] = kcount[1] = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -179,265 +378,136 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) pdl_launch_dependents();
 
-  const WSeg& g = p.seg[tc_seg_of(p, nt)];
-  const int lt = nt - g.t0;
-
   if (warp == 0) {
     if (lane == 0) {
       // ---- producer -------------------------------------------------------------
       const uint64_t pol_w = policy_evict_last(), pol_a = policy_evict_last();
       pdl_wait();
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % TC_STAGES, use = kb / TC_STAGES;
-        if (use > 0 && !mbar_wait(bar_empty + 8 * s, (use - 1) & 1)) {
-          atomicOr(p.status, ST_TIMEOUT);
-          *abort_flag = 1;
-          break;
-        }
-        if (*abort_flag) break;
-        mbar_arrive_expect_tx(bar_full + 8 * s, TC_STAGE_TX);
-        const int src = kb / p.kc_per_src, lk = kb - src * p.kc_per_src;
-        tma_load_2d(sbase + s * TC_A_BYTES, &p.amap[src], bar_full + 8 * s, lk * TC_BK,
-                    mt * TC_BM, pol_a);
-        if (g.kind == SK_SWIGLU) {   // 128 gate rows then the same 128 up rows
-          tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES, &p.bmap[g.map], bar_full + 8 * s,
-                      kb * TC_BK, lt * (TC_BN / 2), pol_w);
-          tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES + TC_B_BYTES / 2, &p.bmap[g.map2],
-                      bar_full + 8 * s, kb * TC_BK, lt * (TC_BN / 2), pol_w);
-        } else {
-          tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES, &p.bmap[g.map], bar_full + 8 * s,
-                      kb * TC_BK, lt * TC_BN, pol_w);
+      int kg = 0;   // k-blocks issued over this CTA's tiles
+      for (int j = 0; j < my_tiles && !*abort_flag; ++j) {
+        int mt, nt;
+        tile_of(j, mt, nt);
+        const WSeg& g = p.seg[tc_seg_of(p, nt)];
+        const int lt = nt - g.t0;
+        for (int kb = 0; kb < nk; ++kb, ++kg) {
+          const int s = kg % TC_STAGES, use = kg / TC_STAGES;
+          if (use > 0 && !mbar_wait(bar_empty + 8 * s, (use - 1) & 1)) {
+            atomicOr(p.status, ST_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          if (*abort_flag) break;
+          mbar_arrive_expect_tx(bar_full + 8 * s, TC_STAGE_TX);
+          const int src = kb / p.kc_per_src, lk = kb - src * p.kc_per_src;
+          tma_load_2d(sbase + s * TC_A_BYTES, &p.amap[src], bar_full + 8 * s, lk * TC_BK,
+                      mt * TC_BM, pol_a);
+          if (g.kind == SK_SWIGLU) {   // BN/2 gate rows then the same BN/2 up rows
+            tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES, &p.bmap[g.map], bar_full + 8 * s,
+                        kb * TC_BK, lt * (BN / 2), pol_w);
+            tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES + TC_B_BYTES / 2, &p.bmap[g.map2],
+                        bar_full + 8 * s, kb * TC_BK, lt * (BN / 2), pol_w);
+          } else {
+            tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES, &p.bmap[g.map], bar_full + 8 * s,
+                        kb * TC_BK, lt * BN, pol_w);
+          }
         }
       }
+      kcount[0] = kg;
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer ---------------------------------------------------------------
-      const uint32_t idesc = idesc_bf16_f32(TC_BM, TC_BN);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % TC_STAGES, use = kb / TC_STAGES;
-        if (*abort_flag || !mbar_wait(bar_full + 8 * s, use & 1)) {
+      // ---- MMA issuer: tile j accumulates into TMEM buffer j & 1 -----------------
+      const uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
+      int kg = 0;   // k-blocks consumed
+      for (int j = 0; j < my_tiles; ++j) {
+        const int b = j & 1, ub = j >> 1;
+        if (*abort_flag) break;
+        // the epilogue of tile j - 2 has read this buffer
+        if (ub > 0 && !mbar_wait(bar_tempty + 8 * b, (ub - 1) & 1)) {
           atomicOr(p.status, ST_TIMEOUT);
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = sbase + s * TC_A_BYTES, b0 = sbase + TC_OFF_B + s * TC_B_BYTES;
+        const uint32_t acc = tmem + (uint32_t)(b * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++kg) {
+          const int s = kg % TC_STAGES, use = kg / TC_STAGES;
+          if (*abort_flag || !mbar_wait(bar_full + 8 * s, use & 1)) {
+            atomicOr(p.status, ST_TIMEOUT);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sbase + s * TC_A_BYTES, b0 = sbase + TC_OFF_B + s * TC_B_BYTES;
 #pragma unroll
-        for (int j = 0; j < TC_BK / 16; ++j)
-          tc_mma(tmem, sdesc_sw128(a0 + j * 32), sdesc_sw128(b0 + j * 32), idesc,
-                 (kb > 0 || j > 0) ? 1u : 0u);
-        tc_commit(bar_empty + 8 * s);
+          for (int jj = 0; jj < TC_BK / 16; ++jj)
+            tc_mma(acc, sdesc_sw128(a0 + jj * 32), sdesc_sw128(b0 + jj * 32), idesc,
+                   (kb > 0 || jj > 0) ? 1u : 0u);
+          tc_commit(bar_empty + 8 * s);
+        }
+        if (!ok) break;
+        tc_commit(bar_tfull + 8 * b);
       }
-      tc_commit(bar_done);
+      kcount[1] = kg;
     }
     __syncwarp();
   } else {
     // ---- epilogue: warps 2-5, TMEM lane quarter (warp % 4) -----------------------
+    // Every warp walks all of the CTA's tiles (after an abort without waiting),
+    // so the four warps always meet at the same named barriers.
     pdl_wait();                                     // cache lengths come from earlier kernels
     const int q = warp & 3;
     const int r = q * 32 + lane;                    // row within the tile
-    const int row = mt * TC_BM + r;
-    const bool ok = mbar_wait(bar_done, 0, 4000000000ull) && !(*abort_flag & 1);
-    tc_fence_after();
-    if (ok) {
-      const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
-      if (g.kind == SK_F32) {
-        float* dst = (float*)g.dst;
-        for (int c = 0; c < TC_BN / 32; ++c) {
-          float v[32];
-          tc_ld32(trow + c * 32, v);
-          const int n = lt * TC_BN + c * 32;
-          if (row < p.M && n < g.n_valid) {
-            float4* o = (float4*)(dst + (int64_t)row * g.ld + n);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-          }
-        }
-      } else if (g.kind == SK_RESID) {
-        float* dst = (float*)g.dst;
-        for (int c = 0; c < TC_BN / 32; ++c) {
-          float v[32];
-          tc_ld32(trow + c * 32, v);
-          const int n = lt * TC_BN + c * 32;
-          if (row < p.M && n < g.n_valid) {
-            float4* o = (float4*)(dst + (int64_t)row * g.ld + n);
-            float4 old[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) old[i] = o[i];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[i] = make_float4(old[i].x + v[4 * i], old[i].y + v[4 * i + 1], old[i].z + v[4 * i + 2],
-                                 old[i].w + v[4 * i + 3]);
-          }
-        }
-      } else if (g.kind == SK_SWIGLU) {
-        bf16* dst = (bf16*)g.dst;
-        for (int c = 0; c < TC_BN / 64; ++c) {
-          float gv[32], uv[32];
-          tc_ld32(trow + c * 32, gv);
-          tc_ld32(trow + TC_BN / 2 + c * 32, uv);
-          const int f = lt * (TC_BN / 2) + c * 32;
-          if (row < p.M && f < g.n_valid) {
-            uint4* o = (uint4*)(dst + (int64_t)row * g.ld + f);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float a[8];
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const float x = gv[8 * i + k];
-                a[k] = x / (1.0f + expf(-x)) * uv[8 * i + k];
-              }
-              __nv_bfloat162 t0 = __floats2bfloat162_rn(a[0], a[1]);
-              __nv_bfloat162 t1 = __floats2bfloat162_rn(a[2], a[3]);
-              __nv_bfloat162 t2 = __floats2bfloat162_rn(a[4], a[5]);
-              __nv_bfloat162 t3 = __floats2bfloat162_rn(a[6], a[7]);
-              uint4 w;
-              w.x = *reinterpret_cast<uint32_t*>(&t0);
-              w.y = *reinterpret_cast<uint32_t*>(&t1);
-              w.z = *reinterpret_cast<uint32_t*>(&t2);
-              w.w = *reinterpret_cast<uint32_t*>(&t3);
-              o[i] = w;
-            }
-          }
-        }
-      } else if (g.kind == SK_ARGMAX) {
-        // top-2 of this row over the tile's columns (lowest index on ties)
-        float t1 = -INFINITY, t2 = -INFINITY;
-        int i1 = 0x7fffffff;
-        for (int c = 0; c < TC_BN / 32; ++c) {
-          float v[32];
-          tc_ld32(trow + c * 32, v);
-          const int n0 = lt * TC_BN + c * 32;
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            if (n0 + k >= g.n_valid) break;
-            const float x = v[k];
-            if (x > t1) {
-              t2 = t1;
-              t1 = x;
-              i1 = n0 + k;
-            } else if (x > t2) {
-              t2 = x;
-            }
-          }
-        }
-        if (row < p.M) p.amx[(int64_t)nt * p.M + row] = make_float4(t1, __int_as_float(i1), t2, 0.f);
-      } else if (g.kind == SK_HEAD && g.d == 128) {
-        int b = -1, i = 0;
-        const bool mapped = row < p.M && p.rm.map(row, b, i);
-        const int pos = mapped ? p.len[b] + i : -1;
-        for (int hh = 0; hh < TC_BN / 128; ++hh) {
-          float x[128];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tc_ld32(trow + hh * 128 + c * 32, x + 32 * c);
-          if (!mapped) continue;
-          const int head = lt * (TC_BN / 128) + hh;
-          if (g.gain != nullptr) {
-            float ss = 0.f;
-#pragma unroll
-            for (int e = 0; e < 128; ++e) ss += x[e] * x[e];
-            const float rinv = 1.0f / sqrtf(ss / 128.0f + p.eps);
-#pragma unroll
-            for (int e = 0; e < 128; ++e) x[e] = x[e] * rinv * g.gain[e];
-          }
-          if (g.rope) {
-            if (pos < 0 || pos >= p.max_pos) {
-              atomicOr(p.status, ST_BOUNDS);
-              continue;
-            }
-            const float2* cs = p.rope_tab + (int64_t)pos * 64;
-#pragma unroll
-            for (int e = 0; e < 64; ++e) {
-              const float2 t = cs[e];
-              const float y1 = x[e] * t.x - x[e + 64] * t.y;
-              const float y2 = x[e + 64] * t.x + x[e] * t.y;
-              x[e] = y1;
-              x[e + 64] = y2;
-            }
-          }
-          bf16* o;
-          if (g.cache_cap > 0) {
-            if (b >= g.cache_batch || pos < 0 || pos >= g.cache_cap) {
-              atomicOr(p.status, ST_CAPACITY);
-              continue;
-            }
-            o = (bf16*)g.dst + (((int64_t)b * g.cache_heads + head) * g.cache_cap + pos) * 128;
-          } else {
-            o = (bf16*)g.dst + (int64_t)row * g.ld + (int64_t)head * 128;
-          }
-#pragma unroll
-          for (int e = 0; e < 128; e += 8) {
-            uint4 w;
-            __nv_bfloat162 t0 = __floats2bfloat162_rn(x[e], x[e + 1]);
-            __nv_bfloat162 t1 = __floats2bfloat162_rn(x[e + 2], x[e + 3]);
-            __nv_bfloat162 t2 = __floats2bfloat162_rn(x[e + 4], x[e + 5]);
-            __nv_bfloat162 t3 = __floats2bfloat162_rn(x[e + 6], x[e + 7]);
-            w.x = *reinterpret_cast<uint32_t*>(&t0);
-            w.y = *reinterpret_cast<uint32_t*>(&t1);
-            w.z = *reinterpret_cast<uint32_t*>(&t2);
-            w.w = *reinterpret_cast<uint32_t*>(&t3);
-            *reinterpret_cast<uint4*>(o + e) = w;
-          }
-        }
+    for (int j = 0; j < my_tiles; ++j) {
+      const int b = j & 1, ub = j >> 1;
+      int mt, nt;
+      tile_of(j, mt, nt);
+      const WSeg& g = p.seg[tc_seg_of(p, nt)];
+      const int lt = nt - g.t0;
+      const int row = mt * TC_BM + r;
+      const bool ok = !(*abort_flag & 1) && mbar_wait(bar_tfull + 8 * b, ub & 1, 4000000000ull);
+      if (!ok && !(*abort_flag & 1)) {
+        atomicOr(p.status, ST_TIMEOUT);
+        *abort_flag = 1;
       }
-    }
-  }
-  if (g.kind == SK_ARGMAX) {
-    // the CTA that finishes the last column tile of this row tile merges the
-    // records of its 128 rows over all column tiles, in column-tile order
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const int old = atomicAdd(&p.counters[mt], 1);
-      const int last = (old == p.n_ntiles - 1);
-      if (last) p.counters[mt] = 0;
-      *abort_flag = *abort_flag | (last ? 2 : 0);
-    }
-    __syncthreads();
-    if ((*abort_flag & 2) && warp >= 2) {
-      __threadfence();
-      const int r = (warp & 3) * 32 + lane, row = mt * TC_BM + r;
-      if (row < p.M) {
-        float t1 = -INFINITY, t2 = -INFINITY;
-        int i1 = 0x7fffffff;
-        for (int n0 = 0; n0 < p.n_ntiles; n0 += 8) {
-          float4 rec[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            rec[k] = (n0 + k < p.n_ntiles) ? __ldcg(&p.amx[(int64_t)(n0 + k) * p.M + row])
-                                           : make_float4(-INFINITY, __int_as_float(0x7fffffff), -INFINITY, 0.f);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float a1 = rec[k].x, a2 = rec[k].z;
-            const int ai = __float_as_int(rec[k].y);
-            const float lo = fminf(t1, a1);
-            if (a1 > t1 || (a1 == t1 && ai < i1)) {
-              t1 = a1;
-              i1 = ai;
-            }
-            t2 = fmaxf(lo, fmaxf(t2, a2));
-          }
+      tc_fence_after();
+      if (ok) tc_tile_epilogue<BN>(p, g, lt, nt, row, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty + 8 * b);
+      if (g.kind == SK_ARGMAX) {
+        // the CTA that finishes the last column tile of this row tile merges the
+        // records of its 128 rows over all column tiles
+        __threadfence();
+        named_bar(1, 128);
+        if (warp == 2 && lane == 0) {
+          const int old = atomicAdd(&p.counters[mt], 1);
+          const int last = (old == p.n_ntiles - 1);
+          if (last) p.counters[mt] = 0;
+          *last_flag = last;
         }
-        int64_t out = row, gout = row;
-        if (p.rps_out > 0) {
-          const int per = p.rps_out - 1;
-          const int64_t b = row / per, i = row % per + 1;
-          out = b * p.rps_out + i;
-          gout = b * per + (i - 1);
-          if (i == 1) p.ids[b * p.rps_out] = p.anchor[b];
+        named_bar(1, 128);
+        if (*last_flag) {
+          __threadfence();
+          if (row < p.M) tc_merge_row(p, row);
         }
-        p.ids[out] = i1;
-        if (p.gap) p.gap[gout] = t1 - t2;
+        named_bar(1, 128);   // the flag is read before the next tile rewrites it
       }
     }
   }
   tc_fence_before();
   __syncthreads();
   if ((*abort_flag & 1) && threadIdx.x == 0) {
-    // let any TMA loads still in flight land before the shared memory is released
-    for (int s = 0; s < TC_STAGES; ++s) mbar_wait(bar_full + 8 * s, 0, 20000000ull);
+    // let the TMA loads still in flight land and the issued MMAs finish before
+    // the shared memory and TMEM are released (each wait bounded)
+    const int issued = kcount[0], used = kcount[1];
+    for (int i = used; i < issued && i < used + TC_STAGES; ++i)
+      mbar_wait(bar_full + 8 * (i % TC_STAGES), (i / TC_STAGES) & 1, 20000000ull);
+    if (used > 0)
+      mbar_wait(bar_empty + 8 * ((used - 1) % TC_STAGES), ((used - 1) / TC_STAGES) & 1, 20000000ull);
   }
   if (warp == 1) {
     tc_fence_after();
@@ -495,7 +565,9 @@ int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
     attr_set[bi] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)tiles);
+  // persistent: one CTA per SM (its shared memory admits no second), each
+  // walking every grid-th tile
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(tiles, h->num_sms));
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
