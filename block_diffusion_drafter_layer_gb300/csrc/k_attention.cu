@@ -242,6 +242,20 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
     const bf16* vbb = p.vb + (int64_t)b * p.B * (p.G * DH) + (int64_t)g * DH;
     auto load_kv = [&](int k0, int stage) {
       const uint32_t dk = sK0 + stage * AT_KSUB * DH * 2, dv = sV0 + stage * AT_KSUB * DH * 2;
+      if (k0 + AT_KSUB <= min(L, k_end)) {
+        // all 64 keys in the cache: the same (row, chunk) pairs as below with
+        // the chunk fixed per thread and rows a constant stride apart
+        constexpr int RSTEP = AT_THREADS / CH;
+        const int c = tid % CH, r0 = tid / CH;
+        const bf16* ks = kcb + (int64_t)(k0 + r0) * DH + c * 8;
+        const bf16* vs = vcb + (int64_t)(k0 + r0) * DH + c * 8;
+#pragma unroll
+        for (int i = 0; i < AT_KSUB / RSTEP; ++i) {
+          cp_async16(dk + tile_off<DH>(r0 + i * RSTEP, c), ks + (int64_t)i * RSTEP * DH, true);
+          cp_async16(dv + tile_off<DH>(r0 + i * RSTEP, c), vs + (int64_t)i * RSTEP * DH, true);
+        }
+        return;
+      }
       for (int e = tid; e < AT_KSUB * CH; e += AT_THREADS) {
         const int r = e / CH, c = e - r * CH;
         const int j = k0 + r;
@@ -308,17 +322,30 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
             mma_bf16_16816(s[2 * pp + 1], qa[ks], b2, b3);
           }
         }
-        // online softmax over this sub-chunk (base-2 exponent, scale folded in)
+        // online softmax over this sub-chunk (base-2 exponent, scale folded in);
+        // plain: a bidirectional layer and all 64 keys inside the item, so
+        // every key is visible and the visibility tests drop out
+        const bool plain = !p.causal && p.window <= 0 && kbase + AT_KSUB <= k_end;
         float mnew[2] = {mrow[0], mrow[1]};
+        if (plain) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+          for (int j = 0; j < 8; ++j)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int key = kbase + j * 8 + 2 * tg + (q & 1);
-            const bool vis = key < k_end && key >= klo[q >> 1] && key < khi[q >> 1];
-            s[j][q] = vis ? s[j][q] * p.scale_log2 : -INFINITY;
-            mnew[q >> 1] = fmaxf(mnew[q >> 1], s[j][q]);
-          }
+            for (int q = 0; q < 4; ++q) {
+              s[j][q] *= p.scale_log2;
+              mnew[q >> 1] = fmaxf(mnew[q >> 1], s[j][q]);
+            }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int key = kbase + j * 8 + 2 * tg + (q & 1);
+              const bool vis = key < k_end && key >= klo[q >> 1] && key < khi[q >> 1];
+              s[j][q] = vis ? s[j][q] * p.scale_log2 : -INFINITY;
+              mnew[q >> 1] = fmaxf(mnew[q >> 1], s[j][q]);
+            }
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           mnew[h] = fmaxf(mnew[h], __shfl_xor_sync(0xffffffffu, mnew[h], 1));
@@ -332,7 +359,7 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             // a row may see no key of this item yet (masked layers): weight 0
-            const float e = mnew[q >> 1] == -INFINITY ? 0.f : exp2f(s[j][q] - mnew[q >> 1]);
+            const float e = (!plain && mnew[q >> 1] == -INFINITY) ? 0.f : exp2f(s[j][q] - mnew[q >> 1]);
             s[j][q] = e;
             lsum[q >> 1] += e;
           }
@@ -341,12 +368,15 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
           lrow[h] = lrow[h] * alpha[h] + lsum[h];
           mrow[h] = mnew[h];
         }
+        // once the running maxima settle alpha is exactly 1: skip the rescale
+        if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          acc[j][0] *= alpha[0];
-          acc[j][1] *= alpha[0];
-          acc[j][2] *= alpha[1];
-          acc[j][3] *= alpha[1];
+          for (int j = 0; j < NT; ++j) {
+            acc[j][0] *= alpha[0];
+            acc[j][1] *= alpha[0];
+            acc[j][2] *= alpha[1];
+            acc[j][3] *= alpha[1];
+          }
         }
         // O += P V with P rounded to bf16 (the row sum above keeps fp32 P)
 #pragma unroll
