@@ -290,11 +290,15 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
 
     for (int sc = 0; sc < nsub; ++sc) {
       const int stage = sc % AT_STAGES;
+      // groups 0 .. sc + AT_STAGES - 2 are committed: sub-chunk sc has landed
+      // once at most AT_STAGES - 2 remain in flight
+      cp_async_wait<AT_STAGES - 2>();
+      // all warps see sub-chunk sc and have finished sub-chunk sc - 1, whose
+      // stage the next prefetch overwrites
+      __syncthreads();
       const int pre = sc + AT_STAGES - 1;
       if (pre < nsub) load_kv(k_begin + pre * AT_KSUB, pre % AT_STAGES);
       cp_async_commit();
-      cp_async_wait<AT_STAGES - 1>();
-      __syncthreads();
       if (sc == 0 && active) {
 #pragma unroll
         for (int ks = 0; ks < DH / 16; ++ks) {
@@ -399,7 +403,6 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
           }
         }
       }
-      __syncthreads();
     }
     cp_async_wait<0>();
 
