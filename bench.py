@@ -333,7 +333,7 @@ def run_reference(args, rank, world):
     (the whole batch's rows are independent), scaled to blocks/s."""
     if rank != 0:
         return
-    w = synth.WORKLOADS[args.workload]
+    w = _workload(args)
     st = Draft(w, 0, 1, with_model=False)
     W, cK, cV, hid, anchors, post, start = oracle_inputs(st)
     del st
@@ -381,6 +381,8 @@ def main():
     ap.add_argument("--trace", action="store_true",
                     help="print the persistent kernel's per-phase timeline of one step "
                          "(a table, not the JSON line) and exit")
+    ap.add_argument("--ctx-len", type=int, default=0, metavar="L",
+                    help="replace the workload's context length (fixed-length workloads)")
     ap.add_argument("--lm-head", type=int, default=0, metavar="ROWS",
                     help="time the LM head + argmax alone on ROWS rows of the workload's "
                          "shape (a one-layer draft, so a profiler capture stays small), "
@@ -418,7 +420,7 @@ def run_lm_head(args):
     import dataclasses
     import block_diffusion_drafter_layer_gb300 as dfl
     from synth.gpu import draft_model
-    w = synth.WORKLOADS[args.workload]
+    w = _workload(args)
     s = dataclasses.replace(w.draft, n_layers=1)
     weights = synth.draft_weights(s, w.dtype, w.seed, device="cuda")
     m = draft_model(s, w.dtype, weights, max_pos=64)
@@ -452,7 +454,7 @@ PHASE_NAMES = ("q/k/v", "q/k/v reduce", "attention", "combine", "o_proj", "o_pro
 def run_trace(args):
     """Per-phase device timeline of the draft block in one bench step."""
     import block_diffusion_drafter_layer_gb300 as dfl
-    w = synth.WORKLOADS[args.workload]
+    w = _workload(args)
     st = Draft(w, 0, 8)
     st.prefill()
     for _ in range(max(args.warmup, 3)):
@@ -510,9 +512,20 @@ def _traffic(kernel, workload):
     return r.get("dram_bytes_per_launch") if h.hexdigest() == r.get("sha256") else None
 
 
+def _workload(args):
+    """The named workload, with its context length replaced by --ctx-len
+    (fixed-length workloads only; a smaller case for profiler captures)."""
+    w = synth.WORKLOADS[args.workload]
+    if args.ctx_len > 0:
+        if w.ctx_range is not None:
+            raise SystemExit("--ctx-len applies to fixed-length workloads")
+        w = synth.with_(w, ctx_len=args.ctx_len)
+    return w
+
+
 def run_ours(args, rank, world, local):
     import block_diffusion_drafter_layer_gb300 as dfl
-    w = synth.WORKLOADS[args.workload]
+    w = _workload(args)
     if w.dtype != "bf16" or w.target is not None:
         raise SystemExit("bench.py times the bf16 draft workloads")
     hbm, tf_burst, tf_sust, peak_kind = _peaks()

@@ -700,28 +700,33 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
         float4 sum[IT];
 #pragma unroll
         for (int q = 0; q < IT; ++q) sum[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c0 = lo; c0 <= hi; c0 += 8) {
-          const float4* src[8];
+        // CB contributors' partials per batch, all of a thread's float4s of
+        // each in flight together (at 64 rows one whole partial per batch:
+        // as many dependent batches as contributors, not one per float4);
+        // every element still adds the contributors in CTA (= k) order
+        constexpr int CB = IT >= 16 ? 1 : IT >= 8 ? 2 : 8;
+        for (int c0 = lo; c0 <= hi; c0 += CB) {
+          float4 v[CB][IT];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < CB; ++k) {
             const int c = min(c0 + k, hi);
             const int ft = first_unit(c, U, G) / p.kc;
-            src[k] = (const float4*)(p.partial + (int64_t)(2 * c + (t == ft ? 0 : 1)) * (MT * 16 * 128));
+            const float4* src =
+                (const float4*)(p.partial + (int64_t)(2 * c + (t == ft ? 0 : 1)) * (MT * 16 * 128));
+#pragma unroll
+            for (int q = 0; q < IT; ++q) v[k][q] = __ldcg(src + tid + q * WS_CT);
           }
 #pragma unroll
-          for (int q = 0; q < IT; ++q) {
-            float4 v[8];
+          for (int k = 0; k < CB; ++k)
+            if (c0 + k <= hi) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = __ldcg(src[k] + tid + q * WS_CT);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              if (c0 + k <= hi) {
-                sum[q].x += v[k].x;
-                sum[q].y += v[k].y;
-                sum[q].z += v[k].z;
-                sum[q].w += v[k].w;
+              for (int q = 0; q < IT; ++q) {
+                sum[q].x += v[k][q].x;
+                sum[q].y += v[k][q].y;
+                sum[q].z += v[k][q].z;
+                sum[q].w += v[k][q].w;
               }
-          }
+            }
         }
 #pragma unroll
         for (int q = 0; q < IT; ++q) {
