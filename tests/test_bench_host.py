@@ -72,3 +72,15 @@ def test_clocks_without_nvidia_smi(tmp_path, monkeypatch):
     c.mark(0)
     c.mark(1)
     assert c.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_ctx_len_override():
+    """--ctx-len replaces a fixed-length workload's context length only."""
+    import argparse
+    bench = pytest.importorskip("bench")
+    w = bench._workload(argparse.Namespace(workload="qwen35_a3b_32k", ctx_len=2048))
+    assert w.ctx_len == 2048 and w.draft.D == 2048 and w.batch == 4
+    w0 = bench._workload(argparse.Namespace(workload="qwen35_a3b_32k", ctx_len=0))
+    assert w0.ctx_len == 32768
+    with pytest.raises(SystemExit):
+        bench._workload(argparse.Namespace(workload="qwen3_8b_b32_ragged", ctx_len=2048))
