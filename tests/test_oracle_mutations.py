@@ -5,7 +5,11 @@ import pytest
 
 import oracle as O
 import oracle.dflash_oracle as OM
+import test_oracle_conv as C
+import test_oracle_masks as M
 import test_oracle_pins as P
+import test_oracle_sampling as S
+import test_oracle_selector as SEL
 
 
 def _patch(monkeypatch, name, fn):
@@ -120,6 +124,108 @@ def _layer_drop_attn_residual(x, layer, ctx_K, ctx_V, pos, H, G, d, theta, eps, 
     return OM.f32(x + OM.linear(a, layer["wd"]))
 
 
+# ---- mutants of the sampling, selection, conv and mask functions ----------
+def _visible_causal_excludes_self(L, B, causal, window):
+    p = np.arange(L, L + B)[:, None]
+    j = np.arange(L + B)[None, :]
+    vis = np.ones((B, L + B), dtype=bool)
+    if causal:
+        vis &= j < p                     # a row loses its own key
+    if window > 0:
+        vis &= j > p - window
+    return vis
+
+
+def _visible_window_one_wider(L, B, causal, window):
+    p = np.arange(L, L + B)[:, None]
+    j = np.arange(L + B)[None, :]
+    vis = np.ones((B, L + B), dtype=bool)
+    if causal:
+        vis &= j <= p
+    if window > 0:
+        vis &= j >= p - window           # W + 1 keys
+    return vis
+
+
+def _conv_taps_swapped(x, corr, base, group):
+    x = np.asarray(x, np.float64)
+    k = np.asarray(base, np.float64)[None] + np.repeat(np.asarray(corr, np.float64), group, axis=-1)
+    prev = np.concatenate([np.zeros((1, x.shape[1])), x[:-1]], axis=0)
+    return k[:, 1] * x + k[:, 0] * prev
+
+
+def _conv_wraps_first_row(x, corr, base, group):
+    x = np.asarray(x, np.float64)
+    k = np.asarray(base, np.float64)[None] + np.repeat(np.asarray(corr, np.float64), group, axis=-1)
+    return k[:, 0] * x + k[:, 1] * np.roll(x, 1, axis=0)
+
+
+def _conv_groups_interleaved(x, corr, base, group):
+    x = np.asarray(x, np.float64)
+    corr = np.asarray(corr, np.float64)
+    k = np.asarray(base, np.float64)[None] + np.tile(corr, (1, 1, group))   # channel c -> group c % n
+    prev = np.concatenate([np.zeros((1, x.shape[1])), x[:-1]], axis=0)
+    return k[:, 0] * x + k[:, 1] * prev
+
+
+def _sample_left(weights, u):
+    c = np.cumsum(np.asarray(weights, dtype=np.float64))
+    return min(int(np.searchsorted(c, u * c[-1], side="left")), len(c) - 1)
+
+
+def _verify_rejection_with(accept_rule, residual_rule):
+    """verify_rejection with its acceptance test and residual replaced."""
+    def verify(draft, q, p, u_accept, u_sample, start):
+        draft = np.asarray(draft)
+        batch, B = draft.shape
+        accept = np.zeros(batch, dtype=np.int32)
+        token = np.zeros(batch, dtype=np.int32)
+        out = np.full((batch, B), -1, dtype=np.int32)
+        new_len = np.zeros(batch, dtype=np.int32)
+        for b in range(batch):
+            a = 0
+            while a < B - 1:
+                d = int(draft[b, a + 1])
+                if not accept_rule(u_accept[b, a], q[b, a][d], p[b, a][d]):
+                    break
+                a += 1
+            if a < B - 1:
+                res = residual_rule(np.asarray(p[b, a], np.float64), np.asarray(q[b, a], np.float64))
+                tok = OM.sample_from(res if res.sum() > 0 else p[b, a], float(u_sample[b]))
+            else:
+                tok = OM.sample_from(p[b, B - 1], float(u_sample[b]))
+            accept[b], token[b] = a, tok
+            out[b, :a] = draft[b, 1:a + 1]
+            out[b, a] = tok
+            new_len[b] = int(start[b]) + a + 1
+        return accept, token, out, new_len
+    return verify
+
+
+# u * q > p instead of u * q < p
+_verify_accept_flipped = _verify_rejection_with(lambda u, qd, pd: u * qd > pd,
+                                                lambda p, q: np.maximum(p - q, 0.0))
+# residual max(q - p, 0) instead of max(p - q, 0)
+_verify_residual_reversed = _verify_rejection_with(lambda u, qd, pd: u * qd < pd,
+                                                   lambda p, q: np.maximum(q - p, 0.0))
+
+
+def _topk_highest_on_ties(z, k):
+    z = np.asarray(z)
+    out = np.empty(z.shape[:-1] + (k,), dtype=np.int32)
+    for idx in np.ndindex(*z.shape[:-1]):
+        row = z[idx]
+        out[idx] = np.lexsort((-np.arange(row.shape[0]), -row))[:k]
+    return out
+
+
+_real_select = OM.select_candidates
+
+
+def _select_codebooks_swapped(logits, hidden, anchor, W_h, code_pred, code_succ, top_k):
+    return _real_select(logits, hidden, anchor, W_h, code_succ, code_pred, top_k)
+
+
 MUTATIONS = [
     ("rope", _rope_wrong_sign, lambda: P.test_rope_complex_form()),
     ("rope", _rope_interleaved, lambda: P.test_rope_complex_form()),
@@ -133,6 +239,16 @@ MUTATIONS = [
     ("build_target_layer_ids", _ids_wrong_end, lambda: P.test_layer_ids_configs(36, [1, 9, 17, 25, 33])),
     ("bf16", _bf16_truncate, lambda: P.test_bf16_rounding_matches_torch()),
     ("draft_layer", _layer_drop_attn_residual, lambda: P.test_draft_layer_identity_without_outputs()),
+    ("draft_key_visible", _visible_causal_excludes_self, lambda: M.test_causal_anchor_is_full_attention_over_sliced_keys()),
+    ("draft_key_visible", _visible_window_one_wider, lambda: M.test_window_ignores_older_context(True)),
+    ("dynamic_conv", _conv_taps_swapped, lambda: C.test_identity_and_shift_taps()),
+    ("dynamic_conv", _conv_wraps_first_row, lambda: C.test_identity_and_shift_taps()),
+    ("dynamic_conv", _conv_groups_interleaved, lambda: C.test_one_correction_per_channel_group()),
+    ("sample_from", _sample_left, lambda: S.test_sample_from_buckets()),
+    ("verify_rejection", _verify_accept_flipped, lambda: S.test_equal_distributions_accept_everything()),
+    ("verify_rejection", _verify_residual_reversed, lambda: S.test_emitted_token_follows_target(0)),
+    ("topk_lowest", _topk_highest_on_ties, lambda: SEL.test_topk_matches_brute_force_with_ties(0)),
+    ("select_candidates", _select_codebooks_swapped, lambda: SEL.test_planted_bigram_chain_is_followed()),
 ]
 
 
