@@ -519,8 +519,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 
 // ---------------------------------------------------------------------------
 int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float4* amx) {
-  if ((L.bn != 128 && L.bn != 256) || L.M < 1 || L.K % TC_BK != 0 || L.nseg < 1 || L.nseg > WS_MAXMAP || L.nsrc < 1 ||
-      L.nsrc > WS_MAXSRC || (L.K / TC_BK) % L.nsrc != 0)
+  if ((L.bn != 128 && L.bn != 256) || L.M < 1 || L.K % TC_BK != 0 || L.nseg < 1 ||
+      L.nseg > WS_MAXMAP || L.nsrc < 1 || L.nsrc > WS_MAXSRC || (L.K / TC_BK) % L.nsrc != 0)
     return DFLASH_ERR_SHAPE;
   for (int i = 0; i < L.nseg; ++i)
     if (L.seg[i].kind == SK_HEAD && L.seg[i].d != 128) return DFLASH_ERR_SHAPE;
