@@ -21,6 +21,17 @@ from . import (KVCache, Model, dflash_build_target_layer_ids, dflash_draft_block
                dflash_verify_greedy, dflash_verify_rejection)
 
 
+def next_block_size(sizes: Sequence[int], B: int, longest_tau: int) -> int:
+    """Block size for the next rounds of the resident loop, from the longest
+    tau of the last window: the largest listed size once tau reached the
+    current size (every draft accepted: a longer block may pay), else the
+    smallest listed size that still covers longest_tau + 1 (a block that is
+    never filled costs target and draft rows for nothing).  sizes ascending."""
+    if longest_tau >= B:
+        return sizes[-1]
+    fit = [b for b in sizes if b >= longest_tau + 1]
+    return fit[0] if fit else sizes[-1]
+
 class SpecDecoder:
     def __init__(self, target: Model, draft: Model, *, t_layers: int, t_kv_heads: int,
                  d_layers: int, d_kv_heads: int, head_dim: int, D: int, n_target_layers: int,
@@ -170,9 +181,7 @@ class SpecDecoder:
                     break
                 if len(sizes) > 1:
                     recent = tau_log[0, rounds - check_every:rounds]
-                    longest = int(recent.max().item())
-                    fit = [b for b in sizes if b >= longest + 1]
-                    B = sizes[-1] if longest >= B else (fit[0] if fit else sizes[-1])
+                    B = next_block_size(sizes, B, int(recent.max().item()))
         taus = tau_log[0, :int(n_rounds.item())].tolist()
         n = min(int(out_len.item()), cap)
         return out_buf[0, :n].tolist()[:n_new], taus
