@@ -39,9 +39,23 @@ What pins each function (tests/test_oracle_*.py):
                            causal (a row ignores later rows); in a layer,
                            identity convs change nothing and a shifting
                            finish conv shifts the sublayer's increment
+  inject_kv                identity k/v projections of distinct scales:
+                           K is the per-head RMSNorm (torch) with the k_norm
+                           gains, V the scaled slice; a row appended at
+                           positions p is the position-0 K rotated by p
+                           (complex form): k_norm before RoPE, at the cache
+                           positions
   draft_layer/draft_block  reductions: zero W_o and W_d give the identity;
                            zero W_q gives uniform attention (closed form);
-                           context enters only through K/V
+                           context enters only through K/V; SwiGLU with
+                           diagonal gate/up/down equals torch's
+                           silu(gate) * up; zero q_norm gains give the mean of
+                           all values, and a scaled W_q changes nothing;
+                           a d = 2 head places the anchor at position L (it
+                           scores a key turned by L radians like its own);
+                           planted LM-head rows: drafts come from rows 1..B-1
+                           through the final norm (torch rms_norm gap)
+  embed_block              identity layers return scale x the block's rows
   lm_head_argmax           brute force with planted ties / gaps
   verify_greedy            exhaustive enumeration on tiny B and V;
                            tau in [1, B]; E[tau] closed form under planted

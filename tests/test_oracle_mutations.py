@@ -8,6 +8,7 @@ import oracle.dflash_oracle as OM
 import test_oracle_conv as C
 import test_oracle_masks as M
 import test_oracle_pins as P
+import test_oracle_pins_layer as PL
 import test_oracle_sampling as S
 import test_oracle_selector as SEL
 
@@ -226,6 +227,81 @@ def _select_codebooks_swapped(logits, hidden, anchor, W_h, code_pred, code_succ,
     return _real_select(logits, hidden, anchor, W_h, code_succ, code_pred, top_k)
 
 
+_INJECT = OM.inject_kv
+
+
+def _inject_swapped(H_t, layer, pos, G, d, theta, eps, store=OM.f32, qk_norm=True):
+    return _INJECT(H_t, dict(layer, wk=layer["wv"], wv=layer["wk"]), pos, G, d, theta, eps, store,
+                   qk_norm)
+
+
+def _inject_no_knorm(H_t, layer, pos, G, d, theta, eps, store=OM.f32, qk_norm=True):
+    return _INJECT(H_t, layer, pos, G, d, theta, eps, store, False)
+
+
+def _inject_rope_at_row_index(H_t, layer, pos, G, d, theta, eps, store=OM.f32, qk_norm=True):
+    return _INJECT(H_t, layer, np.arange(H_t.shape[0]), G, d, theta, eps, store, qk_norm)
+
+
+def _inject_norm_after_rope(H_t, layer, pos, G, d, theta, eps, store=OM.f32, qk_norm=True):
+    T = H_t.shape[0]
+    k = OM.linear(H_t, layer["wk"]).reshape(T, G, d)
+    k = OM.rmsnorm(OM.rope(k, pos, theta), layer["k_norm"], eps)
+    v = OM.linear(H_t, layer["wv"]).reshape(T, G, d)
+    return store(k), store(v)
+
+
+def _layer_variant(swiglu_reversed=False, q_norm=True):
+    """draft_layer (no conv) with one planted mistake."""
+    def layer_fn(x, layer, ctx_K, ctx_V, pos, H, G, d, theta, eps, store=OM.f32, mask=None,
+                 conv_group=0):
+        B = x.shape[0]
+        h = store(OM.rmsnorm(x, layer["g_in"], eps))
+        q = OM.linear(h, layer["wq"]).reshape(B, H, d)
+        k = OM.linear(h, layer["wk"]).reshape(B, G, d)
+        v = OM.linear(h, layer["wv"]).reshape(B, G, d)
+        q = store(OM.rope(OM.rmsnorm(q, layer["q_norm"], eps) if q_norm else q, pos, theta))
+        k = store(OM.rope(OM.rmsnorm(k, layer["k_norm"], eps), pos, theta))
+        o = store(OM.attention(q, np.concatenate([ctx_K, k]), np.concatenate([ctx_V, store(v)]),
+                               mask).reshape(B, H * d))
+        x = OM.f32(x + OM.linear(o, layer["wo"]))
+        h2 = store(OM.rmsnorm(x, layer["g_post"], eps))
+        g, u = OM.linear(h2, layer["wg"]), OM.linear(h2, layer["wu"])
+        a = store(OM.silu(u) * g if swiglu_reversed else OM.silu(g) * u)
+        return OM.f32(x + OM.linear(a, layer["wd"]))
+    return layer_fn
+
+
+def _block_variant(pos_from_zero=False, logit_rows_from_anchor=False, final_norm=True):
+    """draft_block (bidirectional layers, one planted mistake)."""
+    def block_fn(shape, W, ctx_K, ctx_V, anchors, B, store=OM.f32, return_logits=False,
+                 lm_head=True, return_hidden=False):
+        ids = np.zeros((len(anchors), B), np.int32)
+        gaps = np.zeros((len(anchors), B - 1))
+        hidden = []
+        for b, a in enumerate(anchors):
+            L = ctx_K[0][b].shape[0]
+            pos = np.arange(B) if pos_from_zero else np.arange(L, L + B)
+            x = OM.embed_block(W["embed"], a, shape.mask_id, B, shape.embed_scale)
+            for l, layer in enumerate(W["layers"]):
+                x = OM.draft_layer(x, layer, ctx_K[l][b], ctx_V[l][b], pos, shape.H, shape.G,
+                                   shape.d, shape.rope_theta, shape.eps, store)
+            hidden.append(x)
+            ids[b, 0] = a
+            if lm_head:
+                rows = x[:-1] if logit_rows_from_anchor else x[1:]
+                hf = store(OM.rmsnorm(rows, W["g_f"], shape.eps)) if final_norm else rows
+                z = OM.lm_head_logits(hf, W["lm_head"])
+                ids[b, 1:] = OM.argmax_lowest(z)
+                gaps[b] = OM.top2_gap(z)
+        return (ids, gaps, np.stack(hidden)) if return_hidden else (ids, gaps)
+    return block_fn
+
+
+def _embed_no_scale(embed, anchor, mask_id, B, scale):
+    return OM.f32(np.asarray(embed[[int(anchor)] + [int(mask_id)] * (B - 1)], np.float64))
+
+
 MUTATIONS = [
     ("rope", _rope_wrong_sign, lambda: P.test_rope_complex_form()),
     ("rope", _rope_interleaved, lambda: P.test_rope_complex_form()),
@@ -249,6 +325,16 @@ MUTATIONS = [
     ("verify_rejection", _verify_residual_reversed, lambda: S.test_emitted_token_follows_target(0)),
     ("topk_lowest", _topk_highest_on_ties, lambda: SEL.test_topk_matches_brute_force_with_ties(0)),
     ("select_candidates", _select_codebooks_swapped, lambda: SEL.test_planted_bigram_chain_is_followed()),
+    ("inject_kv", _inject_swapped, lambda: PL.test_inject_kv_identity_projections_and_positions()),
+    ("inject_kv", _inject_no_knorm, lambda: PL.test_inject_kv_identity_projections_and_positions()),
+    ("inject_kv", _inject_rope_at_row_index, lambda: PL.test_inject_kv_identity_projections_and_positions()),
+    ("inject_kv", _inject_norm_after_rope, lambda: PL.test_inject_kv_identity_projections_and_positions()),
+    ("draft_layer", _layer_variant(swiglu_reversed=True), lambda: PL.test_draft_layer_swiglu_orientation()),
+    ("draft_layer", _layer_variant(q_norm=False), lambda: PL.test_draft_layer_query_norm()),
+    ("draft_block", _block_variant(pos_from_zero=True), lambda: PL.test_draft_block_anchor_at_position_after_context()),
+    ("draft_block", _block_variant(logit_rows_from_anchor=True), lambda: PL.test_draft_block_final_norm_and_logit_rows()),
+    ("draft_block", _block_variant(final_norm=False), lambda: PL.test_draft_block_final_norm_and_logit_rows()),
+    ("embed_block", _embed_no_scale, lambda: PL.test_embed_block_scale()),
 ]
 
 
