@@ -162,10 +162,38 @@ def rmsnorm(x: np.ndarray, gain: np.ndarray, eps: float) -> np.ndarray:
     return x / np.sqrt(ms + eps) * np.asarray(gain, dtype=np.float64)
 
 
-def linear(x: np.ndarray, W: np.ndarray, chunk: int = 1 << 14) -> np.ndarray:
+def _f32_order(arith: str):
+    """None for fp64 arithmetic; else the seed of the order fp32 sums take
+    (0: natural order; k > 0: the reduction axis permuted by a permutation
+    seeded with k, the same sum in another order)."""
+    if arith == "f64":
+        return None
+    if arith == "f32":
+        return 0
+    if arith.startswith("f32."):
+        return int(arith[4:])
+    raise ValueError(arith)
+
+
+def linear(x: np.ndarray, W: np.ndarray, chunk: int = 1 << 14, arith: str = "f64") -> np.ndarray:
     """y = x W^T with W stored out x in (``nn.Linear.weight``), fp64.
 
-    Large W are upcast a block of output rows at a time."""
+    Large W are upcast a block of output rows at a time.  arith="f32" (or
+    "f32.k", the sum over the input axis in the order of a seeded
+    permutation) takes the products and sums in fp32 instead (numpy's fp32
+    matmul): the arithmetic-precision reference the bf16 tests measure their
+    floor with (the storage points are unchanged)."""
+    order = _f32_order(arith)
+    if order is not None:
+        x32 = np.asarray(x, dtype=np.float32)
+        perm = np.random.default_rng(order).permutation(x32.shape[-1]) if order else None
+        if perm is not None:
+            x32 = x32[..., perm]
+        out = np.empty(x32.shape[:-1] + (W.shape[0],), dtype=np.float64)
+        for s in range(0, W.shape[0], chunk):
+            Wc = np.asarray(W[s:s + chunk], dtype=np.float32)
+            out[..., s:s + chunk] = x32 @ (Wc[:, perm] if perm is not None else Wc).T
+        return out
     x = np.asarray(x, dtype=np.float64)
     n_out = W.shape[0]
     if W.dtype == np.float64 or n_out <= chunk:
@@ -200,21 +228,31 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
 
 
 def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray,
-              key_visible: Optional[np.ndarray] = None) -> np.ndarray:
+              key_visible: Optional[np.ndarray] = None, arith: str = "f64") -> np.ndarray:
     """Softmax attention with grouped K/V heads, fp64.
 
     q: [n, H, d]; K, V: [m, G, d]; query head h reads K/V head
     h // (H / G).  Scale 1/sqrt(d).  ``key_visible`` [n, m] (bool) masks
     keys; None means every key is visible (the draft's bidirectional block
     over [context ; block], [reading] §6: full-attention layers are
-    non-causal).  Returns [n, H, d]."""
+    non-causal).  arith="f32" / "f32.k": scores, softmax and the weighted
+    sum in fp32, for "f32.k" over the keys in a seeded permuted order (see
+    ``linear``).  Returns [n, H, d]."""
     n, H, d = q.shape
     m, G, _ = K.shape
     rep = H // G
+    order = _f32_order(arith)
+    if order is not None:
+        q, K, V = (np.asarray(a, dtype=np.float32) for a in (q, K, V))
+        if order:
+            perm = np.random.default_rng(order).permutation(m)
+            K, V = K[perm], V[perm]
+            if key_visible is not None:
+                key_visible = key_visible[:, perm]
     out = np.empty((n, H, d), dtype=np.float64)
     for h in range(H):
         g = h // rep
-        s = (q[:, h, :] @ K[:, g, :].T) / math.sqrt(d)      # [n, m]
+        s = (q[:, h, :] @ K[:, g, :].T) / q.dtype.type(math.sqrt(d))   # [n, m]
         if key_visible is not None:
             s = np.where(key_visible, s, -np.inf)
         s = s - s.max(axis=1, keepdims=True)
@@ -307,7 +345,7 @@ def dynamic_conv(x: np.ndarray, corr: np.ndarray, base: np.ndarray, group: int) 
     return k[:, 0] * x + k[:, 1] * prev
 
 
-def _conv_pair(x: np.ndarray, kp: np.ndarray, base: np.ndarray, group: int):
+def _conv_pair(x: np.ndarray, kp: np.ndarray, base: np.ndarray, group: int, arith: str = "f64"):
     """The corrections of a conv module's two calls from the rows x:
     kernel_projection kp [2 * 2 * (D // group), D] (no bias), read as
     [call, tap, group]; base [2 (call), 2 (tap), D].  Returns the prepare
@@ -315,14 +353,15 @@ def _conv_pair(x: np.ndarray, kp: np.ndarray, base: np.ndarray, group: int):
     prepared rows are stored in fp32, and the sublayer output y is stored in
     fp32 before its finish conv)."""
     B, D = x.shape
-    corr = linear(x, kp).reshape(B, 2, 2, D // group)
+    corr = linear(x, kp, arith=arith).reshape(B, 2, 2, D // group)
     return (lambda y: f32(dynamic_conv(y, corr[:, 0], base[0], group)),
             lambda y: dynamic_conv(f32(y), corr[:, 1], base[1], group))
 
 
 def draft_layer(x: np.ndarray, layer: dict, ctx_K: np.ndarray, ctx_V: np.ndarray,
                 pos: np.ndarray, H: int, G: int, d: int, theta: float, eps: float,
-                store=f32, mask: Optional[np.ndarray] = None, conv_group: int = 0) -> np.ndarray:
+                store=f32, mask: Optional[np.ndarray] = None, conv_group: int = 0,
+                arith: str = "f64") -> np.ndarray:
     """One Qwen3-style draft decoder layer over one sequence's block.
 
     x: [B, D] fp32 residual.  ctx_K, ctx_V: [L, G, d] injected context.
@@ -341,28 +380,28 @@ def draft_layer(x: np.ndarray, layer: dict, ctx_K: np.ndarray, ctx_V: np.ndarray
     B = x.shape[0]
     prep = fin = lambda y: y
     if conv_group:
-        prep, fin = _conv_pair(x, layer["conv_att_kp"], layer["conv_att_base"], conv_group)
+        prep, fin = _conv_pair(x, layer["conv_att_kp"], layer["conv_att_base"], conv_group, arith)
     h = store(rmsnorm(prep(x), layer["g_in"], eps))
-    q = linear(h, layer["wq"]).reshape(B, H, d)
-    k = linear(h, layer["wk"]).reshape(B, G, d)
-    v = linear(h, layer["wv"]).reshape(B, G, d)
+    q = linear(h, layer["wq"], arith=arith).reshape(B, H, d)
+    k = linear(h, layer["wk"], arith=arith).reshape(B, G, d)
+    v = linear(h, layer["wv"], arith=arith).reshape(B, G, d)
     q = store(rope(rmsnorm(q, layer["q_norm"], eps), pos, theta))
     k = store(rope(rmsnorm(k, layer["k_norm"], eps), pos, theta))
     v = store(v)
     K = np.concatenate([ctx_K, k], axis=0)
     Vv = np.concatenate([ctx_V, v], axis=0)
-    o = store(attention(q, K, Vv, mask).reshape(B, H * d))
-    x = f32(x + fin(linear(o, layer["wo"])))
+    o = store(attention(q, K, Vv, mask, arith=arith).reshape(B, H * d))
+    x = f32(x + fin(linear(o, layer["wo"], arith=arith)))
     if conv_group:
-        prep, fin = _conv_pair(x, layer["conv_mlp_kp"], layer["conv_mlp_base"], conv_group)
+        prep, fin = _conv_pair(x, layer["conv_mlp_kp"], layer["conv_mlp_base"], conv_group, arith)
     h2 = store(rmsnorm(prep(x), layer["g_post"], eps))
-    a = store(silu(linear(h2, layer["wg"])) * linear(h2, layer["wu"]))
-    return f32(x + fin(linear(a, layer["wd"])))
+    a = store(silu(linear(h2, layer["wg"], arith=arith)) * linear(h2, layer["wu"], arith=arith))
+    return f32(x + fin(linear(a, layer["wd"], arith=arith)))
 
 
-def lm_head_logits(hf: np.ndarray, W_lm: np.ndarray) -> np.ndarray:
+def lm_head_logits(hf: np.ndarray, W_lm: np.ndarray, arith: str = "f64") -> np.ndarray:
     """fp32 logits hf W_lm^T (the target's shared LM head)."""
-    return f32(linear(hf, W_lm))
+    return f32(linear(hf, W_lm, arith=arith))
 
 
 def argmax_lowest(z: np.ndarray) -> np.ndarray:
@@ -379,7 +418,7 @@ def top2_gap(z: np.ndarray) -> np.ndarray:
 def draft_block(shape, W: dict, ctx_K: List[List[np.ndarray]],
                 ctx_V: List[List[np.ndarray]], anchors: Sequence[int], B: int,
                 store=f32, return_logits: bool = False, lm_head: bool = True,
-                return_hidden: bool = False):
+                return_hidden: bool = False, arith: str = "f64"):
     """Single-pass draft of one block per sequence.
 
     ``shape`` has D, H, G, d, eps, rope_theta, mask_id, embed_scale.
@@ -396,7 +435,10 @@ def draft_block(shape, W: dict, ctx_K: List[List[np.ndarray]],
     Returns ids [batch, B] (column 0 = anchor), gap [batch, B-1] and,
     if asked, logits [batch, B-1, V] and the fp32 residual stream after the
     last layer [batch, B, D].  With lm_head=False only the residual stream is
-    computed (ids and gaps are left zero)."""
+    computed (ids and gaps are left zero).  arith="f32" runs every product
+    and sum in fp32 with the same storage points (``linear``): the distance
+    of that run from the fp64 one is the floor any fp32 implementation of
+    the block sits at."""
     batch = len(anchors)
     ids = np.zeros((batch, B), dtype=np.int32)
     gaps = np.zeros((batch, B - 1), dtype=np.float64)
@@ -412,13 +454,13 @@ def draft_block(shape, W: dict, ctx_K: List[List[np.ndarray]],
             mask = draft_key_visible(L, B, causal, window) if causal or window else None
             x = draft_layer(x, layer, ctx_K[l][b], ctx_V[l][b], pos, shape.H,
                             shape.G, shape.d, shape.rope_theta, shape.eps, store, mask,
-                            getattr(shape, "conv_group", 0))
+                            getattr(shape, "conv_group", 0), arith=arith)
         hidden.append(x)
         ids[b, 0] = anchors[b]
         if not lm_head:
             continue
         hf = store(rmsnorm(x[1:], W["g_f"], shape.eps))
-        z = lm_head_logits(hf, W["lm_head"])
+        z = lm_head_logits(hf, W["lm_head"], arith=arith)
         ids[b, 1:] = argmax_lowest(z)
         gaps[b] = top2_gap(z)
         if return_logits:

@@ -40,7 +40,7 @@ def _rope_interleaved(x, pos, theta):
     return out
 
 
-def _attention_modulo_groups(q, K, V, key_visible=None):
+def _attention_modulo_groups(q, K, V, key_visible=None, arith="f64"):
     n, H, d = q.shape
     G = K.shape[1]
     out = np.empty((n, H, d))
@@ -58,7 +58,7 @@ _ATTENTION = OM.attention
 _VERIFY = OM.verify_greedy
 
 
-def _attention_no_scale(q, K, V, key_visible=None):
+def _attention_no_scale(q, K, V, key_visible=None, arith="f64"):
     return _ATTENTION(q * np.sqrt(q.shape[-1]), K, V, key_visible)
 
 
@@ -112,7 +112,8 @@ def _bf16_truncate(x):
     return (a.view(np.uint32) & 0xFFFF0000).view(np.float32).astype(np.float64)
 
 
-def _layer_drop_attn_residual(x, layer, ctx_K, ctx_V, pos, H, G, d, theta, eps, store=OM.f32):
+def _layer_drop_attn_residual(x, layer, ctx_K, ctx_V, pos, H, G, d, theta, eps, store=OM.f32,
+                              mask=None, conv_group=0, arith="f64"):
     B = x.shape[0]
     h = store(OM.rmsnorm(x, layer["g_in"], eps))
     q = store(OM.rope(OM.rmsnorm(OM.linear(h, layer["wq"]).reshape(B, H, d), layer["q_norm"], eps), pos, theta))
@@ -254,7 +255,7 @@ def _inject_norm_after_rope(H_t, layer, pos, G, d, theta, eps, store=OM.f32, qk_
 def _layer_variant(swiglu_reversed=False, q_norm=True):
     """draft_layer (no conv) with one planted mistake."""
     def layer_fn(x, layer, ctx_K, ctx_V, pos, H, G, d, theta, eps, store=OM.f32, mask=None,
-                 conv_group=0):
+                 conv_group=0, arith="f64"):
         B = x.shape[0]
         h = store(OM.rmsnorm(x, layer["g_in"], eps))
         q = OM.linear(h, layer["wq"]).reshape(B, H, d)
@@ -275,7 +276,7 @@ def _layer_variant(swiglu_reversed=False, q_norm=True):
 def _block_variant(pos_from_zero=False, logit_rows_from_anchor=False, final_norm=True):
     """draft_block (bidirectional layers, one planted mistake)."""
     def block_fn(shape, W, ctx_K, ctx_V, anchors, B, store=OM.f32, return_logits=False,
-                 lm_head=True, return_hidden=False):
+                 lm_head=True, return_hidden=False, arith="f64"):
         ids = np.zeros((len(anchors), B), np.int32)
         gaps = np.zeros((len(anchors), B - 1))
         hidden = []
