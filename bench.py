@@ -49,6 +49,21 @@ def layer_weight_bytes(s, esz):
     return per * s.n_layers * esz
 
 
+def step_flops(w, lens):
+    """Multiply-add flops of one round (x2): every projection over the rows
+    it multiplies, the LM head over rows 1..B-1, and attention (scores and
+    weighted sum) of every block row over [context ; block]."""
+    s = w.draft
+    batch, B = w.batch, w.B
+    rows = batch * B
+    per_layer = s.H * s.d * s.D + 2 * s.G * s.d * s.D + s.D * s.H * s.d + 3 * s.F * s.D
+    f = 2.0 * rows * per_layer * s.n_layers
+    f += 2.0 * batch * (B - 1) * s.V * s.D
+    f += 2.0 * rows * (s.n_pick * s.D * s.D + 2 * s.G * s.d * s.D * s.n_layers)
+    f += sum(4.0 * (int(l) + B) * B * s.H * s.d for l in lens) * s.n_layers
+    return f
+
+
 def step_bytes(w, lens, esz):
     """Bytes a step must move at least once: every weight it reads, the
     cached context K/V, and the small activations in and out."""
@@ -154,7 +169,7 @@ class Clocks:
 class Draft:
     """Device state of one replica: weights, cache, workspace, step buffers."""
 
-    def __init__(self, w, rank, n_steps_total, with_model=True):
+    def __init__(self, w, rank, n_steps_total, with_model=True, weights=None):
         self.w = w
         s = w.draft
         dev = "cuda"
@@ -165,7 +180,8 @@ class Draft:
         self.rows = rows
         td = synth.torch_dtype(w.dtype)
         seed = w.seed + 100 * rank
-        self.weights = synth.draft_weights(s, w.dtype, seed, device=dev)
+        self.weights = weights if weights is not None else synth.draft_weights(s, w.dtype, seed,
+                                                                                device=dev)
         self.len0 = torch.tensor(self.lens, dtype=torch.int32, device=dev)
         # a step's inputs (the 5 target feature slices, anchors, posterior) and
         # results (ids, accepted, tau, bonus, tokens) each live in one buffer,
@@ -378,6 +394,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sustain-s", type=float, default=1.0, metavar="S",
+                    help="seconds of the sustained region after the timed steps (0: K steps)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the batch-32 and long-context blocks of the default line")
     ap.add_argument("--trace", action="store_true",
                     help="print the persistent kernel's per-phase timeline of one step "
                          "(a table, not the JSON line) and exit")
@@ -523,6 +543,39 @@ def _workload(args):
     return w
 
 
+def extra_block(args, w, hbm, tf_sust, weights=None, min_s=0.3):
+    """Time the round of another workload (its own weights unless given,
+    its own caches, prefilled): at least args.steps steps and at least
+    min_s seconds, after args.warmup untimed steps.  Returns the JSON object
+    and the replica (so a second block size can share its weights)."""
+    st = Draft(w, 0, 1, weights=weights)
+    st.prefill()
+    for _ in range(max(args.warmup, 3)):
+        st.step()
+    t1 = time_steps(st.step, 3, 1) / 3
+    k = max(args.steps, int(np.ceil(min_s / max(t1, 1e-6))))
+    t = time_steps(st.step, k, 1)
+    ms = t / k * 1e3
+    nbytes = step_bytes(w, st.lens, 2)
+    by = sum(nbytes[c] for c in ("weight_gemm", "lm_head", "attention", "dense_gemm"))
+    fl = step_flops(w, st.lens)
+    hb = by / (ms / 1e3) / 1e9
+    tf = fl / (ms / 1e3) / 1e12
+    roof_h, roof_t = by / hbm / 1e9 * 1e3, fl / tf_sust / 1e12 * 1e3
+    out = {"workload": w.name, "batch": w.batch, "B": w.B,
+           "ctx_len": w.ctx_len if w.ctx_range is None else
+           {"range": list(w.ctx_range), "mean": float(np.mean(st.lens))},
+           "steps": k, "ms_per_step": ms, "blocks_per_s": w.batch / (ms / 1e3),
+           "us_per_sequence_block": ms * 1e3 / w.batch,
+           "algorithmic_bytes_per_step": by, "flops_per_step": fl,
+           "hbm": {"achieved_gbs": hb, "frac_measured": hb / hbm, "frac_8tbs": hb / 8000.0,
+                   "roof_ms": roof_h},
+           "tensor": {"achieved_tflops": tf, "frac_sustained": tf / tf_sust, "roof_ms": roof_t},
+           "binding": "hbm" if roof_h >= roof_t else "tensor",
+           "frac_of_binding_roof": max(roof_h, roof_t) / ms}
+    return out, st
+
+
 def run_ours(args, rank, world, local):
     import block_diffusion_drafter_layer_gb300 as dfl
     w = _workload(args)
@@ -558,13 +611,19 @@ def run_ours(args, rank, world, local):
     clocks.start()
     clocks.mark(0)
     t = time_steps(st.step, args.steps, world)
+    launches = dfl.dflash_launch_count() - n0
+    # the same step again for at least a second, so the clock record of the
+    # measurement holds many samples (the value above stays the K-step time)
+    n_sus = max(args.steps, int(np.ceil(args.sustain_s / max(t / args.steps, 1e-6))))
+    t_sus = _max_over_ranks(time_steps(st.step, n_sus, world), world)
     clocks.mark(1)
     clk = clocks.stop()
-    launches = dfl.dflash_launch_count() - n0
+    clk["region"] = f"the {args.steps} timed steps and the {n_sus} sustained steps after them"
     t = _max_over_ranks(t, world)
     blocks = w.batch * args.steps * world
     value = blocks / t
     ms_step = t / args.steps * 1e3
+    sustained = {"steps": n_sus, "seconds": t_sus, "ms_per_step": t_sus / n_sus * 1e3}
 
     # per-kernel-class device time over an identical region (events per launch)
     dfl.dflash_timing_enable(st.model.handle, True)
@@ -584,7 +643,7 @@ def run_ours(args, rank, world, local):
               key=lambda k: cls[k][0])
     ach = nbytes[dom] / (cls[dom][0] / 1e3) / 1e9
     roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
-            "frac": ach / hbm, "peak_kind": peak_kind,
+            "frac": ach / hbm, "peak_kind": peak_kind, "frac_of_8tbs": ach / 8000.0,
             "traffic": _traffic(dom, w.name), "launches_per_step": cls[dom][1],
             "algorithmic_bytes_per_step": nbytes[dom],
             "class_ms_per_step": {k: round(v[0], 4) for k, v in cls.items()}}
@@ -623,6 +682,23 @@ def run_ours(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(st)
 
+    # the metric's batch-32 block and the long-context block (one GPU only)
+    batch32 = long_ctx = None
+    if world == 1 and not args.no_extra and w.name == DEFAULT_WORKLOAD:
+        kept = argparse.Namespace(lens=st.lens, T_pre=st.T_pre)
+        del st, h_hidden, h_ints_in, h_ints_out, e2e_step
+        torch.cuda.empty_cache()
+        st = kept
+        batch32, st32 = extra_block(args, synth.WORKLOADS["qwen3_8b_b32_ragged"], hbm, tf_sust)
+        del st32
+        torch.cuda.empty_cache()
+        w4 = synth.WORKLOADS["qwen35_a3b_32k"]
+        b16, st4 = extra_block(args, w4, hbm, tf_sust)
+        b8, st8 = extra_block(args, synth.with_(w4, B=8), hbm, tf_sust, weights=st4.weights)
+        del st4, st8
+        torch.cuda.empty_cache()
+        long_ctx = {"B16": b16, "B8": b8}
+
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -636,7 +712,8 @@ def run_ours(args, rank, world, local):
                                        "frac": fuse_tf / tf_burst, "unit": "TFLOP/s",
                                        "peak_kind": f"bf16 burst, {peak_kind}"},
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
-                "clocks": clk}
+                "clocks": clk, "sustained": sustained, "batch32": batch32,
+                "long_context": long_ctx}
         print(json.dumps(line), flush=True)
 
 

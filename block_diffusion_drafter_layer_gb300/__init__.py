@@ -101,6 +101,7 @@ _sig = {
                                         C.POINTER(C.c_int32), C.c_int32, _P, _P, _P, C.c_size_t,
                                         _P]),
     "dflash_lm_head_argmax_noalloc": (C.c_int, [_P, _P, C.c_int32, _P, _P, _P, _P]),
+    "dflash_selftest_wait": (C.c_int, [_P, C.c_int32, C.c_int64, _P]),
     "dflash_get_status": (C.c_int, [_P, _P]),
     "dflash_strerror": (C.c_char_p, [C.c_int]),
     "dflash_launch_count": (C.c_int64, []),
@@ -321,6 +322,12 @@ def dflash_lm_head_argmax_noalloc(h: int, x: torch.Tensor, rows: int, norm_gain:
     _check(_lib.dflash_lm_head_argmax_noalloc(h, _ptr(x), rows, _ptr(norm_gain), _ptr(ids),
                                               _ptr(top2_gap), _stream(stream)),
            "dflash_lm_head_argmax_noalloc")
+
+
+def dflash_selftest_wait(h: int, which: int, limit_ns: int, stream=None):
+    """One bounded wait that nothing completes (0: an mbarrier, 1: a device
+    counter); the next dflash_get_status reports the timeout."""
+    _check(_lib.dflash_selftest_wait(h, which, limit_ns, _stream(stream)), "dflash_selftest_wait")
 
 
 def dflash_get_status(h: int, stream=None) -> int:

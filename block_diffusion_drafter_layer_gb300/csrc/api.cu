@@ -1235,6 +1235,12 @@ int dflash_target_forward(dflash_handle* h, const int32_t* tokens, int32_t batch
   return advance_len(h, s, kv->len, nullptr, T, batch, kv->cap);
 }
 
+int dflash_selftest_wait(dflash_handle* h, int32_t which, int64_t limit_ns, dflash_stream_t s) {
+  if (!h || (which != 0 && which != 1) || limit_ns < 1000 || limit_ns > 1000000000)
+    return DFLASH_ERR_INVALID_ARG;
+  return selftest_wait(h, (cudaStream_t)s, which, limit_ns);
+}
+
 int dflash_get_status(dflash_handle* h, dflash_stream_t st) {
   if (!h) return DFLASH_ERR_INVALID_ARG;
   if (cudaStreamSynchronize((cudaStream_t)st) != cudaSuccess) return DFLASH_ERR_CUDA;
@@ -1334,7 +1340,8 @@ namespace dflash {
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int dtype) {
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, int dtype,
+                  bool swizzle128) {
   if (!g_encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -1351,7 +1358,8 @@ bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
   const CUtensorMapDataType ty =
       dtype == DFLASH_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   return g_encode(m, ty, 2, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }

@@ -30,6 +30,18 @@ template <> __device__ __forceinline__ float from_f<float>(float x) { return x; 
 template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
 
 // ---- deterministic block reductions (fixed shuffle tree, then warp 0) ------
+// The id an argmax writes.  A row whose logits hold no maximum (all NaN or
+// all -inf: only an overflow upstream makes them) leaves the merge's
+// sentinel index; the row then gets id 0 (all tied: the lowest index) and
+// gap 0, and the status word records ST_BOUNDS instead of an id past the
+// vocabulary reaching the caller.
+__device__ __forceinline__ int argmax_id(int i1, float& gap, int* status) {
+  if (i1 >= 0 && i1 != 0x7fffffff) return i1;
+  gap = 0.f;
+  atomicOr(status, ST_BOUNDS);
+  return 0;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -113,6 +125,9 @@ constexpr int kMaxTiles = 8192;   // 128-row weight tiles per projection launch
 // d_counters: [0, kMaxTiles) tile arrival counters (tensor-core LM head),
 // then the persistent kernel's grid barrier (kMaxTiles + 1) and the
 // streaming kernel's grid barrier (kMaxTiles + 2)
+// words: per-tile arrival counters; kMaxTiles + 1: the persistent draft
+// kernel's grid barrier; + 2: the streaming kernel's; + 3: a word nothing
+// writes (the bounded-wait self-test waits on it)
 constexpr int kCounters = kMaxTiles + 4;
 // phases of the persistent draft-block kernel: embed, 10 per layer, LM head
 // and its reduce
@@ -215,9 +230,11 @@ struct WLaunch {
 
 // 2-D TMA descriptor with the 128-byte swizzle (box_inner x element size must
 // be 128 bytes or less); dtype DFLASH_BF16 or DFLASH_F32.
+// swizzle128: 128-byte swizzled boxes (box_inner * element size <= 128);
+// false: plain row-major boxes (any inner size up to 256 elements)
 bool make_tmap_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-                  int dtype = DFLASH_BF16);
+                  int dtype = DFLASH_BF16, bool swizzle128 = true);
 size_t wstream_scratch_bytes(const dflash_handle* h, int M);
 int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float* partial,
             float4* amx);
@@ -246,7 +263,7 @@ struct ChainArgs {
   int32_t* ids;
   float* gap;
   float* x;                     // [R, D] fp32 residual
-  float* xg;                    // [R, D] space for bf16 residual x next RMSNorm gain
+  float* xg;                    // [R, D] fp32 residual x the next RMSNorm's gain
   void *q, *kb, *vb, *o, *a;    // bf16 [R, H*d], [R, G*d] x 2, [R, H*d], [R, F]
   float* ssq;                   // [D / 128, 16] sums of squares, 8 floats apart
   float* partial;               // split-K fix-up tiles
@@ -295,6 +312,8 @@ int head_norm_rope(dflash_handle* h, cudaStream_t s, int dtype, const float* in,
 int swiglu(dflash_handle* h, cudaStream_t s, int dtype, const float* g, const float* u, void* a,
            int64_t n);
 int cast_rows(dflash_handle* h, cudaStream_t s, int dtype, const float* in, void* out, int64_t n);
+// One bounded wait that nothing completes (see dflash_selftest_wait).
+int selftest_wait(dflash_handle* h, cudaStream_t s, int which, int64_t limit_ns);
 int advance_len(dflash_handle* h, cudaStream_t s, int32_t* len, const int32_t* nrows, int uniform,
                 int batch, int cap);
 // Attention of block rows over [cache(0..len) ; block] (draft) or cache(0..pos) (causal target).

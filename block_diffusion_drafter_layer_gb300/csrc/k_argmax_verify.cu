@@ -26,7 +26,7 @@ __device__ __forceinline__ Top2 merge_top2(Top2 a, Top2 b) {
 
 __global__ void __launch_bounds__(256) argmax_rows_kernel(const float* __restrict__ logits, int V,
                                                           int32_t* ids, float* gap, int rps_out,
-                                                          const int32_t* anchor) {
+                                                          const int32_t* anchor, int* status) {
   __shared__ Top2 part[8];
   const int64_t r = blockIdx.x;
   const float* z = logits + r * V;
@@ -63,8 +63,9 @@ __global__ void __launch_bounds__(256) argmax_rows_kernel(const float* __restric
       gout = b * per + (i - 1);
       if (i == 1) ids[b * rps_out] = anchor[b];
     }
-    ids[out] = a.i1;
-    if (gap) gap[gout] = a.t1 - a.t2;
+    float g = a.t1 - a.t2;
+    ids[out] = argmax_id(a.i1, g, status);
+    if (gap) gap[gout] = g;
   }
 }
 
@@ -73,7 +74,8 @@ int argmax_rows(dflash_handle* h, cudaStream_t s, const float* logits, int64_t r
   if (rows <= 0) return DFLASH_OK;
   Timer t;
   launch_begin(h, DFLASH_K_LM_HEAD, s, &t);
-  argmax_rows_kernel<<<(unsigned)rows, 256, 0, s>>>(logits, V, ids, gap, rows_per_seq_out, anchor);
+  argmax_rows_kernel<<<(unsigned)rows, 256, 0, s>>>(logits, V, ids, gap, rows_per_seq_out, anchor,
+                                                    h->d_status);
   return launch_end(h, s, &t);
 }
 

@@ -25,6 +25,11 @@
 #include "common.cuh"
 #include "ptx.cuh"
 
+// attention probabilities enter P V as a bf16 (hi, lo) pair (1) or as bf16 (0)
+#ifndef DFLASH_AT_PLO
+#define DFLASH_AT_PLO 1
+#endif
+
 namespace dflash {
 
 using namespace ptx;
@@ -382,16 +387,24 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
             acc[j][3] *= alpha[1];
           }
         }
-        // O += P V with P rounded to bf16 (the row sum above keeps fp32 P)
+        // O += P V with P as a bf16 pair hi + lo (hi = bf16(P), lo = bf16(P - hi):
+        // P to about 16 bits) when DFLASH_AT_PLO, else hi alone; the row sum
+        // above keeps fp32 P
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          uint32_t ph[4];
           const float* s0 = s[2 * kk];
           const float* s1 = s[2 * kk + 1];
-          ph[0] = pack_bf16(s0[0], s0[1]);
-          ph[1] = pack_bf16(s0[2], s0[3]);
-          ph[2] = pack_bf16(s1[0], s1[1]);
-          ph[3] = pack_bf16(s1[2], s1[3]);
+          const float v[8] = {s0[0], s0[1], s0[2], s0[3], s1[0], s1[1], s1[2], s1[3]};
+          float hi[8], lo[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            hi[q] = __bfloat162float(__float2bfloat16_rn(v[q]));
+            lo[q] = v[q] - hi[q];
+          }
+          const uint32_t ph[4] = {pack_bf16(hi[0], hi[1]), pack_bf16(hi[2], hi[3]),
+                                  pack_bf16(hi[4], hi[5]), pack_bf16(hi[6], hi[7])};
+          const uint32_t pl[4] = {pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]),
+                                  pack_bf16(lo[4], lo[5]), pack_bf16(lo[6], lo[7])};
 #pragma unroll
           for (int np = 0; np < NT / 2; ++np) {
             const int row = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -400,6 +413,10 @@ __global__ void __launch_bounds__(AT_THREADS, AT_CTAS_PER_SM) attn_split_kernel(
             ldsm_x4_t(sV + tile_off<DH>(row, ch), b0, b1, b2, b3);
             mma_bf16_16816(acc[2 * np], ph, b0, b1);
             mma_bf16_16816(acc[2 * np + 1], ph, b2, b3);
+            if (DFLASH_AT_PLO) {
+              mma_bf16_16816(acc[2 * np], pl, b0, b1);
+              mma_bf16_16816(acc[2 * np + 1], pl, b2, b3);
+            }
           }
         }
       }

@@ -22,12 +22,13 @@
 //   waits at a barrier (weights do not depend on activations); only the
 //   activation loads wait for the barrier.
 // * The RMSNorms in front of q/k/v, gate/up and the LM head are folded into
-//   those projections.  RMSNorm scales each row by one number, 1 / rms(x), so
-//   W (x g / rms) = (W (x g)) / rms: the residual epilogues (and the
-//   embedding) write the residual x, bf16(x * g) for the next norm's gain g,
-//   and one sum of squares of x per (128-column tile, row); the next
-//   projection multiplies bf16(x * g) like any other operand and its
-//   epilogue scales the fp32 rows by 1 / rms from those sums.
+//   those projections' operand loads.  The residual epilogues (and the
+//   embedding) write the residual x, x * g in fp32 for the next norm's gain
+//   g, and one sum of squares of x per (128-column tile, row).  The next
+//   projection takes 1 / rms of each row from those sums at its start
+//   (while its first fp32 (x * g) chunks are in flight) and its MMA warps
+//   round each chunk to bf16(x * g / rms) — the normalised row at the same
+//   storage point as a separate RMSNorm — before they multiply it.
 // * Attention cuts the keys of each (sequence, kv head) into equal runs of
 //   32-key sub-chunks, one run per work item, items dealt round-robin to the
 //   CTAs; each item keeps (max, sum, unnormalised output) per query row, and
@@ -49,7 +50,7 @@ using namespace ptx;
 #endif
 // attention probabilities enter P V as a bf16 (hi, lo) pair (1) or as bf16 (0)
 #ifndef DFLASH_CH_PLO
-#define DFLASH_CH_PLO 0
+#define DFLASH_CH_PLO 1
 #endif
 // pause of the producer lane between polls when nothing can be issued (ns)
 #ifndef DFLASH_CH_IDLE_NS
@@ -61,6 +62,8 @@ constexpr int CH_CT = 128;                 // consumer threads
 constexpr int CH_STAGES = DFLASH_CH_STAGES;
 constexpr int CH_W = 128 * 64 * 2;         // weight chunk: 128 rows x 64 k, bf16
 constexpr int CH_A = 16 * 64 * 2;          // activation chunk: 16 rows x 64 k, bf16
+constexpr int CH_AF = 16 * 64 * 4;         // fp32 (x * g) chunk of a normalised operand
+constexpr int CH_AS = CH_AF;               // ring bytes per activation stage
 constexpr int CH_DH = 128;                 // head dim of the attention phases
 constexpr int CH_AK = 32;                  // keys per attention sub-chunk
 constexpr int CH_DP = CH_DH + 4;           // attention partial row: max, sum, 2 pad, output
@@ -79,17 +82,18 @@ constexpr int CH_SSQ = DFLASH_CH_SSQ_STRIDE;
 // after attention(l) until this CTA has finished attention(l), and every
 // earlier ring entry has been consumed before attention(l) starts.
 constexpr int CH_OFF_A = CH_STAGES * CH_W;
-constexpr int CH_RING_BYTES = CH_OFF_A + CH_STAGES * CH_A;
+constexpr int CH_RING_BYTES = CH_OFF_A + CH_STAGES * CH_AS;
 constexpr int CH_OFF_ATT = 0;
 constexpr int CH_ATT_Q = 64 * CH_DH * 2;              // 64 query rows
 constexpr int CH_ATT_KV = CH_AK * CH_DH * 2;          // one K (or V) sub-chunk
 constexpr int CH_ATT_BYTES = CH_ATT_Q + 4 * CH_ATT_KV; // Q + 2 stages x (K, V)
 constexpr int CH_OFF_E = CH_RING_BYTES;               // fp32 output tile [16][CH_EPAD]
-constexpr int CH_OFF_BAR = CH_OFF_E + CH_ROWS * CH_EPAD * 4;
+constexpr int CH_OFF_BAR = CH_OFF_E + CH_ROWS * CH_EPAD * 4;   // full, empty per stage
 constexpr int CH_OFF_MISC = CH_OFF_BAR + 2 * CH_STAGES * 8;
 constexpr int CH_MISC_BYTES = 2048;
 constexpr int CH_SMEM = CH_OFF_MISC + CH_MISC_BYTES + 1024;
 static_assert(CH_ATT_BYTES <= CH_RING_BYTES, "the attention buffers alias the ring");
+static_assert(2 * CH_A <= CH_ROWS * CH_EPAD * 4, "the rounded operand buffers alias E");
 static_assert(CH_SMEM <= 233472 / 2 - 1024, "two CTAs per SM");
 
 enum ChainPhase : int {
@@ -115,7 +119,7 @@ struct ChainLayer {
 struct ChainParams {
   CUtensorMap map_hid[DFLASH_MAX_PICK];   // round: the pending target features [n_in, D], box 64 x 16
   CUtensorMap map_ht;         // round: the fused context feature H_t [n_in, D], box 64 x 16
-  CUtensorMap map_xg;         // bf16 x * g [R, D], box 64 x 16
+  CUtensorMap map_xg;         // fp32 x * g [R, D], box 64 x 16, unswizzled
   CUtensorMap map_o;          // bf16 attention output [R, H*d], box 64 x 16
   CUtensorMap map_a;          // bf16 SwiGLU output [R, F], box 64 x 16
   const CUtensorMap* wmaps;   // [n_layers * 7 + 2]: q k v o gate up down per layer, LM head, W_c
@@ -133,7 +137,7 @@ struct ChainParams {
   int32_t* ids;
   float* gap;
   float* x;
-  bf16* xg;
+  float* xg;
   bf16* q;
   bf16* kb;
   bf16* vb;
@@ -164,7 +168,7 @@ static_assert(sizeof(ChainParams) <= 4096, "kernel parameters must fit the 4 KB 
 // consumer thread 0, read by the producer).
 enum : int { MS_ABORT = 0, MS_LAST = 1, MS_ISSUED = 2, MS_CONSUMED = 3, MS_GO = 4, MS_ATT_DONE = 5 };
 // [0, 16) ints: flags; [16, 48): rowpos (sequence, position) per row;
-// [48, 64): rinv per row; [64, 192): attention item tables; [192, 384):
+// [48, 64): 1 / rms per row; [64, 192): attention item tables; [192, 384):
 // LM-head top-2 records, [4 warps][16 rows][3]; [384, 416): injpos
 // (sequence, cache position) per pending row of a round
 
@@ -192,8 +196,8 @@ __device__ __forceinline__ int phase_kind(const ChainParams& P, int p, int& l) {
   return kLayerSeq[q % kLayerPhases];
 }
 
-// nin: the phase's input RMSNorm is folded in (its operand is bf16(x * g);
-// the epilogue scales the fp32 result rows by 1 / rms(x))
+// nin: the phase's input RMSNorm is folded in (its operand arrives as fp32
+// x * g and is rounded to bf16(x * g / rms(x)) in shared memory)
 struct Geo {
   int n_tiles, kc, nin;
 };
@@ -260,19 +264,8 @@ __device__ __forceinline__ void unit_range(const ChainParams& P, int kind, int c
 // Phase p may start once every CTA has arrived p times.  Gives up (and flags
 // ST_TIMEOUT) after the wall-clock limit or as soon as another CTA has.
 __device__ bool grid_wait(const ChainParams& P, int target) {
-  const int* bar = P.counters + kMaxTiles + 1;
-  if (ld_acquire_gpu(bar) >= target) return true;
-  const uint64_t t0 = globaltimer();
-  for (int it = 0;; ++it) {
-    if (ld_acquire_gpu(bar) >= target) return true;
-    if ((it & 63) == 63) {
-      if (*(volatile int*)P.status & ST_TIMEOUT) return false;
-      if (globaltimer() - t0 > 2000000000ull) {
-        atomicOr(P.status, ST_TIMEOUT);
-        return false;
-      }
-    }
-  }
+  return bounded_wait_geq(P.counters + kMaxTiles + 1, target, P.status, ST_TIMEOUT,
+                          2000000000ull, 0);
 }
 
 // ---- producer ----------------------------------------------------------------
@@ -291,6 +284,7 @@ struct Cursor {
   // fusion's sources), and the attention phases the unit's weights wait for
   const CUtensorMap* amap;
   int aper, asrc, alk, att_need;
+  int abytes;   // activation bytes of a unit: CH_AF (fp32 x * g) or CH_A (bf16)
 };
 
 // Weight map(s) and row of the cursor's tile.
@@ -361,6 +355,7 @@ __device__ __forceinline__ bool cursor_phase(const ChainParams& P, Cursor& c, in
     }
     c.asrc = c.kk / c.aper;
     c.alk = c.kk - c.asrc * c.aper;
+    c.abytes = g.nin ? CH_AF : CH_A;
     // ring memory doubles as the attention buffers: a weight unit may be
     // loaded only once this CTA has finished every attention phase before
     // the unit's phase (q/k/v(l) follows attention(l-1); o_proj(l) onward
@@ -400,8 +395,11 @@ __device__ __forceinline__ void issue_a(const ChainParams& P, const Cursor& c, u
   tma_load_2d(dst, c.amap + c.asrc, bar, c.alk * 64, 0, pol);
 }
 
+struct Items;
+__device__ void prefetch_ctx_kv(const ChainParams& P, const Items* it, int l);
+
 template <bool RD>
-__device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full,
+__device__ void producer(const ChainParams& P, const Items* items, uint32_t sbase, uint32_t bar_full,
                          uint32_t bar_empty, volatile int* misc) {
   const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
   Cursor w{}, a{};
@@ -413,15 +411,22 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
   uint64_t t_idle = 0;
   uint32_t idle = 0;
   bool abort = false;
+  int pf_layer = -1;             // layers whose attention context is prefetched
   while (a_more) {
     bool prog = false;
+    // entering a layer's q/k/v weights: start its attention's cached K/V
+    // toward L2 (they depend on nothing this launch computes after them)
+    if (w_more && w.kind == PH_QKV && w.l > pf_layer) {
+      pf_layer = w.l;
+      prefetch_ctx_kv(P, items, w.l);
+    }
     const bool w_held = w_more && misc[MS_ATT_DONE] < w.att_need;
     if (w_more && !abort && !w_held) {
       const int s = w.i % CH_STAGES, use = w.i / CH_STAGES;
       // with no activation load owed, block in the barrier wait instead of spinning
       if (use == 0 || (a.i == w.i ? mbar_try_wait(bar_empty + 8 * s, (use - 1) & 1)
                                   : mbar_test_wait(bar_empty + 8 * s, (use - 1) & 1))) {
-        mbar_arrive_expect_tx(bar_full + 8 * s, CH_W + CH_A);
+        mbar_arrive_expect_tx(bar_full + 8 * s, CH_W + w.abytes);
         issue_w(P, w, sbase + s * CH_W, bar_full + 8 * s, pol_w);
         if (DFLASH_CH_EVLOG) {
           int e0, e1;
@@ -444,7 +449,7 @@ __device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full
       }
       if (ok) {
         const int s = a.i % CH_STAGES;
-        issue_a(P, a, sbase + CH_OFF_A + s * CH_A, bar_full + 8 * s, pol_a);
+        issue_a(P, a, sbase + CH_OFF_A + s * CH_AS, bar_full + 8 * s, pol_a);
         if (DFLASH_CH_EVLOG) {
           int e0, e1;
           unit_range(P, a.kind, blockIdx.x, e0, e1);
@@ -562,23 +567,16 @@ __device__ __forceinline__ RowIn row_in(const ChainParams& P, int kind, int t, i
   return in;
 }
 
-// ri: 1 / rms of row r where the phase's input norm is folded in (q/k/v,
-// gate/up, LM head: the operand was bf16(x * g), so the row of the product is
-// scaled here), else 1.
 __device__ __forceinline__ void row_apply(const ChainParams& P, int kind, int t, int r, float4 v,
-                                          float ri, float4 g, const RowIn& in, const int* rowpos,
+                                          float4 g, const RowIn& in, const int* rowpos,
                                           float* rec /* [16][3] of this warp */) {
   const int lane = threadIdx.x & 31;
-  v = make_float4(v.x * ri, v.y * ri, v.z * ri, v.w * ri);
   if (kind == PH_O || kind == PH_DN) {
     // x += v; x * g for the next norm; the row's sum of squares over the tile
     const float4 nv = make_float4(in.a.x + v.x, in.a.y + v.y, in.a.z + v.z, in.a.w + v.w);
     const int64_t off = (int64_t)r * P.D + t * 128 + 4 * lane;
     *(float4*)(P.x + off) = nv;
-    uint2 pk;
-    pk.x = pack_bf16(nv.x * g.x, nv.y * g.y);
-    pk.y = pack_bf16(nv.z * g.z, nv.w * g.w);
-    *(uint2*)(P.xg + off) = pk;
+    *(float4*)(P.xg + off) = make_float4(nv.x * g.x, nv.y * g.y, nv.z * g.z, nv.w * g.w);
     const float ss = warp_sum(nv.x * nv.x + nv.y * nv.y + nv.z * nv.z + nv.w * nv.w);
     if (lane == 0) P.ssq[(t * CH_ROWS + r) * CH_SSQ] = ss;
   } else if (kind == PH_GU) {
@@ -704,6 +702,34 @@ __device__ void rinv_rows(const ChainParams& P, float* rinv_s) {
   named_bar(1, CH_CT);
 }
 
+// A normalised operand's unit: round its fp32 (x * g) chunk [16 rows][64 k]
+// from the ring stage into the bf16 tile bf16(x * g / rms) at dst (the
+// 128-byte swizzled layout of the bf16 loads), one of two buffers at the
+// start of the epilogue tile E, which no TMA load writes.  A buffer is
+// rewritten two units later, after every warp has passed the barrier of the
+// unit between; after a flush (E rewritten and read by the epilogues)
+// `sync_first` waits for every warp first.  Every consumer thread takes the
+// barriers whatever `ok` says, so the warps stay in step after an abort.
+__device__ __forceinline__ void normalise_chunk(const uint8_t* st, uint8_t* dst,
+                                                const float* rinv_s, bool ok, bool sync_first) {
+  const int tid = threadIdx.x - 32;
+  if (sync_first) named_bar(1, CH_CT);
+  if (ok) {
+    const int c = tid & 15;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float4 f = ((const float4*)st)[tid + h * CH_CT];   // row tid / 16 + 8 h, k 4 c ..
+      const int r = (tid >> 4) + 8 * h;
+      const float ri = rinv_s[r];
+      uint2 pk;
+      pk.x = pack_bf16(f.x * ri, f.y * ri);
+      pk.y = pack_bf16(f.z * ri, f.w * ri);
+      *(uint2*)(dst + r * 128 + (((c >> 1) ^ (r & 7)) << 4) + (c & 1) * 8) = pk;
+    }
+  }
+  named_bar(1, CH_CT);   // the tile is complete before any warp reads it
+}
+
 // One projection phase: this CTA's units [u0, u1) of the phase's
 // (tile, k-chunk) grid.  A tile whose units this CTA owns entirely is
 // finished here (row epilogues); every other tile leaves this CTA's partial
@@ -723,9 +749,12 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
   float* E = (float*)(smem + CH_OFF_E);
   const int g = lane >> 2, tg = lane & 3;
   const int nrows = rows_of<RD>(P, kind);
-  bool have_rinv = false;   // 1 / rms of the rows, computed when a first tile finishes here
+  // 1 / rms of every row from the sums of squares the previous phases wrote
+  // (these loads overlap the first units' activation loads)
+  if (geo.nin) rinv_rows(P, rinv_s);
   float acc[4][4];
   int cur = -1, kbeg = 0, kend = 0;
+  bool flushed = false;   // E was written since the last rounded unit
 
   auto flush = [&](int t) -> void {
     named_bar(1, CH_CT);   // the previous tile's rows have been read out of E
@@ -738,10 +767,6 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
     named_bar(1, CH_CT);
     if (kbeg == 0 && kend == geo.kc) {
       // whole tile: finish its rows here (warp cw: rows cw, cw + 4, ...)
-      if (geo.nin && !have_rinv) {
-        rinv_rows(P, rinv_s);
-        have_rinv = true;
-      }
       const float4 gt = tile_gain(P, kind, l, t);
       RowIn in[4];
 #pragma unroll
@@ -756,8 +781,8 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
         if (RD && (kind == PH_FUSE || kind == PH_INJ))
           row_round(P, kind, t, r, *(const float4*)&E[r * CH_EPAD + 4 * lane], rowpos);
         else
-          row_apply(P, kind, t, r, *(const float4*)&E[r * CH_EPAD + 4 * lane],
-                    geo.nin ? rinv_s[r] : 1.f, gt, in[q], rowpos, recs + cw * 48);
+          row_apply(P, kind, t, r, *(const float4*)&E[r * CH_EPAD + 4 * lane], gt, in[q], rowpos,
+                    recs + cw * 48);
       }
     } else {
       const int slot_i = (uint32_t)u0 / (uint32_t)geo.kc == (uint32_t)t ? 0 : 1;
@@ -777,7 +802,10 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
       ++t;
     }
     if (t != cur) {
-      if (cur >= 0) flush(cur);
+      if (cur >= 0) {
+        flush(cur);
+        flushed = true;
+      }
       cur = t;
       kbeg = kk;
 #pragma unroll
@@ -785,15 +813,21 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
     }
     const int s = ri % CH_STAGES;
     kend = kk + 1;
-    if (misc[MS_ABORT]) continue;
-    if (!__any_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (ri / CH_STAGES) & 1))) {
+    bool ok = misc[MS_ABORT] == 0;
+    if (ok && !__any_sync(0xffffffffu, mbar_wait(bar_full + 8 * s, (ri / CH_STAGES) & 1))) {
       if (lane == 0) atomicOr(P.status, ST_TIMEOUT);
       misc[MS_ABORT] = 1;
-      continue;
+      ok = false;
     }
+    if (geo.nin) {
+      normalise_chunk(smem + CH_OFF_A + s * CH_AS, smem + CH_OFF_E + (u & 1) * CH_A, rinv_s, ok,
+                      flushed);
+      flushed = false;
+    }
+    if (!ok) continue;
     if (DFLASH_CH_EVLOG && tid == 0 && u - u0 < kEvUnits) ev(P, phase, 2 + (u - u0));
     const uint32_t wb = sbase + s * CH_W;
-    const uint32_t ab = sbase + CH_OFF_A + s * CH_A;
+    const uint32_t ab = geo.nin ? sbase + CH_OFF_E + (u & 1) * CH_A : sbase + CH_OFF_A + s * CH_AS;
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       uint32_t af[4];
@@ -836,15 +870,9 @@ __device__ void gemm_phase(const ChainParams& P, int phase, int kind, int l, int
 // (its first tile) except lo when lo began in an earlier tile (slot 1); with
 // fewer units than CTAs every unit has its own owner, holding t in slot 0.
 template <bool RD>
-__device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* rowpos, float* recs,
-                             float* rinv_s) {
+__device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* rowpos, float* recs) {
   const int warp = (threadIdx.x - 32) >> 5, lane = threadIdx.x & 31;
   const Geo geo = gemm_geo(P, kind);
-  // 1 / rms of each row: once per CTA where a warp may take several tasks;
-  // with at most one task per warp (q/k/v) it comes from the task's own load
-  // batch instead (one round trip fewer)
-  const bool rinv_in_task = geo.nin && geo.n_tiles * P.R <= P.grid * 4;
-  if (geo.nin && !rinv_in_task) rinv_rows(P, rinv_s);
   const uint32_t Uu = (uint32_t)geo.n_tiles * geo.kc;
   if (kind == PH_LM && Uu >= 2u * geo.kc * P.grid) {
     // At least two whole tiles' units per CTA: a split tile contains exactly
@@ -872,7 +900,7 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
         if (r >= P.R) break;
         const float4 sum = make_float4(0.f + va[q].x + vb[q].x, 0.f + va[q].y + vb[q].y,
                                        0.f + va[q].z + vb[q].z, 0.f + va[q].w + vb[q].w);
-        row_apply(P, kind, t, r, sum, rinv_s[r], make_float4(1.f, 1.f, 1.f, 1.f), none, rowpos,
+        row_apply(P, kind, t, r, sum, make_float4(1.f, 1.f, 1.f, 1.f), none, rowpos,
                   recs + warp * 48);
       }
     }
@@ -916,7 +944,7 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
           sum.z += v[j][q].z;
           sum.w += v[j][q].w;
         }
-        row_apply(P, kind, t, r, sum, rinv_s[r], make_float4(1.f, 1.f, 1.f, 1.f), none, rowpos,
+        row_apply(P, kind, t, r, sum, make_float4(1.f, 1.f, 1.f, 1.f), none, rowpos,
                   recs + warp * 48);
       }
     }
@@ -936,9 +964,6 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
     const bool lo_slot1 = dense && (uint32_t)lo * U / G < (uint32_t)t * kc;
     const float4 gt = tile_gain(P, kind, l, t);
     const RowIn in = row_in(P, kind, t, r, rowpos);
-    float ss = 0.f;
-    if (rinv_in_task)
-      for (int tt = lane; tt < P.D / 128; tt += 32) ss += __ldcg(P.ssq + (tt * CH_ROWS + r) * CH_SSQ);
     float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j0 = 0; j0 < n; j0 += RB) {
       float4 v[RB];
@@ -960,12 +985,10 @@ __device__ void reduce_phase(const ChainParams& P, int kind, int l, const int* r
         sum.w += v[j].w;
       }
     }
-    const float ri = !geo.nin ? 1.f
-                     : rinv_in_task ? 1.0f / sqrtf(warp_sum(ss) / (float)P.D + P.eps) : rinv_s[r];
     if (RD && (kind == PH_FUSE || kind == PH_INJ))
       row_round(P, kind, t, r, sum, rowpos);
     else
-      row_apply(P, kind, t, r, sum, ri, gt, in, rowpos, recs + warp * 48);
+      row_apply(P, kind, t, r, sum, gt, in, rowpos, recs + warp * 48);
   }
 }
 
@@ -1011,8 +1034,9 @@ __device__ void lm_merge(const ChainParams& P) {
     }
     tt = top2_warp(tt);
     if (lane == 0) {
-      P.ids[(int64_t)b * P.B + i] = tt.i1;
-      if (P.gap) P.gap[(int64_t)b * (P.B - 1) + i - 1] = tt.t1 - tt.t2;
+      float g = tt.t1 - tt.t2;
+      P.ids[(int64_t)b * P.B + i] = argmax_id(tt.i1, g, P.status);
+      if (P.gap) P.gap[(int64_t)b * (P.B - 1) + i - 1] = g;
     }
   }
 }
@@ -1067,6 +1091,23 @@ __device__ __forceinline__ ItemGeo item_geo(const ChainParams& P, const Items* i
   q.k_begin = run * it->chunk * CH_AK;
   q.k_end = min(q.L + P.B, q.k_begin + it->chunk * CH_AK);
   return q;
+}
+
+// L2 prefetch of the cached K and V entries of this CTA's attention items of
+// layer l (the keys below the item's context length; the block's own keys
+// are computed later).  An entry run of one (sequence, kv head) is
+// contiguous in the cache, 256 bytes a key.
+__device__ void prefetch_ctx_kv(const ChainParams& P, const Items* it, int l) {
+  const int total = min(it->total, P.n_items_max);
+  for (int j = blockIdx.x; j < total; j += P.grid) {
+    const ItemGeo ig = item_geo(P, it, j);
+    const int hi = min(ig.k_end, ig.L);
+    if (hi <= ig.k_begin) continue;
+    const int64_t off = (((int64_t)ig.b * P.G + ig.g) * P.cap + ig.k_begin) * CH_DH;
+    const uint32_t bytes = (uint32_t)(hi - ig.k_begin) * CH_DH * 2;
+    prefetch_l2_bulk(P.kc[l] + off, bytes);
+    prefetch_l2_bulk(P.vc[l] + off, bytes);
+  }
 }
 
 __device__ void attention_phase(const ChainParams& P, int phase, int l, const Items* it, uint8_t* smem,
@@ -1378,17 +1419,20 @@ __device__ void embed_phase(const ChainParams& P) {
     }
     *((float4*)(P.x + (int64_t)r * P.D + t * 128) + lane) = v;
     const float4 g4 = __ldg((const float4*)(P.lay[0].g_in + t * 128) + lane);
-    uint2 pk;
-    pk.x = pack_bf16(v.x * g4.x, v.y * g4.y);
-    pk.y = pack_bf16(v.z * g4.z, v.w * g4.w);
-    *((uint2*)(P.xg + (int64_t)r * P.D + t * 128) + lane) = pk;
+    *((float4*)(P.xg + (int64_t)r * P.D + t * 128) + lane) =
+        make_float4(v.x * g4.x, v.y * g4.y, v.z * g4.z, v.w * g4.w);
     const float ss = warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w);
     if (lane == 0) P.ssq[(t * CH_ROWS + r) * CH_SSQ] = ss;
   }
 }
 
+// Register budget of two CTAs of 192 threads per SM (170 a thread) although
+// 160 run: with it the compiler keeps every value in registers (168); with
+// the 204 that two CTAs of 160 would allow it chose 168 and spilled, and the
+// step took 13 us longer.
+constexpr int CH_REG_THREADS = 192;
 template <bool RD>
-__global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_constant__ ChainParams P) {
+__global__ void __launch_bounds__(CH_REG_THREADS, 2) chain_kernel(const __grid_constant__ ChainParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
@@ -1442,7 +1486,7 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
   __syncthreads();
 
   if (warp == 0) {
-    if (lane == 0) producer<RD>(P, sbase, bar_full, bar_empty, misc);
+    if (lane == 0) producer<RD>(P, items, sbase, bar_full, bar_empty, misc);
     __syncwarp();
   } else {
     const int tid = threadIdx.x - 32;
@@ -1455,6 +1499,7 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
           go = false;
         }
         misc[MS_GO] = go;
+
       }
       named_bar(1, CH_CT);
       if (!misc[MS_GO]) break;
@@ -1479,7 +1524,7 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
       } else if (kind == PH_RED) {
         int lp;
         const int pk = phase_kind<RD>(P, p - 1, lp);
-        reduce_phase<RD>(P, pk, lp, RD && pk == PH_INJ ? injpos : rowpos, recs, rinv_s);
+        reduce_phase<RD>(P, pk, lp, RD && pk == PH_INJ ? injpos : rowpos, recs);
         if (pk == PH_LM) lm_publish(P, recs);
       } else if (kind == PH_LMFIN) {
         lm_merge(P);
@@ -1493,7 +1538,7 @@ __global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_const
           named_bar(1, CH_CT);
         }
         gemm_phase<RD>(P, p, kind, l, ri, smem, sbase, bar_full, bar_empty, misc,
-                   RD && kind == PH_INJ ? injpos : rowpos, rinv_s, recs);
+                       RD && kind == PH_INJ ? injpos : rowpos, rinv_s, recs);
       }
       named_bar(1, CH_CT);
       if (tid == 0) {
@@ -1574,7 +1619,7 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
   const int D = c.hidden, Hd = c.n_heads * c.head_dim, Gd = c.n_kv_heads * c.head_dim, F = c.ffn;
   ChainParams P;
   memset(&P, 0, sizeof(P));
-  if (!make_tmap_2d(&P.map_xg, A.xg, D, R, (uint64_t)D * 2, 64, 16) ||
+  if (!make_tmap_2d(&P.map_xg, A.xg, D, R, (uint64_t)D * 4, 64, 16, DFLASH_F32, false) ||
       !make_tmap_2d(&P.map_o, A.o, Hd, R, (uint64_t)Hd * 2, 64, 16) ||
       !make_tmap_2d(&P.map_a, A.a, F, R, (uint64_t)F * 2, 64, 16))
     return DFLASH_ERR_CUDA;
@@ -1610,7 +1655,7 @@ int draft_chain(dflash_handle* h, cudaStream_t s, const ChainArgs& A) {
   P.ids = A.ids;
   P.gap = A.gap;
   P.x = A.x;
-  P.xg = (bf16*)A.xg;
+  P.xg = A.xg;
   P.q = (bf16*)A.q;
   P.kb = (bf16*)A.kb;
   P.vb = (bf16*)A.vb;

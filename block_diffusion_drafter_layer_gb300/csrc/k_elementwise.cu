@@ -2,6 +2,7 @@
 // q/k norm + RoPE (+ store into a dense buffer or a K/V cache), SwiGLU, and
 // cache-length bookkeeping.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace dflash {
 
@@ -298,6 +299,31 @@ int cast_rows(dflash_handle* h, cudaStream_t s, int dtype, const float* in, void
     cast_kernel<bf16><<<blocks, 256, 0, s>>>(in, (bf16*)out, n);
   else
     cast_kernel<float><<<blocks, 256, 0, s>>>(in, (float*)out, n);
+  return launch_end(h, s, &t);
+}
+
+// Bounded-wait self-test: one thread waits, limit_ns at most, on a wait that
+// nothing will complete, with the same routines the persistent kernels use —
+// which = 0: an mbarrier of this CTA that no thread arrives at; which = 1: a
+// device counter that nothing raises (the grid barrier's wait) — and the
+// timeout lands in the status word.
+__global__ void selftest_wait_kernel(const int* never, int* status, uint64_t limit_ns, int which) {
+  __shared__ __align__(8) uint64_t bar;
+  if (which == 0) {
+    const uint32_t b = ptx::smem_u32(&bar);
+    ptx::mbar_init(b, 1);
+    ptx::fence_barrier_init();
+    if (!ptx::mbar_wait(b, 0, limit_ns)) atomicOr(status, ST_TIMEOUT);
+  } else {
+    ptx::bounded_wait_geq(never, 1, status, ST_TIMEOUT, limit_ns, 0);
+  }
+}
+
+int selftest_wait(dflash_handle* h, cudaStream_t s, int which, int64_t limit_ns) {
+  Timer t;
+  launch_begin(h, DFLASH_K_ELEMENTWISE, s, &t);
+  selftest_wait_kernel<<<1, 1, 0, s>>>(h->d_counters + kMaxTiles + 3, h->d_status,
+                                       (uint64_t)limit_ns, which);
   return launch_end(h, s, &t);
 }
 

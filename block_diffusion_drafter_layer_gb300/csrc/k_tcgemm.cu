@@ -50,9 +50,10 @@ struct TcCfg {
   static constexpr int B_BYTES = BN * TC_BK * 2;   // 32 KB or 16 KB
   static constexpr int STAGE_TX = TC_A_BYTES + B_BYTES;
   static constexpr int OFF_B = STAGES * TC_A_BYTES;
-  static constexpr int OFF_GUARD = OFF_B + STAGES * B_BYTES;
-  static constexpr int GUARD = 16384;              // slack after the ring
-  static constexpr int OFF_BAR = OFF_GUARD + GUARD;
+  // every TMA load writes exactly one stage: the A box is 128 rows x 64 k,
+  // the B box(es) BN rows (or BN/2 gate rows + BN/2 up rows) x 64 k, and
+  // each launch pairs BN with weight maps of that box height
+  static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
   static constexpr int SMEM = OFF_BAR + 8 * (2 * STAGES + 4) + 64 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;   // two accumulators
 };
@@ -316,8 +317,9 @@ __device__ __forceinline__ void tc_merge_row(const TcParams& p, int row) {
     gout = b * per + (i - 1);
     if (i == 1) p.ids[b * p.rps_out] = p.anchor[b];
   }
-  p.ids[out] = i1;
-  if (p.gap) p.gap[gout] = t1 - t2;
+  float g = t1 - t2;
+  p.ids[out] = argmax_id(i1, g, p.status);
+  if (p.gap) p.gap[gout] = g;
 }
 
 // Persistent: CTA c takes tiles c, c + grid, ... in launch order; the ring

@@ -85,10 +85,13 @@ static_assert(sizeof(WParams) <= 4096, "kernel parameters must fit the 4 KB limi
 // CTAs per SM.  One, with the deeper ring it leaves room for: with two
 // co-resident CTAs a rare result error was seen (one consumer warp's 32
 // output columns of one tile, in a few of 300 identical LM-head launches),
-// never with one, and one is as fast.
+// never with one, and one is as fast.  Its cause has not been found, so
+// other values are refused.
 #ifndef DFLASH_WS_MINBLOCKS
 #define DFLASH_WS_MINBLOCKS 1
 #endif
+static_assert(DFLASH_WS_MINBLOCKS == 1,
+              "two streaming CTAs per SM gave rare wrong results whose cause is not located");
 
 template <int MT>
 struct WCfg {
@@ -378,18 +381,7 @@ __device__ void ws_row(const WParams& p, int t, int r, float4 v, const int* rowp
 
 // ---- grid barrier (bounded; every CTA of the grid is resident) ---------------
 __device__ bool ws_grid_wait(const WParams& p, int target) {
-  if (ld_acquire_gpu(p.bar) >= target) return true;
-  const uint64_t t0 = globaltimer();
-  for (int it = 0;; ++it) {
-    if (ld_acquire_gpu(p.bar) >= target) return true;
-    if ((it & 63) == 63) {
-      if (*(volatile int*)p.status & ST_TIMEOUT) return false;
-      if (globaltimer() - t0 > 2000000000ull) {
-        atomicOr(p.status, ST_TIMEOUT);
-        return false;
-      }
-    }
-  }
+  return bounded_wait_geq(p.bar, target, p.status, ST_TIMEOUT, 2000000000ull, 0);
 }
 // Consumers of every CTA arrive; true once all CTAs have arrived k times.
 // After a timeout (here or in another CTA) the CTA stops taking part.
@@ -482,8 +474,9 @@ __device__ void ws_merge(const WParams& p) {
         gout = b * per + (i - 1);
         if (i == 1) p.ids[b * p.rps_out] = p.anchor[b];
       }
-      p.ids[out] = tt.i1;
-      if (p.gap) p.gap[gout] = tt.t1 - tt.t2;
+      float g = tt.t1 - tt.t2;
+      p.ids[out] = argmax_id(tt.i1, g, p.status);
+      if (p.gap) p.gap[gout] = g;
     }
   }
 }

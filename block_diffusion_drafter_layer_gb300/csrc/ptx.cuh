@@ -57,6 +57,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   return true;
 }
 
+// mbar_wait for a waiter that expects to wait long: it sleeps sleep_ns
+// between polls, leaving the issue slots to the warps it shares them with.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint32_t sleep_ns,
+                                                uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    __nanosleep(sleep_ns);
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
 // Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -94,6 +107,27 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Wait until *word >= target (an acquire load per poll).  Gives up once
+// limit_ns of wall time has passed, recording timeout_bit in *status, or as
+// soon as another waiter has recorded it; sleep_ns > 0 pauses between polls.
+__device__ __forceinline__ bool bounded_wait_geq(const int* word, int target, int* status,
+                                                 int timeout_bit, uint64_t limit_ns,
+                                                 int sleep_ns) {
+  if (ld_acquire_gpu(word) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  for (int it = 0;; ++it) {
+    if (sleep_ns) __nanosleep(sleep_ns);
+    if (ld_acquire_gpu(word) >= target) return true;
+    if ((it & 63) == 63) {
+      if (*(volatile int*)status & timeout_bit) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        atomicOr(status, timeout_bit);
+        return false;
+      }
+    }
+  }
+}
+
 // ---- cp.async (16-byte, L2 only) ---------------------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
   const int n = pred ? 16 : 0;
@@ -129,6 +163,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 }
 
 // Prefetch a 2-D box into L2 (no shared memory, no completion to wait for).
+// Bring [p, p + bytes) toward L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),

@@ -36,6 +36,10 @@
  *     device can see (a sequence outgrowing its cache, a token id out of
  *     range, a position beyond the RoPE table) skip the offending writes and
  *     set the handle's device status word, read by dflash_get_status.
+ *   - An argmax over a row whose logits hold no maximum (all NaN or all
+ *     -inf: an overflow upstream) writes id 0 and gap 0 and records
+ *     DFLASH_ERR_DEVICE_BOUNDS, so no id past the vocabulary reaches the
+ *     caller.
  */
 #ifndef DFLASH_H
 #define DFLASH_H
@@ -388,6 +392,18 @@ int dflash_target_forward(dflash_handle* h, const int32_t* tokens, int32_t batch
 int dflash_lm_head_argmax_noalloc(dflash_handle* h, const float* x, int32_t rows,
                                   const float* norm_gain, int32_t* ids, float* top2_gap,
                                   dflash_stream_t s);
+
+/* Test of the failure handling (the paper has no counterpart).  Every wait
+ * inside the kernels is bounded: on running out it records
+ * DFLASH_ERR_DEVICE_TIMEOUT in the handle's status word and returns instead
+ * of hanging the GPU.  This call launches one thread that waits, at most
+ * limit_ns nanoseconds (1000 .. 1e9), with the kernels' own wait routines on
+ * something nothing will complete — which = 0: an mbarrier no thread
+ * arrives at; which = 1: a device counter nothing raises (the grid
+ * barrier's wait) — so the next dflash_get_status returns
+ * DFLASH_ERR_DEVICE_TIMEOUT, and the handle stays usable.  Asynchronous on
+ * s; DFLASH_ERR_INVALID_ARG for another which or limit. */
+int dflash_selftest_wait(dflash_handle* h, int32_t which, int64_t limit_ns, dflash_stream_t s);
 
 /* Synchronise stream s, then read and clear the handle's device status word.
  * Returns DFLASH_OK or the first device-detected error code. */

@@ -12,7 +12,7 @@ import torch
 
 import oracle as O
 import synth
-from helpers import make_all_accept, to_np, to_np64
+from helpers import make_all_accept, make_partial_accept, to_np, to_np64
 
 pytestmark = pytest.mark.gpu
 
@@ -58,12 +58,53 @@ def test_e2e_lossless_256_tokens(dfl):
     prompt = synth.random_ids(w.prompt_len, w.target.V, seed=w.seed).tolist()
     spec, ar_gpu, taus = _run(dfl, w, TW, DW, prompt, w.new_tokens)
     ar_ref = O.ar_generate(w.target, to_np64(TW), prompt, w.new_tokens)
+    ref, ref_taus = O.speculative_generate(w.target, to_np64(TW), w.draft, to_np64(DW), prompt,
+                                           w.new_tokens, w.B)
     hist = collections.Counter(taus)
     print(f"e2e: rounds {len(taus)}, mean tau {np.mean(taus):.3f}, "
           f"tau histogram {dict(sorted(hist.items()))}")
     np.testing.assert_array_equal(ar_gpu, ar_ref)
     np.testing.assert_array_equal(spec, ar_ref)
+    np.testing.assert_array_equal(ref, ar_ref)
+    assert list(taus) == list(ref_taus)
     assert all(1 <= t <= w.B for t in taus)
+
+
+def test_e2e_partial_acceptance(dfl):
+    """A planted greedy cycle that the draft matches one step at a time:
+    rounds accept one draft (tau = 2 of B = 16: the target cache is trimmed
+    inside the verified block and two rows carry over) or none.  Tokens equal
+    the oracle target's greedy decode, and the tau sequence equals the
+    oracle loop's, on the host-synchronised and the device-resident loops."""
+    from synth.gpu import draft_model, spec_decoder, target_model
+    w = synth.with_(synth.WORKLOADS["e2e_f32"], new_tokens=120)
+    TW, DW = _weights(w)
+    cycle = [11, 222, 3333, 444, 55, 666, 7]
+    TW, DW = make_partial_accept(TW, DW, w.target, cycle, m_index=2)
+    prompt = synth.random_ids(w.prompt_len - 1, w.target.V, seed=3).tolist() + [cycle[0]]
+    ar_ref = O.ar_generate(w.target, to_np64(TW), prompt, w.new_tokens)
+    ref, ref_taus = O.speculative_generate(w.target, to_np64(TW), w.draft, to_np64(DW), prompt,
+                                           w.new_tokens, w.B)
+    np.testing.assert_array_equal(ref, ar_ref)
+    assert 2 in ref_taus and 1 in ref_taus and max(ref_taus) == 2
+    Tg, Dg = _upload(TW), _upload(DW)
+    Dg["embed"], Dg["lm_head"] = Tg["embed"], Tg["lm_head"]
+    cap = w.prompt_len + w.new_tokens + 12 * w.B
+    target = target_model(w.target, w.dtype, Tg, max_pos=cap)
+    draft = draft_model(w.draft, w.dtype, Dg, max_pos=cap)
+    dec = spec_decoder(w, target, draft, cap=cap)
+    spec, taus = dec.generate(prompt, w.new_tokens)
+    res, res_taus = dec.generate_resident(prompt, w.new_tokens)
+    assert dfl.dflash_get_status(target.handle) == 0
+    assert dfl.dflash_get_status(draft.handle) == 0
+    target.close()
+    draft.close()
+    print(f"partial acceptance: {len(taus)} rounds, tau histogram "
+          f"{dict(sorted(collections.Counter(taus).items()))}")
+    np.testing.assert_array_equal(np.array(spec), ar_ref)
+    np.testing.assert_array_equal(np.array(res)[:w.new_tokens], ar_ref)
+    assert list(taus) == list(ref_taus)
+    assert list(res_taus)[:len(ref_taus)] == list(ref_taus)
 
 
 def test_e2e_lossless_all_blocks_accepted(dfl):

@@ -8,13 +8,14 @@ import torch
 
 import oracle as O
 import synth
-from helpers import float_parity, to_np, to_np64
+from helpers import F32_DRAWS, float_parity, oracle_block, to_np, to_np64
 from test_gpu_draft import SMALL_BF16, _compare
 
 pytestmark = pytest.mark.gpu
 
 
-def _round_case(dfl, w, B, lens, nrows):
+def _round_case(dfl, w, B, lens, nrows, compare=None):
+    """compare: test_gpu_draft._compare unless given (same arguments)."""
     from synth.gpu import draft_model, kv_cache
     s = w.draft
     dev = "cuda"
@@ -79,7 +80,7 @@ def _round_case(dfl, w, B, lens, nrows):
                 _, ek = float_parity(Kg[b, :, L:L + n].transpose(1, 0, 2), k, w.dtype, f"K l{l} b{b}")
                 _, ev = float_parity(Vg[b, :, L:L + n].transpose(1, 0, 2), v, w.dtype, f"V l{l} b{b}")
                 print(f"{label}: layer {l} seq {b}: K bit-equal {ek:.4f}, V {ev:.4f}")
-                assert ek > 0.95 and ev > 0.95
+                assert ek > 0.9 and ev > 0.9
             # the old context is untouched and nothing past the new length is written
             np.testing.assert_array_equal(Kg[b, :, :L], K0[l][b, :, :L])
             np.testing.assert_array_equal(Vg[b, :, :L], V0[l][b, :, :L])
@@ -93,10 +94,11 @@ def _round_case(dfl, w, B, lens, nrows):
     if B == 1:
         m.close()
         return
-    oids, ogap, ohid = O.draft_block(s, W, cK, cV, anchors, B, store, return_hidden=True)
-    _, g32, h32 = O.draft_block(s, W, cK, cV, anchors, B, O.f32, return_hidden=True)
-    _compare(w, ids, gap, hid, oids, ogap, ohid, label, (h32, g32), W)
     m.close()
+    o64 = oracle_block(s, W, cK, cV, anchors, B, store, with_logits=True)
+    o32 = ([oracle_block(s, W, cK, cV, anchors, B, store, arith=a) for a in F32_DRAWS]
+           if w.dtype == "bf16" else None)
+    (compare or _compare)(w, ids, gap, hid, o64, label, o32)
 
 
 @pytest.mark.parametrize("B,lens,nrows", [
