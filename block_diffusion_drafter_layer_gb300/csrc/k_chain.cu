@@ -57,7 +57,13 @@ using namespace ptx;
 #define DFLASH_CH_IDLE_NS 64
 #endif
 
-constexpr int CH_THREADS = 160;            // warp 0: TMA producer; warps 1-4: consumers
+// warp 0: TMA producer; warps 1-4: consumers; warp 5 only waits at the
+// kernel's final barrier.  The sixth warp measured 6 us faster per
+// Qwen3-8B-shaped round than five (same code otherwise, alternating builds),
+// with the register budget of 192 threads (below) also keeping every value
+// in registers; the likely cause is where the two CTAs' warps, the producers
+// among them, land on the SM's four sub-partitions.
+constexpr int CH_THREADS = 192;
 constexpr int CH_CT = 128;                 // consumer threads
 constexpr int CH_STAGES = DFLASH_CH_STAGES;
 constexpr int CH_W = 128 * 64 * 2;         // weight chunk: 128 rows x 64 k, bf16
@@ -395,11 +401,8 @@ __device__ __forceinline__ void issue_a(const ChainParams& P, const Cursor& c, u
   tma_load_2d(dst, c.amap + c.asrc, bar, c.alk * 64, 0, pol);
 }
 
-struct Items;
-__device__ void prefetch_ctx_kv(const ChainParams& P, const Items* it, int l);
-
 template <bool RD>
-__device__ void producer(const ChainParams& P, const Items* items, uint32_t sbase, uint32_t bar_full,
+__device__ void producer(const ChainParams& P, uint32_t sbase, uint32_t bar_full,
                          uint32_t bar_empty, volatile int* misc) {
   const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
   Cursor w{}, a{};
@@ -411,15 +414,8 @@ __device__ void producer(const ChainParams& P, const Items* items, uint32_t sbas
   uint64_t t_idle = 0;
   uint32_t idle = 0;
   bool abort = false;
-  int pf_layer = -1;             // layers whose attention context is prefetched
   while (a_more) {
     bool prog = false;
-    // entering a layer's q/k/v weights: start its attention's cached K/V
-    // toward L2 (they depend on nothing this launch computes after them)
-    if (w_more && w.kind == PH_QKV && w.l > pf_layer) {
-      pf_layer = w.l;
-      prefetch_ctx_kv(P, items, w.l);
-    }
     const bool w_held = w_more && misc[MS_ATT_DONE] < w.att_need;
     if (w_more && !abort && !w_held) {
       const int s = w.i % CH_STAGES, use = w.i / CH_STAGES;
@@ -1093,23 +1089,6 @@ __device__ __forceinline__ ItemGeo item_geo(const ChainParams& P, const Items* i
   return q;
 }
 
-// L2 prefetch of the cached K and V entries of this CTA's attention items of
-// layer l (the keys below the item's context length; the block's own keys
-// are computed later).  An entry run of one (sequence, kv head) is
-// contiguous in the cache, 256 bytes a key.
-__device__ void prefetch_ctx_kv(const ChainParams& P, const Items* it, int l) {
-  const int total = min(it->total, P.n_items_max);
-  for (int j = blockIdx.x; j < total; j += P.grid) {
-    const ItemGeo ig = item_geo(P, it, j);
-    const int hi = min(ig.k_end, ig.L);
-    if (hi <= ig.k_begin) continue;
-    const int64_t off = (((int64_t)ig.b * P.G + ig.g) * P.cap + ig.k_begin) * CH_DH;
-    const uint32_t bytes = (uint32_t)(hi - ig.k_begin) * CH_DH * 2;
-    prefetch_l2_bulk(P.kc[l] + off, bytes);
-    prefetch_l2_bulk(P.vc[l] + off, bytes);
-  }
-}
-
 __device__ void attention_phase(const ChainParams& P, int phase, int l, const Items* it, uint8_t* smem,
                                 const int* rowpos) {
   const int tid = threadIdx.x - 32, warp = tid >> 5, lane = threadIdx.x & 31;
@@ -1426,13 +1405,8 @@ __device__ void embed_phase(const ChainParams& P) {
   }
 }
 
-// Register budget of two CTAs of 192 threads per SM (170 a thread) although
-// 160 run: with it the compiler keeps every value in registers (168); with
-// the 204 that two CTAs of 160 would allow it chose 168 and spilled, and the
-// step took 13 us longer.
-constexpr int CH_REG_THREADS = 192;
 template <bool RD>
-__global__ void __launch_bounds__(CH_REG_THREADS, 2) chain_kernel(const __grid_constant__ ChainParams P) {
+__global__ void __launch_bounds__(CH_THREADS, 2) chain_kernel(const __grid_constant__ ChainParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
@@ -1486,8 +1460,10 @@ __global__ void __launch_bounds__(CH_REG_THREADS, 2) chain_kernel(const __grid_c
   __syncthreads();
 
   if (warp == 0) {
-    if (lane == 0) producer<RD>(P, items, sbase, bar_full, bar_empty, misc);
+    if (lane == 0) producer<RD>(P, sbase, bar_full, bar_empty, misc);
     __syncwarp();
+  } else if (warp == 5) {
+    // no work (see CH_THREADS)
   } else {
     const int tid = threadIdx.x - 32;
     int ri = 0;
