@@ -496,13 +496,17 @@ def run_trace(args):
     t0 = tr[0][0]
     print(f"# {w.name}: persistent draft-block launch, {len(tr)} phases; times in us from the "
           f"first CTA's start (device %globaltimer, ~1 us resolution)")
-    print("| phase | start | first CTA in -> last CTA done | gap after previous |")
-    print("|---|---|---|---|")
+    print("| phase | start | first CTA in -> last CTA done | gap after previous | last CTA in | "
+          "marks (latest over the grid, from the phase start) |")
+    print("|---|---|---|---|---|---|")
     prev = t0
     tot = {}
     for nm, row in zip(names, tr):
         s0, e1 = row[0], row[3]
-        print(f"| {nm} | {(s0 - t0) / 1e3:.1f} | {(e1 - s0) / 1e3:.2f} | {(s0 - prev) / 1e3:.2f} |")
+        marks = " ".join(f"{c}={(v - s0) / 1e3:.2f}" for c, v in
+                         zip(("mma_done", "a", "b", "c"), row[4:8]) if v)
+        print(f"| {nm} | {(s0 - t0) / 1e3:.1f} | {(e1 - s0) / 1e3:.2f} | {(s0 - prev) / 1e3:.2f} | "
+              f"{(row[1] - s0) / 1e3:.2f} | {marks} |")
         key = nm.split(" ", 2)[-1] if nm.startswith("layer") else nm
         tot[key] = tot.get(key, 0.0) + (e1 - prev) / 1e3
         prev = e1

@@ -349,7 +349,7 @@ def dflash_chain_trace_enable(h: int, on: bool):
 
 
 TRACE_COLS = ("first_start", "last_start", "first_end", "last_end", "mma_done",
-              "fixup_start", "fixup_sum", "epilogue_end")
+              "mark_a", "mark_b", "mark_c")
 
 
 def dflash_chain_trace_read(h: int, n: int = 128):
@@ -362,7 +362,7 @@ def dflash_chain_trace_read(h: int, n: int = 128):
     return [tuple(buf[k * i: k * i + k]) for i in range(min(np_.value, n))]
 
 
-EV_CTAS, EV_PHASES, EV_UNITS = 4, 164, 12
+EV_CTAS, EV_PHASES, EV_UNITS = 4, 169, 12
 EV_SLOTS = 2 + 4 * EV_UNITS
 
 
