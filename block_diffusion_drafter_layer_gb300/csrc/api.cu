@@ -784,7 +784,9 @@ int dflash_fuse_context(dflash_handle* h, const void* const* hidden, int64_t T, 
       const int64_t n = std::min(chunk, T - r0);
       WLaunch L;
       L.nmap = 1;
-      L.wmaps[0] = &h->map_tc_wc;
+      // CTA pairs load half of a 256-column tile's weight rows each
+      L.pair = tc_pair_units(h) > 0;
+      L.wmaps[0] = L.pair ? &h->map_wc : &h->map_tc_wc;
       L.nseg = 1;
       L.seg[0] = make_seg(0, D / 256, SK_F32, 0, D, Yc, D);
       L.nsrc = c.n_pick;
@@ -979,7 +981,7 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
       return rc;
     if (tcore) {
       if ((rc = qkv_tc(h, s, l, f, R, rm, kv->len))) return rc;
-      if ((rc = attention_fast(h, s, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch,
+      if ((rc = attention_fast(h, s, f.q, kv->k[l], kv->v[l], kv->cap, kv->batch_cap, kv->len, f.kb, f.vb, batch,
                                B, f.o, f.attn, layer_causal(c, l), layer_window(c, l))))
         return rc;
       if ((rc = mlp_tc(h, s, l, f, R))) return rc;
@@ -988,7 +990,7 @@ int dflash_draft_block(dflash_handle* h, const int32_t* anchor, int32_t batch, i
     if (stream) {
       if ((rc = qkv_stream(h, s, l, f, R, rm, kv->len))) return rc;
       if (attn_fast_ok(h, B))
-        rc = attention_fast(h, s, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch, B,
+        rc = attention_fast(h, s, f.q, kv->k[l], kv->v[l], kv->cap, kv->batch_cap, kv->len, f.kb, f.vb, batch, B,
                             f.o, f.attn, layer_causal(c, l), layer_window(c, l));
       else
         rc = attention(h, s, dt, f.q, kv->k[l], kv->v[l], kv->cap, kv->len, f.kb, f.vb, batch, B,

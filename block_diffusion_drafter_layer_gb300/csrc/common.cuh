@@ -129,12 +129,14 @@ constexpr int kMaxTiles = 8192;   // 128-row weight tiles per projection launch
 // kernel's grid barrier; + 2: the streaming kernel's; + 3: a word nothing
 // writes (the bounded-wait self-test waits on it)
 constexpr int kCounters = kMaxTiles + 4;
-// phases of the persistent draft-block kernel: embed, 10 per layer, LM head
-// and its reduce
-constexpr int kChainMaxPhases = 9 + 10 * DFLASH_MAX_LAYERS;   // 5 round phases, embed, layers, LM head
+// phases of the persistent draft-block kernel: 5 of a round, embed, 10 per
+// layer, the LM head, its reduce and the merge of its top-2 records
+constexpr int kChainMaxPhases = 9 + 10 * DFLASH_MAX_LAYERS;
 // timeline columns per phase: first start, last start, first end, last end,
-// last CTA done with its multiply-adds, and for the split-K fix-ups (the CTA
-// that completes a tile): latest fix-up start, sum done, epilogue done
+// last CTA done with its multiply-adds, then up to three phase-specific
+// marks, each the latest over the grid (projections: first unit done, half
+// of the units done; attention: first K/V sub-chunk in, arithmetic done,
+// partial written; combine: weights and outputs in)
 constexpr int kChainTraceCols = 8;
 // per-CTA event log of the persistent kernel (compiled in with
 // -DDFLASH_CH_EVLOG=1): kEvCtas sampled CTAs x kChainMaxPhases phases x
@@ -226,6 +228,7 @@ struct WLaunch {
   int rps_out = 0;
   const int32_t* anchor = nullptr;
   int bn = 256;         // tcgen05 kernel: output tile width (segment tiles and weight boxes match it)
+  bool pair = false;    // tcgen05 kernel: 256-row tiles on CTA pairs (bn 256, weight boxes of 128 rows)
 };
 
 // 2-D TMA descriptor with the 128-byte swizzle (box_inner x element size must
@@ -243,6 +246,8 @@ int wstream(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
 // Same launch description as wstream; 128 x 256 output tiles, SK_F32 and
 // SK_HEAD (d = 128) epilogues; segments are in units of 256 columns.
 int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float4* amx = nullptr);
+// CTA pairs of the tcgen05 kernel that can be resident at once (0: none)
+int tc_pair_units(const dflash_handle* h);
 
 // ---- split-K attention of the draft block (k_attention.cu) ------------------
 size_t attn_scratch_bytes(const dflash_handle* h, int batch, int B);
@@ -252,8 +257,8 @@ int attn_plan(dflash_handle* h, cudaStream_t s, const int32_t* len, int cap, int
               float* scratch);
 bool attn_fast_ok(const dflash_handle* h, int B);
 int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* kc, const void* vc,
-                   int cap, const int32_t* len, const void* kb, const void* vb, int batch, int B,
-                   void* o, float* scratch, int causal, int window);
+                   int cap, int kv_batch, const int32_t* len, const void* kb, const void* vb,
+                   int batch, int B, void* o, float* scratch, int causal, int window);
 
 // ---- persistent draft block for at most 16 rows (k_chain.cu) ----------------
 struct ChainArgs {

@@ -24,6 +24,7 @@
 // deterministic.
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tc05.cuh"
 
 // attention probabilities enter P V as a bf16 (hi, lo) pair (1) or as bf16 (0)
 #ifndef DFLASH_AT_PLO
@@ -109,7 +110,7 @@ size_t attn_scratch_bytes(const dflash_handle* h, int batch, int B) {
 
 // ---- plan: items of equal length over all units ----------------------------
 __global__ void __launch_bounds__(256) attn_plan_kernel(const int32_t* len, int batch, int B,
-                                                        int cap, int per_b, int slots,
+                                                        int cap, int per_b, int slots, int cmul,
                                                         int max_items, int* hdr, int* unit_begin,
                                                         AttnItem* items, int* status) {
   pdl_launch_dependents();
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(256) attn_plan_kernel(const int32_t* len, int 
     long long c = cw > AT_MIN_SUB ? cw : AT_MIN_SUB;
     const long long cm = (M + AT_MAX_ITEMS_UNIT - 1) / AT_MAX_ITEMS_UNIT;
     if (cm > c) c = cm;
+    c = (c + cmul - 1) / cmul * cmul;   // whole sub-chunks of the kernel that takes the items
     const int C = (int)c;
     int n = 0;
     for (int b = 0; b < batch; ++b) {
@@ -508,6 +510,387 @@ __global__ void __launch_bounds__(AT_COMB_WARPS * 32) attn_combine_kernel(const 
   *reinterpret_cast<uint2*>(dst) = pk;
 }
 
+// ---- the items on tcgen05 (blocks of 8, 16, 32 or 64 rows, d = 128) -----------
+// One CTA per SM walks the items like attn_split_kernel and writes the same
+// partials.  Per 128-key sub-chunk of an item: S = Q K^T on the tensor cores
+// (M = 128 with the unit's query rows in rows 0-63, N = 128 keys, K = d) into
+// one of two TMEM buffers; four softmax warps (TMEM lanes 0-63: a query row
+// per thread, each key half in its own warp) take the row max over the
+// sub-chunk, exchange it with the other half, and overwrite the S columns they
+// have read with P as a bf16 pair (hi = bf16(p), lo = bf16(p - hi));
+// O += P_hi V + P_lo V with A = P from TMEM and B = the V sub-chunk read
+// MN-major from shared memory accumulates in TMEM.  The max used in the
+// exponents moves only when a row's max rises by more than AT_TC_SLACK
+// (log2), so O is rescaled rarely (p <= 2^8) and the softmax of a sub-chunk
+// waits for the previous P V only then.  K/V sub-chunks of the cache (and
+// the block's own rows, last) arrive by TMA in a 3-stage ring; V rows at
+// positions >= len (stale cache memory) are zeroed before P V reads them.
+// Warp 2 lane 0 issues the MMAs, warp 3 lane 0 the loads.
+constexpr int AT_TC_THREADS = 192;
+constexpr int AT_TC_KSUB = 128;
+constexpr int AT_TC_STAGES = 3;
+constexpr int AT_TC_HALF = 16384;                   // 128 rows x 64 d (one 64-d half)
+constexpr int AT_TC_OFF_KV = 2 * AT_TC_HALF;        // after the Q tile
+constexpr int AT_TC_STAGE = 4 * AT_TC_HALF;         // K (two halves), then V
+constexpr int AT_TC_OFF_BAR = AT_TC_OFF_KV + AT_TC_STAGES * AT_TC_STAGE;
+// [3][2 halves][64 rows] floats: the row maxima of sub-chunks with S buffer
+// 0 and 1, then the row sums at the end of an item
+constexpr int AT_TC_OFF_RED = AT_TC_OFF_BAR + 128;
+constexpr int AT_TC_SMEM = AT_TC_OFF_RED + 3 * 2 * 64 * 4 + 1024;
+static_assert(AT_TC_SMEM <= 232448, "shared memory per CTA");
+// TMEM columns: S / P (two buffers), O
+constexpr uint32_t AT_TM_S = 0, AT_TM_O = 256, AT_TM_COLS = 512;
+constexpr float AT_TC_SLACK = 8.f;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// (lo, hi) -> bf16x2 with lo in the low half, round to nearest even
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+struct AttnTcParams {
+  AttnParams a;
+  CUtensorMap qmap;    // q [R, H d]: box 64 x B rows
+  CUtensorMap kmap;    // the K cache as [kv_batch G cap, d]: box 64 x 128
+  CUtensorMap vmap;
+  CUtensorMap kbmap;   // the block's K [R, G d]: box 64 x 16
+  CUtensorMap vbmap;
+  int nb;              // block rows loaded per unit: max(16, B)
+};
+
+// Geometry of an item: unit (b, g, query rows q0 ..), keys [k0, k1); nc cache
+// sub-chunks over [k0, min(k1, L)), then one block sub-chunk if k1 > L.
+struct TcGeo {
+  int b, g, q0, qrows, L, k0, k1, nc, nsub;
+};
+__device__ __forceinline__ TcGeo tc_geo(const AttnParams& p, const AttnItem& it) {
+  TcGeo q;
+  const int u = it.unit;
+  const int qg = u % p.qgroups, bg = u / p.qgroups;
+  q.g = bg % p.G;
+  q.b = bg / p.G;
+  q.q0 = qg * 64;
+  q.qrows = min(64, p.B * p.rep - q.q0);
+  q.L = p.len[q.b];
+  q.k0 = it.k0;
+  q.k1 = it.k1;
+  const int ce = min(q.k1, q.L);
+  q.nc = ce > q.k0 ? (ce - q.k0 + AT_TC_KSUB - 1) / AT_TC_KSUB : 0;
+  q.nsub = q.nc + (q.k1 > q.L ? 1 : 0);
+  return q;
+}
+
+__global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_constant__ AttnTcParams tp) {
+  const AttnParams& p = tp.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const uint32_t sQ = smem_u32(smem), sKV = sQ + AT_TC_OFF_KV;
+  const uint32_t bar = sQ + AT_TC_OFF_BAR;
+  // barriers: kv_full[3], kv_empty[3], q_full, q_empty, s_full[2], p_full, pv_done
+  const uint32_t b_kvf = bar, b_kve = bar + 24, b_qf = bar + 48, b_qe = bar + 56, b_sf = bar + 64,
+                 b_pf = bar + 80, b_pv = bar + 88;
+  volatile uint32_t* tmem_slot = (volatile uint32_t*)(smem + AT_TC_OFF_BAR + 96);
+  volatile int* abort_flag = (volatile int*)(smem + AT_TC_OFF_BAR + 100);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < AT_TC_STAGES; ++s) {
+      mbar_init(b_kvf + 8 * s, 1);
+      mbar_init(b_kve + 8 * s, 1);
+    }
+    mbar_init(b_qf, 1);
+    mbar_init(b_qe, 1);
+    mbar_init(b_sf, 1);
+    mbar_init(b_sf + 8, 1);
+    mbar_init(b_pf, 128);
+    mbar_init(b_pv, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32((const void*)tmem_slot)),
+                 "r"(AT_TM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int n_items = *p.n_items;
+  const int nb = tp.nb;
+  auto fail = [&]() {
+    atomicOr(p.status, ST_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 3) {
+    if (lane == 0) {
+      // ---- loads ----------------------------------------------------------------
+      int qn = 0, ni = 0;
+      for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x, ++ni) {
+        const TcGeo q = tc_geo(p, p.items[it]);
+        // the Q tile: rows hh * B - q0 .. of the heads hh that hold rows q0 .. q0 + qrows
+        if (ni > 0 && !mbar_wait(b_qe, (ni - 1) & 1)) { fail(); break; }
+        const int h0 = q.q0 / p.B, h1 = (q.q0 + q.qrows - 1) / p.B;
+        mbar_arrive_expect_tx(b_qf, (uint32_t)(2 * (h1 - h0 + 1) * p.B * 128));
+        for (int hh = h0; hh <= h1; ++hh)
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(sQ + h * AT_TC_HALF + (hh * p.B - q.q0) * 128, &tp.qmap, b_qf,
+                        (q.g * p.rep + hh) * 128 + h * 64, q.b * p.B, policy_evict_first());
+        for (int j = 0; j < q.nsub; ++j) {
+          const int qq = qn + j, st = qq % AT_TC_STAGES, use = qq / AT_TC_STAGES;
+          if (use > 0 && !mbar_wait(b_kve + 8 * st, (use - 1) & 1)) { fail(); break; }
+          const uint32_t dK = sKV + st * AT_TC_STAGE, dV = dK + 2 * AT_TC_HALF;
+          const uint32_t fb = b_kvf + 8 * st;
+          if (j < q.nc) {
+            const int key0 = q.k0 + j * AT_TC_KSUB;
+            const int row = (q.b * p.G + q.g) * p.cap + key0;
+            mbar_arrive_expect_tx(fb, 4 * AT_TC_HALF);
+            for (int h = 0; h < 2; ++h) {
+              tma_load_2d(dK + h * AT_TC_HALF, &tp.kmap, fb, h * 64, row, policy_evict_first());
+              tma_load_2d(dV + h * AT_TC_HALF, &tp.vmap, fb, h * 64, row, policy_evict_first());
+            }
+          } else {
+            mbar_arrive_expect_tx(fb, (uint32_t)(4 * nb * 128));
+            for (int i = 0; i < nb; i += 16)
+              for (int h = 0; h < 2; ++h) {
+                tma_load_2d(dK + h * AT_TC_HALF + i * 128, &tp.kbmap, fb, q.g * 128 + h * 64,
+                            q.b * p.B + i, policy_evict_first());
+                tma_load_2d(dV + h * AT_TC_HALF + i * 128, &tp.vbmap, fb, q.g * 128 + h * 64,
+                            q.b * p.B + i, policy_evict_first());
+              }
+          }
+        }
+        qn += q.nsub;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ---- MMAs -------------------------------------------------------------------
+      int qn = 0, ni = 0;
+      auto issue_s = [&](const TcGeo& q, int j) -> bool {
+        const int qq = qn + j, st = qq % AT_TC_STAGES;
+        if (!mbar_wait(b_kvf + 8 * st, (qq / AT_TC_STAGES) & 1)) return false;
+        tc_fence_after();
+        const int n = j < q.nc ? AT_TC_KSUB : nb;
+        const uint32_t idesc = idesc_bf16_f32(128, n);
+        const uint32_t dK = sKV + st * AT_TC_STAGE;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma(tmem + AT_TM_S + (qq & 1) * 128, sdesc_sw128(sQ + (kk >> 2) * AT_TC_HALF + (kk & 3) * 32),
+                 sdesc_sw128(dK + (kk >> 2) * AT_TC_HALF + (kk & 3) * 32), idesc, kk > 0);
+        tc_commit(b_sf + 8 * (qq & 1));
+        return true;
+      };
+      for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x, ++ni) {
+        const TcGeo q = tc_geo(p, p.items[it]);
+        if (!mbar_wait(b_qf, ni & 1)) { fail(); break; }
+        tc_fence_after();
+        bool ok = true;
+        for (int j = 0; ok && j < q.nsub && j < 2; ++j) ok = issue_s(q, j);
+        if (ok && q.nsub <= 2) tc_commit(b_qe);
+        for (int j = 0; ok && j < q.nsub; ++j) {
+          const int qq = qn + j, st = qq % AT_TC_STAGES;
+          if (!mbar_wait(b_pf, qq & 1)) { ok = false; break; }
+          tc_fence_after();
+          const int n = j < q.nc ? AT_TC_KSUB : nb;
+          const uint32_t idesc = idesc_bf16_f32_bmn(128, 128);
+          const uint32_t dV = sKV + st * AT_TC_STAGE + 2 * AT_TC_HALF;
+          // P of keys 32c .. 32c + 31: hi in S columns 32c .. 32c + 15, lo in the next 16
+          const uint32_t pb = tmem + AT_TM_S + (qq & 1) * 128;
+          for (int ks = 0; ks < n / 16; ++ks) {
+            const uint64_t vd = sdesc_sw128_lbo(dV + ks * 2048, AT_TC_HALF, 1024);
+            const uint32_t pa = pb + 32 * (ks >> 1) + 8 * (ks & 1);
+            tc_mma_ts(tmem + AT_TM_O, pa, vd, idesc, (j > 0 || ks > 0) ? 1u : 0u);
+            tc_mma_ts(tmem + AT_TM_O, pa + 16, vd, idesc, 1u);
+          }
+          tc_commit(b_kve + 8 * st);
+          tc_commit(b_pv);
+          if (j + 2 < q.nsub) {
+            ok = issue_s(q, j + 2);
+            if (ok && j + 2 == q.nsub - 1) tc_commit(b_qe);
+          }
+        }
+        if (!ok) { fail(); break; }
+        qn += q.nsub;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- softmax and partials: warps 0, 1 (keys 0-63 of a sub-chunk) and 4, 5
+    // (keys 64-127); thread = query row r of the tile (TMEM lane r) ----------
+    const int kh = warp >> 2;                        // key half
+    const int r = (warp & 1) * 32 + lane;
+    const int st_tid = kh * 64 + r;                  // 0 .. 127 over the four warps
+    const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+    float* red = (float*)(smem + AT_TC_OFF_RED);     // [3][2][64]
+    // After a timed-out wait the warps go on without waiting (results are
+    // void, the status says so) so that all four meet at every named barrier.
+    int qn = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      const TcGeo q = tc_geo(p, p.items[it]);
+      const bool row_ok = r < q.qrows;
+      const int qr = q.q0 + (row_ok ? r : 0), i = qr % p.B;
+      const int pq = q.L + i;
+      const int klo = p.window > 0 ? max(0, pq - p.window + 1) : 0;
+      const int khi = p.causal ? min(pq + 1, q.k1) : q.k1;
+      const int lo = max(q.k0, klo);   // visible keys of this row in the item: [lo, khi)
+      float m_use = -INFINITY, l = 0.f;
+      for (int j = 0; j < q.nsub; ++j) {
+        const int qq = qn + j, sb = qq & 1;
+        const bool cache = j < q.nc;
+        const int key0 = cache ? q.k0 + j * AT_TC_KSUB : q.L;
+        const int n = cache ? AT_TC_KSUB : nb;
+        // this row's visible columns of the sub-chunk: [vlo, vhi)
+        const int lim = cache ? q.L : q.L + p.B;
+        const int vlo = row_ok ? max(lo - key0, 0) : 0;
+        const int vhi = row_ok ? max(min(min(khi, lim) - key0, n), vlo) : 0;
+        const int c0 = kh * 64;   // this warp's columns c0 .. c0 + 63 (those below n)
+        const uint32_t sbuf = tmem + lanes + AT_TM_S + sb * 128;
+        if (ok) ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(b_sf + 8 * sb, (qq >> 1) & 1, 4000000000ull));
+        tc_fence_after();
+        // pass 1: the row max over this half's visible keys
+        float mx = -INFINITY;
+        float v[2][32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int cb = c0 + 32 * h;
+          if (cb < n) {
+            tc_ld32(sbuf + cb, v[h]);
+            if (vlo <= cb && vhi >= cb + 32) {
+              float m2 = v[h][0];
+#pragma unroll
+              for (int k = 1; k < 32; ++k) m2 = fmaxf(m2, v[h][k]);
+              mx = fmaxf(mx, m2);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                if (cb + k >= vlo && cb + k < vhi) mx = fmaxf(mx, v[h][k]);
+            }
+          }
+        }
+        red[(sb * 2 + kh) * 64 + r] = mx;
+        named_bar(1, 128);
+        mx = fmaxf(mx, red[(sb * 2 + (kh ^ 1)) * 64 + r]);
+        const float mnew = mx == -INFINITY ? m_use : fmaxf(m_use, mx * p.scale_log2);
+        const bool resc = mnew > m_use + AT_TC_SLACK || (m_use == -INFINITY && mnew > -INFINITY);
+        float alpha = 1.f;
+        if (resc) {
+          alpha = m_use == -INFINITY ? 0.f : ex2_approx(m_use - mnew);
+          m_use = mnew;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          // O holds every earlier sub-chunk's P V: rescale this half of its columns
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_pv, (qq - 1) & 1, 4000000000ull));
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            float o[32];
+            tc_ld32(tmem + lanes + AT_TM_O + kh * 64 + c * 32, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= alpha;
+            tc_st32(tmem + lanes + AT_TM_O + kh * 64 + c * 32, o);
+          }
+        }
+        l *= alpha;
+        // pass 2: p = 2^(s * scale - m_use) for visible keys as (hi, lo) bf16
+        // pairs, over the S columns just read
+        const float sc = p.scale_log2, nm = m_use == -INFINITY ? 0.f : -m_use;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int cb = c0 + 32 * h;
+          if (cb < n) {
+            const bool all = vlo <= cb && vhi >= cb + 32 && m_use > -INFINITY;
+            uint32_t ph[16], pl[16];
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              float e0 = ex2_approx(fmaf(v[h][k], sc, nm));
+              float e1 = ex2_approx(fmaf(v[h][k + 1], sc, nm));
+              if (!all) {
+                const bool m0 = m_use > -INFINITY && cb + k >= vlo && cb + k < vhi;
+                const bool m1 = m_use > -INFINITY && cb + k + 1 >= vlo && cb + k + 1 < vhi;
+                e0 = m0 ? e0 : 0.f;
+                e1 = m1 ? e1 : 0.f;
+              }
+              l += e0 + e1;
+              const uint32_t hi = bf16x2_rn(e0, e1);
+              const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+              ph[k >> 1] = hi;
+              pl[k >> 1] = bf16x2_rn(e0 - h0, e1 - h1);
+            }
+            // columns 32c .. 32c + 15 take hi of keys 32c .. 32c + 31 (two per column),
+            // the next 16 columns lo
+            tc_st16(sbuf + cb, ph);
+            tc_st16(sbuf + cb + 16, pl);
+          }
+        }
+        // V rows at positions >= len in a cache sub-chunk: stale memory, zeroed
+        if (cache && key0 + AT_TC_KSUB > q.L) {
+          const int st = qq % AT_TC_STAGES;
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_kvf + 8 * st, (qq / AT_TC_STAGES) & 1));
+          const int z0 = max(0, q.L - key0);
+          uint8_t* dV = smem + AT_TC_OFF_KV + st * AT_TC_STAGE + 2 * AT_TC_HALF;
+          for (int e = st_tid; e < (AT_TC_KSUB - z0) * 16; e += 128) {
+            const int row = z0 + (e >> 4), c16 = e & 15;
+            *(uint4*)(dV + (c16 >> 3) * AT_TC_HALF + row * 128 + (c16 & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(b_pf);
+      }
+      qn += q.nsub;
+      // the item's partial: (max, sum, unnormalised O) of this row; each half
+      // writes its 64 columns of O, half 0 the row's (max, sum of both halves)
+      red[(4 + kh) * 64 + r] = l;
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_pv, (qn - 1) & 1, 4000000000ull));
+      tc_fence_after();
+      named_bar(1, 128);
+      float* part = p.part + ((int64_t)it * 64 + r) * AT_DP;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        float o[32];
+        tc_ld32(tmem + lanes + AT_TM_O + kh * 64 + c * 32, o);
+        if (row_ok) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            __stcg((float4*)&part[4 + kh * 64 + c * 32 + k], make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]));
+        }
+      }
+      if (row_ok && kh == 0) __stcg((float2*)part, make_float2(m_use, l + red[5 * 64 + r]));
+      tc_fence_before();
+      named_bar(1, 128);   // the sums are read before the next item writes them
+    }
+    if (!ok) fail();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    // loads or MMAs may still be in flight: let them land (bounded) before
+    // the shared memory and TMEM are released
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 200000ull) __nanosleep(1000);
+  }
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(AT_TM_COLS)
+                 : "memory");
+  }
+}
+
 bool attn_fast_ok(const dflash_handle* h, int B) {
   const dflash_config& c = h->cfg;
   return c.dtype == DFLASH_BF16 && c.head_dim == 128 && h->num_sms > 0 && B >= 1;
@@ -526,6 +909,17 @@ static void pdl_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, dim3 
   cfg->numAttrs = 1;
 }
 
+// The tcgen05 items kernel: bf16, d = 128, blocks of 8, 16, 32 or 64 rows
+// (whole 8-row groups per query head in the 64-row tile).
+#ifndef DFLASH_AT_TC
+#define DFLASH_AT_TC 1
+#endif
+static bool attn_tc_ok(const dflash_handle* h, int B) {
+  const dflash_config& c = h->cfg;
+  return DFLASH_AT_TC && c.dtype == DFLASH_BF16 && c.head_dim == 128 &&
+         (B == 8 || B == 16 || B == 32 || B == 64) && h->num_sms > 0;
+}
+
 int attn_plan(dflash_handle* h, cudaStream_t s, const int32_t* len, int cap, int batch, int B,
               float* scratch) {
   const dflash_config& c = h->cfg;
@@ -539,14 +933,17 @@ int attn_plan(dflash_handle* h, cudaStream_t s, const int32_t* len, int cap, int
   pdl_config(&cfg, attr, dim3(1), dim3(256), 0, s);
   Timer t;
   launch_begin(h, DFLASH_K_ATTENTION, s, &t);
+  // the tcgen05 kernel: one CTA per SM, items of whole 128-key sub-chunks
+  const bool tc = attn_tc_ok(h, B);
   cudaLaunchKernelEx(&cfg, attn_plan_kernel, len, batch, B, cap, c.n_kv_heads * qgroups,
-                     attn_slots(h), (int)mi, sc.hdr, sc.unit_begin, sc.items, h->d_status);
+                     tc ? h->num_sms : attn_slots(h), tc ? 2 : 1, (int)mi, sc.hdr, sc.unit_begin,
+                     sc.items, h->d_status);
   return launch_end(h, s, &t);
 }
 
 int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* kc, const void* vc,
-                   int cap, const int32_t* len, const void* kb, const void* vb, int batch, int B,
-                   void* o, float* scratch, int causal, int window) {
+                   int cap, int kv_batch, const int32_t* len, const void* kb, const void* vb,
+                   int batch, int B, void* o, float* scratch, int causal, int window) {
   const dflash_config& c = h->cfg;
   constexpr int DH = 128;
   const int units = attn_units(h, batch, B);
@@ -574,6 +971,40 @@ int attention_fast(dflash_handle* h, cudaStream_t s, const void* q, const void* 
   p.unit_begin = sc.unit_begin;
   p.part = sc.part;
   p.status = h->d_status;
+  if (attn_tc_ok(h, B)) {
+    AttnTcParams tp;
+    memset(&tp, 0, sizeof(tp));
+    tp.a = p;
+    tp.nb = std::max(16, B);
+    const uint64_t Hd = (uint64_t)p.H * DH, Gd = (uint64_t)p.G * DH, R = (uint64_t)batch * B;
+    if (!make_tmap_2d(&tp.qmap, q, Hd, R, Hd * 2, 64, (uint32_t)B) ||
+        !make_tmap_2d(&tp.kmap, kc, DH, (uint64_t)kv_batch * p.G * cap, DH * 2, 64, AT_TC_KSUB) ||
+        !make_tmap_2d(&tp.vmap, vc, DH, (uint64_t)kv_batch * p.G * cap, DH * 2, 64, AT_TC_KSUB) ||
+        !make_tmap_2d(&tp.kbmap, kb, Gd, R, Gd * 2, 64, 16) ||
+        !make_tmap_2d(&tp.vbmap, vb, Gd, R, Gd * 2, 64, 16))
+      return DFLASH_ERR_CUDA;
+    static bool tc_attr = false;
+    if (!tc_attr) {
+      if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               AT_TC_SMEM) != cudaSuccess)
+        return DFLASH_ERR_CUDA;
+      tc_attr = true;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    pdl_config(&cfg, attr, dim3((unsigned)std::min<int64_t>(mi, h->num_sms)), dim3(AT_TC_THREADS),
+               AT_TC_SMEM, s);
+    Timer t;
+    launch_begin(h, DFLASH_K_ATTENTION, s, &t);
+    cudaLaunchKernelEx(&cfg, attn_tc_kernel, tp);
+    int rc = launch_end(h, s, &t);
+    if (rc) return rc;
+    const int cgrid = (units * 64 + AT_COMB_WARPS - 1) / AT_COMB_WARPS;
+    pdl_config(&cfg, attr, dim3(cgrid), dim3(AT_COMB_WARPS * 32), 0, s);
+    launch_begin(h, DFLASH_K_ATTENTION, s, &t);
+    cudaLaunchKernelEx(&cfg, attn_combine_kernel<DH>, p);
+    return launch_end(h, s, &t);
+  }
   // Q + AT_STAGES x (K, V) sub-chunks
   const size_t smem = (size_t)(64 + 2 * AT_STAGES * AT_KSUB) * DH * 2 + 128;
   static bool attr_set = false;

@@ -22,6 +22,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tc05.cuh"
 
 namespace dflash {
 
@@ -42,22 +43,29 @@ constexpr int TC_BM = 128, TC_BK = 64;
 constexpr int TC_THREADS = 192;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;   // 16 KB
 
-// Shared-memory layout of the ring for a BN-column tile.
-template <int BN>
+// Shared-memory layout of the ring for a BN-column tile.  PAIR: a cluster of
+// two CTAs computes a 256-row tile with one tcgen05.mma.cta_group::2 stream
+// (issued by the even CTA): each CTA loads its own 128 activation rows and
+// half of the tile's weight rows, and holds its 128 rows of the accumulator.
+template <int BN, bool PAIR = false>
 struct TcCfg {
   static_assert(BN == 128 || BN == 256, "tile width");
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
-  static constexpr int B_BYTES = BN * TC_BK * 2;   // 32 KB or 16 KB
-  static constexpr int STAGE_TX = TC_A_BYTES + B_BYTES;
+  static_assert(!PAIR || BN == 256, "CTA pairs take 256-column tiles");
+  static constexpr int BM = PAIR ? 2 * TC_BM : TC_BM;          // rows of a tile
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;           // weight rows a CTA loads per stage
+  static constexpr int B_BYTES = B_ROWS * TC_BK * 2;
+  static constexpr int STAGE_TX = TC_A_BYTES + B_BYTES;       // bytes a CTA loads per stage
+  static constexpr int STAGES = 196608 / STAGE_TX;            // 4 (256), 6 (128 or a pair)
   static constexpr int OFF_B = STAGES * TC_A_BYTES;
   // every TMA load writes exactly one stage: the A box is 128 rows x 64 k,
-  // the B box(es) BN rows (or BN/2 gate rows + BN/2 up rows) x 64 k, and
-  // each launch pairs BN with weight maps of that box height
+  // the B box(es) B_ROWS rows (or B_ROWS/2 gate rows + B_ROWS/2 up rows) x
+  // 64 k, and each launch pairs the tile with weight maps of that box height
   static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
   static constexpr int SMEM = OFF_BAR + 8 * (2 * STAGES + 4) + 64 + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN;   // two accumulators
 };
-static_assert(TcCfg<256>::SMEM <= 232448 && TcCfg<128>::SMEM <= 232448, "shared memory per CTA");
+static_assert(TcCfg<256>::SMEM <= 232448 && TcCfg<128>::SMEM <= 232448 &&
+                  TcCfg<256, true>::SMEM <= 232448, "shared memory per CTA");
 
 struct TcParams {
   CUtensorMap amap[WS_MAXSRC];
@@ -78,60 +86,6 @@ struct TcParams {
   const int32_t* anchor;
 };
 static_assert(sizeof(TcParams) <= 4096, "kernel parameters must fit the 4 KB limit");
-
-// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
-// the 128-byte swizzle: rows of 128 B, 8-row groups 1024 B apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);        // start address
-  d |= (uint64_t)1u << 16;                          // leading byte offset (unused here)
-  d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset: 8 rows x 128 B
-  d |= (uint64_t)1u << 46;                          // descriptor version
-  d |= (uint64_t)2u << 61;                          // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor: kind::f16, bf16 A and B (K-major), fp32 D, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-// 32 lanes x 32 consecutive fp32 columns: thread t gets lane (base lane + t).
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 __device__ __forceinline__ int tc_seg_of(const TcParams& p, int t) {
   int s = 0;
@@ -322,12 +276,12 @@ __device__ __forceinline__ void tc_merge_row(const TcParams& p, int row) {
   if (p.gap) p.gap[gout] = g;
 }
 
-// Persistent: CTA c takes tiles c, c + grid, ... in launch order; the ring
-// runs on across its tiles and two TMEM accumulators let the epilogue of
-// one tile overlap the MMAs of the next.
-template <int BN>
+// Persistent: CTA c (a pair: cluster c) takes tiles c, c + grid, ... in
+// launch order; the ring runs on across its tiles and two TMEM accumulators
+// let the epilogue of one tile overlap the MMAs of the next.
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, PAIR>;
   constexpr int TC_STAGES = C::STAGES, TC_B_BYTES = C::B_BYTES;
   constexpr int TC_STAGE_TX = C::STAGE_TX, TC_OFF_B = C::OFF_B, TC_OFF_BAR = C::OFF_BAR;
   constexpr uint32_t TC_TMEM_COLS = C::TMEM_COLS;
@@ -335,7 +289,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
   // ring full / empty per stage; accumulator full (MMA commit) / empty (the
-  // four epilogue warps) per TMEM buffer
+  // four epilogue warps, of both CTAs of a pair) per TMEM buffer
   const uint32_t bar_full = sbase + TC_OFF_BAR, bar_empty = bar_full + 8 * TC_STAGES,
                  bar_tfull = bar_empty + 8 * TC_STAGES, bar_tempty = bar_tfull + 16;
   volatile uint32_t* tmem_slot = (volatile uint32_t*)(smem + TC_OFF_BAR + 8 * (2 * TC_STAGES + 4));
@@ -343,13 +297,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
   volatile int* last_flag = (volatile int*)(tmem_slot + 2);
   volatile int* kcount = (volatile int*)(tmem_slot + 3);   // k-blocks issued, consumed
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a pair: the even CTA (rank 0) issues the MMAs; the loads of both CTAs
+  // complete on its full barriers and both epilogues free its accumulators
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const uint32_t bar_full_l = PAIR ? mapa_shared(bar_full, 0) : bar_full;
+  const uint32_t bar_tempty_l = PAIR ? mapa_shared(bar_tempty, 0) : bar_tempty;
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const int nk = p.K / TC_BK;
   const int tiles = p.n_mtiles * p.n_ntiles;
-  const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int my_tiles = unit < tiles ? (tiles - 1 - unit) / units + 1 : 0;
   // m_fast: the row tiles that share a weight column tile run side by side,
   // so the column comes from HBM once and from L2 for the others
   auto tile_of = [&](int j, int& mt, int& nt) {
-    const int t = (int)blockIdx.x + j * (int)gridDim.x;
+    const int t = unit + j * units;
     mt = p.m_fast ? t % p.n_mtiles : t / p.n_ntiles;
     nt = p.m_fast ? t / p.n_mtiles : t - mt * p.n_ntiles;
   };
@@ -361,21 +322,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
-      mbar_init(bar_tempty + 8 * b, 4);
+      mbar_init(bar_tempty + 8 * b, PAIR ? 8 : 4);
     }
     *abort_flag = 0;
     kcount[0] = kcount[1] = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32((const void*)tmem_slot)),
-                 "r"(TC_TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (PAIR) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32((const void*)tmem_slot)),
+                   "r"(TC_TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32((const void*)tmem_slot)),
+                   "r"(TC_TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();   // both CTAs' barriers and TMEM exist before either signals the other
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) pdl_launch_dependents();
@@ -383,7 +353,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
   if (warp == 0) {
     if (lane == 0) {
       // ---- producer -------------------------------------------------------------
-      const uint64_t pol_w = policy_evict_last(), pol_a = policy_evict_last();
+      // the operand other CTAs read again later stays in L2: the activations
+      // when consecutive CTAs share a weight column tile (every column tile
+      // re-reads them), the weights otherwise
+      const uint64_t pol_w = p.m_fast ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_a = p.m_fast ? policy_evict_last() : policy_evict_first();
+      auto load = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                      uint64_t pol) {
+        if (PAIR) tma_load_2d_pair(dst, map, bar, c0, c1, pol);
+        else tma_load_2d(dst, map, bar, c0, c1, pol);
+      };
       pdl_wait();
       int kg = 0;   // k-blocks issued over this CTA's tiles
       for (int j = 0; j < my_tiles && !*abort_flag; ++j) {
@@ -391,6 +370,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         tile_of(j, mt, nt);
         const WSeg& g = p.seg[tc_seg_of(p, nt)];
         const int lt = nt - g.t0;
+        const int arow = mt * C::BM + (int)rank * TC_BM;
         for (int kb = 0; kb < nk; ++kb, ++kg) {
           const int s = kg % TC_STAGES, use = kg / TC_STAGES;
           if (use > 0 && !mbar_wait(bar_empty + 8 * s, (use - 1) & 1)) {
@@ -399,18 +379,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             break;
           }
           if (*abort_flag) break;
-          mbar_arrive_expect_tx(bar_full + 8 * s, TC_STAGE_TX);
+          if (rank == 0) mbar_arrive_expect_tx(bar_full + 8 * s, (PAIR ? 2 : 1) * TC_STAGE_TX);
+          const uint32_t fb = bar_full_l + 8 * s;
           const int src = kb / p.kc_per_src, lk = kb - src * p.kc_per_src;
-          tma_load_2d(sbase + s * TC_A_BYTES, &p.amap[src], bar_full + 8 * s, lk * TC_BK,
-                      mt * TC_BM, pol_a);
-          if (g.kind == SK_SWIGLU) {   // BN/2 gate rows then the same BN/2 up rows
-            tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES, &p.bmap[g.map], bar_full + 8 * s,
-                        kb * TC_BK, lt * (BN / 2), pol_w);
-            tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES + TC_B_BYTES / 2, &p.bmap[g.map2],
-                        bar_full + 8 * s, kb * TC_BK, lt * (BN / 2), pol_w);
+          load(sbase + s * TC_A_BYTES, &p.amap[src], fb, lk * TC_BK, arow, pol_a);
+          const uint32_t bdst = sbase + TC_OFF_B + s * TC_B_BYTES;
+          if (g.kind == SK_SWIGLU) {
+            // gate and up rows of the tile's BN/2 FFN columns: a pair's even
+            // CTA loads the gate rows, the odd one the up rows
+            if (PAIR) {
+              load(bdst, &p.bmap[rank ? g.map2 : g.map], fb, kb * TC_BK, lt * (BN / 2), pol_w);
+            } else {
+              load(bdst, &p.bmap[g.map], fb, kb * TC_BK, lt * (BN / 2), pol_w);
+              load(bdst + TC_B_BYTES / 2, &p.bmap[g.map2], fb, kb * TC_BK, lt * (BN / 2), pol_w);
+            }
           } else {
-            tma_load_2d(sbase + TC_OFF_B + s * TC_B_BYTES, &p.bmap[g.map], bar_full + 8 * s,
-                        kb * TC_BK, lt * BN, pol_w);
+            load(bdst, &p.bmap[g.map], fb, kb * TC_BK, lt * BN + (int)rank * C::B_ROWS, pol_w);
           }
         }
       }
@@ -418,14 +402,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ---- MMA issuer: tile j accumulates into TMEM buffer j & 1 -----------------
-      const uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
+      const uint32_t idesc = idesc_bf16_f32(C::BM, BN);
       int kg = 0;   // k-blocks consumed
       for (int j = 0; j < my_tiles; ++j) {
         const int b = j & 1, ub = j >> 1;
         if (*abort_flag) break;
-        // the epilogue of tile j - 2 has read this buffer
+        // the epilogue(s) of tile j - 2 have read this buffer
         if (ub > 0 && !mbar_wait(bar_tempty + 8 * b, (ub - 1) & 1)) {
           atomicOr(p.status, ST_TIMEOUT);
           *abort_flag = 1;
@@ -445,13 +429,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
           tc_fence_after();
           const uint32_t a0 = sbase + s * TC_A_BYTES, b0 = sbase + TC_OFF_B + s * TC_B_BYTES;
 #pragma unroll
-          for (int jj = 0; jj < TC_BK / 16; ++jj)
-            tc_mma(acc, sdesc_sw128(a0 + jj * 32), sdesc_sw128(b0 + jj * 32), idesc,
-                   (kb > 0 || jj > 0) ? 1u : 0u);
-          tc_commit(bar_empty + 8 * s);
+          for (int jj = 0; jj < TC_BK / 16; ++jj) {
+            const uint32_t accum = (kb > 0 || jj > 0) ? 1u : 0u;
+            if (PAIR) tc_mma2(acc, sdesc_sw128(a0 + jj * 32), sdesc_sw128(b0 + jj * 32), idesc, accum);
+            else tc_mma(acc, sdesc_sw128(a0 + jj * 32), sdesc_sw128(b0 + jj * 32), idesc, accum);
+          }
+          if (PAIR) tc_commit2(bar_empty + 8 * s);
+          else tc_commit(bar_empty + 8 * s);
         }
         if (!ok) break;
-        tc_commit(bar_tfull + 8 * b);
+        if (PAIR) tc_commit2(bar_tfull + 8 * b);
+        else tc_commit(bar_tfull + 8 * b);
       }
       kcount[1] = kg;
     }
@@ -462,14 +450,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     // so the four warps always meet at the same named barriers.
     pdl_wait();                                     // cache lengths come from earlier kernels
     const int q = warp & 3;
-    const int r = q * 32 + lane;                    // row within the tile
+    const int r = q * 32 + lane;                    // row within this CTA's 128 rows of the tile
     for (int j = 0; j < my_tiles; ++j) {
       const int b = j & 1, ub = j >> 1;
       int mt, nt;
       tile_of(j, mt, nt);
       const WSeg& g = p.seg[tc_seg_of(p, nt)];
       const int lt = nt - g.t0;
-      const int row = mt * TC_BM + r;
+      const int rt = mt * (C::BM / TC_BM) + (int)rank;   // this CTA's 128-row tile
+      const int row = rt * TC_BM + r;
       const bool ok = !(*abort_flag & 1) && mbar_wait(bar_tfull + 8 * b, ub & 1, 4000000000ull);
       if (!ok && !(*abort_flag & 1)) {
         atomicOr(p.status, ST_TIMEOUT);
@@ -479,16 +468,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
       if (ok) tc_tile_epilogue<BN>(p, g, lt, nt, row, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN));
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty + 8 * b);
+      if (lane == 0) {
+        if (PAIR) mbar_arrive_cluster(bar_tempty_l + 8 * b);
+        else mbar_arrive(bar_tempty + 8 * b);
+      }
       if (g.kind == SK_ARGMAX) {
-        // the CTA that finishes the last column tile of this row tile merges the
-        // records of its 128 rows over all column tiles
+        // the CTA that finishes the last column tile of this 128-row tile
+        // merges the records of its rows over all column tiles
         __threadfence();
         named_bar(1, 128);
         if (warp == 2 && lane == 0) {
-          const int old = atomicAdd(&p.counters[mt], 1);
+          const int old = atomicAdd(&p.counters[rt], 1);
           const int last = (old == p.n_ntiles - 1);
-          if (last) p.counters[mt] = 0;
+          if (last) p.counters[rt] = 0;
           *last_flag = last;
         }
         named_bar(1, 128);
@@ -503,23 +495,84 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
   tc_fence_before();
   __syncthreads();
   if ((*abort_flag & 1) && threadIdx.x == 0) {
-    // let the TMA loads still in flight land and the issued MMAs finish before
-    // the shared memory and TMEM are released (each wait bounded)
-    const int issued = kcount[0], used = kcount[1];
-    for (int i = used; i < issued && i < used + TC_STAGES; ++i)
-      mbar_wait(bar_full + 8 * (i % TC_STAGES), (i / TC_STAGES) & 1, 20000000ull);
-    if (used > 0)
-      mbar_wait(bar_empty + 8 * ((used - 1) % TC_STAGES), ((used - 1) / TC_STAGES) & 1, 20000000ull);
+    if (PAIR) {
+      // loads of this CTA may still be in flight, counted on the even CTA's
+      // barriers: give them time to land (bounded) before shared memory goes
+      const uint64_t t0 = globaltimer();
+      while (globaltimer() - t0 < 200000ull) __nanosleep(1000);
+    } else {
+      // let the TMA loads still in flight land and the issued MMAs finish
+      // before the shared memory and TMEM are released (each wait bounded)
+      const int issued = kcount[0], used = kcount[1];
+      for (int i = used; i < issued && i < used + TC_STAGES; ++i)
+        mbar_wait(bar_full + 8 * (i % TC_STAGES), (i / TC_STAGES) & 1, 20000000ull);
+      if (used > 0)
+        mbar_wait(bar_empty + 8 * ((used - 1) % TC_STAGES), ((used - 1) / TC_STAGES) & 1, 20000000ull);
+    }
+  }
+  if (PAIR) {
+    // neither CTA leaves while the other may still arrive on its barriers or
+    // the even CTA's MMAs may still use the odd CTA's TMEM
+    __syncthreads();
+    cluster_sync();
   }
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(TC_TMEM_COLS)
-                 : "memory");
+    if (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(TC_TMEM_COLS)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                   "r"(TC_TMEM_COLS)
+                   : "memory");
   }
 }
 
 // ---------------------------------------------------------------------------
+// The three variants: 256-column tiles, 128-column tiles, 256-row x 256-column
+// tiles on CTA pairs.
+using TcKernel = void (*)(TcParams);
+static TcKernel tc_kernel(int bi) {
+  return bi == 2 ? tc_gemm_kernel<256, true> : bi == 1 ? tc_gemm_kernel<128, false>
+                                                       : tc_gemm_kernel<256, false>;
+}
+static int tc_smem(int bi) {
+  return bi == 2 ? TcCfg<256, true>::SMEM : bi == 1 ? TcCfg<128>::SMEM : TcCfg<256>::SMEM;
+}
+static cudaError_t tc_set_smem(int bi) {
+  static bool done[3] = {false, false, false};
+  if (done[bi]) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(tc_kernel(bi), cudaFuncAttributeMaxDynamicSharedMemorySize, tc_smem(bi));
+  done[bi] = e == cudaSuccess;
+  return e;
+}
+
+// CTA pairs that can be resident at once (0: clusters unavailable).
+int tc_pair_units(const dflash_handle* h) {
+  static int units = -1;
+  if (units >= 0) return units;
+  units = 0;
+  if (tc_set_smem(2) != cudaSuccess) return units;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * std::max(1, h->num_sms / 2));
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = tc_smem(2);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_kernel(2), &cfg) == cudaSuccess && n > 0)
+    units = std::min(n, h->num_sms / 2);
+  cudaGetLastError();
+  return units;
+}
+
 int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, float4* amx) {
   if ((L.bn != 128 && L.bn != 256) || L.M < 1 || L.K % TC_BK != 0 || L.nseg < 1 ||
       L.nseg > WS_MAXMAP || L.nsrc < 1 || L.nsrc > WS_MAXSRC || (L.K / TC_BK) % L.nsrc != 0)
@@ -539,9 +592,14 @@ int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
   prm.M = L.M;
   prm.K = L.K;
   prm.kc_per_src = kc_per_src;
+  // CTA pairs (256-column tiles; the caller's weight maps have boxes of 128
+  // rows, half a tile)
+  const bool pair = L.pair;
+  if (pair && (L.bn != 256 || tc_pair_units(h) <= 0)) return DFLASH_ERR_SHAPE;
+  const int bm = pair ? 2 * TC_BM : TC_BM;
   prm.n_ntiles = L.seg[L.nseg - 1].t1;
-  prm.n_mtiles = (L.M + TC_BM - 1) / TC_BM;
-  prm.m_fast = DFLASH_TC_MFAST && prm.n_mtiles * 8 <= h->num_sms;
+  prm.n_mtiles = (L.M + bm - 1) / bm;
+  prm.m_fast = DFLASH_TC_MFAST && prm.n_mtiles * 8 <= (pair ? tc_pair_units(h) : h->num_sms);
   prm.rm = L.rm;
   prm.len = L.len;
   prm.rope_tab = h->d_rope;
@@ -555,29 +613,30 @@ int tc_gemm(dflash_handle* h, cudaStream_t s, int kclass, const WLaunch& L, floa
   prm.rps_out = L.rps_out;
   prm.anchor = L.anchor;
   const int64_t tiles = (int64_t)prm.n_mtiles * prm.n_ntiles;
-  if (L.seg[0].kind == SK_ARGMAX && (prm.n_mtiles > kMaxTiles || !amx)) return DFLASH_ERR_SHAPE;
+  if (L.seg[0].kind == SK_ARGMAX && (prm.n_mtiles * (bm / TC_BM) > kMaxTiles || !amx))
+    return DFLASH_ERR_SHAPE;
   if (tiles > 0x7fffffff) return DFLASH_ERR_SHAPE;
-  static bool attr_set[2] = {false, false};
-  const int bi = L.bn == 128 ? 1 : 0;
-  auto kern = bi ? tc_gemm_kernel<128> : tc_gemm_kernel<256>;
-  const int smem = bi ? TcCfg<128>::SMEM : TcCfg<256>::SMEM;
-  if (!attr_set[bi]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return DFLASH_ERR_CUDA;
-    attr_set[bi] = true;
-  }
+  const int bi = pair ? 2 : L.bn == 128 ? 1 : 0;
+  if (tc_set_smem(bi) != cudaSuccess) return DFLASH_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   // persistent: one CTA per SM (its shared memory admits no second), each
-  // walking every grid-th tile
-  cfg.gridDim = dim3((unsigned)std::min<int64_t>(tiles, h->num_sms));
+  // CTA (or pair of CTAs) walking every grid-th tile
+  const int64_t units = pair ? std::min<int64_t>(tiles, tc_pair_units(h))
+                             : std::min<int64_t>(tiles, h->num_sms);
+  cfg.gridDim = dim3((unsigned)(pair ? 2 * units : units));
   cfg.blockDim = dim3(TC_THREADS);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = tc_smem(bi);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pair ? 2 : 1;
+  auto kern = tc_kernel(bi);
   Timer t;
   launch_begin(h, kclass, s, &t);
   cudaLaunchKernelEx(&cfg, kern, prm);
