@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(AT_COMB_WARPS * 32) attn_combine_kernel(const 
 // One CTA per SM walks the items like attn_split_kernel and writes the same
 // partials.  Per 128-key sub-chunk of an item: S = Q K^T on the tensor cores
 // (M = 128 with the unit's query rows in rows 0-63, N = 128 keys, K = d) into
-// one of two TMEM buffers; four softmax warps (TMEM lanes 0-63: a query row
+// one of three TMEM buffers; four softmax warps (TMEM lanes 0-63: a query row
 // per thread, each key half in its own warp) take the row max over the
 // sub-chunk, exchange it with the other half, and overwrite the S columns they
 // have read with P as a bf16 pair (hi = bf16(p), lo = bf16(p - hi));
@@ -538,8 +538,9 @@ constexpr int AT_TC_OFF_BAR = AT_TC_OFF_KV + AT_TC_STAGES * AT_TC_STAGE;
 constexpr int AT_TC_OFF_RED = AT_TC_OFF_BAR + 128;
 constexpr int AT_TC_SMEM = AT_TC_OFF_RED + 3 * 2 * 64 * 4 + 1024;
 static_assert(AT_TC_SMEM <= 232448, "shared memory per CTA");
-// TMEM columns: S / P (two buffers), O
-constexpr uint32_t AT_TM_S = 0, AT_TM_O = 256, AT_TM_COLS = 512;
+// TMEM columns: S / P (three buffers: an S MMA into a buffer waits for the
+// P V that read the buffer's P, issued two sub-chunks earlier), O
+constexpr uint32_t AT_TM_S = 0, AT_TM_O = 384, AT_TM_COLS = 512;
 constexpr float AT_TC_SLACK = 8.f;
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -592,11 +593,12 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   const uint32_t sQ = smem_u32(smem), sKV = sQ + AT_TC_OFF_KV;
   const uint32_t bar = sQ + AT_TC_OFF_BAR;
-  // barriers: kv_full[3], kv_empty[3], q_full, q_empty, s_full[2], p_full, pv_done
+  // barriers: kv_full[3], kv_empty[3], q_full, q_empty, s_full[3] and
+  // pv_done[3] (per S / P buffer), p_full
   const uint32_t b_kvf = bar, b_kve = bar + 24, b_qf = bar + 48, b_qe = bar + 56, b_sf = bar + 64,
-                 b_pf = bar + 80, b_pv = bar + 88;
-  volatile uint32_t* tmem_slot = (volatile uint32_t*)(smem + AT_TC_OFF_BAR + 96);
-  volatile int* abort_flag = (volatile int*)(smem + AT_TC_OFF_BAR + 100);
+                 b_pf = bar + 88, b_pv = bar + 96;
+  volatile uint32_t* tmem_slot = (volatile uint32_t*)(smem + AT_TC_OFF_BAR + 120);
+  volatile int* abort_flag = (volatile int*)(smem + AT_TC_OFF_BAR + 124);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < AT_TC_STAGES; ++s) {
@@ -605,10 +607,11 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_
     }
     mbar_init(b_qf, 1);
     mbar_init(b_qe, 1);
-    mbar_init(b_sf, 1);
-    mbar_init(b_sf + 8, 1);
+    for (int b = 0; b < 3; ++b) {
+      mbar_init(b_sf + 8 * b, 1);
+      mbar_init(b_pv + 8 * b, 1);
+    }
     mbar_init(b_pf, 128);
-    mbar_init(b_pv, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -679,7 +682,9 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_
       // ---- MMAs -------------------------------------------------------------------
       int qn = 0, ni = 0;
       auto issue_s = [&](const TcGeo& q, int j) -> bool {
-        const int qq = qn + j, st = qq % AT_TC_STAGES;
+        const int qq = qn + j, st = qq % AT_TC_STAGES, sb = qq % 3;
+        // the P V of sub-chunk qq - 3 read this buffer's P: done before S overwrites it
+        if (qq >= 3 && !mbar_wait(b_pv + 8 * sb, (qq / 3 - 1) & 1)) return false;
         if (!mbar_wait(b_kvf + 8 * st, (qq / AT_TC_STAGES) & 1)) return false;
         tc_fence_after();
         const int n = j < q.nc ? AT_TC_KSUB : nb;
@@ -687,9 +692,9 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_
         const uint32_t dK = sKV + st * AT_TC_STAGE;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma(tmem + AT_TM_S + (qq & 1) * 128, sdesc_sw128(sQ + (kk >> 2) * AT_TC_HALF + (kk & 3) * 32),
+          tc_mma(tmem + AT_TM_S + sb * 128, sdesc_sw128(sQ + (kk >> 2) * AT_TC_HALF + (kk & 3) * 32),
                  sdesc_sw128(dK + (kk >> 2) * AT_TC_HALF + (kk & 3) * 32), idesc, kk > 0);
-        tc_commit(b_sf + 8 * (qq & 1));
+        tc_commit(b_sf + 8 * sb);
         return true;
       };
       for (int it = blockIdx.x; it < n_items && !*abort_flag; it += gridDim.x, ++ni) {
@@ -707,7 +712,7 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_
           const uint32_t idesc = idesc_bf16_f32_bmn(128, 128);
           const uint32_t dV = sKV + st * AT_TC_STAGE + 2 * AT_TC_HALF;
           // P of keys 32c .. 32c + 31: hi in S columns 32c .. 32c + 15, lo in the next 16
-          const uint32_t pb = tmem + AT_TM_S + (qq & 1) * 128;
+          const uint32_t pb = tmem + AT_TM_S + (qq % 3) * 128;
           for (int ks = 0; ks < n / 16; ++ks) {
             const uint64_t vd = sdesc_sw128_lbo(dV + ks * 2048, AT_TC_HALF, 1024);
             const uint32_t pa = pb + 32 * (ks >> 1) + 8 * (ks & 1);
@@ -715,7 +720,7 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_
             tc_mma_ts(tmem + AT_TM_O, pa + 16, vd, idesc, 1u);
           }
           tc_commit(b_kve + 8 * st);
-          tc_commit(b_pv);
+          tc_commit(b_pv + 8 * (qq % 3));
           if (j + 2 < q.nsub) {
             ok = issue_s(q, j + 2);
             if (ok && j + 2 == q.nsub - 1) tc_commit(b_qe);
@@ -748,7 +753,7 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_
       const int lo = max(q.k0, klo);   // visible keys of this row in the item: [lo, khi)
       float m_use = -INFINITY, l = 0.f;
       for (int j = 0; j < q.nsub; ++j) {
-        const int qq = qn + j, sb = qq & 1;
+        const int qq = qn + j, sb = qq & 1, tb = qq % 3;   // exchange buffer, S / P buffer
         const bool cache = j < q.nc;
         const int key0 = cache ? q.k0 + j * AT_TC_KSUB : q.L;
         const int n = cache ? AT_TC_KSUB : nb;
@@ -757,17 +762,18 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_
         const int vlo = row_ok ? max(lo - key0, 0) : 0;
         const int vhi = row_ok ? max(min(min(khi, lim) - key0, n), vlo) : 0;
         const int c0 = kh * 64;   // this warp's columns c0 .. c0 + 63 (those below n)
-        const uint32_t sbuf = tmem + lanes + AT_TM_S + sb * 128;
-        if (ok) ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(b_sf + 8 * sb, (qq >> 1) & 1, 4000000000ull));
+        const uint32_t sbuf = tmem + lanes + AT_TM_S + tb * 128;
+        if (ok) ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(b_sf + 8 * tb, (qq / 3) & 1, 4000000000ull));
         tc_fence_after();
-        // pass 1: the row max over this half's visible keys
+        // pass 1: the row max over this half's visible keys (columns at or
+        // past n are stale and invisible)
         float mx = -INFINITY;
         float v[2][32];
+        if (c0 < n) {
+          tc_ld64(sbuf + c0, &v[0][0]);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int cb = c0 + 32 * h;
-          if (cb < n) {
-            tc_ld32(sbuf + cb, v[h]);
+          for (int h = 0; h < 2; ++h) {
+            const int cb = c0 + 32 * h;
             if (vlo <= cb && vhi >= cb + 32) {
               float m2 = v[h][0];
 #pragma unroll
@@ -792,7 +798,7 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_
         }
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
           // O holds every earlier sub-chunk's P V: rescale this half of its columns
-          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_pv, (qq - 1) & 1, 4000000000ull));
+          if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_pv + 8 * ((qq - 1) % 3), ((qq - 1) / 3) & 1, 4000000000ull));
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
@@ -855,18 +861,17 @@ __global__ void __launch_bounds__(AT_TC_THREADS, 1) attn_tc_kernel(const __grid_
       // the item's partial: (max, sum, unnormalised O) of this row; each half
       // writes its 64 columns of O, half 0 the row's (max, sum of both halves)
       red[(4 + kh) * 64 + r] = l;
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_pv, (qn - 1) & 1, 4000000000ull));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(b_pv + 8 * ((qn - 1) % 3), ((qn - 1) / 3) & 1, 4000000000ull));
       tc_fence_after();
       named_bar(1, 128);
       float* part = p.part + ((int64_t)it * 64 + r) * AT_DP;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float o[32];
-        tc_ld32(tmem + lanes + AT_TM_O + kh * 64 + c * 32, o);
+      {
+        float o[64];
+        tc_ld64(tmem + lanes + AT_TM_O + kh * 64, o);
         if (row_ok) {
 #pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            __stcg((float4*)&part[4 + kh * 64 + c * 32 + k], make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]));
+          for (int k = 0; k < 64; k += 4)
+            __stcg((float4*)&part[4 + kh * 64 + k], make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]));
         }
       }
       if (row_ok && kh == 0) __stcg((float2*)part, make_float2(m_use, l + red[5 * 64 + r]));
