@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(WS_THREADS, DFLASH_WS_MINBLOCKS) wstream_kerne
         // each in flight together (at 64 rows one whole partial per batch:
         // as many dependent batches as contributors, not one per float4);
         // every element still adds the contributors in CTA (= k) order
-        constexpr int CB = IT >= 16 ? 1 : IT >= 8 ? 2 : 8;
+        constexpr int CB = IT >= 16 ? 2 : IT >= 8 ? 2 : 8;
         for (int c0 = lo; c0 <= hi; c0 += CB) {
           float4 v[CB][IT];
 #pragma unroll
