@@ -223,6 +223,9 @@ static int lm_head_tc(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows, in
 static int lm_head_stream(dflash_handle* h, cudaStream_t s, Fwd& f, int64_t rows, int32_t* ids,
                           float* gap, int rps_out, const int32_t* anchor);
 
+#ifndef DFLASH_LM_TC_MIN_ROWS
+#define DFLASH_LM_TC_MIN_ROWS 33
+#endif
 static int lm_head(dflash_handle* h, cudaStream_t s, Fwd& f, const float* x, int64_t rows,
                    const float* gain, int skip_first_of, int32_t* ids, float* gap, int rps_out,
                    const int32_t* anchor) {
@@ -232,6 +235,11 @@ static int lm_head(dflash_handle* h, cudaStream_t s, Fwd& f, const float* x, int
   if ((rc = rmsnorm_rows(h, s, DFLASH_F32, dt, x, D, f.hf, D, gain, rows, D, c.rms_eps,
                          skip_first_of)))
     return rc;
+  // From DFLASH_LM_TC_MIN_ROWS rows the LM head (a weight of vocabulary x D)
+  // goes to the tensor cores: the streaming kernel's warp-level MMAs bound it
+  // there, not HBM
+  if (h->have_tc && rows >= DFLASH_LM_TC_MIN_ROWS)
+    return lm_head_tc(h, s, f, rows, ids, gap, rps_out, anchor);
   if (streaming(h, rows)) return lm_head_stream(h, s, f, rows, ids, gap, rps_out, anchor);
   if (dense_tc(h, rows)) return lm_head_tc(h, s, f, rows, ids, gap, rps_out, anchor);
   if ((rc = gemm(h, s, DFLASH_K_LM_HEAD, dt, one_src(f.hf, D, D), h->w.lm_head, D, f.logits, V,
