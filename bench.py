@@ -654,9 +654,10 @@ def run_ours(args, rank, world, local):
     total_bytes = sum(nbytes[k] for k in ("weight_gemm", "lm_head", "attention", "dense_gemm"))
     step_frac = total_bytes / (ms_step / 1e3) / 1e9 / hbm
 
-    # end to end through the C ABI from pinned host memory: every step copies
-    # its inputs in (features, anchors, posterior: one buffer each) and its
-    # results out (one buffer), then waits for them
+    # end to end through the C ABI from pinned host memory: every step is one
+    # dflash_round_host call, which copies the inputs in (features, anchors
+    # and posterior: two buffers), drafts and verifies, and copies the results
+    # out (one buffer); the host then waits for them
     h_hidden = torch.empty_like(st.hidden_all, device="cpu").pin_memory()
     h_hidden.copy_(st.hidden_all)
     h_ints_in = st.ints_in.cpu().pin_memory()
@@ -664,11 +665,13 @@ def run_ours(args, rank, world, local):
     h2d = h_hidden.numel() * h_hidden.element_size() + h_ints_in.numel() * 4
     d2h = h_ints_out.numel() * 4
 
+    assert h_ints_out.numel() == dfl.dflash_round_out_len(st.batch, st.B)
+
     def e2e_step():
-        st.hidden_all.copy_(h_hidden, non_blocking=True)
-        st.ints_in.copy_(h_ints_in, non_blocking=True)
-        st.step()
-        h_ints_out.copy_(st.ints_out, non_blocking=True)
+        st.kv.len.copy_(st.len0)
+        dfl.dflash_round_host(st.model.handle, h_hidden, st.hidden_all, st.rows, h_ints_in,
+                              st.ints_in, h_ints_out, st.ints_out, st.row0, st.nrow, st.Ht,
+                              st.batch, st.B, st.kv.struct, st.start, None, st.ws)
         torch.cuda.current_stream().synchronize()
 
     for _ in range(args.warmup):

@@ -84,6 +84,9 @@ _sig = {
     "dflash_verify_greedy": (C.c_int, [_P, _P, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P, _P]),
     "dflash_emit_tokens": (C.c_int, [_P, _P, _P, C.c_int32, C.c_int32, _P, C.c_int32, _P, _P,
                                      C.c_int32, _P, _P]),
+    "dflash_round_host": (C.c_int, [_P, _P, _P, C.c_int32, _P, _P, _P, _P, _P, _P, _P, C.c_int32,
+                                    C.c_int32, C.POINTER(dflash_kv), _P, _P, _P, C.c_size_t, _P]),
+    "dflash_round_out_len": (C.c_int64, [C.c_int32, C.c_int32]),
     "dflash_lm_head_argmax": (C.c_int, [_P, _P, C.c_int32, _P, _P, _P, _P, C.c_size_t, _P]),
     "dflash_lm_head_logits": (C.c_int, [_P, _P, C.c_int32, _P, C.c_int32, _P, _P, C.c_size_t,
                                         _P]),
@@ -218,6 +221,26 @@ def dflash_emit_tokens(h: int, out_tokens: torch.Tensor, tau: torch.Tensor, batc
     _check(_lib.dflash_emit_tokens(h, _ptr(out_tokens), _ptr(tau), batch, B, _ptr(out_buf),
                                    out_buf.shape[-1], _ptr(out_len), _ptr(tau_log), log_cap,
                                    _ptr(n_rounds), _stream(stream)), "dflash_emit_tokens")
+
+
+def dflash_round_out_len(batch: int, B: int) -> int:
+    return int(_lib.dflash_round_out_len(batch, B))
+
+
+def dflash_round_host(h: int, host_features: Optional[torch.Tensor],
+                      dev_features: Optional[torch.Tensor], n_rows: int, host_in: torch.Tensor,
+                      dev_in: torch.Tensor, host_out: torch.Tensor, dev_out: torch.Tensor,
+                      seq_row0: torch.Tensor, seq_rows: torch.Tensor, h_t_out: torch.Tensor,
+                      batch: int, B: int, kv: dflash_kv, start: torch.Tensor,
+                      new_len: Optional[torch.Tensor], ws: torch.Tensor, stream=None):
+    """One greedy round from host buffers to host buffers (copies queued on
+    the stream; host_out is valid once the stream is synchronised)."""
+    _check(_lib.dflash_round_host(h, _ptr(host_features), _ptr(dev_features), n_rows,
+                                  _ptr(host_in), _ptr(dev_in), _ptr(host_out), _ptr(dev_out),
+                                  _ptr(seq_row0), _ptr(seq_rows), _ptr(h_t_out), batch, B,
+                                  C.byref(kv), _ptr(start), _ptr(new_len), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream)),
+           "dflash_round_host")
 
 
 def dflash_lm_head_logits(h: int, x: torch.Tensor, rows: int, norm_gain: torch.Tensor,

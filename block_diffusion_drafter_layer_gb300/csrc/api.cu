@@ -1111,6 +1111,51 @@ int dflash_emit_tokens(dflash_handle* h, const int32_t* out_tokens, const int32_
                      tau_log, log_cap, n_rounds, h->d_status);
 }
 
+int64_t dflash_round_out_len(int32_t batch, int32_t B) {
+  if (batch < 1 || B < 1) return -1;
+  const int64_t P = ((int64_t)batch + 3) / 4 * 4;
+  return 2 * (int64_t)batch * B + 3 * P;
+}
+
+int dflash_round_host(dflash_handle* h, const void* host_features, void* dev_features,
+                      int32_t n_rows, const int32_t* host_in, int32_t* dev_in, int32_t* host_out,
+                      int32_t* dev_out, const int32_t* seq_row0, const int32_t* seq_rows,
+                      void* h_t_out, int32_t batch, int32_t B, const dflash_kv* kv,
+                      const int32_t* start, int32_t* new_len, void* ws, size_t ws_bytes,
+                      dflash_stream_t st) {
+  if (!h || n_rows < 0 || batch < 1 || B < 1 || !host_in || !dev_in || !host_out || !dev_out ||
+      !start || (n_rows > 0 && (!host_features || !dev_features)))
+    return DFLASH_ERR_INVALID_ARG;
+  const dflash_config& c = h->cfg;
+  if (c.n_pick < 1 || c.n_pick > 8) return DFLASH_ERR_INVALID_ARG;
+  if ((n_rows > 0 && !aligned16(dev_features)) || !aligned16(dev_out)) return DFLASH_ERR_ALIGNMENT;
+  cudaStream_t s = (cudaStream_t)st;
+  const int64_t slice = (int64_t)n_rows * c.hidden * esize(c.dtype);
+  const int64_t n_in = (int64_t)batch + (int64_t)batch * B;
+  const int64_t n_out = dflash_round_out_len(batch, B);
+  if (n_rows > 0 && cudaMemcpyAsync(dev_features, host_features, slice * c.n_pick,
+                                    cudaMemcpyHostToDevice, s))
+    return DFLASH_ERR_CUDA;
+  if (cudaMemcpyAsync(dev_in, host_in, n_in * sizeof(int32_t), cudaMemcpyHostToDevice, s))
+    return DFLASH_ERR_CUDA;
+  const void* hidden[8] = {};
+  for (int i = 0; i < c.n_pick && n_rows > 0; ++i)
+    hidden[i] = (const char*)dev_features + i * slice;
+  const int64_t bB = (int64_t)batch * B, P = ((int64_t)batch + 3) / 4 * 4;
+  int32_t* ids = dev_out;
+  int32_t* tokens = dev_out + bB;
+  int32_t* accept = dev_out + 2 * bB;
+  int rc = dflash_draft_round(h, n_rows ? hidden : nullptr, n_rows, seq_row0, seq_rows, h_t_out,
+                              dev_in, batch, B, kv, ids, nullptr, nullptr, ws, ws_bytes, st);
+  if (rc) return rc;
+  rc = dflash_verify_greedy(ids, dev_in + batch, batch, B, start, accept, accept + P, accept + 2 * P,
+                            tokens, new_len, st);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(host_out, dev_out, n_out * sizeof(int32_t), cudaMemcpyDeviceToHost, s))
+    return DFLASH_ERR_CUDA;
+  return DFLASH_OK;
+}
+
 int dflash_lm_head_argmax(dflash_handle* h, const float* x, int32_t rows, const float* norm_gain,
                           int32_t* ids, float* top2_gap, void* ws, size_t ws_bytes,
                           dflash_stream_t st) {

@@ -260,6 +260,38 @@ int dflash_emit_tokens(dflash_handle* h, const int32_t* out_tokens, const int32_
                        int32_t* out_len, int32_t* tau_log, int32_t log_cap, int32_t* n_rounds,
                        dflash_stream_t s);
 
+/* One greedy round from and to host memory (txtmix §9: draft a block from
+ * the new target features, verify it against the target's argmax): the
+ * round's inputs are copied in, dflash_draft_round and dflash_verify_greedy
+ * run, and the results are copied out, all queued on stream s with one
+ * cudaMemcpyAsync per buffer and direction.  The call returns once the work
+ * is queued; host_out holds the results after the stream is synchronised.
+ *   host_features: host [n_pick, n_rows, D] in the handle's dtype, pinned
+ *     for an asynchronous copy (NULL when n_rows == 0); dev_features: device
+ *     buffer of the same size, 16-byte aligned; slice i becomes hidden[i]
+ *     of dflash_draft_round.
+ *   host_in: host int32 [batch + batch*B], anchor [batch] then post
+ *     [batch, B] (the target's argmax, as for dflash_verify_greedy);
+ *     dev_in: device int32 of the same size.
+ *   host_out, dev_out: host and device int32 [dflash_round_out_len(batch,
+ *     B)]: draft_ids [batch, B] at 0, out_tokens [batch, B] at batch*B, then
+ *     accept, tau and bonus [batch] at 2*batch*B, 2*batch*B + P and
+ *     2*batch*B + 2P, P = batch rounded up to a multiple of 4.
+ *   seq_row0, seq_rows, h_t_out, kv, ws: as for dflash_draft_round; start
+ *     and new_len (nullable): as for dflash_verify_greedy, device int32.
+ * Errors: those of the two calls; DFLASH_ERR_CUDA when a copy cannot be
+ * queued.  All buffers are the caller's; nothing is allocated. */
+int dflash_round_host(dflash_handle* h, const void* host_features, void* dev_features,
+                      int32_t n_rows, const int32_t* host_in, int32_t* dev_in, int32_t* host_out,
+                      int32_t* dev_out, const int32_t* seq_row0, const int32_t* seq_rows,
+                      void* h_t_out, int32_t batch, int32_t B, const dflash_kv* kv,
+                      const int32_t* start, int32_t* new_len, void* ws, size_t ws_bytes,
+                      dflash_stream_t s);
+
+/* Entries of dflash_round_host's result buffer: 2*batch*B + 3*P, P = batch
+ * rounded up to a multiple of 4.  Host only; -1 for batch < 1 or B < 1. */
+int64_t dflash_round_out_len(int32_t batch, int32_t B);
+
 /* Final RMSNorm + shared LM head + fused argmax over rows of an fp32
  * residual stream.  x: device fp32 [rows, D]; norm_gain: device fp32 [D];
  * ids: device int32 [rows]; top2_gap: nullable device fp32 [rows]. */
