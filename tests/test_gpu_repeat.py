@@ -6,7 +6,8 @@ between identical launches is a race.  With two co-resident CTAs per SM, the
 streaming kernel once returned one consumer warp's 32 output columns wrong
 in a few of 300 such launches.  It runs one CTA per SM since then. These
 tests keep watching it, the persistent draft-block kernel (two CTAs per SM)
-and the tensor-core projection, at the Qwen3-8B shape."""
+and the tensor-core projection, at the Qwen3-8B shape, and the tcgen05 split
+attention at the 35B-A3B shape."""
 import dataclasses
 
 import numpy as np
@@ -106,4 +107,37 @@ def test_persistent_draft_block_repeat(dfl):
     assert dfl.dflash_get_status(m.handle) == 0
     m.close()
     print(f"persistent draft block: {bad} of 299 repeats differ")
+    assert bad == 0
+
+
+@pytest.mark.parametrize("B", [8, 16])
+def test_tcgen05_attention_block_repeat(dfl, B):
+    """A two-layer 35B-A3B-shaped draft block at batch 4 with ragged contexts
+    (32 or 64 rows: the streaming projections and the tcgen05 split
+    attention with its TMEM buffers and stage barriers), 200 times."""
+    from synth.gpu import draft_model, kv_cache
+    w = synth.WORKLOADS["qwen35_a3b_32k"]
+    s = dataclasses.replace(w.draft, n_layers=2)
+    lens = [5000, 2048, 777, 3333]
+    cap = max(lens) + 8
+    weights = synth.draft_weights(s, w.dtype, w.seed, device="cuda")
+    K, V = synth.random_kv_cache(4, s.G, cap, s.d, s.n_layers, 0.02 * np.sqrt(s.D), w.dtype,
+                                 w.seed, device="cuda")
+    kv = kv_cache(s, 4, cap, w.dtype, k=K, v=V)
+    kv.len.copy_(torch.tensor(lens, dtype=torch.int32))
+    m = draft_model(s, w.dtype, weights, max_pos=cap + B + 8)
+    anchors = torch.from_numpy(synth.anchors(4, s.V, s.mask_id, w.seed)).cuda()
+    ids = torch.empty(4, B, dtype=torch.int32, device="cuda")
+    gap = torch.empty(4, B - 1, device="cuda")
+    hid = torch.empty(4 * B, s.D, device="cuda")
+    ws = m.workspace(4 * B, max_batch=4, max_block=B)
+
+    def call():
+        dfl.dflash_draft_block(m.handle, anchors, 4, B, kv.struct, ids, gap, hid, ws)
+        return ids, gap, hid
+
+    bad = _repeat(call, 200)
+    assert dfl.dflash_get_status(m.handle) == 0
+    m.close()
+    print(f"tcgen05 attention block B={B}: {bad} of 199 repeats differ")
     assert bad == 0
