@@ -82,3 +82,21 @@ def test_sampling_scratch_and_argument_errors(dfl):
     assert lib.dflash_verify_rejection(None, None, None, None, 16, None, None, 1, 4, None, None,
                                        None, None, None, None, None, 0, None) == 1
     assert lib.dflash_lm_head_logits(None, None, 1, None, 0, None, None, 0, None) == 1
+
+
+def test_round_host_layout_and_argument_errors(dfl):
+    """dflash_round_host's result length (ids and tokens [batch, B], then
+    accept, tau and bonus [batch] each padded to a multiple of 4) and its
+    host-side argument checks, which reject before any copy is queued."""
+    assert dfl.dflash_round_out_len(1, 16) == 2 * 16 + 3 * 4
+    assert dfl.dflash_round_out_len(4, 8) == 2 * 32 + 3 * 4
+    assert dfl.dflash_round_out_len(5, 8) == 2 * 40 + 3 * 8
+    assert dfl.dflash_round_out_len(32, 16) == 2 * 512 + 3 * 32
+    assert dfl.dflash_round_out_len(0, 16) == -1
+    assert dfl.dflash_round_out_len(4, 0) == -1
+    lib = dfl._lib
+    args = [None] * 19
+    args[3], args[11], args[12], args[17] = 16, 1, 16, 0
+    assert lib.dflash_round_host(*args) == 1          # no handle, no buffers
+    args[3] = -1
+    assert lib.dflash_round_host(*args) == 1          # negative pending rows
