@@ -68,7 +68,10 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const TI* __restrict__ in,
                                                       const float* __restrict__ g, int D, float eps,
                                                       int skip_first_of) {
   __shared__ float red[33];
+  // launched as a programmatic dependent: it may be resident while the kernel
+  // before it finishes, and reads its input only after that kernel is done
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t r = blockIdx.x;
   int64_t ri = r;
   if (skip_first_of > 1) {
@@ -242,19 +245,27 @@ int rmsnorm_rows(dflash_handle* h, cudaStream_t s, int in_dtype, int out_dtype, 
   if (rows <= 0) return DFLASH_OK;
   Timer t;
   launch_begin(h, DFLASH_K_ELEMENTWISE, s, &t);
-  const dim3 grid((unsigned)rows);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)rows);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (in_dtype == DFLASH_F32 && out_dtype == DFLASH_F32)
-    rmsnorm_kernel<float, float><<<grid, 256, 0, s>>>((const float*)in, ld_in, (float*)out, ld_out,
-                                                      g, D, eps, skip_first_of);
+    cudaLaunchKernelEx(&cfg, rmsnorm_kernel<float, float>, (const float*)in, ld_in, (float*)out,
+                       ld_out, g, D, eps, skip_first_of);
   else if (in_dtype == DFLASH_F32 && out_dtype == DFLASH_BF16)
-    rmsnorm_kernel<float, bf16><<<grid, 256, 0, s>>>((const float*)in, ld_in, (bf16*)out, ld_out,
-                                                     g, D, eps, skip_first_of);
+    cudaLaunchKernelEx(&cfg, rmsnorm_kernel<float, bf16>, (const float*)in, ld_in, (bf16*)out,
+                       ld_out, g, D, eps, skip_first_of);
   else if (in_dtype == DFLASH_BF16 && out_dtype == DFLASH_BF16)
-    rmsnorm_kernel<bf16, bf16><<<grid, 256, 0, s>>>((const bf16*)in, ld_in, (bf16*)out, ld_out, g,
-                                                    D, eps, skip_first_of);
+    cudaLaunchKernelEx(&cfg, rmsnorm_kernel<bf16, bf16>, (const bf16*)in, ld_in, (bf16*)out,
+                       ld_out, g, D, eps, skip_first_of);
   else
-    rmsnorm_kernel<bf16, float><<<grid, 256, 0, s>>>((const bf16*)in, ld_in, (float*)out, ld_out,
-                                                     g, D, eps, skip_first_of);
+    cudaLaunchKernelEx(&cfg, rmsnorm_kernel<bf16, float>, (const bf16*)in, ld_in, (float*)out,
+                       ld_out, g, D, eps, skip_first_of);
   return launch_end(h, s, &t);
 }
 
